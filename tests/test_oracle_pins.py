@@ -1,0 +1,423 @@
+"""Pins for the CPU oracle: checks it against what the pages and the
+mathematics fix, never against itself.
+
+Each test names the kind of evidence: a value the pages print (golden
+fixtures under tests/golden/), a closed form, an invariant, a special case
+that reduces to a library routine, or brute force on a tiny case.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle as O
+from oracle import fp8 as F
+import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _rand_problem(rng, H=3, n=17, Dc=O.D_C, Dr=O.D_R, Dn=O.D_NOPE, Dv=O.D_V):
+    q_nope = rng.standard_normal((H, Dn))
+    q_rope = rng.standard_normal((H, Dr))
+    w_uk = rng.standard_normal((H, Dc, Dn)) / math.sqrt(Dc)
+    w_uv = rng.standard_normal((H, Dc, Dv)) / math.sqrt(Dc)
+    c_kv = rng.standard_normal((n, Dc))
+    k_rope = rng.standard_normal((n, Dr))
+    return q_nope, q_rope, w_uk, w_uv, c_kv, k_rope
+
+
+# ---------------------------------------------------------------------------
+# values the pages print
+# ---------------------------------------------------------------------------
+def test_kv_bytes_per_token_closed_form():
+    g = _golden("kv_bytes_per_token.json")
+    got = O.kv_cache_bytes_per_token(g["n_layers"], g["kv_lora_rank"], g["qk_rope_head_dim"],
+                                     g["bytes_per_elem"])
+    assert got == g["bytes_per_token_all_layers"]
+    assert round(got / 1024, 1) == g["kib_per_token_rounded"]
+    assert O.kv_cache_bytes_per_token(1) == g["bytes_per_token_one_layer"]
+    # the generator's caches hold exactly that many bytes per token and layer
+    b = W.generate(W.WORKLOADS["tiny"])
+    assert b.cache_bf16.nbytes // (b.num_pages * b.workload.page_size) == g["bytes_per_token_one_layer"]
+    assert W.FP8_ROW_BYTES == O.D_QK + O.D_QK // g["fp8_values_per_scale"] == F.ROW_BYTES
+
+
+def test_topk_buffer_width_golden():
+    for c in _golden("topk_width.json")["cases"]:
+        assert O.topk_buffer_width(c["topk"], c["kpool"]) == c["width"], c
+        assert O.topk_buffer_width(c["topk"], c["kpool"]) % 128 == 0
+
+
+def test_paged_gather_golden():
+    g = _golden("paged_gather.json")
+    pages, slots = O.physical_rows(np.array(g["block_table_row"]), np.array(g["positions"]),
+                                   g["page_size"])
+    assert pages.tolist() == g["pages"]
+    assert slots.tolist() == g["slots"]
+
+
+def test_visibility_golden():
+    g = _golden("visibility.json")
+    for c in g["dense"]:
+        got = O.visible_positions(c["T"], c["Q"], c["j"], causal=True)
+        assert got.tolist() == c["visible"], c
+    for c in g["sparse"]:
+        got = O.visible_positions(c["T"], c["Q"], c["j"], causal=True,
+                                  topk_row=np.array(c["row"]))
+        assert got.tolist() == c["visible"], c
+
+
+def _hex(s):
+    return int(s, 16)
+
+
+def test_fp8_codes_golden():
+    g = _golden("fp8_codes.json")
+    for code, val in g["e4m3"]:
+        got = F.e4m3_to_f64(np.array([_hex(code)], dtype=np.uint8))[0]
+        if val == "nan":
+            assert np.isnan(got)
+        else:
+            assert got == val and math.copysign(1, got) == math.copysign(1, val), code
+    for code, val in g["e8m0"]:
+        got = F.e8m0_to_f64(np.array([_hex(code)], dtype=np.uint8))[0]
+        if val == "nan":
+            assert np.isnan(got)
+        else:
+            assert got == val, code
+
+
+def test_fp8_quantiser_golden_groups():
+    row = np.zeros((1, F.D_QK))
+    row[0, 0:32] = 448.0           # group 0
+    row[0, 32] = 1.0               # group 1
+    # group 2 all zero
+    row[0, 96] = -896.0            # group 3
+    q = F.quantize_rows(row)[0]
+    vals, scales = q[:F.D_QK], q[F.D_QK:]
+    assert scales[0] == 127 and (vals[0:32] == 0x7E).all()
+    assert scales[1] == 119 and vals[32] == 0x78 and (vals[33:64] == 0).all()
+    assert scales[2] == 0 and (vals[64:96] == 0).all()
+    assert scales[3] == 128 and vals[96] == 0xFE and (vals[97:128] == 0).all()
+
+
+# ---------------------------------------------------------------------------
+# library routines
+# ---------------------------------------------------------------------------
+def test_e4m3_table_matches_torch():
+    torch = pytest.importorskip("torch")
+    codes = np.arange(256, dtype=np.uint8)
+    mine = F.e4m3_to_f64(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(mine), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(mine[ok], ref[ok])
+    assert np.array_equal(np.signbit(mine[ok]), np.signbit(ref[ok]))
+
+
+def test_e8m0_table_matches_torch():
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e8m0fnu"):
+        pytest.skip("torch lacks float8_e8m0fnu")
+    codes = np.arange(256, dtype=np.uint8)
+    mine = F.e8m0_to_f64(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e8m0fnu).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(mine), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(mine[ok], ref[ok])
+
+
+def test_fp8_quantiser_round_trip_matches_torch_rounding():
+    """x / 2**e rounded by torch's float8_e4m3fn cast (round to nearest even)
+    must equal the quantiser's codes, and dequantising gives back the value
+    within half a quantum."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((64, F.D_QK)) * np.exp(rng.uniform(-6, 6, size=(64, 1)))
+    q = F.quantize_rows(x)
+    scales = F.e8m0_to_f64(q[:, F.D_QK:])
+    scaled = x / np.repeat(scales, 32, axis=1)
+    assert np.abs(scaled).max() <= 448.0
+    ref_codes = torch.from_numpy(scaled).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ref_codes, q[:, :F.D_QK])
+    back = F.dequant_rows(q)
+    amax = np.abs(x.reshape(64, 18, 32)).max(axis=2)
+    # largest spacing in a group is 32 * 2**e (binade [256, 448] has spacing 32)
+    bound = np.repeat(scales * 16.0, 32, axis=1)
+    assert (np.abs(back - x) <= bound + 1e-300).all()
+    # amax lands in (224, 448] after scaling: e is the smallest fitting power
+    s_amax = amax / scales
+    assert (s_amax <= 448.0).all() and (s_amax > 224.0).all()
+
+
+def test_matches_torch_sdpa():
+    """Softmax attention on the decompressed per-head K/V equals torch's
+    scaled_dot_product_attention (float64, CPU); lse equals torch.logsumexp."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(11)
+    q_nope, q_rope, w_uk, w_uv, c_kv, k_rope = _rand_problem(rng, H=4, n=50)
+    scale = 1.0 / 16.0
+    o, lse, o_lat = O.attend_non_absorbed(q_nope, q_rope, w_uk, w_uv, c_kv, k_rope, scale)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a))
+    for h in range(4):
+        K = torch.cat([t(c_kv) @ t(w_uk[h]), t(k_rope)], dim=1)         # [n, 256]
+        V = t(c_kv) @ t(w_uv[h])                                          # [n, 256]
+        qv = torch.cat([t(q_nope[h]), t(q_rope[h])])[None, None, None, :]
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            qv, K[None, None], V[None, None], scale=scale)[0, 0, 0].numpy()
+        assert np.allclose(o[h], ref, rtol=1e-12, atol=1e-13)
+        ref_lse = torch.logsumexp((K @ qv[0, 0, 0]) * scale, dim=0).item()
+        assert abs(lse[h] - ref_lse) < 1e-12
+        # latent output up-projects to o
+        assert np.allclose(o_lat[h] @ w_uv[h], o[h], rtol=1e-12, atol=1e-13)
+
+
+# ---------------------------------------------------------------------------
+# closed forms and special cases
+# ---------------------------------------------------------------------------
+def test_hand_worked_tiny_dims():
+    """Dc=2, Dr=1, Dn=1, Dv=1, one head, two tokens, scale 1: every quantity
+    worked by hand.  k_nope = c @ W_UK = [1, 3]; scores = [1*1 + 0*2, 3*1 + 1*2]
+    = [1, 5]; v = c @ W_UV = [2, 4]."""
+    q_nope = np.array([[1.0]])
+    q_rope = np.array([[2.0]])
+    w_uk = np.array([[[1.0], [0.0]]])
+    w_uv = np.array([[[0.0], [1.0]]])
+    c_kv = np.array([[1.0, 2.0], [3.0, 4.0]])
+    k_rope = np.array([[0.0], [1.0]])
+    o, lse, o_lat = O.attend_non_absorbed(q_nope, q_rope, w_uk, w_uv, c_kv, k_rope, 1.0)
+    e1, e5 = math.exp(1.0), math.exp(5.0)
+    assert abs(lse[0] - (5.0 + math.log1p(math.exp(-4.0)))) < 1e-14
+    assert abs(o[0, 0] - (2 * e1 + 4 * e5) / (e1 + e5)) < 1e-14
+    p0 = e1 / (e1 + e5)
+    assert np.allclose(o_lat[0], [p0 * 1 + (1 - p0) * 3, p0 * 2 + (1 - p0) * 4], rtol=1e-14)
+
+
+def test_single_token():
+    rng = np.random.default_rng(1)
+    q_nope, q_rope, w_uk, w_uv, c_kv, k_rope = _rand_problem(rng, H=2, n=1)
+    o, lse, o_lat = O.attend_non_absorbed(q_nope, q_rope, w_uk, w_uv, c_kv, k_rope, 0.0625)
+    for h in range(2):
+        s0 = (c_kv[0] @ w_uk[h] @ q_nope[h] + k_rope[0] @ q_rope[h]) * 0.0625
+        assert abs(lse[h] - s0) < 1e-12
+        assert np.allclose(o[h], w_uv[h].T @ c_kv[0], rtol=1e-13, atol=1e-14)
+        assert np.array_equal(o_lat[h], c_kv[0])
+
+
+def test_zero_query_gives_mean_and_log_count():
+    rng = np.random.default_rng(2)
+    q_nope, q_rope, w_uk, w_uv, c_kv, k_rope = _rand_problem(rng, H=2, n=37)
+    q_nope[:] = 0
+    q_rope[:] = 0
+    o, lse, o_lat = O.attend_non_absorbed(q_nope, q_rope, w_uk, w_uv, c_kv, k_rope, 0.0625)
+    for h in range(2):
+        assert abs(lse[h] - math.log(37)) < 1e-13
+        assert np.allclose(o[h], (c_kv @ w_uv[h]).mean(axis=0), rtol=1e-12, atol=1e-14)
+        assert np.allclose(o_lat[h], c_kv.mean(axis=0), rtol=1e-12, atol=1e-14)
+
+
+def test_two_tokens_sigmoid():
+    rng = np.random.default_rng(3)
+    q_nope, q_rope, w_uk, w_uv, c_kv, k_rope = _rand_problem(rng, H=1, n=2)
+    o, lse, _ = O.attend_non_absorbed(q_nope, q_rope, w_uk, w_uv, c_kv, k_rope, 0.0625)
+    s = [(c_kv[t] @ w_uk[0] @ q_nope[0] + k_rope[t] @ q_rope[0]) * 0.0625 for t in range(2)]
+    p0 = 1.0 / (1.0 + math.exp(s[1] - s[0]))
+    v = c_kv @ w_uv[0]
+    assert np.allclose(o[0], p0 * v[0] + (1 - p0) * v[1], rtol=1e-12, atol=1e-14)
+    assert abs(lse[0] - max(s) - math.log1p(math.exp(min(s) - max(s)))) < 1e-13
+
+
+def test_rope_only_and_nope_only_scores():
+    """q_nope = 0 leaves the RoPE part alone in the scores; k_rope = q_rope = 0
+    (the NoPE special case: vllm API docs, vllm.models.glm5next.common.model,
+    load_weights: NoPE checkpoints zero-pad the RoPE rows) leaves the latent
+    part alone, equal to an oracle run with the RoPE dims removed."""
+    rng = np.random.default_rng(4)
+    q_nope, q_rope, w_uk, w_uv, c_kv, k_rope = _rand_problem(rng, H=2, n=9)
+    qn0 = np.zeros_like(q_nope)
+    o, lse, _ = O.attend_non_absorbed(qn0, q_rope, w_uk, w_uv, c_kv, k_rope, 0.5)
+    for h in range(2):
+        s = (k_rope @ q_rope[h]) * 0.5
+        m = s.max()
+        assert abs(lse[h] - (m + math.log(np.exp(s - m).sum()))) < 1e-12
+    o1, lse1, _ = O.attend_non_absorbed(q_nope, np.zeros_like(q_rope), w_uk, w_uv, c_kv,
+                                        np.zeros_like(k_rope), 0.5)
+    o2, lse2, _ = O.attend_non_absorbed(q_nope, q_rope[:, :0], w_uk, w_uv, c_kv,
+                                        k_rope[:, :0], 0.5)
+    assert np.allclose(o1, o2, rtol=1e-13, atol=1e-15) and np.allclose(lse1, lse2, rtol=1e-13)
+
+
+def test_one_hot_dominant_token():
+    """A token whose score exceeds all others by > 100 nats takes all the
+    weight: o_lat equals its latent row (to float64 resolution)."""
+    rng = np.random.default_rng(6)
+    q_nope, q_rope, w_uk, w_uv, c_kv, k_rope = _rand_problem(rng, H=1, n=40)
+    k_rope[17] = q_rope[0] * 40.0          # + 40 * |q_rope|^2 * scale >> 100
+    o, lse, o_lat = O.attend_non_absorbed(q_nope, q_rope, w_uk, w_uv, c_kv, k_rope, 0.0625)
+    assert np.allclose(o_lat[0], c_kv[17], rtol=1e-15, atol=1e-300)
+    assert np.allclose(o[0], w_uv[0].T @ c_kv[17], rtol=1e-12)
+
+
+def test_score_shift_invariance():
+    """Adding the same vector u to every k_rope shifts every score by
+    scale * q_rope . u: o is unchanged, lse moves by exactly that."""
+    rng = np.random.default_rng(7)
+    q_nope, q_rope, w_uk, w_uv, c_kv, k_rope = _rand_problem(rng, H=3, n=25)
+    u = rng.standard_normal(O.D_R)
+    o1, lse1, _ = O.attend_non_absorbed(q_nope, q_rope, w_uk, w_uv, c_kv, k_rope, 0.0625)
+    o2, lse2, _ = O.attend_non_absorbed(q_nope, q_rope, w_uk, w_uv, c_kv, k_rope + u, 0.0625)
+    assert np.allclose(o1, o2, rtol=1e-11, atol=1e-13)
+    assert np.allclose(lse2 - lse1, (q_rope @ u) * 0.0625, rtol=1e-11, atol=1e-12)
+
+
+def test_token_permutation_invariance():
+    rng = np.random.default_rng(8)
+    q_nope, q_rope, w_uk, w_uv, c_kv, k_rope = _rand_problem(rng, H=2, n=30)
+    perm = rng.permutation(30)
+    a = O.attend_non_absorbed(q_nope, q_rope, w_uk, w_uv, c_kv, k_rope, 0.0625)
+    b = O.attend_non_absorbed(q_nope, q_rope, w_uk, w_uv, c_kv[perm], k_rope[perm], 0.0625)
+    for x, y in zip(a, b):
+        assert np.allclose(x, y, rtol=1e-12, atol=1e-14)
+
+
+def test_absorbed_equals_non_absorbed():
+    """Associativity: scoring W_UK q_nope against the latent, and up-projecting
+    the latent-space output, is the same as decompressing K and V."""
+    rng = np.random.default_rng(9)
+    q_nope, q_rope, w_uk, w_uv, c_kv, k_rope = _rand_problem(rng, H=5, n=300)
+    a = O.attend_non_absorbed(q_nope, q_rope, w_uk, w_uv, c_kv, k_rope, 0.0625)
+    b = O.attend_absorbed(O.absorb_query(q_nope, w_uk), q_rope, w_uv, c_kv, k_rope, 0.0625)
+    for x, y in zip(a, b):
+        assert np.linalg.norm(x - y) <= 1e-10 * np.linalg.norm(x)
+
+
+def test_absorb_query_brute_force():
+    rng = np.random.default_rng(10)
+    H, Dc, Dn = 2, 6, 3
+    w_uk = rng.standard_normal((H, Dc, Dn))
+    q = rng.standard_normal((H, Dn))
+    got = O.absorb_query(q, w_uk)
+    for h in range(H):
+        for c in range(Dc):
+            ref = sum(w_uk[h, c, n] * q[h, n] for n in range(Dn))
+            assert abs(got[h, c] - ref) < 1e-13
+
+
+def test_split_and_combine_equals_whole():
+    """Attention over a token set equals the LSE-merge of attention over any
+    partition of it (including an empty part)."""
+    rng = np.random.default_rng(12)
+    q_nope, q_rope, w_uk, w_uv, c_kv, k_rope = _rand_problem(rng, H=3, n=90)
+    whole = O.attend_non_absorbed(q_nope, q_rope, w_uk, w_uv, c_kv, k_rope, 0.0625)
+    cuts = [0, 13, 13, 64, 90]
+    parts = [O.attend_non_absorbed(q_nope, q_rope, w_uk, w_uv, c_kv[a:b], k_rope[a:b], 0.0625)
+             for a, b in zip(cuts[:-1], cuts[1:])]
+    o, lse = O.combine_partials([p[2] for p in parts], [p[1] for p in parts])
+    assert np.allclose(lse, whole[1], rtol=1e-13)
+    assert np.allclose(o, whole[2], rtol=1e-12, atol=1e-14)
+
+
+def test_empty_visible_set():
+    rng = np.random.default_rng(13)
+    q_nope, q_rope, w_uk, w_uv, c_kv, k_rope = _rand_problem(rng, H=2, n=0)
+    o, lse, o_lat = O.attend_non_absorbed(q_nope, q_rope, w_uk, w_uv, c_kv, k_rope, 0.0625)
+    assert (o == 0).all() and (o_lat == 0).all() and np.isneginf(lse).all()
+
+
+def test_round_to_bf16_matches_torch():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(14)
+    x = rng.standard_normal(10000) * np.exp(rng.uniform(-30, 30, 10000))
+    x[:4] = [0.0, -0.0, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8]   # ties to even
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(O.round_to_bf16(x), ref)
+
+
+# ---------------------------------------------------------------------------
+# batch driver: paging and sparse handling
+# ---------------------------------------------------------------------------
+def test_decode_page_permutation_invariance():
+    """Relabelling physical pages (with a consistent block table) leaves every
+    output bit-identical."""
+    w = W.with_overrides(W.SMALL_WORKLOADS["dense_small"], batch=2, heads=3)
+    b = W.generate(w)
+    ref = O.decode(b)
+    perm = np.random.default_rng(0).permutation(b.num_pages)
+    inv = np.empty_like(perm)
+    inv[perm] = np.arange(b.num_pages)
+    b.cache_bf16 = b.cache_bf16[perm]        # new page i holds old page perm[i]
+    bt = b.block_table.copy()
+    bt[bt >= 0] = inv[bt[bt >= 0]]
+    b.block_table = bt
+    got = O.decode(b)
+    for k in ref:
+        for x, y in zip(ref[k], got[k]):
+            assert np.array_equal(x, y)
+
+
+def test_decode_sparse_full_window_equals_dense_and_minus_one_is_absent():
+    w = W.with_overrides(W.SMALL_WORKLOADS["sparse_small"], batch=1, heads=2, q_len=2,
+                         seq_lo=300, seq_hi=300, topk=0, topk_pad_slots=0)
+    b = W.generate(w)
+    dense = O.decode(b)
+    # sparse rows listing each query token's full window in order, plus -1 pads
+    ws = W.with_overrides(w, topk=300, topk_pad_slots=84)
+    bs = W.generate(w)
+    bs.workload = ws
+    rows = np.full((2, 384), -1, dtype=np.int32)
+    for j in range(2):
+        vis = np.arange(300 - 2 + j + 1)
+        slots = np.sort(np.random.default_rng(j).choice(384, size=len(vis), replace=False))
+        rows[j, slots] = vis
+    bs.topk_idx = rows
+    sparse = O.decode(bs)
+    for k in dense:
+        for x, y in zip(dense[k], sparse[k]):
+            assert np.allclose(x, y, rtol=1e-12, atol=1e-14)
+
+
+def test_fp8_decode_uses_dequantised_bytes():
+    """The FP8 path of the driver attends over exactly e4m3 * 2**(s-127) of the
+    stored bytes: equal to the bf16-free float path on the dequantised rows."""
+    w = W.with_overrides(W.SMALL_WORKLOADS["fp8_small"], batch=2, heads=2, seq_lo=70,
+                         seq_hi=140)
+    b = W.generate(w)
+    b.extra["cache_fp8"] = F.quantize_pages(b.latent_f32, b.slot_valid)
+    got = O.decode(b)
+    raw = b.extra["cache_fp8"].reshape(b.num_pages, w.page_size, F.ROW_BYTES)
+    for (bi, j), (o, lse, o_lat) in got.items():
+        T = int(b.seq_lens[bi])
+        pages, slots = O.physical_rows(b.block_table[bi], np.arange(T), w.page_size)
+        rows = F.dequant_rows(raw[pages, slots])
+        ref = O.attend_non_absorbed(O.bf16_to_f64(b.q_nope[bi, j]), O.bf16_to_f64(b.q_rope[bi, j]),
+                                    O.bf16_to_f64(b.w_uk), O.bf16_to_f64(b.w_uv),
+                                    rows[:, :512], rows[:, 512:], w.sm_scale)
+        assert np.allclose(o, ref[0], rtol=1e-13, atol=1e-15)
+        # dequantised rows stay close to the float latent they came from
+        assert np.abs(rows - b.latent_f32[pages, slots]).max() < 0.07 * np.abs(rows).max()
+
+
+def test_generator_structure():
+    """Block tables reference distinct in-range pages; live slots match
+    seq_lens; sparse rows hold distinct in-window indices and -1 pads."""
+    for name, w in W.SMALL_WORKLOADS.items():
+        b = W.generate(w)
+        used = b.block_table[b.block_table >= 0]
+        assert len(np.unique(used)) == len(used) and used.max() < b.num_pages
+        assert b.slot_valid.sum() == b.seq_lens.sum()
+        if w.topk:
+            for r in range(w.batch * w.q_len):
+                bi, j = divmod(r, w.q_len)
+                row = b.topk_idx[r]
+                live = row[row >= 0]
+                assert len(np.unique(live)) == len(live) == min(w.topk, int(b.seq_lens[bi]) - w.q_len + j + 1)
+                assert live.max() <= int(b.seq_lens[bi]) - w.q_len + j
+                assert (row == -1).sum() == w.topk_width - len(live)

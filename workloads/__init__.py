@@ -1,0 +1,252 @@
+"""Seeded synthetic inputs for paged MLA latent-cache decode.
+
+This module only draws random tensors with the shapes, sizes and value
+distributions of the decode workloads.  It holds none of the attention
+arithmetic (no query absorption, no scores, no softmax, no quantisation):
+both the CUDA path (through the tests and the benchmark) and the CPU oracle
+consume what it returns.
+
+Geometry (GLM-4.7-Flash record, phantomic12 inference-research, the MLA
+configuration clause): each cached token of one layer holds a 512-dim shared
+latent c_kv (kv_lora_rank) and a 64-dim decoupled RoPE key; queries are split
+into a 192-dim no-RoPE part and a 64-dim RoPE part; the value head is 256.
+
+bf16 tensors are returned as uint16 bit patterns (numpy has no bfloat16).
+
+Draw order for one workload (one ``numpy.random.default_rng(seed)``):
+seq_lens -> block table -> cache -> q_nope -> q_rope -> W_UK -> W_UV ->
+sparse indices.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field, replace
+from typing import Optional
+
+import numpy as np
+
+D_C = 512      # kv_lora_rank: shared latent width
+D_R = 64       # qk_rope_head_dim: decoupled RoPE key width
+D_QK = D_C + D_R  # 576: one cached row
+D_NOPE = 192   # qk_nope_head_dim
+D_V = 256      # v_head_dim
+N_LAYERS = 47  # GLM-4.7-Flash decoder layers
+FP8_GROUP = 32                      # values per e8m0 scale
+FP8_ROW_BYTES = D_QK + D_QK // FP8_GROUP  # 576 e4m3 + 18 e8m0 = 594
+
+BF16_NAN = np.uint16(0x7FC0)
+
+
+# ----------------------------------------------------------------------------
+# bf16 bit-pattern conversion (a dtype cast, not part of the method)
+# ----------------------------------------------------------------------------
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to bf16 (round to nearest, ties to even)."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    rounded = u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))
+    out = (rounded >> np.uint32(16)).astype(np.uint16)
+    nan = np.isnan(x)
+    if nan.any():
+        out[nan] = BF16_NAN
+    return out
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+# ----------------------------------------------------------------------------
+# workloads
+# ----------------------------------------------------------------------------
+@dataclass(frozen=True)
+class Workload:
+    """One decode batch of one layer.
+
+    seq_lens: explicit tuple, or drawn uniformly from [seq_lo, seq_hi]
+    (integers, both ends inclusive).  For the sparse workload every request
+    has the same context length ``seq_lo == seq_hi``.
+    """
+
+    name: str
+    batch: int
+    heads: int
+    q_len: int = 1
+    seq_lens: Optional[tuple] = None
+    seq_lo: int = 0
+    seq_hi: int = 0
+    page_size: int = 64
+    kv_dtype: str = "bf16"          # "bf16" | "fp8"
+    topk: int = 0                   # 0 = dense
+    topk_pad_slots: int = 0         # extra -1 slots (width = topk + pad)
+    causal: bool = True             # draft tokens see their prefix only
+    spare_frac: float = 0.10        # spare physical pages in the pool
+    seed: int = 0
+    sm_scale: float = 1.0 / 16.0    # 1/sqrt(192 + 64)
+
+    @property
+    def topk_width(self) -> int:
+        return self.topk + self.topk_pad_slots if self.topk else 0
+
+    @property
+    def cache_row_bytes(self) -> int:
+        return 2 * D_QK if self.kv_dtype == "bf16" else FP8_ROW_BYTES
+
+
+WORKLOADS = {
+    # batch 2, H=4, seq_lens {37, 130}, page 64, random block table
+    "tiny": Workload("tiny", batch=2, heads=4, seq_lens=(37, 130), page_size=64),
+    # GLM-4.7-Flash-shaped dense decode: B=64, H=20, T~U[1024, 8192], page 64
+    "dense": Workload("dense", batch=64, heads=20, seq_lo=1024, seq_hi=8192, page_size=64),
+    # long-context split-KV: B=8, T~U[65536, 131072], page 128
+    "long": Workload("long", batch=8, heads=20, seq_lo=65536, seq_hi=131072, page_size=128),
+    # FP8 latent (e4m3 + e8m0 per 32): B=128, T~U[2048, 16384], page 64
+    "fp8": Workload("fp8", batch=128, heads=20, seq_lo=2048, seq_hi=16384, page_size=64,
+                    kv_dtype="fp8"),
+    # sparse top-2048, q_len 4 causal drafts, context 65536, page 64
+    "sparse": Workload("sparse", batch=32, heads=20, q_len=4, seq_lo=65536, seq_hi=65536,
+                       page_size=64, topk=2048),
+}
+
+# Reduced sizes the oracle checks element by element: several tiles and a
+# ragged tail per request, both page sizes, a forced split and padded slots.
+SMALL_WORKLOADS = {
+    "tiny": WORKLOADS["tiny"],
+    "dense_small": Workload("dense_small", batch=5, heads=20, seq_lo=65, seq_hi=700,
+                            page_size=64, seed=1),
+    "long_small": Workload("long_small", batch=3, heads=20, seq_lo=2000, seq_hi=5000,
+                           page_size=128, seed=2),
+    "fp8_small": Workload("fp8_small", batch=4, heads=20, seq_lo=100, seq_hi=900,
+                          page_size=64, kv_dtype="fp8", seed=3),
+    "sparse_small": Workload("sparse_small", batch=2, heads=20, q_len=4, seq_lo=1500,
+                             seq_hi=1500, page_size=64, topk=256, topk_pad_slots=128,
+                             seed=4),
+}
+
+
+def with_overrides(w: Workload, **kw) -> Workload:
+    return replace(w, **kw)
+
+
+def draw_seq_lens(w: Workload, rng: np.random.Generator) -> np.ndarray:
+    if w.seq_lens is not None:
+        return np.asarray(w.seq_lens, dtype=np.int32)
+    return rng.integers(w.seq_lo, w.seq_hi, size=w.batch, endpoint=True).astype(np.int32)
+
+
+def _normal_bf16(rng: np.random.Generator, shape, scale: float = 1.0,
+                 chunk: int = 1 << 24) -> np.ndarray:
+    """N(0, scale^2) drawn in float32 and rounded to bf16 bit patterns."""
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.uint16)
+    for s in range(0, n, chunk):
+        e = min(n, s + chunk)
+        x = rng.standard_normal(e - s, dtype=np.float32)
+        if scale != 1.0:
+            x *= np.float32(scale)
+        out[s:e] = f32_to_bf16_bits(x)
+    return out.reshape(shape)
+
+
+def _normal_f32(rng: np.random.Generator, shape, chunk: int = 1 << 24) -> np.ndarray:
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.float32)
+    for s in range(0, n, chunk):
+        e = min(n, s + chunk)
+        out[s:e] = rng.standard_normal(e - s, dtype=np.float32)
+    return out.reshape(shape)
+
+
+@dataclass
+class Batch:
+    """Arrays of one decode batch (host, numpy)."""
+
+    workload: Workload
+    seq_lens: np.ndarray        # int32 [B]
+    block_table: np.ndarray     # int32 [B, max_pages]; unused entries -1
+    num_pages: int
+    slot_valid: np.ndarray      # bool [num_pages, P]: holds a live token
+    cache_bf16: Optional[np.ndarray]  # uint16 [num_pages, P, 576] (bf16 workloads)
+    latent_f32: Optional[np.ndarray]  # float32 [num_pages, P, 576] (fp8 workloads, pre-quantisation)
+    q_nope: np.ndarray          # uint16 bf16 [B, Q, H, 192]
+    q_rope: np.ndarray          # uint16 bf16 [B, Q, H, 64]
+    w_uk: np.ndarray            # uint16 bf16 [H, 512, 192]
+    w_uv: np.ndarray            # uint16 bf16 [H, 512, 256]
+    topk_idx: Optional[np.ndarray]  # int32 [B*Q, width]; -1 = masked slot
+    extra: dict = field(default_factory=dict)
+
+    @property
+    def latent_bytes_read(self) -> int:
+        """Bytes of cached rows the decode must read (one row per visible token,
+        per request for dense; per query token for sparse)."""
+        w = self.workload
+        if w.topk:
+            valid = int((self.topk_idx >= 0).sum())
+            return valid * w.cache_row_bytes
+        return int(self.seq_lens.astype(np.int64).sum()) * w.cache_row_bytes
+
+
+def generate(w: Workload, garbage: str = "finite") -> Batch:
+    """Draw one batch.  ``garbage`` fills slots that hold no live token (tail
+    slots of a request's last page and spare pages): "finite" uses bf16 values
+    of magnitude up to 1e4, "nan" uses bf16 NaN."""
+    rng = np.random.default_rng(w.seed)
+    B, Q, H, P = w.batch, w.q_len, w.heads, w.page_size
+    seq_lens = draw_seq_lens(w, rng)
+    pages_per_req = (seq_lens.astype(np.int64) + P - 1) // P
+    used = int(pages_per_req.sum())
+    num_pages = max(1, int(np.ceil(used * (1.0 + w.spare_frac))))
+    max_pages = max(1, int(pages_per_req.max()) if B else 1)
+    perm = rng.permutation(num_pages).astype(np.int32)
+    block_table = np.full((B, max_pages), -1, dtype=np.int32)
+    slot_valid = np.zeros((num_pages, P), dtype=bool)
+    cursor = 0
+    for b in range(B):
+        n = int(pages_per_req[b])
+        block_table[b, :n] = perm[cursor:cursor + n]
+        cursor += n
+        for j in range(n):
+            live = min(P, int(seq_lens[b]) - j * P)
+            slot_valid[block_table[b, j], :live] = True
+
+    cache_bf16 = latent_f32 = None
+    if w.kv_dtype == "bf16":
+        cache_bf16 = _normal_bf16(rng, (num_pages, P, D_QK))
+    else:
+        latent_f32 = _normal_f32(rng, (num_pages, P, D_QK))
+    inv = ~slot_valid
+    if inv.any():
+        n_inv = int(inv.sum())
+        if garbage == "nan":
+            fill_bits = np.full((n_inv, D_QK), BF16_NAN, dtype=np.uint16)
+            fill_f32 = np.full((n_inv, D_QK), np.nan, dtype=np.float32)
+        else:
+            fill_f32 = rng.uniform(-1e4, 1e4, size=(n_inv, D_QK)).astype(np.float32)
+            fill_bits = f32_to_bf16_bits(fill_f32)
+        if cache_bf16 is not None:
+            cache_bf16[inv] = fill_bits
+        else:
+            latent_f32[inv] = fill_f32
+
+    q_nope = _normal_bf16(rng, (B, Q, H, D_NOPE))
+    q_rope = _normal_bf16(rng, (B, Q, H, D_R))
+    w_uk = _normal_bf16(rng, (H, D_C, D_NOPE), scale=1.0 / np.sqrt(D_C))
+    w_uv = _normal_bf16(rng, (H, D_C, D_V), scale=1.0 / np.sqrt(D_C))
+
+    topk_idx = None
+    if w.topk:
+        width = w.topk_width
+        topk_idx = np.full((B * Q, width), -1, dtype=np.int32)
+        for b in range(B):
+            for j in range(Q):
+                window = int(seq_lens[b]) - Q + j + 1 if w.causal else int(seq_lens[b])
+                k = min(w.topk, window)
+                picks = rng.choice(window, size=k, replace=False).astype(np.int32)
+                row = np.full(width, -1, dtype=np.int32)
+                if w.topk_pad_slots:
+                    slots = np.sort(rng.choice(width, size=k, replace=False))
+                    row[slots] = picks
+                else:
+                    row[:k] = picks
+                topk_idx[b * Q + j] = row
+
+    return Batch(w, seq_lens, block_table, num_pages, slot_valid, cache_bf16, latent_f32,
+                 q_nope, q_rope, w_uk, w_uv, topk_idx)
