@@ -1,0 +1,183 @@
+"""Python binding of libmla_gb300.so (paged MLA latent-cache decode, sm_103a).
+
+Argument marshalling only: every step of the decode runs in the library's
+CUDA kernels.  Functions mirror the C ABI in include/mla_decode.h and take
+device addresses as ints (or any object with ``data_ptr()``, e.g. a torch
+tensor) and CUDA streams as ints (``torch.cuda.current_stream().cuda_stream``)
+or None for the default stream.  There is no fallback: if the library cannot
+be loaded every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmla_gb300.so")
+
+MLA_OK = 0
+MLA_ERR_INVALID_ARGUMENT = -1
+MLA_ERR_UNSUPPORTED = -2
+MLA_ERR_MISALIGNED = -3
+MLA_ERR_WORKSPACE_TOO_SMALL = -4
+MLA_ERR_CUDA = -5
+
+MLA_KV_BF16 = 0
+MLA_KV_FP8_E4M3_E8M0 = 1
+
+MLA_STATUS_BAD_PAGE = 0x1
+MLA_STATUS_BAD_INDEX = 0x2
+MLA_STATUS_TIMEOUT = 0x4
+
+MLA_TILE_TOKENS = 64
+
+EXPORTED = (
+    "mla_decode_plan", "mla_q_absorb", "mla_decode_run", "mla_combine", "mla_uv_proj",
+    "mla_get_status", "mla_clear_status", "mla_strerror", "mla_version",
+)
+
+
+class MlaProblem(ctypes.Structure):
+    _fields_ = [
+        ("batch", ctypes.c_int32), ("q_len", ctypes.c_int32), ("num_heads", ctypes.c_int32),
+        ("kv_lora_rank", ctypes.c_int32), ("rope_dim", ctypes.c_int32),
+        ("nope_dim", ctypes.c_int32), ("v_head_dim", ctypes.c_int32),
+        ("page_size", ctypes.c_int32), ("num_pages", ctypes.c_int32),
+        ("max_pages_per_seq", ctypes.c_int32), ("kv_dtype", ctypes.c_int32),
+        ("topk_width", ctypes.c_int32), ("causal", ctypes.c_int32), ("sm_scale", ctypes.c_float),
+    ]
+
+
+class MlaPlan(ctypes.Structure):
+    _fields_ = [
+        ("problem", MlaProblem), ("num_streams", ctypes.c_int32), ("num_ctas", ctypes.c_int32),
+        ("num_slots", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
+        ("ws_partial_o", ctypes.c_int64), ("ws_partial_lse", ctypes.c_int64),
+        ("ws_status", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64),
+        ("planned_tiles", ctypes.c_int64), ("reserved", ctypes.c_int32 * 8),
+    ]
+
+
+class MlaError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        self.code = code
+        super().__init__(f"{fn} failed: {code} ({strerror(code)})")
+
+
+_lib = None
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load the shared library (once).  Raises if it is missing."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"{p} is missing: build it with __graft_entry__.build()")
+    lib = ctypes.CDLL(p)
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    P = ctypes.POINTER
+    lib.mla_decode_plan.argtypes = [P(MlaProblem), P(ctypes.c_int32), i32, P(MlaPlan)]
+    lib.mla_q_absorb.argtypes = [P(MlaPlan), vp, vp, vp, vp, vp]
+    lib.mla_decode_run.argtypes = [P(MlaPlan), vp, vp, vp, vp, vp, vp, vp]
+    lib.mla_combine.argtypes = [P(MlaPlan), vp, vp, vp, vp, vp]
+    lib.mla_uv_proj.argtypes = [vp, vp, vp, i32, i32, vp]
+    lib.mla_get_status.argtypes = [P(MlaPlan), vp, P(ctypes.c_uint32), vp]
+    lib.mla_clear_status.argtypes = [P(MlaPlan), vp, vp]
+    lib.mla_strerror.argtypes = [ctypes.c_int]
+    lib.mla_strerror.restype = ctypes.c_char_p
+    lib.mla_version.argtypes = []
+    for name in EXPORTED:
+        if name not in ("mla_strerror",):
+            getattr(lib, name).restype = ctypes.c_int
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _ptr(x) -> Optional[int]:
+    if x is None:
+        return None
+    if hasattr(x, "data_ptr"):
+        return int(x.data_ptr())
+    return int(x)
+
+
+def _stream(s) -> Optional[int]:
+    if s is None:
+        return None
+    if hasattr(s, "cuda_stream"):
+        return int(s.cuda_stream)
+    return int(s)
+
+
+def _check(fn: str, rc: int) -> None:
+    if rc != MLA_OK:
+        raise MlaError(fn, rc)
+
+
+def strerror(code: int) -> str:
+    return load().mla_strerror(code).decode()
+
+
+def version() -> int:
+    return load().mla_version()
+
+
+def make_problem(batch, q_len, num_heads, page_size, num_pages, max_pages_per_seq,
+                 kv_dtype=MLA_KV_BF16, topk_width=0, causal=1, sm_scale=1.0 / 16.0,
+                 kv_lora_rank=512, rope_dim=64, nope_dim=192, v_head_dim=256) -> MlaProblem:
+    return MlaProblem(batch, q_len, num_heads, kv_lora_rank, rope_dim, nope_dim, v_head_dim,
+                      page_size, num_pages, max_pages_per_seq, kv_dtype, topk_width, causal,
+                      sm_scale)
+
+
+def mla_decode_plan(problem: MlaProblem, seq_lens_host=None, sm_count: int = 152) -> MlaPlan:
+    plan = MlaPlan()
+    arr = None
+    if seq_lens_host is not None:
+        arr = np.ascontiguousarray(seq_lens_host, dtype=np.int32)
+        ptr = arr.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+    else:
+        ptr = None
+    _check("mla_decode_plan", load().mla_decode_plan(ctypes.byref(problem), ptr, int(sm_count),
+                                                     ctypes.byref(plan)))
+    return plan
+
+
+def mla_q_absorb(plan: MlaPlan, q_nope, q_rope, w_uk, q_hat, stream=None) -> None:
+    _check("mla_q_absorb", load().mla_q_absorb(ctypes.byref(plan), _ptr(q_nope), _ptr(q_rope),
+                                               _ptr(w_uk), _ptr(q_hat), _stream(stream)))
+
+
+def mla_decode_run(plan: MlaPlan, q_hat, kv_cache, block_table, seq_lens, topk_idx, workspace,
+                   stream=None) -> None:
+    _check("mla_decode_run", load().mla_decode_run(
+        ctypes.byref(plan), _ptr(q_hat), _ptr(kv_cache), _ptr(block_table), _ptr(seq_lens),
+        _ptr(topk_idx), _ptr(workspace), _stream(stream)))
+
+
+def mla_combine(plan: MlaPlan, seq_lens, workspace, o_lat, lse, stream=None) -> None:
+    _check("mla_combine", load().mla_combine(ctypes.byref(plan), _ptr(seq_lens), _ptr(workspace),
+                                             _ptr(o_lat), _ptr(lse), _stream(stream)))
+
+
+def mla_uv_proj(o_lat, w_uv, out, rows: int, num_heads: int, stream=None) -> None:
+    _check("mla_uv_proj", load().mla_uv_proj(_ptr(o_lat), _ptr(w_uv), _ptr(out), int(rows),
+                                             int(num_heads), _stream(stream)))
+
+
+def mla_get_status(plan: MlaPlan, workspace, stream=None) -> int:
+    bits = ctypes.c_uint32(0)
+    _check("mla_get_status", load().mla_get_status(ctypes.byref(plan), _ptr(workspace),
+                                                   ctypes.byref(bits), _stream(stream)))
+    return int(bits.value)
+
+
+def mla_clear_status(plan: MlaPlan, workspace, stream=None) -> None:
+    _check("mla_clear_status", load().mla_clear_status(ctypes.byref(plan), _ptr(workspace),
+                                                       _stream(stream)))

@@ -1,0 +1,94 @@
+// Internal declarations shared by the host API and the kernel launchers.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/mla_decode.h"
+
+namespace mla {
+
+constexpr int kDc = 512;          // latent width
+constexpr int kDr = 64;           // RoPE key width
+constexpr int kDqk = kDc + kDr;   // 576: one cached row
+constexpr int kDnope = 192;
+constexpr int kDv = 256;
+constexpr int kTile = MLA_TILE_TOKENS;   // 64 cached rows per tile
+constexpr int kChunkElems = 64;           // one 128-byte swizzle row of bf16
+constexpr int kChunks = kDqk / kChunkElems;  // 9
+constexpr int kChunkBytes = kTile * 128;     // 8 KB: 64 rows x 128 B
+constexpr int kTileBytes = kChunks * kChunkBytes;  // 73,728
+constexpr int kFp8RowBytes = kDqk + kDqk / 32;     // 594
+constexpr int kMaxHeads = 48;
+constexpr int kMaxStreams = 1024;
+constexpr int kStages = 2;
+
+enum DecodeMode : int { kModeDenseBf16 = 0, kModeSparseBf16 = 1, kModeDenseFp8 = 2 };
+
+struct DecodeParams {
+  const uint16_t* q_hat;        // bf16 [S][H][576]
+  const uint8_t* kv;            // cache base (bytes)
+  const int32_t* block_table;   // [B][max_pages]
+  const int32_t* seq_lens;      // [B]
+  const int32_t* topk_idx;      // [S][width] or null
+  float* part_o;                // [slots][H][512]
+  float* part_lse;              // [slots][H]
+  uint32_t* status;
+  int32_t batch, q_len, heads, heads_pad;  // heads_pad: N of the PV MMA (multiple of 16)
+  int32_t page_size, num_pages, max_pages, topk_width, causal;
+  int32_t num_streams, num_ctas;
+  float scale_log2;             // sm_scale * log2(e)
+};
+
+struct DecodeLayout {   // dynamic shared memory layout of the decode kernel
+  int32_t q_group_bytes;  // ceil(H/8) * 1024: stride between K-chunks of Q
+  int32_t q_buf_bytes;    // one stream's queries: 9 chunks
+  int32_t q_bufs;         // 1 or 2 query buffers
+  int32_t off_q, off_stage, off_p, off_ctrl, total;
+};
+
+DecodeLayout decode_layout(int heads, int heads_pad, int num_streams, int mode);
+int decode_smem_bytes(int heads, int heads_pad, int num_streams, int mode);
+
+cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap* kv_map,
+                          const CUtensorMap* q_map, int mode, cudaStream_t stream);
+
+struct CombineParams {
+  const float* part_o;
+  const float* part_lse;
+  const int32_t* seq_lens;
+  float* o_lat;
+  float* lse;
+  int32_t batch, q_len, heads, page_size, max_pages, topk_width, causal;
+  int32_t num_streams, num_ctas;
+};
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
+
+cudaError_t launch_uv_proj_tma(const CUtensorMap* w_map, const float* o_lat, uint16_t* out,
+                               int rows, int heads, cudaStream_t stream);
+
+cudaError_t launch_q_absorb(const uint16_t* q_nope, const uint16_t* q_rope,
+                            const uint16_t* w_uk, uint16_t* q_hat, int rows, int heads,
+                            cudaStream_t stream);
+
+// Tiles of one (request, query token) row set; identical on host and device.
+__host__ __device__ inline int32_t stream_len(int32_t seq_len, int32_t q_len, int32_t j,
+                                              int32_t causal, int32_t topk_width,
+                                              int32_t max_tokens) {
+  if (topk_width > 0) return topk_width;
+  int32_t t = seq_len < 0 ? 0 : (seq_len > max_tokens ? max_tokens : seq_len);
+  if (causal) {
+    int32_t v = t - q_len + j + 1;
+    t = v < 0 ? 0 : (v > t ? t : v);
+  }
+  return t;
+}
+
+// CTA that owns global tile x when `total` tiles are split over `ctas` CTAs
+// as [c*total/ctas, (c+1)*total/ctas).
+__host__ __device__ inline int32_t tile_owner(int64_t x, int64_t total, int32_t ctas) {
+  return static_cast<int32_t>(((x + 1) * ctas - 1) / total);
+}
+
+}  // namespace mla

@@ -1,0 +1,210 @@
+/*
+ * mla_decode.h -- C ABI of the GB300 (sm_103a) paged MLA latent-cache decode
+ * library (libmla_gb300.so).
+ *
+ * The operation: Multi-head Latent Attention decode over a paged, low-rank
+ * latent KV cache.  Each cached token of a layer holds a shared 512-dim latent
+ * c_kv and a decoupled 64-dim RoPE key, not per-head K/V (GLM-4.7-Flash
+ * record, phantomic12 inference-research: the MLA family paragraph and the
+ * configuration clause kv_lora_rank 512 / qk_rope_head_dim 64 /
+ * qk_nope_head_dim 192 / v_head_dim 256; 576 bf16 values = 1,152 bytes per
+ * token and layer, 54,144 bytes per token over 47 layers).  The per-head
+ * query is absorbed into the 576-dim latent space through W_UK (the kv_b_proj
+ * up-projection), scored against every visible cached row, softmaxed, the
+ * weighted latent rows are summed (o_lat) and finally up-projected through
+ * W_UV:
+ *
+ *     q_hat[h]  = [W_UK[h] q_nope[h] || q_rope[h]]                 (576)
+ *     s[h,t]    = sm_scale * q_hat[h] . row[t]                      row = [c_kv || k_rope]
+ *     lse[h]    = ln sum_t exp(s[h,t])
+ *     o_lat[h]  = sum_t exp(s[h,t] - lse[h]) c_kv[t]                 (512)
+ *     o[h]      = W_UV[h]^T o_lat[h]                                 (256)
+ *
+ * Paged cache: logical position t of request b is slot t % P of physical page
+ * block_table[b][t / P]; P is 64 or 128 (fix: Add glm4_moe_lite to MLA
+ * detection, the note that CUTLASS_MLA enforces block_size=128; GLM-4.7-Flash
+ * record: decode kernels are instantiated per KV cache page-block size and a
+ * planner hard-codes 64).  The call split plan / run mirrors the
+ * planner + kernel split of the FlashInfer MLA decode the record describes.
+ *
+ * Conventions for every entry point:
+ *   - The caller owns every buffer.  The library allocates no device memory;
+ *     `mla_plan` is a plain struct the caller keeps.
+ *   - Device pointers are CUDA device addresses on the current device and
+ *     must be 16-byte aligned (TMA and bulk copies require it).
+ *   - Every call that takes a stream is asynchronous on that stream
+ *     (NULL = the legacy default stream) unless stated otherwise.
+ *   - Return value 0 is success; a negative MLA_ERR_* code means nothing was
+ *     launched (argument errors) or a launch failed (MLA_ERR_CUDA).  No
+ *     exception or abort crosses the ABI.
+ *   - Data errors found on the device (a block-table entry outside
+ *     [0, num_pages), a sparse index outside [-1, visible window)) never
+ *     fault: the offending rows are masked out and a sticky bit is set in the
+ *     status word read by mla_get_status.
+ */
+#ifndef MLA_DECODE_H_
+#define MLA_DECODE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MLA_API __attribute__((visibility("default")))
+#else
+#define MLA_API
+#endif
+
+/* A cudaStream_t. */
+typedef struct CUstream_st* mla_stream_t;
+
+/* return codes */
+#define MLA_OK 0
+#define MLA_ERR_INVALID_ARGUMENT (-1)   /* null pointer, negative or inconsistent size */
+#define MLA_ERR_UNSUPPORTED (-2)        /* a shape or option this library does not implement */
+#define MLA_ERR_MISALIGNED (-3)         /* a device pointer not 16-byte aligned */
+#define MLA_ERR_WORKSPACE_TOO_SMALL (-4)
+#define MLA_ERR_CUDA (-5)               /* a CUDA runtime / driver call or launch failed */
+
+/* latent-cache element formats */
+#define MLA_KV_BF16 0
+/* 576 float8_e4m3 values followed by 18 float8_e8m0 scales (one per 32
+ * consecutive values, value = e4m3 * 2^(scale - 127)) per token: 594 bytes
+ * per token, a page of P tokens is P contiguous rows.  All 576 dims are
+ * quantised, RoPE dims included (GLM-4.7-Flash record, engine-kernel
+ * constraint (2): FP8 latent with per-token inlined e8m0 scales, one per 32
+ * e4m3 values). */
+#define MLA_KV_FP8_E4M3_E8M0 1
+
+/* status-word bits (sticky until mla_clear_status) */
+#define MLA_STATUS_BAD_PAGE 0x1u     /* a block-table entry outside [0, num_pages) was masked */
+#define MLA_STATUS_BAD_INDEX 0x2u    /* a sparse index outside [-1, window) was masked */
+#define MLA_STATUS_TIMEOUT 0x4u      /* an internal pipeline wait hit its time limit */
+
+#define MLA_TILE_TOKENS 64           /* cached rows per pipeline tile */
+
+/* One decode step of one layer.  All sizes are element counts. */
+typedef struct {
+  int32_t batch;            /* B: requests */
+  int32_t q_len;            /* Q: query tokens per request (speculative drafts), >= 1 */
+  int32_t num_heads;        /* H: query heads, 1..48 */
+  int32_t kv_lora_rank;     /* must be 512 */
+  int32_t rope_dim;         /* must be 64 */
+  int32_t nope_dim;         /* must be 192 (only read by mla_q_absorb) */
+  int32_t v_head_dim;       /* must be 256 */
+  int32_t page_size;        /* P: 64 or 128 */
+  int32_t num_pages;        /* physical pages in the cache pool */
+  int32_t max_pages_per_seq;/* row stride of block_table */
+  int32_t kv_dtype;         /* MLA_KV_BF16 or MLA_KV_FP8_E4M3_E8M0 */
+  int32_t topk_width;       /* 0: dense; else sparse row width, a multiple of 128
+                               (vllm API docs, vllm.models.glm5next.common.model,
+                               Glm5NextModel.__init__: top-k is tiled in 128
+                               columns and padded slots stay masked) */
+  int32_t causal;           /* 1: query token j sees positions <= T_b - Q + j;
+                               0: every query token sees all T_b positions */
+  float sm_scale;           /* softmax scale on q_hat . row; 1/sqrt(192 + 64) for GLM-4.7-Flash */
+} mla_problem;
+
+/* Filled by mla_decode_plan; treat as opaque, keep it alive while in use. */
+typedef struct {
+  mla_problem problem;
+  int32_t num_streams;      /* B * Q: independent (request, query token) row sets */
+  int32_t num_ctas;         /* decode grid size */
+  int32_t num_slots;        /* partial-result slots: num_streams + num_ctas - 1 */
+  int32_t smem_bytes;       /* dynamic shared memory of the decode kernel */
+  int64_t ws_partial_o;     /* byte offset of f32 [num_slots][H][512] */
+  int64_t ws_partial_lse;   /* byte offset of f32 [num_slots][H] */
+  int64_t ws_status;        /* byte offset of the uint32 status word */
+  int64_t workspace_bytes;  /* total workspace size */
+  int64_t planned_tiles;    /* tiles implied by seq_lens_host (0 if not given) */
+  int32_t reserved[8];
+} mla_plan;
+
+/*
+ * mla_decode_plan -- validate a problem and build the launch plan (host only,
+ * no CUDA call).
+ *   problem        : the step's shape and options (copied into the plan).
+ *   seq_lens_host  : host int32 [batch] context lengths, or NULL.  Used only to
+ *                    size the grid: the device kernels re-derive the exact
+ *                    work split from the device seq_lens they are given.
+ *   sm_count       : streaming multiprocessors to fill (152 on GB300); > 0.
+ *   plan_out       : written on success.
+ * Returns MLA_OK, MLA_ERR_INVALID_ARGUMENT or MLA_ERR_UNSUPPORTED.
+ */
+MLA_API int mla_decode_plan(const mla_problem* problem, const int32_t* seq_lens_host,
+                    int32_t sm_count, mla_plan* plan_out);
+
+/*
+ * mla_q_absorb -- q_hat[r][h] = [bf16(W_UK[h] q_nope[r][h]) || q_rope[r][h]]
+ * (weight absorption of the kv_b_proj key half into the query; fp32
+ * accumulation, one rounding to bf16).  r = b * Q + j.
+ *   q_nope : bf16 [B*Q][H][192];  q_rope : bf16 [B*Q][H][64]
+ *   w_uk   : bf16 [H][512][192]   (k_nope[t] = W_UK[h]^T c_kv[t])
+ *   q_hat  : bf16 [B*Q][H][576]   output
+ */
+MLA_API int mla_q_absorb(const mla_plan* plan, const void* q_nope, const void* q_rope,
+                 const void* w_uk, void* q_hat, mla_stream_t stream);
+
+/*
+ * mla_decode_run -- the attention pass over the paged cache.  Writes, for
+ * every (request, query token) row set and every KV split of it that this
+ * plan's grid produces, a partial result (normalised latent output and its
+ * natural-log LSE) into the workspace.  mla_combine turns them into o_lat.
+ *   q_hat       : bf16 [B*Q][H][576] absorbed queries
+ *   kv_cache    : MLA_KV_BF16: bf16 [num_pages][P][576];
+ *                 MLA_KV_FP8_E4M3_E8M0: uint8 [num_pages][P * 594]
+ *   block_table : int32 [B][max_pages_per_seq]; entries past a request's
+ *                 last page are never read
+ *   seq_lens    : device int32 [B], 0 <= T_b <= max_pages_per_seq * P
+ *   topk_idx    : NULL for dense; sparse: int32 [B*Q][topk_width] logical
+ *                 positions of the request, -1 = masked slot
+ *   workspace   : device buffer of plan->workspace_bytes, zeroed once before
+ *                 its first use (the status word must start at 0)
+ * Returns MLA_OK, MLA_ERR_INVALID_ARGUMENT, MLA_ERR_MISALIGNED,
+ * MLA_ERR_UNSUPPORTED or MLA_ERR_CUDA.
+ */
+MLA_API int mla_decode_run(const mla_plan* plan, const void* q_hat, const void* kv_cache,
+                   const int32_t* block_table, const int32_t* seq_lens,
+                   const int32_t* topk_idx, void* workspace, mla_stream_t stream);
+
+/*
+ * mla_combine -- merge the partial results of each row set: lse = ln sum_i
+ * exp(lse_i), o_lat = sum_i exp(lse_i - lse) o_i.  A row set with no visible
+ * token gets o_lat = 0 and lse = -inf.
+ *   seq_lens : the same device int32 [B] given to mla_decode_run
+ *   o_lat    : f32 [B*Q][H][512] output;  lse : f32 [B*Q][H] output
+ */
+MLA_API int mla_combine(const mla_plan* plan, const int32_t* seq_lens, const void* workspace,
+                float* o_lat, float* lse, mla_stream_t stream);
+
+/*
+ * mla_uv_proj -- o[r][h] = bf16(W_UV[h]^T o_lat[r][h]) (the kv_b_proj value
+ * half applied after attention, in latent space).
+ *   o_lat : f32 [rows][num_heads][512];  w_uv : bf16 [num_heads][512][256]
+ *   out   : bf16 [rows][num_heads][256]
+ * rows >= 0, 1 <= num_heads <= 128.
+ */
+MLA_API int mla_uv_proj(const float* o_lat, const void* w_uv, void* out, int32_t rows,
+                int32_t num_heads, mla_stream_t stream);
+
+/* Synchronous read of the device status word (waits for `stream`). */
+MLA_API int mla_get_status(const mla_plan* plan, const void* workspace, uint32_t* bits,
+                   mla_stream_t stream);
+
+/* Zero the status word (asynchronous). */
+MLA_API int mla_clear_status(const mla_plan* plan, void* workspace, mla_stream_t stream);
+
+/* Static description of an error code; never NULL. */
+MLA_API const char* mla_strerror(int code);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+MLA_API int mla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_DECODE_H_ */

@@ -1,0 +1,82 @@
+"""Shared helpers for the GPU parity tests: run a workload through the C ABI
+and compare with the CPU oracle."""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle as O
+from oracle import fp8 as F
+import workloads as W
+
+# Tolerances for the bf16 and FP8 paths: max |err| <= 2e-2 and relative L2
+# <= 5e-3 on outputs, |lse err| <= 1e-3 (natural log).
+ATOL_MAX = 2e-2
+REL_L2 = 5e-3
+LSE_TOL = 1e-3
+
+
+def ensure_built():
+    from head_latent_attention_paged_gb300 import _build
+    _build.build()
+
+
+def make_step(batch: W.Batch, sm_count=None, absorb=True, device="cuda:0", fp8_bytes=None):
+    from head_latent_attention_paged_gb300 import MLA_KV_BF16, MLA_KV_FP8_E4M3_E8M0
+    from head_latent_attention_paged_gb300.runner import DecodeStep
+    w = batch.workload
+    if w.kv_dtype == "fp8":
+        cache = fp8_bytes if fp8_bytes is not None else batch.extra["cache_fp8"]
+        kv_dtype = MLA_KV_FP8_E4M3_E8M0
+    else:
+        cache = batch.cache_bf16
+        kv_dtype = MLA_KV_BF16
+    return DecodeStep(q_nope=batch.q_nope, q_rope=batch.q_rope, w_uk=batch.w_uk, w_uv=batch.w_uv,
+                      cache=cache, block_table=batch.block_table, seq_lens=batch.seq_lens,
+                      page_size=w.page_size, kv_dtype=kv_dtype, topk_idx=batch.topk_idx,
+                      causal=w.causal, sm_scale=w.sm_scale, sm_count=sm_count, device=device,
+                      absorb_on_device=absorb)
+
+
+def gpu_outputs(step):
+    import torch
+    torch.cuda.synchronize()
+    o = step.out.float().cpu().numpy().reshape(step.B, step.Q, step.H, 256)
+    o_lat = step.o_lat.cpu().numpy().reshape(step.B, step.Q, step.H, 512)
+    lse = step.lse.cpu().numpy().reshape(step.B, step.Q, step.H)
+    return o, o_lat, lse
+
+
+def compare(ref: dict, o, o_lat, lse, heads=None, label=""):
+    """Check every (b, j) the oracle computed.  Returns the worst figures."""
+    worst = {"max_abs": 0.0, "rel_l2": 0.0, "lse": 0.0, "lat_rel_l2": 0.0}
+    for (b, j), (ro, rlse, rlat) in ref.items():
+        hs = slice(None) if heads is None else list(heads)
+        go, glat, glse = o[b, j][hs], o_lat[b, j][hs], lse[b, j][hs]
+        if np.all(np.isneginf(rlse)):
+            assert np.all(np.isneginf(glse)), (label, b, j, glse)
+            assert np.all(go == 0) and np.all(glat == 0), (label, b, j)
+            continue
+        ro_b = O.round_to_bf16(ro)
+        err = np.abs(go - ro_b)
+        assert np.isfinite(go).all() and np.isfinite(glat).all(), (label, b, j)
+        max_abs = float(err.max())
+        rel = float(np.linalg.norm(go - ro) / max(np.linalg.norm(ro), 1e-30))
+        lat_rel = float(np.linalg.norm(glat - rlat) / max(np.linalg.norm(rlat), 1e-30))
+        lse_err = float(np.abs(glse - rlse).max())
+        worst["max_abs"] = max(worst["max_abs"], max_abs)
+        worst["rel_l2"] = max(worst["rel_l2"], rel)
+        worst["lat_rel_l2"] = max(worst["lat_rel_l2"], lat_rel)
+        worst["lse"] = max(worst["lse"], lse_err)
+        assert max_abs <= ATOL_MAX, (label, b, j, "max abs", max_abs)
+        assert rel <= REL_L2, (label, b, j, "rel L2", rel)
+        assert lat_rel <= REL_L2, (label, b, j, "latent rel L2", lat_rel)
+        assert lse_err <= LSE_TOL, (label, b, j, "lse", lse_err)
+    return worst
+
+
+def with_fp8(batch: W.Batch, garbage="finite") -> W.Batch:
+    """Attach the paged FP8 bytes (oracle quantiser) to an FP8 workload."""
+    if batch.workload.kv_dtype == "fp8" and "cache_fp8" not in batch.extra:
+        batch.extra["cache_fp8"] = F.quantize_pages(batch.latent_f32, batch.slot_valid,
+                                                    rng_seed=batch.workload.seed, garbage=garbage)
+    return batch

@@ -1,0 +1,148 @@
+"""The C ABI on the CPU: the library loads without a GPU, exports every entry
+point the header declares, and rejects bad arguments with error codes before
+any CUDA call."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def m():
+    from head_latent_attention_paged_gb300 import _build
+    _build.build()
+    import head_latent_attention_paged_gb300 as mod
+    mod.load()
+    return mod
+
+
+def _declared_entry_points():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", f)).read()
+            names |= set(re.findall(r"MLA_API\s+[\w\s\*]+?\b(mla_\w+)\s*\(", text))
+    return names
+
+
+def test_library_exports_every_declared_symbol(m):
+    declared = _declared_entry_points()
+    assert {"mla_decode_plan", "mla_decode_run", "mla_combine", "mla_uv_proj"} <= declared
+    lib = ctypes.CDLL(m.LIB_PATH)
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert declared == set(m.EXPORTED)
+
+
+def test_version_and_strerror(m):
+    assert m.version() == 10000
+    for code in (0, -1, -2, -3, -4, -5, -99):
+        assert isinstance(m.strerror(code), str) and m.strerror(code)
+
+
+def _problem(m, **kw):
+    base = dict(batch=4, q_len=1, num_heads=20, page_size=64, num_pages=100, max_pages_per_seq=30)
+    base.update(kw)
+    return m.make_problem(**base)
+
+
+def test_plan_ok_and_workspace_layout(m):
+    seq = np.array([100, 1000, 64, 0], dtype=np.int32)
+    plan = m.mla_decode_plan(_problem(m), seq, 152)
+    tiles = sum((int(t) + 63) // 64 for t in seq)
+    assert plan.planned_tiles == tiles
+    assert plan.num_ctas == min(152, tiles)
+    assert plan.num_slots == 4 + plan.num_ctas - 1
+    assert plan.ws_partial_o == 0
+    assert plan.ws_partial_lse >= plan.num_slots * 20 * 512 * 4
+    assert plan.ws_status >= plan.ws_partial_lse + plan.num_slots * 20 * 4
+    assert plan.workspace_bytes > plan.ws_status
+    assert plan.smem_bytes <= 232448
+    # no host seq_lens: fill every SM
+    assert m.mla_decode_plan(_problem(m), None, 152).num_ctas == 152
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(page_size=96), -2), (dict(page_size=32), -2), (dict(num_heads=0), -1),
+    (dict(num_heads=49), -2), (dict(q_len=0), -1), (dict(batch=-1), -1),
+    (dict(topk_width=100), -2), (dict(topk_width=-128), -1), (dict(kv_lora_rank=256), -2),
+    (dict(rope_dim=32), -2), (dict(v_head_dim=128), -2), (dict(nope_dim=128), -2),
+    (dict(causal=2), -1), (dict(sm_scale=0.0), -1), (dict(sm_scale=float("nan")), -1),
+    (dict(num_pages=0), -1), (dict(max_pages_per_seq=0), -1), (dict(batch=2000), -2),
+])
+def test_plan_rejects(m, kw, code):
+    with pytest.raises(m.MlaError) as e:
+        m.mla_decode_plan(_problem(m, **kw), None, 152)
+    assert e.value.code == code
+
+
+def test_plan_rejects_negative_seq_len_and_bad_sm_count(m):
+    with pytest.raises(m.MlaError) as e:
+        m.mla_decode_plan(_problem(m), np.array([1, -2, 3, 4], dtype=np.int32), 152)
+    assert e.value.code == -1
+    with pytest.raises(m.MlaError) as e:
+        m.mla_decode_plan(_problem(m), None, 0)
+    assert e.value.code == -1
+
+
+def test_calls_reject_null_and_misaligned_pointers_before_cuda(m):
+    plan = m.mla_decode_plan(_problem(m), None, 152)
+    A = 1 << 20    # an aligned fake address: never dereferenced, the call fails first
+    with pytest.raises(m.MlaError) as e:
+        m.mla_decode_run(plan, None, A, A, A, None, A)
+    assert e.value.code == -1
+    with pytest.raises(m.MlaError) as e:   # dense problem given a top-k list
+        m.mla_decode_run(plan, A, A, A, A, A, A)
+    assert e.value.code == -1
+    with pytest.raises(m.MlaError) as e:
+        m.mla_decode_run(plan, A + 8, A, A, A, None, A)
+    assert e.value.code == -3
+    with pytest.raises(m.MlaError) as e:
+        m.mla_combine(plan, A, A, A + 4, A)
+    assert e.value.code == -3
+    with pytest.raises(m.MlaError) as e:
+        m.mla_uv_proj(A, A, A, -1, 20)
+    assert e.value.code == -1
+    with pytest.raises(m.MlaError) as e:
+        m.mla_uv_proj(A, A + 2, A, 4, 20)
+    assert e.value.code == -3
+    with pytest.raises(m.MlaError) as e:
+        m.mla_q_absorb(plan, A, None, A, A)
+    assert e.value.code == -1
+    sparse = m.mla_decode_plan(_problem(m, topk_width=256), None, 152)
+    with pytest.raises(m.MlaError) as e:   # sparse problem without a top-k list
+        m.mla_decode_run(sparse, A, A, A, A, None, A)
+    assert e.value.code == -1
+
+
+def test_stream_split_matches_kernel_rule():
+    """Host restatement of the tile split the kernels use: CTA c owns global
+    tiles [c*T/C, (c+1)*T/C); every tile has exactly one owner and partial
+    slot s + c is unique for every (stream, CTA) pair that shares a tile."""
+    rng = np.random.default_rng(0)
+    for _ in range(50):
+        S = int(rng.integers(1, 40))
+        tiles = rng.integers(0, 30, size=S)
+        T = int(tiles.sum())
+        if T == 0:
+            continue
+        C = int(rng.integers(1, min(T, 200) + 1))
+        starts = [c * T // C for c in range(C + 1)]
+        owner = np.empty(T, dtype=np.int64)
+        for c in range(C):
+            owner[starts[c]:starts[c + 1]] = c
+        formula = np.array([((x + 1) * C - 1) // T for x in range(T)])
+        assert np.array_equal(owner, formula)
+        slots = set()
+        pre = np.concatenate([[0], np.cumsum(tiles)])
+        for s in range(S):
+            for x in range(pre[s], pre[s + 1]):
+                slots.add((s, int(owner[x])))
+        keys = [s + c for s, c in slots]
+        assert len(keys) == len(set(keys)) and max(keys) < S + C - 1 + 1

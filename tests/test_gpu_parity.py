@@ -1,0 +1,219 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Small workloads are compared element by element for every (request, query
+token, head); the full-size workloads run in the benchmark's launch
+configuration and are compared on sampled requests and heads.
+"""
+import numpy as np
+import pytest
+
+import oracle as O
+import workloads as W
+from mla_testlib import compare, ensure_built, gpu_outputs, make_step, with_fp8
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+
+
+def _run_and_compare(batch, sm_count=None, absorb=True, requests=None, heads=None, label=""):
+    step = make_step(batch, sm_count=sm_count, absorb=absorb)
+    step.step()
+    o, o_lat, lse = gpu_outputs(step)
+    assert step.status() == 0, label
+    ref = O.decode(batch, requests=requests, heads=heads)
+    worst = compare(ref, o, o_lat, lse, heads=heads, label=label)
+    return step, worst
+
+
+@pytest.mark.parametrize("name", ["tiny", "dense_small", "long_small", "sparse_small"])
+@pytest.mark.parametrize("garbage", ["finite", "nan"])
+def test_small_workloads_match_oracle(name, garbage):
+    batch = with_fp8(W.generate(W.SMALL_WORKLOADS[name], garbage=garbage), garbage)
+    _run_and_compare(batch, label=f"{name}/{garbage}")
+
+
+@pytest.mark.parametrize("sm_count", [1, 3, 7, 40, 152])
+def test_split_invariance(sm_count):
+    """Every way of cutting the streams over CTAs (one split, many, uneven)
+    gives the same result to fp32 rounding, and matches the oracle."""
+    batch = W.generate(W.SMALL_WORKLOADS["long_small"])
+    ref_step = make_step(batch, sm_count=1)
+    ref_step.step()
+    o1, lat1, lse1 = gpu_outputs(ref_step)
+    step, _ = _run_and_compare(batch, sm_count=sm_count, label=f"split{sm_count}")
+    o2, lat2, lse2 = gpu_outputs(step)
+    assert np.linalg.norm(lat2 - lat1) <= 1e-5 * np.linalg.norm(lat1)
+    assert np.abs(lse2 - lse1).max() <= 1e-5
+
+
+def test_absorb_matches_oracle():
+    batch = W.generate(W.SMALL_WORKLOADS["dense_small"])
+    step = make_step(batch)
+    torch.cuda.synchronize()
+    got = step.q_hat.float().cpu().numpy().reshape(batch.workload.batch, 1, 20, 576)
+    for b in range(batch.workload.batch):
+        qn = O.bf16_to_f64(batch.q_nope[b, 0])
+        ref = O.absorb_query(qn, O.bf16_to_f64(batch.w_uk))
+        err = np.abs(got[b, 0, :, :512] - ref)
+        # one bf16 rounding of an fp32 sum: within one bf16 ulp
+        assert (err <= np.abs(ref) * 2.0 ** -7 + 1e-6).all()
+        assert np.array_equal(got[b, 0, :, 512:], O.bf16_to_f64(batch.q_rope[b, 0]))
+
+
+def test_uv_projection_matches_float64():
+    from head_latent_attention_paged_gb300 import mla_uv_proj
+    rng = np.random.default_rng(3)
+    for rows, H in [(1, 1), (64, 20), (130, 20), (200, 7)]:
+        o_lat = rng.standard_normal((rows, H, 512)).astype(np.float32)
+        w_bits = W.f32_to_bf16_bits(rng.standard_normal((H, 512, 256)).astype(np.float32) / np.sqrt(512))
+        o_dev = torch.from_numpy(o_lat).cuda()
+        w_dev = torch.from_numpy(w_bits.view(np.int16)).cuda().view(torch.bfloat16)
+        out = torch.empty((rows, H, 256), dtype=torch.bfloat16, device="cuda")
+        mla_uv_proj(o_dev, w_dev, out, rows, H, torch.cuda.current_stream())
+        got = out.float().cpu().numpy()
+        # o_lat enters the MMA as bf16: the reference rounds it the same way
+        lat_b = O.round_to_bf16(o_lat.astype(np.float64))
+        ref = np.einsum("rhk,hkn->rhn", lat_b, O.bf16_to_f64(w_bits))
+        assert np.abs(got - O.round_to_bf16(ref)).max() <= 2e-2
+        assert np.linalg.norm(got - ref) <= 5e-3 * np.linalg.norm(ref)
+
+
+@pytest.mark.parametrize("page_size", [64, 128])
+def test_one_hot_gather_is_bit_exact(page_size):
+    """Each head's query selects one planted token by > 100 nats: the latent
+    output must equal that token's cached latent row bit for bit, whatever
+    page and slot the block table maps it to."""
+    w = W.with_overrides(W.SMALL_WORKLOADS["dense_small"], page_size=page_size, batch=3,
+                         seq_lo=300, seq_hi=900)
+    batch = W.generate(w)
+    H = w.heads
+    rng = np.random.default_rng(0)
+    step = make_step(batch, absorb=False)
+    q = np.zeros((w.batch, 1, H, 576), dtype=np.float32)
+    cache = batch.cache_bf16.copy()
+    planted = {}
+    for b in range(w.batch):
+        T = int(batch.seq_lens[b])
+        # positions spread over pages, including page edges and the last token
+        cands = [0, page_size - 1, page_size, T - 1] + list(rng.choice(T, size=H, replace=False))
+        for h in range(H):
+            t = int(cands[h % len(cands)]) if h < 4 else int(cands[h])
+            planted[(b, h)] = t
+        # rope dims: head h uses dim 512 + h; planted rows carry 1 there, others 0
+        for t in range(T):
+            page, slot = batch.block_table[b, t // page_size], t % page_size
+            cache[page, slot, 512:512 + H] = 0
+        for h in range(H):
+            t = planted[(b, h)]
+            page, slot = batch.block_table[b, t // page_size], t % page_size
+            cache[page, slot, 512 + h] = W.f32_to_bf16_bits(np.float32(1.0))
+            q[b, 0, h, 512 + h] = 2048.0          # score 2048 / 16 = 128 nats
+    # a token planted for two heads carries both flags; distinct heads still
+    # see exactly one live row with a large score
+    step.cache.copy_(torch.from_numpy(cache.view(np.int16)).view(torch.bfloat16))
+    step.q_hat.copy_(torch.from_numpy(W.f32_to_bf16_bits(q.reshape(-1, H, 576)).view(np.int16)).view(torch.bfloat16))
+    step.step()
+    _, o_lat, lse = gpu_outputs(step)
+    for (b, h), t in planted.items():
+        page, slot = batch.block_table[b, t // page_size], t % page_size
+        expect = W.bf16_bits_to_f32(cache[page, slot, :512])
+        assert np.array_equal(o_lat[b, 0, h], expect), (b, h, t)
+        assert abs(lse[b, 0, h] - 128.0) < 1e-3
+
+
+def test_page_relabelling_gives_identical_bits():
+    batch = W.generate(W.SMALL_WORKLOADS["dense_small"])
+    s1 = make_step(batch)
+    s1.step()
+    _, lat1, lse1 = gpu_outputs(s1)
+    perm = np.random.default_rng(1).permutation(batch.num_pages)
+    inv = np.empty_like(perm)
+    inv[perm] = np.arange(batch.num_pages)
+    batch.cache_bf16 = batch.cache_bf16[perm]
+    bt = batch.block_table.copy()
+    bt[bt >= 0] = inv[bt[bt >= 0]]
+    batch.block_table = bt
+    s2 = make_step(batch)
+    s2.step()
+    _, lat2, lse2 = gpu_outputs(s2)
+    assert np.array_equal(lat1, lat2) and np.array_equal(lse1, lse2)
+
+
+def test_bad_page_is_masked_and_reported():
+    from head_latent_attention_paged_gb300 import MLA_STATUS_BAD_PAGE
+    batch = W.generate(W.SMALL_WORKLOADS["dense_small"])
+    clean = make_step(batch)
+    clean.step()
+    _, lat_clean, _ = gpu_outputs(clean)
+    bt = batch.block_table.copy()
+    bt[2, 1] = batch.num_pages + 5        # request 2, second page: out of range
+    bt[3, 0] = -3                         # request 3, first page: negative
+    batch.block_table = bt
+    step = make_step(batch)
+    step.step()
+    _, lat, lse = gpu_outputs(step)
+    assert step.status() & MLA_STATUS_BAD_PAGE
+    for b in (0, 1, 4):
+        assert np.array_equal(lat[b], lat_clean[b])
+    assert np.isfinite(lat).all() and np.isfinite(lse[[0, 1, 2, 4]]).all()
+    step.clear_status()
+    assert step.status() == 0
+
+
+def test_bad_sparse_index_is_masked_and_reported():
+    from head_latent_attention_paged_gb300 import MLA_STATUS_BAD_INDEX
+    batch = W.generate(W.SMALL_WORKLOADS["sparse_small"])
+    idx = batch.topk_idx.copy()
+    live = np.flatnonzero(idx[1] >= 0)
+    idx[1, live[0]] = 10 ** 6       # past the window
+    idx[1, live[1]] = -7            # negative but not -1
+    ref_idx = batch.topk_idx.copy()
+    ref_idx[1, live[0]] = -1
+    ref_idx[1, live[1]] = -1
+    batch.topk_idx = idx
+    step = make_step(batch)
+    step.step()
+    o, o_lat, lse = gpu_outputs(step)
+    assert step.status() & MLA_STATUS_BAD_INDEX
+    batch.topk_idx = ref_idx
+    ref = O.decode(batch)
+    compare(ref, o, o_lat, lse, label="bad-index")
+
+
+def test_empty_and_single_token_requests():
+    w = W.with_overrides(W.SMALL_WORKLOADS["dense_small"], seq_lens=(0, 1, 64, 65, 0, 129),
+                         batch=6)
+    batch = W.generate(w)
+    _run_and_compare(batch, label="edge-lengths")
+
+
+def test_multi_token_causal_dense():
+    """q_len 4 draft tokens on the dense path: token j sees T - 4 + j + 1."""
+    w = W.with_overrides(W.SMALL_WORKLOADS["dense_small"], q_len=4, batch=3, seq_lo=60, seq_hi=300)
+    _run_and_compare(W.generate(w), label="dense-q4")
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads, benchmark launch configuration, sampled outputs
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("name,requests,heads", [
+    ("dense", [0, 37, 63], [0, 7, 19]),
+    ("long", [3], [0, 19]),
+    ("sparse", [0, 31], [0, 11, 19]),
+])
+def test_full_size_sampled(name, requests, heads):
+    batch = W.generate(W.WORKLOADS[name])
+    step = make_step(batch)
+    step.step()
+    o, o_lat, lse = gpu_outputs(step)
+    assert step.status() == 0
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    ref = O.decode(batch, requests=requests, heads=heads)
+    compare(ref, o, o_lat, lse, heads=heads, label=name)
