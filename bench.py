@@ -1,0 +1,421 @@
+#!/usr/bin/env python3
+"""Benchmark of one paged MLA decode step (one layer) on GB300.
+
+A step is the whole hot path over one synthetic decode batch: the attention
+pass over the paged latent cache with the LSE merge of split partials fused
+in, and the W_UV up-projection (the absorbed query is an input, precomputed
+once).  The
+default workload is the GLM-4.7-Flash-shaped dense decode: batch 64, 20
+heads, q_len 1, seq_lens ~ U[1024, 8192], page 64, bf16 latent cache.
+
+Metric: latent-cache GB/s (bytes of cached rows the step must read, over the
+step time) and decode tokens/s per layer.  Prints one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the CPU oracle as the reference arm
+
+Under torchrun each rank runs an independent replica of the workload on its
+own GPU (the path shards by request and has no exchange step); rank 0 prints
+the line with the bytes of all ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MLA decode latent-cache GB/s (% of HBM peak) and decode tokens/s per layer"
+L2_FLUSH_BYTES = 512 * 1024 * 1024
+DECODE_SOURCES = ["csrc/mla_decode.cu", "csrc/sm103_ptx.cuh", "csrc/mla_internal.h"]
+
+
+def workload_description(w, batch) -> dict:
+    seq = batch.seq_lens
+    d = {
+        "workload": f"{w.name}: MLA decode, 1 layer, B={w.batch}, H={w.heads}, q_len={w.q_len}, "
+                    f"page {w.page_size}, {w.kv_dtype} latent (512 + 64 rope)"
+                    + (f", top-{w.topk} sparse (width {w.topk_width})" if w.topk else "")
+                    + (f", seq_lens U[{w.seq_lo},{w.seq_hi}]" if w.seq_lens is None
+                       else f", seq_lens {list(w.seq_lens)}"),
+        "batch": w.batch, "heads": w.heads, "q_len": w.q_len, "page_size": w.page_size,
+        "kv_dtype": w.kv_dtype, "topk": w.topk, "seed": w.seed,
+        "total_context_tokens": int(seq.sum()),
+        "latent_bytes_per_step": int(batch.latent_bytes_read),
+        "bytes_per_token_row": w.cache_row_bytes,
+        "l2": f"flushed before every timed step by writing {L2_FLUSH_BYTES >> 20} MiB "
+              "(step time from CUDA events excludes the flush)",
+    }
+    return d
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f)
+    return {}
+
+
+def decode_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in DECODE_SOURCES:
+        with open(os.path.join(ROOT, "head_latent_attention_paged_gb300", rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on this workload with the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    entry = rec.get(workload)
+    if not entry or entry.get("source_hash") != decode_source_hash():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self._stop = threading.Event()
+        self._thread = threading.Thread(target=self._run, daemon=True)
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                out = subprocess.run(
+                    ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                     "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=5)
+                if out.returncode == 0 and out.stdout.strip():
+                    self.samples.append([x.strip() for x in out.stdout.strip().split(",")])
+            except Exception:
+                pass
+            self._stop.wait(0.05)
+
+    def __enter__(self):
+        self._thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        self._thread.join(timeout=10)
+
+    def summary(self) -> dict:
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"],
+                    "samples": 0}
+        sm = [float(s[0]) for s in self.samples if s[0].replace(".", "").isdigit()]
+        smax = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for s in self.samples:
+            for name, val in zip(names, s[4:8]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        power = [float(s[2]) for s in self.samples if s[2].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(self.samples),
+                "power_w_max": max(power) if power else None}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(value_bytes: float, seconds: float, world: int, device=None):
+    """Sum of bytes over ranks and the slowest rank's time (replicas)."""
+    if world == 1:
+        return value_bytes, seconds
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value_bytes, seconds], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    b = t[0:1].clone()
+    s = t[1:2].clone()
+    dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    dist.all_reduce(s, op=dist.ReduceOp.MAX)
+    return float(b.item()), float(s.item())
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (baseline leg and reference arm)
+# ---------------------------------------------------------------------------
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        info = threadpool_info()
+        if info:
+            return max(int(i.get("num_threads", 1)) for i in info)
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var):
+            return int(os.environ[var])
+    return os.cpu_count() or 1
+
+
+def oracle_sample(batch, budget_s: float, max_tokens: int = None):
+    """Time the (non-absorbed, float64) oracle on a bounded sample: whole
+    requests in order until `budget_s` is spent, or a prefix of the first
+    request of at most `max_tokens` tokens.  Returns (bytes, seconds, what)."""
+    import numpy as np
+    import oracle as O
+    w = batch.workload
+    if max_tokens is not None:
+        sub = _prefix_batch(batch, max_tokens)
+        t0 = time.perf_counter()
+        O.decode(sub, requests=[0])
+        dt = time.perf_counter() - t0
+        return sub.latent_bytes_read_req(0), dt, f"first {int(sub.seq_lens[0])} tokens of request 0, all {w.heads} heads"
+    done_bytes, t0, n = 0, time.perf_counter(), 0
+    for b in range(w.batch):
+        O.decode(batch, requests=[b])
+        n += 1
+        done_bytes += _request_bytes(batch, b)
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    return done_bytes, time.perf_counter() - t0, f"{n} whole request(s) of {w.batch}, all {w.heads} heads"
+
+
+def _request_bytes(batch, b):
+    w = batch.workload
+    if w.topk:
+        return int((batch.topk_idx[b * w.q_len:(b + 1) * w.q_len] >= 0).sum()) * w.cache_row_bytes
+    return int(batch.seq_lens[b]) * w.cache_row_bytes
+
+
+def _prefix_batch(batch, tokens):
+    import copy
+    import numpy as np
+    sub = copy.copy(batch)
+    seq = batch.seq_lens.copy()
+    seq[0] = min(int(seq[0]), tokens)
+    sub.seq_lens = seq
+    sub.latent_bytes_read_req = lambda b: _request_bytes(sub, b)
+    return sub
+
+
+def run_reference(args, world, rank):
+    import numpy as np
+    import workloads as W
+    if rank != 0:
+        return 0
+    w = W.WORKLOADS[args.workload]
+    batch = W.generate(w)
+    if w.kv_dtype == "fp8":
+        from oracle import fp8 as F
+        batch.extra["cache_fp8"] = F.quantize_pages(batch.latent_f32, batch.slot_valid, w.seed)
+    # calibrate: tokens per step so the whole run stays within ~2 minutes
+    b_cal, t_cal, _ = oracle_sample(batch, 0, max_tokens=256)
+    rate = b_cal / max(t_cal, 1e-9) / w.cache_row_bytes        # tokens per second
+    per_step_s = min(2.0, 120.0 / max(1, args.steps + args.warmup))
+    tokens = int(max(64, min(int(batch.seq_lens[0]), rate * per_step_s)))
+    for _ in range(args.warmup):
+        oracle_sample(batch, 0, max_tokens=tokens)
+    times, byts = [], 0
+    what = ""
+    for _ in range(args.steps):
+        bb, dt, what = oracle_sample(batch, 0, max_tokens=tokens)
+        times.append(dt)
+        byts += bb
+    total = sum(times)
+    value = byts / total / 1e9
+    cores = blas_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_description(w, batch),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"each step: {what} (non-absorbed float64 numpy oracle)"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def run_gpu(args, world, rank, local):
+    import numpy as np
+    import torch
+    import workloads as W
+    import __graft_entry__ as graft
+    from head_latent_attention_paged_gb300 import MLA_KV_BF16, MLA_KV_FP8_E4M3_E8M0
+    from head_latent_attention_paged_gb300.runner import DecodeStep
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    graft.build()
+    w = W.WORKLOADS[args.workload]
+    batch = W.generate(w)
+    if w.kv_dtype == "fp8":
+        raise SystemExit("the FP8 workload is not built yet")
+    step = DecodeStep(q_nope=batch.q_nope, q_rope=batch.q_rope, w_uk=batch.w_uk, w_uv=batch.w_uv,
+                      cache=batch.cache_bf16, block_table=batch.block_table,
+                      seq_lens=batch.seq_lens, page_size=w.page_size, kv_dtype=MLA_KV_BF16,
+                      topk_idx=batch.topk_idx, causal=w.causal, sm_scale=w.sm_scale,
+                      device=device)
+    stream = torch.cuda.current_stream(device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    byts = batch.latent_bytes_read
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step.step()
+    torch.cuda.synchronize(device)
+    if step.status() != 0:
+        raise SystemExit(f"decode reported status {step.status():#x}")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(device)
+    with ClockSampler(local) as clocks:
+        t_wall = time.perf_counter()
+        for k in range(args.steps):
+            flush.zero_()
+            ev[k][0].record(stream)
+            step.run()
+            ev[k][1].record(stream)
+            step.uv()
+            ev[k][2].record(stream)
+        torch.cuda.synchronize(device)
+        t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(device)
+    run_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
+    step_s = sum(step_ms) / 1e3
+    tot_bytes, max_s = aggregate(float(byts) * args.steps, step_s, world, device)
+    value = tot_bytes / max_s / 1e9
+    ms_per_step = 1e3 * max_s / args.steps
+    decode_ms = statistics.mean(run_ms)
+
+    # end to end through the C ABI with host buffers: pinned host inputs are
+    # copied in, the step runs, the outputs are read back, every step
+    e2e = None
+    if args.e2e_steps > 0:
+        host_cache = step.cache.cpu().pin_memory()
+        host_q = step.q_hat.cpu().pin_memory()
+        host_bt = step.block_table.cpu().pin_memory()
+        host_seq = step.seq_lens.cpu().pin_memory()
+        host_idx = None if step.topk_idx is None else step.topk_idx.cpu().pin_memory()
+        out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+        lse_host = torch.empty(step.lse.shape, dtype=step.lse.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in (host_cache, host_q, host_bt, host_seq)
+                  + ((host_idx,) if host_idx is not None else ()))
+        d2h = out_host.numel() * out_host.element_size() + lse_host.numel() * lse_host.element_size()
+        e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.e2e_steps)]
+        for k in range(args.e2e_steps + 2):
+            if k >= 2:
+                e2e_ev[k - 2][0].record(stream)
+            step.cache.copy_(host_cache, non_blocking=True)
+            step.q_hat.copy_(host_q, non_blocking=True)
+            step.block_table.copy_(host_bt, non_blocking=True)
+            step.seq_lens.copy_(host_seq, non_blocking=True)
+            if host_idx is not None:
+                step.topk_idx.copy_(host_idx, non_blocking=True)
+            step.step()
+            out_host.copy_(step.out, non_blocking=True)
+            lse_host.copy_(step.lse, non_blocking=True)
+            if k >= 2:
+                e2e_ev[k - 2][1].record(stream)
+        torch.cuda.synchronize(device)
+        e2e_s = sum(a.elapsed_time(b) for a, b in e2e_ev) / 1e3
+        eb, es = aggregate(float(byts) * args.e2e_steps, e2e_s, world, device)
+        e2e = {"value": eb / es / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "steps": args.e2e_steps}
+
+    if rank != 0:
+        return 0
+    peaks = measured_peaks()
+    hbm = peaks.get("hbm_gbs")
+    peak_src = "measured (MEASURED_PEAKS.json hbm_gbs)"
+    if not hbm:
+        hbm, peak_src = 6800.0, "fallback 6.8 TB/s"
+    achieved = byts / (decode_ms / 1e3) / 1e9
+    traffic = recorded_traffic(args.workload)
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_description(w, batch),
+        "tokens_per_s_per_layer": w.batch * w.q_len * world / (max_s / args.steps),
+        "hbm_fraction_of_measured": value / hbm,
+        "kernel_ms": {"decode_with_merge": decode_ms, "step": statistics.mean(step_ms),
+                      "uv_after_decode": statistics.mean(step_ms) - decode_ms},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": traffic,
+                     "kernel": "mla_decode_kernel<dense bf16>",
+                     "peak_source": peak_src,
+                     "algorithmic_bytes_per_launch": int(byts)},
+        "e2e": e2e,
+        "gpu_launches": DecodeStep.KERNELS_PER_STEP * args.steps,
+        "clocks": clocks.summary(),
+        "wall_s_timed_region": t_wall,
+        "status": step.status(),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        cb, ct, what = oracle_sample(batch, args.cpu_budget)
+        line["cpu_baseline"] = {"value": cb / ct / 1e9, "unit": "GB/s", "cores": blas_threads(),
+                                "kind": "oracle",
+                                "sample": f"{what}: non-absorbed float64 numpy oracle, {ct:.1f} s"}
+    print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="dense",
+                    choices=["tiny", "dense", "long", "sparse"])
+    ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    return run_gpu(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

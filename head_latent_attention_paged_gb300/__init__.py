@@ -56,7 +56,8 @@ class MlaPlan(ctypes.Structure):
         ("problem", MlaProblem), ("num_streams", ctypes.c_int32), ("num_ctas", ctypes.c_int32),
         ("num_slots", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
         ("ws_partial_o", ctypes.c_int64), ("ws_partial_lse", ctypes.c_int64),
-        ("ws_status", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64),
+        ("ws_counters", ctypes.c_int64), ("ws_status", ctypes.c_int64),
+        ("workspace_bytes", ctypes.c_int64),
         ("planned_tiles", ctypes.c_int64), ("reserved", ctypes.c_int32 * 8),
     ]
 
@@ -83,7 +84,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     P = ctypes.POINTER
     lib.mla_decode_plan.argtypes = [P(MlaProblem), P(ctypes.c_int32), i32, P(MlaPlan)]
     lib.mla_q_absorb.argtypes = [P(MlaPlan), vp, vp, vp, vp, vp]
-    lib.mla_decode_run.argtypes = [P(MlaPlan), vp, vp, vp, vp, vp, vp, vp]
+    lib.mla_decode_run.argtypes = [P(MlaPlan), vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.mla_combine.argtypes = [P(MlaPlan), vp, vp, vp, vp, vp]
     lib.mla_uv_proj.argtypes = [vp, vp, vp, i32, i32, vp]
     lib.mla_get_status.argtypes = [P(MlaPlan), vp, P(ctypes.c_uint32), vp]
@@ -155,10 +156,10 @@ def mla_q_absorb(plan: MlaPlan, q_nope, q_rope, w_uk, q_hat, stream=None) -> Non
 
 
 def mla_decode_run(plan: MlaPlan, q_hat, kv_cache, block_table, seq_lens, topk_idx, workspace,
-                   stream=None) -> None:
+                   o_lat, lse, stream=None) -> None:
     _check("mla_decode_run", load().mla_decode_run(
         ctypes.byref(plan), _ptr(q_hat), _ptr(kv_cache), _ptr(block_table), _ptr(seq_lens),
-        _ptr(topk_idx), _ptr(workspace), _stream(stream)))
+        _ptr(topk_idx), _ptr(workspace), _ptr(o_lat), _ptr(lse), _stream(stream)))
 
 
 def mla_combine(plan: MlaPlan, seq_lens, workspace, o_lat, lse, stream=None) -> None:

@@ -145,6 +145,8 @@ int mla_decode_plan(const mla_problem* problem, const int32_t* seq_lens_host, in
   off = align_up(off + static_cast<int64_t>(pl.num_slots) * pr.num_heads * kDc * 4, kAlign);
   pl.ws_partial_lse = off;
   off = align_up(off + static_cast<int64_t>(pl.num_slots) * pr.num_heads * 4, kAlign);
+  pl.ws_counters = off;
+  off = align_up(off + static_cast<int64_t>(pl.num_streams) * 4, kAlign);
   pl.ws_status = off;
   off = align_up(off + 4, kAlign);
   pl.workspace_bytes = off;
@@ -168,24 +170,23 @@ int mla_q_absorb(const mla_plan* plan, const void* q_nope, const void* q_rope, c
 
 int mla_decode_run(const mla_plan* plan, const void* q_hat, const void* kv_cache,
                    const int32_t* block_table, const int32_t* seq_lens, const int32_t* topk_idx,
-                   void* workspace, mla_stream_t stream) {
+                   void* workspace, float* o_lat, float* lse, mla_stream_t stream) {
   int rc = plan_check(plan);
   if (rc != MLA_OK) return rc;
   const mla_problem& pr = plan->problem;
-  if (!q_hat || !kv_cache || !block_table || !seq_lens || !workspace) return MLA_ERR_INVALID_ARGUMENT;
+  if (!q_hat || !kv_cache || !block_table || !seq_lens || !workspace || !o_lat || !lse)
+    return MLA_ERR_INVALID_ARGUMENT;
   if ((pr.topk_width > 0) != (topk_idx != nullptr)) return MLA_ERR_INVALID_ARGUMENT;
-  if (!aligned16(q_hat) || !aligned16(kv_cache) || !aligned16(workspace) ||
+  if (!aligned16(q_hat) || !aligned16(kv_cache) || !aligned16(workspace) || !aligned16(o_lat) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u) ||
       (reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
       (topk_idx && (reinterpret_cast<uintptr_t>(topk_idx) & 3u)))
     return MLA_ERR_MISALIGNED;
   if (plan->num_streams == 0) return MLA_OK;
   const int mode = decode_mode(pr);
-  CUtensorMap kv_map, q_map;
+  CUtensorMap kv_map;
   if (!make_map_bf16(&kv_map, kv_cache, kDqk, static_cast<uint64_t>(pr.num_pages) * pr.page_size,
                      kDqk * 2, kChunkElems, kTile))
-    return MLA_ERR_CUDA;
-  if (!make_map_bf16(&q_map, q_hat, kDqk, static_cast<uint64_t>(plan->num_streams) * pr.num_heads,
-                     kDqk * 2, kChunkElems, static_cast<uint32_t>(pr.num_heads)))
     return MLA_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   DecodeParams p;
@@ -196,6 +197,9 @@ int mla_decode_run(const mla_plan* plan, const void* q_hat, const void* kv_cache
   p.topk_idx = topk_idx;
   p.part_o = reinterpret_cast<float*>(ws + plan->ws_partial_o);
   p.part_lse = reinterpret_cast<float*>(ws + plan->ws_partial_lse);
+  p.counters = reinterpret_cast<int32_t*>(ws + plan->ws_counters);
+  p.o_lat = o_lat;
+  p.lse = lse;
   p.status = reinterpret_cast<uint32_t*>(ws + plan->ws_status);
   p.batch = pr.batch;
   p.q_len = pr.q_len;
@@ -209,7 +213,7 @@ int mla_decode_run(const mla_plan* plan, const void* q_hat, const void* kv_cache
   p.num_streams = plan->num_streams;
   p.num_ctas = plan->num_ctas;
   p.scale_log2 = pr.sm_scale * 1.4426950408889634f;
-  const cudaError_t err = launch_decode(p, &kv_map, &q_map, mode, reinterpret_cast<cudaStream_t>(stream));
+  const cudaError_t err = launch_decode(p, &kv_map, mode, reinterpret_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 

@@ -64,6 +64,7 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(const CombineParams p)
   if (ntiles > 0) {
     const int c0 = tile_owner(before, tot, p.num_ctas);
     const int c1 = tile_owner(before + ntiles - 1, tot, p.num_ctas);
+    if (c0 == c1) return;   // one CTA held the whole row set: its result is final
     float m = -INFINITY;
     for (int c = c0; c <= c1; ++c) m = fmaxf(m, p.part_lse[static_cast<int64_t>(s + c) * p.heads + h]);
     if (m != -INFINITY) {
@@ -141,6 +142,9 @@ __global__ void __launch_bounds__(128, 1)
         tma_load_2d(sA + (kb * 2 + nc) * kChunkBytes, &w_map, &bars[0], mt * 128 + nc * 64,
                     h * kDc + kb * 64, 0ull);
   }
+  // o_lat is produced by the preceding decode launch: wait for it (the W_UV
+  // loads above already overlap its tail when launched as a dependent).
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // B: o_lat[r0 + r][h][k] -> bf16, [kb][r][128 B] swizzled
   for (int e = tid; e < kUvRows * 64; e += 128) {
     const int r = e >> 6, piece = e & 63;        // piece: 8 consecutive k
@@ -211,8 +215,18 @@ cudaError_t launch_uv_proj_tma(const CUtensorMap* w_map, const float* o_lat, uin
   if (rows == 0) return cudaSuccess;
   cudaError_t err = cudaFuncSetAttribute(mla_uv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kUvSmem);
   if (err != cudaSuccess) return err;
-  dim3 grid(heads, kDv / 128, (rows + kUvRows - 1) / kUvRows);
-  mla_uv_kernel<<<grid, 128, kUvSmem, stream>>>(*w_map, o_lat, out, rows, heads);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(heads, kDv / 128, (rows + kUvRows - 1) / kUvRows);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = kUvSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  err = cudaLaunchKernelEx(&cfg, mla_uv_kernel, *w_map, o_lat, out, rows, heads);
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 

@@ -7,17 +7,20 @@
 //                   memory once -- TMA tiles for dense pages, 16-byte
 //                   cp.async gathers for sparse top-k rows -- as nine
 //                   [64 rows x 128 B] chunks in the 128-byte swizzle layout,
-//                   and the stream's absorbed queries (TMA, double buffered).
+//                   three tiles in flight.
 //   MMA warp      : S[h, t]   = q_hat[h, :576] . row[t, :576]      (tcgen05,
-//                   M = 64 head rows, N = 64 tokens, K = 576, f32 in TMEM);
+//                   M = 64 head rows with q_hat read from TMEM, N = 64
+//                   tokens from shared memory, K = 576, f32 in TMEM);
 //                   O^T[d, h] += sum_t row[t, d] P[h, t]            (tcgen05,
 //                   M = 128 latent dims x 4, N = padded heads, K = 64 tokens,
 //                   A = the same staged tile read MN-major).
 //   softmax warps : online softmax in the exp2 domain on S read from TMEM
-//                   (one thread per head row), P written to shared memory as
+//                   (two lanes per head row), P written to shared memory as
 //                   bf16, lazy rescale of O^T in TMEM when the running max
-//                   grows by more than 2^8, and at the end of each segment the
-//                   normalised partial (o_lat, lse) written to the workspace.
+//                   grows by more than 2^8; at a stream change they write the
+//                   next stream's q_hat into TMEM, and at the end of each
+//                   segment the normalised result (or a partial plus its lse,
+//                   merged by whichever CTA delivers a stream's last partial).
 //
 // All heads of a request reuse each staged tile, so every cached byte is read
 // from HBM once per stream.  Waits are bounded (sm103_ptx.cuh); a timeout
@@ -42,24 +45,30 @@ constexpr int kThreads = 192;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s per wait
 constexpr float kRescaleThreshold = 8.0f;           // log2 units: rescale if max grows > 2^8
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr int kMaxSmem = 232448;                    // 227 KB per CTA
+
+// Tensor memory columns (512 allocated): q_hat as the QK A operand (M=64
+// layout, 576 bf16 = 288 columns), S (64 token columns), O^T (4 x 32).
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColQ = 0;
+constexpr uint32_t kColS = 288;
+constexpr uint32_t kColO = 352;
 
 // Control block placed after the data buffers in shared memory.
 struct __align__(8) Ctrl {
   uint64_t full[kStages];    // producer -> MMA/softmax: tile staged
   uint64_t empty[kStages];   // MMA -> producer: stage consumed by PV
-  uint64_t s_full[kStages];  // MMA -> softmax: S buffer written
-  uint64_t s_free[kStages];  // softmax -> MMA: S buffer read
-  uint64_t p_full[kStages];  // softmax -> MMA: P written (and O^T rescaled)
-  uint64_t q_full[2];        // producer -> MMA: a stream's queries staged
-  uint64_t q_empty[2];       // MMA -> producer: last QK on a Q buffer done
+  uint64_t s_full;           // MMA -> softmax: S written
+  uint64_t s_free;           // softmax -> MMA: S read
+  uint64_t p_full[2];        // softmax -> MMA: P written (and O^T rescaled)
+  uint64_t q_ready;          // softmax -> MMA: a stream's q_hat is in TMEM
   uint64_t o_done;           // MMA -> softmax: one PV completed
   uint64_t o_free;           // softmax -> MMA: epilogue has read O^T
   uint64_t mma_drain;        // MMA warp's final commit
   uint64_t mask[kStages];    // per-stage live-row mask (bit t = row t live)
   uint32_t tmem_base;
   int32_t abort_flag;
-  int32_t rescale_tile[kStages];
+  int32_t rescale_tile[2];
+  int32_t merge_flag;
   float alpha[2][kMaxHeads];
   float l_final[kMaxHeads];
 };
@@ -95,45 +104,157 @@ struct Walker {
   }
 };
 
+// 2^x with the hardware approximation (ex2.approx.ftz: 2^-inf = +0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__device__ __forceinline__ uint32_t tmem_cols(int NP) { return (128 + 4 * NP) <= 256 ? 256u : 512u; }
+// D[tmem] (+)= A[tmem] * B[smem desc]
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+// Write stream s's absorbed queries into TMEM as the M=64 A operand: head h
+// = 16w + l (l < 16) goes to lane 32w + l, 576 bf16 packed two per column.
+// Called by all four softmax warps (each writes its own lane quarter);
+// rows of absent heads are written as zeros.  Three chunks of 64 values are
+// loaded per batch so several global loads are in flight.
+__device__ __forceinline__ void load_q_tmem(const uint16_t* q_hat, int32_t s, int H,
+                                            uint32_t taddr_lane, int lane, int w) {
+  const int h = w * 16 + (lane & 15);
+  const bool live = lane < 16 && h < H;
+  const uint4* src =
+      reinterpret_cast<const uint4*>(q_hat + (static_cast<int64_t>(s) * H + (live ? h : 0)) * kDqk);
+#pragma unroll 1
+  for (int cb = 0; cb < kChunks; cb += 3) {
+    uint4 v[3][8];
+#pragma unroll
+    for (int c = 0; c < 3; ++c)
+#pragma unroll
+      for (int q = 0; q < 8; ++q) v[c][q] = live ? __ldg(src + (cb + c) * 8 + q) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int c = 0; c < 3; ++c) {
+      uint32_t r[32];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        r[4 * q] = v[c][q].x;
+        r[4 * q + 1] = v[c][q].y;
+        r[4 * q + 2] = v[c][q].z;
+        r[4 * q + 3] = v[c][q].w;
+      }
+      tmem_st32(taddr_lane + kColQ + (cb + c) * 32, r);
+    }
+  }
+}
+
+// Merge the nseg partials (slots s + c_first ...) of row set s into o_lat and
+// lse.  128 threads; thread t owns latent dims [4t, 4t + 4) of every head.
+// The partials were written by other CTAs (L2-resident): loads bypass L1
+// and are batched 4 heads x 4 partials at a time to keep many in flight.
+__device__ __forceinline__ void merge_partials(const DecodeParams& p, int32_t s, int32_t c_first,
+                                               int32_t nseg, int H, int tid, float* tot_sm) {
+  const float* plse = p.part_lse + static_cast<int64_t>(s + c_first) * H;
+  const float4* po = reinterpret_cast<const float4*>(p.part_o + static_cast<int64_t>(s + c_first) * H * kDc);
+  if (tid < H) {
+    float m = -INFINITY;
+    for (int k = 0; k < nseg; ++k) m = fmaxf(m, __ldcg(plse + static_cast<int64_t>(k) * H + tid));
+    float tot = -INFINITY;
+    if (m != -INFINITY) {
+      float sum = 0.f;
+      for (int k = 0; k < nseg; ++k) sum += __expf(__ldcg(plse + static_cast<int64_t>(k) * H + tid) - m);
+      tot = m + __logf(sum);
+    }
+    tot_sm[tid] = tot;
+    p.lse[static_cast<int64_t>(s) * H + tid] = tot;
+  }
+  named_bar_sync(1, 128);
+  for (int hb = 0; hb < H; hb += 4) {
+    float tot[4];
+    float4 acc[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      tot[j] = (hb + j < H) ? tot_sm[hb + j] : -INFINITY;
+      acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int kb = 0; kb < nseg; kb += 4) {
+      float lv[4][4];
+      float4 v[4][4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const int k = kb + kk;
+          const bool use = k < nseg && tot[j] != -INFINITY;
+          const int64_t row = static_cast<int64_t>(k) * H + hb + j;
+          lv[j][kk] = use ? __ldcg(plse + row) : -INFINITY;
+          v[j][kk] = use ? __ldcg(po + row * (kDc / 4) + tid) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const float wgt = (lv[j][kk] == -INFINITY) ? 0.f : __expf(lv[j][kk] - tot[j]);
+          acc[j].x = fmaf(wgt, v[j][kk].x, acc[j].x);
+          acc[j].y = fmaf(wgt, v[j][kk].y, acc[j].y);
+          acc[j].z = fmaf(wgt, v[j][kk].z, acc[j].z);
+          acc[j].w = fmaf(wgt, v[j][kk].w, acc[j].w);
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (hb + j < H)
+        reinterpret_cast<float4*>(p.o_lat + (static_cast<int64_t>(s) * H + hb + j) * kDc)[tid] = acc[j];
+  }
+}
 
 }  // namespace
 
 DecodeLayout decode_layout(int heads, int heads_pad, int num_streams, int mode) {
   (void)mode;
+  (void)heads;
   DecodeLayout L;
-  const int groups = (heads + 7) / 8;
-  L.q_group_bytes = groups * 1024;
-  L.q_buf_bytes = kChunks * L.q_group_bytes;
-  L.off_q = 0;
-  const int rest = kStages * kTileBytes + kStages * heads_pad * 128 +
-                   static_cast<int>(sizeof(Ctrl)) + (num_streams + 1) * 4 + 1024;
-  // Two query buffers when they fit, so the next stream's queries load
-  // while the current one computes.  The M=64 QK MMA reads 64 rows from each
-  // Q chunk start; rows >= H land in the following memory (later chunks or
-  // the stages) and only feed S rows nobody reads.
-  L.q_bufs = (2 * L.q_buf_bytes + rest <= kMaxSmem) ? 2 : 1;
-  L.off_stage = L.q_bufs * L.q_buf_bytes;
-  L.off_p = L.off_stage + kStages * kTileBytes;
-  L.off_ctrl = L.off_p + kStages * heads_pad * 128;
-  L.total = L.off_ctrl + static_cast<int>(sizeof(Ctrl)) + (num_streams + 1) * 4 + 1024;
+  L.off_stage = 0;
+  L.off_p = kStages * kTileBytes;
+  L.off_ctrl = L.off_p + 2 * heads_pad * 128;
+  L.total = L.off_ctrl + static_cast<int>(sizeof(Ctrl)) + (num_streams + 1) * 4;
   return L;
 }
 
 template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
-    mla_decode_kernel(const __grid_constant__ CUtensorMap kv_map,
-                      const __grid_constant__ CUtensorMap q_map, const DecodeParams p,
+    mla_decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p,
                       const DecodeLayout L) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* sQ = smem + L.off_q;
+  // The buffers need 1024-byte alignment (128-byte swizzle atoms); the
+  // dynamic shared window starts aligned, which is checked below.
+  extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* sStage = smem + L.off_stage;
   uint8_t* sP = smem + L.off_p;
   Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + L.off_ctrl);
@@ -145,24 +266,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int S = p.num_streams;
   const int H = p.heads;
   const int NP = p.heads_pad;
-  const int QB = L.q_bufs;
   const int max_tokens = p.max_pages * p.page_size;
   volatile int32_t* abort_flag = &ctrl->abort_flag;
 
+  if ((smem_u32(smem) & 1023u) != 0) {   // never expected; refuse rather than corrupt
+    if (tid == 0) set_status(p.status, MLA_STATUS_TIMEOUT);
+    return;
+  }
+
   // ---------------------------------------------------------------- setup
+  // Let a dependent launch (the W_UV projection) start its prologue as soon
+  // as SMs free up; it waits for this grid's completion before reading.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&ctrl->full[i], kMode == kModeSparseBf16 ? 33 : 1);
       mbar_init(&ctrl->empty[i], 1);
-      mbar_init(&ctrl->s_full[i], 1);
-      mbar_init(&ctrl->s_free[i], kSoftmaxWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&ctrl->p_full[i], kSoftmaxWarps);
       ctrl->rescale_tile[i] = -1;
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&ctrl->q_full[i], 1);
-      mbar_init(&ctrl->q_empty[i], 1);
-    }
+    mbar_init(&ctrl->s_full, 1);
+    mbar_init(&ctrl->s_free, kSoftmaxWarps);
+    mbar_init(&ctrl->q_ready, kSoftmaxWarps);
     mbar_init(&ctrl->o_done, 1);
     mbar_init(&ctrl->o_free, kSoftmaxWarps);
     mbar_init(&ctrl->mma_drain, 1);
@@ -170,13 +297,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 0) {
-    tmem_alloc(&ctrl->tmem_base, tmem_cols(NP));
+    tmem_alloc(&ctrl->tmem_base, kTmemCols);
     tmem_relinquish();
   }
-  if (warp == kProducerWarp && lane == 0) {
-    if constexpr (kMode == kModeDenseBf16) prefetch_tmap(&kv_map);
-    prefetch_tmap(&q_map);
-  }
+  if (warp == kProducerWarp && lane == 0 && kMode == kModeDenseBf16) prefetch_tmap(&kv_map);
   // tiles per stream (stream lengths from the device seq_lens)
   for (int s = tid; s < S; s += kThreads) {
     const int b = s / p.q_len, j = s - b * p.q_len;
@@ -184,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefix[s + 1] = (len + kTile - 1) / kTile;
   }
   // P buffers start at zero: rows of padded heads are never written again
-  for (int i = tid; i < kStages * NP * 128 / 16; i += kThreads)
+  for (int i = tid; i < 2 * NP * 128 / 16; i += kThreads)
     reinterpret_cast<uint4*>(sP)[i] = make_uint4(0, 0, 0, 0);
   __syncthreads();
   if (warp == 0) {   // exclusive prefix sum of tiles over streams
@@ -220,49 +344,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol = l2_policy_evict_first();
       Walker wk;
       wk.init(prefix, S, g0);
-      int32_t issued = 0, seg = -1;
+      int32_t issued = 0;
       bool failed = false;
       for (int32_t i = 0; i < ntiles; ++i) {
-        const int stage = i & 1;
-        const bool first = (i == 0) || (wk.lt == 0);
+        const int stage = i % kStages;
+        const uint32_t reuse_parity = ((i / kStages) - 1) & 1;
         const int b = wk.s / p.q_len, j = wk.s - b * p.q_len;
-        if (first) {
-          ++seg;
-          const int qb = seg % QB;
-          if (seg >= QB && !warp_wait(&ctrl->q_empty[qb], ((seg / QB) - 1) & 1, abort_flag)) {
-            failed = true;
-            break;
-          }
-          if (lane == 0) {
-            mbar_arrive_expect_tx(&ctrl->q_full[qb], static_cast<uint32_t>(kChunks * H * 128));
-#pragma unroll
-            for (int ch = 0; ch < kChunks; ++ch)
-              tma_load_2d(sQ + qb * L.q_buf_bytes + ch * L.q_group_bytes, &q_map, &ctrl->q_full[qb],
-                          ch * kChunkElems, wk.s * H, 0ull);
-          }
-        }
-        if (i >= 2 && !warp_wait(&ctrl->empty[stage], ((i >> 1) - 1) & 1, abort_flag)) {
-          failed = true;
-          break;
-        }
         uint8_t* dst = sStage + stage * kTileBytes;
+        // Describe the tile first: its global lookups overlap the stage wait.
         if constexpr (kMode == kModeDenseBf16) {
+          int32_t row0 = 0;
+          uint64_t mask = 0;
+          bool ok = false;
           if (lane == 0) {
             const int32_t tok0 = wk.lt * kTile;
             const int32_t len = stream_len(p.seq_lens[b], p.q_len, j, p.causal, 0, max_tokens);
             const int32_t page =
                 p.block_table[static_cast<int64_t>(b) * p.max_pages + tok0 / p.page_size];
             const int32_t nvalid = min(kTile, len - tok0);
-            uint64_t mask = nvalid >= 64 ? ~0ull : ((1ull << nvalid) - 1ull);
-            const bool ok = page >= 0 && page < p.num_pages;
+            mask = nvalid >= 64 ? ~0ull : ((1ull << nvalid) - 1ull);
+            ok = page >= 0 && page < p.num_pages;
             if (!ok) {
               mask = 0;
               set_status(p.status, MLA_STATUS_BAD_PAGE);
             }
+            row0 = ok ? page * p.page_size + (tok0 % p.page_size) : 0;
+          }
+          if (i >= kStages && !warp_wait(&ctrl->empty[stage], reuse_parity, abort_flag)) {
+            failed = true;
+            break;
+          }
+          if (lane == 0) {
             ctrl->mask[stage] = mask;
             if (ok) {
               mbar_arrive_expect_tx(&ctrl->full[stage], kTileBytes);
-              const int32_t row0 = page * p.page_size + (tok0 % p.page_size);
 #pragma unroll
               for (int ch = 0; ch < kChunks; ++ch)
                 tma_load_2d(dst + ch * kChunkBytes, &kv_map, &ctrl->full[stage], ch * kChunkElems,
@@ -300,6 +415,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (bad) set_status(p.status, bad);
           const uint32_t lo = __ballot_sync(0xffffffffu, valid[0]);
           const uint32_t hi = __ballot_sync(0xffffffffu, valid[1]);
+          if (i >= kStages && !warp_wait(&ctrl->empty[stage], reuse_parity, abort_flag)) {
+            failed = true;
+            break;
+          }
           for (int r = 0; r < kTile; ++r) {
             const uint8_t* s_row = reinterpret_cast<const uint8_t*>(__shfl_sync(
                 0xffffffffu, reinterpret_cast<unsigned long long>(r < 32 ? src[0] : src[1]), r & 31));
@@ -329,86 +448,97 @@ __global__ void __launch_bounds__(kThreads, 1)
       // drain: everything this warp issued has landed before the CTA exits
       if constexpr (kMode == kModeSparseBf16) asm volatile("cp.async.wait_all;" ::: "memory");
       if (lane == 0) {
-        for (int32_t i = max(0, issued - 2); i < issued; ++i)
-          (void)mbar_wait(&ctrl->full[i & 1], (i >> 1) & 1, nullptr, kWaitLimitNs);
-        for (int32_t k = max(0, seg - QB + 1); k <= seg; ++k)   // last use of each Q buffer
-          (void)mbar_wait(&ctrl->q_full[k % QB], (k / QB) & 1, nullptr, kWaitLimitNs);
+        for (int32_t i = max(0, issued - kStages); i < issued; ++i)
+          (void)mbar_wait(&ctrl->full[i % kStages], (i / kStages) & 1, nullptr, kWaitLimitNs);
       }
       __syncwarp();
     } else if (warp == kMmaWarp) {
       // ================================================================= MMA
       const uint32_t idesc_qk = make_idesc_bf16(64, 64, false, false);
       const uint32_t idesc_pv = make_idesc_bf16(128, static_cast<uint32_t>(NP), true, false);
-      const uint32_t q_base = smem_u32(sQ);
       const uint32_t st_base = smem_u32(sStage);
       const uint32_t p_base = smem_u32(sP);
-      Walker wk;
-      wk.init(prefix, S, g0);
-      int32_t seg = -1;
+      // Single-thread event loop: issue PV(pv) as soon as its P is written
+      // (checked first: it releases a stage), and QK(qk) once its tile, the
+      // stream's q_hat and the S buffer are ready.  QK(qk) is only issued
+      // after PV(qk-2), so the commit that signals S(qk) also covers the PV
+      // that last read P buffer qk&1.
       bool failed = false;
-      bool prev_first = false;
-      int32_t prev_seg = 0;
-      // PV of local tile k; `first`: k opens a segment, `kseg`: its index
-      auto issue_pv = [&](int32_t k, bool first, int32_t kseg) -> bool {
-        const int st = k & 1;
-        if (!warp_wait(&ctrl->p_full[st], (k >> 1) & 1, abort_flag)) return false;
-        if (first && kseg > 0 && !warp_wait(&ctrl->o_free, (kseg - 1) & 1, abort_flag)) return false;
-        tc_fence_after();
-        if (lane == 0) {
-          const uint32_t a0 = st_base + st * kTileBytes;
-          const uint32_t b0 = p_base + st * NP * 128;
+      if (lane == 0) {
+        Walker wq, wp;
+        wq.init(prefix, S, g0);
+        wp.init(prefix, S, g0);
+        int32_t qk = 0, pv = 0, seg_q = -1, seg_p = -1;
+        uint64_t t_last = globaltimer_ns();
+        while (pv < ntiles) {
+          bool progressed = false;
+          if (pv < qk) {
+            const int st = pv % kStages;
+            const bool first = (pv == 0) || (wp.lt == 0);
+            const int32_t sp = first ? seg_p + 1 : seg_p;
+            const bool ready = mbar_poll(&ctrl->p_full[pv & 1], (pv >> 1) & 1) &&
+                               (!first || sp == 0 || mbar_poll(&ctrl->o_free, (sp - 1) & 1));
+            if (ready) {
+              seg_p = sp;
+              tc_fence_after();
+              const uint32_t a0 = st_base + st * kTileBytes;
+              const uint32_t b0 = p_base + (pv & 1) * NP * 128;
 #pragma unroll
-          for (int mt = 0; mt < 4; ++mt) {
+              for (int mt = 0; mt < 4; ++mt) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t ad = make_smem_desc(a0 + (2 * mt) * kChunkBytes + kk * 2048,
-                                                 kChunkBytes, 1024, kSmemLayoutSW128);
-              const uint64_t bd = make_smem_desc(b0 + kk * 32, 16, 1024, kSmemLayoutSW128);
-              mma_bf16_ss(tmem + 128 + mt * NP, ad, bd, idesc_pv, (first && kk == 0) ? 0u : 1u);
+                for (int kk = 0; kk < 4; ++kk) {
+                  const uint64_t ad = make_smem_desc(a0 + (2 * mt) * kChunkBytes + kk * 2048,
+                                                     kChunkBytes, 1024, kSmemLayoutSW128);
+                  const uint64_t bd = make_smem_desc(b0 + kk * 32, 16, 1024, kSmemLayoutSW128);
+                  mma_bf16_ss(tmem + kColO + mt * NP, ad, bd, idesc_pv, (first && kk == 0) ? 0u : 1u);
+                }
+              }
+              mma_commit(&ctrl->empty[st]);
+              mma_commit(&ctrl->o_done);
+              wp.next(prefix, S);
+              ++pv;
+              progressed = true;
             }
           }
-          mma_commit(&ctrl->empty[st]);
-          mma_commit(&ctrl->o_done);
-        }
-        __syncwarp();
-        return true;
-      };
-      for (int32_t i = 0; i < ntiles; ++i) {
-        const int stage = i & 1;
-        const bool first = (i == 0) || (wk.lt == 0);
-        const bool last = (i == ntiles - 1) || (wk.lt == wk.ntiles - 1);
-        if (first) ++seg;
-        const int qb = seg % QB;
-        if (first && !warp_wait(&ctrl->q_full[qb], (seg / QB) & 1, abort_flag)) { failed = true; break; }
-        if (!warp_wait(&ctrl->full[stage], (i >> 1) & 1, abort_flag)) { failed = true; break; }
-        if (i >= 2 && !warp_wait(&ctrl->s_free[stage], ((i >> 1) - 1) & 1, abort_flag)) {
-          failed = true;
-          break;
-        }
-        tc_fence_after();
-        if (lane == 0) {
-          const uint32_t s_col = tmem + stage * 64;
-          const uint32_t a0 = q_base + qb * L.q_buf_bytes;
-          const uint32_t b0 = st_base + stage * kTileBytes;
+          if (qk < ntiles && qk - pv < 2) {
+            const int st = qk % kStages;
+            const bool first = (qk == 0) || (wq.lt == 0);
+            const int32_t sq = first ? seg_q + 1 : seg_q;
+            const bool ready = (!first || mbar_poll(&ctrl->q_ready, sq & 1)) &&
+                               mbar_poll(&ctrl->full[st], (qk / kStages) & 1) &&
+                               (qk < 1 || mbar_poll(&ctrl->s_free, (qk - 1) & 1));
+            if (ready) {
+              seg_q = sq;
+              // cp.async fills are generic-proxy writes: order them before
+              // the tensor core's async-proxy reads
+              if constexpr (kMode == kModeSparseBf16) fence_proxy_async_smem();
+              tc_fence_after();
+              const uint32_t b0 = st_base + st * kTileBytes;
 #pragma unroll
-          for (int ch = 0; ch < kChunks; ++ch) {
+              for (int ch = 0; ch < kChunks; ++ch) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint64_t ad = make_smem_desc(a0 + ch * L.q_group_bytes + k * 32, 16, 1024, kSmemLayoutSW128);
-              const uint64_t bd = make_smem_desc(b0 + ch * kChunkBytes + k * 32, 16, 1024, kSmemLayoutSW128);
-              mma_bf16_ss(s_col, ad, bd, idesc_qk, (ch | k) ? 1u : 0u);
+                for (int k = 0; k < 4; ++k) {
+                  const uint64_t bd =
+                      make_smem_desc(b0 + ch * kChunkBytes + k * 32, 16, 1024, kSmemLayoutSW128);
+                  mma_bf16_ts(tmem + kColS, tmem + kColQ + (ch * 4 + k) * 8, bd, idesc_qk,
+                              (ch | k) ? 1u : 0u);
+                }
+              }
+              mma_commit(&ctrl->s_full);
+              wq.next(prefix, S);
+              ++qk;
+              progressed = true;
             }
           }
-          mma_commit(&ctrl->s_full[stage]);
-          if (last) mma_commit(&ctrl->q_empty[qb]);
+          if (progressed) {
+            t_last = globaltimer_ns();
+          } else if (*abort_flag || globaltimer_ns() - t_last > kWaitLimitNs) {
+            failed = true;
+            break;
+          }
         }
-        __syncwarp();
-        if (i > 0 && !issue_pv(i - 1, prev_first, prev_seg)) { failed = true; break; }
-        prev_first = first;
-        prev_seg = seg;
-        wk.next(prefix, S);
       }
-      if (!failed && !issue_pv(ntiles - 1, prev_first, prev_seg)) failed = true;
+      __syncwarp();
       if (failed && lane == 0) {
         set_status(p.status, MLA_STATUS_TIMEOUT);
         ctrl->abort_flag = 1;
@@ -421,70 +551,112 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     } else {
       // ============================================================ softmax
-      const int w = warp;                 // 0..3: TMEM lanes [32w, 32w+32)
-      const int h = w * 16 + lane;        // head row owned (M=64 accumulator layout)
-      const bool owner = lane < 16 && h < H;
+      // Warp w reads TMEM lanes [32w, 32w+32).  In the M=64 accumulator
+      // layout S row r sits in lane (r/16)*32 + r%16, so head h = 16w + l
+      // (l < 16) is in lane l of warp w and lanes 16..31 hold no row: lane
+      // l + 16 takes the upper 32 token columns of head h (handed over with
+      // one shuffle per column) and the pair combines max and sum.
+      const int w = warp;
+      const int hl = lane & 15;
+      const int half = lane >> 4;
+      const int h = w * 16 + hl;
+      const bool owner = h < H;
       const bool warp_has_heads = w * 16 < H;
       const uint32_t lane_base = static_cast<uint32_t>(w * 32) << 16;
+      const float scale = p.scale_log2;
       float m_used = -INFINITY, l_run = 0.f;
       Walker wk;
       wk.init(prefix, S, g0);
       bool failed = false;
+      // the first stream's queries
+      load_q_tmem(p.q_hat, wk.s, H, tmem + lane_base, lane, w);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctrl->q_ready);
       for (int32_t i = 0; i < ntiles; ++i) {
-        const int stage = i & 1;
+        const int stage = i % kStages;
+        const int pb = i & 1;
         const bool first = (i == 0) || (wk.lt == 0);
         const bool last = (i == ntiles - 1) || (wk.lt == wk.ntiles - 1);
-        bool ok = !failed && warp_wait(&ctrl->full[stage], (i >> 1) & 1, abort_flag);
+        bool ok = !failed && warp_wait(&ctrl->full[stage], (i / kStages) & 1, abort_flag);
         const uint64_t mask = ctrl->mask[stage];
-        ok = ok && warp_wait(&ctrl->s_full[stage], (i >> 1) & 1, abort_flag);
-        float x[64];
+        ok = ok && warp_wait(&ctrl->s_full, i & 1, abort_flag);
         if (ok) {
           tc_fence_after();
+          float y[32];
           if (warp_has_heads) {
             uint32_t r[32];
-            tmem_ld32(tmem + lane_base + stage * 64, r);
+            tmem_ld32(tmem + lane_base + kColS, r);
 #pragma unroll
-            for (int t = 0; t < 32; ++t) x[t] = __uint_as_float(r[t]);
-            tmem_ld32(tmem + lane_base + stage * 64 + 32, r);
+            for (int t = 0; t < 32; ++t) y[t] = __uint_as_float(r[t]);
+            tmem_ld32(tmem + lane_base + kColS + 32, r);
 #pragma unroll
-            for (int t = 0; t < 32; ++t) x[32 + t] = __uint_as_float(r[t]);
+            for (int t = 0; t < 32; ++t) {
+              const float hi_col = __shfl_xor_sync(0xffffffffu, __uint_as_float(r[t]), 16);
+              if (half) y[t] = hi_col;   // lane l+16 <- columns 32..63 of lane l
+            }
           }
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&ctrl->s_free[stage]);
-          if (owner) {
+          if (lane == 0) mbar_arrive(&ctrl->s_free);
+          if (last && i + 1 < ntiles) {
+            // The next tile opens another stream: its queries replace this
+            // stream's in TMEM.  S(i) was this stream's last QK and it has
+            // completed, so nothing reads the old queries any more.
+            Walker nx = wk;
+            nx.next(prefix, S);
+            load_q_tmem(p.q_hat, nx.s, H, tmem + lane_base, lane, w);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctrl->q_ready);
+          }
+          if (warp_has_heads) {
+            // token of y[t] is 32*half + t
+            const uint32_t hmask = static_cast<uint32_t>(mask >> (32 * half));
             float mt = -INFINITY;
+            if (hmask == 0xffffffffu) {
 #pragma unroll
-            for (int t = 0; t < 64; ++t) {
-              x[t] = ((mask >> t) & 1ull) ? x[t] * p.scale_log2 : -INFINITY;
-              mt = fmaxf(mt, x[t]);
+              for (int t = 0; t < 32; ++t) mt = fmaxf(mt, y[t]);
+            } else {
+#pragma unroll
+              for (int t = 0; t < 32; ++t) {
+                y[t] = ((hmask >> t) & 1u) ? y[t] : -INFINITY;
+                mt = fmaxf(mt, y[t]);
+              }
             }
+            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16)) * scale;
             float alpha = 1.f;
             if (first) {
               m_used = mt;
               l_run = 0.f;
             } else if (mt > m_used + kRescaleThreshold) {
-              alpha = exp2f(m_used - mt);
+              alpha = fast_exp2(m_used - mt);
               m_used = mt;
               l_run *= alpha;
-              ctrl->rescale_tile[stage] = i;
+              if (owner && half == 0) ctrl->rescale_tile[pb] = i;
             }
-            const float ref = (m_used == -INFINITY) ? 0.f : m_used;
-            uint8_t* prow = sP + stage * NP * 128 + h * 128;
+            const float nref = (m_used == -INFINITY) ? 0.f : -m_used;
+            uint8_t* prow = sP + pb * NP * 128 + h * 128;
             float lsum = 0.f;
 #pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) {
+            for (int c8 = 0; c8 < 4; ++c8) {
               uint32_t u[4];
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                u[e] = pack_bf16x2(exp2f(x[c8 * 8 + 2 * e] - ref), exp2f(x[c8 * 8 + 2 * e + 1] - ref));
+                const float a = fast_exp2(fmaf(y[c8 * 8 + 2 * e], scale, nref));
+                const float b = fast_exp2(fmaf(y[c8 * 8 + 2 * e + 1], scale, nref));
+                u[e] = pack_bf16x2(a, b);
                 const __nv_bfloat162 v2 = *reinterpret_cast<__nv_bfloat162*>(&u[e]);
                 lsum += __low2float(v2) + __high2float(v2);
               }
-              *reinterpret_cast<uint4*>(prow + ((c8 ^ (h & 7)) << 4)) = make_uint4(u[0], u[1], u[2], u[3]);
+              if (owner) {
+                const int chunk = 4 * half + c8;
+                *reinterpret_cast<uint4*>(prow + ((chunk ^ (h & 7)) << 4)) =
+                    make_uint4(u[0], u[1], u[2], u[3]);
+              }
             }
-            l_run += lsum;
-            ctrl->alpha[i & 1][h] = alpha;
+            l_run += lsum + __shfl_xor_sync(0xffffffffu, lsum, 16);
+            if (owner && half == 0) ctrl->alpha[pb][h] = alpha;
           }
           if constexpr (kMode != kModeSparseBf16) {
             // Dead rows (tail slots, bad pages): P is 0 there but 0 * NaN
@@ -501,8 +673,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (named_bar_or(1, 128, !ok)) { failed = true; break; }
-        if (!first && ctrl->rescale_tile[stage] == i) {
+        if (!first && ctrl->rescale_tile[pb] == i) {
           // every earlier PV has completed before O^T is rescaled in place
+          // (PV(i-2) is covered by the commit that signalled S(i), so the
+          // barrier is at most one phase behind this wait)
           ok = warp_wait(&ctrl->o_done, (i - 1) & 1, abort_flag);
           failed = !ok;
           if (ok) {
@@ -510,12 +684,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int mt = 0; mt < 4; ++mt) {
               for (int hb = 0; hb < H; hb += 16) {
                 uint32_t v[16];
-                const uint32_t addr = tmem + lane_base + 128 + mt * NP + hb;
+                const uint32_t addr = tmem + lane_base + kColO + mt * NP + hb;
                 tmem_ld16(addr, v);
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                   const int hh = hb + e;
-                  const float a = hh < H ? ctrl->alpha[i & 1][hh] : 1.f;
+                  const float a = hh < H ? ctrl->alpha[pb][hh] : 1.f;
                   v[e] = __float_as_uint(__uint_as_float(v[e]) * a);
                 }
                 tmem_st16(addr, v);
@@ -526,30 +700,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&ctrl->p_full[stage]);
+        if (lane == 0) mbar_arrive(&ctrl->p_full[pb]);
         if (last) {
-          // ---- segment epilogue: normalised partial o_lat and its lse
+          // ---- segment epilogue.  PV(i-1) may still be in flight (QK(i)
+          // is usually issued before it), so wait for its phase first: a
+          // parity wait must never be more than one phase ahead of the
+          // barrier.  PV(i-2) is complete: the commit that signalled S(i)
+          // covers it.
+          if (i >= 1) ok = ok && warp_wait(&ctrl->o_done, (i - 1) & 1, abort_flag);
           ok = ok && warp_wait(&ctrl->o_done, i & 1, abort_flag);
-          const int32_t slot = wk.s + c;
-          if (ok && owner) {
+          const int32_t s = wk.s;
+          const int32_t c_first = tile_owner(prefix[s], total, p.num_ctas);
+          const int32_t c_last = tile_owner(prefix[s + 1] - 1, total, p.num_ctas);
+          const bool split = c_first != c_last;
+          // an unsplit stream's result is final: straight to the outputs
+          float* dst_o = split ? p.part_o + static_cast<int64_t>(s + c) * H * kDc
+                               : p.o_lat + static_cast<int64_t>(s) * H * kDc;
+          float* dst_lse = split ? p.part_lse + static_cast<int64_t>(s + c) * H
+                                 : p.lse + static_cast<int64_t>(s) * H;
+          if (ok && owner && half == 0) {
             ctrl->l_final[h] = l_run;
-            p.part_lse[static_cast<int64_t>(slot) * H + h] =
-                l_run > 0.f ? (m_used + log2f(l_run)) * kLn2 : -INFINITY;
+            dst_lse[h] = l_run > 0.f ? (m_used + __log2f(l_run)) * kLn2 : -INFINITY;
           }
           if (named_bar_or(1, 128, !ok || failed)) { failed = true; break; }
           tc_fence_after();
-          float* out = p.part_o + static_cast<int64_t>(slot) * H * kDc;
           for (int mt = 0; mt < 4; ++mt) {
             const int d = mt * 128 + w * 32 + lane;
             for (int hb = 0; hb < H; hb += 16) {
               uint32_t v[16];
-              tmem_ld16(tmem + lane_base + 128 + mt * NP + hb, v);
+              tmem_ld16(tmem + lane_base + kColO + mt * NP + hb, v);
 #pragma unroll
               for (int e = 0; e < 16; ++e) {
                 const int hh = hb + e;
                 if (hh < H) {
                   const float lf = ctrl->l_final[hh];
-                  out[static_cast<int64_t>(hh) * kDc + d] = lf > 0.f ? __uint_as_float(v[e]) / lf : 0.f;
+                  dst_o[static_cast<int64_t>(hh) * kDc + d] = lf > 0.f ? __uint_as_float(v[e]) / lf : 0.f;
                 }
               }
             }
@@ -557,6 +742,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&ctrl->o_free);
+          if (split) {
+            // The CTA that delivers a stream's last partial merges them all:
+            // lse = ln sum_i exp(lse_i), o = sum_i exp(lse_i - lse) o_i.
+            __threadfence();
+            named_bar_sync(1, 128);
+            if (tid == 0) {
+              const int prev = atomicAdd(&p.counters[s], 1);
+              const int merge = prev == c_last - c_first;
+              if (merge) p.counters[s] = 0;     // ready for the next launch
+              ctrl->merge_flag = merge;
+            }
+            named_bar_sync(1, 128);
+            if (ctrl->merge_flag) {
+              __threadfence();
+              merge_partials(p, s, c_first, c_last - c_first + 1, H, tid, ctrl->l_final);
+            }
+          }
         }
         wk.next(prefix, S);
       }
@@ -567,16 +769,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  // Row sets with no visible token (no tile anywhere): o_lat = 0, lse = -inf.
+  for (int s = c; s < S; s += p.num_ctas) {
+    if (prefix[s + 1] != prefix[s]) continue;
+    float4* o = reinterpret_cast<float4*>(p.o_lat + static_cast<int64_t>(s) * H * kDc);
+    for (int e = tid; e < H * kDc / 4; e += kThreads) o[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int e = tid; e < H; e += kThreads) p.lse[static_cast<int64_t>(s) * H + e] = -INFINITY;
+  }
+
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, tmem_cols(NP));
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
-cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap* kv_map,
-                          const CUtensorMap* q_map, int mode, cudaStream_t stream) {
+cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap* kv_map, int mode,
+                          cudaStream_t stream) {
   const DecodeLayout L = decode_layout(p.heads, p.heads_pad, p.num_streams, mode);
   dim3 grid(p.num_ctas), block(kThreads);
   cudaError_t err;
@@ -585,13 +795,13 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap* kv_map,
       err = cudaFuncSetAttribute(mla_decode_kernel<kModeDenseBf16>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
       if (err != cudaSuccess) return err;
-      mla_decode_kernel<kModeDenseBf16><<<grid, block, L.total, stream>>>(*kv_map, *q_map, p, L);
+      mla_decode_kernel<kModeDenseBf16><<<grid, block, L.total, stream>>>(*kv_map, p, L);
       break;
     case kModeSparseBf16:
       err = cudaFuncSetAttribute(mla_decode_kernel<kModeSparseBf16>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
       if (err != cudaSuccess) return err;
-      mla_decode_kernel<kModeSparseBf16><<<grid, block, L.total, stream>>>(*kv_map, *q_map, p, L);
+      mla_decode_kernel<kModeSparseBf16><<<grid, block, L.total, stream>>>(*kv_map, p, L);
       break;
     default:
       return cudaErrorInvalidValue;

@@ -20,9 +20,9 @@ constexpr int kChunks = kDqk / kChunkElems;  // 9
 constexpr int kChunkBytes = kTile * 128;     // 8 KB: 64 rows x 128 B
 constexpr int kTileBytes = kChunks * kChunkBytes;  // 73,728
 constexpr int kFp8RowBytes = kDqk + kDqk / 32;     // 594
-constexpr int kMaxHeads = 48;
-constexpr int kMaxStreams = 1024;
-constexpr int kStages = 2;
+constexpr int kMaxHeads = 32;     // TMEM: q_hat 288 + S 64 + O^T 4 x 32 columns
+constexpr int kMaxStreams = 256;  // per-stream tile prefix kept in shared memory
+constexpr int kStages = 3;        // 72 KB tiles in flight per CTA
 
 enum DecodeMode : int { kModeDenseBf16 = 0, kModeSparseBf16 = 1, kModeDenseFp8 = 2 };
 
@@ -34,6 +34,9 @@ struct DecodeParams {
   const int32_t* topk_idx;      // [S][width] or null
   float* part_o;                // [slots][H][512]
   float* part_lse;              // [slots][H]
+  int32_t* counters;            // [S] partials delivered per stream (left at 0)
+  float* o_lat;                 // [S][H][512] output
+  float* lse;                   // [S][H] output
   uint32_t* status;
   int32_t batch, q_len, heads, heads_pad;  // heads_pad: N of the PV MMA (multiple of 16)
   int32_t page_size, num_pages, max_pages, topk_width, causal;
@@ -42,17 +45,14 @@ struct DecodeParams {
 };
 
 struct DecodeLayout {   // dynamic shared memory layout of the decode kernel
-  int32_t q_group_bytes;  // ceil(H/8) * 1024: stride between K-chunks of Q
-  int32_t q_buf_bytes;    // one stream's queries: 9 chunks
-  int32_t q_bufs;         // 1 or 2 query buffers
-  int32_t off_q, off_stage, off_p, off_ctrl, total;
+  int32_t off_stage, off_p, off_ctrl, total;
 };
 
 DecodeLayout decode_layout(int heads, int heads_pad, int num_streams, int mode);
 int decode_smem_bytes(int heads, int heads_pad, int num_streams, int mode);
 
-cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap* kv_map,
-                          const CUtensorMap* q_map, int mode, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap* kv_map, int mode,
+                          cudaStream_t stream);
 
 struct CombineParams {
   const float* part_o;

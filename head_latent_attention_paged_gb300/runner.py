@@ -73,19 +73,21 @@ class DecodeStep:
         mla_q_absorb(self.plan, self.q_nope, self.q_rope, self.w_uk, self.q_hat, self.stream)
 
     def run(self):
+        """Attention pass with the split merge fused in: writes o_lat and lse."""
         mla_decode_run(self.plan, self.q_hat, self.cache, self.block_table, self.seq_lens,
-                       self.topk_idx, self.workspace, self.stream)
+                       self.topk_idx, self.workspace, self.o_lat, self.lse, self.stream)
 
     def combine(self):
+        """Re-run the split merge from the partials left in the workspace."""
         mla_combine(self.plan, self.seq_lens, self.workspace, self.o_lat, self.lse, self.stream)
 
     def uv(self):
         mla_uv_proj(self.o_lat, self.w_uv, self.out, self.rows, self.H, self.stream)
 
     def step(self):
-        """run + combine + UV projection (the absorbed query is an input)."""
+        """Attention pass (merge fused) + W_UV projection; the absorbed query
+        is an input."""
         self.run()
-        self.combine()
         self.uv()
 
     def status(self) -> int:
@@ -94,4 +96,4 @@ class DecodeStep:
     def clear_status(self):
         mla_clear_status(self.plan, self.workspace, self.stream)
 
-    KERNELS_PER_STEP = 3
+    KERNELS_PER_STEP = 2

@@ -90,7 +90,7 @@ typedef struct CUstream_st* mla_stream_t;
 typedef struct {
   int32_t batch;            /* B: requests */
   int32_t q_len;            /* Q: query tokens per request (speculative drafts), >= 1 */
-  int32_t num_heads;        /* H: query heads, 1..48 */
+  int32_t num_heads;        /* H: query heads, 1..32 */
   int32_t kv_lora_rank;     /* must be 512 */
   int32_t rope_dim;         /* must be 64 */
   int32_t nope_dim;         /* must be 192 (only read by mla_q_absorb) */
@@ -117,6 +117,7 @@ typedef struct {
   int32_t smem_bytes;       /* dynamic shared memory of the decode kernel */
   int64_t ws_partial_o;     /* byte offset of f32 [num_slots][H][512] */
   int64_t ws_partial_lse;   /* byte offset of f32 [num_slots][H] */
+  int64_t ws_counters;      /* byte offset of int32 [num_streams] merge counters */
   int64_t ws_status;        /* byte offset of the uint32 status word */
   int64_t workspace_bytes;  /* total workspace size */
   int64_t planned_tiles;    /* tiles implied by seq_lens_host (0 if not given) */
@@ -149,10 +150,14 @@ MLA_API int mla_q_absorb(const mla_plan* plan, const void* q_nope, const void* q
                  const void* w_uk, void* q_hat, mla_stream_t stream);
 
 /*
- * mla_decode_run -- the attention pass over the paged cache.  Writes, for
- * every (request, query token) row set and every KV split of it that this
- * plan's grid produces, a partial result (normalised latent output and its
- * natural-log LSE) into the workspace.  mla_combine turns them into o_lat.
+ * mla_decode_run -- the attention pass over the paged cache, with the
+ * split-KV merge fused in.  Each (request, query token) row set is cut into
+ * contiguous 64-token tiles spread evenly over the plan's CTAs; a row set
+ * handled by one CTA writes its result directly, one split over several
+ * CTAs leaves normalised partials (o_i, lse_i) in the workspace and the CTA
+ * delivering the last of them merges: lse = ln sum_i exp(lse_i),
+ * o_lat = sum_i exp(lse_i - lse) o_i.  A row set with no visible token gets
+ * o_lat = 0 and lse = -inf.
  *   q_hat       : bf16 [B*Q][H][576] absorbed queries
  *   kv_cache    : MLA_KV_BF16: bf16 [num_pages][P][576];
  *                 MLA_KV_FP8_E4M3_E8M0: uint8 [num_pages][P * 594]
@@ -162,20 +167,26 @@ MLA_API int mla_q_absorb(const mla_plan* plan, const void* q_nope, const void* q
  *   topk_idx    : NULL for dense; sparse: int32 [B*Q][topk_width] logical
  *                 positions of the request, -1 = masked slot
  *   workspace   : device buffer of plan->workspace_bytes, zeroed once before
- *                 its first use (the status word must start at 0)
+ *                 its first use; the library leaves its counters at zero
+ *                 after every complete run (re-zero it after a run that
+ *                 reported MLA_STATUS_TIMEOUT)
+ *   o_lat       : f32 [B*Q][H][512] output (latent-space attention output)
+ *   lse         : f32 [B*Q][H] output (natural-log LSE of the scaled scores)
+ * Calls on one workspace must not overlap on the device.
  * Returns MLA_OK, MLA_ERR_INVALID_ARGUMENT, MLA_ERR_MISALIGNED,
  * MLA_ERR_UNSUPPORTED or MLA_ERR_CUDA.
  */
 MLA_API int mla_decode_run(const mla_plan* plan, const void* q_hat, const void* kv_cache,
                    const int32_t* block_table, const int32_t* seq_lens,
-                   const int32_t* topk_idx, void* workspace, mla_stream_t stream);
+                   const int32_t* topk_idx, void* workspace, float* o_lat, float* lse,
+                   mla_stream_t stream);
 
 /*
- * mla_combine -- merge the partial results of each row set: lse = ln sum_i
- * exp(lse_i), o_lat = sum_i exp(lse_i - lse) o_i.  A row set with no visible
- * token gets o_lat = 0 and lse = -inf.
- *   seq_lens : the same device int32 [B] given to mla_decode_run
- *   o_lat    : f32 [B*Q][H][512] output;  lse : f32 [B*Q][H] output
+ * mla_combine -- the split-KV merge as a separate pass over the partials a
+ * previous mla_decode_run left in the workspace (same plan, seq_lens and
+ * workspace): rewrites o_lat and lse of every row set that was split over
+ * several CTAs and leaves the others untouched.  mla_decode_run already
+ * performs this merge; the call exists to re-derive or check it.
  */
 MLA_API int mla_combine(const mla_plan* plan, const int32_t* seq_lens, const void* workspace,
                 float* o_lat, float* lse, mla_stream_t stream);

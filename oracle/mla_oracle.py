@@ -216,8 +216,13 @@ def cache_rows_f64(batch, pages: np.ndarray, slots: np.ndarray) -> np.ndarray:
 
 
 def decode(batch, requests: Optional[Iterable[int]] = None,
-           heads: Optional[Sequence[int]] = None, form: str = "non_absorbed"):
+           heads: Optional[Sequence[int]] = None, form: str = "non_absorbed",
+           q_hat: Optional[np.ndarray] = None):
     """Run the oracle over (a subset of) a batch.
+
+    form "non_absorbed" (the definition) or "absorbed" (the cross-check).
+    q_hat: optional float64 [B, Q, H, 576] absorbed query to attend with
+    directly (absorbed form), e.g. one already rounded to bf16.
 
     Returns dict (b, j) -> (o [h, 256], lse [h], o_lat [h, 512]) for the
     requested heads (default all)."""
@@ -239,7 +244,10 @@ def decode(batch, requests: Optional[Iterable[int]] = None,
             c_kv, k_rope = rows[:, :D_C], rows[:, D_C:]
             qn = bf16_to_f64(batch.q_nope[b, j])[heads]
             qr = bf16_to_f64(batch.q_rope[b, j])[heads]
-            if form == "non_absorbed":
+            if q_hat is not None:
+                qh = np.asarray(q_hat[b, j], dtype=np.float64)[heads]
+                res = attend_absorbed(qh[:, :D_C], qh[:, D_C:], w_uv, c_kv, k_rope, w.sm_scale)
+            elif form == "non_absorbed":
                 res = attend_non_absorbed(qn, qr, w_uk, w_uv, c_kv, k_rope, w.sm_scale)
             else:
                 res = attend_absorbed(absorb_query(qn, w_uk), qr, w_uv, c_kv, k_rope,

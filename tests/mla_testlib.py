@@ -46,8 +46,28 @@ def gpu_outputs(step):
     return o, o_lat, lse
 
 
-def compare(ref: dict, o, o_lat, lse, heads=None, label=""):
-    """Check every (b, j) the oracle computed.  Returns the worst figures."""
+def oracle_q_hat(batch: W.Batch) -> np.ndarray:
+    """The absorbed query computed by the oracle in float64 and rounded to
+    bf16 (float64 values, shape [B, Q, H, 576])."""
+    w = batch.workload
+    out = np.empty((w.batch, w.q_len, w.heads, 576))
+    w_uk = O.bf16_to_f64(batch.w_uk)
+    for b in range(w.batch):
+        for j in range(w.q_len):
+            out[b, j, :, :512] = O.round_to_bf16(O.absorb_query(O.bf16_to_f64(batch.q_nope[b, j]), w_uk))
+            out[b, j, :, 512:] = O.bf16_to_f64(batch.q_rope[b, j])
+    return out
+
+
+def upload_q_hat(step, q_hat_f64):
+    import torch
+    bits = W.f32_to_bf16_bits(q_hat_f64.astype(np.float32).reshape(step.rows, step.H, 576))
+    step.q_hat.copy_(torch.from_numpy(bits.view(np.int16)).to(step.q_hat.device).view(torch.bfloat16))
+
+
+def compare(ref: dict, o, o_lat, lse, heads=None, label="", lse_ref=None):
+    """Check every (b, j) the oracle computed.  Returns the worst figures.
+    lse_ref: optional dict (b, j) -> lse to compare lse with instead."""
     worst = {"max_abs": 0.0, "rel_l2": 0.0, "lse": 0.0, "lat_rel_l2": 0.0}
     for (b, j), (ro, rlse, rlat) in ref.items():
         hs = slice(None) if heads is None else list(heads)
@@ -62,6 +82,8 @@ def compare(ref: dict, o, o_lat, lse, heads=None, label=""):
         max_abs = float(err.max())
         rel = float(np.linalg.norm(go - ro) / max(np.linalg.norm(ro), 1e-30))
         lat_rel = float(np.linalg.norm(glat - rlat) / max(np.linalg.norm(rlat), 1e-30))
+        if lse_ref is not None:
+            rlse = lse_ref[(b, j)][1]
         lse_err = float(np.abs(glse - rlse).max())
         worst["max_abs"] = max(worst["max_abs"], max_abs)
         worst["rel_l2"] = max(worst["rel_l2"], rel)

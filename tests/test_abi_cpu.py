@@ -61,7 +61,8 @@ def test_plan_ok_and_workspace_layout(m):
     assert plan.num_slots == 4 + plan.num_ctas - 1
     assert plan.ws_partial_o == 0
     assert plan.ws_partial_lse >= plan.num_slots * 20 * 512 * 4
-    assert plan.ws_status >= plan.ws_partial_lse + plan.num_slots * 20 * 4
+    assert plan.ws_counters >= plan.ws_partial_lse + plan.num_slots * 20 * 4
+    assert plan.ws_status >= plan.ws_counters + 4 * 4
     assert plan.workspace_bytes > plan.ws_status
     assert plan.smem_bytes <= 232448
     # no host seq_lens: fill every SM
@@ -70,11 +71,11 @@ def test_plan_ok_and_workspace_layout(m):
 
 @pytest.mark.parametrize("kw,code", [
     (dict(page_size=96), -2), (dict(page_size=32), -2), (dict(num_heads=0), -1),
-    (dict(num_heads=49), -2), (dict(q_len=0), -1), (dict(batch=-1), -1),
+    (dict(num_heads=33), -2), (dict(q_len=0), -1), (dict(batch=-1), -1),
     (dict(topk_width=100), -2), (dict(topk_width=-128), -1), (dict(kv_lora_rank=256), -2),
     (dict(rope_dim=32), -2), (dict(v_head_dim=128), -2), (dict(nope_dim=128), -2),
     (dict(causal=2), -1), (dict(sm_scale=0.0), -1), (dict(sm_scale=float("nan")), -1),
-    (dict(num_pages=0), -1), (dict(max_pages_per_seq=0), -1), (dict(batch=2000), -2),
+    (dict(num_pages=0), -1), (dict(max_pages_per_seq=0), -1), (dict(batch=257), -2), (dict(batch=65, q_len=4), -2),
 ])
 def test_plan_rejects(m, kw, code):
     with pytest.raises(m.MlaError) as e:
@@ -95,16 +96,22 @@ def test_calls_reject_null_and_misaligned_pointers_before_cuda(m):
     plan = m.mla_decode_plan(_problem(m), None, 152)
     A = 1 << 20    # an aligned fake address: never dereferenced, the call fails first
     with pytest.raises(m.MlaError) as e:
-        m.mla_decode_run(plan, None, A, A, A, None, A)
+        m.mla_decode_run(plan, None, A, A, A, None, A, A, A)
     assert e.value.code == -1
     with pytest.raises(m.MlaError) as e:   # dense problem given a top-k list
-        m.mla_decode_run(plan, A, A, A, A, A, A)
+        m.mla_decode_run(plan, A, A, A, A, A, A, A, A)
     assert e.value.code == -1
     with pytest.raises(m.MlaError) as e:
-        m.mla_decode_run(plan, A + 8, A, A, A, None, A)
+        m.mla_decode_run(plan, A + 8, A, A, A, None, A, A, A)
     assert e.value.code == -3
     with pytest.raises(m.MlaError) as e:
         m.mla_combine(plan, A, A, A + 4, A)
+    assert e.value.code == -3
+    with pytest.raises(m.MlaError) as e:   # output pointers are required
+        m.mla_decode_run(plan, A, A, A, A, None, A, None, A)
+    assert e.value.code == -1
+    with pytest.raises(m.MlaError) as e:
+        m.mla_decode_run(plan, A, A, A, A, None, A, A + 8, A)
     assert e.value.code == -3
     with pytest.raises(m.MlaError) as e:
         m.mla_uv_proj(A, A, A, -1, 20)
@@ -117,7 +124,7 @@ def test_calls_reject_null_and_misaligned_pointers_before_cuda(m):
     assert e.value.code == -1
     sparse = m.mla_decode_plan(_problem(m, topk_width=256), None, 152)
     with pytest.raises(m.MlaError) as e:   # sparse problem without a top-k list
-        m.mla_decode_run(sparse, A, A, A, A, None, A)
+        m.mla_decode_run(sparse, A, A, A, A, None, A, A, A)
     assert e.value.code == -1
 
 

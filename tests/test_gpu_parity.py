@@ -9,7 +9,8 @@ import pytest
 
 import oracle as O
 import workloads as W
-from mla_testlib import compare, ensure_built, gpu_outputs, make_step, with_fp8
+from mla_testlib import (compare, ensure_built, gpu_outputs, make_step, oracle_q_hat,
+                         upload_q_hat, with_fp8)
 
 pytestmark = pytest.mark.gpu
 
@@ -42,15 +43,42 @@ def test_small_workloads_match_oracle(name, garbage):
 @pytest.mark.parametrize("sm_count", [1, 3, 7, 40, 152])
 def test_split_invariance(sm_count):
     """Every way of cutting the streams over CTAs (one split, many, uneven)
-    gives the same result to fp32 rounding, and matches the oracle."""
+    matches the oracle, and the splits agree with each other to the bf16
+    rounding of P: probabilities are rounded to bf16 (relative error up to
+    2^-9) against each split's own running maximum, so two splits round
+    differently; the latent outputs agree to 2e-3 relative L2 and lse to
+    5e-4."""
     batch = W.generate(W.SMALL_WORKLOADS["long_small"])
     ref_step = make_step(batch, sm_count=1)
     ref_step.step()
     o1, lat1, lse1 = gpu_outputs(ref_step)
     step, _ = _run_and_compare(batch, sm_count=sm_count, label=f"split{sm_count}")
     o2, lat2, lse2 = gpu_outputs(step)
-    assert np.linalg.norm(lat2 - lat1) <= 1e-5 * np.linalg.norm(lat1)
-    assert np.abs(lse2 - lse1).max() <= 1e-5
+    assert np.linalg.norm(lat2 - lat1) <= 2e-3 * np.linalg.norm(lat1)
+    assert np.abs(lse2 - lse1).max() <= 5e-4
+
+
+@pytest.mark.parametrize("sm_count", [7, 40])
+def test_fused_merge_equals_separate_combine(sm_count):
+    """The merge fused into the decode launch and the separate combine pass
+    over the same partials give the same o_lat and lse, and the merge
+    counters are back at zero after each launch (a second launch on the same
+    workspace gives identical results)."""
+    batch = W.generate(W.SMALL_WORKLOADS["long_small"])
+    step = make_step(batch, sm_count=sm_count)
+    step.run()
+    _, lat1, lse1 = gpu_outputs(step)
+    pl = step.plan
+    counters = step.workspace[pl.ws_counters: pl.ws_counters + 4 * pl.num_streams]
+    assert int(counters.view(torch.int32).abs().sum()) == 0
+    step.o_lat.fill_(float("nan"))
+    step.lse.fill_(float("nan"))
+    step.run()
+    _, lat2, lse2 = gpu_outputs(step)
+    assert np.array_equal(lat1, lat2) and np.array_equal(lse1, lse2)
+    step.combine()
+    _, lat3, lse3 = gpu_outputs(step)
+    assert np.allclose(lat3, lat1, rtol=1e-5, atol=1e-6) and np.allclose(lse3, lse1, atol=1e-5)
 
 
 def test_absorb_matches_oracle():
@@ -113,7 +141,7 @@ def test_one_hot_gather_is_bit_exact(page_size):
         for h in range(H):
             t = planted[(b, h)]
             page, slot = batch.block_table[b, t // page_size], t % page_size
-            cache[page, slot, 512 + h] = W.f32_to_bf16_bits(np.float32(1.0))
+            cache[page, slot, 512 + h] = 0x3F80                 # bf16 1.0
             q[b, 0, h, 512 + h] = 2048.0          # score 2048 / 16 = 128 nats
     # a token planted for two heads carries both flags; distinct heads still
     # see exactly one live row with a large score
@@ -188,10 +216,23 @@ def test_bad_sparse_index_is_masked_and_reported():
 
 
 def test_empty_and_single_token_requests():
+    """Lengths 0, 1, one page, one page + 1.  At T = 1 the lse is the single
+    score, so the bf16 rounding of the absorbed query alone moves it by up to a
+    few 1e-3: the decode is fed the oracle's own bf16 absorbed query and its
+    lse is compared with the oracle's absorbed form on exactly that query;
+    outputs are compared with the non-absorbed definition."""
     w = W.with_overrides(W.SMALL_WORKLOADS["dense_small"], seq_lens=(0, 1, 64, 65, 0, 129),
                          batch=6)
     batch = W.generate(w)
-    _run_and_compare(batch, label="edge-lengths")
+    q_hat = oracle_q_hat(batch)
+    step = make_step(batch, absorb=False)
+    upload_q_hat(step, q_hat)
+    step.step()
+    o, o_lat, lse = gpu_outputs(step)
+    assert step.status() == 0
+    ref = O.decode(batch)
+    lse_ref = O.decode(batch, q_hat=q_hat)
+    compare(ref, o, o_lat, lse, label="edge-lengths", lse_ref=lse_ref)
 
 
 def test_multi_token_causal_dense():
