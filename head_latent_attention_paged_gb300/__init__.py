@@ -37,6 +37,7 @@ MLA_TILE_TOKENS = 64
 EXPORTED = (
     "mla_decode_plan", "mla_q_absorb", "mla_decode_run", "mla_combine", "mla_uv_proj",
     "mla_get_status", "mla_clear_status", "mla_strerror", "mla_version",
+    "mla_decode_run_static",
 )
 
 
@@ -86,6 +87,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.mla_q_absorb.argtypes = [P(MlaPlan), vp, vp, vp, vp, vp]
     lib.mla_decode_run.argtypes = [P(MlaPlan), vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.mla_combine.argtypes = [P(MlaPlan), vp, vp, vp, vp, vp]
+    lib.mla_decode_run_static.argtypes = [P(MlaPlan), vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.mla_uv_proj.argtypes = [vp, vp, vp, i32, i32, vp]
     lib.mla_get_status.argtypes = [P(MlaPlan), vp, P(ctypes.c_uint32), vp]
     lib.mla_clear_status.argtypes = [P(MlaPlan), vp, vp]
@@ -160,6 +162,15 @@ def mla_decode_run(plan: MlaPlan, q_hat, kv_cache, block_table, seq_lens, topk_i
     _check("mla_decode_run", load().mla_decode_run(
         ctypes.byref(plan), _ptr(q_hat), _ptr(kv_cache), _ptr(block_table), _ptr(seq_lens),
         _ptr(topk_idx), _ptr(workspace), _ptr(o_lat), _ptr(lse), _stream(stream)))
+
+
+def mla_decode_run_static(plan: MlaPlan, q_hat, kv_cache, block_table, seq_lens, topk_idx,
+                          o_lat, lse, status=None, stream=None) -> None:
+    """mla_decode_run without a caller workspace: the scratch is the library's
+    fixed 16 MiB device array (for callers that cannot allocate)."""
+    _check("mla_decode_run_static", load().mla_decode_run_static(
+        ctypes.byref(plan), _ptr(q_hat), _ptr(kv_cache), _ptr(block_table), _ptr(seq_lens),
+        _ptr(topk_idx), _ptr(o_lat), _ptr(lse), _ptr(status), _stream(stream)))
 
 
 def mla_combine(plan: MlaPlan, seq_lens, workspace, o_lat, lse, stream=None) -> None:

@@ -201,6 +201,32 @@ MLA_API int mla_combine(const mla_plan* plan, const int32_t* seq_lens, const voi
 MLA_API int mla_uv_proj(const float* o_lat, const void* w_uv, void* out, int32_t rows,
                 int32_t num_heads, mla_stream_t stream);
 
+/*
+ * mla_decode_run_static -- mla_decode_run for callers that cannot allocate
+ * device memory (the pages describe no such call; this library adds it).
+ * Code that runs while a CUDA graph is being captured, or inside a runtime
+ * that only hands out the input and output buffers it owns, cannot create
+ * the workspace mla_decode_run needs.  This call uses instead one fixed
+ * 16 MiB scratch array that the library keeps in device memory (every GPU
+ * that loads the library holds it until exit); it calls no allocator.
+ *   plan            : from mla_decode_plan; plan->workspace_bytes must be at
+ *                     most 16 MiB, else MLA_ERR_WORKSPACE_TOO_SMALL and
+ *                     nothing is launched.
+ *   q_hat ... lse   : as for mla_decode_run (caller-owned inputs, outputs).
+ *   status          : optional device uint32 that receives this call's
+ *                     status bits (MLA_STATUS_*), or NULL.
+ * The scratch array is shared by all calls on a device and keeps the last
+ * call's contents; each call clears the parts that must start at zero on
+ * `stream` before launching.  Calls that overlap on the GPU race on the
+ * array: order them on one stream.  The first call on a device looks up
+ * the array's address with that device current; make it before any stream
+ * capture starts.
+ */
+MLA_API int mla_decode_run_static(const mla_plan* plan, const void* q_hat, const void* kv_cache,
+                          const int32_t* block_table, const int32_t* seq_lens,
+                          const int32_t* topk_idx, float* o_lat, float* lse, uint32_t* status,
+                          mla_stream_t stream);
+
 /* Synchronous read of the device status word (waits for `stream`). */
 MLA_API int mla_get_status(const mla_plan* plan, const void* workspace, uint32_t* bits,
                    mla_stream_t stream);
