@@ -140,99 +140,139 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 
-// Write stream s's absorbed queries into TMEM as the M=64 A operand: head h
-// = 16w + l (l < 16) goes to lane 32w + l, 576 bf16 packed two per column.
-// Called by all four softmax warps (each writes its own lane quarter);
-// rows of absent heads are written as zeros.  Three chunks of 64 values are
-// loaded per batch so several global loads are in flight.
+// Write stream s's absorbed queries into TMEM as the M=64 A operand.  Head
+// h sits in row 32 + h, i.e. lane 64 + h for h < 16 and lane 96 + (h - 16)
+// for 16 <= h < 32 (row r of the M=64 layout lives in lane
+// (r/16)*32 + r%16), so only softmax warps 2 and 3 hold heads and warps 0
+// and 1 leave their SM sub-partitions to the producer and MMA warps.
+// Called by warps 2 and 3 (each writes its own lane quarter); 576 bf16 are
+// packed two per column; rows of absent heads are written as zeros.  The
+// loads go in two batches (5 + 4 chunks of 64 values) to keep many in flight.
 __device__ __forceinline__ void load_q_tmem(const uint16_t* q_hat, int32_t s, int H,
                                             uint32_t taddr_lane, int lane, int w) {
-  const int h = w * 16 + (lane & 15);
+  const int h = (w - 2) * 16 + (lane & 15);
   const bool live = lane < 16 && h < H;
   const uint4* src =
       reinterpret_cast<const uint4*>(q_hat + (static_cast<int64_t>(s) * H + (live ? h : 0)) * kDqk);
-#pragma unroll 1
-  for (int cb = 0; cb < kChunks; cb += 3) {
-    uint4 v[3][8];
 #pragma unroll
-    for (int c = 0; c < 3; ++c)
+  for (int cb = 0; cb < kChunks; cb += 5) {
+    const int n = (cb == 0) ? 5 : 4;
+    uint4 v[5][8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) v[c][q] = live ? __ldg(src + (cb + c) * 8 + q) : make_uint4(0, 0, 0, 0);
+    for (int c = 0; c < 5; ++c)
 #pragma unroll
-    for (int c = 0; c < 3; ++c) {
-      uint32_t r[32];
+      for (int q = 0; q < 8; ++q)
+        v[c][q] = (live && c < n) ? __ldg(src + (cb + c) * 8 + q) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        r[4 * q] = v[c][q].x;
-        r[4 * q + 1] = v[c][q].y;
-        r[4 * q + 2] = v[c][q].z;
-        r[4 * q + 3] = v[c][q].w;
+    for (int c = 0; c < 5; ++c) {
+      if (c < n) {
+        uint32_t r[32];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          r[4 * q] = v[c][q].x;
+          r[4 * q + 1] = v[c][q].y;
+          r[4 * q + 2] = v[c][q].z;
+          r[4 * q + 3] = v[c][q].w;
+        }
+        tmem_st32(taddr_lane + kColQ + (cb + c) * 32, r);
       }
-      tmem_st32(taddr_lane + kColQ + (cb + c) * 32, r);
     }
   }
 }
 
+// Ask L2 to fetch stream s's absorbed queries ahead of their TMEM load.
+__device__ __forceinline__ void prefetch_q(const uint16_t* q_hat, int32_t s, int H, int t, int nt) {
+  const char* base = reinterpret_cast<const char*>(q_hat + static_cast<int64_t>(s) * H * kDqk);
+  const int lines = (H * kDqk * 2 + 127) / 128;
+  for (int i = t; i < lines; i += nt)
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(base + static_cast<int64_t>(i) * 128));
+}
+
 // Merge the nseg partials (slots s + c_first ...) of row set s into o_lat and
-// lse.  128 threads; thread t owns latent dims [4t, 4t + 4) of every head.
-// The partials were written by other CTAs (L2-resident): loads bypass L1
-// and are batched 4 heads x 4 partials at a time to keep many in flight.
+// lse: lse = ln sum_i exp(lse_i), o = sum_i exp(lse_i - lse) o_i.  Run by the
+// 128 softmax threads after the tile loop; thread t owns latent dims
+// [4t, 4t + 4) of every head.  The partials were written by other CTAs
+// (L2-resident): the lse values go through shared memory in one round trip
+// (`scratch`, `scratch_floats` floats, free once the tile loop is over), the
+// weights are formed there, and the partial outputs are loaded 8 heads x 4
+// partials at a time so many loads are in flight.
 __device__ __forceinline__ void merge_partials(const DecodeParams& p, int32_t s, int32_t c_first,
-                                               int32_t nseg, int H, int tid, float* tot_sm) {
+                                               int32_t nseg, int H, int tid, float* tot_sm,
+                                               float* scratch, int scratch_floats) {
   const float* plse = p.part_lse + static_cast<int64_t>(s + c_first) * H;
   const float4* po = reinterpret_cast<const float4*>(p.part_o + static_cast<int64_t>(s + c_first) * H * kDc);
-  if (tid < H) {
-    float m = -INFINITY;
-    for (int k = 0; k < nseg; ++k) m = fmaxf(m, __ldcg(plse + static_cast<int64_t>(k) * H + tid));
-    float tot = -INFINITY;
-    if (m != -INFINITY) {
-      float sum = 0.f;
-      for (int k = 0; k < nseg; ++k) sum += __expf(__ldcg(plse + static_cast<int64_t>(k) * H + tid) - m);
-      tot = m + __logf(sum);
+  const int kc = max(1, min(nseg, scratch_floats / H));   // partials per chunk
+  // ---- per-head total lse (running max / sum over chunks of partials)
+  float m = -INFINITY, sum = 0.f;
+  for (int k0 = 0; k0 < nseg; k0 += kc) {
+    const int n = min(kc, nseg - k0);
+    for (int e = tid; e < n * H; e += 128) scratch[e] = __ldcg(plse + static_cast<int64_t>(k0) * H + e);
+    named_bar_sync(1, 128);
+    if (tid < H) {
+      float mc = m;
+      for (int k = 0; k < n; ++k) mc = fmaxf(mc, scratch[k * H + tid]);
+      if (mc != -INFINITY) {
+        float acc = (m == -INFINITY) ? 0.f : sum * __expf(m - mc);
+        for (int k = 0; k < n; ++k) acc += __expf(scratch[k * H + tid] - mc);
+        m = mc;
+        sum = acc;
+      }
     }
+    named_bar_sync(1, 128);
+  }
+  if (tid < H) {
+    const float tot = (m == -INFINITY) ? -INFINITY : m + __logf(sum);
     tot_sm[tid] = tot;
     p.lse[static_cast<int64_t>(s) * H + tid] = tot;
   }
   named_bar_sync(1, 128);
-  for (int hb = 0; hb < H; hb += 4) {
-    float tot[4];
-    float4 acc[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      tot[j] = (hb + j < H) ? tot_sm[hb + j] : -INFINITY;
-      acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  // ---- weighted sum of the partial outputs, chunk by chunk (the weights of a
+  // chunk live in scratch; 8 heads x 4 partials of loads in flight)
+  for (int k0 = 0; k0 < nseg; k0 += kc) {
+    const int n = min(kc, nseg - k0);
+    for (int e = tid; e < n * H; e += 128) {
+      const int hh = e % H;
+      const float lv = __ldcg(plse + static_cast<int64_t>(k0) * H + e);
+      scratch[e] = (tot_sm[hh] == -INFINITY || lv == -INFINITY) ? 0.f : __expf(lv - tot_sm[hh]);
     }
-    for (int kb = 0; kb < nseg; kb += 4) {
-      float lv[4][4];
-      float4 v[4][4];
+    named_bar_sync(1, 128);
+    for (int hb = 0; hb < H; hb += 8) {
+      float4 acc[8];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
+      for (int j = 0; j < 8; ++j) {
+        acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (k0 > 0 && hb + j < H)   // continue the sums of earlier chunks
+          acc[j] = reinterpret_cast<const float4*>(p.o_lat + (static_cast<int64_t>(s) * H + hb + j) * kDc)[tid];
+      }
+      for (int kb = 0; kb < n; kb += 4) {
+        float4 v[8][4];
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const int k = kb + kk;
-          const bool use = k < nseg && tot[j] != -INFINITY;
-          const int64_t row = static_cast<int64_t>(k) * H + hb + j;
-          lv[j][kk] = use ? __ldcg(plse + row) : -INFINITY;
-          v[j][kk] = use ? __ldcg(po + row * (kDc / 4) + tid) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+        for (int j = 0; j < 8; ++j)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const bool use = hb + j < H && kb + kk < n;
+            v[j][kk] = use ? __ldcg(po + (static_cast<int64_t>(k0 + kb + kk) * H + hb + j) * (kDc / 4) + tid)
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const float wgt = (hb + j < H && kb + kk < n) ? scratch[(kb + kk) * H + hb + j] : 0.f;
+            acc[j].x = fmaf(wgt, v[j][kk].x, acc[j].x);
+            acc[j].y = fmaf(wgt, v[j][kk].y, acc[j].y);
+            acc[j].z = fmaf(wgt, v[j][kk].z, acc[j].z);
+            acc[j].w = fmaf(wgt, v[j][kk].w, acc[j].w);
+          }
       }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const float wgt = (lv[j][kk] == -INFINITY) ? 0.f : __expf(lv[j][kk] - tot[j]);
-          acc[j].x = fmaf(wgt, v[j][kk].x, acc[j].x);
-          acc[j].y = fmaf(wgt, v[j][kk].y, acc[j].y);
-          acc[j].z = fmaf(wgt, v[j][kk].z, acc[j].z);
-          acc[j].w = fmaf(wgt, v[j][kk].w, acc[j].w);
-        }
-      }
+      for (int j = 0; j < 8; ++j)
+        if (hb + j < H)
+          reinterpret_cast<float4*>(p.o_lat + (static_cast<int64_t>(s) * H + hb + j) * kDc)[tid] = acc[j];
     }
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if (hb + j < H)
-        reinterpret_cast<float4*>(p.o_lat + (static_cast<int64_t>(s) * H + hb + j) * kDc)[tid] = acc[j];
+    named_bar_sync(1, 128);   // scratch is rewritten by the next chunk
   }
+  named_bar_sync(1, 128);   // tot_sm may be reused by the next merge
 }
 
 }  // namespace
@@ -456,8 +496,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ================================================================= MMA
       const uint32_t idesc_qk = make_idesc_bf16(64, 64, false, false);
       const uint32_t idesc_pv = make_idesc_bf16(128, static_cast<uint32_t>(NP), true, false);
-      const uint32_t st_base = smem_u32(sStage);
-      const uint32_t p_base = smem_u32(sP);
+      // Descriptors at the buffers' bases; an operand at byte offset x is
+      // base + (x >> 4) (the start-address field holds address >> 4 and the
+      // whole buffer lies below 256 KB, so the field never carries).
+      const uint64_t qk_b0 = make_smem_desc(smem_u32(sStage), 16, 1024, kSmemLayoutSW128);
+      const uint64_t pv_a0 = make_smem_desc(smem_u32(sStage), kChunkBytes, 1024, kSmemLayoutSW128);
+      const uint64_t pv_b0 = make_smem_desc(smem_u32(sP), 16, 1024, kSmemLayoutSW128);
       // Single-thread event loop: issue PV(pv) as soon as its P is written
       // (checked first: it releases a stage), and QK(qk) once its tile, the
       // stream's q_hat and the S buffer are ready.  QK(qk) is only issued
@@ -481,17 +525,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ready) {
               seg_p = sp;
               tc_fence_after();
-              const uint32_t a0 = st_base + st * kTileBytes;
-              const uint32_t b0 = p_base + (pv & 1) * NP * 128;
+              const uint64_t a0 = pv_a0 + static_cast<uint64_t>((st * kTileBytes) >> 4);
+              const uint64_t b0 = pv_b0 + static_cast<uint64_t>(((pv & 1) * NP * 128) >> 4);
 #pragma unroll
               for (int mt = 0; mt < 4; ++mt) {
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                  const uint64_t ad = make_smem_desc(a0 + (2 * mt) * kChunkBytes + kk * 2048,
-                                                     kChunkBytes, 1024, kSmemLayoutSW128);
-                  const uint64_t bd = make_smem_desc(b0 + kk * 32, 16, 1024, kSmemLayoutSW128);
-                  mma_bf16_ss(tmem + kColO + mt * NP, ad, bd, idesc_pv, (first && kk == 0) ? 0u : 1u);
-                }
+                for (int kk = 0; kk < 4; ++kk)
+                  mma_bf16_ss(tmem + kColO + mt * NP, a0 + ((2 * mt * kChunkBytes + kk * 2048) >> 4),
+                              b0 + ((kk * 32) >> 4), idesc_pv, (first && kk == 0) ? 0u : 1u);
               }
               mma_commit(&ctrl->empty[st]);
               mma_commit(&ctrl->o_done);
@@ -513,16 +554,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               // the tensor core's async-proxy reads
               if constexpr (kMode == kModeSparseBf16) fence_proxy_async_smem();
               tc_fence_after();
-              const uint32_t b0 = st_base + st * kTileBytes;
+              const uint64_t b0 = qk_b0 + static_cast<uint64_t>((st * kTileBytes) >> 4);
 #pragma unroll
               for (int ch = 0; ch < kChunks; ++ch) {
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                  const uint64_t bd =
-                      make_smem_desc(b0 + ch * kChunkBytes + k * 32, 16, 1024, kSmemLayoutSW128);
-                  mma_bf16_ts(tmem + kColS, tmem + kColQ + (ch * 4 + k) * 8, bd, idesc_qk,
-                              (ch | k) ? 1u : 0u);
-                }
+                for (int k = 0; k < 4; ++k)
+                  mma_bf16_ts(tmem + kColS, tmem + kColQ + (ch * 4 + k) * 8,
+                              b0 + ((ch * kChunkBytes + k * 32) >> 4), idesc_qk, (ch | k) ? 1u : 0u);
               }
               mma_commit(&ctrl->s_full);
               wq.next(prefix, S);
@@ -535,6 +573,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else if (*abort_flag || globaltimer_ns() - t_last > kWaitLimitNs) {
             failed = true;
             break;
+          } else {
+            __nanosleep(20);   // back off: polling shares the SM with the math
           }
         }
       }
@@ -551,25 +591,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     } else {
       // ============================================================ softmax
-      // Warp w reads TMEM lanes [32w, 32w+32).  In the M=64 accumulator
-      // layout S row r sits in lane (r/16)*32 + r%16, so head h = 16w + l
-      // (l < 16) is in lane l of warp w and lanes 16..31 hold no row: lane
-      // l + 16 takes the upper 32 token columns of head h (handed over with
-      // one shuffle per column) and the pair combines max and sum.
+      // Warp w reads TMEM lanes [32w, 32w+32).  Head h is S row 32 + h: in
+      // the M=64 accumulator layout (row r in lane (r/16)*32 + r%16) heads
+      // 0..15 are lanes 0..15 of warp 2 and heads 16..31 lanes 0..15 of warp
+      // 3; lanes 16..31 hold no row, so lane l + 16 takes the upper 32 token
+      // columns of lane l's head (one shuffle per column) and the pair
+      // combines max and sum.  Warps 0 and 1 only join the epilogue, the
+      // rescale and the dead-row zeroing.
       const int w = warp;
       const int hl = lane & 15;
       const int half = lane >> 4;
-      const int h = w * 16 + hl;
-      const bool owner = h < H;
-      const bool warp_has_heads = w * 16 < H;
+      const int h = (w - 2) * 16 + hl;
+      const bool warp_has_heads = w >= 2 && (w - 2) * 16 < H;
+      const bool owner = warp_has_heads && h < H;
       const uint32_t lane_base = static_cast<uint32_t>(w * 32) << 16;
       const float scale = p.scale_log2;
       float m_used = -INFINITY, l_run = 0.f;
       Walker wk;
       wk.init(prefix, S, g0);
       bool failed = false;
+      int npend = 0;
+      int32_t pend_s0 = 0, pend_f0 = 0, pend_l0 = 0, pend_s1 = 0, pend_f1 = 0, pend_l1 = 0;
       // the first stream's queries
-      load_q_tmem(p.q_hat, wk.s, H, tmem + lane_base, lane, w);
+      if (w >= 2) load_q_tmem(p.q_hat, wk.s, H, tmem + lane_base, lane, w);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctrl->q_ready);
@@ -578,6 +622,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int pb = i & 1;
         const bool first = (i == 0) || (wk.lt == 0);
         const bool last = (i == ntiles - 1) || (wk.lt == wk.ntiles - 1);
+        if (first && w < 2) {
+          // warm L2 with the next stream's queries (loaded into TMEM when
+          // this segment ends)
+          int32_t sn = wk.s + 1;
+          while (sn < S && prefix[sn + 1] == prefix[sn]) ++sn;
+          if (sn < S && prefix[sn] < g1) prefetch_q(p.q_hat, sn, H, tid, 64);
+        }
         bool ok = !failed && warp_wait(&ctrl->full[stage], (i / kStages) & 1, abort_flag);
         const uint64_t mask = ctrl->mask[stage];
         ok = ok && warp_wait(&ctrl->s_full, i & 1, abort_flag);
@@ -605,7 +656,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // completed, so nothing reads the old queries any more.
             Walker nx = wk;
             nx.next(prefix, S);
-            load_q_tmem(p.q_hat, nx.s, H, tmem + lane_base, lane, w);
+            if (w >= 2) load_q_tmem(p.q_hat, nx.s, H, tmem + lane_base, lane, w);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctrl->q_ready);
@@ -719,7 +770,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float* dst_lse = split ? p.part_lse + static_cast<int64_t>(s + c) * H
                                  : p.lse + static_cast<int64_t>(s) * H;
           if (ok && owner && half == 0) {
-            ctrl->l_final[h] = l_run;
+            ctrl->l_final[h] = l_run > 0.f ? 1.f / l_run : 0.f;   // o = O / l
             dst_lse[h] = l_run > 0.f ? (m_used + __log2f(l_run)) * kLn2 : -INFINITY;
           }
           if (named_bar_or(1, 128, !ok || failed)) { failed = true; break; }
@@ -732,35 +783,52 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int e = 0; e < 16; ++e) {
                 const int hh = hb + e;
-                if (hh < H) {
-                  const float lf = ctrl->l_final[hh];
-                  dst_o[static_cast<int64_t>(hh) * kDc + d] = lf > 0.f ? __uint_as_float(v[e]) / lf : 0.f;
-                }
+                if (hh < H) dst_o[static_cast<int64_t>(hh) * kDc + d] = __uint_as_float(v[e]) * ctrl->l_final[hh];
               }
             }
           }
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&ctrl->o_free);
-          if (split) {
-            // The CTA that delivers a stream's last partial merges them all:
-            // lse = ln sum_i exp(lse_i), o = sum_i exp(lse_i - lse) o_i.
-            __threadfence();
-            named_bar_sync(1, 128);
-            if (tid == 0) {
-              const int prev = atomicAdd(&p.counters[s], 1);
-              const int merge = prev == c_last - c_first;
-              if (merge) p.counters[s] = 0;     // ready for the next launch
-              ctrl->merge_flag = merge;
-            }
-            named_bar_sync(1, 128);
-            if (ctrl->merge_flag) {
-              __threadfence();
-              merge_partials(p, s, c_first, c_last - c_first + 1, H, tid, ctrl->l_final);
-            }
+          if (split) {   // merged after this CTA's last tile (see below)
+            if (npend == 0) { pend_s0 = s; pend_f0 = c_first; pend_l0 = c_last; }
+            else { pend_s1 = s; pend_f1 = c_first; pend_l1 = c_last; }
+            ++npend;
           }
         }
         wk.next(prefix, S);
+      }
+      // Split row sets (at most the CTA's first and last): count this CTA's
+      // partials in; the CTA delivering a row set's last partial merges them
+      // all, lse = ln sum_i exp(lse_i), o = sum_i exp(lse_i - lse) o_i.  Done
+      // after the tile loop so the fence and the atomic never stall it.
+      if (!failed && npend > 0) {
+        __threadfence();
+        named_bar_sync(1, 128);
+        if (tid == 0) {
+          int flags = 0;
+          for (int k = 0; k < npend; ++k) {
+            const int32_t ps = k == 0 ? pend_s0 : pend_s1;
+            const int32_t nseg = (k == 0 ? pend_l0 - pend_f0 : pend_l1 - pend_f1) + 1;
+            const int prev = atomicAdd(&p.counters[ps], 1);
+            if (prev == nseg - 1) {
+              p.counters[ps] = 0;        // ready for the next launch
+              flags |= 1 << k;
+            }
+          }
+          ctrl->merge_flag = flags;
+        }
+        named_bar_sync(1, 128);
+        const int flags = ctrl->merge_flag;
+        if (flags) __threadfence();
+        for (int k = 0; k < npend; ++k) {
+          if (!((flags >> k) & 1)) continue;
+          const int32_t ps = k == 0 ? pend_s0 : pend_s1;
+          const int32_t pf = k == 0 ? pend_f0 : pend_f1;
+          const int32_t pl = k == 0 ? pend_l0 : pend_l1;
+          merge_partials(p, ps, pf, pl - pf + 1, H, tid, ctrl->l_final,
+                         reinterpret_cast<float*>(sP), 2 * NP * 128 / 4);
+        }
       }
       if (failed && lane == 0) {
         set_status(p.status, MLA_STATUS_TIMEOUT);
@@ -768,6 +836,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
+
 
   // Row sets with no visible token (no tile anywhere): o_lat = 0, lse = -inf.
   for (int s = c; s < S; s += p.num_ctas) {
