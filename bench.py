@@ -226,9 +226,6 @@ def run_reference(args, world, rank):
         return 0
     w = W.WORKLOADS[args.workload]
     batch = W.generate(w)
-    if w.kv_dtype == "fp8":
-        from oracle import fp8 as F
-        batch.extra["cache_fp8"] = F.quantize_pages(batch.latent_f32, batch.slot_valid, w.seed)
     # calibrate: tokens per step so the whole run stays within ~2 minutes
     b_cal, t_cal, _ = oracle_sample(batch, 0, max_tokens=256)
     rate = b_cal / max(t_cal, 1e-9) / w.cache_row_bytes        # tokens per second
@@ -277,11 +274,12 @@ def run_gpu(args, world, rank, local):
     graft.build()
     w = W.WORKLOADS[args.workload]
     batch = W.generate(w)
-    if w.kv_dtype == "fp8":
-        raise SystemExit("the FP8 workload is not built yet")
+    fp8 = w.kv_dtype == "fp8"
     step = DecodeStep(q_nope=batch.q_nope, q_rope=batch.q_rope, w_uk=batch.w_uk, w_uv=batch.w_uv,
-                      cache=batch.cache_bf16, block_table=batch.block_table,
-                      seq_lens=batch.seq_lens, page_size=w.page_size, kv_dtype=MLA_KV_BF16,
+                      cache=batch.cache_fp8 if fp8 else batch.cache_bf16,
+                      block_table=batch.block_table, seq_lens=batch.seq_lens,
+                      page_size=w.page_size,
+                      kv_dtype=MLA_KV_FP8_E4M3_E8M0 if fp8 else MLA_KV_BF16,
                       topk_idx=batch.topk_idx, causal=w.causal, sm_scale=w.sm_scale,
                       device=device)
     stream = torch.cuda.current_stream(device)
@@ -369,7 +367,9 @@ def run_gpu(args, world, rank, local):
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8-e4m3+e8m0 cache, bf16 tensor-core math" if fp8 else "bf16",
+        "data": "synthetic",
         "config": workload_description(w, batch),
         "tokens_per_s_per_layer": w.batch * w.q_len * world / (max_s / args.steps),
         "hbm_fraction_of_measured": value / hbm,
@@ -377,7 +377,8 @@ def run_gpu(args, world, rank, local):
                       "uv_after_decode": statistics.mean(step_ms) - decode_ms},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": traffic,
-                     "kernel": "mla_decode_kernel<dense bf16>",
+                     "kernel": "mla_decode_kernel<%s>" % ("dense fp8" if fp8 else
+                                                          ("sparse bf16" if w.topk else "dense bf16")),
                      "peak_source": peak_src,
                      "algorithmic_bytes_per_launch": int(byts)},
         "e2e": e2e,
@@ -403,7 +404,7 @@ def main():
     ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="dense",
-                    choices=["tiny", "dense", "long", "sparse"])
+                    choices=["tiny", "dense", "long", "fp8", "sparse"])
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-budget", type=float, default=10.0)

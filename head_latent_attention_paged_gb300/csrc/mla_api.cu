@@ -69,7 +69,7 @@ int validate_problem(const mla_problem* pr) {
   if (pr->num_heads > kMaxHeads) return MLA_ERR_UNSUPPORTED;
   if (pr->topk_width % 128 != 0) return MLA_ERR_UNSUPPORTED;
   if (pr->kv_dtype != MLA_KV_BF16 && pr->kv_dtype != MLA_KV_FP8_E4M3_E8M0) return MLA_ERR_UNSUPPORTED;
-  if (pr->kv_dtype == MLA_KV_FP8_E4M3_E8M0) return MLA_ERR_UNSUPPORTED;   // FP8 kernel not built
+  if (pr->kv_dtype == MLA_KV_FP8_E4M3_E8M0 && pr->topk_width > 0) return MLA_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(pr->batch) * pr->q_len > kMaxStreams) return MLA_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(pr->num_pages) * pr->page_size > INT32_MAX) return MLA_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(pr->max_pages_per_seq) * pr->page_size > INT32_MAX) return MLA_ERR_UNSUPPORTED;
@@ -185,7 +185,9 @@ int mla_decode_run(const mla_plan* plan, const void* q_hat, const void* kv_cache
   if (plan->num_streams == 0) return MLA_OK;
   const int mode = decode_mode(pr);
   CUtensorMap kv_map;
-  if (!make_map_bf16(&kv_map, kv_cache, kDqk, static_cast<uint64_t>(pr.num_pages) * pr.page_size,
+  std::memset(&kv_map, 0, sizeof(kv_map));   // FP8 caches are read with bulk copies
+  if (mode != kModeDenseFp8 &&
+      !make_map_bf16(&kv_map, kv_cache, kDqk, static_cast<uint64_t>(pr.num_pages) * pr.page_size,
                      kDqk * 2, kChunkElems, kTile))
     return MLA_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);

@@ -7,7 +7,12 @@
 //                   memory once -- TMA tiles for dense pages, 16-byte
 //                   cp.async gathers for sparse top-k rows -- as nine
 //                   [64 rows x 128 B] chunks in the 128-byte swizzle layout,
-//                   three tiles in flight.
+//                   three tiles in flight.  FP8 caches: one bulk copy of the
+//                   tile's 594-byte rows, two tiles in flight, and
+//   dequant warps : (FP8 only) turn each row's 576 e4m3 codes and 18 e8m0
+//                   scales into bf16 values e4m3 * 2^(scale - 127), exactly,
+//                   written into the same swizzled bf16 tile layout (two
+//                   tiles in flight); rows with no live token become zeros.
 //   MMA warp      : S[h, t]   = q_hat[h, :576] . row[t, :576]      (tcgen05,
 //                   M = 64 head rows with q_hat read from TMEM, N = 64
 //                   tokens from shared memory, K = 576, f32 in TMEM);
@@ -27,6 +32,7 @@
 // sets MLA_STATUS_TIMEOUT and the CTA unwinds after draining its own copies
 // and MMAs, then releases its tensor memory.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -41,7 +47,16 @@ namespace {
 constexpr int kSoftmaxWarps = 4;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
-constexpr int kThreads = 192;
+constexpr int kDequantWarp0 = 6;    // FP8 mode: warps 6..9 dequantise
+constexpr int kDequantWarps = 4;
+
+template <int kMode>
+struct ModeTraits {
+  static constexpr bool kFp8 = kMode == kModeDenseFp8;
+  static constexpr int kThreads = kFp8 ? 32 * (kDequantWarp0 + kDequantWarps) : 192;
+  static constexpr int kNumStages = kFp8 ? kFp8Stages : kStages;   // bf16 tiles
+  static constexpr int kPBufs = kFp8 ? 1 : 2;                       // P buffers
+};
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s per wait
 constexpr float kRescaleThreshold = 8.0f;           // log2 units: rescale if max grows > 2^8
 constexpr float kLn2 = 0.6931471805599453f;
@@ -65,6 +80,9 @@ struct __align__(8) Ctrl {
   uint64_t o_free;           // softmax -> MMA: epilogue has read O^T
   uint64_t mma_drain;        // MMA warp's final commit
   uint64_t mask[kStages];    // per-stage live-row mask (bit t = row t live)
+  uint64_t raw_full[kRawStages];    // FP8: producer -> dequant, bytes landed
+  uint64_t raw_empty[kRawStages];   // FP8: dequant -> producer, bytes consumed
+  uint64_t raw_mask[kRawStages];    // FP8: live-row mask of the raw tile
   uint32_t tmem_base;
   int32_t abort_flag;
   int32_t rescale_tile[2];
@@ -188,6 +206,69 @@ __device__ __forceinline__ void prefetch_q(const uint16_t* q_hat, int32_t s, int
     asm volatile("prefetch.global.L2 [%0];" ::"l"(base + static_cast<int64_t>(i) * 128));
 }
 
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t lds_u8(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u8 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+
+// Two e4m3 codes (low byte = lower address) -> two f16 (exact: every e4m3
+// value, subnormals included, is a normal f16).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+  uint32_t h;
+  asm("{\n .reg .b16 c;\n cvt.u16.u32 c, %1;\n cvt.rn.f16x2.e4m3x2 %0, c;\n}"
+      : "=r"(h) : "r"(two_codes));
+  return h;
+}
+
+// 2^(b - 127) as a float for an e8m0 byte b (b = 0 gives the subnormal
+// 2^-127, b = 255 is NaN).
+__device__ __forceinline__ float e8m0_to_f32(uint32_t b) {
+  const uint32_t bits = b == 0 ? 0x00400000u : (b == 255 ? 0x7FC00000u : (b << 23));
+  return __uint_as_float(bits);
+}
+
+// Two f16 (packed) times a power of two -> two bf16 (packed).  The product
+// is exact in f32 and has at most 4 significant bits, so the bf16 rounding
+// is exact too (barring under/overflow of the bf16 range).
+__device__ __forceinline__ uint32_t f16x2_scaled_to_bf16x2(uint32_t h2, float scale) {
+  const __half2 hv = *reinterpret_cast<const __half2*>(&h2);
+  const float2 f = __half22float2(hv);
+  return pack_bf16x2(f.x * scale, f.y * scale);
+}
+
+// Dequantise group g (values 32g .. 32g+31) of one FP8 row in shared memory
+// (row_addr: 2-byte aligned start of the row's 594 bytes) into 4 x 16 bytes
+// of bf16 (8 values each, in dimension order).
+__device__ __forceinline__ void dequant_group(uint32_t row_addr, int g, uint4 (&o)[4]) {
+  const uint32_t a = row_addr + 32u * g;
+  const uint32_t a4 = a & ~3u;
+  const bool odd = (a & 2u) != 0;
+  uint32_t w[9];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) w[k] = lds_u32(a4 + 4u * k);
+  w[8] = odd ? lds_u32(a4 + 32u) : 0u;
+  const float scale = e8m0_to_f32(lds_u8(row_addr + kDqk + g));
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t r[4];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int wi = 2 * q + k;
+      const uint32_t v = odd ? __funnelshift_r(w[wi], w[wi + 1], 16) : w[wi];
+      r[2 * k] = f16x2_scaled_to_bf16x2(e4m3x2_to_f16x2(v & 0xFFFFu), scale);
+      r[2 * k + 1] = f16x2_scaled_to_bf16x2(e4m3x2_to_f16x2(v >> 16), scale);
+    }
+    o[q] = make_uint4(r[0], r[1], r[2], r[3]);
+  }
+}
+
 // Merge the nseg partials (slots s + c_first ...) of row set s into o_lat and
 // lse: lse = ln sum_i exp(lse_i), o = sum_i exp(lse_i - lse) o_i.  Run by the
 // 128 softmax threads after the tile loop; thread t owns latent dims
@@ -278,24 +359,31 @@ __device__ __forceinline__ void merge_partials(const DecodeParams& p, int32_t s,
 }  // namespace
 
 DecodeLayout decode_layout(int heads, int heads_pad, int num_streams, int mode) {
-  (void)mode;
   (void)heads;
+  const bool fp8 = mode == kModeDenseFp8;
   DecodeLayout L;
   L.off_stage = 0;
-  L.off_p = kStages * kTileBytes;
-  L.off_ctrl = L.off_p + 2 * heads_pad * 128;
+  L.off_raw = (fp8 ? kFp8Stages : kStages) * kTileBytes;
+  const int raw_end = L.off_raw + (fp8 ? kRawStages * kFp8TileBytes : 0);
+  L.off_p = (raw_end + 1023) / 1024 * 1024;   // 128-byte swizzle atoms: 1 KB aligned
+  L.off_ctrl = L.off_p + (fp8 ? 1 : 2) * heads_pad * 128;
   L.total = L.off_ctrl + static_cast<int>(sizeof(Ctrl)) + (num_streams + 1) * 4;
   return L;
 }
 
 template <int kMode>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p,
                       const DecodeLayout L) {
+  using MT = ModeTraits<kMode>;
+  constexpr int kThreads = MT::kThreads;
+  constexpr int kNumStages = MT::kNumStages;
+  constexpr int kPBufs = MT::kPBufs;
   // The buffers need 1024-byte alignment (128-byte swizzle atoms); the
   // dynamic shared window starts aligned, which is checked below.
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* sStage = smem + L.off_stage;
+  uint8_t* sRaw = smem + L.off_raw;
   uint8_t* sP = smem + L.off_p;
   Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + L.off_ctrl);
   int32_t* prefix = reinterpret_cast<int32_t*>(smem + L.off_ctrl + sizeof(Ctrl));
@@ -319,9 +407,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   // as SMs free up; it waits for this grid's completion before reading.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0) {
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(&ctrl->full[i], kMode == kModeSparseBf16 ? 33 : 1);
+    for (int i = 0; i < kNumStages; ++i) {
+      mbar_init(&ctrl->full[i], kMode == kModeSparseBf16 ? 33 : (MT::kFp8 ? kDequantWarps : 1));
       mbar_init(&ctrl->empty[i], 1);
+    }
+    for (int i = 0; i < kRawStages; ++i) {
+      mbar_init(&ctrl->raw_full[i], 1);
+      mbar_init(&ctrl->raw_empty[i], kDequantWarps);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctrl->p_full[i], kSoftmaxWarps);
@@ -348,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefix[s + 1] = (len + kTile - 1) / kTile;
   }
   // P buffers start at zero: rows of padded heads are never written again
-  for (int i = tid; i < 2 * NP * 128 / 16; i += kThreads)
+  for (int i = tid; i < kPBufs * NP * 128 / 16; i += kThreads)
     reinterpret_cast<uint4*>(sP)[i] = make_uint4(0, 0, 0, 0);
   __syncthreads();
   if (warp == 0) {   // exclusive prefix sum of tiles over streams
@@ -387,8 +479,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int32_t issued = 0;
       bool failed = false;
       for (int32_t i = 0; i < ntiles; ++i) {
-        const int stage = i % kStages;
-        const uint32_t reuse_parity = ((i / kStages) - 1) & 1;
+        const int stage = i % kNumStages;
+        const uint32_t reuse_parity = ((i / kNumStages) - 1) & 1;
         const int b = wk.s / p.q_len, j = wk.s - b * p.q_len;
         uint8_t* dst = sStage + stage * kTileBytes;
         // Describe the tile first: its global lookups overlap the stage wait.
@@ -410,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             row0 = ok ? page * p.page_size + (tok0 % p.page_size) : 0;
           }
-          if (i >= kStages && !warp_wait(&ctrl->empty[stage], reuse_parity, abort_flag)) {
+          if (i >= kNumStages && !warp_wait(&ctrl->empty[stage], reuse_parity, abort_flag)) {
             failed = true;
             break;
           }
@@ -455,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (bad) set_status(p.status, bad);
           const uint32_t lo = __ballot_sync(0xffffffffu, valid[0]);
           const uint32_t hi = __ballot_sync(0xffffffffu, valid[1]);
-          if (i >= kStages && !warp_wait(&ctrl->empty[stage], reuse_parity, abort_flag)) {
+          if (i >= kNumStages && !warp_wait(&ctrl->empty[stage], reuse_parity, abort_flag)) {
             failed = true;
             break;
           }
@@ -476,6 +568,44 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) ctrl->mask[stage] = (static_cast<uint64_t>(hi) << 32) | lo;
           cp_async_mbar_arrive(&ctrl->full[stage]);
           if (lane == 0) mbar_arrive(&ctrl->full[stage]);
+        } else {   // kModeDenseFp8: the tile's FP8 rows, one bulk copy
+          const int rs = i % kRawStages;
+          uint64_t mask = 0;
+          bool ok = false;
+          const uint8_t* src = p.kv;
+          uint32_t bytes = 0;
+          if (lane == 0) {
+            const int32_t tok0 = wk.lt * kTile;
+            const int32_t len = stream_len(p.seq_lens[b], p.q_len, j, p.causal, 0, max_tokens);
+            const int32_t page =
+                p.block_table[static_cast<int64_t>(b) * p.max_pages + tok0 / p.page_size];
+            const int32_t nvalid = min(kTile, len - tok0);
+            mask = nvalid >= 64 ? ~0ull : ((1ull << nvalid) - 1ull);
+            ok = page >= 0 && page < p.num_pages;
+            if (!ok) {
+              mask = 0;
+              set_status(p.status, MLA_STATUS_BAD_PAGE);
+            }
+            // rows tok0 .. tok0 + 63 of a page are contiguous; copy the live
+            // ones rounded up to 8 rows (8 x 594 B is a multiple of 16 B)
+            src = p.kv + (static_cast<int64_t>(page) * p.page_size + tok0 % p.page_size) *
+                             kFp8RowBytes;
+            bytes = static_cast<uint32_t>((nvalid + 7) & ~7) * kFp8RowBytes;
+          }
+          if (i >= kRawStages &&
+              !warp_wait(&ctrl->raw_empty[rs], ((i / kRawStages) - 1) & 1, abort_flag)) {
+            failed = true;
+            break;
+          }
+          if (lane == 0) {
+            ctrl->raw_mask[rs] = mask;
+            if (ok) {
+              mbar_arrive_expect_tx(&ctrl->raw_full[rs], bytes);
+              bulk_load(sRaw + rs * kFp8TileBytes, src, bytes, &ctrl->raw_full[rs], pol);
+            } else {
+              mbar_arrive(&ctrl->raw_full[rs]);
+            }
+          }
         }
         __syncwarp();
         ++issued;
@@ -488,8 +618,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       // drain: everything this warp issued has landed before the CTA exits
       if constexpr (kMode == kModeSparseBf16) asm volatile("cp.async.wait_all;" ::: "memory");
       if (lane == 0) {
-        for (int32_t i = max(0, issued - kStages); i < issued; ++i)
-          (void)mbar_wait(&ctrl->full[i % kStages], (i / kStages) & 1, nullptr, kWaitLimitNs);
+        if constexpr (MT::kFp8) {
+          for (int32_t i = max(0, issued - kRawStages); i < issued; ++i)
+            (void)mbar_wait(&ctrl->raw_full[i % kRawStages], (i / kRawStages) & 1, nullptr,
+                            kWaitLimitNs);
+        } else {
+          for (int32_t i = max(0, issued - kNumStages); i < issued; ++i)
+            (void)mbar_wait(&ctrl->full[i % kNumStages], (i / kNumStages) & 1, nullptr,
+                            kWaitLimitNs);
+        }
       }
       __syncwarp();
     } else if (warp == kMmaWarp) {
@@ -517,7 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         while (pv < ntiles) {
           bool progressed = false;
           if (pv < qk) {
-            const int st = pv % kStages;
+            const int st = pv % kNumStages;
             const bool first = (pv == 0) || (wp.lt == 0);
             const int32_t sp = first ? seg_p + 1 : seg_p;
             const bool ready = mbar_poll(&ctrl->p_full[pv & 1], (pv >> 1) & 1) &&
@@ -526,7 +663,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               seg_p = sp;
               tc_fence_after();
               const uint64_t a0 = pv_a0 + static_cast<uint64_t>((st * kTileBytes) >> 4);
-              const uint64_t b0 = pv_b0 + static_cast<uint64_t>(((pv & 1) * NP * 128) >> 4);
+              const uint64_t b0 =
+                  pv_b0 + static_cast<uint64_t>((((kPBufs == 2) ? (pv & 1) : 0) * NP * 128) >> 4);
 #pragma unroll
               for (int mt = 0; mt < 4; ++mt) {
 #pragma unroll
@@ -542,11 +680,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (qk < ntiles && qk - pv < 2) {
-            const int st = qk % kStages;
+            const int st = qk % kNumStages;
             const bool first = (qk == 0) || (wq.lt == 0);
             const int32_t sq = first ? seg_q + 1 : seg_q;
             const bool ready = (!first || mbar_poll(&ctrl->q_ready, sq & 1)) &&
-                               mbar_poll(&ctrl->full[st], (qk / kStages) & 1) &&
+                               mbar_poll(&ctrl->full[st], (qk / kNumStages) & 1) &&
                                (qk < 1 || mbar_poll(&ctrl->s_free, (qk - 1) & 1));
             if (ready) {
               seg_q = sq;
@@ -589,6 +727,57 @@ __global__ void __launch_bounds__(kThreads, 1)
         (void)mbar_wait(&ctrl->mma_drain, 0, nullptr, kWaitLimitNs);
       }
       __syncwarp();
+    } else if (MT::kFp8 && warp >= kDequantWarp0) {
+      // ============================================================ dequant
+      // Thread t of the 128 owns row t % 64 and the groups of one parity
+      // (t / 64): a warp covers 32 consecutive rows, so its shared loads
+      // (row stride 594 B) and its swizzled 16-byte stores spread over the
+      // banks.
+      const int dt = tid - kDequantWarp0 * 32;
+      const int r = dt & 63;
+      const int gpar = dt >> 6;
+      bool failed = false;
+      for (int32_t i = 0; i < ntiles; ++i) {
+        const int rs = i % kRawStages;
+        const int bs = i % kNumStages;
+        if (!warp_wait(&ctrl->raw_full[rs], (i / kRawStages) & 1, abort_flag) ||
+            (i >= kNumStages &&
+             !warp_wait(&ctrl->empty[bs], ((i / kNumStages) - 1) & 1, abort_flag))) {
+          failed = true;
+          break;
+        }
+        const uint64_t mask = ctrl->raw_mask[rs];
+        const bool live = (mask >> r) & 1ull;
+        const uint32_t row_addr = smem_u32(sRaw + rs * kFp8TileBytes + r * kFp8RowBytes);
+        uint8_t* dst = sStage + bs * kTileBytes + r * 128;
+#pragma unroll 1
+        for (int k = 0; k < kDqk / 64; ++k) {
+          const int g = gpar + 2 * k;
+          uint4 o[4];
+          if (live) {
+            dequant_group(row_addr, g, o);
+          } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) o[q] = make_uint4(0, 0, 0, 0);
+          }
+          const int u0 = (g & 1) * 4;
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(dst + (g >> 1) * kChunkBytes + (((u0 + q) ^ (r & 7)) << 4)) =
+                o[q];
+        }
+        if (dt == 0) ctrl->mask[bs] = mask;
+        fence_proxy_async_smem();   // generic stores -> tensor-core reads
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&ctrl->raw_empty[rs]);
+          mbar_arrive(&ctrl->full[bs]);
+        }
+      }
+      if (failed && lane == 0) {
+        set_status(p.status, MLA_STATUS_TIMEOUT);
+        ctrl->abort_flag = 1;
+      }
     } else {
       // ============================================================ softmax
       // Warp w reads TMEM lanes [32w, 32w+32).  Head h is S row 32 + h: in
@@ -606,7 +795,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool owner = warp_has_heads && h < H;
       const uint32_t lane_base = static_cast<uint32_t>(w * 32) << 16;
       const float scale = p.scale_log2;
-      float m_used = -INFINITY, l_run = 0.f;
+      // l_run sums the bf16-rounded P the PV uses (it normalises O); l_exp
+      // sums the unrounded exponentials (it gives lse).
+      float m_used = -INFINITY, l_run = 0.f, l_exp = 0.f;
       Walker wk;
       wk.init(prefix, S, g0);
       bool failed = false;
@@ -618,7 +809,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctrl->q_ready);
       for (int32_t i = 0; i < ntiles; ++i) {
-        const int stage = i % kStages;
+        const int stage = i % kNumStages;
         const int pb = i & 1;
         const bool first = (i == 0) || (wk.lt == 0);
         const bool last = (i == ntiles - 1) || (wk.lt == wk.ntiles - 1);
@@ -629,7 +820,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           while (sn < S && prefix[sn + 1] == prefix[sn]) ++sn;
           if (sn < S && prefix[sn] < g1) prefetch_q(p.q_hat, sn, H, tid, 64);
         }
-        bool ok = !failed && warp_wait(&ctrl->full[stage], (i / kStages) & 1, abort_flag);
+        bool ok = !failed && warp_wait(&ctrl->full[stage], (i / kNumStages) & 1, abort_flag);
         const uint64_t mask = ctrl->mask[stage];
         ok = ok && warp_wait(&ctrl->s_full, i & 1, abort_flag);
         if (ok) {
@@ -661,7 +852,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctrl->q_ready);
           }
-          if (warp_has_heads) {
+          // One P buffer: PV(i-1) must have read it.  PV(i) cannot be issued
+          // before P(i) is written, so this parity wait cannot run ahead.
+          if constexpr (kPBufs == 1) {
+            if (i >= 1) ok = warp_wait(&ctrl->o_done, (i - 1) & 1, abort_flag);
+          }
+          if (ok && warp_has_heads) {
             // token of y[t] is 32*half + t
             const uint32_t hmask = static_cast<uint32_t>(mask >> (32 * half));
             float mt = -INFINITY;
@@ -680,15 +876,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (first) {
               m_used = mt;
               l_run = 0.f;
+              l_exp = 0.f;
             } else if (mt > m_used + kRescaleThreshold) {
               alpha = fast_exp2(m_used - mt);
               m_used = mt;
               l_run *= alpha;
+              l_exp *= alpha;
               if (owner && half == 0) ctrl->rescale_tile[pb] = i;
             }
             const float nref = (m_used == -INFINITY) ? 0.f : -m_used;
-            uint8_t* prow = sP + pb * NP * 128 + h * 128;
-            float lsum = 0.f;
+            uint8_t* prow = sP + ((kPBufs == 2) ? pb : 0) * NP * 128 + h * 128;
+            float lsum = 0.f, lsum_exp = 0.f;
 #pragma unroll
             for (int c8 = 0; c8 < 4; ++c8) {
               uint32_t u[4];
@@ -699,6 +897,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 u[e] = pack_bf16x2(a, b);
                 const __nv_bfloat162 v2 = *reinterpret_cast<__nv_bfloat162*>(&u[e]);
                 lsum += __low2float(v2) + __high2float(v2);
+                lsum_exp += a + b;
               }
               if (owner) {
                 const int chunk = 4 * half + c8;
@@ -707,11 +906,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
             l_run += lsum + __shfl_xor_sync(0xffffffffu, lsum, 16);
+            l_exp += lsum_exp + __shfl_xor_sync(0xffffffffu, lsum_exp, 16);
             if (owner && half == 0) ctrl->alpha[pb][h] = alpha;
           }
-          if constexpr (kMode != kModeSparseBf16) {
+          if constexpr (kMode == kModeDenseBf16) {
             // Dead rows (tail slots, bad pages): P is 0 there but 0 * NaN
-            // would poison the PV sum, so zero their latent values.
+            // would poison the PV sum, so zero their latent values.  (The
+            // sparse producer zero-fills them; the FP8 dequant writes zeros.)
             if (mask != ~0ull) {
               uint8_t* tile = sStage + stage * kTileBytes;
               for (int u = tid; u < kTile * 64; u += 128) {
@@ -748,18 +949,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+        // A segment ends here: its epilogue waits for PV(i), one phase after
+        // PV(i-1).  A parity wait must never run more than one phase ahead of
+        // the barrier, so PV(i-1) is awaited first, while PV(i) cannot have
+        // been issued yet (P(i) is not announced).  PV(i-2) is complete: the
+        // commit that signalled S(i) covers it.
+        if (last && i >= 1 && !failed) {
+          ok = warp_wait(&ctrl->o_done, (i - 1) & 1, abort_flag);
+          if (!ok) failed = true;
+        }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctrl->p_full[pb]);
         if (last) {
-          // ---- segment epilogue.  PV(i-1) may still be in flight (QK(i)
-          // is usually issued before it), so wait for its phase first: a
-          // parity wait must never be more than one phase ahead of the
-          // barrier.  PV(i-2) is complete: the commit that signalled S(i)
-          // covers it.
-          if (i >= 1) ok = ok && warp_wait(&ctrl->o_done, (i - 1) & 1, abort_flag);
-          ok = ok && warp_wait(&ctrl->o_done, i & 1, abort_flag);
+          // ---- segment epilogue
+          ok = !failed && warp_wait(&ctrl->o_done, i & 1, abort_flag);
           const int32_t s = wk.s;
           const int32_t c_first = tile_owner(prefix[s], total, p.num_ctas);
           const int32_t c_last = tile_owner(prefix[s + 1] - 1, total, p.num_ctas);
@@ -771,7 +976,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  : p.lse + static_cast<int64_t>(s) * H;
           if (ok && owner && half == 0) {
             ctrl->l_final[h] = l_run > 0.f ? 1.f / l_run : 0.f;   // o = O / l
-            dst_lse[h] = l_run > 0.f ? (m_used + __log2f(l_run)) * kLn2 : -INFINITY;
+            dst_lse[h] = l_run > 0.f ? (m_used + __log2f(l_exp)) * kLn2 : -INFINITY;
           }
           if (named_bar_or(1, 128, !ok || failed)) { failed = true; break; }
           tc_fence_after();
@@ -827,7 +1032,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int32_t pf = k == 0 ? pend_f0 : pend_f1;
           const int32_t pl = k == 0 ? pend_l0 : pend_l1;
           merge_partials(p, ps, pf, pl - pf + 1, H, tid, ctrl->l_final,
-                         reinterpret_cast<float*>(sP), 2 * NP * 128 / 4);
+                         reinterpret_cast<float*>(sP), kPBufs * NP * 128 / 4);
         }
       }
       if (failed && lane == 0) {
@@ -857,7 +1062,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap* kv_map, int mode,
                           cudaStream_t stream) {
   const DecodeLayout L = decode_layout(p.heads, p.heads_pad, p.num_streams, mode);
-  dim3 grid(p.num_ctas), block(kThreads);
+  dim3 grid(p.num_ctas), block(ModeTraits<kModeDenseBf16>::kThreads);
   cudaError_t err;
   switch (mode) {
     case kModeDenseBf16:
@@ -871,6 +1076,13 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap* kv_map, int 
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
       if (err != cudaSuccess) return err;
       mla_decode_kernel<kModeSparseBf16><<<grid, block, L.total, stream>>>(*kv_map, p, L);
+      break;
+    case kModeDenseFp8:
+      err = cudaFuncSetAttribute(mla_decode_kernel<kModeDenseFp8>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
+      if (err != cudaSuccess) return err;
+      block = dim3(ModeTraits<kModeDenseFp8>::kThreads);
+      mla_decode_kernel<kModeDenseFp8><<<grid, block, L.total, stream>>>(*kv_map, p, L);
       break;
     default:
       return cudaErrorInvalidValue;

@@ -22,7 +22,10 @@ constexpr int kTileBytes = kChunks * kChunkBytes;  // 73,728
 constexpr int kFp8RowBytes = kDqk + kDqk / 32;     // 594
 constexpr int kMaxHeads = 32;     // TMEM: q_hat 288 + S 64 + O^T 4 x 32 columns
 constexpr int kMaxStreams = 256;  // per-stream tile prefix kept in shared memory
-constexpr int kStages = 3;        // 72 KB tiles in flight per CTA
+constexpr int kStages = 3;        // 72 KB tiles in flight per CTA (bf16 caches)
+constexpr int kFp8TileBytes = kTile * kFp8RowBytes;  // 38,016: one tile of FP8 rows
+constexpr int kFp8Stages = 2;     // dequantised bf16 tiles in flight (FP8 caches)
+constexpr int kRawStages = 2;     // FP8 byte tiles in flight (FP8 caches)
 
 enum DecodeMode : int { kModeDenseBf16 = 0, kModeSparseBf16 = 1, kModeDenseFp8 = 2 };
 
@@ -45,7 +48,7 @@ struct DecodeParams {
 };
 
 struct DecodeLayout {   // dynamic shared memory layout of the decode kernel
-  int32_t off_stage, off_p, off_ctrl, total;
+  int32_t off_stage, off_raw, off_p, off_ctrl, total;
 };
 
 DecodeLayout decode_layout(int heads, int heads_pad, int num_streams, int mode);

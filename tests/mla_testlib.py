@@ -97,7 +97,8 @@ def compare(ref: dict, o, o_lat, lse, heads=None, label="", lse_ref=None):
 
 
 def with_fp8(batch: W.Batch, garbage="finite") -> W.Batch:
-    """Attach the paged FP8 bytes (oracle quantiser) to an FP8 workload."""
+    """FP8 workloads drawn with fp8_source="float": attach the paged FP8
+    bytes made by the oracle's quantiser (codes-drawn batches have them)."""
     if batch.workload.kv_dtype == "fp8" and "cache_fp8" not in batch.extra:
         batch.extra["cache_fp8"] = F.quantize_pages(batch.latent_f32, batch.slot_valid,
                                                     rng_seed=batch.workload.seed, garbage=garbage)

@@ -76,11 +76,24 @@ def test_plan_ok_and_workspace_layout(m):
     (dict(rope_dim=32), -2), (dict(v_head_dim=128), -2), (dict(nope_dim=128), -2),
     (dict(causal=2), -1), (dict(sm_scale=0.0), -1), (dict(sm_scale=float("nan")), -1),
     (dict(num_pages=0), -1), (dict(max_pages_per_seq=0), -1), (dict(batch=257), -2), (dict(batch=65, q_len=4), -2),
+    (dict(kv_dtype=1, topk_width=128), -2), (dict(kv_dtype=2), -2),
 ])
 def test_plan_rejects(m, kw, code):
     with pytest.raises(m.MlaError) as e:
         m.mla_decode_plan(_problem(m, **kw), None, 152)
     assert e.value.code == code
+
+
+def test_fp8_plan_fits_shared_memory(m):
+    """FP8 caches plan like bf16 ones; the FP8 kernel's staging (two bf16
+    tiles, two FP8 byte tiles, one P buffer) fits the 227 KB window at the
+    largest head and row-set counts."""
+    seq = np.array([100, 1000, 64, 0], dtype=np.int32)
+    plan = m.mla_decode_plan(_problem(m, kv_dtype=m.MLA_KV_FP8_E4M3_E8M0), seq, 152)
+    assert plan.planned_tiles == sum((int(t) + 63) // 64 for t in seq)
+    big = m.mla_decode_plan(_problem(m, kv_dtype=m.MLA_KV_FP8_E4M3_E8M0, batch=256, num_heads=32),
+                            None, 152)
+    assert 2 * 73728 + 2 * 64 * 594 + 32 * 128 < big.smem_bytes <= 232448
 
 
 def test_plan_rejects_negative_seq_len_and_bad_sm_count(m):

@@ -389,7 +389,7 @@ def test_fp8_decode_uses_dequantised_bytes():
     stored bytes: equal to the bf16-free float path on the dequantised rows."""
     w = W.with_overrides(W.SMALL_WORKLOADS["fp8_small"], batch=2, heads=2, seq_lo=70,
                          seq_hi=140)
-    b = W.generate(w)
+    b = W.generate(w, fp8_source="float")
     b.extra["cache_fp8"] = F.quantize_pages(b.latent_f32, b.slot_valid)
     got = O.decode(b)
     raw = b.extra["cache_fp8"].reshape(b.num_pages, w.page_size, F.ROW_BYTES)

@@ -13,6 +13,16 @@ into a 192-dim no-RoPE part and a 64-dim RoPE part; the value head is 256.
 
 bf16 tensors are returned as uint16 bit patterns (numpy has no bfloat16).
 
+FP8 caches (576 e4m3 codes then 18 e8m0 scale bytes per cached row) are drawn
+directly as bytes: the decode's input is the byte layout, so no quantiser is
+involved.  Live rows: ~99% of codes have a random sign, an exponent field
+distributed as round(N(10, 0.75)) clipped to [0, 12] and a uniform 3-bit
+mantissa, the other ~1% are uniform over the codes with exponent field <= 8
+(zeros and subnormals included); scale bytes are uniform in [121, 124]
+(2**-6 .. 2**-3), so live values have magnitudes around 0.5 and at most 7.5,
+like the N(0, 1) bf16 cache.  ``fp8_source="float"`` instead returns a float32 latent for the
+oracle's quantiser (small cases only).
+
 Draw order for one workload (one ``numpy.random.default_rng(seed)``):
 seq_lens -> block table -> cache -> q_nope -> q_rope -> W_UK -> W_UV ->
 sparse indices.
@@ -165,13 +175,18 @@ class Batch:
     num_pages: int
     slot_valid: np.ndarray      # bool [num_pages, P]: holds a live token
     cache_bf16: Optional[np.ndarray]  # uint16 [num_pages, P, 576] (bf16 workloads)
-    latent_f32: Optional[np.ndarray]  # float32 [num_pages, P, 576] (fp8 workloads, pre-quantisation)
+    latent_f32: Optional[np.ndarray]  # float32 [num_pages, P, 576] (fp8_source="float" only)
     q_nope: np.ndarray          # uint16 bf16 [B, Q, H, 192]
     q_rope: np.ndarray          # uint16 bf16 [B, Q, H, 64]
     w_uk: np.ndarray            # uint16 bf16 [H, 512, 192]
     w_uv: np.ndarray            # uint16 bf16 [H, 512, 256]
     topk_idx: Optional[np.ndarray]  # int32 [B*Q, width]; -1 = masked slot
     extra: dict = field(default_factory=dict)
+
+    @property
+    def cache_fp8(self) -> Optional[np.ndarray]:
+        """uint8 [num_pages, P * 594] FP8 cache bytes, if drawn."""
+        return self.extra.get("cache_fp8")
 
     @property
     def latent_bytes_read(self) -> int:
@@ -184,10 +199,55 @@ class Batch:
         return int(self.seq_lens.astype(np.int64).sum()) * w.cache_row_bytes
 
 
-def generate(w: Workload, garbage: str = "finite") -> Batch:
+def _exponent_table() -> np.ndarray:
+    """256-entry table: a uniform random byte -> an e4m3 exponent field with
+    the probabilities of round(N(10, 0.75)) clipped to [0, 12]."""
+    from math import erf, sqrt
+    cdf = [0.5 * (1.0 + erf((e + 0.5 - 10.0) / (0.75 * sqrt(2.0)))) for e in range(12)] + [1.0]
+    edges = np.rint(np.asarray(cdf) * 256).astype(np.int64)
+    return np.searchsorted(edges, np.arange(256), side="right").clip(0, 12).astype(np.uint8)
+
+
+_EXP_TABLE = _exponent_table()
+
+
+def _fp8_rows(rng: np.random.Generator, n: int, chunk: int = 1 << 16) -> np.ndarray:
+    """n live FP8 rows (uint8 [n, 594]) drawn as codes, as described above.
+    One random 32-bit word per code: bits 0-7 pick the exponent field, 8-10
+    the mantissa, 11 the sign; bits 12-19 below 3 (~1.2%) replace the code
+    by the small code in bits 20-26 (taken modulo 0x48)."""
+    out = np.empty((n, FP8_ROW_BYTES), dtype=np.uint8)
+    for s in range(0, n, chunk):
+        e = min(n, s + chunk)
+        m = e - s
+        r = rng.integers(0, 1 << 32, size=(m, D_QK), dtype=np.uint32)
+        exp = _EXP_TABLE[(r & 0xFF).astype(np.uint8)]
+        man = ((r >> 8) & 7).astype(np.uint8)
+        codes = (exp << 3) | man
+        wild = ((r >> 12) & 0xFF) < 3
+        small = (((r >> 20) & 0x7F) % 0x48).astype(np.uint8)
+        codes = np.where(wild, small, codes)
+        codes |= (((r >> 11) & 1).astype(np.uint8) << 7)
+        out[s:e, :D_QK] = codes
+        out[s:e, D_QK:] = rng.integers(121, 125, size=(m, D_QK // FP8_GROUP), dtype=np.uint8)
+    return out
+
+
+def _fp8_garbage(rng: np.random.Generator, n: int, garbage: str) -> np.ndarray:
+    if garbage == "nan":     # e4m3 NaN values, scale byte 0x7F
+        return np.full((n, FP8_ROW_BYTES), 0x7F, dtype=np.uint8)
+    out = rng.integers(0, 0x7F, size=(n, FP8_ROW_BYTES), dtype=np.uint8)
+    out[:, :D_QK] |= rng.integers(0, 2, size=(n, D_QK), dtype=np.uint8) << 7
+    out[:, D_QK:] = rng.integers(120, 135, size=(n, D_QK // FP8_GROUP), dtype=np.uint8)
+    return out
+
+
+def generate(w: Workload, garbage: str = "finite", fp8_source: str = "codes") -> Batch:
     """Draw one batch.  ``garbage`` fills slots that hold no live token (tail
     slots of a request's last page and spare pages): "finite" uses bf16 values
-    of magnitude up to 1e4, "nan" uses bf16 NaN."""
+    of magnitude up to 1e4 (FP8: random finite codes with scales up to 2**7),
+    "nan" uses NaN.  ``fp8_source`` ("codes" or "float") is described in the
+    module docstring."""
     rng = np.random.default_rng(w.seed)
     B, Q, H, P = w.batch, w.q_len, w.heads, w.page_size
     seq_lens = draw_seq_lens(w, rng)
@@ -207,13 +267,17 @@ def generate(w: Workload, garbage: str = "finite") -> Batch:
             live = min(P, int(seq_lens[b]) - j * P)
             slot_valid[block_table[b, j], :live] = True
 
-    cache_bf16 = latent_f32 = None
+    cache_bf16 = latent_f32 = cache_fp8 = None
     if w.kv_dtype == "bf16":
         cache_bf16 = _normal_bf16(rng, (num_pages, P, D_QK))
+    elif fp8_source == "codes":
+        cache_fp8 = _fp8_rows(rng, num_pages * P).reshape(num_pages, P, FP8_ROW_BYTES)
     else:
         latent_f32 = _normal_f32(rng, (num_pages, P, D_QK))
     inv = ~slot_valid
-    if inv.any():
+    if cache_fp8 is not None and inv.any():
+        cache_fp8[inv] = _fp8_garbage(rng, int(inv.sum()), garbage)
+    elif inv.any():
         n_inv = int(inv.sum())
         if garbage == "nan":
             fill_bits = np.full((n_inv, D_QK), BF16_NAN, dtype=np.uint16)
@@ -248,5 +312,8 @@ def generate(w: Workload, garbage: str = "finite") -> Batch:
                     row[:k] = picks
                 topk_idx[b * Q + j] = row
 
-    return Batch(w, seq_lens, block_table, num_pages, slot_valid, cache_bf16, latent_f32,
-                 q_nope, q_rope, w_uk, w_uv, topk_idx)
+    batch = Batch(w, seq_lens, block_table, num_pages, slot_valid, cache_bf16, latent_f32,
+                  q_nope, q_rope, w_uk, w_uv, topk_idx)
+    if cache_fp8 is not None:
+        batch.extra["cache_fp8"] = cache_fp8.reshape(num_pages, P * FP8_ROW_BYTES)
+    return batch
