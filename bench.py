@@ -2,9 +2,9 @@
 """Benchmark of one paged MLA decode step (one layer) on GB300.
 
 A step is the whole hot path over one synthetic decode batch: the attention
-pass over the paged latent cache with the LSE merge of split partials fused
-in, and the W_UV up-projection (the absorbed query is an input, precomputed
-once).  The
+pass over the paged latent cache, the LSE merge of split partials, and the
+W_UV up-projection (three kernels, each launched as a programmatic dependent
+of the one before; the absorbed query is an input, precomputed once).  The
 default workload is the GLM-4.7-Flash-shaped dense decode: batch 64, 20
 heads, q_len 1, seq_lens ~ U[1024, 8192], page 64, bf16 latent cache.
 

@@ -88,6 +88,26 @@ int64_t stream_tiles_host(const mla_problem& pr, const int32_t* seq_lens) {
   return total;
 }
 
+void fill_combine_params(const mla_plan& plan, const uint8_t* ws, const int32_t* seq_lens,
+                         float* o_lat, float* lse, CombineParams* out) {
+  const mla_problem& pr = plan.problem;
+  CombineParams& p = *out;
+  p.part_o = reinterpret_cast<const float*>(ws + plan.ws_partial_o);
+  p.part_lse = reinterpret_cast<const float*>(ws + plan.ws_partial_lse);
+  p.seq_lens = seq_lens;
+  p.o_lat = o_lat;
+  p.lse = lse;
+  p.batch = pr.batch;
+  p.q_len = pr.q_len;
+  p.heads = pr.num_heads;
+  p.page_size = pr.page_size;
+  p.max_pages = pr.max_pages_per_seq;
+  p.topk_width = pr.topk_width;
+  p.causal = pr.causal;
+  p.num_streams = plan.num_streams;
+  p.num_ctas = plan.num_ctas;
+}
+
 int plan_check(const mla_plan* plan) {
   if (plan == nullptr) return MLA_ERR_INVALID_ARGUMENT;
   const int rc = validate_problem(&plan->problem);
@@ -199,7 +219,6 @@ int mla_decode_run(const mla_plan* plan, const void* q_hat, const void* kv_cache
   p.topk_idx = topk_idx;
   p.part_o = reinterpret_cast<float*>(ws + plan->ws_partial_o);
   p.part_lse = reinterpret_cast<float*>(ws + plan->ws_partial_lse);
-  p.counters = reinterpret_cast<int32_t*>(ws + plan->ws_counters);
   p.o_lat = o_lat;
   p.lse = lse;
   p.status = reinterpret_cast<uint32_t*>(ws + plan->ws_status);
@@ -215,7 +234,13 @@ int mla_decode_run(const mla_plan* plan, const void* q_hat, const void* kv_cache
   p.num_streams = plan->num_streams;
   p.num_ctas = plan->num_ctas;
   p.scale_log2 = pr.sm_scale * 1.4426950408889634f;
-  const cudaError_t err = launch_decode(p, &kv_map, mode, reinterpret_cast<cudaStream_t>(stream));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t err = launch_decode(p, &kv_map, mode, st);
+  if (err != cudaSuccess) return MLA_ERR_CUDA;
+  // split row sets: merge their partials (all SMs, dependent launch)
+  CombineParams cp;
+  fill_combine_params(*plan, ws, seq_lens, o_lat, lse, &cp);
+  err = launch_combine(cp, st);
   return err == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
@@ -226,23 +251,8 @@ int mla_combine(const mla_plan* plan, const int32_t* seq_lens, const void* works
   if (!seq_lens || !workspace || !o_lat || !lse) return MLA_ERR_INVALID_ARGUMENT;
   if (!aligned16(workspace) || !aligned16(o_lat) || (reinterpret_cast<uintptr_t>(lse) & 3u))
     return MLA_ERR_MISALIGNED;
-  const mla_problem& pr = plan->problem;
-  const uint8_t* ws = static_cast<const uint8_t*>(workspace);
   CombineParams p;
-  p.part_o = reinterpret_cast<const float*>(ws + plan->ws_partial_o);
-  p.part_lse = reinterpret_cast<const float*>(ws + plan->ws_partial_lse);
-  p.seq_lens = seq_lens;
-  p.o_lat = o_lat;
-  p.lse = lse;
-  p.batch = pr.batch;
-  p.q_len = pr.q_len;
-  p.heads = pr.num_heads;
-  p.page_size = pr.page_size;
-  p.max_pages = pr.max_pages_per_seq;
-  p.topk_width = pr.topk_width;
-  p.causal = pr.causal;
-  p.num_streams = plan->num_streams;
-  p.num_ctas = plan->num_ctas;
+  fill_combine_params(*plan, static_cast<const uint8_t*>(workspace), seq_lens, o_lat, lse, &p);
   const cudaError_t err = launch_combine(p, reinterpret_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }

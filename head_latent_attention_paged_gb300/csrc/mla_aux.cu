@@ -25,93 +25,133 @@ __device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
 }  // namespace
 
 // ----------------------------------------------------------------------------
-// combine: one block per (row set, 4 heads); one warp per head, 16 dims/lane
+// combine: one block per (row set, head); thread t owns latent dims
+// [4t, 4t + 4).  Launched as a programmatic dependent of the decode kernel:
+// the work split is derived from seq_lens while the decode runs, then every
+// block waits for the decode grid (whose partials it reads) before touching
+// its outputs.  Every block waits, even one with nothing to merge, so this
+// grid never completes before the decode grid does (the W_UV launch after
+// it relies on that for the rows the decode wrote directly).
 // ----------------------------------------------------------------------------
-__global__ void __launch_bounds__(128) mla_combine_kernel(const CombineParams p) {
-  const int s = blockIdx.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.y * 4 + warp;
+namespace {
+constexpr int kCombineThreads = 128;   // x 4 dims = 512 latent dims
+}  // namespace
+
+__global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(const CombineParams p) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int s = blockIdx.x, h = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = p.num_streams;
   const int max_tokens = p.max_pages * p.page_size;
-  // tiles before stream s, tiles of s, tiles in total (same split as the decode grid)
+  __shared__ int64_t red64[2][kCombineThreads / 32];
+  // tiles before stream s and in total (the decode grid's split)
   int64_t before = 0, tot = 0;
-  for (int t = threadIdx.x; t < S; t += blockDim.x) {
+  for (int t = tid; t < S; t += kCombineThreads) {
     const int b = t / p.q_len, j = t - b * p.q_len;
     const int32_t len = stream_len(p.seq_lens[b], p.q_len, j, p.causal, p.topk_width, max_tokens);
     const int64_t n = (len + kTile - 1) / kTile;
     tot += n;
     if (t < s) before += n;
   }
-  __shared__ int64_t red[2][4];
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     before += __shfl_xor_sync(0xffffffffu, before, o);
     tot += __shfl_xor_sync(0xffffffffu, tot, o);
   }
-  if (lane == 0) { red[0][warp] = before; red[1][warp] = tot; }
+  if (lane == 0) { red64[0][warp] = before; red64[1][warp] = tot; }
   __syncthreads();
-  before = red[0][0] + red[0][1] + red[0][2] + red[0][3];
-  tot = red[1][0] + red[1][1] + red[1][2] + red[1][3];
-  if (h >= p.heads) return;
+  before = tot = 0;
+#pragma unroll
+  for (int w = 0; w < kCombineThreads / 32; ++w) { before += red64[0][w]; tot += red64[1][w]; }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int b = s / p.q_len, j = s - b * p.q_len;
   const int32_t len = stream_len(p.seq_lens[b], p.q_len, j, p.causal, p.topk_width, max_tokens);
   const int64_t ntiles = (len + kTile - 1) / kTile;
-  float4* out = reinterpret_cast<float4*>(p.o_lat + (static_cast<int64_t>(s) * p.heads + h) * kDc);
-  float4 acc[4];
+  if (ntiles == 0) return;   // the decode wrote o_lat = 0, lse = -inf
+  const int c0 = tile_owner(before, tot, p.num_ctas);
+  const int c1 = tile_owner(before + ntiles - 1, tot, p.num_ctas);
+  if (c0 == c1) return;      // one CTA held the whole row set: its result is final
+  const int nseg = c1 - c0 + 1;
+  // One pass over the partials, 8 at a time (their lse values and this
+  // thread's 4 dims loaded together): running max m, sum = sum_i exp(lse_i -
+  // m), acc = sum_i exp(lse_i - m) o_i, rescaled when m grows; finally
+  // lse = m + ln(sum), o = acc / sum.
+  const float* plse = p.part_lse + static_cast<int64_t>(s + c0) * p.heads + h;
+  const float4* po = reinterpret_cast<const float4*>(p.part_o) +
+                     (static_cast<int64_t>(s + c0) * p.heads + h) * (kDc / 4) + tid;
+  const int64_t lstride = p.heads;
+  const int64_t ostride = static_cast<int64_t>(p.heads) * (kDc / 4);
+  float m = -INFINITY, sum = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k0 = 0; k0 < nseg; k0 += 8) {
+    float lv[8];
+    float4 v[8];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-  float lse = -INFINITY;
-  if (ntiles > 0) {
-    const int c0 = tile_owner(before, tot, p.num_ctas);
-    const int c1 = tile_owner(before + ntiles - 1, tot, p.num_ctas);
-    if (c0 == c1) return;   // one CTA held the whole row set: its result is final
-    float m = -INFINITY;
-    for (int c = c0; c <= c1; ++c) m = fmaxf(m, p.part_lse[static_cast<int64_t>(s + c) * p.heads + h]);
-    if (m != -INFINITY) {
-      float sum = 0.f;
-      for (int c = c0; c <= c1; ++c) sum += __expf(p.part_lse[static_cast<int64_t>(s + c) * p.heads + h] - m);
-      lse = m + __logf(sum);
-      for (int c = c0; c <= c1; ++c) {
-        const int64_t slot = s + c;
-        const float wgt = __expf(p.part_lse[slot * p.heads + h] - lse);
-        if (wgt == 0.f) continue;
-        const float4* src = reinterpret_cast<const float4*>(p.part_o + (slot * p.heads + h) * kDc);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float4 v = src[lane + 32 * k];
-          acc[k].x += wgt * v.x; acc[k].y += wgt * v.y;
-          acc[k].z += wgt * v.z; acc[k].w += wgt * v.w;
-        }
-      }
+    for (int u = 0; u < 8; ++u) {
+      const bool in = k0 + u < nseg;
+      lv[u] = in ? plse[(k0 + u) * lstride] : -INFINITY;
+      v[u] = in ? po[(k0 + u) * ostride] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-  }
+    float mc = m;
 #pragma unroll
-  for (int k = 0; k < 4; ++k) out[lane + 32 * k] = acc[k];
-  if (lane == 0) p.lse[static_cast<int64_t>(s) * p.heads + h] = lse;
+    for (int u = 0; u < 8; ++u) mc = fmaxf(mc, lv[u]);
+    if (mc == -INFINITY) continue;     // nothing live so far
+    const float r = (m == -INFINITY) ? 0.f : __expf(m - mc);
+    sum *= r;
+    acc.x *= r; acc.y *= r; acc.z *= r; acc.w *= r;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float w = (lv[u] == -INFINITY) ? 0.f : __expf(lv[u] - mc);
+      sum += w;
+      acc.x = fmaf(w, v[u].x, acc.x);
+      acc.y = fmaf(w, v[u].y, acc.y);
+      acc.z = fmaf(w, v[u].z, acc.z);
+      acc.w = fmaf(w, v[u].w, acc.w);
+    }
+    m = mc;
+  }
+  const float lse = (m == -INFINITY) ? -INFINITY : m + __logf(sum);
+  const float inv = (m == -INFINITY) ? 0.f : 1.f / sum;
+  acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
+  reinterpret_cast<float4*>(p.o_lat + (static_cast<int64_t>(s) * p.heads + h) * kDc)[tid] = acc;
+  if (tid == 0) p.lse[static_cast<int64_t>(s) * p.heads + h] = lse;
 }
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {
   if (p.num_streams == 0) return cudaSuccess;
-  dim3 grid(p.num_streams, (p.heads + 3) / 4);
-  mla_combine_kernel<<<grid, 128, 0, stream>>>(p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.num_streams, p.heads);
+  cfg.blockDim = dim3(kCombineThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t err = cudaLaunchKernelEx(&cfg, mla_combine_kernel, p);
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 
 // ----------------------------------------------------------------------------
-// UV projection: per (head h, 128 output dims, 64 rows):
+// UV projection: per (head h, 128 output dims, 32 rows):
 //   D^T[n, r] = sum_k W_UV[h][k][n] * o_lat[r][h][k]
 // A = W_UV[h] slice (MN-major, TMA), B = o_lat rows converted to bf16
-// (K-major, written by the threads), D in TMEM (128 lanes x 64 columns).
+// (K-major, written by the threads), D in TMEM (128 lanes x 32 columns).
+// 32 rows per CTA keeps the grid wide (dense batch 64 x 20 heads: 80 CTAs)
+// and each thread issues all its o_lat loads (16 x 32 B) before using them.
 // ----------------------------------------------------------------------------
 namespace {
-constexpr int kUvRows = 64;                 // N of the MMA
+constexpr int kUvRows = 32;                 // N of the MMA
 constexpr int kUvA = 8 * 2 * kChunkBytes;   // 8 K-blocks x 2 n-chunks x 8 KB = 128 KB
-constexpr int kUvB = 8 * kUvRows * 128;     // 8 K-blocks x 64 rows x 128 B = 64 KB
+constexpr int kUvB = 8 * kUvRows * 128;     // 8 K-blocks x 32 rows x 128 B = 32 KB
+constexpr int kUvItems = kUvRows * 64 / 128;   // 16-byte B pieces per thread
 constexpr int kUvSmem = kUvA + kUvB + 1024 + 64;
 }  // namespace
 
 __global__ void __launch_bounds__(128, 1)
-    mla_uv_kernel(const __grid_constant__ CUtensorMap w_map, const float* __restrict__ o_lat,
+    mla_uv_kernel(const __grid_constant__ CUtensorMap w_map, const float* o_lat,
                   uint16_t* __restrict__ out, int rows, int heads) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -130,7 +170,7 @@ __global__ void __launch_bounds__(128, 1)
     fence_mbar_init();
   }
   if (warp == 0) {
-    tmem_alloc(tslot, 64);
+    tmem_alloc(tslot, 32);
     tmem_relinquish();
   }
   __syncthreads();
@@ -142,24 +182,39 @@ __global__ void __launch_bounds__(128, 1)
         tma_load_2d(sA + (kb * 2 + nc) * kChunkBytes, &w_map, &bars[0], mt * 128 + nc * 64,
                     h * kDc + kb * 64, 0ull);
   }
-  // o_lat is produced by the preceding decode launch: wait for it (the W_UV
-  // loads above already overlap its tail when launched as a dependent).
+  // o_lat is produced by the launches this one depends on: wait for them
+  // (the W_UV loads above already overlap their tail).  o_lat is not a
+  // restrict-qualified pointer on purpose: read-only-for-the-kernel loads
+  // could be scheduled ahead of this wait.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  // B: o_lat[r0 + r][h][k] -> bf16, [kb][r][128 B] swizzled
-  for (int e = tid; e < kUvRows * 64; e += 128) {
-    const int r = e >> 6, piece = e & 63;        // piece: 8 consecutive k
-    const int kb = piece >> 3, w16 = piece & 7;
-    uint4 v = make_uint4(0, 0, 0, 0);
+  // B: o_lat[r0 + r][h][k] -> bf16, [kb][r][128 B] swizzled.  Item e of
+  // this thread is piece (tid + 128 e): row (tid + 128 e) / 64, 8 consecutive
+  // k; all loads are issued before any is used.
+  float4 va[kUvItems], vb[kUvItems];
+#pragma unroll
+  for (int e = 0; e < kUvItems; ++e) {
+    const int idx = tid + 128 * e;
+    const int r = idx >> 6, piece = idx & 63;
     if (r0 + r < rows) {
       const float4* src = reinterpret_cast<const float4*>(
           o_lat + (static_cast<int64_t>(r0 + r) * heads + h) * kDc + piece * 8);
-      const float4 a = src[0], b = src[1];
-      __nv_bfloat162 x0 = __floats2bfloat162_rn(a.x, a.y), x1 = __floats2bfloat162_rn(a.z, a.w);
-      __nv_bfloat162 x2 = __floats2bfloat162_rn(b.x, b.y), x3 = __floats2bfloat162_rn(b.z, b.w);
-      v = make_uint4(*reinterpret_cast<uint32_t*>(&x0), *reinterpret_cast<uint32_t*>(&x1),
-                     *reinterpret_cast<uint32_t*>(&x2), *reinterpret_cast<uint32_t*>(&x3));
+      va[e] = src[0];
+      vb[e] = src[1];
+    } else {
+      va[e] = vb[e] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    *reinterpret_cast<uint4*>(sB + kb * (kUvRows * 128) + r * 128 + ((w16 ^ (r & 7)) << 4)) = v;
+  }
+#pragma unroll
+  for (int e = 0; e < kUvItems; ++e) {
+    const int idx = tid + 128 * e;
+    const int r = idx >> 6, piece = idx & 63;
+    const int kb = piece >> 3, w16 = piece & 7;
+    const float4 a = va[e], b = vb[e];
+    __nv_bfloat162 x0 = __floats2bfloat162_rn(a.x, a.y), x1 = __floats2bfloat162_rn(a.z, a.w);
+    __nv_bfloat162 x2 = __floats2bfloat162_rn(b.x, b.y), x3 = __floats2bfloat162_rn(b.z, b.w);
+    *reinterpret_cast<uint4*>(sB + kb * (kUvRows * 128) + r * 128 + ((w16 ^ (r & 7)) << 4)) =
+        make_uint4(*reinterpret_cast<uint32_t*>(&x0), *reinterpret_cast<uint32_t*>(&x1),
+                   *reinterpret_cast<uint32_t*>(&x2), *reinterpret_cast<uint32_t*>(&x3));
   }
   fence_proxy_async_smem();
   tc_fence_before();
@@ -206,7 +261,7 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 64);
+    tmem_dealloc(tmem, 32);
   }
 }
 

@@ -24,8 +24,9 @@
 //                   bf16, lazy rescale of O^T in TMEM when the running max
 //                   grows by more than 2^8; at a stream change they write the
 //                   next stream's q_hat into TMEM, and at the end of each
-//                   segment the normalised result (or a partial plus its lse,
-//                   merged by whichever CTA delivers a stream's last partial).
+//                   segment the normalised result (or, for a stream split
+//                   over several CTAs, a partial plus its lse, merged by the
+//                   combine kernel that follows this one).
 //
 // All heads of a request reuse each staged tile, so every cached byte is read
 // from HBM once per stream.  Waits are bounded (sm103_ptx.cuh); a timeout
@@ -86,7 +87,6 @@ struct __align__(8) Ctrl {
   uint32_t tmem_base;
   int32_t abort_flag;
   int32_t rescale_tile[2];
-  int32_t merge_flag;
   float alpha[2][kMaxHeads];
   float l_final[kMaxHeads];
 };
@@ -267,93 +267,6 @@ __device__ __forceinline__ void dequant_group(uint32_t row_addr, int g, uint4 (&
     }
     o[q] = make_uint4(r[0], r[1], r[2], r[3]);
   }
-}
-
-// Merge the nseg partials (slots s + c_first ...) of row set s into o_lat and
-// lse: lse = ln sum_i exp(lse_i), o = sum_i exp(lse_i - lse) o_i.  Run by the
-// 128 softmax threads after the tile loop; thread t owns latent dims
-// [4t, 4t + 4) of every head.  The partials were written by other CTAs
-// (L2-resident): the lse values go through shared memory in one round trip
-// (`scratch`, `scratch_floats` floats, free once the tile loop is over), the
-// weights are formed there, and the partial outputs are loaded 8 heads x 4
-// partials at a time so many loads are in flight.
-__device__ __forceinline__ void merge_partials(const DecodeParams& p, int32_t s, int32_t c_first,
-                                               int32_t nseg, int H, int tid, float* tot_sm,
-                                               float* scratch, int scratch_floats) {
-  const float* plse = p.part_lse + static_cast<int64_t>(s + c_first) * H;
-  const float4* po = reinterpret_cast<const float4*>(p.part_o + static_cast<int64_t>(s + c_first) * H * kDc);
-  const int kc = max(1, min(nseg, scratch_floats / H));   // partials per chunk
-  // ---- per-head total lse (running max / sum over chunks of partials)
-  float m = -INFINITY, sum = 0.f;
-  for (int k0 = 0; k0 < nseg; k0 += kc) {
-    const int n = min(kc, nseg - k0);
-    for (int e = tid; e < n * H; e += 128) scratch[e] = __ldcg(plse + static_cast<int64_t>(k0) * H + e);
-    named_bar_sync(1, 128);
-    if (tid < H) {
-      float mc = m;
-      for (int k = 0; k < n; ++k) mc = fmaxf(mc, scratch[k * H + tid]);
-      if (mc != -INFINITY) {
-        float acc = (m == -INFINITY) ? 0.f : sum * __expf(m - mc);
-        for (int k = 0; k < n; ++k) acc += __expf(scratch[k * H + tid] - mc);
-        m = mc;
-        sum = acc;
-      }
-    }
-    named_bar_sync(1, 128);
-  }
-  if (tid < H) {
-    const float tot = (m == -INFINITY) ? -INFINITY : m + __logf(sum);
-    tot_sm[tid] = tot;
-    p.lse[static_cast<int64_t>(s) * H + tid] = tot;
-  }
-  named_bar_sync(1, 128);
-  // ---- weighted sum of the partial outputs, chunk by chunk (the weights of a
-  // chunk live in scratch; 8 heads x 4 partials of loads in flight)
-  for (int k0 = 0; k0 < nseg; k0 += kc) {
-    const int n = min(kc, nseg - k0);
-    for (int e = tid; e < n * H; e += 128) {
-      const int hh = e % H;
-      const float lv = __ldcg(plse + static_cast<int64_t>(k0) * H + e);
-      scratch[e] = (tot_sm[hh] == -INFINITY || lv == -INFINITY) ? 0.f : __expf(lv - tot_sm[hh]);
-    }
-    named_bar_sync(1, 128);
-    for (int hb = 0; hb < H; hb += 8) {
-      float4 acc[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (k0 > 0 && hb + j < H)   // continue the sums of earlier chunks
-          acc[j] = reinterpret_cast<const float4*>(p.o_lat + (static_cast<int64_t>(s) * H + hb + j) * kDc)[tid];
-      }
-      for (int kb = 0; kb < n; kb += 4) {
-        float4 v[8][4];
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const bool use = hb + j < H && kb + kk < n;
-            v[j][kk] = use ? __ldcg(po + (static_cast<int64_t>(k0 + kb + kk) * H + hb + j) * (kDc / 4) + tid)
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const float wgt = (hb + j < H && kb + kk < n) ? scratch[(kb + kk) * H + hb + j] : 0.f;
-            acc[j].x = fmaf(wgt, v[j][kk].x, acc[j].x);
-            acc[j].y = fmaf(wgt, v[j][kk].y, acc[j].y);
-            acc[j].z = fmaf(wgt, v[j][kk].z, acc[j].z);
-            acc[j].w = fmaf(wgt, v[j][kk].w, acc[j].w);
-          }
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (hb + j < H)
-          reinterpret_cast<float4*>(p.o_lat + (static_cast<int64_t>(s) * H + hb + j) * kDc)[tid] = acc[j];
-    }
-    named_bar_sync(1, 128);   // scratch is rewritten by the next chunk
-  }
-  named_bar_sync(1, 128);   // tot_sm may be reused by the next merge
 }
 
 }  // namespace
@@ -801,8 +714,6 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
       Walker wk;
       wk.init(prefix, S, g0);
       bool failed = false;
-      int npend = 0;
-      int32_t pend_s0 = 0, pend_f0 = 0, pend_l0 = 0, pend_s1 = 0, pend_f1 = 0, pend_l1 = 0;
       // the first stream's queries
       if (w >= 2) load_q_tmem(p.q_hat, wk.s, H, tmem + lane_base, lane, w);
       tc_fence_before();
@@ -995,45 +906,8 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&ctrl->o_free);
-          if (split) {   // merged after this CTA's last tile (see below)
-            if (npend == 0) { pend_s0 = s; pend_f0 = c_first; pend_l0 = c_last; }
-            else { pend_s1 = s; pend_f1 = c_first; pend_l1 = c_last; }
-            ++npend;
-          }
         }
         wk.next(prefix, S);
-      }
-      // Split row sets (at most the CTA's first and last): count this CTA's
-      // partials in; the CTA delivering a row set's last partial merges them
-      // all, lse = ln sum_i exp(lse_i), o = sum_i exp(lse_i - lse) o_i.  Done
-      // after the tile loop so the fence and the atomic never stall it.
-      if (!failed && npend > 0) {
-        __threadfence();
-        named_bar_sync(1, 128);
-        if (tid == 0) {
-          int flags = 0;
-          for (int k = 0; k < npend; ++k) {
-            const int32_t ps = k == 0 ? pend_s0 : pend_s1;
-            const int32_t nseg = (k == 0 ? pend_l0 - pend_f0 : pend_l1 - pend_f1) + 1;
-            const int prev = atomicAdd(&p.counters[ps], 1);
-            if (prev == nseg - 1) {
-              p.counters[ps] = 0;        // ready for the next launch
-              flags |= 1 << k;
-            }
-          }
-          ctrl->merge_flag = flags;
-        }
-        named_bar_sync(1, 128);
-        const int flags = ctrl->merge_flag;
-        if (flags) __threadfence();
-        for (int k = 0; k < npend; ++k) {
-          if (!((flags >> k) & 1)) continue;
-          const int32_t ps = k == 0 ? pend_s0 : pend_s1;
-          const int32_t pf = k == 0 ? pend_f0 : pend_f1;
-          const int32_t pl = k == 0 ? pend_l0 : pend_l1;
-          merge_partials(p, ps, pf, pl - pf + 1, H, tid, ctrl->l_final,
-                         reinterpret_cast<float*>(sP), kPBufs * NP * 128 / 4);
-        }
       }
       if (failed && lane == 0) {
         set_status(p.status, MLA_STATUS_TIMEOUT);

@@ -37,7 +37,6 @@ struct DecodeParams {
   const int32_t* topk_idx;      // [S][width] or null
   float* part_o;                // [slots][H][512]
   float* part_lse;              // [slots][H]
-  int32_t* counters;            // [S] partials delivered per stream (left at 0)
   float* o_lat;                 // [S][H][512] output
   float* lse;                   // [S][H] output
   uint32_t* status;

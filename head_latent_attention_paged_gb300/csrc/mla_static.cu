@@ -5,8 +5,7 @@
 // running while a CUDA graph is being captured or replayed, runtimes that
 // hand out only the input and output buffers they manage themselves, or
 // allocators that forbid growth after start-up.  This entry point needs no
-// workspace from them: its scratch (split partials, merge counters and, when
-// the caller passes none, the status word) lives in one fixed-size array in
+// workspace from them: its scratch (split partials and the status word) lives in one fixed-size array in
 // device memory that belongs to this library.
 //
 // Properties of that array, for users:
@@ -16,7 +15,7 @@
 //     overlap on the GPU (different streams without ordering between them)
 //     race on it and give undefined results; order them on one stream.
 //   * It keeps the previous call's contents.  Each call clears the parts
-//     that must start at zero (merge counters and the internal status word)
+//     that must start at zero (the reserved words and the status word)
 //     on the caller's stream before launching.
 //   * The first call on a device looks up the array's device address (a
 //     runtime query, no allocation) with that device current.  Make that
@@ -74,7 +73,7 @@ extern "C" MLA_API int mla_decode_run_static(const mla_plan* plan, const void* q
   if (scratch_address(&scratch) != cudaSuccess) return MLA_ERR_CUDA;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(scratch);
-  // The merge counters and the status word must start at zero; they sit at
+  // The reserved words and the status word must start at zero; they sit at
   // the end of the workspace layout, from ws_counters on.
   if (cudaMemsetAsync(ws + plan->ws_counters, 0,
                       static_cast<size_t>(plan->workspace_bytes - plan->ws_counters),

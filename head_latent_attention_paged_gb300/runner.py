@@ -73,7 +73,8 @@ class DecodeStep:
         mla_q_absorb(self.plan, self.q_nope, self.q_rope, self.w_uk, self.q_hat, self.stream)
 
     def run(self):
-        """Attention pass with the split merge fused in: writes o_lat and lse."""
+        """Attention pass and the split merge (two kernels, the second a
+        programmatic dependent of the first): writes o_lat and lse."""
         mla_decode_run(self.plan, self.q_hat, self.cache, self.block_table, self.seq_lens,
                        self.topk_idx, self.workspace, self.o_lat, self.lse, self.stream)
 
@@ -85,8 +86,8 @@ class DecodeStep:
         mla_uv_proj(self.o_lat, self.w_uv, self.out, self.rows, self.H, self.stream)
 
     def step(self):
-        """Attention pass (merge fused) + W_UV projection; the absorbed query
-        is an input."""
+        """Attention pass, split merge and W_UV projection; the absorbed
+        query is an input."""
         self.run()
         self.uv()
 
@@ -96,4 +97,4 @@ class DecodeStep:
     def clear_status(self):
         mla_clear_status(self.plan, self.workspace, self.stream)
 
-    KERNELS_PER_STEP = 2
+    KERNELS_PER_STEP = 3

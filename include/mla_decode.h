@@ -117,7 +117,7 @@ typedef struct {
   int32_t smem_bytes;       /* dynamic shared memory of the decode kernel */
   int64_t ws_partial_o;     /* byte offset of f32 [num_slots][H][512] */
   int64_t ws_partial_lse;   /* byte offset of f32 [num_slots][H] */
-  int64_t ws_counters;      /* byte offset of int32 [num_streams] merge counters */
+  int64_t ws_counters;      /* byte offset of int32 [num_streams], reserved (left at 0) */
   int64_t ws_status;        /* byte offset of the uint32 status word */
   int64_t workspace_bytes;  /* total workspace size */
   int64_t planned_tiles;    /* tiles implied by seq_lens_host (0 if not given) */
@@ -150,12 +150,13 @@ MLA_API int mla_q_absorb(const mla_plan* plan, const void* q_nope, const void* q
                  const void* w_uk, void* q_hat, mla_stream_t stream);
 
 /*
- * mla_decode_run -- the attention pass over the paged cache, with the
- * split-KV merge fused in.  Each (request, query token) row set is cut into
+ * mla_decode_run -- the attention pass over the paged cache, followed by the
+ * split-KV merge.  Each (request, query token) row set is cut into
  * contiguous 64-token tiles spread evenly over the plan's CTAs; a row set
  * handled by one CTA writes its result directly, one split over several
- * CTAs leaves normalised partials (o_i, lse_i) in the workspace and the CTA
- * delivering the last of them merges: lse = ln sum_i exp(lse_i),
+ * CTAs leaves normalised partials (o_i, lse_i) in the workspace, merged by a
+ * second kernel launched right behind the first as a programmatic dependent
+ * (its set-up overlaps the attention pass): lse = ln sum_i exp(lse_i),
  * o_lat = sum_i exp(lse_i - lse) o_i.  A row set with no visible token gets
  * o_lat = 0 and lse = -inf.
  *   q_hat       : bf16 [B*Q][H][576] absorbed queries
@@ -167,9 +168,8 @@ MLA_API int mla_q_absorb(const mla_plan* plan, const void* q_nope, const void* q
  *   topk_idx    : NULL for dense; sparse: int32 [B*Q][topk_width] logical
  *                 positions of the request, -1 = masked slot
  *   workspace   : device buffer of plan->workspace_bytes, zeroed once before
- *                 its first use; the library leaves its counters at zero
- *                 after every complete run (re-zero it after a run that
- *                 reported MLA_STATUS_TIMEOUT)
+ *                 its first use (its reserved words must stay zero; the
+ *                 status word collects MLA_STATUS_* bits until cleared)
  *   o_lat       : f32 [B*Q][H][512] output (latent-space attention output)
  *   lse         : f32 [B*Q][H] output (natural-log LSE of the scaled scores)
  * Calls on one workspace must not overlap on the device.
@@ -186,7 +186,7 @@ MLA_API int mla_decode_run(const mla_plan* plan, const void* q_hat, const void* 
  * previous mla_decode_run left in the workspace (same plan, seq_lens and
  * workspace): rewrites o_lat and lse of every row set that was split over
  * several CTAs and leaves the others untouched.  mla_decode_run already
- * performs this merge; the call exists to re-derive or check it.
+ * launches this merge; the call exists to re-derive or check it.
  */
 MLA_API int mla_combine(const mla_plan* plan, const int32_t* seq_lens, const void* workspace,
                 float* o_lat, float* lse, mla_stream_t stream);
