@@ -33,7 +33,6 @@
 // sets MLA_STATUS_TIMEOUT and the CTA unwinds after draining its own copies
 // and MMAs, then releases its tensor memory.
 #include <cuda_bf16.h>
-#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -48,15 +47,18 @@ namespace {
 constexpr int kSoftmaxWarps = 4;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
-constexpr int kDequantWarp0 = 6;    // FP8 mode: warps 6..9 dequantise
-constexpr int kDequantWarps = 4;
+constexpr int kDequantWarp0 = 6;    // FP8 mode: warps 6..11 dequantise
+constexpr int kDequantWarps = 6;
+// P (bf16 [padded heads][64 tokens], the B operand of PV) lives in the RoPE
+// chunk of its own tile's stage: QK(i) is the only reader of that chunk and
+// P(i) is written after S(i) is complete, so every stage carries its own P.
+constexpr int kPChunkOffset = (kChunks - 1) * kChunkBytes;
 
 template <int kMode>
 struct ModeTraits {
   static constexpr bool kFp8 = kMode == kModeDenseFp8;
   static constexpr int kThreads = kFp8 ? 32 * (kDequantWarp0 + kDequantWarps) : 192;
   static constexpr int kNumStages = kFp8 ? kFp8Stages : kStages;   // bf16 tiles
-  static constexpr int kPBufs = kFp8 ? 1 : 2;                       // P buffers
 };
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s per wait
 constexpr float kRescaleThreshold = 8.0f;           // log2 units: rescale if max grows > 2^8
@@ -218,34 +220,56 @@ __device__ __forceinline__ uint32_t lds_u8(uint32_t addr) {
   return v;
 }
 
-// Two e4m3 codes (low byte = lower address) -> two f16 (exact: every e4m3
-// value, subnormals included, is a normal f16).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
-  uint32_t h;
-  asm("{\n .reg .b16 c;\n cvt.u16.u32 c, %1;\n cvt.rn.f16x2.e4m3x2 %0, c;\n}"
-      : "=r"(h) : "r"(two_codes));
-  return h;
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 
-// 2^(b - 127) as a float for an e8m0 byte b (b = 0 gives the subnormal
-// 2^-127, b = 255 is NaN).
-__device__ __forceinline__ float e8m0_to_f32(uint32_t b) {
-  const uint32_t bits = b == 0 ? 0x00400000u : (b == 255 ? 0x7FC00000u : (b << 23));
-  return __uint_as_float(bits);
+// Two e4m3 codes (bytes 0 and 1 of `four` if hi == 0, else bytes 2 and 3)
+// as two bf16 holding value * 2^-120, exactly.  An e4m3 code s.eeee.mmm
+// placed as the bf16 s.0000eeee.mmm0000 has value 2^(e-127) (1 + m/8) for
+// e > 0, which is 2^-120 times the e4m3 value 2^(e-7) (1 + m/8); for e = 0
+// both formats are subnormal, (m/8) 2^-126 and (m/8) 2^-6, again a factor
+// 2^-120; zeros map to zeros.  The byte permute sign-extends each code to
+// 16 bits; the shift and mask then keep the sign bit and the 7 low bits.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2_scaled(uint32_t four, int hi) {
+  // prmt selector nibbles: bits 0-2 pick a byte, bit 3 replicates its sign
+  uint32_t sx;
+  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(sx) : "r"(four), "r"(hi ? 0xB3A2u : 0x9180u));
+  return (sx << 4) & 0x87F087F0u;
 }
 
-// Two f16 (packed) times a power of two -> two bf16 (packed).  The product
-// is exact in f32 and has at most 4 significant bits, so the bf16 rounding
-// is exact too (barring under/overflow of the bf16 range).
-__device__ __forceinline__ uint32_t f16x2_scaled_to_bf16x2(uint32_t h2, float scale) {
-  const __half2 hv = *reinterpret_cast<const __half2*>(&h2);
-  const float2 f = __half22float2(hv);
-  return pack_bf16x2(f.x * scale, f.y * scale);
+// bf16x2 multiplier that, applied after the placement above, gives
+// value * 2^(b - 127) for an e8m0 byte b: 2^(b - 7) when it is a normal bf16
+// (b <= 134), split in two factors beyond; NaN for b = 255.
+struct ScaleX2 {
+  uint32_t f1, f2;
+  bool two;
+};
+__device__ __forceinline__ ScaleX2 e8m0_scale_x2(uint32_t b) {
+  ScaleX2 sc;
+  if (b == 255u) {
+    sc.f1 = 0x7FC07FC0u;
+    sc.two = false;
+  } else if (b <= 134u) {
+    const uint32_t e = (b + 120u) << 7;      // 2^(b - 7), b + 120 in [120, 254]
+    sc.f1 = e | (e << 16);
+    sc.two = false;
+  } else {
+    sc.f1 = 0x7F007F00u;                     // 2^127
+    const uint32_t e = (b - 7u) << 7;        // 2^(b - 134), b - 7 in [128, 247]
+    sc.f2 = e | (e << 16);
+    sc.two = true;
+  }
+  if (!sc.two) sc.f2 = 0x3F803F80u;          // 1.0
+  return sc;
 }
 
 // Dequantise group g (values 32g .. 32g+31) of one FP8 row in shared memory
 // (row_addr: 2-byte aligned start of the row's 594 bytes) into 4 x 16 bytes
-// of bf16 (8 values each, in dimension order).
+// of bf16 (8 values each, in dimension order).  Exact: every product is an
+// e4m3 value (4 significant bits) times a power of two.
 __device__ __forceinline__ void dequant_group(uint32_t row_addr, int g, uint4 (&o)[4]) {
   const uint32_t a = row_addr + 32u * g;
   const uint32_t a4 = a & ~3u;
@@ -254,7 +278,7 @@ __device__ __forceinline__ void dequant_group(uint32_t row_addr, int g, uint4 (&
 #pragma unroll
   for (int k = 0; k < 8; ++k) w[k] = lds_u32(a4 + 4u * k);
   w[8] = odd ? lds_u32(a4 + 32u) : 0u;
-  const float scale = e8m0_to_f32(lds_u8(row_addr + kDqk + g));
+  const ScaleX2 sc = e8m0_scale_x2(lds_u8(row_addr + kDqk + g));
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     uint32_t r[4];
@@ -262,8 +286,14 @@ __device__ __forceinline__ void dequant_group(uint32_t row_addr, int g, uint4 (&
     for (int k = 0; k < 2; ++k) {
       const int wi = 2 * q + k;
       const uint32_t v = odd ? __funnelshift_r(w[wi], w[wi + 1], 16) : w[wi];
-      r[2 * k] = f16x2_scaled_to_bf16x2(e4m3x2_to_f16x2(v & 0xFFFFu), scale);
-      r[2 * k + 1] = f16x2_scaled_to_bf16x2(e4m3x2_to_f16x2(v >> 16), scale);
+      uint32_t lo = bf16x2_mul(e4m3x2_to_bf16x2_scaled(v, 0), sc.f1);
+      uint32_t hi = bf16x2_mul(e4m3x2_to_bf16x2_scaled(v, 1), sc.f1);
+      if (sc.two) {
+        lo = bf16x2_mul(lo, sc.f2);
+        hi = bf16x2_mul(hi, sc.f2);
+      }
+      r[2 * k] = lo;
+      r[2 * k + 1] = hi;
     }
     o[q] = make_uint4(r[0], r[1], r[2], r[3]);
   }
@@ -277,9 +307,9 @@ DecodeLayout decode_layout(int heads, int heads_pad, int num_streams, int mode) 
   DecodeLayout L;
   L.off_stage = 0;
   L.off_raw = (fp8 ? kFp8Stages : kStages) * kTileBytes;
-  const int raw_end = L.off_raw + (fp8 ? kRawStages * kFp8TileBytes : 0);
-  L.off_p = (raw_end + 1023) / 1024 * 1024;   // 128-byte swizzle atoms: 1 KB aligned
-  L.off_ctrl = L.off_p + (fp8 ? 1 : 2) * heads_pad * 128;
+  (void)heads_pad;
+  L.off_p = L.off_stage + kPChunkOffset;     // first stage's P; stride kTileBytes
+  L.off_ctrl = L.off_raw + (fp8 ? kRawStages * kFp8TileBytes : 0);
   L.total = L.off_ctrl + static_cast<int>(sizeof(Ctrl)) + (num_streams + 1) * 4;
   return L;
 }
@@ -291,13 +321,11 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
   using MT = ModeTraits<kMode>;
   constexpr int kThreads = MT::kThreads;
   constexpr int kNumStages = MT::kNumStages;
-  constexpr int kPBufs = MT::kPBufs;
   // The buffers need 1024-byte alignment (128-byte swizzle atoms); the
   // dynamic shared window starts aligned, which is checked below.
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* sStage = smem + L.off_stage;
   uint8_t* sRaw = smem + L.off_raw;
-  uint8_t* sP = smem + L.off_p;
   Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + L.off_ctrl);
   int32_t* prefix = reinterpret_cast<int32_t*>(smem + L.off_ctrl + sizeof(Ctrl));
 
@@ -352,9 +380,6 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
     const int32_t len = stream_len(p.seq_lens[b], p.q_len, j, p.causal, p.topk_width, max_tokens);
     prefix[s + 1] = (len + kTile - 1) / kTile;
   }
-  // P buffers start at zero: rows of padded heads are never written again
-  for (int i = tid; i < kPBufs * NP * 128 / 16; i += kThreads)
-    reinterpret_cast<uint4*>(sP)[i] = make_uint4(0, 0, 0, 0);
   __syncthreads();
   if (warp == 0) {   // exclusive prefix sum of tiles over streams
     int32_t carry = 0;
@@ -551,12 +576,15 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
       // whole buffer lies below 256 KB, so the field never carries).
       const uint64_t qk_b0 = make_smem_desc(smem_u32(sStage), 16, 1024, kSmemLayoutSW128);
       const uint64_t pv_a0 = make_smem_desc(smem_u32(sStage), kChunkBytes, 1024, kSmemLayoutSW128);
-      const uint64_t pv_b0 = make_smem_desc(smem_u32(sP), 16, 1024, kSmemLayoutSW128);
+      const uint64_t pv_b0 = make_smem_desc(smem_u32(sStage + kPChunkOffset), 16, 1024,
+                                            kSmemLayoutSW128);
       // Single-thread event loop: issue PV(pv) as soon as its P is written
       // (checked first: it releases a stage), and QK(qk) once its tile, the
       // stream's q_hat and the S buffer are ready.  QK(qk) is only issued
-      // after PV(qk-2), so the commit that signals S(qk) also covers the PV
-      // that last read P buffer qk&1.
+      // after PV(qk-2), so the commit that signals S(qk) also covers PV(qk-2)
+      // (the softmax's o_done parity waits rely on it).  Padded head rows of
+      // P hold stale RoPE bytes: they only reach O^T columns that are never
+      // read.
       bool failed = false;
       if (lane == 0) {
         Walker wq, wp;
@@ -576,8 +604,7 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
               seg_p = sp;
               tc_fence_after();
               const uint64_t a0 = pv_a0 + static_cast<uint64_t>((st * kTileBytes) >> 4);
-              const uint64_t b0 =
-                  pv_b0 + static_cast<uint64_t>((((kPBufs == 2) ? (pv & 1) : 0) * NP * 128) >> 4);
+              const uint64_t b0 = pv_b0 + static_cast<uint64_t>((st * kTileBytes) >> 4);
 #pragma unroll
               for (int mt = 0; mt < 4; ++mt) {
 #pragma unroll
@@ -642,13 +669,12 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
       __syncwarp();
     } else if (MT::kFp8 && warp >= kDequantWarp0) {
       // ============================================================ dequant
-      // Thread t of the 128 owns row t % 64 and the groups of one parity
-      // (t / 64): a warp covers 32 consecutive rows, so its shared loads
-      // (row stride 594 B) and its swizzled 16-byte stores spread over the
-      // banks.
+      // Thread t of the 192 owns row t % 64 and groups t / 64 + 3k: a warp
+      // covers 32 consecutive rows, so its shared loads (row stride 594 B)
+      // and its swizzled 16-byte stores spread over the banks.
       const int dt = tid - kDequantWarp0 * 32;
       const int r = dt & 63;
-      const int gpar = dt >> 6;
+      const int gset = dt >> 6;
       bool failed = false;
       for (int32_t i = 0; i < ntiles; ++i) {
         const int rs = i % kRawStages;
@@ -663,9 +689,9 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
         const bool live = (mask >> r) & 1ull;
         const uint32_t row_addr = smem_u32(sRaw + rs * kFp8TileBytes + r * kFp8RowBytes);
         uint8_t* dst = sStage + bs * kTileBytes + r * 128;
-#pragma unroll 1
-        for (int k = 0; k < kDqk / 64; ++k) {
-          const int g = gpar + 2 * k;
+#pragma unroll 2
+        for (int k = 0; k < kDqk / 96; ++k) {
+          const int g = gset + 3 * k;
           uint4 o[4];
           if (live) {
             dequant_group(row_addr, g, o);
@@ -763,11 +789,6 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctrl->q_ready);
           }
-          // One P buffer: PV(i-1) must have read it.  PV(i) cannot be issued
-          // before P(i) is written, so this parity wait cannot run ahead.
-          if constexpr (kPBufs == 1) {
-            if (i >= 1) ok = warp_wait(&ctrl->o_done, (i - 1) & 1, abort_flag);
-          }
           if (ok && warp_has_heads) {
             // token of y[t] is 32*half + t
             const uint32_t hmask = static_cast<uint32_t>(mask >> (32 * half));
@@ -796,7 +817,7 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
               if (owner && half == 0) ctrl->rescale_tile[pb] = i;
             }
             const float nref = (m_used == -INFINITY) ? 0.f : -m_used;
-            uint8_t* prow = sP + ((kPBufs == 2) ? pb : 0) * NP * 128 + h * 128;
+            uint8_t* prow = sStage + stage * kTileBytes + kPChunkOffset + h * 128;
             float lsum = 0.f, lsum_exp = 0.f;
 #pragma unroll
             for (int c8 = 0; c8 < 4; ++c8) {
