@@ -74,6 +74,14 @@ int validate_problem(const mla_problem* pr) {
   if (static_cast<int64_t>(pr->num_pages) * pr->page_size > INT32_MAX) return MLA_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(pr->max_pages_per_seq) * pr->page_size > INT32_MAX) return MLA_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(pr->batch) * pr->q_len * pr->num_heads > INT32_MAX) return MLA_ERR_UNSUPPORTED;
+  {  // the kernels' cost prefix over row sets is 32-bit
+    const int64_t longest = pr->topk_width > 0
+                                ? pr->topk_width
+                                : static_cast<int64_t>(pr->max_pages_per_seq) * pr->page_size;
+    const int64_t per_stream = (longest + kTile - 1) / kTile * kTileCost + kStreamCost;
+    if (static_cast<int64_t>(pr->batch) * pr->q_len * per_stream > INT32_MAX)
+      return MLA_ERR_UNSUPPORTED;
+  }
   return MLA_OK;
 }
 

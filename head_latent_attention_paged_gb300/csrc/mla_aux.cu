@@ -44,12 +44,12 @@ __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(const Comb
   const int S = p.num_streams;
   const int max_tokens = p.max_pages * p.page_size;
   __shared__ int64_t red64[2][kCombineThreads / 32];
-  // tiles before stream s and in total (the decode grid's split)
+  // cost before stream s and in total (the decode grid's split)
   int64_t before = 0, tot = 0;
   for (int t = tid; t < S; t += kCombineThreads) {
     const int b = t / p.q_len, j = t - b * p.q_len;
     const int32_t len = stream_len(p.seq_lens[b], p.q_len, j, p.causal, p.topk_width, max_tokens);
-    const int64_t n = (len + kTile - 1) / kTile;
+    const int64_t n = stream_cost((len + kTile - 1) / kTile);
     tot += n;
     if (t < s) before += n;
   }
@@ -68,8 +68,8 @@ __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(const Comb
   const int32_t len = stream_len(p.seq_lens[b], p.q_len, j, p.causal, p.topk_width, max_tokens);
   const int64_t ntiles = (len + kTile - 1) / kTile;
   if (ntiles == 0) return;   // the decode wrote o_lat = 0, lse = -inf
-  const int c0 = tile_owner(before, tot, p.num_ctas);
-  const int c1 = tile_owner(before + ntiles - 1, tot, p.num_ctas);
+  const int c0 = tile_owner(tile_cost_pos(before, 0), tot, p.num_ctas);
+  const int c1 = tile_owner(tile_cost_pos(before, static_cast<int32_t>(ntiles - 1)), tot, p.num_ctas);
   if (c0 == c1) return;      // one CTA held the whole row set: its result is final
   const int nseg = c1 - c0 + 1;
   // One pass over the partials, 8 at a time (their lse values and this

@@ -103,6 +103,21 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __all_sync(0xffffffffu, ok);
 }
 
+// First global tile (in stream order) whose cost position is >= u; tile and
+// cost prefixes over the S streams, U = cost[S].
+__device__ __forceinline__ int32_t first_tile_at(const int32_t* tiles, const int32_t* cost,
+                                                 int32_t S, int32_t u) {
+  if (u >= cost[S]) return tiles[S];
+  int32_t lo = 0, hi = S;                 // largest s with cost[s] <= u
+  while (hi - lo > 1) {
+    const int32_t mid = (lo + hi) >> 1;
+    if (cost[mid] <= u) lo = mid; else hi = mid;
+  }
+  const int32_t off = u - cost[lo];
+  const int32_t k = off <= kStreamCost ? 0 : (off - kStreamCost + kTileCost - 1) / kTileCost;
+  return (k < tiles[lo + 1] - tiles[lo]) ? tiles[lo] + k : tiles[lo + 1];
+}
+
 struct Walker {
   int32_t s, lt, ntiles;
   __device__ __forceinline__ void init(const int32_t* prefix, int32_t S, int32_t g) {
@@ -310,7 +325,7 @@ DecodeLayout decode_layout(int heads, int heads_pad, int num_streams, int mode) 
   (void)heads_pad;
   L.off_p = L.off_stage + kPChunkOffset;     // first stage's P; stride kTileBytes
   L.off_ctrl = L.off_raw + (fp8 ? kRawStages * kFp8TileBytes : 0);
-  L.total = L.off_ctrl + static_cast<int>(sizeof(Ctrl)) + (num_streams + 1) * 4;
+  L.total = L.off_ctrl + static_cast<int>(sizeof(Ctrl)) + 2 * (num_streams + 1) * 4;
   return L;
 }
 
@@ -327,7 +342,8 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
   uint8_t* sStage = smem + L.off_stage;
   uint8_t* sRaw = smem + L.off_raw;
   Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + L.off_ctrl);
-  int32_t* prefix = reinterpret_cast<int32_t*>(smem + L.off_ctrl + sizeof(Ctrl));
+  int32_t* prefix = reinterpret_cast<int32_t*>(smem + L.off_ctrl + sizeof(Ctrl));  // tiles
+  int32_t* cprefix = prefix + (p.num_streams + 1);                                   // cost
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -374,25 +390,28 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
     tmem_relinquish();
   }
   if (warp == kProducerWarp && lane == 0 && kMode == kModeDenseBf16) prefetch_tmap(&kv_map);
-  // tiles per stream (stream lengths from the device seq_lens)
+  // tiles and cost per stream (stream lengths from the device seq_lens)
   for (int s = tid; s < S; s += kThreads) {
     const int b = s / p.q_len, j = s - b * p.q_len;
     const int32_t len = stream_len(p.seq_lens[b], p.q_len, j, p.causal, p.topk_width, max_tokens);
-    prefix[s + 1] = (len + kTile - 1) / kTile;
+    const int32_t nt = (len + kTile - 1) / kTile;
+    prefix[s + 1] = nt;
+    cprefix[s + 1] = stream_cost(nt);
   }
   __syncthreads();
-  if (warp == 0) {   // exclusive prefix sum of tiles over streams
+  if (warp < 2) {   // exclusive prefix sums: warp 0 of tiles, warp 1 of cost
+    int32_t* arr = warp == 0 ? prefix : cprefix;
     int32_t carry = 0;
-    if (lane == 0) prefix[0] = 0;
+    if (lane == 0) arr[0] = 0;
     for (int base = 0; base < S; base += 32) {
       const int s = base + lane;
-      int32_t v = (s < S) ? prefix[s + 1] : 0;
+      int32_t v = (s < S) ? arr[s + 1] : 0;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int32_t n = __shfl_up_sync(0xffffffffu, v, o);
         if (lane >= o) v += n;
       }
-      if (s < S) prefix[s + 1] = v + carry;
+      if (s < S) arr[s + 1] = v + carry;
       carry += __shfl_sync(0xffffffffu, v, 31);
     }
   }
@@ -401,10 +420,12 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
 
-  const int32_t total = prefix[S];
+  const int32_t ucost = cprefix[S];
   const int32_t c = blockIdx.x;
-  const int32_t g0 = static_cast<int32_t>((static_cast<int64_t>(c) * total) / p.num_ctas);
-  const int32_t g1 = static_cast<int32_t>((static_cast<int64_t>(c + 1) * total) / p.num_ctas);
+  const int32_t g0 = first_tile_at(
+      prefix, cprefix, S, static_cast<int32_t>((static_cast<int64_t>(c) * ucost) / p.num_ctas));
+  const int32_t g1 = first_tile_at(
+      prefix, cprefix, S, static_cast<int32_t>((static_cast<int64_t>(c + 1) * ucost) / p.num_ctas));
   const int32_t ntiles = g1 - g0;
   const uint32_t tmem = ctrl->tmem_base;
 
@@ -898,8 +919,9 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
           // ---- segment epilogue
           ok = !failed && warp_wait(&ctrl->o_done, i & 1, abort_flag);
           const int32_t s = wk.s;
-          const int32_t c_first = tile_owner(prefix[s], total, p.num_ctas);
-          const int32_t c_last = tile_owner(prefix[s + 1] - 1, total, p.num_ctas);
+          const int32_t c_first = tile_owner(tile_cost_pos(cprefix[s], 0), ucost, p.num_ctas);
+          const int32_t c_last = tile_owner(
+              tile_cost_pos(cprefix[s], prefix[s + 1] - prefix[s] - 1), ucost, p.num_ctas);
           const bool split = c_first != c_last;
           // an unsplit stream's result is final: straight to the outputs
           float* dst_o = split ? p.part_o + static_cast<int64_t>(s + c) * H * kDc

@@ -87,8 +87,25 @@ __host__ __device__ inline int32_t stream_len(int32_t seq_len, int32_t q_len, in
   return t;
 }
 
-// CTA that owns global tile x when `total` tiles are split over `ctas` CTAs
-// as [c*total/ctas, (c+1)*total/ctas).
+// Work split.  Every tile gets a cost position: a stream with n > 0 tiles
+// spans kStreamCost + n * kTileCost cost units, its fixed overhead (query
+// load into TMEM, epilogue) first, then one kTileCost slot per tile, so tile
+// k of a stream starting at cost pc sits at pc + kStreamCost + k * kTileCost.
+// CTA c takes the tiles whose position lies in [c*U/C, (c+1)*U/C) for U the
+// total cost: a CTA that opens more streams gets fewer tiles.
+constexpr int32_t kTileCost = 4;
+constexpr int32_t kStreamCost = 7;
+
+__host__ __device__ inline int32_t stream_cost(int32_t ntiles) {
+  return ntiles > 0 ? kStreamCost + ntiles * kTileCost : 0;
+}
+
+__host__ __device__ inline int64_t tile_cost_pos(int64_t stream_cost_start, int32_t k) {
+  return stream_cost_start + kStreamCost + static_cast<int64_t>(k) * kTileCost;
+}
+
+// CTA that owns cost position x when `total` cost units are split over
+// `ctas` CTAs as [c*total/ctas, (c+1)*total/ctas).
 __host__ __device__ inline int32_t tile_owner(int64_t x, int64_t total, int32_t ctas) {
   return static_cast<int32_t>(((x + 1) * ctas - 1) / total);
 }

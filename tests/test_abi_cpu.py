@@ -86,14 +86,14 @@ def test_plan_rejects(m, kw, code):
 
 def test_fp8_plan_fits_shared_memory(m):
     """FP8 caches plan like bf16 ones; the FP8 kernel's staging (two bf16
-    tiles, two FP8 byte tiles, one P buffer) fits the 227 KB window at the
-    largest head and row-set counts."""
+    tiles, each with its P in the RoPE chunk, and two FP8 byte tiles) fits
+    the 227 KB window at the largest head and row-set counts."""
     seq = np.array([100, 1000, 64, 0], dtype=np.int32)
     plan = m.mla_decode_plan(_problem(m, kv_dtype=m.MLA_KV_FP8_E4M3_E8M0), seq, 152)
     assert plan.planned_tiles == sum((int(t) + 63) // 64 for t in seq)
     big = m.mla_decode_plan(_problem(m, kv_dtype=m.MLA_KV_FP8_E4M3_E8M0, batch=256, num_heads=32),
                             None, 152)
-    assert 2 * 73728 + 2 * 64 * 594 + 32 * 128 < big.smem_bytes <= 232448
+    assert 2 * 73728 + 2 * 64 * 594 < big.smem_bytes <= 232448
 
 
 def test_plan_rejects_negative_seq_len_and_bad_sm_count(m):
@@ -141,28 +141,54 @@ def test_calls_reject_null_and_misaligned_pointers_before_cuda(m):
     assert e.value.code == -1
 
 
+TILE_COST, STREAM_COST = 4, 7   # the kernels' cost weights (tile, stream start)
+
+
+def _first_tile_at(tiles_pre, cost_pre, u):
+    """Host restatement of the kernel's search: first tile whose cost
+    position (stream cost start + STREAM_COST + k * TILE_COST) is >= u."""
+    S = len(tiles_pre) - 1
+    if u >= cost_pre[S]:
+        return int(tiles_pre[S])
+    s = int(np.searchsorted(cost_pre, u, side="right") - 1)
+    off = u - cost_pre[s]
+    k = 0 if off <= STREAM_COST else -(-(off - STREAM_COST) // TILE_COST)
+    nt = tiles_pre[s + 1] - tiles_pre[s]
+    return int(tiles_pre[s] + k) if k < nt else int(tiles_pre[s + 1])
+
+
 def test_stream_split_matches_kernel_rule():
-    """Host restatement of the tile split the kernels use: CTA c owns global
-    tiles [c*T/C, (c+1)*T/C); every tile has exactly one owner and partial
-    slot s + c is unique for every (stream, CTA) pair that shares a tile."""
+    """Host restatement of the cost-weighted split the kernels use: tile k of
+    stream s sits at cost position P_s + 7 + 4k (P_s: cost of the streams
+    before it, a stream with n > 0 tiles costing 7 + 4n); CTA c owns the
+    tiles at positions [c*U/C, (c+1)*U/C).  The tile ranges the decode
+    derives by search partition the tiles in order, the owner formula the
+    merge uses agrees with them, partial slot s + c is unique, and a CTA
+    that opens more streams gets fewer tiles."""
     rng = np.random.default_rng(0)
-    for _ in range(50):
+    for _ in range(200):
         S = int(rng.integers(1, 40))
         tiles = rng.integers(0, 30, size=S)
+        tiles[rng.random(S) < 0.2] = 0
         T = int(tiles.sum())
         if T == 0:
             continue
         C = int(rng.integers(1, min(T, 200) + 1))
-        starts = [c * T // C for c in range(C + 1)]
+        cost = np.where(tiles > 0, STREAM_COST + TILE_COST * tiles, 0)
+        tpre = np.concatenate([[0], np.cumsum(tiles)])
+        cpre = np.concatenate([[0], np.cumsum(cost)])
+        U = int(cpre[-1])
+        bounds = [_first_tile_at(tpre, cpre, (c * U) // C) for c in range(C + 1)]
+        assert bounds[0] == 0 and bounds[-1] == T and all(np.diff(bounds) >= 0)
         owner = np.empty(T, dtype=np.int64)
         for c in range(C):
-            owner[starts[c]:starts[c + 1]] = c
-        formula = np.array([((x + 1) * C - 1) // T for x in range(T)])
-        assert np.array_equal(owner, formula)
+            owner[bounds[c]:bounds[c + 1]] = c
         slots = set()
-        pre = np.concatenate([[0], np.cumsum(tiles)])
         for s in range(S):
-            for x in range(pre[s], pre[s + 1]):
-                slots.add((s, int(owner[x])))
+            for k in range(int(tiles[s])):
+                x = int(cpre[s]) + STREAM_COST + TILE_COST * k
+                c = ((x + 1) * C - 1) // U
+                assert c == owner[tpre[s] + k]
+                slots.add((s, c))
         keys = [s + c for s, c in slots]
         assert len(keys) == len(set(keys)) and max(keys) < S + C - 1 + 1
