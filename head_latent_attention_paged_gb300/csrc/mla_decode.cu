@@ -4,8 +4,9 @@
 // concatenated (request, query token) row sets ("streams").  Per tile:
 //
 //   producer warp : stages the 64 cached rows (576 bf16 each) in shared
-//                   memory once -- TMA tiles for dense pages, 16-byte
-//                   cp.async gathers for sparse top-k rows -- as nine
+//                   memory once -- TMA tiles for dense pages (for sparse
+//                   top-k rows, four gather warps issue 16-byte cp.async
+//                   copies, 16 rows each) -- as nine
 //                   [64 rows x 128 B] chunks in the 128-byte swizzle layout,
 //                   three tiles in flight.  FP8 caches: one bulk copy of the
 //                   tile's 594-byte rows, two tiles in flight, and
@@ -54,10 +55,17 @@ constexpr int kDequantWarps = 6;
 // P(i) is written after S(i) is complete, so every stage carries its own P.
 constexpr int kPChunkOffset = (kChunks - 1) * kChunkBytes;
 
+constexpr int kGatherWarp0 = 6;     // sparse mode: warps 6..9 gather top-k rows
+constexpr int kGatherWarps = 4;
+constexpr int kGatherRows = kTile / kGatherWarps;   // 16 rows per gather warp
+
 template <int kMode>
 struct ModeTraits {
   static constexpr bool kFp8 = kMode == kModeDenseFp8;
-  static constexpr int kThreads = kFp8 ? 32 * (kDequantWarp0 + kDequantWarps) : 192;
+  static constexpr bool kSparse = kMode == kModeSparseBf16;
+  static constexpr int kThreads = kFp8      ? 32 * (kDequantWarp0 + kDequantWarps)
+                                  : kSparse ? 32 * (kGatherWarp0 + kGatherWarps)
+                                            : 192;
   static constexpr int kNumStages = kFp8 ? kFp8Stages : kStages;   // bf16 tiles
 };
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s per wait
@@ -365,7 +373,9 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0) {
     for (int i = 0; i < kNumStages; ++i) {
-      mbar_init(&ctrl->full[i], kMode == kModeSparseBf16 ? 33 : (MT::kFp8 ? kDequantWarps : 1));
+      // sparse: every gather lane's cp.async arrival plus one arrive per warp
+      mbar_init(&ctrl->full[i],
+                MT::kFp8 ? kDequantWarps : (MT::kSparse ? kGatherWarps * 33 : 1));
       mbar_init(&ctrl->empty[i], 1);
     }
     for (int i = 0; i < kRawStages; ++i) {
@@ -430,7 +440,7 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
   const uint32_t tmem = ctrl->tmem_base;
 
   if (ntiles > 0) {
-    if (warp == kProducerWarp) {
+    if (warp == kProducerWarp && !MT::kSparse) {
       // ============================================================ producer
       const uint64_t pol = l2_policy_evict_first();
       Walker wk;
@@ -477,56 +487,6 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
               mbar_arrive(&ctrl->full[stage]);
             }
           }
-        } else if constexpr (kMode == kModeSparseBf16) {
-          const int32_t T = min(max(p.seq_lens[b], 0), max_tokens);
-          const int32_t window = p.causal ? min(max(T - p.q_len + j + 1, 0), T) : T;
-          const int32_t* idx_row =
-              p.topk_idx + static_cast<int64_t>(wk.s) * p.topk_width + wk.lt * kTile;
-          const uint8_t* src[2];
-          bool valid[2];
-          uint32_t bad = 0;
-#pragma unroll
-          for (int k = 0; k < 2; ++k) {
-            const int32_t idx = idx_row[lane + 32 * k];
-            bool v = idx >= 0 && idx < window;
-            if (!v && idx != -1) bad |= MLA_STATUS_BAD_INDEX;
-            int32_t page = -1;
-            if (v) {
-              page = p.block_table[static_cast<int64_t>(b) * p.max_pages + idx / p.page_size];
-              if (page < 0 || page >= p.num_pages) {
-                v = false;
-                bad |= MLA_STATUS_BAD_PAGE;
-              }
-            }
-            valid[k] = v;
-            src[k] = v ? p.kv + (static_cast<int64_t>(page) * p.page_size + idx % p.page_size) *
-                                    (kDqk * 2)
-                       : p.kv;
-          }
-          if (bad) set_status(p.status, bad);
-          const uint32_t lo = __ballot_sync(0xffffffffu, valid[0]);
-          const uint32_t hi = __ballot_sync(0xffffffffu, valid[1]);
-          if (i >= kNumStages && !warp_wait(&ctrl->empty[stage], reuse_parity, abort_flag)) {
-            failed = true;
-            break;
-          }
-          for (int r = 0; r < kTile; ++r) {
-            const uint8_t* s_row = reinterpret_cast<const uint8_t*>(__shfl_sync(
-                0xffffffffu, reinterpret_cast<unsigned long long>(r < 32 ? src[0] : src[1]), r & 31));
-            const uint32_t nbytes = (((r < 32 ? lo : hi) >> (r & 31)) & 1u) ? 16u : 0u;
-#pragma unroll
-            for (int q = 0; q < 3; ++q) {
-              const int piece = lane + 32 * q;   // 16-byte piece of the row, 0..71
-              if (piece < kDqk * 2 / 16) {
-                const int ch = piece >> 3, w16 = piece & 7;
-                cp_async_16(dst + ch * kChunkBytes + r * 128 + ((w16 ^ (r & 7)) << 4),
-                            s_row + piece * 16, nbytes);
-              }
-            }
-          }
-          if (lane == 0) ctrl->mask[stage] = (static_cast<uint64_t>(hi) << 32) | lo;
-          cp_async_mbar_arrive(&ctrl->full[stage]);
-          if (lane == 0) mbar_arrive(&ctrl->full[stage]);
         } else {   // kModeDenseFp8: the tile's FP8 rows, one bulk copy
           const int rs = i % kRawStages;
           uint64_t mask = 0;
@@ -575,7 +535,6 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
         ctrl->abort_flag = 1;
       }
       // drain: everything this warp issued has landed before the CTA exits
-      if constexpr (kMode == kModeSparseBf16) asm volatile("cp.async.wait_all;" ::: "memory");
       if (lane == 0) {
         if constexpr (MT::kFp8) {
           for (int32_t i = max(0, issued - kRawStages); i < issued; ++i)
@@ -738,6 +697,77 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
         set_status(p.status, MLA_STATUS_TIMEOUT);
         ctrl->abort_flag = 1;
       }
+    } else if (MT::kSparse && warp >= kGatherWarp0) {
+      // ============================================================= gather
+      // Gather warp gw stages tile rows [16 gw, 16 gw + 16): lanes 0..15
+      // resolve one top-k slot each (index -> page -> cache row), then the
+      // warp copies the 16 rows as 16-byte cp.async pieces, zero-filling dead
+      // rows, and writes its 16 bits of the tile's live-row mask.
+      const int gw = warp - kGatherWarp0;
+      const uint64_t pol = l2_policy_evict_first();
+      (void)pol;
+      Walker wk;
+      wk.init(prefix, S, g0);
+      bool failed = false;
+      for (int32_t i = 0; i < ntiles; ++i) {
+        const int stage = i % kNumStages;
+        const uint32_t reuse_parity = ((i / kNumStages) - 1) & 1;
+        const int b = wk.s / p.q_len, j = wk.s - b * p.q_len;
+        uint8_t* dst = sStage + stage * kTileBytes;
+        const int32_t T = min(max(p.seq_lens[b], 0), max_tokens);
+        const int32_t window = p.causal ? min(max(T - p.q_len + j + 1, 0), T) : T;
+        const int rl = kGatherRows * gw + (lane & 15);
+        const int32_t idx =
+            p.topk_idx[static_cast<int64_t>(wk.s) * p.topk_width + wk.lt * kTile + rl];
+        bool v = idx >= 0 && idx < window;
+        uint32_t bad = (!v && idx != -1) ? MLA_STATUS_BAD_INDEX : 0u;
+        int32_t page = -1;
+        if (v) {
+          page = p.block_table[static_cast<int64_t>(b) * p.max_pages + idx / p.page_size];
+          if (page < 0 || page >= p.num_pages) {
+            v = false;
+            bad |= MLA_STATUS_BAD_PAGE;
+          }
+        }
+        if (bad && lane < 16) set_status(p.status, bad);
+        const uint8_t* src =
+            v ? p.kv + (static_cast<int64_t>(page) * p.page_size + idx % p.page_size) * (kDqk * 2)
+              : p.kv;
+        const uint32_t live = __ballot_sync(0xffffffffu, v) & 0xFFFFu;
+        if (i >= kNumStages && !warp_wait(&ctrl->empty[stage], reuse_parity, abort_flag)) {
+          failed = true;
+          break;
+        }
+        for (int rr = 0; rr < kGatherRows; ++rr) {
+          const int r = kGatherRows * gw + rr;
+          const uint8_t* s_row = reinterpret_cast<const uint8_t*>(
+              __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(src), rr));
+          const uint32_t nbytes = ((live >> rr) & 1u) ? 16u : 0u;
+#pragma unroll
+          for (int q = 0; q < 3; ++q) {
+            const int piece = lane + 32 * q;   // 16-byte piece of the row, 0..71
+            if (piece < kDqk * 2 / 16) {
+              const int ch = piece >> 3, w16 = piece & 7;
+              cp_async_16(dst + ch * kChunkBytes + r * 128 + ((w16 ^ (r & 7)) << 4),
+                          s_row + piece * 16, nbytes);
+            }
+          }
+        }
+        if (lane == 0)
+          reinterpret_cast<volatile uint16_t*>(&ctrl->mask[stage])[gw] = static_cast<uint16_t>(live);
+        cp_async_mbar_arrive(&ctrl->full[stage]);
+        if (lane == 0) mbar_arrive(&ctrl->full[stage]);
+        wk.next(prefix, S);
+      }
+      if (failed && lane == 0) {
+        set_status(p.status, MLA_STATUS_TIMEOUT);
+        ctrl->abort_flag = 1;
+      }
+      // every copy this warp issued has landed before the CTA exits
+      asm volatile("cp.async.wait_all;" ::: "memory");
+      __syncwarp();
+    } else if (warp == kProducerWarp) {
+      // sparse mode: the gather warps stage the tiles
     } else {
       // ============================================================ softmax
       // Warp w reads TMEM lanes [32w, 32w+32).  Head h is S row 32 + h: in
@@ -992,6 +1022,7 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap* kv_map, int 
       err = cudaFuncSetAttribute(mla_decode_kernel<kModeSparseBf16>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
       if (err != cudaSuccess) return err;
+      block = dim3(ModeTraits<kModeSparseBf16>::kThreads);
       mla_decode_kernel<kModeSparseBf16><<<grid, block, L.total, stream>>>(*kv_map, p, L);
       break;
     case kModeDenseFp8:
