@@ -231,17 +231,6 @@ __device__ __forceinline__ void prefetch_q(const uint16_t* q_hat, int32_t s, int
     asm volatile("prefetch.global.L2 [%0];" ::"l"(base + static_cast<int64_t>(i) * 128));
 }
 
-__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
-}
-
-__device__ __forceinline__ uint32_t lds_u8(uint32_t addr) {
-  uint16_t v;
-  asm volatile("ld.shared.u8 %0, [%1];" : "=h"(v) : "r"(addr));
-  return v;
-}
 
 __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
   uint32_t d;
@@ -290,18 +279,19 @@ __device__ __forceinline__ ScaleX2 e8m0_scale_x2(uint32_t b) {
 }
 
 // Dequantise group g (values 32g .. 32g+31) of one FP8 row in shared memory
-// (row_addr: 2-byte aligned start of the row's 594 bytes) into 4 x 16 bytes
-// of bf16 (8 values each, in dimension order).  Exact: every product is an
-// e4m3 value (4 significant bits) times a power of two.
-__device__ __forceinline__ void dequant_group(uint32_t row_addr, int g, uint4 (&o)[4]) {
-  const uint32_t a = row_addr + 32u * g;
-  const uint32_t a4 = a & ~3u;
-  const bool odd = (a & 2u) != 0;
+// (row: 2-byte aligned start of the row's 594 bytes) into 4 x 16 bytes of
+// bf16 (8 values each, in dimension order).  Exact: every product is an
+// e4m3 value (4 significant bits) times a power of two.  Plain loads, so the
+// compiler may overlap the groups of one thread.
+__device__ __forceinline__ void dequant_group(const uint8_t* row, int g, uint4 (&o)[4]) {
+  const uint8_t* a = row + 32 * g;
+  const uint32_t* a4 = reinterpret_cast<const uint32_t*>(reinterpret_cast<uintptr_t>(a) & ~uintptr_t(3));
+  const bool odd = (reinterpret_cast<uintptr_t>(a) & 2u) != 0;
   uint32_t w[9];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) w[k] = lds_u32(a4 + 4u * k);
-  w[8] = odd ? lds_u32(a4 + 32u) : 0u;
-  const ScaleX2 sc = e8m0_scale_x2(lds_u8(row_addr + kDqk + g));
+  for (int k = 0; k < 8; ++k) w[k] = a4[k];
+  w[8] = odd ? a4[8] : 0u;
+  const ScaleX2 sc = e8m0_scale_x2(row[kDqk + g]);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     uint32_t r[4];
@@ -667,14 +657,14 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
         }
         const uint64_t mask = ctrl->raw_mask[rs];
         const bool live = (mask >> r) & 1ull;
-        const uint32_t row_addr = smem_u32(sRaw + rs * kFp8TileBytes + r * kFp8RowBytes);
+        const uint8_t* row_ptr = sRaw + rs * kFp8TileBytes + r * kFp8RowBytes;
         uint8_t* dst = sStage + bs * kTileBytes + r * 128;
 #pragma unroll 2
         for (int k = 0; k < kDqk / 96; ++k) {
           const int g = gset + 3 * k;
           uint4 o[4];
           if (live) {
-            dequant_group(row_addr, g, o);
+            dequant_group(row_ptr, g, o);
           } else {
 #pragma unroll
             for (int q = 0; q < 4; ++q) o[q] = make_uint4(0, 0, 0, 0);
