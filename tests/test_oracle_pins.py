@@ -421,3 +421,40 @@ def test_generator_structure():
                 assert len(np.unique(live)) == len(live) == min(w.topk, int(b.seq_lens[bi]) - w.q_len + j + 1)
                 assert live.max() <= int(b.seq_lens[bi]) - w.q_len + j
                 assert (row == -1).sum() == w.topk_width - len(live)
+
+
+def test_cache_append_places_rows_and_leaves_the_rest():
+    """The appended row lands at page block_table[b, pos // P], slot pos % P
+    (bf16: bit for bit; FP8: the quantiser's bytes, which dequantise to within
+    half an e4m3 step of each value); every other byte is unchanged; -1 and
+    out-of-range positions or pages append nothing."""
+    from oracle import cache_append as CA
+    rng = np.random.default_rng(5)
+    P, num_pages, B = 64, 12, 5
+    bt = rng.permutation(num_pages)[: B * 2].reshape(B, 2).astype(np.int32)
+    bt[4, 1] = num_pages + 3                      # a page id outside the pool
+    rows = W.f32_to_bf16_bits(rng.standard_normal((B, 576)).astype(np.float32))
+    pos = np.array([0, 63, 64, -1, 100], dtype=np.int32)   # request 4 -> bad page
+    cache = W.f32_to_bf16_bits(rng.standard_normal((num_pages, P, 576)).astype(np.float32))
+    out = CA.append_rows(cache, rows, pos, bt, P, "bf16")
+    written = {(int(bt[0, 0]), 0): 0, (int(bt[1, 0]), 63): 1, (int(bt[2, 1]), 0): 2}
+    for (pg, sl), b in written.items():
+        assert np.array_equal(out[pg, sl], rows[b])
+    mask = np.ones((num_pages, P), dtype=bool)
+    for (pg, sl) in written:
+        mask[pg, sl] = False
+    assert np.array_equal(out[mask], cache[mask])
+    # FP8: same placement, quantised bytes
+    raw = np.zeros((num_pages, P * F.ROW_BYTES), dtype=np.uint8)
+    out8 = CA.append_rows(raw, rows, pos, bt, P, "fp8").reshape(num_pages, P, F.ROW_BYTES)
+    for (pg, sl), b in written.items():
+        got = F.dequant_rows(out8[pg, sl])
+        x = O.bf16_to_f64(rows[b])
+        scale = np.repeat(F.e8m0_to_f64(out8[pg, sl, 576:]), 32)
+        # e4m3 has 3 fraction bits: |error| <= half a step <= 2^-4 * |value| + subnormal step
+        assert np.all(np.abs(got - x) <= np.maximum(np.abs(x) * 2.0 ** -4, scale * 2.0 ** -10))
+        assert np.array_equal(out8[pg, sl], F.quantize_rows(x[None, :])[0])
+    mask8 = np.ones((num_pages, P), dtype=bool)
+    for (pg, sl) in written:
+        mask8[pg, sl] = False
+    assert not out8[mask8].any()
