@@ -37,7 +37,7 @@ MLA_TILE_TOKENS = 64
 EXPORTED = (
     "mla_decode_plan", "mla_q_absorb", "mla_decode_run", "mla_combine", "mla_uv_proj",
     "mla_get_status", "mla_clear_status", "mla_strerror", "mla_version",
-    "mla_decode_run_static",
+    "mla_decode_run_static", "mla_cache_append",
 )
 
 
@@ -89,6 +89,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.mla_combine.argtypes = [P(MlaPlan), vp, vp, vp, vp, vp]
     lib.mla_decode_run_static.argtypes = [P(MlaPlan), vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.mla_uv_proj.argtypes = [vp, vp, vp, i32, i32, vp]
+    lib.mla_cache_append.argtypes = [P(MlaProblem), vp, vp, vp, vp, vp, vp]
     lib.mla_get_status.argtypes = [P(MlaPlan), vp, P(ctypes.c_uint32), vp]
     lib.mla_clear_status.argtypes = [P(MlaPlan), vp, vp]
     lib.mla_strerror.argtypes = [ctypes.c_int]
@@ -176,6 +177,15 @@ def mla_decode_run_static(plan: MlaPlan, q_hat, kv_cache, block_table, seq_lens,
 def mla_combine(plan: MlaPlan, seq_lens, workspace, o_lat, lse, stream=None) -> None:
     _check("mla_combine", load().mla_combine(ctypes.byref(plan), _ptr(seq_lens), _ptr(workspace),
                                              _ptr(o_lat), _ptr(lse), _stream(stream)))
+
+
+def mla_cache_append(problem: MlaProblem, new_rows, positions, block_table, kv_cache,
+                     status=None, stream=None) -> None:
+    """Write row b of new_rows (bf16 [batch][576]) at logical position
+    positions[b] of request b (bf16 copy or on-GPU FP8 quantisation)."""
+    _check("mla_cache_append", load().mla_cache_append(
+        ctypes.byref(problem), _ptr(new_rows), _ptr(positions), _ptr(block_table),
+        _ptr(kv_cache), _ptr(status), _stream(stream)))
 
 
 def mla_uv_proj(o_lat, w_uv, out, rows: int, num_heads: int, stream=None) -> None:

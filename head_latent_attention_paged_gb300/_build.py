@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB_NAME = "libmla_gb300.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
-SOURCES = ["mla_api.cu", "mla_decode.cu", "mla_aux.cu", "mla_static.cu"]
+SOURCES = ["mla_api.cu", "mla_decode.cu", "mla_aux.cu", "mla_static.cu", "mla_append.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
           "--expt-relaxed-constexpr", "-Xptxas", "-v"]

@@ -279,6 +279,32 @@ int mla_uv_proj(const float* o_lat, const void* w_uv, void* out, int32_t rows, i
   return err == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
+int mla_cache_append(const mla_problem* problem, const void* new_rows, const int32_t* positions,
+                     const int32_t* block_table, void* kv_cache, uint32_t* status,
+                     mla_stream_t stream) {
+  const int rc = validate_problem(problem);
+  if (rc != MLA_OK) return rc;
+  if (!new_rows || !positions || !block_table || !kv_cache) return MLA_ERR_INVALID_ARGUMENT;
+  if (!aligned16(new_rows) || !aligned16(kv_cache) ||
+      (reinterpret_cast<uintptr_t>(positions) & 3u) ||
+      (reinterpret_cast<uintptr_t>(block_table) & 3u) ||
+      (status && (reinterpret_cast<uintptr_t>(status) & 3u)))
+    return MLA_ERR_MISALIGNED;
+  AppendParams p;
+  p.new_rows = static_cast<const uint16_t*>(new_rows);
+  p.positions = positions;
+  p.block_table = block_table;
+  p.kv = static_cast<uint8_t*>(kv_cache);
+  p.status = status;
+  p.rows = problem->batch;
+  p.page_size = problem->page_size;
+  p.num_pages = problem->num_pages;
+  p.max_pages = problem->max_pages_per_seq;
+  p.fp8 = problem->kv_dtype == MLA_KV_FP8_E4M3_E8M0 ? 1 : 0;
+  const cudaError_t err = launch_append(p, reinterpret_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
 int mla_get_status(const mla_plan* plan, const void* workspace, uint32_t* bits, mla_stream_t stream) {
   if (!plan || !workspace || !bits) return MLA_ERR_INVALID_ARGUMENT;
   const uint8_t* ws = static_cast<const uint8_t*>(workspace);

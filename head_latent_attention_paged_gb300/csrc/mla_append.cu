@@ -1,0 +1,103 @@
+// Cache append: write each request's newest token row (the shared latent
+// c_kv and the rotated RoPE key, 576 values) into the paged latent cache, as
+// bf16 or in the FP8 layout (576 e4m3 || 18 e8m0 per token) with the
+// quantiser run on the GPU.
+//
+// One warp per row.  FP8: for each 32-value group the warp takes the group's
+// absolute maximum, picks the scale 2^e with e = ceil(log2(amax / 448))
+// (clamped to [-127, 127]; an all-zero group gets e = -127 and zero codes),
+// and converts x / 2^e to e4m3 with round-to-nearest-even and saturation at
+// 448.  Every step is exact for bf16 inputs: amax and the choice of e are
+// read off the float bits, x / 2^e is a power-of-two scaling, and the only
+// rounding is the e4m3 conversion itself.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "mla_internal.h"
+
+namespace mla {
+
+namespace {
+
+constexpr int kAppendWarps = 4;   // rows per block
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// ceil(log2(a / 448)) for a > 0 finite, exactly: a = m 2^E with m in [1, 2),
+// 448 = 1.75 2^8, so a / 448 = (m / 1.75) 2^(E - 8) and m / 1.75 lies in
+// (0.5, 1] unless m > 1.75.  Subnormal a gives a value below -127.
+__device__ __forceinline__ int ceil_log2_over_448(float a) {
+  const uint32_t bits = __float_as_uint(a);
+  const int ef = static_cast<int>((bits >> 23) & 0xFFu);
+  if (ef == 0) return -200;
+  const uint32_t man = bits & 0x7FFFFFu;
+  return (ef - 127) - 8 + (man > 0x600000u ? 1 : 0);
+}
+
+// 2^-e as a float for e in [-127, 127] (2^-127 is the subnormal 0x00400000).
+__device__ __forceinline__ float pow2_neg(int e) {
+  return e == 127 ? __uint_as_float(0x00400000u) : __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+}
+
+// Round-to-nearest-even conversion to e4m3 with saturation at +-448.
+__device__ __forceinline__ uint32_t f32_to_e4m3(float v) {
+  uint16_t two;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %1;" : "=h"(two) : "f"(v));
+  return two & 0xFFu;
+}
+
+__global__ void __launch_bounds__(32 * kAppendWarps) mla_append_kernel(const AppendParams p) {
+  const int lane = threadIdx.x & 31;
+  const int b = blockIdx.x * kAppendWarps + (threadIdx.x >> 5);
+  if (b >= p.rows) return;
+  const int32_t pos = p.positions[b];
+  if (pos < 0) return;   // nothing to append for this request
+  const int64_t max_tokens = static_cast<int64_t>(p.max_pages) * p.page_size;
+  if (pos >= max_tokens) {
+    if (lane == 0 && p.status) atomicOr(p.status, MLA_STATUS_BAD_INDEX);
+    return;
+  }
+  const int32_t page = p.block_table[static_cast<int64_t>(b) * p.max_pages + pos / p.page_size];
+  if (page < 0 || page >= p.num_pages) {
+    if (lane == 0 && p.status) atomicOr(p.status, MLA_STATUS_BAD_PAGE);
+    return;
+  }
+  const int64_t row = static_cast<int64_t>(page) * p.page_size + pos % p.page_size;
+  const uint16_t* src = p.new_rows + static_cast<int64_t>(b) * kDqk;
+  if (!p.fp8) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    uint4* d4 = reinterpret_cast<uint4*>(p.kv + row * (kDqk * 2));
+    for (int i = lane; i < kDqk * 2 / 16; i += 32) d4[i] = s4[i];
+    return;
+  }
+  uint8_t* dst = p.kv + row * kFp8RowBytes;
+  for (int g = 0; g < kDqk / 32; ++g) {
+    const float x = bf16_bits_to_f32(src[32 * g + lane]);
+    float amax = fabsf(x);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    int e = -127;
+    uint32_t code = 0;
+    if (amax > 0.f) {
+      e = max(-127, min(127, ceil_log2_over_448(amax)));
+      code = f32_to_e4m3(x * pow2_neg(e));
+    }
+    dst[32 * g + lane] = static_cast<uint8_t>(code);
+    if (lane == 0) dst[kDqk + g] = static_cast<uint8_t>(e + 127);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_append(const AppendParams& p, cudaStream_t stream) {
+  if (p.rows == 0) return cudaSuccess;
+  const int blocks = (p.rows + kAppendWarps - 1) / kAppendWarps;
+  mla_append_kernel<<<blocks, 32 * kAppendWarps, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -70,6 +70,16 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
 cudaError_t launch_uv_proj_tma(const CUtensorMap* w_map, const float* o_lat, uint16_t* out,
                                int rows, int heads, cudaStream_t stream);
 
+struct AppendParams {
+  const uint16_t* new_rows;     // bf16 [rows][576]
+  const int32_t* positions;     // [rows] token index to write, -1 = none
+  const int32_t* block_table;   // [rows][max_pages]
+  uint8_t* kv;                  // cache base (bytes)
+  uint32_t* status;             // nullable
+  int32_t rows, page_size, num_pages, max_pages, fp8;
+};
+cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
+
 cudaError_t launch_q_absorb(const uint16_t* q_nope, const uint16_t* q_rope,
                             const uint16_t* w_uk, uint16_t* q_hat, int rows, int heads,
                             cudaStream_t stream);

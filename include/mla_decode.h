@@ -192,6 +192,39 @@ MLA_API int mla_combine(const mla_plan* plan, const int32_t* seq_lens, const voi
                 float* o_lat, float* lse, mla_stream_t stream);
 
 /*
+ * mla_cache_append -- write each request's newest token row into the paged
+ * latent cache (the step before decode).  The row is the kv_a projection's
+ * output for that token, [c_kv (512) || k_rope (64)] with the RoPE already
+ * applied ("vllm.models.glm5next.common.model", load_weights: the
+ * kv_a_proj_with_mqa output, fused into fused_qkv_a_proj).  Row b goes to
+ * logical position positions[b] of request b: page
+ * block_table[b][pos / P], slot pos % P.
+ *   problem     : the cache's shape (batch = number of rows, page_size,
+ *                 num_pages, max_pages_per_seq, kv_dtype); other fields as
+ *                 for mla_decode_plan
+ *   new_rows    : bf16 [batch][576], 16-byte aligned
+ *   positions   : device int32 [batch]; -1 appends nothing for that request
+ *   block_table : device int32 [batch][max_pages_per_seq]
+ *   kv_cache    : written in place.  MLA_KV_BF16: the row is stored as is.
+ *                 MLA_KV_FP8_E4M3_E8M0: each 32-value group is quantised on
+ *                 the GPU (GLM-4.7-Flash record, phantomic12
+ *                 inference-research: FP8 latent, one e8m0 scale per 32 e4m3
+ *                 values inlined per token): scale 2^e, e = ceil(log2(amax /
+ *                 448)) clamped to [-127, 127]; values round-to-nearest-even
+ *                 e4m3 of x / 2^e, saturating at 448; an all-zero group gets
+ *                 scale byte 0 and zero codes.
+ *   status      : nullable device uint32; a position past the request's pages
+ *                 sets MLA_STATUS_BAD_INDEX, a page id outside [0, num_pages)
+ *                 MLA_STATUS_BAD_PAGE, and that row is not written.
+ * Rows of one call must go to distinct slots.  Returns MLA_OK,
+ * MLA_ERR_INVALID_ARGUMENT, MLA_ERR_MISALIGNED, MLA_ERR_UNSUPPORTED or
+ * MLA_ERR_CUDA.
+ */
+MLA_API int mla_cache_append(const mla_problem* problem, const void* new_rows,
+                     const int32_t* positions, const int32_t* block_table, void* kv_cache,
+                     uint32_t* status, mla_stream_t stream);
+
+/*
  * mla_uv_proj -- o[r][h] = bf16(W_UV[h]^T o_lat[r][h]) (the kv_b_proj value
  * half applied after attention, in latent space).
  *   o_lat : f32 [rows][num_heads][512];  w_uv : bf16 [num_heads][512][256]

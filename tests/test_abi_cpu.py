@@ -40,6 +40,15 @@ def test_library_exports_every_declared_symbol(m):
     assert declared == set(m.EXPORTED)
 
 
+def test_every_entry_point_has_declared_argument_types(m):
+    """ctypes passes undeclared integer arguments as 32-bit ints, which would
+    cut device pointers: every exported call must declare its argument
+    types."""
+    lib = m.load()
+    for name in m.EXPORTED:
+        assert getattr(lib, name).argtypes is not None, name
+
+
 def test_version_and_strerror(m):
     assert m.version() == 10000
     for code in (0, -1, -2, -3, -4, -5, -99):
@@ -155,6 +164,20 @@ def _first_tile_at(tiles_pre, cost_pre, u):
     k = 0 if off <= STREAM_COST else -(-(off - STREAM_COST) // TILE_COST)
     nt = tiles_pre[s + 1] - tiles_pre[s]
     return int(tiles_pre[s] + k) if k < nt else int(tiles_pre[s + 1])
+
+
+def test_cache_append_rejects_bad_arguments_before_cuda(m):
+    A = 1 << 20    # an aligned fake address: never dereferenced, the call fails first
+    prob = _problem(m)
+    with pytest.raises(m.MlaError) as e:
+        m.mla_cache_append(prob, None, A, A, A)
+    assert e.value.code == -1
+    with pytest.raises(m.MlaError) as e:
+        m.mla_cache_append(prob, A + 8, A, A, A)
+    assert e.value.code == -3
+    with pytest.raises(m.MlaError) as e:
+        m.mla_cache_append(_problem(m, page_size=96), A, A, A, A)
+    assert e.value.code == -2
 
 
 def test_stream_split_matches_kernel_rule():
