@@ -339,29 +339,30 @@ def run_gpu(args, world, rank, local):
     # is device-resident state (as in serving); what a decode step gets from
     # the host is its inputs: the absorbed queries, the block table, the
     # context lengths, the top-k lists (sparse) and each request's newest
-    # cached row (the token just produced, appended at its slot).  Every step
-    # copies those in from pinned host memory, runs the step and reads the
-    # outputs (o and lse) back.
+    # token row, which mla_cache_append writes at its slot.  Every step
+    # copies those in from pinned host memory, appends, runs the step and
+    # reads the outputs (o and lse) back.
     e2e = None
     if args.e2e_steps > 0:
-        row_elems = step.cache.numel() // (step.cache.shape[0] * w.page_size)
-        cache_rows = step.cache.view(step.cache.shape[0] * w.page_size, row_elems)
-        last = []
-        for b_ in range(w.batch):
-            t = int(batch.seq_lens[b_]) - 1
-            if t >= 0:
-                last.append(int(batch.block_table[b_, t // w.page_size]) * w.page_size
-                            + t % w.page_size)
-        new_idx = torch.tensor(last, dtype=torch.int64, device=device)
-        host_rows = cache_rows[new_idx].cpu().pin_memory()
+        from head_latent_attention_paged_gb300 import mla_cache_append
+        # the newest token of each request: a synthetic bf16 row [B][576]
+        # (N(0, 1) like the cache, seeded), appended by the step at position
+        # T_b - 1 with mla_cache_append (an FP8 cache quantises it on the GPU)
+        last_pos = (batch.seq_lens.astype(np.int64) - 1).astype(np.int32)
+        rng = np.random.default_rng(w.seed + 1)
+        rows_np = W.f32_to_bf16_bits(rng.standard_normal((w.batch, 576)).astype(np.float32))
+        host_rows = torch.from_numpy(rows_np.view(np.int16)).pin_memory()
+        host_pos = torch.from_numpy(last_pos).pin_memory()
         dev_rows = torch.empty_like(host_rows, device=device)
+        dev_pos = torch.empty_like(host_pos, device=device)
         host_q = step.q_hat.cpu().pin_memory()
         host_bt = step.block_table.cpu().pin_memory()
         host_seq = step.seq_lens.cpu().pin_memory()
         host_idx = None if step.topk_idx is None else step.topk_idx.cpu().pin_memory()
         out_host = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
         lse_host = torch.empty(step.lse.shape, dtype=step.lse.dtype).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in (host_rows, host_q, host_bt, host_seq)
+        h2d = sum(t.numel() * t.element_size()
+                  for t in (host_rows, host_pos, host_q, host_bt, host_seq)
                   + ((host_idx,) if host_idx is not None else ()))
         d2h = out_host.numel() * out_host.element_size() + lse_host.numel() * lse_host.element_size()
         e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -371,9 +372,11 @@ def run_gpu(args, world, rank, local):
             if k >= 2:
                 e2e_ev[k - 2][0].record(stream)
             dev_rows.copy_(host_rows, non_blocking=True)
-            cache_rows.index_copy_(0, new_idx, dev_rows)
-            step.q_hat.copy_(host_q, non_blocking=True)
+            dev_pos.copy_(host_pos, non_blocking=True)
             step.block_table.copy_(host_bt, non_blocking=True)
+            mla_cache_append(step.problem, dev_rows, dev_pos, step.block_table, step.cache,
+                             stream=stream)
+            step.q_hat.copy_(host_q, non_blocking=True)
             step.seq_lens.copy_(host_seq, non_blocking=True)
             if host_idx is not None:
                 step.topk_idx.copy_(host_idx, non_blocking=True)
@@ -387,8 +390,9 @@ def run_gpu(args, world, rank, local):
         eb, es = aggregate(float(byts) * args.e2e_steps, e2e_s, world, device)
         e2e = {"value": eb / es / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "steps": args.e2e_steps,
-               "inputs": "q_hat, block table, seq_lens, top-k lists, newest cached row per "
-                         "request (cache resident); L2 flushed before each step"}
+               "inputs": "q_hat, block table, seq_lens, top-k lists, newest token row per "
+                         "request (appended with mla_cache_append; cache resident); "
+                         "L2 flushed before each step"}
 
     if rank != 0:
         return 0
