@@ -65,7 +65,8 @@ int validate_problem(const mla_problem* pr) {
   if (pr->kv_lora_rank != kDc || pr->rope_dim != kDr || pr->nope_dim != kDnope ||
       pr->v_head_dim != kDv)
     return MLA_ERR_UNSUPPORTED;
-  if (pr->page_size != 64 && pr->page_size != 128) return MLA_ERR_UNSUPPORTED;
+  if (pr->page_size != 16 && pr->page_size != 32 && pr->page_size != 64 && pr->page_size != 128)
+    return MLA_ERR_UNSUPPORTED;
   if (pr->num_heads > kMaxHeads) return MLA_ERR_UNSUPPORTED;
   if (pr->topk_width % 128 != 0) return MLA_ERR_UNSUPPORTED;
   if (pr->kv_dtype != MLA_KV_BF16 && pr->kv_dtype != MLA_KV_FP8_E4M3_E8M0) return MLA_ERR_UNSUPPORTED;
@@ -216,7 +217,7 @@ int mla_decode_run(const mla_plan* plan, const void* q_hat, const void* kv_cache
   std::memset(&kv_map, 0, sizeof(kv_map));   // FP8 caches are read with bulk copies
   if (mode != kModeDenseFp8 &&
       !make_map_bf16(&kv_map, kv_cache, kDqk, static_cast<uint64_t>(pr.num_pages) * pr.page_size,
-                     kDqk * 2, kChunkElems, kTile))
+                     kDqk * 2, kChunkElems, pr.page_size < kTile ? pr.page_size : kTile))
     return MLA_ERR_CUDA;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   DecodeParams p;

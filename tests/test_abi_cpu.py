@@ -79,7 +79,7 @@ def test_plan_ok_and_workspace_layout(m):
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(page_size=96), -2), (dict(page_size=32), -2), (dict(num_heads=0), -1),
+    (dict(page_size=96), -2), (dict(page_size=8), -2), (dict(page_size=256), -2), (dict(num_heads=0), -1),
     (dict(num_heads=33), -2), (dict(q_len=0), -1), (dict(batch=-1), -1),
     (dict(topk_width=100), -2), (dict(topk_width=-128), -1), (dict(kv_lora_rank=256), -2),
     (dict(rope_dim=32), -2), (dict(v_head_dim=128), -2), (dict(nope_dim=128), -2),
@@ -164,6 +164,16 @@ def _first_tile_at(tiles_pre, cost_pre, u):
     k = 0 if off <= STREAM_COST else -(-(off - STREAM_COST) // TILE_COST)
     nt = tiles_pre[s + 1] - tiles_pre[s]
     return int(tiles_pre[s] + k) if k < nt else int(tiles_pre[s + 1])
+
+
+@pytest.mark.parametrize("page_size", [16, 32, 64, 128])
+def test_plan_accepts_every_supported_page_size(m, page_size):
+    """Pages of 16 and 32 tokens (compressed layers: block_size / compress
+    ratio) as well as 64 and 128."""
+    seq = np.array([100, 1000, 64, 0], dtype=np.int32)
+    plan = m.mla_decode_plan(_problem(m, page_size=page_size, num_pages=4000,
+                                      max_pages_per_seq=1024 // page_size + 1), seq, 152)
+    assert plan.planned_tiles == sum((int(t) + 63) // 64 for t in seq)
 
 
 def test_cache_append_rejects_bad_arguments_before_cuda(m):
