@@ -24,7 +24,8 @@
  * block_table[b][t / P]; P is 64 or 128 (fix: Add glm4_moe_lite to MLA
  * detection, the note that CUTLASS_MLA enforces block_size=128; GLM-4.7-Flash
  * record: decode kernels are instantiated per KV cache page-block size and a
- * planner hard-codes 64).  The call split plan / run mirrors the
+ * planner hard-codes 64), or 16 or 32 for compressed layers (same record:
+ * the page block size block_size / compress_ratio).  The call split plan / run mirrors the
  * planner + kernel split of the FlashInfer MLA decode the record describes.
  *
  * Conventions for every entry point:
@@ -95,7 +96,7 @@ typedef struct {
   int32_t rope_dim;         /* must be 64 */
   int32_t nope_dim;         /* must be 192 (only read by mla_q_absorb) */
   int32_t v_head_dim;       /* must be 256 */
-  int32_t page_size;        /* P: 64 or 128 */
+  int32_t page_size;        /* P: 16, 32, 64 or 128 */
   int32_t num_pages;        /* physical pages in the cache pool */
   int32_t max_pages_per_seq;/* row stride of block_table */
   int32_t kv_dtype;         /* MLA_KV_BF16 or MLA_KV_FP8_E4M3_E8M0 */
