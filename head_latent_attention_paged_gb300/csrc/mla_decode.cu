@@ -144,21 +144,22 @@ __device__ __forceinline__ TilePieces describe_tile(const DecodeParams& p, int b
                                                     int32_t lt, int lane, int32_t max_tokens) {
   TilePieces t;
   const int32_t tok0 = lt * kTile;
-  const int32_t len = stream_len(p.seq_lens[b], p.q_len, j, p.causal, 0, max_tokens);
-  t.nvalid = min(kTile, len - tok0);
   t.rows = min(p.page_size, kTile);
   t.npieces = kTile / t.rows;
   t.slot0 = tok0 % p.page_size;   // 0 unless P > 64
+  // the length and the block-table entry are loaded together (one memory
+  // latency); a piece past the request's last page reads an in-bounds entry
+  // of its row and ignores it
+  const int32_t seq_len = p.seq_lens[b];
   int32_t page = -1;
-  bool live = false, good = false;
   if (lane < t.npieces) {
-    const int32_t tk = tok0 + lane * t.rows;
-    live = tk - tok0 < t.nvalid;   // never read past the request's pages
-    if (live) {
-      page = p.block_table[static_cast<int64_t>(b) * p.max_pages + tk / p.page_size];
-      good = page >= 0 && page < p.num_pages;
-    }
+    const int32_t pi = min((tok0 + lane * t.rows) / p.page_size, p.max_pages - 1);
+    page = p.block_table[static_cast<int64_t>(b) * p.max_pages + pi];
   }
+  const int32_t len = stream_len(seq_len, p.q_len, j, p.causal, 0, max_tokens);
+  t.nvalid = min(kTile, len - tok0);
+  const bool live = lane < t.npieces && lane * t.rows < t.nvalid;
+  const bool good = live && page >= 0 && page < p.num_pages;
   t.ok = __ballot_sync(0xffffffffu, good);
   t.bad = (__ballot_sync(0xffffffffu, live && !good) != 0u) ? MLA_STATUS_BAD_PAGE : 0u;
 #pragma unroll
@@ -493,62 +494,142 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
         uint8_t* dst = sStage + stage * kTileBytes;
         // Describe the tile first: its global lookups overlap the stage wait.
         if constexpr (kMode == kModeDenseBf16) {
-          const TilePieces tp = describe_tile(p, b, j, wk.lt, lane, max_tokens);
-          const uint64_t mask = tile_mask(tp);
-          if (lane == 0 && tp.bad) set_status(p.status, tp.bad);
-          if (i >= kNumStages && !warp_wait(&ctrl->empty[stage], reuse_parity, abort_flag)) {
-            failed = true;
-            break;
-          }
-          if (lane == 0) {
-            ctrl->mask[stage] = mask;
-            if (tp.ok) {
-              // the map's box is one piece (min(P, 64) rows) of one 64-dim chunk
-              mbar_arrive_expect_tx(&ctrl->full[stage],
-                                    __popc(tp.ok) * tp.rows * kChunks * kChunkElems * 2);
-              for (int k = 0; k < tp.npieces; ++k) {
-                if (!((tp.ok >> k) & 1u)) continue;
-                const int32_t row0 = tp.page[k] * p.page_size + tp.slot0;
+          if (p.page_size >= kTile) {
+            // one page holds the whole tile: one lane describes it
+            int32_t row0 = 0;
+            uint64_t mask = 0;
+            bool ok = false;
+            if (lane == 0) {
+              const int32_t tok0 = wk.lt * kTile;
+              const int32_t len = stream_len(p.seq_lens[b], p.q_len, j, p.causal, 0, max_tokens);
+              const int32_t page =
+                  p.block_table[static_cast<int64_t>(b) * p.max_pages + tok0 / p.page_size];
+              const int32_t nvalid = min(kTile, len - tok0);
+              mask = nvalid >= 64 ? ~0ull : ((1ull << nvalid) - 1ull);
+              ok = page >= 0 && page < p.num_pages;
+              if (!ok) {
+                mask = 0;
+                set_status(p.status, MLA_STATUS_BAD_PAGE);
+              }
+              row0 = ok ? page * p.page_size + (tok0 % p.page_size) : 0;
+            }
+            if (i >= kNumStages && !warp_wait(&ctrl->empty[stage], reuse_parity, abort_flag)) {
+              failed = true;
+              break;
+            }
+            if (lane == 0) {
+              ctrl->mask[stage] = mask;
+              if (ok) {
+                mbar_arrive_expect_tx(&ctrl->full[stage], kTileBytes);
 #pragma unroll
                 for (int ch = 0; ch < kChunks; ++ch)
-                  tma_load_2d(dst + ch * kChunkBytes + k * tp.rows * 128, &kv_map,
-                              &ctrl->full[stage], ch * kChunkElems, row0, pol);
+                  tma_load_2d(dst + ch * kChunkBytes, &kv_map, &ctrl->full[stage], ch * kChunkElems,
+                              row0, pol);
+              } else {
+                mbar_arrive(&ctrl->full[stage]);
               }
-            } else {
-              mbar_arrive(&ctrl->full[stage]);
+            }
+          } else {
+            // 16- or 32-token pages: the tile spans 64 / P pages
+            const TilePieces tp = describe_tile(p, b, j, wk.lt, lane, max_tokens);
+            const uint64_t mask = tile_mask(tp);
+            if (lane == 0 && tp.bad) set_status(p.status, tp.bad);
+            if (i >= kNumStages && !warp_wait(&ctrl->empty[stage], reuse_parity, abort_flag)) {
+              failed = true;
+              break;
+            }
+            if (lane == 0) {
+              ctrl->mask[stage] = mask;
+              if (tp.ok) {
+                // the map's box is one piece (P rows) of one 64-dim chunk
+                mbar_arrive_expect_tx(&ctrl->full[stage],
+                                      __popc(tp.ok) * tp.rows * kChunks * kChunkElems * 2);
+                for (int k = 0; k < tp.npieces; ++k) {
+                  if (!((tp.ok >> k) & 1u)) continue;
+                  const int32_t row0 = tp.page[k] * p.page_size + tp.slot0;
+#pragma unroll
+                  for (int ch = 0; ch < kChunks; ++ch)
+                    tma_load_2d(dst + ch * kChunkBytes + k * tp.rows * 128, &kv_map,
+                                &ctrl->full[stage], ch * kChunkElems, row0, pol);
+                }
+              } else {
+                mbar_arrive(&ctrl->full[stage]);
+              }
             }
           }
         } else {   // kModeDenseFp8: the tile's FP8 rows, one bulk copy
           const int rs = i % kRawStages;
-          const TilePieces tp = describe_tile(p, b, j, wk.lt, lane, max_tokens);
-          const uint64_t mask = tile_mask(tp);
-          if (lane == 0 && tp.bad) set_status(p.status, tp.bad);
-          if (i >= kRawStages &&
-              !warp_wait(&ctrl->raw_empty[rs], ((i / kRawStages) - 1) & 1, abort_flag)) {
-            failed = true;
-            break;
-          }
-          if (lane == 0) {
-            ctrl->raw_mask[rs] = mask;
-            if (tp.ok) {
-              // a piece's rows are contiguous in its page; copy the live ones
-              // rounded up to 8 rows (8 x 594 B is a multiple of 16 B)
-              uint32_t total = 0;
-              for (int k = 0; k < tp.npieces; ++k)
-                if ((tp.ok >> k) & 1u)
-                  total += static_cast<uint32_t>((min(tp.rows, tp.nvalid - k * tp.rows) + 7) & ~7);
-              mbar_arrive_expect_tx(&ctrl->raw_full[rs], total * kFp8RowBytes);
-              for (int k = 0; k < tp.npieces; ++k) {
-                if (!((tp.ok >> k) & 1u)) continue;
-                const uint32_t nrows =
-                    static_cast<uint32_t>((min(tp.rows, tp.nvalid - k * tp.rows) + 7) & ~7);
-                const uint8_t* src =
-                    p.kv + (static_cast<int64_t>(tp.page[k]) * p.page_size + tp.slot0) * kFp8RowBytes;
-                bulk_load(sRaw + rs * kFp8TileBytes + k * tp.rows * kFp8RowBytes, src,
-                          nrows * kFp8RowBytes, &ctrl->raw_full[rs], pol);
+          if (p.page_size >= kTile) {
+            // one page holds the whole tile: one lane describes it
+            uint64_t mask = 0;
+            bool ok = false;
+            const uint8_t* src = p.kv;
+            uint32_t bytes = 0;
+            if (lane == 0) {
+              const int32_t tok0 = wk.lt * kTile;
+              const int32_t len = stream_len(p.seq_lens[b], p.q_len, j, p.causal, 0, max_tokens);
+              const int32_t page =
+                  p.block_table[static_cast<int64_t>(b) * p.max_pages + tok0 / p.page_size];
+              const int32_t nvalid = min(kTile, len - tok0);
+              mask = nvalid >= 64 ? ~0ull : ((1ull << nvalid) - 1ull);
+              ok = page >= 0 && page < p.num_pages;
+              if (!ok) {
+                mask = 0;
+                set_status(p.status, MLA_STATUS_BAD_PAGE);
               }
-            } else {
-              mbar_arrive(&ctrl->raw_full[rs]);
+              // rows tok0 .. tok0 + 63 of a page are contiguous; copy the live
+              // ones rounded up to 8 rows (8 x 594 B is a multiple of 16 B)
+              src = p.kv + (static_cast<int64_t>(page) * p.page_size + tok0 % p.page_size) *
+                               kFp8RowBytes;
+              bytes = static_cast<uint32_t>((nvalid + 7) & ~7) * kFp8RowBytes;
+            }
+            if (i >= kRawStages &&
+                !warp_wait(&ctrl->raw_empty[rs], ((i / kRawStages) - 1) & 1, abort_flag)) {
+              failed = true;
+              break;
+            }
+            if (lane == 0) {
+              ctrl->raw_mask[rs] = mask;
+              if (ok) {
+                mbar_arrive_expect_tx(&ctrl->raw_full[rs], bytes);
+                bulk_load(sRaw + rs * kFp8TileBytes, src, bytes, &ctrl->raw_full[rs], pol);
+              } else {
+                mbar_arrive(&ctrl->raw_full[rs]);
+              }
+            }
+          } else {
+            // 16- or 32-token pages: one bulk copy per page piece
+            const TilePieces tp = describe_tile(p, b, j, wk.lt, lane, max_tokens);
+            const uint64_t mask = tile_mask(tp);
+            if (lane == 0 && tp.bad) set_status(p.status, tp.bad);
+            if (i >= kRawStages &&
+                !warp_wait(&ctrl->raw_empty[rs], ((i / kRawStages) - 1) & 1, abort_flag)) {
+              failed = true;
+              break;
+            }
+            if (lane == 0) {
+              ctrl->raw_mask[rs] = mask;
+              if (tp.ok) {
+                // a piece's rows are contiguous in its page; copy the live ones
+                // rounded up to 8 rows (8 x 594 B is a multiple of 16 B)
+                uint32_t total = 0;
+                for (int k = 0; k < tp.npieces; ++k)
+                  if ((tp.ok >> k) & 1u)
+                    total += static_cast<uint32_t>((min(tp.rows, tp.nvalid - k * tp.rows) + 7) & ~7);
+                mbar_arrive_expect_tx(&ctrl->raw_full[rs], total * kFp8RowBytes);
+                for (int k = 0; k < tp.npieces; ++k) {
+                  if (!((tp.ok >> k) & 1u)) continue;
+                  const uint32_t nrows =
+                      static_cast<uint32_t>((min(tp.rows, tp.nvalid - k * tp.rows) + 7) & ~7);
+                  const uint8_t* src =
+                      p.kv + (static_cast<int64_t>(tp.page[k]) * p.page_size + tp.slot0) *
+                                 kFp8RowBytes;
+                  bulk_load(sRaw + rs * kFp8TileBytes + k * tp.rows * kFp8RowBytes, src,
+                            nrows * kFp8RowBytes, &ctrl->raw_full[rs], pol);
+                }
+              } else {
+                mbar_arrive(&ctrl->raw_full[rs]);
+              }
             }
           }
         }
