@@ -15,6 +15,10 @@ i.e. physical page block_table[b, pos // P], slot pos % P.
     2^e with e = ceil(log2(amax / 448)) clamped to [-127, 127], values
     rounded to nearest-even e4m3 of x / 2^e, saturating at 448; an all-zero
     group gets scale byte 0 and zero codes).
+  * FP4 cache (288 bytes of packed e2m1 || 36 e8m0 per token): every
+    16-value group is quantised with oracle.fp4.quantize_rows (e =
+    ceil(log2(amax / 6)) clamped to [-127, 127], values rounded to the nearest
+    e2m1 value with ties to the even code).
 
 A position of -1 appends nothing for that request.  A position outside the
 request's pages or a page id outside the pool appends nothing either (the
@@ -24,6 +28,7 @@ from __future__ import annotations
 
 import numpy as np
 
+from . import fp4 as _fp4
 from . import fp8 as _fp8
 
 D_QK = 576
@@ -34,8 +39,8 @@ def append_rows(cache: np.ndarray, rows_bf16: np.ndarray, positions: np.ndarray,
     """Return a copy of `cache` with row b of `rows_bf16` (uint16 bf16 bits,
     [B, 576]) written at logical position positions[b] of request b.
 
-    cache: bf16 bits uint16 [num_pages, P, 576], or FP8 bytes uint8
-    [num_pages, P * 594]."""
+    cache: bf16 bits uint16 [num_pages, P, 576], FP8 bytes uint8
+    [num_pages, P * 594] or FP4 bytes uint8 [num_pages, P * 324]."""
     out = np.array(cache, copy=True)
     num_pages = out.shape[0]
     max_pages = block_table.shape[1]
@@ -50,6 +55,7 @@ def append_rows(cache: np.ndarray, rows_bf16: np.ndarray, positions: np.ndarray,
             out[page, slot, :] = rows_bf16[b]
         else:
             x = (np.asarray(rows_bf16[b], dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
-            row = _fp8.quantize_rows(x.astype(np.float64)[None, :])[0]
-            out[page, slot * _fp8.ROW_BYTES:(slot + 1) * _fp8.ROW_BYTES] = row
+            enc = _fp4 if kv_dtype == "fp4" else _fp8
+            row = enc.quantize_rows(x.astype(np.float64)[None, :])[0]
+            out[page, slot * enc.ROW_BYTES:(slot + 1) * enc.ROW_BYTES] = row
     return out

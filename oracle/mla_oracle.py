@@ -38,8 +38,8 @@ The visible set of tokens (readings of the pages, stated where they apply):
 Logical position t of request b lives at physical page block_table[b, t // P],
 slot t % P, where P is the page size (64 or 128: fix: Add glm4_moe_lite to MLA
 detection, the note on CUTLASS_MLA enforcing block_size=128; GLM-4.7-Flash
-record, decode kernels "instantiated per KV cache page-block size" and the
-planner that hard-codes 64).
+record: the decode kernels are built per KV-cache page-block size and a
+planner fixes 64).
 
 An independent ABSORBED form (q_lat = W_UK[h] q_nope, scores against the
 576-wide cached row, output accumulated in latent space and up-projected by
@@ -52,6 +52,7 @@ from typing import Iterable, Optional, Sequence
 
 import numpy as np
 
+from . import fp4 as _fp4
 from . import fp8 as _fp8
 
 D_C, D_R, D_NOPE, D_V = 512, 64, 192, 256
@@ -205,11 +206,16 @@ def combine_partials(o_parts: Sequence[np.ndarray], lse_parts: Sequence[np.ndarr
 # ----------------------------------------------------------------------------
 def cache_rows_f64(batch, pages: np.ndarray, slots: np.ndarray) -> np.ndarray:
     """Cached rows [n, 576] in float64 for the given physical locations:
-    bf16 decoded, or FP8 dequantised from the exact bytes the GPU reads
-    (``batch.extra['cache_fp8']``, uint8 [num_pages, P * 594])."""
+    bf16 decoded, or FP8 / FP4 dequantised from the exact bytes the GPU reads
+    (``batch.extra['cache_fp8']``, uint8 [num_pages, P * 594];
+    ``batch.extra['cache_fp4']``, uint8 [num_pages, P * 324])."""
     w = batch.workload
     if w.kv_dtype == "bf16":
         return bf16_to_f64(batch.cache_bf16[pages, slots])
+    if w.kv_dtype == "fp4":
+        raw = batch.extra["cache_fp4"]
+        rows = raw.reshape(raw.shape[0], w.page_size, _fp4.ROW_BYTES)[pages, slots]
+        return _fp4.dequant_rows(rows)
     raw = batch.extra["cache_fp8"]
     rows = raw.reshape(raw.shape[0], w.page_size, _fp8.ROW_BYTES)[pages, slots]
     return _fp8.dequant_rows(rows)

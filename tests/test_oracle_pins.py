@@ -13,6 +13,7 @@ import numpy as np
 import pytest
 
 import oracle as O
+from oracle import fp4 as F4
 from oracle import fp8 as F
 import workloads as W
 
@@ -107,6 +108,76 @@ def test_fp8_quantiser_golden_groups():
     assert scales[1] == 119 and vals[32] == 0x78 and (vals[33:64] == 0).all()
     assert scales[2] == 0 and (vals[64:96] == 0).all()
     assert scales[3] == 128 and vals[96] == 0xFE and (vals[97:128] == 0).all()
+
+
+def test_fp4_codes_golden():
+    g = _golden("fp4_codes.json")
+    for code, val in g["e2m1"]:
+        got = F4.e2m1_to_f64(np.array([code]))[0]
+        assert got == val and math.copysign(1, got) == math.copysign(1, val), code
+    assert F4.ROW_BYTES == g["row_bytes_576"]
+    # the same reading on the 512-value rows of the record gives its 288 bytes
+    assert 512 // 2 + 512 // F4.GROUP == g["row_bytes_512"]
+    pk = g["packing"]
+    packed = F4.pack_codes(np.array(pk["codes"], dtype=np.uint8))
+    assert [int(x) for x in packed] == [int(b, 16) for b in pk["bytes"]]
+    assert list(F4.unpack_codes(packed)) == pk["codes"]
+    for code, val in _golden("fp8_codes.json")["e8m0"]:
+        got = F4.e8m0_to_f64(np.array([_hex(code)], dtype=np.uint8))[0]
+        assert np.isnan(got) if val == "nan" else got == val, code
+
+
+def test_fp4_quantiser_golden_groups():
+    g = _golden("fp4_codes.json")["quantise_groups"]
+    row = np.zeros((1, F4.D_QK))
+    row[0, 0:16] = 6.0                                   # group 0
+    row[0, 16] = 1.0                                     # group 1
+    # group 2 all zero
+    row[0, 48] = -12.0                                   # group 3
+    ties = [float(v) for v in g[4]["group"].split(", ")]
+    row[0, 64:80] = ties                                 # group 4
+    q = F4.quantize_rows(row)[0]
+    codes, scales = F4.unpack_codes(q[:F4.CODE_BYTES]), q[F4.CODE_BYTES:]
+    assert scales[0] == g[0]["scale_byte"] and (codes[0:16] == 7).all()
+    assert scales[1] == g[1]["scale_byte"] and codes[16] == g[1]["first_code"]
+    assert (codes[17:32] == 0).all()
+    assert scales[2] == g[2]["scale_byte"] and (codes[32:48] == 0).all()
+    assert scales[3] == g[3]["scale_byte"] and codes[48] == g[3]["first_code"]
+    assert (codes[49:64] == 0).all()
+    assert scales[4] == g[4]["scale_byte"] and list(codes[64:80]) == g[4]["codes"]
+
+
+def test_fp4_quantiser_brute_force_nearest_code():
+    """Brute force over the 16 codes: each value's code is the one nearest
+    to x / 2**e, ties to the even code; the scale is the smallest power of two
+    that brings the group's amax to 6 or below; the round trip is within half
+    the widest grid step (2**e)."""
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((48, F4.D_QK)) * np.exp(rng.uniform(-8, 8, size=(48, 1)))
+    x[0, :40] = 0.0
+    q = F4.quantize_rows(x)
+    codes = F4.unpack_codes(q[:, :F4.CODE_BYTES]).astype(np.int64)
+    e = q[:, F4.CODE_BYTES:].astype(np.int64) - 127
+    grid = np.array([F4.e2m1_to_f64(np.array([c]))[0] for c in range(16)])
+    for r in range(x.shape[0]):
+        for gi in range(F4.N_GROUPS):
+            xs = x[r, 16 * gi:16 * gi + 16]
+            amax = np.abs(xs).max()
+            if amax == 0:
+                assert e[r, gi] == -127 and (codes[r, 16 * gi:16 * gi + 16] == 0).all()
+                continue
+            k = int(e[r, gi])
+            assert amax / 2.0 ** k <= 6.0 < amax / 2.0 ** (k - 1)
+            for i, v in enumerate(xs / 2.0 ** k):
+                d = np.abs(grid - v)
+                best = [c for c in range(16) if d[c] == d.min()]
+                # the nearest magnitude, its sign from the value
+                cand = [c for c in best if (c >= 8) == (np.signbit(v))] or best
+                want = min(cand, key=lambda c: (c & 1, c))   # ties: even code
+                assert codes[r, 16 * gi + i] == want, (r, gi, i, v)
+    back = F4.dequant_rows(q)
+    bound = np.repeat(2.0 ** e.astype(np.float64), 16, axis=1)
+    assert (np.abs(back - x) <= bound + 1e-300).all()
 
 
 # ---------------------------------------------------------------------------
@@ -405,6 +476,27 @@ def test_fp8_decode_uses_dequantised_bytes():
         assert np.abs(rows - b.latent_f32[pages, slots]).max() < 0.07 * np.abs(rows).max()
 
 
+def test_fp4_decode_uses_dequantised_bytes():
+    """The FP4 path of the driver attends over exactly e2m1 * 2**(s-127) of the
+    stored bytes: equal to the float path on the dequantised rows."""
+    w = W.with_overrides(W.SMALL_WORKLOADS["fp4_small"], batch=2, heads=2, seq_lo=70,
+                         seq_hi=140)
+    b = W.generate(w, fp8_source="float")
+    b.extra["cache_fp4"] = F4.quantize_pages(b.latent_f32, b.slot_valid)
+    got = O.decode(b)
+    raw = b.extra["cache_fp4"].reshape(b.num_pages, w.page_size, F4.ROW_BYTES)
+    for (bi, j), (o, lse, o_lat) in got.items():
+        T = int(b.seq_lens[bi])
+        pages, slots = O.physical_rows(b.block_table[bi], np.arange(T), w.page_size)
+        rows = F4.dequant_rows(raw[pages, slots])
+        ref = O.attend_non_absorbed(O.bf16_to_f64(b.q_nope[bi, j]), O.bf16_to_f64(b.q_rope[bi, j]),
+                                    O.bf16_to_f64(b.w_uk), O.bf16_to_f64(b.w_uv),
+                                    rows[:, :512], rows[:, 512:], w.sm_scale)
+        assert np.allclose(o, ref[0], rtol=1e-13, atol=1e-15)
+        # FP4 keeps one fraction bit: within 2**e of the float latent
+        assert np.abs(rows - b.latent_f32[pages, slots]).max() < 0.35 * np.abs(rows).max()
+
+
 def test_generator_structure():
     """Block tables reference distinct in-range pages; live slots match
     seq_lens; sparse rows hold distinct in-window indices and -1 pads."""
@@ -458,3 +550,12 @@ def test_cache_append_places_rows_and_leaves_the_rest():
     for (pg, sl) in written:
         mask8[pg, sl] = False
     assert not out8[mask8].any()
+    # FP4: same placement, 324-byte rows of the FP4 quantiser
+    raw4 = np.zeros((num_pages, P * F4.ROW_BYTES), dtype=np.uint8)
+    out4 = CA.append_rows(raw4, rows, pos, bt, P, "fp4").reshape(num_pages, P, F4.ROW_BYTES)
+    for (pg, sl), b in written.items():
+        x = O.bf16_to_f64(rows[b])
+        assert np.array_equal(out4[pg, sl], F4.quantize_rows(x[None, :])[0])
+        scale = np.repeat(F4.e8m0_to_f64(out4[pg, sl, F4.CODE_BYTES:]), 16)
+        assert np.all(np.abs(F4.dequant_rows(out4[pg, sl]) - x) <= scale)
+    assert not out4[mask8].any()

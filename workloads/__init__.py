@@ -20,8 +20,14 @@ distributed as round(N(10, 0.75)) clipped to [0, 12] and a uniform 3-bit
 mantissa, the other ~1% are uniform over the codes with exponent field <= 8
 (zeros and subnormals included); scale bytes are uniform in [121, 124]
 (2**-6 .. 2**-3), so live values have magnitudes around 0.5 and at most 7.5,
-like the N(0, 1) bf16 cache.  ``fp8_source="float"`` instead returns a float32 latent for the
-oracle's quantiser (small cases only).
+like the N(0, 1) bf16 cache.  FP4 caches (288 bytes of e2m1 codes, two per
+byte with the even value in the low nibble, then 36 e8m0 scale bytes, one per
+16 values) are drawn the same way: each code's magnitude index 0..7 (values
+0, 0.5, 1, 1.5, 2, 3, 4, 6) with probabilities 12, 22, 20, 16, 14, 9, 5 and 2
+percent and a random sign; scale bytes uniform in [125, 126] (2**-2, 2**-1),
+so live values have magnitudes up to 3.  ``fp8_source="float"`` instead
+returns a float32 latent for the oracle's quantisers (FP8 and FP4; small
+cases only).
 
 Draw order for one workload (one ``numpy.random.default_rng(seed)``):
 seq_lens -> block table -> cache -> q_nope -> q_rope -> W_UK -> W_UV ->
@@ -42,6 +48,8 @@ D_V = 256      # v_head_dim
 N_LAYERS = 47  # GLM-4.7-Flash decoder layers
 FP8_GROUP = 32                      # values per e8m0 scale
 FP8_ROW_BYTES = D_QK + D_QK // FP8_GROUP  # 576 e4m3 + 18 e8m0 = 594
+FP4_GROUP = 16                      # values per e8m0 scale (FP4 reading)
+FP4_ROW_BYTES = D_QK // 2 + D_QK // FP4_GROUP  # 288 packed e2m1 + 36 e8m0 = 324
 
 BF16_NAN = np.uint16(0x7FC0)
 
@@ -84,7 +92,7 @@ class Workload:
     seq_lo: int = 0
     seq_hi: int = 0
     page_size: int = 64
-    kv_dtype: str = "bf16"          # "bf16" | "fp8"
+    kv_dtype: str = "bf16"          # "bf16" | "fp8" | "fp4"
     topk: int = 0                   # 0 = dense
     topk_pad_slots: int = 0         # extra -1 slots (width = topk + pad)
     causal: bool = True             # draft tokens see their prefix only
@@ -98,7 +106,7 @@ class Workload:
 
     @property
     def cache_row_bytes(self) -> int:
-        return 2 * D_QK if self.kv_dtype == "bf16" else FP8_ROW_BYTES
+        return {"bf16": 2 * D_QK, "fp8": FP8_ROW_BYTES, "fp4": FP4_ROW_BYTES}[self.kv_dtype]
 
 
 WORKLOADS = {
@@ -114,6 +122,9 @@ WORKLOADS = {
     # sparse top-2048, q_len 4 causal drafts, context 65536, page 64
     "sparse": Workload("sparse", batch=32, heads=20, q_len=4, seq_lo=65536, seq_hi=65536,
                        page_size=64, topk=2048),
+    # FP4 latent (e2m1 + e8m0 per 16), on the FP8 workload's shape
+    "fp4": Workload("fp4", batch=128, heads=20, seq_lo=2048, seq_hi=16384, page_size=64,
+                    kv_dtype="fp4"),
 }
 
 # Reduced sizes the oracle checks element by element: several tiles and a
@@ -126,6 +137,8 @@ SMALL_WORKLOADS = {
                            page_size=128, seed=2),
     "fp8_small": Workload("fp8_small", batch=4, heads=20, seq_lo=100, seq_hi=900,
                           page_size=64, kv_dtype="fp8", seed=3),
+    "fp4_small": Workload("fp4_small", batch=4, heads=20, seq_lo=100, seq_hi=900,
+                          page_size=64, kv_dtype="fp4", seed=5),
     "sparse_small": Workload("sparse_small", batch=2, heads=20, q_len=4, seq_lo=1500,
                              seq_hi=1500, page_size=64, topk=256, topk_pad_slots=128,
                              seed=4),
@@ -189,6 +202,16 @@ class Batch:
         return self.extra.get("cache_fp8")
 
     @property
+    def cache_fp4(self) -> Optional[np.ndarray]:
+        """uint8 [num_pages, P * 324] FP4 cache bytes, if drawn."""
+        return self.extra.get("cache_fp4")
+
+    @property
+    def cache_quant(self) -> Optional[np.ndarray]:
+        """The FP8 or FP4 cache bytes of a quantised workload."""
+        return self.extra.get("cache_" + self.workload.kv_dtype)
+
+    @property
     def latent_bytes_read(self) -> int:
         """Bytes of cached rows the decode must read (one row per visible token,
         per request for dense; per query token for sparse)."""
@@ -233,6 +256,34 @@ def _fp8_rows(rng: np.random.Generator, n: int, chunk: int = 1 << 16) -> np.ndar
     return out
 
 
+_FP4_MAG_TABLE = np.searchsorted(
+    np.rint(np.cumsum([12, 22, 20, 16, 14, 9, 5, 2]) * 2.56).astype(np.int64),
+    np.arange(256), side="right").clip(0, 7).astype(np.uint8)
+
+
+def _fp4_rows(rng: np.random.Generator, n: int, chunk: int = 1 << 16) -> np.ndarray:
+    """n live FP4 rows (uint8 [n, 324]) drawn as codes, as described above.
+    One random 16-bit word per code: bits 0-7 pick the magnitude index, bit 8
+    the sign."""
+    out = np.empty((n, FP4_ROW_BYTES), dtype=np.uint8)
+    for s in range(0, n, chunk):
+        e = min(n, s + chunk)
+        m = e - s
+        r = rng.integers(0, 1 << 16, size=(m, D_QK), dtype=np.uint32)
+        codes = _FP4_MAG_TABLE[(r & 0xFF).astype(np.uint8)] | (((r >> 8) & 1).astype(np.uint8) << 3)
+        out[s:e, :D_QK // 2] = codes[:, 0::2] | (codes[:, 1::2] << 4)
+        out[s:e, D_QK // 2:] = rng.integers(125, 127, size=(m, D_QK // FP4_GROUP), dtype=np.uint8)
+    return out
+
+
+def _fp4_garbage(rng: np.random.Generator, n: int, garbage: str) -> np.ndarray:
+    if garbage == "nan":     # e8m0 NaN scale bytes make every value NaN
+        return np.full((n, FP4_ROW_BYTES), 0xFF, dtype=np.uint8)
+    out = rng.integers(0, 256, size=(n, FP4_ROW_BYTES), dtype=np.uint8)
+    out[:, D_QK // 2:] = rng.integers(120, 135, size=(n, D_QK // FP4_GROUP), dtype=np.uint8)
+    return out
+
+
 def _fp8_garbage(rng: np.random.Generator, n: int, garbage: str) -> np.ndarray:
     if garbage == "nan":     # e4m3 NaN values, scale byte 0x7F
         return np.full((n, FP8_ROW_BYTES), 0x7F, dtype=np.uint8)
@@ -245,9 +296,9 @@ def _fp8_garbage(rng: np.random.Generator, n: int, garbage: str) -> np.ndarray:
 def generate(w: Workload, garbage: str = "finite", fp8_source: str = "codes") -> Batch:
     """Draw one batch.  ``garbage`` fills slots that hold no live token (tail
     slots of a request's last page and spare pages): "finite" uses bf16 values
-    of magnitude up to 1e4 (FP8: random finite codes with scales up to 2**7),
-    "nan" uses NaN.  ``fp8_source`` ("codes" or "float") is described in the
-    module docstring."""
+    of magnitude up to 1e4 (FP8 and FP4: random finite codes with scales up to
+    2**7), "nan" uses NaN.  ``fp8_source`` ("codes" or "float", for FP8 and
+    FP4 caches) is described in the module docstring."""
     rng = np.random.default_rng(w.seed)
     B, Q, H, P = w.batch, w.q_len, w.heads, w.page_size
     seq_lens = draw_seq_lens(w, rng)
@@ -267,16 +318,18 @@ def generate(w: Workload, garbage: str = "finite", fp8_source: str = "codes") ->
             live = min(P, int(seq_lens[b]) - j * P)
             slot_valid[block_table[b, j], :live] = True
 
-    cache_bf16 = latent_f32 = cache_fp8 = None
+    cache_bf16 = latent_f32 = cache_q = None
     if w.kv_dtype == "bf16":
         cache_bf16 = _normal_bf16(rng, (num_pages, P, D_QK))
     elif fp8_source == "codes":
-        cache_fp8 = _fp8_rows(rng, num_pages * P).reshape(num_pages, P, FP8_ROW_BYTES)
+        draw = _fp8_rows if w.kv_dtype == "fp8" else _fp4_rows
+        cache_q = draw(rng, num_pages * P).reshape(num_pages, P, w.cache_row_bytes)
     else:
         latent_f32 = _normal_f32(rng, (num_pages, P, D_QK))
     inv = ~slot_valid
-    if cache_fp8 is not None and inv.any():
-        cache_fp8[inv] = _fp8_garbage(rng, int(inv.sum()), garbage)
+    if cache_q is not None and inv.any():
+        junk = _fp8_garbage if w.kv_dtype == "fp8" else _fp4_garbage
+        cache_q[inv] = junk(rng, int(inv.sum()), garbage)
     elif inv.any():
         n_inv = int(inv.sum())
         if garbage == "nan":
@@ -314,6 +367,6 @@ def generate(w: Workload, garbage: str = "finite", fp8_source: str = "codes") ->
 
     batch = Batch(w, seq_lens, block_table, num_pages, slot_valid, cache_bf16, latent_f32,
                   q_nope, q_rope, w_uk, w_uv, topk_idx)
-    if cache_fp8 is not None:
-        batch.extra["cache_fp8"] = cache_fp8.reshape(num_pages, P * FP8_ROW_BYTES)
+    if cache_q is not None:
+        batch.extra["cache_" + w.kv_dtype] = cache_q.reshape(num_pages, P * w.cache_row_bytes)
     return batch
