@@ -263,7 +263,8 @@ def run_gpu(args, world, rank, local):
     import torch
     import workloads as W
     import __graft_entry__ as graft
-    from head_latent_attention_paged_gb300 import MLA_KV_BF16, MLA_KV_FP8_E4M3_E8M0
+    from head_latent_attention_paged_gb300 import (MLA_KV_BF16, MLA_KV_FP4_E2M1_E8M0,
+                                                   MLA_KV_FP8_E4M3_E8M0)
     from head_latent_attention_paged_gb300.runner import DecodeStep
 
     torch.cuda.set_device(local)
@@ -274,12 +275,13 @@ def run_gpu(args, world, rank, local):
     graft.build()
     w = W.WORKLOADS[args.workload]
     batch = W.generate(w)
-    fp8 = w.kv_dtype == "fp8"
+    quant = w.kv_dtype in ("fp8", "fp4")
     step = DecodeStep(q_nope=batch.q_nope, q_rope=batch.q_rope, w_uk=batch.w_uk, w_uv=batch.w_uv,
-                      cache=batch.cache_fp8 if fp8 else batch.cache_bf16,
+                      cache=batch.cache_quant if quant else batch.cache_bf16,
                       block_table=batch.block_table, seq_lens=batch.seq_lens,
                       page_size=w.page_size,
-                      kv_dtype=MLA_KV_FP8_E4M3_E8M0 if fp8 else MLA_KV_BF16,
+                      kv_dtype={"bf16": MLA_KV_BF16, "fp8": MLA_KV_FP8_E4M3_E8M0,
+                                "fp4": MLA_KV_FP4_E2M1_E8M0}[w.kv_dtype],
                       topk_idx=batch.topk_idx, causal=w.causal, sm_scale=w.sm_scale,
                       device=device)
     stream = torch.cuda.current_stream(device)
@@ -407,7 +409,8 @@ def run_gpu(args, world, rank, local):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": "fp8-e4m3+e8m0 cache, bf16 tensor-core math" if fp8 else "bf16",
+        "dtype": {"bf16": "bf16", "fp8": "fp8-e4m3+e8m0 cache, bf16 tensor-core math",
+                  "fp4": "fp4-e2m1+e8m0 cache, bf16 tensor-core math"}[w.kv_dtype],
         "data": "synthetic",
         "config": workload_description(w, batch),
         "tokens_per_s_per_layer": w.batch * w.q_len * world / (max_s / args.steps),
@@ -416,8 +419,9 @@ def run_gpu(args, world, rank, local):
                       "decode_timed_steps": len(run_ms)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": traffic,
-                     "kernel": "mla_decode_kernel<%s>" % ("dense fp8" if fp8 else
-                                                          ("sparse bf16" if w.topk else "dense bf16")),
+                     "kernel": "mla_decode_kernel<%s>" % (
+                         "dense " + w.kv_dtype if quant else
+                         ("sparse bf16" if w.topk else "dense bf16")),
                      "peak_source": peak_src,
                      "algorithmic_bytes_per_launch": int(byts)},
         "e2e": e2e,
@@ -443,7 +447,7 @@ def main():
     ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="dense",
-                    choices=["tiny", "dense", "long", "fp8", "sparse"])
+                    choices=["tiny", "dense", "long", "fp8", "sparse", "fp4"])
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-budget", type=float, default=10.0)

@@ -27,6 +27,7 @@ MLA_ERR_CUDA = -5
 
 MLA_KV_BF16 = 0
 MLA_KV_FP8_E4M3_E8M0 = 1
+MLA_KV_FP4_E2M1_E8M0 = 2
 
 MLA_STATUS_BAD_PAGE = 0x1
 MLA_STATUS_BAD_INDEX = 0x2
@@ -182,7 +183,7 @@ def mla_combine(plan: MlaPlan, seq_lens, workspace, o_lat, lse, stream=None) -> 
 def mla_cache_append(problem: MlaProblem, new_rows, positions, block_table, kv_cache,
                      status=None, stream=None) -> None:
     """Write row b of new_rows (bf16 [batch][576]) at logical position
-    positions[b] of request b (bf16 copy or on-GPU FP8 quantisation)."""
+    positions[b] of request b (bf16 copy or on-GPU FP8 / FP4 quantisation)."""
     _check("mla_cache_append", load().mla_cache_append(
         ctypes.byref(problem), _ptr(new_rows), _ptr(positions), _ptr(block_table),
         _ptr(kv_cache), _ptr(status), _stream(stream)))

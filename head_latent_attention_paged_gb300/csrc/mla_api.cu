@@ -53,6 +53,7 @@ bool make_map_bf16(CUtensorMap* map, const void* base, uint64_t cols, uint64_t r
 
 int decode_mode(const mla_problem& pr) {
   if (pr.kv_dtype == MLA_KV_FP8_E4M3_E8M0) return kModeDenseFp8;
+  if (pr.kv_dtype == MLA_KV_FP4_E2M1_E8M0) return kModeDenseFp4;
   return pr.topk_width > 0 ? kModeSparseBf16 : kModeDenseBf16;
 }
 
@@ -69,8 +70,10 @@ int validate_problem(const mla_problem* pr) {
     return MLA_ERR_UNSUPPORTED;
   if (pr->num_heads > kMaxHeads) return MLA_ERR_UNSUPPORTED;
   if (pr->topk_width % 128 != 0) return MLA_ERR_UNSUPPORTED;
-  if (pr->kv_dtype != MLA_KV_BF16 && pr->kv_dtype != MLA_KV_FP8_E4M3_E8M0) return MLA_ERR_UNSUPPORTED;
-  if (pr->kv_dtype == MLA_KV_FP8_E4M3_E8M0 && pr->topk_width > 0) return MLA_ERR_UNSUPPORTED;
+  if (pr->kv_dtype != MLA_KV_BF16 && pr->kv_dtype != MLA_KV_FP8_E4M3_E8M0 &&
+      pr->kv_dtype != MLA_KV_FP4_E2M1_E8M0)
+    return MLA_ERR_UNSUPPORTED;
+  if (pr->kv_dtype != MLA_KV_BF16 && pr->topk_width > 0) return MLA_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(pr->batch) * pr->q_len > kMaxStreams) return MLA_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(pr->num_pages) * pr->page_size > INT32_MAX) return MLA_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(pr->max_pages_per_seq) * pr->page_size > INT32_MAX) return MLA_ERR_UNSUPPORTED;
@@ -214,8 +217,8 @@ int mla_decode_run(const mla_plan* plan, const void* q_hat, const void* kv_cache
   if (plan->num_streams == 0) return MLA_OK;
   const int mode = decode_mode(pr);
   CUtensorMap kv_map;
-  std::memset(&kv_map, 0, sizeof(kv_map));   // FP8 caches are read with bulk copies
-  if (mode != kModeDenseFp8 &&
+  std::memset(&kv_map, 0, sizeof(kv_map));   // FP8 / FP4 caches are read with bulk copies
+  if (mode != kModeDenseFp8 && mode != kModeDenseFp4 &&
       !make_map_bf16(&kv_map, kv_cache, kDqk, static_cast<uint64_t>(pr.num_pages) * pr.page_size,
                      kDqk * 2, kChunkElems, pr.page_size < kTile ? pr.page_size : kTile))
     return MLA_ERR_CUDA;
@@ -301,7 +304,7 @@ int mla_cache_append(const mla_problem* problem, const void* new_rows, const int
   p.page_size = problem->page_size;
   p.num_pages = problem->num_pages;
   p.max_pages = problem->max_pages_per_seq;
-  p.fp8 = problem->kv_dtype == MLA_KV_FP8_E4M3_E8M0 ? 1 : 0;
+  p.kv_dtype = problem->kv_dtype;
   const cudaError_t err = launch_append(p, reinterpret_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }

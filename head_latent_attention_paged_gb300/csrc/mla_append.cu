@@ -1,7 +1,8 @@
 // Cache append: write each request's newest token row (the shared latent
 // c_kv and the rotated RoPE key, 576 values) into the paged latent cache, as
-// bf16 or in the FP8 layout (576 e4m3 || 18 e8m0 per token) with the
-// quantiser run on the GPU.
+// bf16, in the FP8 layout (576 e4m3 || 18 e8m0 per token) or in the FP4
+// layout (288 bytes of packed e2m1 || 36 e8m0 per token) with the quantiser
+// run on the GPU.
 //
 // One warp per row.  FP8: for each 32-value group the warp takes the group's
 // absolute maximum, picks the scale 2^e with e = ceil(log2(amax / 448))
@@ -10,6 +11,10 @@
 // 448.  Every step is exact for bf16 inputs: amax and the choice of e are
 // read off the float bits, x / 2^e is a power-of-two scaling, and the only
 // rounding is the e4m3 conversion itself.
+//
+// FP4: the same with 16-value groups, e = ceil(log2(amax / 6)) and the
+// nearest e2m1 value (ties to the even code, saturating at 6) of x / 2^e;
+// value 2i goes to the low nibble of code byte i.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -36,6 +41,28 @@ __device__ __forceinline__ int ceil_log2_over_448(float a) {
   if (ef == 0) return -200;
   const uint32_t man = bits & 0x7FFFFFu;
   return (ef - 127) - 8 + (man > 0x600000u ? 1 : 0);
+}
+
+// ceil(log2(a / 6)) for a > 0 finite, exactly: 6 = 1.5 2^2, so a / 6 =
+// (m / 1.5) 2^(E - 2) with m / 1.5 in [2/3, 1] unless m > 1.5.
+__device__ __forceinline__ int ceil_log2_over_6(float a) {
+  const uint32_t bits = __float_as_uint(a);
+  const int ef = static_cast<int>((bits >> 23) & 0xFFu);
+  if (ef == 0) return -200;
+  const uint32_t man = bits & 0x7FFFFFu;
+  return (ef - 127) - 2 + (man > 0x400000u ? 1 : 0);
+}
+
+// Nearest e2m1 code of v (magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6), ties to
+// the even code, saturating at 6; the sign bit of v becomes bit 3.  Each
+// comparison moves past one midpoint of the grid: a midpoint between an
+// even and the next odd code counts only when exceeded, one between an odd
+// and the next even code already when reached.
+__device__ __forceinline__ uint32_t f32_to_e2m1(float v) {
+  const float a = fabsf(v);
+  const uint32_t mag = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) +
+                       (a >= 3.5f) + (a > 5.0f);
+  return mag | ((__float_as_uint(v) >> 28) & 8u);
 }
 
 // 2^-e as a float for e in [-127, 127] (2^-127 is the subnormal 0x00400000).
@@ -68,10 +95,31 @@ __global__ void __launch_bounds__(32 * kAppendWarps) mla_append_kernel(const App
   }
   const int64_t row = static_cast<int64_t>(page) * p.page_size + pos % p.page_size;
   const uint16_t* src = p.new_rows + static_cast<int64_t>(b) * kDqk;
-  if (!p.fp8) {
+  if (p.kv_dtype == MLA_KV_BF16) {
     const uint4* s4 = reinterpret_cast<const uint4*>(src);
     uint4* d4 = reinterpret_cast<uint4*>(p.kv + row * (kDqk * 2));
     for (int i = lane; i < kDqk * 2 / 16; i += 32) d4[i] = s4[i];
+    return;
+  }
+  if (p.kv_dtype == MLA_KV_FP4_E2M1_E8M0) {
+    // each pass covers 32 values: lanes 0-15 one 16-value group, 16-31 the next
+    uint8_t* dst = p.kv + row * kFp4RowBytes;
+    for (int it = 0; it < kDqk / 32; ++it) {
+      const int g = 2 * it + (lane >> 4);
+      const float x = bf16_bits_to_f32(src[32 * it + lane]);
+      float amax = fabsf(x);
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      int e = -127;
+      uint32_t code = 0;
+      if (amax > 0.f) {
+        e = max(-127, min(127, ceil_log2_over_6(amax)));
+        code = f32_to_e2m1(x * pow2_neg(e));
+      }
+      const uint32_t hi = __shfl_down_sync(0xffffffffu, code, 1);
+      if ((lane & 1) == 0) dst[16 * it + (lane >> 1)] = static_cast<uint8_t>(code | (hi << 4));
+      if ((lane & 15) == 0) dst[kFp4CodeBytes + g] = static_cast<uint8_t>(e + 127);
+    }
     return;
   }
   uint8_t* dst = p.kv + row * kFp8RowBytes;

@@ -62,11 +62,15 @@ constexpr int kGatherRows = kTile / kGatherWarps;   // 16 rows per gather warp
 template <int kMode>
 struct ModeTraits {
   static constexpr bool kFp8 = kMode == kModeDenseFp8;
+  static constexpr bool kFp4 = kMode == kModeDenseFp4;
+  static constexpr bool kQuant = kFp8 || kFp4;   // quantised bytes, dequantised in the CTA
+  static constexpr int kRowBytes = kFp4 ? kFp4RowBytes : kFp8RowBytes;    // quantised row
+  static constexpr int kRawTileBytes = kTile * kRowBytes;
   static constexpr bool kSparse = kMode == kModeSparseBf16;
-  static constexpr int kThreads = kFp8      ? 32 * (kDequantWarp0 + kDequantWarps)
+  static constexpr int kThreads = kQuant    ? 32 * (kDequantWarp0 + kDequantWarps)
                                   : kSparse ? 32 * (kGatherWarp0 + kGatherWarps)
                                             : 192;
-  static constexpr int kNumStages = kFp8 ? kFp8Stages : kStages;   // bf16 tiles
+  static constexpr int kNumStages = kQuant ? kFp8Stages : kStages;   // bf16 tiles
 };
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s per wait
 constexpr float kRescaleThreshold = 8.0f;           // log2 units: rescale if max grows > 2^8
@@ -302,25 +306,28 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2_scaled(uint32_t four, int h
   return (sx << 4) & 0x87F087F0u;
 }
 
-// bf16x2 multiplier that, applied after the placement above, gives
-// value * 2^(b - 127) for an e8m0 byte b: 2^(b - 7) when it is a normal bf16
-// (b <= 134), split in two factors beyond; NaN for b = 255.
+// bf16x2 multiplier that, applied to a code placed as value * 2^-kPlace
+// (kPlace = 120 for e4m3 above, 126 for e2m1 below), gives value *
+// 2^(b - 127) for an e8m0 byte b: the factor 2^(b - 127 + kPlace) when it is
+// a normal bf16 (b + kPlace <= 254), split in two factors (2^127 and the
+// rest) beyond; NaN for b = 255.
 struct ScaleX2 {
   uint32_t f1, f2;
   bool two;
 };
+template <uint32_t kPlace>
 __device__ __forceinline__ ScaleX2 e8m0_scale_x2(uint32_t b) {
   ScaleX2 sc;
   if (b == 255u) {
     sc.f1 = 0x7FC07FC0u;
     sc.two = false;
-  } else if (b <= 134u) {
-    const uint32_t e = (b + 120u) << 7;      // 2^(b - 7), b + 120 in [120, 254]
+  } else if (b + kPlace <= 254u) {
+    const uint32_t e = (b + kPlace) << 7;    // bf16 exponent field of 2^(b - 127 + kPlace)
     sc.f1 = e | (e << 16);
     sc.two = false;
   } else {
     sc.f1 = 0x7F007F00u;                     // 2^127
-    const uint32_t e = (b - 7u) << 7;        // 2^(b - 134), b - 7 in [128, 247]
+    const uint32_t e = (b + kPlace - 127u) << 7;   // the remaining power, field in [1, 253]
     sc.f2 = e | (e << 16);
     sc.two = true;
   }
@@ -341,7 +348,7 @@ __device__ __forceinline__ void dequant_group(const uint8_t* row, int g, uint4 (
 #pragma unroll
   for (int k = 0; k < 8; ++k) w[k] = a4[k];
   w[8] = odd ? a4[8] : 0u;
-  const ScaleX2 sc = e8m0_scale_x2(row[kDqk + g]);
+  const ScaleX2 sc = e8m0_scale_x2<120u>(row[kDqk + g]);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     uint32_t r[4];
@@ -362,17 +369,60 @@ __device__ __forceinline__ void dequant_group(const uint8_t* row, int g, uint4 (
   }
 }
 
+// Eight e2m1 codes (one 32-bit word, value 2i in the low nibble of byte i)
+// as four bf16x2 words holding value * 2^-126, exactly.  An e2m1 code
+// s.ee.m placed as the bf16 s.000000ee.m000000 (bits 15, 8-7, 6) has value
+// 2^(e-127) (1 + m/2) for e > 0, which is 2^-126 times the e2m1 value
+// 2^(e-1) (1 + m/2); for e = 0 the bf16 is subnormal, (m/2) 2^-126, against
+// the e2m1 subnormal m/2: again a factor 2^-126.  The byte permute puts the
+// codes of values 2k and 2k+1 in the low nibbles of the two 16-bit halves
+// (selector bit 3 replicates the top bit of a byte that is 0 after the
+// mask, giving a zero byte).
+__device__ __forceinline__ void e2m1x8_to_bf16x2_scaled(uint32_t w, uint32_t (&r)[4]) {
+  const uint32_t even = w & 0x0F0F0F0Fu;          // values 0, 2, 4, 6
+  const uint32_t odd = (w >> 4) & 0x0F0F0F0Fu;    // values 1, 3, 5, 7
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    uint32_t v;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(v) : "r"(even), "r"(odd), "r"(0xC480u + 0x1111u * k));
+    r[k] = ((v & 0x00080008u) << 12) | ((v & 0x00070007u) << 6);
+  }
+}
+
+// Dequantise group g (values 16g .. 16g+15) of one FP4 row in shared memory
+// (row: 4-byte aligned start of the row's 324 bytes) into 2 x 16 bytes of
+// bf16 in dimension order.  Exact: every product is an e2m1 value (2
+// significant bits) times a power of two.
+__device__ __forceinline__ void dequant_group_fp4(const uint8_t* row, int g, uint4 (&o)[2]) {
+  const uint32_t* a4 = reinterpret_cast<const uint32_t*>(row + 8 * g);
+  const uint32_t w0 = a4[0], w1 = a4[1];
+  const ScaleX2 sc = e8m0_scale_x2<126u>(row[kFp4CodeBytes + g]);
+  uint32_t r[2][4];
+  e2m1x8_to_bf16x2_scaled(w0, r[0]);
+  e2m1x8_to_bf16x2_scaled(w1, r[1]);
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      r[q][k] = bf16x2_mul(r[q][k], sc.f1);
+      if (sc.two) r[q][k] = bf16x2_mul(r[q][k], sc.f2);
+    }
+    o[q] = make_uint4(r[q][0], r[q][1], r[q][2], r[q][3]);
+  }
+}
+
 }  // namespace
 
 DecodeLayout decode_layout(int heads, int heads_pad, int num_streams, int mode) {
   (void)heads;
-  const bool fp8 = mode == kModeDenseFp8;
+  const bool quant = mode == kModeDenseFp8 || mode == kModeDenseFp4;
+  const int raw_tile = mode == kModeDenseFp4 ? kFp4TileBytes : kFp8TileBytes;
   DecodeLayout L;
   L.off_stage = 0;
-  L.off_raw = (fp8 ? kFp8Stages : kStages) * kTileBytes;
+  L.off_raw = (quant ? kFp8Stages : kStages) * kTileBytes;
   (void)heads_pad;
   L.off_p = L.off_stage + kPChunkOffset;     // first stage's P; stride kTileBytes
-  L.off_ctrl = L.off_raw + (fp8 ? kRawStages * kFp8TileBytes : 0);
+  L.off_ctrl = L.off_raw + (quant ? kRawStages * raw_tile : 0);
   L.total = L.off_ctrl + static_cast<int>(sizeof(Ctrl)) + 2 * (num_streams + 1) * 4;
   return L;
 }
@@ -415,7 +465,7 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
     for (int i = 0; i < kNumStages; ++i) {
       // sparse: every gather lane's cp.async arrival plus one arrive per warp
       mbar_init(&ctrl->full[i],
-                MT::kFp8 ? kDequantWarps : (MT::kSparse ? kGatherWarps * 33 : 1));
+                MT::kQuant ? kDequantWarps : (MT::kSparse ? kGatherWarps * 33 : 1));
       mbar_init(&ctrl->empty[i], 1);
     }
     for (int i = 0; i < kRawStages; ++i) {
@@ -557,7 +607,7 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
               }
             }
           }
-        } else {   // kModeDenseFp8: the tile's FP8 rows, one bulk copy
+        } else {   // FP8 / FP4 caches: the tile's quantised rows, one bulk copy
           const int rs = i % kRawStages;
           if (p.page_size >= kTile) {
             // one page holds the whole tile: one lane describes it
@@ -578,10 +628,11 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
                 set_status(p.status, MLA_STATUS_BAD_PAGE);
               }
               // rows tok0 .. tok0 + 63 of a page are contiguous; copy the live
-              // ones rounded up to 8 rows (8 x 594 B is a multiple of 16 B)
+              // ones rounded up to 8 rows (8 rows of 594 or 324 bytes are a
+              // multiple of 16 B)
               src = p.kv + (static_cast<int64_t>(page) * p.page_size + tok0 % p.page_size) *
-                               kFp8RowBytes;
-              bytes = static_cast<uint32_t>((nvalid + 7) & ~7) * kFp8RowBytes;
+                               MT::kRowBytes;
+              bytes = static_cast<uint32_t>((nvalid + 7) & ~7) * MT::kRowBytes;
             }
             if (i >= kRawStages &&
                 !warp_wait(&ctrl->raw_empty[rs], ((i / kRawStages) - 1) & 1, abort_flag)) {
@@ -592,7 +643,7 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
               ctrl->raw_mask[rs] = mask;
               if (ok) {
                 mbar_arrive_expect_tx(&ctrl->raw_full[rs], bytes);
-                bulk_load(sRaw + rs * kFp8TileBytes, src, bytes, &ctrl->raw_full[rs], pol);
+                bulk_load(sRaw + rs * MT::kRawTileBytes, src, bytes, &ctrl->raw_full[rs], pol);
               } else {
                 mbar_arrive(&ctrl->raw_full[rs]);
               }
@@ -611,21 +662,21 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
               ctrl->raw_mask[rs] = mask;
               if (tp.ok) {
                 // a piece's rows are contiguous in its page; copy the live ones
-                // rounded up to 8 rows (8 x 594 B is a multiple of 16 B)
+                // rounded up to 8 rows (a multiple of 16 B)
                 uint32_t total = 0;
                 for (int k = 0; k < tp.npieces; ++k)
                   if ((tp.ok >> k) & 1u)
                     total += static_cast<uint32_t>((min(tp.rows, tp.nvalid - k * tp.rows) + 7) & ~7);
-                mbar_arrive_expect_tx(&ctrl->raw_full[rs], total * kFp8RowBytes);
+                mbar_arrive_expect_tx(&ctrl->raw_full[rs], total * MT::kRowBytes);
                 for (int k = 0; k < tp.npieces; ++k) {
                   if (!((tp.ok >> k) & 1u)) continue;
                   const uint32_t nrows =
                       static_cast<uint32_t>((min(tp.rows, tp.nvalid - k * tp.rows) + 7) & ~7);
                   const uint8_t* src =
                       p.kv + (static_cast<int64_t>(tp.page[k]) * p.page_size + tp.slot0) *
-                                 kFp8RowBytes;
-                  bulk_load(sRaw + rs * kFp8TileBytes + k * tp.rows * kFp8RowBytes, src,
-                            nrows * kFp8RowBytes, &ctrl->raw_full[rs], pol);
+                                 MT::kRowBytes;
+                  bulk_load(sRaw + rs * MT::kRawTileBytes + k * tp.rows * MT::kRowBytes, src,
+                            nrows * MT::kRowBytes, &ctrl->raw_full[rs], pol);
                 }
               } else {
                 mbar_arrive(&ctrl->raw_full[rs]);
@@ -643,7 +694,7 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
       }
       // drain: everything this warp issued has landed before the CTA exits
       if (lane == 0) {
-        if constexpr (MT::kFp8) {
+        if constexpr (MT::kQuant) {
           for (int32_t i = max(0, issued - kRawStages); i < issued; ++i)
             (void)mbar_wait(&ctrl->raw_full[i % kRawStages], (i / kRawStages) & 1, nullptr,
                             kWaitLimitNs);
@@ -754,11 +805,12 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
         (void)mbar_wait(&ctrl->mma_drain, 0, nullptr, kWaitLimitNs);
       }
       __syncwarp();
-    } else if (MT::kFp8 && warp >= kDequantWarp0) {
+    } else if (MT::kQuant && warp >= kDequantWarp0) {
       // ============================================================ dequant
       // Thread t of the 192 owns row t % 64 and groups t / 64 + 3k: a warp
-      // covers 32 consecutive rows, so its shared loads (row stride 594 B)
-      // and its swizzled 16-byte stores spread over the banks.
+      // covers 32 consecutive rows, so its shared loads (row stride 594 B or
+      // 324 B: an odd number of words apart, or 81 words) and its swizzled
+      // 16-byte stores spread over the banks.
       const int dt = tid - kDequantWarp0 * 32;
       const int r = dt & 63;
       const int gset = dt >> 6;
@@ -774,23 +826,44 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
         }
         const uint64_t mask = ctrl->raw_mask[rs];
         const bool live = (mask >> r) & 1ull;
-        const uint8_t* row_ptr = sRaw + rs * kFp8TileBytes + r * kFp8RowBytes;
+        const uint8_t* row_ptr = sRaw + rs * MT::kRawTileBytes + r * MT::kRowBytes;
         uint8_t* dst = sStage + bs * kTileBytes + r * 128;
-#pragma unroll 2
-        for (int k = 0; k < kDqk / 96; ++k) {
-          const int g = gset + 3 * k;
-          uint4 o[4];
-          if (live) {
-            dequant_group(row_ptr, g, o);
-          } else {
+        if constexpr (MT::kFp4) {
+          // 36 groups of 16 values (32 bf16 bytes, two 16-byte units each)
+#pragma unroll 4
+          for (int k = 0; k < kDqk / 48; ++k) {
+            const int g = gset + 3 * k;
+            uint4 o[2];
+            if (live) {
+              dequant_group_fp4(row_ptr, g, o);
+            } else {
+              o[0] = make_uint4(0, 0, 0, 0);
+              o[1] = o[0];
+            }
+            const int u0 = (g & 3) * 2;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) o[q] = make_uint4(0, 0, 0, 0);
+            for (int q = 0; q < 2; ++q)
+              *reinterpret_cast<uint4*>(dst + (g >> 2) * kChunkBytes +
+                                        (((u0 + q) ^ (r & 7)) << 4)) = o[q];
           }
-          const int u0 = (g & 1) * 4;
+        } else {
+          // 18 groups of 32 values (64 bf16 bytes, four 16-byte units each)
+#pragma unroll 2
+          for (int k = 0; k < kDqk / 96; ++k) {
+            const int g = gset + 3 * k;
+            uint4 o[4];
+            if (live) {
+              dequant_group(row_ptr, g, o);
+            } else {
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<uint4*>(dst + (g >> 1) * kChunkBytes + (((u0 + q) ^ (r & 7)) << 4)) =
-                o[q];
+              for (int q = 0; q < 4; ++q) o[q] = make_uint4(0, 0, 0, 0);
+            }
+            const int u0 = (g & 1) * 4;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              *reinterpret_cast<uint4*>(dst + (g >> 1) * kChunkBytes +
+                                        (((u0 + q) ^ (r & 7)) << 4)) = o[q];
+          }
         }
         if (dt == 0) ctrl->mask[bs] = mask;
         fence_proxy_async_smem();   // generic stores -> tensor-core reads
@@ -1138,6 +1211,13 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap* kv_map, int 
       if (err != cudaSuccess) return err;
       block = dim3(ModeTraits<kModeDenseFp8>::kThreads);
       mla_decode_kernel<kModeDenseFp8><<<grid, block, L.total, stream>>>(*kv_map, p, L);
+      break;
+    case kModeDenseFp4:
+      err = cudaFuncSetAttribute(mla_decode_kernel<kModeDenseFp4>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
+      if (err != cudaSuccess) return err;
+      block = dim3(ModeTraits<kModeDenseFp4>::kThreads);
+      mla_decode_kernel<kModeDenseFp4><<<grid, block, L.total, stream>>>(*kv_map, p, L);
       break;
     default:
       return cudaErrorInvalidValue;

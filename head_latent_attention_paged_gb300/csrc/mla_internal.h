@@ -20,14 +20,22 @@ constexpr int kChunks = kDqk / kChunkElems;  // 9
 constexpr int kChunkBytes = kTile * 128;     // 8 KB: 64 rows x 128 B
 constexpr int kTileBytes = kChunks * kChunkBytes;  // 73,728
 constexpr int kFp8RowBytes = kDqk + kDqk / 32;     // 594
+constexpr int kFp4CodeBytes = kDqk / 2;            // 288: two e2m1 codes per byte
+constexpr int kFp4RowBytes = kFp4CodeBytes + kDqk / 16;   // 324
 constexpr int kMaxHeads = 32;     // TMEM: q_hat 288 + S 64 + O^T 4 x 32 columns
 constexpr int kMaxStreams = 256;  // per-stream tile prefix kept in shared memory
 constexpr int kStages = 3;        // 72 KB tiles in flight per CTA (bf16 caches)
 constexpr int kFp8TileBytes = kTile * kFp8RowBytes;  // 38,016: one tile of FP8 rows
-constexpr int kFp8Stages = 2;     // dequantised bf16 tiles in flight (FP8 caches)
-constexpr int kRawStages = 2;     // FP8 byte tiles in flight (FP8 caches)
+constexpr int kFp4TileBytes = kTile * kFp4RowBytes;  // 20,736: one tile of FP4 rows
+constexpr int kFp8Stages = 2;     // dequantised bf16 tiles in flight (FP8 / FP4 caches)
+constexpr int kRawStages = 2;     // quantised byte tiles in flight (FP8 / FP4 caches)
 
-enum DecodeMode : int { kModeDenseBf16 = 0, kModeSparseBf16 = 1, kModeDenseFp8 = 2 };
+enum DecodeMode : int {
+  kModeDenseBf16 = 0,
+  kModeSparseBf16 = 1,
+  kModeDenseFp8 = 2,
+  kModeDenseFp4 = 3,
+};
 
 struct DecodeParams {
   const uint16_t* q_hat;        // bf16 [S][H][576]
@@ -76,7 +84,8 @@ struct AppendParams {
   const int32_t* block_table;   // [rows][max_pages]
   uint8_t* kv;                  // cache base (bytes)
   uint32_t* status;             // nullable
-  int32_t rows, page_size, num_pages, max_pages, fp8;
+  int32_t rows, page_size, num_pages, max_pages;
+  int32_t kv_dtype;             // MLA_KV_BF16, MLA_KV_FP8_E4M3_E8M0 or MLA_KV_FP4_E2M1_E8M0
 };
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
 

@@ -7,7 +7,7 @@ from typing import Optional
 import numpy as np
 import torch
 
-from . import (MLA_KV_BF16, MLA_KV_FP8_E4M3_E8M0, make_problem, mla_clear_status, mla_combine,
+from . import (MLA_KV_BF16, MLA_KV_FP4_E2M1_E8M0, MLA_KV_FP8_E4M3_E8M0, make_problem, mla_clear_status, mla_combine,
                mla_decode_plan, mla_decode_run, mla_get_status, mla_q_absorb, mla_uv_proj)
 
 
@@ -25,7 +25,8 @@ class DecodeStep:
 
     Inputs (numpy, host): q_nope/q_rope bf16 bits [B, Q, H, 192/64],
     w_uk [H, 512, 192] and w_uv [H, 512, 256] bf16 bits, the cache (bf16 bits
-    [num_pages, P, 576] or FP8 bytes [num_pages, P*594]), block_table int32
+    [num_pages, P, 576], FP8 bytes [num_pages, P*594] or FP4 bytes
+    [num_pages, P*324]), block_table int32
     [B, max_pages], seq_lens int32 [B], optional topk_idx int32 [B*Q, width].
     """
 
@@ -50,7 +51,7 @@ class DecodeStep:
         self.q_rope = to_device_bf16(q_rope, dev)
         self.w_uk = to_device_bf16(w_uk, dev)
         self.w_uv = to_device_bf16(w_uv, dev)
-        if kv_dtype == MLA_KV_FP8_E4M3_E8M0:
+        if kv_dtype in (MLA_KV_FP8_E4M3_E8M0, MLA_KV_FP4_E2M1_E8M0):
             self.cache = to_device(cache.astype(np.uint8, copy=False), dev)
         else:
             self.cache = to_device_bf16(cache, dev)

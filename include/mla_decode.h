@@ -79,6 +79,16 @@ typedef struct CUstream_st* mla_stream_t;
  * constraint (2): FP8 latent with per-token inlined e8m0 scales, one per 32
  * e4m3 values). */
 #define MLA_KV_FP8_E4M3_E8M0 1
+/* 576 float4_e2m1 values packed two per byte (value 2i in the low nibble of
+ * byte i: 288 bytes) followed by 36 float8_e8m0 scales (one per 16
+ * consecutive values, value = e2m1 * 2^(scale - 127)) per token: 324 bytes
+ * per token, a page of P tokens is P contiguous rows.  e2m1: sign, 2
+ * exponent bits (bias 1), 1 mantissa bit; magnitudes 0, 0.5, 1, 1.5, 2, 3, 4,
+ * 6.  The record gives only 288 bytes per token for its 512-value row
+ * (GLM-4.7-Flash record, engine-kernel constraint (2): the FP4 variant of the
+ * inlined-scale latent); 256 code bytes + 32 scale bytes is read as one e8m0
+ * scale per 16 values, and the layout follows the FP8 variant's. */
+#define MLA_KV_FP4_E2M1_E8M0 2
 
 /* status-word bits (sticky until mla_clear_status) */
 #define MLA_STATUS_BAD_PAGE 0x1u     /* a block-table entry outside [0, num_pages) was masked */
@@ -99,7 +109,8 @@ typedef struct {
   int32_t page_size;        /* P: 16, 32, 64 or 128 */
   int32_t num_pages;        /* physical pages in the cache pool */
   int32_t max_pages_per_seq;/* row stride of block_table */
-  int32_t kv_dtype;         /* MLA_KV_BF16 or MLA_KV_FP8_E4M3_E8M0 */
+  int32_t kv_dtype;         /* MLA_KV_BF16, MLA_KV_FP8_E4M3_E8M0 or MLA_KV_FP4_E2M1_E8M0
+                               (the quantised formats: dense only, topk_width 0) */
   int32_t topk_width;       /* 0: dense; else sparse row width, a multiple of 128
                                (vllm API docs, vllm.models.glm5next.common.model,
                                Glm5NextModel.__init__: top-k is tiled in 128

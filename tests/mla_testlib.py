@@ -5,10 +5,11 @@ from __future__ import annotations
 import numpy as np
 
 import oracle as O
+from oracle import fp4 as F4
 from oracle import fp8 as F
 import workloads as W
 
-# Tolerances for the bf16 and FP8 paths: max |err| <= 2e-2 and relative L2
+# Tolerances for the bf16, FP8 and FP4 paths: max |err| <= 2e-2 and relative L2
 # <= 5e-3 on outputs, |lse err| <= 1e-3 (natural log).
 ATOL_MAX = 2e-2
 REL_L2 = 5e-3
@@ -21,12 +22,13 @@ def ensure_built():
 
 
 def make_step(batch: W.Batch, sm_count=None, absorb=True, device="cuda:0", fp8_bytes=None):
-    from head_latent_attention_paged_gb300 import MLA_KV_BF16, MLA_KV_FP8_E4M3_E8M0
+    from head_latent_attention_paged_gb300 import (MLA_KV_BF16, MLA_KV_FP4_E2M1_E8M0,
+                                                   MLA_KV_FP8_E4M3_E8M0)
     from head_latent_attention_paged_gb300.runner import DecodeStep
     w = batch.workload
-    if w.kv_dtype == "fp8":
-        cache = fp8_bytes if fp8_bytes is not None else batch.extra["cache_fp8"]
-        kv_dtype = MLA_KV_FP8_E4M3_E8M0
+    if w.kv_dtype in ("fp8", "fp4"):
+        cache = fp8_bytes if fp8_bytes is not None else batch.extra["cache_" + w.kv_dtype]
+        kv_dtype = MLA_KV_FP8_E4M3_E8M0 if w.kv_dtype == "fp8" else MLA_KV_FP4_E2M1_E8M0
     else:
         cache = batch.cache_bf16
         kv_dtype = MLA_KV_BF16
@@ -97,9 +99,12 @@ def compare(ref: dict, o, o_lat, lse, heads=None, label="", lse_ref=None):
 
 
 def with_fp8(batch: W.Batch, garbage="finite") -> W.Batch:
-    """FP8 workloads drawn with fp8_source="float": attach the paged FP8
+    """FP8 / FP4 workloads drawn with fp8_source="float": attach the paged
     bytes made by the oracle's quantiser (codes-drawn batches have them)."""
-    if batch.workload.kv_dtype == "fp8" and "cache_fp8" not in batch.extra:
-        batch.extra["cache_fp8"] = F.quantize_pages(batch.latent_f32, batch.slot_valid,
-                                                    rng_seed=batch.workload.seed, garbage=garbage)
+    kv = batch.workload.kv_dtype
+    if kv in ("fp8", "fp4") and "cache_" + kv not in batch.extra:
+        enc = F if kv == "fp8" else F4
+        batch.extra["cache_" + kv] = enc.quantize_pages(batch.latent_f32, batch.slot_valid,
+                                                        rng_seed=batch.workload.seed,
+                                                        garbage=garbage)
     return batch

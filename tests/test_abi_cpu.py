@@ -85,7 +85,8 @@ def test_plan_ok_and_workspace_layout(m):
     (dict(rope_dim=32), -2), (dict(v_head_dim=128), -2), (dict(nope_dim=128), -2),
     (dict(causal=2), -1), (dict(sm_scale=0.0), -1), (dict(sm_scale=float("nan")), -1),
     (dict(num_pages=0), -1), (dict(max_pages_per_seq=0), -1), (dict(batch=257), -2), (dict(batch=65, q_len=4), -2),
-    (dict(kv_dtype=1, topk_width=128), -2), (dict(kv_dtype=2), -2),
+    (dict(kv_dtype=1, topk_width=128), -2), (dict(kv_dtype=2, topk_width=128), -2),
+    (dict(kv_dtype=3), -2), (dict(kv_dtype=-1), -2),
 ])
 def test_plan_rejects(m, kw, code):
     with pytest.raises(m.MlaError) as e:
@@ -103,6 +104,19 @@ def test_fp8_plan_fits_shared_memory(m):
     big = m.mla_decode_plan(_problem(m, kv_dtype=m.MLA_KV_FP8_E4M3_E8M0, batch=256, num_heads=32),
                             None, 152)
     assert 2 * 73728 + 2 * 64 * 594 < big.smem_bytes <= 232448
+
+
+def test_fp4_plan_fits_shared_memory(m):
+    """FP4 caches (324-byte rows) plan like FP8 ones, with two 20,736-byte
+    raw tiles beside the two bf16 tiles."""
+    seq = np.array([100, 1000, 64, 0], dtype=np.int32)
+    plan = m.mla_decode_plan(_problem(m, kv_dtype=m.MLA_KV_FP4_E2M1_E8M0), seq, 152)
+    assert plan.planned_tiles == sum((int(t) + 63) // 64 for t in seq)
+    big = m.mla_decode_plan(_problem(m, kv_dtype=m.MLA_KV_FP4_E2M1_E8M0, batch=256, num_heads=32),
+                            None, 152)
+    assert 2 * 73728 + 2 * 64 * 324 < big.smem_bytes <= 232448
+    assert big.smem_bytes < m.mla_decode_plan(
+        _problem(m, kv_dtype=m.MLA_KV_FP8_E4M3_E8M0, batch=256, num_heads=32), None, 152).smem_bytes
 
 
 def test_plan_rejects_negative_seq_len_and_bad_sm_count(m):

@@ -1,7 +1,7 @@
 """GPU parity of the cache append (mla_cache_append): each request's newest
-token row written into the paged cache, bf16 as is or quantised to the FP8
-layout on the GPU.  Compared byte for byte with the oracle's append, which
-uses the oracle's quantiser, on the same bf16 rows."""
+token row written into the paged cache, bf16 as is or quantised to the FP8 or
+FP4 layout on the GPU.  Compared byte for byte with the oracle's append, which
+uses the oracle's quantisers, on the same bf16 rows."""
 import numpy as np
 import pytest
 
@@ -36,19 +36,27 @@ def _special_rows(rng, B):
     x[2, 32:64] = rng.standard_normal(32) * 1e30       # huge
     x[2, 64:96] = rng.standard_normal(32) * 1e-38      # bf16 subnormals: scale clamps
     x[3, 0:32] = rng.choice([-3.0, -1.0, 0.5, 2.5, 7.0], 32)   # rounding ties after scaling
+    # FP4 rounding ties (amax 6: scale 1): every midpoint of the e2m1 grid
+    x[5, 0:16] = [6.0, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -0.25, -5.0, -0.75, -1.75,
+                  -2.5, -3.5, -1.25, -0.0]
+    x[5, 16:32] = np.array([12.0, 0.5, 1.5, 2.5, 3.5, 5.0, 7.0, 10.0, -0.5, -1.5, -2.5,
+                            -3.5, -5.0, -7.0, -10.0, 0.1])            # amax 12: scale 2
     return W.f32_to_bf16_bits(x)
 
 
 def _problem(batch, w, num_pages, max_pages, fp8):
-    from head_latent_attention_paged_gb300 import MLA_KV_BF16, MLA_KV_FP8_E4M3_E8M0, make_problem
-    return make_problem(batch, 1, w.heads, w.page_size, num_pages, max_pages,
-                        kv_dtype=MLA_KV_FP8_E4M3_E8M0 if fp8 else MLA_KV_BF16)
+    from head_latent_attention_paged_gb300 import (MLA_KV_BF16, MLA_KV_FP4_E2M1_E8M0,
+                                                   MLA_KV_FP8_E4M3_E8M0, make_problem)
+    kv = {"bf16": MLA_KV_BF16, "fp8": MLA_KV_FP8_E4M3_E8M0, "fp4": MLA_KV_FP4_E2M1_E8M0}[fp8] \
+        if isinstance(fp8, str) else (MLA_KV_FP8_E4M3_E8M0 if fp8 else MLA_KV_BF16)
+    return make_problem(batch, 1, w.heads, w.page_size, num_pages, max_pages, kv_dtype=kv)
 
 
-@pytest.mark.parametrize("kv,page_size", [("bf16", 64), ("bf16", 128), ("fp8", 64), ("fp8", 128)])
+@pytest.mark.parametrize("kv,page_size", [("bf16", 64), ("bf16", 128), ("fp8", 64), ("fp8", 128),
+                                          ("fp4", 64), ("fp4", 128), ("fp4", 16)])
 def test_append_matches_oracle_bytes(kv, page_size):
     from head_latent_attention_paged_gb300 import mla_cache_append
-    base = W.SMALL_WORKLOADS["fp8_small" if kv == "fp8" else "dense_small"]
+    base = W.SMALL_WORKLOADS[{"bf16": "dense_small", "fp8": "fp8_small", "fp4": "fp4_small"}[kv]]
     w = W.with_overrides(base, page_size=page_size, batch=6, seq_lo=1, seq_hi=500)
     batch = W.generate(w)
     rng = np.random.default_rng(7)
@@ -59,7 +67,7 @@ def test_append_matches_oracle_bytes(kv, page_size):
     pos = np.where(seq % page_size != 0, seq, seq - 1).astype(np.int32)   # a mapped slot
     pos[2] = 0
     pos[4] = -1
-    cache = batch.cache_fp8 if kv == "fp8" else batch.cache_bf16
+    cache = batch.cache_bf16 if kv == "bf16" else batch.cache_quant
     expect = CA.append_rows(cache, rows, pos, batch.block_table, page_size, kv)
     dev = torch.device("cuda", 0)
     cache_d = torch.from_numpy(cache.view(np.uint8).copy()).to(dev)
@@ -67,7 +75,7 @@ def test_append_matches_oracle_bytes(kv, page_size):
     pos_d = torch.from_numpy(pos).to(dev)
     bt_d = torch.from_numpy(batch.block_table).to(dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    mla_cache_append(_problem(w.batch, w, batch.num_pages, batch.block_table.shape[1], kv == "fp8"),
+    mla_cache_append(_problem(w.batch, w, batch.num_pages, batch.block_table.shape[1], kv),
                      rows_d, pos_d, bt_d, cache_d, status)
     torch.cuda.synchronize()
     got = cache_d.cpu().numpy()
@@ -99,7 +107,7 @@ def test_append_reports_bad_positions_and_pages():
     assert np.array_equal(got, expect.view(np.uint8).reshape(got.shape))
 
 
-@pytest.mark.parametrize("name", ["dense_small", "fp8_small"])
+@pytest.mark.parametrize("name", ["dense_small", "fp8_small", "fp4_small"])
 def test_decode_sees_appended_token(name):
     """Append the next token of every request, then decode over seq_lens + 1:
     the result matches the oracle decode over the oracle-appended cache."""
@@ -113,8 +121,8 @@ def test_decode_sees_appended_token(name):
     rows = W.f32_to_bf16_bits(rng.standard_normal((w.batch, 576)).astype(np.float32))
     pos = np.full(w.batch, -1, dtype=np.int32)
     pos[keep] = batch.seq_lens[keep]
-    kv = "fp8" if w.kv_dtype == "fp8" else "bf16"
-    cache = batch.cache_fp8 if kv == "fp8" else batch.cache_bf16
+    kv = w.kv_dtype
+    cache = batch.cache_bf16 if kv == "bf16" else batch.cache_quant
     step = make_step(batch, absorb=False)
     q_hat = oracle_q_hat(batch)
     upload_q_hat(step, q_hat)
@@ -127,10 +135,10 @@ def test_decode_sees_appended_token(name):
     o, o_lat, lse = gpu_outputs(step)
     assert step.status() == 0
     appended = CA.append_rows(cache, rows, pos, batch.block_table, w.page_size, kv)
-    if kv == "fp8":
-        batch.extra["cache_fp8"] = appended
-    else:
+    if kv == "bf16":
         batch.cache_bf16 = appended
+    else:
+        batch.extra["cache_" + kv] = appended
     batch.seq_lens = new_lens
     reqs = list(keep)
     # lse against the absorbed form on the decode's own bf16 absorbed query
