@@ -8,12 +8,15 @@
 //                   top-k rows, four gather warps issue 16-byte cp.async
 //                   copies, 16 rows each) -- as nine
 //                   [64 rows x 128 B] chunks in the 128-byte swizzle layout,
-//                   three tiles in flight.  FP8 caches: one bulk copy of the
-//                   tile's 594-byte rows, two tiles in flight, and
-//   dequant warps : (FP8 only) turn each row's 576 e4m3 codes and 18 e8m0
-//                   scales into bf16 values e4m3 * 2^(scale - 127), exactly,
-//                   written into the same swizzled bf16 tile layout (two
-//                   tiles in flight); rows with no live token become zeros.
+//                   three tiles in flight.  FP8 / FP4 caches: one bulk copy
+//                   of the tile's quantised rows (594 or 324 bytes) into the
+//                   tail of the stage it will be dequantised into, and
+//   dequant warps : (FP8 / FP4) turn each row's codes and e8m0 scales into
+//                   bf16 values code * 2^(scale - 127), exactly, written in
+//                   place as the swizzled bf16 tile: first the chunks below
+//                   the raw bytes, then, once every dequant warp holds the
+//                   rest of its groups in registers, the chunks over them;
+//                   rows with no live token become zeros.
 //   MMA warp      : S[h, t]   = q_hat[h, :576] . row[t, :576]      (tcgen05,
 //                   M = 64 head rows with q_hat read from TMEM, N = 64
 //                   tokens from shared memory, K = 576, f32 in TMEM);
@@ -70,7 +73,13 @@ struct ModeTraits {
   static constexpr int kThreads = kQuant    ? 32 * (kDequantWarp0 + kDequantWarps)
                                   : kSparse ? 32 * (kGatherWarp0 + kGatherWarps)
                                             : 192;
-  static constexpr int kNumStages = kQuant ? kFp8Stages : kStages;   // bf16 tiles
+  // FP8: two bf16 stages and a two-slot ring of raw tiles beside them.
+  // FP4: three bf16 stages, each raw tile landing in the last
+  // kRawTileBytes of the stage it is dequantised into.
+  static constexpr bool kRawRing = kFp8;
+  static constexpr int kNumStages = kRawRing ? kFp8Stages : kStages;   // bf16 tiles in flight
+  static constexpr int kRawSlots = kRawRing ? kFp8RawSlots : kStages;
+  static constexpr int kRawOffset = kTileBytes - kRawTileBytes;
 };
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s per wait
 constexpr float kRescaleThreshold = 8.0f;           // log2 units: rescale if max grows > 2^8
@@ -95,9 +104,9 @@ struct __align__(8) Ctrl {
   uint64_t o_free;           // softmax -> MMA: epilogue has read O^T
   uint64_t mma_drain;        // MMA warp's final commit
   uint64_t mask[kStages];    // per-stage live-row mask (bit t = row t live)
-  uint64_t raw_full[kRawStages];    // FP8: producer -> dequant, bytes landed
-  uint64_t raw_empty[kRawStages];   // FP8: dequant -> producer, bytes consumed
-  uint64_t raw_mask[kRawStages];    // FP8: live-row mask of the raw tile
+  uint64_t raw_full[kStages];       // FP8 / FP4: producer -> dequant, bytes landed
+  uint64_t raw_empty[kFp8RawSlots]; // FP8: dequant -> producer, raw slot consumed
+  uint64_t raw_mask[kFp8RawSlots];  // FP8: live-row mask of the raw tile
   uint32_t tmem_base;
   int32_t abort_flag;
   int32_t rescale_tile[2];
@@ -335,27 +344,35 @@ __device__ __forceinline__ ScaleX2 e8m0_scale_x2(uint32_t b) {
   return sc;
 }
 
-// Dequantise group g (values 32g .. 32g+31) of one FP8 row in shared memory
-// (row: 2-byte aligned start of the row's 594 bytes) into 4 x 16 bytes of
-// bf16 (8 values each, in dimension order).  Exact: every product is an
-// e4m3 value (4 significant bits) times a power of two.  Plain loads, so the
-// compiler may overlap the groups of one thread.
-__device__ __forceinline__ void dequant_group(const uint8_t* row, int g, uint4 (&o)[4]) {
+// One group (32 values) of an FP8 row: its codes as nine aligned words
+// (a row starts 2 bytes past a word boundary when `odd`) and its scale byte.
+struct Fp8Group {
+  uint32_t w[9];
+  uint32_t scale;
+};
+
+// Load group g of the FP8 row at `row` (2-byte aligned) from shared memory.
+__device__ __forceinline__ void load_fp8_group(const uint8_t* row, int g, bool odd, Fp8Group& f) {
   const uint8_t* a = row + 32 * g;
   const uint32_t* a4 = reinterpret_cast<const uint32_t*>(reinterpret_cast<uintptr_t>(a) & ~uintptr_t(3));
-  const bool odd = (reinterpret_cast<uintptr_t>(a) & 2u) != 0;
-  uint32_t w[9];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) w[k] = a4[k];
-  w[8] = odd ? a4[8] : 0u;
-  const ScaleX2 sc = e8m0_scale_x2<120u>(row[kDqk + g]);
+  for (int k = 0; k < 8; ++k) f.w[k] = a4[k];
+  f.w[8] = odd ? a4[8] : 0u;
+  f.scale = row[kDqk + g];
+}
+
+// The group as 4 x 16 bytes of bf16 (8 values each, in dimension order).
+// Exact: every product is an e4m3 value (4 significant bits) times a power
+// of two.
+__device__ __forceinline__ void convert_fp8_group(const Fp8Group& f, bool odd, uint4 (&o)[4]) {
+  const ScaleX2 sc = e8m0_scale_x2<120u>(f.scale);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     uint32_t r[4];
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
       const int wi = 2 * q + k;
-      const uint32_t v = odd ? __funnelshift_r(w[wi], w[wi + 1], 16) : w[wi];
+      const uint32_t v = odd ? __funnelshift_r(f.w[wi], f.w[wi + 1], 16) : f.w[wi];
       uint32_t lo = bf16x2_mul(e4m3x2_to_bf16x2_scaled(v, 0), sc.f1);
       uint32_t hi = bf16x2_mul(e4m3x2_to_bf16x2_scaled(v, 1), sc.f1);
       if (sc.two) {
@@ -389,17 +406,26 @@ __device__ __forceinline__ void e2m1x8_to_bf16x2_scaled(uint32_t w, uint32_t (&r
   }
 }
 
-// Dequantise group g (values 16g .. 16g+15) of one FP4 row in shared memory
-// (row: 4-byte aligned start of the row's 324 bytes) into 2 x 16 bytes of
-// bf16 in dimension order.  Exact: every product is an e2m1 value (2
-// significant bits) times a power of two.
-__device__ __forceinline__ void dequant_group_fp4(const uint8_t* row, int g, uint4 (&o)[2]) {
+// One group (16 values) of an FP4 row: two code words and the scale byte.
+struct Fp4Group {
+  uint32_t w0, w1, scale;
+};
+
+// Load group g of the FP4 row at `row` (4-byte aligned) from shared memory.
+__device__ __forceinline__ void load_fp4_group(const uint8_t* row, int g, Fp4Group& f) {
   const uint32_t* a4 = reinterpret_cast<const uint32_t*>(row + 8 * g);
-  const uint32_t w0 = a4[0], w1 = a4[1];
-  const ScaleX2 sc = e8m0_scale_x2<126u>(row[kFp4CodeBytes + g]);
+  f.w0 = a4[0];
+  f.w1 = a4[1];
+  f.scale = row[kFp4CodeBytes + g];
+}
+
+// The group as 2 x 16 bytes of bf16 in dimension order.  Exact: every
+// product is an e2m1 value (2 significant bits) times a power of two.
+__device__ __forceinline__ void convert_fp4_group(const Fp4Group& f, uint4 (&o)[2]) {
+  const ScaleX2 sc = e8m0_scale_x2<126u>(f.scale);
   uint32_t r[2][4];
-  e2m1x8_to_bf16x2_scaled(w0, r[0]);
-  e2m1x8_to_bf16x2_scaled(w1, r[1]);
+  e2m1x8_to_bf16x2_scaled(f.w0, r[0]);
+  e2m1x8_to_bf16x2_scaled(f.w1, r[1]);
 #pragma unroll
   for (int q = 0; q < 2; ++q) {
 #pragma unroll
@@ -415,14 +441,13 @@ __device__ __forceinline__ void dequant_group_fp4(const uint8_t* row, int g, uin
 
 DecodeLayout decode_layout(int heads, int heads_pad, int num_streams, int mode) {
   (void)heads;
-  const bool quant = mode == kModeDenseFp8 || mode == kModeDenseFp4;
-  const int raw_tile = mode == kModeDenseFp4 ? kFp4TileBytes : kFp8TileBytes;
+  const bool ring = mode == kModeDenseFp8;   // FP8: bf16 stages plus a raw ring
   DecodeLayout L;
   L.off_stage = 0;
-  L.off_raw = (quant ? kFp8Stages : kStages) * kTileBytes;
+  L.off_raw = (ring ? kFp8Stages : kStages) * kTileBytes;
   (void)heads_pad;
   L.off_p = L.off_stage + kPChunkOffset;     // first stage's P; stride kTileBytes
-  L.off_ctrl = L.off_raw + (quant ? kRawStages * raw_tile : 0);
+  L.off_ctrl = L.off_raw + (ring ? kFp8RawSlots * kFp8TileBytes : 0);
   L.total = L.off_ctrl + static_cast<int>(sizeof(Ctrl)) + 2 * (num_streams + 1) * 4;
   return L;
 }
@@ -438,7 +463,7 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
   // dynamic shared window starts aligned, which is checked below.
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* sStage = smem + L.off_stage;
-  uint8_t* sRaw = smem + L.off_raw;
+  uint8_t* sRaw = smem + L.off_raw;   // FP8 raw ring
   Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + L.off_ctrl);
   int32_t* prefix = reinterpret_cast<int32_t*>(smem + L.off_ctrl + sizeof(Ctrl));  // tiles
   int32_t* cprefix = prefix + (p.num_streams + 1);                                   // cost
@@ -468,10 +493,8 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
                 MT::kQuant ? kDequantWarps : (MT::kSparse ? kGatherWarps * 33 : 1));
       mbar_init(&ctrl->empty[i], 1);
     }
-    for (int i = 0; i < kRawStages; ++i) {
-      mbar_init(&ctrl->raw_full[i], 1);
-      mbar_init(&ctrl->raw_empty[i], kDequantWarps);
-    }
+    for (int i = 0; i < kStages; ++i) mbar_init(&ctrl->raw_full[i], 1);
+    for (int i = 0; i < kFp8RawSlots; ++i) mbar_init(&ctrl->raw_empty[i], kDequantWarps);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctrl->p_full[i], kSoftmaxWarps);
       ctrl->rescale_tile[i] = -1;
@@ -608,7 +631,14 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
             }
           }
         } else {   // FP8 / FP4 caches: the tile's quantised rows, one bulk copy
-          const int rs = i % kRawStages;
+          // FP8: ring slot rs, reusable once the dequant warps have read it;
+          // FP4: the tail of this tile's stage, reusable once PV has read it
+          const int rs = MT::kRawRing ? i % MT::kRawSlots : stage;
+          uint8_t* raw_dst = MT::kRawRing ? sRaw + rs * MT::kRawTileBytes : dst + MT::kRawOffset;
+          uint64_t* raw_bar = &ctrl->raw_full[rs];
+          uint64_t* mask_slot = MT::kRawRing ? &ctrl->raw_mask[rs] : &ctrl->mask[stage];
+          uint64_t* reuse_bar = MT::kRawRing ? &ctrl->raw_empty[rs] : &ctrl->empty[stage];
+          const uint32_t reuse_par = ((i / MT::kRawSlots) - 1) & 1;
           if (p.page_size >= kTile) {
             // one page holds the whole tile: one lane describes it
             uint64_t mask = 0;
@@ -634,18 +664,17 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
                                MT::kRowBytes;
               bytes = static_cast<uint32_t>((nvalid + 7) & ~7) * MT::kRowBytes;
             }
-            if (i >= kRawStages &&
-                !warp_wait(&ctrl->raw_empty[rs], ((i / kRawStages) - 1) & 1, abort_flag)) {
+            if (i >= MT::kRawSlots && !warp_wait(reuse_bar, reuse_par, abort_flag)) {
               failed = true;
               break;
             }
             if (lane == 0) {
-              ctrl->raw_mask[rs] = mask;
+              *mask_slot = mask;
               if (ok) {
-                mbar_arrive_expect_tx(&ctrl->raw_full[rs], bytes);
-                bulk_load(sRaw + rs * MT::kRawTileBytes, src, bytes, &ctrl->raw_full[rs], pol);
+                mbar_arrive_expect_tx(raw_bar, bytes);
+                bulk_load(raw_dst, src, bytes, raw_bar, pol);
               } else {
-                mbar_arrive(&ctrl->raw_full[rs]);
+                mbar_arrive(raw_bar);
               }
             }
           } else {
@@ -653,13 +682,12 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
             const TilePieces tp = describe_tile(p, b, j, wk.lt, lane, max_tokens);
             const uint64_t mask = tile_mask(tp);
             if (lane == 0 && tp.bad) set_status(p.status, tp.bad);
-            if (i >= kRawStages &&
-                !warp_wait(&ctrl->raw_empty[rs], ((i / kRawStages) - 1) & 1, abort_flag)) {
+            if (i >= MT::kRawSlots && !warp_wait(reuse_bar, reuse_par, abort_flag)) {
               failed = true;
               break;
             }
             if (lane == 0) {
-              ctrl->raw_mask[rs] = mask;
+              *mask_slot = mask;
               if (tp.ok) {
                 // a piece's rows are contiguous in its page; copy the live ones
                 // rounded up to 8 rows (a multiple of 16 B)
@@ -667,7 +695,7 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
                 for (int k = 0; k < tp.npieces; ++k)
                   if ((tp.ok >> k) & 1u)
                     total += static_cast<uint32_t>((min(tp.rows, tp.nvalid - k * tp.rows) + 7) & ~7);
-                mbar_arrive_expect_tx(&ctrl->raw_full[rs], total * MT::kRowBytes);
+                mbar_arrive_expect_tx(raw_bar, total * MT::kRowBytes);
                 for (int k = 0; k < tp.npieces; ++k) {
                   if (!((tp.ok >> k) & 1u)) continue;
                   const uint32_t nrows =
@@ -675,11 +703,11 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
                   const uint8_t* src =
                       p.kv + (static_cast<int64_t>(tp.page[k]) * p.page_size + tp.slot0) *
                                  MT::kRowBytes;
-                  bulk_load(sRaw + rs * MT::kRawTileBytes + k * tp.rows * MT::kRowBytes, src,
-                            nrows * MT::kRowBytes, &ctrl->raw_full[rs], pol);
+                  bulk_load(raw_dst + k * tp.rows * MT::kRowBytes, src, nrows * MT::kRowBytes,
+                            raw_bar, pol);
                 }
               } else {
-                mbar_arrive(&ctrl->raw_full[rs]);
+                mbar_arrive(raw_bar);
               }
             }
           }
@@ -695,8 +723,8 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
       // drain: everything this warp issued has landed before the CTA exits
       if (lane == 0) {
         if constexpr (MT::kQuant) {
-          for (int32_t i = max(0, issued - kRawStages); i < issued; ++i)
-            (void)mbar_wait(&ctrl->raw_full[i % kRawStages], (i / kRawStages) & 1, nullptr,
+          for (int32_t i = max(0, issued - MT::kRawSlots); i < issued; ++i)
+            (void)mbar_wait(&ctrl->raw_full[i % MT::kRawSlots], (i / MT::kRawSlots) & 1, nullptr,
                             kWaitLimitNs);
         } else {
           for (int32_t i = max(0, issued - kNumStages); i < issued; ++i)
@@ -814,63 +842,108 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
       const int dt = tid - kDequantWarp0 * 32;
       const int r = dt & 63;
       const int gset = dt >> 6;
+      const bool odd = (r & 1) != 0;   // FP8 rows of odd index start 2 bytes past a word
       bool failed = false;
-      for (int32_t i = 0; i < ntiles; ++i) {
-        const int rs = i % kRawStages;
-        const int bs = i % kNumStages;
-        if (!warp_wait(&ctrl->raw_full[rs], (i / kRawStages) & 1, abort_flag) ||
-            (i >= kNumStages &&
-             !warp_wait(&ctrl->empty[bs], ((i / kNumStages) - 1) & 1, abort_flag))) {
-          failed = true;
-          break;
-        }
-        const uint64_t mask = ctrl->raw_mask[rs];
-        const bool live = (mask >> r) & 1ull;
-        const uint8_t* row_ptr = sRaw + rs * MT::kRawTileBytes + r * MT::kRowBytes;
-        uint8_t* dst = sStage + bs * kTileBytes + r * 128;
-        if constexpr (MT::kFp4) {
-          // 36 groups of 16 values (32 bf16 bytes, two 16-byte units each)
-#pragma unroll 4
-          for (int k = 0; k < kDqk / 48; ++k) {
-            const int g = gset + 3 * k;
-            uint4 o[2];
-            if (live) {
-              dequant_group_fp4(row_ptr, g, o);
-            } else {
-              o[0] = make_uint4(0, 0, 0, 0);
-              o[1] = o[0];
-            }
-            const int u0 = (g & 3) * 2;
+      // store a converted group: FP8 group g fills units 4(g%2).. of chunk g/2,
+      // FP4 group g units 2(g%4).. of chunk g/4 (16-byte units, swizzled by row)
+      auto store_group = [&](uint8_t* dst, int g, const uint4* o) {
+        constexpr int kUnits = MT::kFp4 ? 2 : 4;
+        constexpr int kPerChunk = 8 / kUnits;
+        const int u0 = (g % kPerChunk) * kUnits;
 #pragma unroll
-            for (int q = 0; q < 2; ++q)
-              *reinterpret_cast<uint4*>(dst + (g >> 2) * kChunkBytes +
-                                        (((u0 + q) ^ (r & 7)) << 4)) = o[q];
+        for (int q = 0; q < kUnits; ++q)
+          *reinterpret_cast<uint4*>(dst + (g / kPerChunk) * kChunkBytes +
+                                    (((u0 + q) ^ (r & 7)) << 4)) = o[q];
+      };
+      if constexpr (MT::kRawRing) {
+        // FP8: raw slot rs -> bf16 stage bs, all 18 groups of a row at once
+        for (int32_t i = 0; i < ntiles; ++i) {
+          const int rs = i % MT::kRawSlots;
+          const int bs = i % kNumStages;
+          if (!warp_wait(&ctrl->raw_full[rs], (i / MT::kRawSlots) & 1, abort_flag) ||
+              (i >= kNumStages &&
+               !warp_wait(&ctrl->empty[bs], ((i / kNumStages) - 1) & 1, abort_flag))) {
+            failed = true;
+            break;
           }
-        } else {
-          // 18 groups of 32 values (64 bf16 bytes, four 16-byte units each)
+          const uint64_t mask = ctrl->raw_mask[rs];
+          const bool live = (mask >> r) & 1ull;
+          const uint8_t* row_ptr = sRaw + rs * MT::kRawTileBytes + r * MT::kRowBytes;
+          uint8_t* dst = sStage + bs * kTileBytes + r * 128;
 #pragma unroll 2
           for (int k = 0; k < kDqk / 96; ++k) {
             const int g = gset + 3 * k;
             uint4 o[4];
             if (live) {
-              dequant_group(row_ptr, g, o);
+              Fp8Group f;
+              load_fp8_group(row_ptr, g, odd, f);
+              convert_fp8_group(f, odd, o);
             } else {
 #pragma unroll
               for (int q = 0; q < 4; ++q) o[q] = make_uint4(0, 0, 0, 0);
             }
-            const int u0 = (g & 1) * 4;
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              *reinterpret_cast<uint4*>(dst + (g >> 1) * kChunkBytes +
-                                        (((u0 + q) ^ (r & 7)) << 4)) = o[q];
+            store_group(dst, g, o);
+          }
+          if (dt == 0) ctrl->mask[bs] = mask;
+          fence_proxy_async_smem();   // generic stores -> tensor-core reads
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&ctrl->raw_empty[rs]);
+            mbar_arrive(&ctrl->full[bs]);
           }
         }
-        if (dt == 0) ctrl->mask[bs] = mask;
-        fence_proxy_async_smem();   // generic stores -> tensor-core reads
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&ctrl->raw_empty[rs]);
-          mbar_arrive(&ctrl->full[bs]);
+      } else {
+        // FP4: the raw bytes occupy the stage from kRawOffset on (inside
+        // chunk 6).  Groups 3k + gset with k < 8 have their bf16 output in
+        // chunks 0-5, below them: converted and stored at once.  The other
+        // four are loaded into registers and stored after every dequant warp
+        // has finished reading raw bytes.
+        for (int32_t i = 0; i < ntiles; ++i) {
+          const int stage = i % kNumStages;
+          const bool ok = warp_wait(&ctrl->raw_full[stage], (i / kNumStages) & 1, abort_flag);
+          const uint64_t mask = ctrl->mask[stage];
+          const bool live = ok && ((mask >> r) & 1ull);
+          uint8_t* tile = sStage + stage * kTileBytes;
+          const uint8_t* row_ptr = tile + MT::kRawOffset + r * MT::kRowBytes;
+          uint8_t* dst = tile + r * 128;
+          constexpr int kDirect = 8;
+          constexpr int kKept = kDqk / 48 - kDirect;
+          Fp4Group keep[kKept];
+          if (ok) {
+#pragma unroll 4
+            for (int k = 0; k < kDirect; ++k) {
+              const int g = gset + 3 * k;
+              uint4 o[2];
+              if (live) {
+                Fp4Group f;
+                load_fp4_group(row_ptr, g, f);
+                convert_fp4_group(f, o);
+              } else {
+                o[0] = o[1] = make_uint4(0, 0, 0, 0);
+              }
+              store_group(dst, g, o);
+            }
+            if (live) {
+#pragma unroll
+              for (int k = 0; k < kKept; ++k) load_fp4_group(row_ptr, gset + 3 * (kDirect + k), keep[k]);
+            }
+          }
+          // every dequant warp reaches this barrier once per tile; a failed
+          // wait in any of them ends all of them here
+          if (named_bar_or(2, kDequantWarps * 32, !ok)) {
+            failed = true;
+            break;
+          }
+#pragma unroll
+          for (int k = 0; k < kKept; ++k) {
+            uint4 o[2];
+            if (live) convert_fp4_group(keep[k], o);
+            else o[0] = o[1] = make_uint4(0, 0, 0, 0);
+            store_group(dst, gset + 3 * (kDirect + k), o);
+          }
+          fence_proxy_async_smem();   // generic stores -> tensor-core reads
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctrl->full[stage]);
         }
       }
       if (failed && lane == 0) {

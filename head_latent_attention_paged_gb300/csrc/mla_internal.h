@@ -24,11 +24,13 @@ constexpr int kFp4CodeBytes = kDqk / 2;            // 288: two e2m1 codes per by
 constexpr int kFp4RowBytes = kFp4CodeBytes + kDqk / 16;   // 324
 constexpr int kMaxHeads = 32;     // TMEM: q_hat 288 + S 64 + O^T 4 x 32 columns
 constexpr int kMaxStreams = 256;  // per-stream tile prefix kept in shared memory
-constexpr int kStages = 3;        // 72 KB tiles in flight per CTA (bf16 caches)
-constexpr int kFp8TileBytes = kTile * kFp8RowBytes;  // 38,016: one tile of FP8 rows
-constexpr int kFp4TileBytes = kTile * kFp4RowBytes;  // 20,736: one tile of FP4 rows
-constexpr int kFp8Stages = 2;     // dequantised bf16 tiles in flight (FP8 / FP4 caches)
-constexpr int kRawStages = 2;     // quantised byte tiles in flight (FP8 / FP4 caches)
+// 72 KB bf16 tiles in flight per CTA.  An FP4 tile of quantised rows
+// (20,736 B) is copied into the tail of the stage it is dequantised into;
+// FP8 tiles (38,016 B) have a ring of their own beside two bf16 stages.
+constexpr int kStages = 3;
+constexpr int kFp8Stages = 2;
+constexpr int kFp8RawSlots = 2;
+constexpr int kFp8TileBytes = kTile * kFp8RowBytes;  // 38,016
 
 enum DecodeMode : int {
   kModeDenseBf16 = 0,
