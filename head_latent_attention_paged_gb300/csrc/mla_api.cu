@@ -51,10 +51,21 @@ bool make_map_bf16(CUtensorMap* map, const void* base, uint64_t cols, uint64_t r
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+int group_of(const mla_problem& pr) {
+  return row_set_group(pr.q_len, pr.num_heads, pr.kv_dtype, pr.topk_width);
+}
+
 int decode_mode(const mla_problem& pr) {
   if (pr.kv_dtype == MLA_KV_FP8_E4M3_E8M0) return kModeDenseFp8;
   if (pr.kv_dtype == MLA_KV_FP4_E2M1_E8M0) return kModeDenseFp4;
-  return pr.topk_width > 0 ? kModeSparseBf16 : kModeDenseBf16;
+  if (pr.topk_width > 0) return kModeSparseBf16;
+  return group_of(pr) >= 2 ? kModeDenseMulti : kModeDenseBf16;
+}
+
+// row sets: one per (request, group of draft tokens)
+int32_t num_row_sets(const mla_problem& pr) {
+  const int32_t g = group_of(pr);
+  return pr.batch * ((pr.q_len + g - 1) / g);
 }
 
 int validate_problem(const mla_problem* pr) {
@@ -92,11 +103,14 @@ int validate_problem(const mla_problem* pr) {
 int64_t stream_tiles_host(const mla_problem& pr, const int32_t* seq_lens) {
   int64_t total = 0;
   const int32_t max_tokens = pr.max_pages_per_seq * pr.page_size;
-  for (int b = 0; b < pr.batch; ++b)
-    for (int j = 0; j < pr.q_len; ++j) {
-      const int32_t len = stream_len(seq_lens[b], pr.q_len, j, pr.causal, pr.topk_width, max_tokens);
-      total += (len + kTile - 1) / kTile;
-    }
+  const int32_t g = group_of(pr);
+  const int32_t S = num_row_sets(pr);
+  for (int32_t s = 0; s < S; ++s) {
+    const StreamGeom gm = stream_geom(s, pr.q_len, g);
+    const int32_t len = stream_len(seq_lens[gm.b], pr.q_len, gm.j0 + gm.nq - 1, pr.causal,
+                                   pr.topk_width, max_tokens);
+    total += (len + kTile - 1) / kTile;
+  }
   return total;
 }
 
@@ -116,6 +130,8 @@ void fill_combine_params(const mla_plan& plan, const uint8_t* ws, const int32_t*
   p.max_pages = pr.max_pages_per_seq;
   p.topk_width = pr.topk_width;
   p.causal = pr.causal;
+  p.group = group_of(pr);
+  p.rows = p.group * pr.num_heads;
   p.num_streams = plan.num_streams;
   p.num_ctas = plan.num_ctas;
 }
@@ -124,7 +140,7 @@ int plan_check(const mla_plan* plan) {
   if (plan == nullptr) return MLA_ERR_INVALID_ARGUMENT;
   const int rc = validate_problem(&plan->problem);
   if (rc != MLA_OK) return rc;
-  if (plan->num_streams != plan->problem.batch * plan->problem.q_len || plan->num_ctas < 1)
+  if (plan->num_streams != num_row_sets(plan->problem) || plan->num_ctas < 1)
     return MLA_ERR_INVALID_ARGUMENT;
   return MLA_OK;
 }
@@ -156,8 +172,9 @@ int mla_decode_plan(const mla_problem* problem, const int32_t* seq_lens_host, in
   std::memset(&pl, 0, sizeof(pl));
   pl.problem = *problem;
   const mla_problem& pr = pl.problem;
-  pl.num_streams = pr.batch * pr.q_len;
-  const int heads_pad = (pr.num_heads + 15) / 16 * 16;
+  pl.num_streams = num_row_sets(pr);
+  const int rows = group_of(pr) * pr.num_heads;   // rows of a full row set
+  const int heads_pad = (rows + 15) / 16 * 16;
   int64_t tiles = 0;
   if (seq_lens_host != nullptr) {
     for (int b = 0; b < pr.batch; ++b)
@@ -174,9 +191,9 @@ int mla_decode_plan(const mla_problem* problem, const int32_t* seq_lens_host, in
   if (pl.smem_bytes > 232448) return MLA_ERR_UNSUPPORTED;
   int64_t off = 0;
   pl.ws_partial_o = off;
-  off = align_up(off + static_cast<int64_t>(pl.num_slots) * pr.num_heads * kDc * 4, kAlign);
+  off = align_up(off + static_cast<int64_t>(pl.num_slots) * rows * kDc * 4, kAlign);
   pl.ws_partial_lse = off;
-  off = align_up(off + static_cast<int64_t>(pl.num_slots) * pr.num_heads * 4, kAlign);
+  off = align_up(off + static_cast<int64_t>(pl.num_slots) * rows * 4, kAlign);
   pl.ws_counters = off;
   off = align_up(off + static_cast<int64_t>(pl.num_streams) * 4, kAlign);
   pl.ws_status = off;
@@ -195,8 +212,9 @@ int mla_q_absorb(const mla_plan* plan, const void* q_nope, const void* q_rope, c
     return MLA_ERR_MISALIGNED;
   const cudaError_t err = launch_q_absorb(
       static_cast<const uint16_t*>(q_nope), static_cast<const uint16_t*>(q_rope),
-      static_cast<const uint16_t*>(w_uk), static_cast<uint16_t*>(q_hat), plan->num_streams,
-      plan->problem.num_heads, reinterpret_cast<cudaStream_t>(stream));
+      static_cast<const uint16_t*>(w_uk), static_cast<uint16_t*>(q_hat),
+      plan->problem.batch * plan->problem.q_len, plan->problem.num_heads,
+      reinterpret_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
@@ -237,7 +255,9 @@ int mla_decode_run(const mla_plan* plan, const void* q_hat, const void* kv_cache
   p.batch = pr.batch;
   p.q_len = pr.q_len;
   p.heads = pr.num_heads;
-  p.heads_pad = (pr.num_heads + 15) / 16 * 16;
+  p.group = group_of(pr);
+  p.rows = p.group * pr.num_heads;
+  p.heads_pad = (p.rows + 15) / 16 * 16;
   p.page_size = pr.page_size;
   p.num_pages = pr.num_pages;
   p.max_pages = pr.max_pages_per_seq;

@@ -25,7 +25,7 @@ __device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
 }  // namespace
 
 // ----------------------------------------------------------------------------
-// combine: one block per (row set, head); thread t owns latent dims
+// combine: one block per (row set, row); thread t owns latent dims
 // [4t, 4t + 4).  Launched as a programmatic dependent of the decode kernel:
 // the work split is derived from seq_lens while the decode runs, then every
 // block waits for the decode grid (whose partials it reads) before touching
@@ -39,7 +39,7 @@ constexpr int kCombineThreads = 128;   // x 4 dims = 512 latent dims
 
 __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(const CombineParams p) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int s = blockIdx.x, h = blockIdx.y;
+  const int s = blockIdx.x, h = blockIdx.y;   // row h of row set s (a head, or draft x head)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = p.num_streams;
   const int max_tokens = p.max_pages * p.page_size;
@@ -47,8 +47,9 @@ __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(const Comb
   // cost before stream s and in total (the decode grid's split)
   int64_t before = 0, tot = 0;
   for (int t = tid; t < S; t += kCombineThreads) {
-    const int b = t / p.q_len, j = t - b * p.q_len;
-    const int32_t len = stream_len(p.seq_lens[b], p.q_len, j, p.causal, p.topk_width, max_tokens);
+    const StreamGeom gt = stream_geom(t, p.q_len, p.group);
+    const int32_t len = stream_len(p.seq_lens[gt.b], p.q_len, gt.j0 + gt.nq - 1, p.causal,
+                                   p.topk_width, max_tokens);
     const int64_t n = stream_cost((len + kTile - 1) / kTile);
     tot += n;
     if (t < s) before += n;
@@ -64,8 +65,10 @@ __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(const Comb
 #pragma unroll
   for (int w = 0; w < kCombineThreads / 32; ++w) { before += red64[0][w]; tot += red64[1][w]; }
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int b = s / p.q_len, j = s - b * p.q_len;
-  const int32_t len = stream_len(p.seq_lens[b], p.q_len, j, p.causal, p.topk_width, max_tokens);
+  const StreamGeom gm = stream_geom(s, p.q_len, p.group);
+  if (h >= gm.nq * p.heads) return;   // a short last group of draft tokens
+  const int32_t len = stream_len(p.seq_lens[gm.b], p.q_len, gm.j0 + gm.nq - 1, p.causal,
+                                 p.topk_width, max_tokens);
   const int64_t ntiles = (len + kTile - 1) / kTile;
   if (ntiles == 0) return;   // the decode wrote o_lat = 0, lse = -inf
   const int c0 = tile_owner(tile_cost_pos(before, 0), tot, p.num_ctas);
@@ -76,11 +79,12 @@ __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(const Comb
   // thread's 4 dims loaded together): running max m, sum = sum_i exp(lse_i -
   // m), acc = sum_i exp(lse_i - m) o_i, rescaled when m grows; finally
   // lse = m + ln(sum), o = acc / sum.
-  const float* plse = p.part_lse + static_cast<int64_t>(s + c0) * p.heads + h;
+  // partial slots hold p.rows rows each
+  const float* plse = p.part_lse + static_cast<int64_t>(s + c0) * p.rows + h;
   const float4* po = reinterpret_cast<const float4*>(p.part_o) +
-                     (static_cast<int64_t>(s + c0) * p.heads + h) * (kDc / 4) + tid;
-  const int64_t lstride = p.heads;
-  const int64_t ostride = static_cast<int64_t>(p.heads) * (kDc / 4);
+                     (static_cast<int64_t>(s + c0) * p.rows + h) * (kDc / 4) + tid;
+  const int64_t lstride = p.rows;
+  const int64_t ostride = static_cast<int64_t>(p.rows) * (kDc / 4);
   float m = -INFINITY, sum = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int k0 = 0; k0 < nseg; k0 += 8) {
@@ -113,14 +117,15 @@ __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(const Comb
   const float lse = (m == -INFINITY) ? -INFINITY : m + __logf(sum);
   const float inv = (m == -INFINITY) ? 0.f : 1.f / sum;
   acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
-  reinterpret_cast<float4*>(p.o_lat + (static_cast<int64_t>(s) * p.heads + h) * kDc)[tid] = acc;
-  if (tid == 0) p.lse[static_cast<int64_t>(s) * p.heads + h] = lse;
+  const int64_t row = (static_cast<int64_t>(gm.b) * p.q_len + gm.j0) * p.heads + h;
+  reinterpret_cast<float4*>(p.o_lat + row * kDc)[tid] = acc;
+  if (tid == 0) p.lse[row] = lse;
 }
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {
   if (p.num_streams == 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.num_streams, p.heads);
+  cfg.gridDim = dim3(p.num_streams, p.rows);
   cfg.blockDim = dim3(kCombineThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;

@@ -70,6 +70,18 @@ struct ModeTraits {
   static constexpr int kRowBytes = kFp4 ? kFp4RowBytes : kFp8RowBytes;    // quantised row
   static constexpr int kRawTileBytes = kTile * kRowBytes;
   static constexpr bool kSparse = kMode == kModeSparseBf16;
+  static constexpr bool kMulti = kMode == kModeDenseMulti;
+  // dense bf16 staging (TMA tiles, dead rows zeroed by the softmax warps)
+  static constexpr bool kDenseBf16 = kMode == kModeDenseBf16 || kMulti;
+  // the first softmax warp whose TMEM lanes hold rows: row r of a row set is
+  // M-row 16 * kRowWarp0 + r of the QK accumulator
+  static constexpr int kRowWarp0 = kMulti ? 1 : 2;
+  // TMEM columns: q_hat (all 576 values, or the 512 latent ones when the
+  // RoPE part is a shared-memory operand), S (64), O^T (4 x heads_pad)
+  static constexpr uint32_t kColQ = 0;
+  static constexpr uint32_t kColS = kMulti ? 256 : 288;
+  static constexpr uint32_t kColO = kColS + 64;
+  static constexpr int kQTmemChunks = kMulti ? kChunks - 1 : kChunks;
   static constexpr int kThreads = kQuant    ? 32 * (kDequantWarp0 + kDequantWarps)
                                   : kSparse ? 32 * (kGatherWarp0 + kGatherWarps)
                                             : 192;
@@ -78,6 +90,7 @@ struct ModeTraits {
   // kRawTileBytes of the stage it is dequantised into.
   static constexpr bool kRawRing = kFp8;
   static constexpr int kNumStages = kRawRing ? kFp8Stages : kStages;   // bf16 tiles in flight
+  static constexpr int kQBatch = kThreads > 192 ? 3 : (kMulti ? 4 : 5);   // q_hat chunks per load batch
   static constexpr int kRawSlots = kRawRing ? kFp8RawSlots : kStages;
   static constexpr int kRawOffset = kTileBytes - kRawTileBytes;
 };
@@ -86,11 +99,10 @@ constexpr float kRescaleThreshold = 8.0f;           // log2 units: rescale if ma
 constexpr float kLn2 = 0.6931471805599453f;
 
 // Tensor memory columns (512 allocated): q_hat as the QK A operand (M=64
-// layout, 576 bf16 = 288 columns), S (64 token columns), O^T (4 x 32).
+// layout, 576 bf16 = 288 columns; 256 in the multi-token mode), S (64 token
+// columns), O^T (4 x padded rows).
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColQ = 0;
-constexpr uint32_t kColS = 288;
-constexpr uint32_t kColO = 352;
+constexpr int kQRopeBytes = 64 * 128;   // multi-token mode: RoPE part of q_hat, 64 M-rows x 128 B
 
 // Control block placed after the data buffers in shared memory.
 struct __align__(8) Ctrl {
@@ -110,8 +122,8 @@ struct __align__(8) Ctrl {
   uint32_t tmem_base;
   int32_t abort_flag;
   int32_t rescale_tile[2];
-  float alpha[2][kMaxHeads];
-  float l_final[kMaxHeads];
+  float alpha[2][kMaxRows];
+  float l_final[kMaxRows];
 };
 
 __device__ __forceinline__ void set_status(uint32_t* status, uint32_t bits) {
@@ -246,50 +258,70 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
 }
 
-// Write stream s's absorbed queries into TMEM as the M=64 A operand.  Head
-// h sits in row 32 + h, i.e. lane 64 + h for h < 16 and lane 96 + (h - 16)
-// for 16 <= h < 32 (row r of the M=64 layout lives in lane
-// (r/16)*32 + r%16), so only softmax warps 2 and 3 hold heads and warps 0
-// and 1 leave their SM sub-partitions to the producer and MMA warps.
-// Called by warps 2 and 3 (each writes its own lane quarter); 576 bf16 are
-// packed two per column; rows of absent heads are written as zeros.  The
-// loads go in two batches (5 + 4 chunks of 64 values) to keep many in flight.
-__device__ __forceinline__ void load_q_tmem(const uint16_t* q_hat, int32_t s, int H,
-                                            uint32_t taddr_lane, int lane, int w) {
-  const int h = (w - 2) * 16 + (lane & 15);
-  const bool live = lane < 16 && h < H;
-  const uint4* src =
-      reinterpret_cast<const uint4*>(q_hat + (static_cast<int64_t>(s) * H + (live ? h : 0)) * kDqk);
+// Write a row set's absorbed queries (q_hat rows q_rows .. q_rows + nrows)
+// as the QK A operand.  Row r of the set is M-row 16 * kRowWarp0 + r of the
+// M=64 layout, which lives in TMEM lane (m/16)*32 + m%16: lanes 0-15 of
+// softmax warp kRowWarp0 + r/16.  Heads of a one-token row set sit in rows
+// 32 + h (warps 2 and 3 only, so warps 0 and 1 leave their SM sub-partitions
+// to the producer and MMA warps) with all 576 values in TMEM, packed two per
+// column.  A multi-token row set (up to 48 rows) starts at M-row 16 (warps
+// 1-3); its 512 latent values go to TMEM and its 64 RoPE values to a
+// shared-memory operand (row m at m * 128 bytes, 16-byte units swizzled by
+// m % 8), where M-rows without a row are written as zeros.  Every softmax
+// warp calls this; absent rows get zeros.  TMEM loads go in batches of
+// kBatch chunks of 64 values to keep many in flight (fewer in the kernels
+// whose thread count leaves fewer registers per thread).
+template <bool kMulti, int kBatch>
+__device__ __forceinline__ void load_q(const uint16_t* q_rows, int nrows, uint32_t taddr_lane,
+                                       uint8_t* q_rope, int lane, int w) {
+  constexpr int kRowWarp0 = kMulti ? 1 : 2;
+  constexpr int kTmemChunks = kMulti ? kChunks - 1 : kChunks;
+  const int r = (w - kRowWarp0) * 16 + (lane & 15);
+  const bool live = w >= kRowWarp0 && lane < 16 && r < nrows;
+  const uint4* src = reinterpret_cast<const uint4*>(q_rows + static_cast<int64_t>(live ? r : 0) * kDqk);
+  if (w >= kRowWarp0) {
 #pragma unroll
-  for (int cb = 0; cb < kChunks; cb += 5) {
-    const int n = (cb == 0) ? 5 : 4;
-    uint4 v[5][8];
+    for (int cb = 0; cb < kTmemChunks; cb += kBatch) {
+      const int n = (kTmemChunks - cb) < kBatch ? (kTmemChunks - cb) : kBatch;
+      uint4 v[kBatch][8];
 #pragma unroll
-    for (int c = 0; c < 5; ++c)
+      for (int c = 0; c < kBatch; ++c)
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        v[c][q] = (live && c < n) ? __ldg(src + (cb + c) * 8 + q) : make_uint4(0, 0, 0, 0);
+        for (int q = 0; q < 8; ++q)
+          v[c][q] = (live && c < n) ? __ldg(src + (cb + c) * 8 + q) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-    for (int c = 0; c < 5; ++c) {
-      if (c < n) {
-        uint32_t r[32];
+      for (int c = 0; c < kBatch; ++c) {
+        if (c < n) {
+          uint32_t rr[32];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          r[4 * q] = v[c][q].x;
-          r[4 * q + 1] = v[c][q].y;
-          r[4 * q + 2] = v[c][q].z;
-          r[4 * q + 3] = v[c][q].w;
+          for (int q = 0; q < 8; ++q) {
+            rr[4 * q] = v[c][q].x;
+            rr[4 * q + 1] = v[c][q].y;
+            rr[4 * q + 2] = v[c][q].z;
+            rr[4 * q + 3] = v[c][q].w;
+          }
+          tmem_st32(taddr_lane + (cb + c) * 32, rr);
         }
-        tmem_st32(taddr_lane + kColQ + (cb + c) * 32, r);
+      }
+    }
+  }
+  if constexpr (kMulti) {
+    if (lane < 16) {
+      const int m = 16 * w + lane;
+      uint8_t* row = q_rope + m * 128;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint4 v = live ? __ldg(src + (kChunks - 1) * 8 + u) : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(row + ((u ^ (m & 7)) << 4)) = v;
       }
     }
   }
 }
 
-// Ask L2 to fetch stream s's absorbed queries ahead of their TMEM load.
-__device__ __forceinline__ void prefetch_q(const uint16_t* q_hat, int32_t s, int H, int t, int nt) {
-  const char* base = reinterpret_cast<const char*>(q_hat + static_cast<int64_t>(s) * H * kDqk);
-  const int lines = (H * kDqk * 2 + 127) / 128;
+// Ask L2 to fetch a row set's absorbed queries ahead of their load.
+__device__ __forceinline__ void prefetch_q(const uint16_t* q_rows, int nrows, int t, int nt) {
+  const char* base = reinterpret_cast<const char*>(q_rows);
+  const int lines = (nrows * kDqk * 2 + 127) / 128;
   for (int i = t; i < lines; i += nt)
     asm volatile("prefetch.global.L2 [%0];" ::"l"(base + static_cast<int64_t>(i) * 128));
 }
@@ -447,7 +479,10 @@ DecodeLayout decode_layout(int heads, int heads_pad, int num_streams, int mode) 
   L.off_raw = (ring ? kFp8Stages : kStages) * kTileBytes;
   (void)heads_pad;
   L.off_p = L.off_stage + kPChunkOffset;     // first stage's P; stride kTileBytes
-  L.off_ctrl = L.off_raw + (ring ? kFp8RawSlots * kFp8TileBytes : 0);
+  // the multi-token mode's RoPE query operand (1024-byte aligned after the stages)
+  L.off_qrope = L.off_raw;
+  L.off_ctrl = L.off_raw + (ring ? kFp8RawSlots * kFp8TileBytes : 0) +
+               (mode == kModeDenseMulti ? kQRopeBytes : 0);
   L.total = L.off_ctrl + static_cast<int>(sizeof(Ctrl)) + 2 * (num_streams + 1) * 4;
   return L;
 }
@@ -464,6 +499,7 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* sStage = smem + L.off_stage;
   uint8_t* sRaw = smem + L.off_raw;   // FP8 raw ring
+  uint8_t* sQr = smem + L.off_qrope;  // multi-token mode: RoPE part of q_hat
   Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + L.off_ctrl);
   int32_t* prefix = reinterpret_cast<int32_t*>(smem + L.off_ctrl + sizeof(Ctrl));  // tiles
   int32_t* cprefix = prefix + (p.num_streams + 1);                                   // cost
@@ -474,6 +510,8 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
   const int S = p.num_streams;
   const int H = p.heads;
   const int NP = p.heads_pad;
+  const int G = p.group;
+  const int RMAX = p.rows;     // rows of a full row set (partial-slot stride)
   const int max_tokens = p.max_pages * p.page_size;
   volatile int32_t* abort_flag = &ctrl->abort_flag;
 
@@ -512,11 +550,12 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
     tmem_alloc(&ctrl->tmem_base, kTmemCols);
     tmem_relinquish();
   }
-  if (warp == kProducerWarp && lane == 0 && kMode == kModeDenseBf16) prefetch_tmap(&kv_map);
+  if (warp == kProducerWarp && lane == 0 && MT::kDenseBf16) prefetch_tmap(&kv_map);
   // tiles and cost per stream (stream lengths from the device seq_lens)
   for (int s = tid; s < S; s += kThreads) {
-    const int b = s / p.q_len, j = s - b * p.q_len;
-    const int32_t len = stream_len(p.seq_lens[b], p.q_len, j, p.causal, p.topk_width, max_tokens);
+    const StreamGeom gm = stream_geom(s, p.q_len, G);
+    const int32_t len = stream_len(p.seq_lens[gm.b], p.q_len, gm.j0 + gm.nq - 1, p.causal,
+                                   p.topk_width, max_tokens);
     const int32_t nt = (len + kTile - 1) / kTile;
     prefix[s + 1] = nt;
     cprefix[s + 1] = stream_cost(nt);
@@ -563,10 +602,13 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
       for (int32_t i = 0; i < ntiles; ++i) {
         const int stage = i % kNumStages;
         const uint32_t reuse_parity = ((i / kNumStages) - 1) & 1;
-        const int b = wk.s / p.q_len, j = wk.s - b * p.q_len;
+        // a row set covers query tokens j0 .. j0 + nq - 1: its tiles reach
+        // the visible window of the last one
+        const StreamGeom gm = stream_geom(wk.s, p.q_len, G);
+        const int b = gm.b, j = gm.j0 + gm.nq - 1;
         uint8_t* dst = sStage + stage * kTileBytes;
         // Describe the tile first: its global lookups overlap the stage wait.
-        if constexpr (kMode == kModeDenseBf16) {
+        if constexpr (MT::kDenseBf16) {
           if (p.page_size >= kTile) {
             // one page holds the whole tile: one lane describes it
             int32_t row0 = 0;
@@ -744,6 +786,8 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
       const uint64_t pv_a0 = make_smem_desc(smem_u32(sStage), kChunkBytes, 1024, kSmemLayoutSW128);
       const uint64_t pv_b0 = make_smem_desc(smem_u32(sStage + kPChunkOffset), 16, 1024,
                                             kSmemLayoutSW128);
+      // multi-token mode: QK's RoPE steps read A (64 M-rows x 64 values, K-major)
+      const uint64_t qr_a0 = make_smem_desc(smem_u32(sQr), 16, 1024, kSmemLayoutSW128);
       // Single-thread event loop: issue PV(pv) as soon as its P is written
       // (checked first: it releases a stage), and QK(qk) once its tile, the
       // stream's q_hat and the S buffer are ready.  QK(qk) is only issued
@@ -775,7 +819,7 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
               for (int mt = 0; mt < 4; ++mt) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                  mma_bf16_ss(tmem + kColO + mt * NP, a0 + ((2 * mt * kChunkBytes + kk * 2048) >> 4),
+                  mma_bf16_ss(tmem + MT::kColO + mt * NP, a0 + ((2 * mt * kChunkBytes + kk * 2048) >> 4),
                               b0 + ((kk * 32) >> 4), idesc_pv, (first && kk == 0) ? 0u : 1u);
               }
               mma_commit(&ctrl->empty[st]);
@@ -800,11 +844,18 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
               tc_fence_after();
               const uint64_t b0 = qk_b0 + static_cast<uint64_t>((st * kTileBytes) >> 4);
 #pragma unroll
-              for (int ch = 0; ch < kChunks; ++ch) {
+              for (int ch = 0; ch < MT::kQTmemChunks; ++ch) {
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                  mma_bf16_ts(tmem + kColS, tmem + kColQ + (ch * 4 + k) * 8,
+                  mma_bf16_ts(tmem + MT::kColS, tmem + MT::kColQ + (ch * 4 + k) * 8,
                               b0 + ((ch * kChunkBytes + k * 32) >> 4), idesc_qk, (ch | k) ? 1u : 0u);
+              }
+              if constexpr (MT::kMulti) {
+                // RoPE dims: A = the shared-memory rows of q_hat's RoPE part
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                  mma_bf16_ss(tmem + MT::kColS, qr_a0 + ((k * 32) >> 4),
+                              b0 + (((kChunks - 1) * kChunkBytes + k * 32) >> 4), idesc_qk, 1u);
               }
               mma_commit(&ctrl->s_full);
               wq.next(prefix, S);
@@ -965,7 +1016,8 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
       for (int32_t i = 0; i < ntiles; ++i) {
         const int stage = i % kNumStages;
         const uint32_t reuse_parity = ((i / kNumStages) - 1) & 1;
-        const int b = wk.s / p.q_len, j = wk.s - b * p.q_len;
+        const StreamGeom gm = stream_geom(wk.s, p.q_len, G);   // one query token per row set
+        const int b = gm.b, j = gm.j0;
         uint8_t* dst = sStage + stage * kTileBytes;
         const int32_t T = min(max(p.seq_lens[b], 0), max_tokens);
         const int32_t window = p.causal ? min(max(T - p.q_len + j + 1, 0), T) : T;
@@ -1023,19 +1075,18 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
       // sparse mode: the gather warps stage the tiles
     } else {
       // ============================================================ softmax
-      // Warp w reads TMEM lanes [32w, 32w+32).  Head h is S row 32 + h: in
-      // the M=64 accumulator layout (row r in lane (r/16)*32 + r%16) heads
-      // 0..15 are lanes 0..15 of warp 2 and heads 16..31 lanes 0..15 of warp
-      // 3; lanes 16..31 hold no row, so lane l + 16 takes the upper 32 token
-      // columns of lane l's head (one shuffle per column) and the pair
-      // combines max and sum.  Warps 0 and 1 only join the epilogue, the
-      // rescale and the dead-row zeroing.
+      // Warp w reads TMEM lanes [32w, 32w+32).  Row h of the row set (a head,
+      // or (draft token h / H, head h % H) in the multi-token mode) is S row
+      // 16 * kRowWarp0 + h: in the M=64 accumulator layout (row r in lane
+      // (r/16)*32 + r%16) rows 0..15 are lanes 0..15 of warp kRowWarp0, and
+      // so on; lanes 16..31 hold no row, so lane l + 16 takes the upper 32
+      // token columns of lane l's row (one shuffle per column) and the pair
+      // combines max and sum.  Warps below kRowWarp0 only join the epilogue,
+      // the rescale and the dead-row zeroing.
       const int w = warp;
       const int hl = lane & 15;
       const int half = lane >> 4;
-      const int h = (w - 2) * 16 + hl;
-      const bool warp_has_heads = w >= 2 && (w - 2) * 16 < H;
-      const bool owner = warp_has_heads && h < H;
+      const int h = (w - MT::kRowWarp0) * 16 + hl;
       const uint32_t lane_base = static_cast<uint32_t>(w * 32) << 16;
       const float scale = p.scale_log2;
       // l_run sums the bf16-rounded P the PV uses (it normalises O); l_exp
@@ -1044,22 +1095,48 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
       Walker wk;
       wk.init(prefix, S, g0);
       bool failed = false;
+      // q_hat / o_lat rows of row set s and how many there are
+      auto first_row = [&](int32_t s) -> int64_t {
+        const StreamGeom gm = stream_geom(s, p.q_len, G);
+        return (static_cast<int64_t>(gm.b) * p.q_len + gm.j0) * H;
+      };
+      auto rows_of = [&](int32_t s) -> int { return stream_geom(s, p.q_len, G).nq * H; };
       // the first stream's queries
-      if (w >= 2) load_q_tmem(p.q_hat, wk.s, H, tmem + lane_base, lane, w);
+      load_q<MT::kMulti, MT::kQBatch>(p.q_hat + first_row(wk.s) * kDqk, rows_of(wk.s),
+                                      tmem + lane_base, sQr, lane, w);
+      if constexpr (MT::kMulti) fence_proxy_async_smem();   // RoPE rows -> tensor-core reads
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctrl->q_ready);
+      // rows of the current row set (one per head outside the multi-token mode)
+      int nrows = H;
+      bool warp_has_heads = w >= MT::kRowWarp0 && (w - MT::kRowWarp0) * 16 < H;
+      bool owner = warp_has_heads && h < H;
+      int32_t win_end = 0;    // multi-token mode: this thread's row sees positions below this
       for (int32_t i = 0; i < ntiles; ++i) {
         const int stage = i % kNumStages;
         const int pb = i & 1;
         const bool first = (i == 0) || (wk.lt == 0);
         const bool last = (i == ntiles - 1) || (wk.lt == wk.ntiles - 1);
-        if (first && w < 2) {
-          // warm L2 with the next stream's queries (loaded into TMEM when
-          // this segment ends)
-          int32_t sn = wk.s + 1;
-          while (sn < S && prefix[sn + 1] == prefix[sn]) ++sn;
-          if (sn < S && prefix[sn] < g1) prefetch_q(p.q_hat, sn, H, tid, 64);
+        if (first) {
+          if constexpr (MT::kMulti) {
+            const StreamGeom gm = stream_geom(wk.s, p.q_len, G);
+            nrows = gm.nq * H;
+            warp_has_heads = w >= MT::kRowWarp0 && (w - MT::kRowWarp0) * 16 < nrows;
+            owner = warp_has_heads && h < nrows;
+            // draft token j0 + h / H sees positions up to its own causal
+            // limit; the row set's tiles reach the last token's limit
+            const int jj = owner ? h / H : gm.nq - 1;
+            win_end = stream_len(p.seq_lens[gm.b], p.q_len, gm.j0 + jj, p.causal, 0, max_tokens);
+          }
+          if (w < MT::kRowWarp0) {
+            // warm L2 with the next stream's queries (loaded when this
+            // segment ends)
+            int32_t sn = wk.s + 1;
+            while (sn < S && prefix[sn + 1] == prefix[sn]) ++sn;
+            if (sn < S && prefix[sn] < g1)
+              prefetch_q(p.q_hat + first_row(sn) * kDqk, rows_of(sn), tid, 32 * MT::kRowWarp0);
+          }
         }
         bool ok = !failed && warp_wait(&ctrl->full[stage], (i / kNumStages) & 1, abort_flag);
         const uint64_t mask = ctrl->mask[stage];
@@ -1069,10 +1146,10 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
           float y[32];
           if (warp_has_heads) {
             uint32_t r[32];
-            tmem_ld32(tmem + lane_base + kColS, r);
+            tmem_ld32(tmem + lane_base + MT::kColS, r);
 #pragma unroll
             for (int t = 0; t < 32; ++t) y[t] = __uint_as_float(r[t]);
-            tmem_ld32(tmem + lane_base + kColS + 32, r);
+            tmem_ld32(tmem + lane_base + MT::kColS + 32, r);
 #pragma unroll
             for (int t = 0; t < 32; ++t) {
               const float hi_col = __shfl_xor_sync(0xffffffffu, __uint_as_float(r[t]), 16);
@@ -1088,14 +1165,21 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
             // completed, so nothing reads the old queries any more.
             Walker nx = wk;
             nx.next(prefix, S);
-            if (w >= 2) load_q_tmem(p.q_hat, nx.s, H, tmem + lane_base, lane, w);
+            load_q<MT::kMulti, MT::kQBatch>(p.q_hat + first_row(nx.s) * kDqk, rows_of(nx.s),
+                                            tmem + lane_base, sQr, lane, w);
+            if constexpr (MT::kMulti) fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctrl->q_ready);
           }
           if (ok && warp_has_heads) {
             // token of y[t] is 32*half + t
-            const uint32_t hmask = static_cast<uint32_t>(mask >> (32 * half));
+            uint32_t hmask = static_cast<uint32_t>(mask >> (32 * half));
+            if constexpr (MT::kMulti) {
+              // this row's own causal limit inside the tile
+              const int32_t lim = win_end - wk.lt * kTile - 32 * half;
+              hmask &= lim <= 0 ? 0u : (lim >= 32 ? ~0u : ((1u << lim) - 1u));
+            }
             float mt = -INFINITY;
             if (hmask == 0xffffffffu) {
 #pragma unroll
@@ -1145,7 +1229,7 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
             l_exp += lsum_exp + __shfl_xor_sync(0xffffffffu, lsum_exp, 16);
             if (owner && half == 0) ctrl->alpha[pb][h] = alpha;
           }
-          if constexpr (kMode == kModeDenseBf16) {
+          if constexpr (MT::kDenseBf16) {
             // Dead rows (tail slots, bad pages): P is 0 there but 0 * NaN
             // would poison the PV sum, so zero their latent values.  (The
             // sparse producer zero-fills them; the FP8 dequant writes zeros.)
@@ -1170,14 +1254,14 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
           if (ok) {
             tc_fence_after();
             for (int mt = 0; mt < 4; ++mt) {
-              for (int hb = 0; hb < H; hb += 16) {
+              for (int hb = 0; hb < nrows; hb += 16) {
                 uint32_t v[16];
-                const uint32_t addr = tmem + lane_base + kColO + mt * NP + hb;
+                const uint32_t addr = tmem + lane_base + MT::kColO + mt * NP + hb;
                 tmem_ld16(addr, v);
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                   const int hh = hb + e;
-                  const float a = hh < H ? ctrl->alpha[pb][hh] : 1.f;
+                  const float a = hh < nrows ? ctrl->alpha[pb][hh] : 1.f;
                   v[e] = __float_as_uint(__uint_as_float(v[e]) * a);
                 }
                 tmem_st16(addr, v);
@@ -1207,10 +1291,11 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
               tile_cost_pos(cprefix[s], prefix[s + 1] - prefix[s] - 1), ucost, p.num_ctas);
           const bool split = c_first != c_last;
           // an unsplit stream's result is final: straight to the outputs
-          float* dst_o = split ? p.part_o + static_cast<int64_t>(s + c) * H * kDc
-                               : p.o_lat + static_cast<int64_t>(s) * H * kDc;
-          float* dst_lse = split ? p.part_lse + static_cast<int64_t>(s + c) * H
-                                 : p.lse + static_cast<int64_t>(s) * H;
+          // (partial slots hold RMAX rows each)
+          float* dst_o = split ? p.part_o + static_cast<int64_t>(s + c) * RMAX * kDc
+                               : p.o_lat + first_row(s) * kDc;
+          float* dst_lse = split ? p.part_lse + static_cast<int64_t>(s + c) * RMAX
+                                 : p.lse + first_row(s);
           if (ok && owner && half == 0) {
             ctrl->l_final[h] = l_run > 0.f ? 1.f / l_run : 0.f;   // o = O / l
             dst_lse[h] = l_run > 0.f ? (m_used + __log2f(l_exp)) * kLn2 : -INFINITY;
@@ -1219,13 +1304,13 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
           tc_fence_after();
           for (int mt = 0; mt < 4; ++mt) {
             const int d = mt * 128 + w * 32 + lane;
-            for (int hb = 0; hb < H; hb += 16) {
+            for (int hb = 0; hb < nrows; hb += 16) {
               uint32_t v[16];
-              tmem_ld16(tmem + lane_base + kColO + mt * NP + hb, v);
+              tmem_ld16(tmem + lane_base + MT::kColO + mt * NP + hb, v);
 #pragma unroll
               for (int e = 0; e < 16; ++e) {
                 const int hh = hb + e;
-                if (hh < H) dst_o[static_cast<int64_t>(hh) * kDc + d] = __uint_as_float(v[e]) * ctrl->l_final[hh];
+                if (hh < nrows) dst_o[static_cast<int64_t>(hh) * kDc + d] = __uint_as_float(v[e]) * ctrl->l_final[hh];
               }
             }
           }
@@ -1246,9 +1331,12 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
   // Row sets with no visible token (no tile anywhere): o_lat = 0, lse = -inf.
   for (int s = c; s < S; s += p.num_ctas) {
     if (prefix[s + 1] != prefix[s]) continue;
-    float4* o = reinterpret_cast<float4*>(p.o_lat + static_cast<int64_t>(s) * H * kDc);
-    for (int e = tid; e < H * kDc / 4; e += kThreads) o[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int e = tid; e < H; e += kThreads) p.lse[static_cast<int64_t>(s) * H + e] = -INFINITY;
+    const StreamGeom gm = stream_geom(s, p.q_len, G);
+    const int64_t row0 = (static_cast<int64_t>(gm.b) * p.q_len + gm.j0) * H;
+    const int nr = gm.nq * H;
+    float4* o = reinterpret_cast<float4*>(p.o_lat + row0 * kDc);
+    for (int e = tid; e < nr * kDc / 4; e += kThreads) o[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int e = tid; e < nr; e += kThreads) p.lse[row0 + e] = -INFINITY;
   }
 
   tc_fence_before();
@@ -1284,6 +1372,13 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap* kv_map, int 
       if (err != cudaSuccess) return err;
       block = dim3(ModeTraits<kModeDenseFp8>::kThreads);
       mla_decode_kernel<kModeDenseFp8><<<grid, block, L.total, stream>>>(*kv_map, p, L);
+      break;
+    case kModeDenseMulti:
+      err = cudaFuncSetAttribute(mla_decode_kernel<kModeDenseMulti>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
+      if (err != cudaSuccess) return err;
+      block = dim3(ModeTraits<kModeDenseMulti>::kThreads);
+      mla_decode_kernel<kModeDenseMulti><<<grid, block, L.total, stream>>>(*kv_map, p, L);
       break;
     case kModeDenseFp4:
       err = cudaFuncSetAttribute(mla_decode_kernel<kModeDenseFp4>,

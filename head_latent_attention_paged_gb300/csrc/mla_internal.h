@@ -23,6 +23,10 @@ constexpr int kFp8RowBytes = kDqk + kDqk / 32;     // 594
 constexpr int kFp4CodeBytes = kDqk / 2;            // 288: two e2m1 codes per byte
 constexpr int kFp4RowBytes = kFp4CodeBytes + kDqk / 16;   // 324
 constexpr int kMaxHeads = 32;     // TMEM: q_hat 288 + S 64 + O^T 4 x 32 columns
+// Dense multi-token mode: G query tokens of one request share a row set of
+// G * H <= 48 rows (TMEM: latent q_hat 256 + S 64 + O^T 4 x 48 columns; the
+// RoPE part of q_hat is a shared-memory operand).
+constexpr int kMaxRows = 48;
 constexpr int kMaxStreams = 256;  // per-stream tile prefix kept in shared memory
 // 72 KB bf16 tiles in flight per CTA.  An FP4 tile of quantised rows
 // (20,736 B) is copied into the tail of the stage it is dequantised into;
@@ -37,6 +41,7 @@ enum DecodeMode : int {
   kModeSparseBf16 = 1,
   kModeDenseFp8 = 2,
   kModeDenseFp4 = 3,
+  kModeDenseMulti = 4,   // bf16, q_len > 1: draft tokens of a request share each staged tile
 };
 
 struct DecodeParams {
@@ -50,14 +55,16 @@ struct DecodeParams {
   float* o_lat;                 // [S][H][512] output
   float* lse;                   // [S][H] output
   uint32_t* status;
-  int32_t batch, q_len, heads, heads_pad;  // heads_pad: N of the PV MMA (multiple of 16)
+  int32_t batch, q_len, heads, heads_pad;  // heads_pad: N of the PV MMA (multiple of 16, >= rows)
+  int32_t group;                // query tokens per row set (1, or G >= 2 in the multi-token mode)
+  int32_t rows;                 // rows of a full row set: group * heads
   int32_t page_size, num_pages, max_pages, topk_width, causal;
   int32_t num_streams, num_ctas;
   float scale_log2;             // sm_scale * log2(e)
 };
 
 struct DecodeLayout {   // dynamic shared memory layout of the decode kernel
-  int32_t off_stage, off_raw, off_p, off_ctrl, total;
+  int32_t off_stage, off_raw, off_p, off_qrope, off_ctrl, total;
 };
 
 DecodeLayout decode_layout(int heads, int heads_pad, int num_streams, int mode);
@@ -73,6 +80,7 @@ struct CombineParams {
   float* o_lat;
   float* lse;
   int32_t batch, q_len, heads, page_size, max_pages, topk_width, causal;
+  int32_t group, rows;          // as in DecodeParams
   int32_t num_streams, num_ctas;
 };
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
@@ -94,6 +102,33 @@ cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_q_absorb(const uint16_t* q_nope, const uint16_t* q_rope,
                             const uint16_t* w_uk, uint16_t* q_hat, int rows, int heads,
                             cudaStream_t stream);
+
+// Row set s covers request b and query tokens j0 .. j0 + nq - 1 (the group
+// of `group` consecutive draft tokens; group = 1 outside the multi-token
+// mode).  Its rows are (token j0 + jj, head h) for jj < nq, h < H, i.e. the
+// contiguous rows (b * q_len + j0) * H .. + nq * H of q_hat and o_lat.
+struct StreamGeom {
+  int32_t b, j0, nq;
+};
+__host__ __device__ inline StreamGeom stream_geom(int32_t s, int32_t q_len, int32_t group) {
+  const int32_t ng = (q_len + group - 1) / group;
+  StreamGeom g;
+  g.b = s / ng;
+  g.j0 = (s - g.b * ng) * group;
+  g.nq = q_len - g.j0 < group ? q_len - g.j0 : group;
+  return g;
+}
+
+// Query tokens per row set for a problem: the multi-token mode groups
+// min(q_len, 48 / H) draft tokens of a request when that is at least 2
+// (dense bf16 caches only).
+__host__ __device__ inline int32_t row_set_group(int32_t q_len, int32_t heads, int32_t kv_dtype,
+                                                 int32_t topk_width) {
+  if (kv_dtype != MLA_KV_BF16 || topk_width > 0 || q_len < 2) return 1;
+  const int32_t g = kMaxRows / heads;
+  const int32_t gq = g < q_len ? g : q_len;
+  return gq >= 2 ? gq : 1;
+}
 
 // Tiles of one (request, query token) row set; identical on host and device.
 __host__ __device__ inline int32_t stream_len(int32_t seq_len, int32_t q_len, int32_t j,

@@ -123,12 +123,14 @@ typedef struct {
 /* Filled by mla_decode_plan; treat as opaque, keep it alive while in use. */
 typedef struct {
   mla_problem problem;
-  int32_t num_streams;      /* B * Q: independent (request, query token) row sets */
+  int32_t num_streams;      /* row sets: B * Q (one per request and query token), or
+                               B * ceil(Q / G) when G draft tokens of a request share one
+                               (dense bf16 cache, Q >= 2, G = min(Q, 48 / H) >= 2) */
   int32_t num_ctas;         /* decode grid size */
   int32_t num_slots;        /* partial-result slots: num_streams + num_ctas - 1 */
   int32_t smem_bytes;       /* dynamic shared memory of the decode kernel */
-  int64_t ws_partial_o;     /* byte offset of f32 [num_slots][H][512] */
-  int64_t ws_partial_lse;   /* byte offset of f32 [num_slots][H] */
+  int64_t ws_partial_o;     /* byte offset of f32 [num_slots][G * H][512] */
+  int64_t ws_partial_lse;   /* byte offset of f32 [num_slots][G * H] */
   int64_t ws_counters;      /* byte offset of int32 [num_streams], reserved (left at 0) */
   int64_t ws_status;        /* byte offset of the uint32 status word */
   int64_t workspace_bytes;  /* total workspace size */

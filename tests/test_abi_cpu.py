@@ -119,6 +119,25 @@ def test_fp4_plan_fits_shared_memory(m):
         _problem(m, batch=256, num_heads=32), None, 152).smem_bytes
 
 
+@pytest.mark.parametrize("q_len,heads,group", [(1, 20, 1), (2, 20, 2), (3, 20, 2), (4, 12, 4),
+                                               (2, 24, 2), (2, 32, 1), (6, 8, 6), (7, 8, 6)])
+def test_multi_token_plan_groups_draft_tokens(m, q_len, heads, group):
+    """Dense bf16 problems with q_len >= 2 group G = min(q_len, 48 / H)
+    draft tokens of a request into one row set (G >= 2, else one per token);
+    the partial slots hold G * H rows; every plan fits shared memory."""
+    seq = np.array([100, 1000, 64, 0], dtype=np.int32)
+    plan = m.mla_decode_plan(_problem(m, q_len=q_len, num_heads=heads), seq, 152)
+    assert plan.num_streams == 4 * -(-q_len // group)
+    rows = group * heads
+    assert plan.ws_partial_lse >= plan.num_slots * rows * 512 * 4
+    assert plan.ws_counters >= plan.ws_partial_lse + plan.num_slots * rows * 4
+    assert plan.smem_bytes <= 232448
+    # quantised caches and top-k lists keep one row set per draft token
+    fp8 = m.mla_decode_plan(_problem(m, q_len=q_len, num_heads=heads,
+                                     kv_dtype=m.MLA_KV_FP8_E4M3_E8M0), seq, 152)
+    assert fp8.num_streams == 4 * q_len
+
+
 def test_plan_rejects_negative_seq_len_and_bad_sm_count(m):
     with pytest.raises(m.MlaError) as e:
         m.mla_decode_plan(_problem(m), np.array([1, -2, 3, 4], dtype=np.int32), 152)
