@@ -421,7 +421,8 @@ def run_gpu(args, world, rank, local):
                      "frac": achieved / hbm, "traffic": traffic,
                      "kernel": "mla_decode_kernel<%s>" % (
                          "dense " + w.kv_dtype if quant else
-                         ("sparse bf16" if w.topk else "dense bf16")),
+                         ("sparse bf16" if w.topk else
+                          ("dense bf16 multi-token" if w.q_len > 1 else "dense bf16"))),
                      "peak_source": peak_src,
                      "algorithmic_bytes_per_launch": int(byts)},
         "e2e": e2e,
@@ -447,7 +448,7 @@ def main():
     ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="dense",
-                    choices=["tiny", "dense", "long", "fp8", "sparse", "fp4"])
+                    choices=["tiny", "dense", "long", "fp8", "sparse", "fp4", "mtp"])
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-budget", type=float, default=10.0)

@@ -271,6 +271,7 @@ def test_multi_token_causal_dense():
     ("dense", [0, 37, 63], [0, 7, 19]),
     ("long", [3], [0, 19]),
     ("sparse", [0, 31], [0, 11, 19]),
+    ("mtp", [0, 40, 63], [0, 13, 19]),
 ])
 def test_full_size_sampled(name, requests, heads):
     batch = W.generate(W.WORKLOADS[name])

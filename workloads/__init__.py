@@ -122,6 +122,9 @@ WORKLOADS = {
     # sparse top-2048, q_len 4 causal drafts, context 65536, page 64
     "sparse": Workload("sparse", batch=32, heads=20, q_len=4, seq_lo=65536, seq_hi=65536,
                        page_size=64, topk=2048),
+    # speculative verify: the dense workload with 2 causal draft tokens per
+    # request (one MTP draft pair); both drafts share each staged page
+    "mtp": Workload("mtp", batch=64, heads=20, q_len=2, seq_lo=1024, seq_hi=8192, page_size=64),
     # FP4 latent (e2m1 + e8m0 per 16), on the FP8 workload's shape
     "fp4": Workload("fp4", batch=128, heads=20, seq_lo=2048, seq_hi=16384, page_size=64,
                     kv_dtype="fp4"),
