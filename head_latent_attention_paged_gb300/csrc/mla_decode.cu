@@ -93,6 +93,7 @@ struct ModeTraits {
   static constexpr int kQBatch = kThreads > 192 ? 3 : (kMulti ? 4 : 5);   // q_hat chunks per load batch
   static constexpr int kRawSlots = kRawRing ? kFp8RawSlots : kStages;
   static constexpr int kRawOffset = kTileBytes - kRawTileBytes;
+  static_assert(kRawSlots >= 1 && kRawOffset % 16 == 0, "raw tiles need 16-byte aligned slots");
 };
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s per wait
 constexpr float kRescaleThreshold = 8.0f;           // log2 units: rescale if max grows > 2^8
