@@ -143,3 +143,12 @@ def test_fp4_full_size_sampled():
     step = _run_and_compare(batch, requests=[0, 64, 127], heads=[0, 9, 19], label="fp4-full")
     o, _, lse = gpu_outputs(step)
     assert np.isfinite(o).all() and np.isfinite(lse).all()
+
+
+@pytest.mark.parametrize("name", ["fp8_small", "fp4_small"])
+def test_quantised_caches_with_draft_tokens(name):
+    """q_len 2 causal drafts over FP8 and FP4 caches: one row set per draft
+    (the quantised modes do not group drafts), each with its own window."""
+    w = W.with_overrides(W.SMALL_WORKLOADS[name], q_len=2, batch=3, seq_lo=60, seq_hi=700)
+    step = _run_and_compare(W.generate(w), sm_count=11, label=f"{name}/q2")
+    assert step.plan.num_streams == 6

@@ -33,7 +33,7 @@ def _run_and_compare(batch, sm_count=None, absorb=True, requests=None, heads=Non
     return step, worst
 
 
-@pytest.mark.parametrize("name", ["tiny", "dense_small", "long_small", "sparse_small"])
+@pytest.mark.parametrize("name", ["tiny", "dense_small", "long_small", "sparse_small", "mtp_small"])
 @pytest.mark.parametrize("garbage", ["finite", "nan"])
 def test_small_workloads_match_oracle(name, garbage):
     batch = with_fp8(W.generate(W.SMALL_WORKLOADS[name], garbage=garbage), garbage)
@@ -59,12 +59,13 @@ def test_split_invariance(sm_count):
 
 
 @pytest.mark.parametrize("sm_count", [7, 40])
-def test_merge_is_repeatable_and_matches_separate_combine(sm_count):
+@pytest.mark.parametrize("q_len", [1, 3])
+def test_merge_is_repeatable_and_matches_separate_combine(sm_count, q_len):
     """The merge launched by mla_decode_run and a separate combine pass over
     the same partials give the same o_lat and lse; the reserved workspace
     words stay zero and a second run on the same workspace gives identical
-    results."""
-    batch = W.generate(W.SMALL_WORKLOADS["long_small"])
+    results.  q_len 3: multi-token row sets (two drafts, then one)."""
+    batch = W.generate(W.with_overrides(W.SMALL_WORKLOADS["long_small"], q_len=q_len))
     step = make_step(batch, sm_count=sm_count)
     step.run()
     _, lat1, lse1 = gpu_outputs(step)
@@ -81,7 +82,7 @@ def test_merge_is_repeatable_and_matches_separate_combine(sm_count):
     assert np.allclose(lat3, lat1, rtol=1e-5, atol=1e-6) and np.allclose(lse3, lse1, atol=1e-5)
 
 
-@pytest.mark.parametrize("name", ["dense_small", "fp8_small"])
+@pytest.mark.parametrize("name", ["dense_small", "fp8_small", "mtp_small"])
 def test_chained_launches_see_their_inputs(name):
     """The decode, merge and W_UV kernels run as programmatic dependents of
     one another: each must read what the one before wrote.  Outputs are

@@ -37,7 +37,7 @@ def _close(a_lat, a_lse, b_lat, b_lse):
 
 
 @pytest.mark.parametrize("name,sm_count", [("dense_small", None), ("long_small", 40),
-                                           ("sparse_small", 7)])
+                                           ("sparse_small", 7), ("mtp_small", 11)])
 def test_static_scratch_matches_workspace_entry_point(name, sm_count):
     from head_latent_attention_paged_gb300 import mla_decode_run_static
     batch = W.generate(W.SMALL_WORKLOADS[name])

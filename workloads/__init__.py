@@ -140,6 +140,8 @@ SMALL_WORKLOADS = {
                            page_size=128, seed=2),
     "fp8_small": Workload("fp8_small", batch=4, heads=20, seq_lo=100, seq_hi=900,
                           page_size=64, kv_dtype="fp8", seed=3),
+    "mtp_small": Workload("mtp_small", batch=4, heads=20, q_len=3, seq_lo=70, seq_hi=900,
+                          page_size=64, seed=6),
     "fp4_small": Workload("fp4_small", batch=4, heads=20, seq_lo=100, seq_hi=900,
                           page_size=64, kv_dtype="fp4", seed=5),
     "sparse_small": Workload("sparse_small", batch=2, heads=20, q_len=4, seq_lo=1500,
