@@ -99,3 +99,131 @@ class DecodeStep:
         mla_clear_status(self.plan, self.workspace, self.stream)
 
     KERNELS_PER_STEP = 3
+
+
+class HostPipeline:
+    """Host <-> device pipeline for a sequence of decode steps.
+
+    Every step's inputs (the absorbed queries, the block table, the context
+    lengths, the top-k lists, each request's newest token row and its
+    position) live in one pinned host arena and go to the device in one copy;
+    the step's outputs (o and lse) come back in one copy.  `depth` sets of
+    arenas rotate, and the copies run on their own streams: the inputs of
+    step k + 1 and the outputs of step k - 1 move while step k computes.
+    Each step appends its newest token rows to the cache (mla_cache_append)
+    and runs the decode, the merge and the W_UV projection on the compute
+    stream.
+
+    The caller refills host arena `k % depth` for step k only after
+    `input_copied(k - depth)` has been synchronised (the static inputs of a
+    benchmark need no refill).
+    """
+
+    ALIGN = 256
+
+    def __init__(self, step: DecodeStep, *, q_hat_bits, block_table, seq_lens, new_rows,
+                 positions, topk_idx=None, depth: int = 2):
+        self.step = step
+        self.depth = depth
+        dev = step.device
+        parts = [("q_hat", np.ascontiguousarray(q_hat_bits).view(np.int16)),
+                 ("block_table", np.ascontiguousarray(block_table, dtype=np.int32)),
+                 ("seq_lens", np.ascontiguousarray(seq_lens, dtype=np.int32)),
+                 ("new_rows", np.ascontiguousarray(new_rows).view(np.int16)),
+                 ("positions", np.ascontiguousarray(positions, dtype=np.int32))]
+        if topk_idx is not None:
+            parts.append(("topk_idx", np.ascontiguousarray(topk_idx, dtype=np.int32)))
+        self.layout, off = {}, 0
+        for name, arr in parts:
+            self.layout[name] = (off, arr.dtype, arr.shape)
+            off += (arr.nbytes + self.ALIGN - 1) // self.ALIGN * self.ALIGN
+        self.in_bytes = off
+        self.h2d_bytes = sum(arr.nbytes for _, arr in parts)
+        out_shape, lse_shape = tuple(step.out.shape), tuple(step.lse.shape)
+        out_nb = int(np.prod(out_shape)) * 2
+        self.out_off = (0, (out_nb + self.ALIGN - 1) // self.ALIGN * self.ALIGN)
+        self.out_bytes = self.out_off[1] + int(np.prod(lse_shape)) * 4
+        self.d2h_bytes = out_nb + int(np.prod(lse_shape)) * 4
+        self.host_in, self.dev_in, self.host_out, self.dev_out, self.views = [], [], [], [], []
+        for _ in range(depth):
+            h = torch.empty(self.in_bytes, dtype=torch.uint8).pin_memory()
+            hn = h.numpy()
+            for name, arr in parts:
+                o, _, _ = self.layout[name]
+                hn[o:o + arr.nbytes] = arr.reshape(-1).view(np.uint8)
+            d = torch.empty(self.in_bytes, dtype=torch.uint8, device=dev)
+            ho = torch.empty(self.out_bytes, dtype=torch.uint8).pin_memory()
+            do = torch.empty(self.out_bytes, dtype=torch.uint8, device=dev)
+            v = {name: self._view(d, name) for name, _ in parts}
+            v["out"] = do[:out_nb].view(torch.bfloat16).view(out_shape)
+            v["lse"] = do[self.out_off[1]:].view(torch.float32).view(lse_shape)
+            self.host_in.append(h)
+            self.dev_in.append(d)
+            self.host_out.append(ho)
+            self.dev_out.append(do)
+            self.views.append(v)
+        self.h2d_stream = torch.cuda.Stream(dev)
+        self.d2h_stream = torch.cuda.Stream(dev)
+        self.h2d_done = [torch.cuda.Event() for _ in range(depth)]
+        self.computed = [torch.cuda.Event() for _ in range(depth)]
+        self.d2h_done = [torch.cuda.Event() for _ in range(depth)]
+        self.used = [False] * depth
+
+    def _view(self, dev_arena, name):
+        off, dtype, shape = self.layout[name]
+        nb = int(np.prod(shape)) * np.dtype(dtype).itemsize
+        t = dev_arena[off:off + nb]
+        tdt = {np.dtype(np.int16): torch.int16, np.dtype(np.int32): torch.int32}[np.dtype(dtype)]
+        return t.view(tdt).view(shape)
+
+    def input_copied(self, k: int) -> torch.cuda.Event:
+        return self.h2d_done[k % self.depth]
+
+    def output_ready(self, k: int) -> torch.cuda.Event:
+        """Recorded once step k's outputs are in host arena k % depth."""
+        return self.d2h_done[k % self.depth]
+
+    def host_outputs(self, k: int):
+        """(o bf16 bits [rows][H][256], lse f32 [rows][H]) of step k (valid
+        after output_ready(k))."""
+        i = k % self.depth
+        hn = self.host_out[i].numpy()
+        nb = self.out_off[1]
+        o = hn[:int(np.prod(self.step.out.shape)) * 2].view(np.uint16).reshape(tuple(self.step.out.shape))
+        lse = hn[nb:].view(np.float32).reshape(tuple(self.step.lse.shape))
+        return o, lse
+
+    def submit(self, k: int, compute_stream=None):
+        """Enqueue step k: input copy, append + decode + merge + W_UV, output copy."""
+        from . import mla_cache_append
+        i = k % self.depth
+        st = self.step
+        cs = compute_stream if compute_stream is not None else torch.cuda.current_stream(st.device)
+        if self.used[i]:
+            self.h2d_stream.wait_event(self.computed[i])   # the compute of step k - depth read set i
+        with torch.cuda.stream(self.h2d_stream):
+            self.dev_in[i].copy_(self.host_in[i], non_blocking=True)
+            self.h2d_done[i].record(self.h2d_stream)
+        cs.wait_event(self.h2d_done[i])
+        if self.used[i]:
+            cs.wait_event(self.d2h_done[i])                 # outputs of step k - depth copied out
+        v = self.views[i]
+        st.q_hat = v["q_hat"].view(torch.bfloat16)
+        st.block_table, st.seq_lens = v["block_table"], v["seq_lens"]
+        st.topk_idx = v.get("topk_idx")
+        st.out, st.lse = v["out"], v["lse"]
+        with torch.cuda.stream(cs):
+            mla_cache_append(st.problem, v["new_rows"], v["positions"], st.block_table, st.cache,
+                             stream=cs)
+            st.step()
+            self.computed[i].record(cs)
+        self.d2h_stream.wait_event(self.computed[i])
+        with torch.cuda.stream(self.d2h_stream):
+            self.host_out[i].copy_(self.dev_out[i], non_blocking=True)
+            self.d2h_done[i].record(self.d2h_stream)
+        self.used[i] = True
+
+    def drain(self, k_last: int, compute_stream=None):
+        """Make the compute stream wait for step k_last's outputs on the host."""
+        cs = compute_stream if compute_stream is not None else torch.cuda.current_stream(self.step.device)
+        cs.wait_event(self.d2h_done[k_last % self.depth])
