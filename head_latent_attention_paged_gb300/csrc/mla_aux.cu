@@ -1,5 +1,6 @@
 // The smaller kernels of the decode step:
-//   * mla_combine_kernel : LSE merge of the split-KV partials of each row set;
+//   * mla_combine_kernel : LSE merge of the split-KV partials of each row set
+//                          (one block per row: a head, or a draft token x head);
 //   * mla_uv_kernel      : o = W_UV[h]^T o_lat (tcgen05, per head);
 //   * mla_absorb_kernel  : q_hat = [W_UK[h] q_nope || q_rope] (query absorption).
 #include <cuda_bf16.h>

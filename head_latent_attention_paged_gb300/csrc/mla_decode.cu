@@ -1,7 +1,10 @@
 // Paged MLA latent-cache decode kernel for sm_103a.
 //
 // One CTA per SM walks a contiguous range of 64-token tiles of the
-// concatenated (request, query token) row sets ("streams").  Per tile:
+// concatenated row sets ("streams"): one per (request, query token), or, in
+// the multi-token mode (dense bf16 cache, several draft tokens), one per
+// group of G draft tokens of a request whose G * H rows share every staged
+// tile.  Per tile:
 //
 //   producer warp : stages the 64 cached rows (576 bf16 each) in shared
 //                   memory once -- TMA tiles for dense pages (for sparse
@@ -9,22 +12,25 @@
 //                   copies, 16 rows each) -- as nine
 //                   [64 rows x 128 B] chunks in the 128-byte swizzle layout,
 //                   three tiles in flight.  FP8 / FP4 caches: one bulk copy
-//                   of the tile's quantised rows (594 or 324 bytes) into the
-//                   tail of the stage it will be dequantised into, and
+//                   of the tile's quantised rows (594 or 324 bytes), FP8
+//                   into a ring of two raw slots beside two bf16 stages, FP4
+//                   into the tail of the bf16 stage it becomes, and
 //   dequant warps : (FP8 / FP4) turn each row's codes and e8m0 scales into
-//                   bf16 values code * 2^(scale - 127), exactly, written in
-//                   place as the swizzled bf16 tile: first the chunks below
-//                   the raw bytes, then, once every dequant warp holds the
-//                   rest of its groups in registers, the chunks over them;
-//                   rows with no live token become zeros.
+//                   bf16 values code * 2^(scale - 127), exactly, written as
+//                   the swizzled bf16 tile (FP4 in place: first the chunks
+//                   below the raw bytes, then, once every dequant warp holds
+//                   the rest of its groups in registers, the chunks over
+//                   them); rows with no live token become zeros.
 //   MMA warp      : S[h, t]   = q_hat[h, :576] . row[t, :576]      (tcgen05,
-//                   M = 64 head rows with q_hat read from TMEM, N = 64
+//                   M = 64 rows with q_hat read from TMEM -- its RoPE part
+//                   from shared memory in the multi-token mode -- N = 64
 //                   tokens from shared memory, K = 576, f32 in TMEM);
 //                   O^T[d, h] += sum_t row[t, d] P[h, t]            (tcgen05,
-//                   M = 128 latent dims x 4, N = padded heads, K = 64 tokens,
+//                   M = 128 latent dims x 4, N = padded rows, K = 64 tokens,
 //                   A = the same staged tile read MN-major).
 //   softmax warps : online softmax in the exp2 domain on S read from TMEM
-//                   (two lanes per head row), P written to shared memory as
+//                   (two lanes per row; in the multi-token mode each row
+//                   masked past its own draft's causal window), P written to shared memory as
 //                   bf16, lazy rescale of O^T in TMEM when the running max
 //                   grows by more than 2^8; at a stream change they write the
 //                   next stream's q_hat into TMEM, and at the end of each
@@ -32,8 +38,8 @@
 //                   over several CTAs, a partial plus its lse, merged by the
 //                   combine kernel that follows this one).
 //
-// All heads of a request reuse each staged tile, so every cached byte is read
-// from HBM once per stream.  Waits are bounded (sm103_ptx.cuh); a timeout
+// All heads of a row set reuse each staged tile, so every cached byte is read
+// from HBM once per row set.  Waits are bounded (sm103_ptx.cuh); a timeout
 // sets MLA_STATUS_TIMEOUT and the CTA unwinds after draining its own copies
 // and MMAs, then releases its tensor memory.
 #include <cuda_bf16.h>
@@ -51,7 +57,7 @@ namespace {
 constexpr int kSoftmaxWarps = 4;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
-constexpr int kDequantWarp0 = 6;    // FP8 mode: warps 6..11 dequantise
+constexpr int kDequantWarp0 = 6;    // FP8 / FP4 modes: warps 6..11 dequantise
 constexpr int kDequantWarps = 6;
 // P (bf16 [padded heads][64 tokens], the B operand of PV) lives in the RoPE
 // chunk of its own tile's stage: QK(i) is the only reader of that chunk and
