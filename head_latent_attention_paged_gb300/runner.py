@@ -116,15 +116,18 @@ class HostPipeline:
 
     The caller refills host arena `k % depth` for step k only after
     `input_copied(k - depth)` has been synchronised (the static inputs of a
-    benchmark need no refill).
+    benchmark need no refill).  `caches` optionally lists identical copies of
+    the latent cache that consecutive steps take in turn (a benchmark uses
+    two so that no step finds the previous one's cache lines in L2).
     """
 
     ALIGN = 256
 
     def __init__(self, step: DecodeStep, *, q_hat_bits, block_table, seq_lens, new_rows,
-                 positions, topk_idx=None, depth: int = 2):
+                 positions, topk_idx=None, depth: int = 2, caches=None):
         self.step = step
         self.depth = depth
+        self.caches = list(caches) if caches else [step.cache]
         dev = step.device
         parts = [("q_hat", np.ascontiguousarray(q_hat_bits).view(np.int16)),
                  ("block_table", np.ascontiguousarray(block_table, dtype=np.int32)),
@@ -212,6 +215,7 @@ class HostPipeline:
         st.block_table, st.seq_lens = v["block_table"], v["seq_lens"]
         st.topk_idx = v.get("topk_idx")
         st.out, st.lse = v["out"], v["lse"]
+        st.cache = self.caches[k % len(self.caches)]
         with torch.cuda.stream(cs):
             mla_cache_append(st.problem, v["new_rows"], v["positions"], st.block_table, st.cache,
                              stream=cs)
@@ -222,6 +226,28 @@ class HostPipeline:
             self.host_out[i].copy_(self.dev_out[i], non_blocking=True)
             self.d2h_done[i].record(self.d2h_stream)
         self.used[i] = True
+
+    def capture(self, k0: int, n: int):
+        """Capture steps k0 .. k0 + n - 1 (copies, append, decode, merge,
+        W_UV and their cross-stream dependencies) in one CUDA graph, so a
+        replay issues the whole pipelined sequence with one launch (on any
+        stream).  The caller synchronises before capturing."""
+        g = torch.cuda.CUDAGraph()
+        compute_stream = torch.cuda.Stream(self.step.device)   # capture needs a side stream
+        self.used = [False] * self.depth     # work recorded before the capture is complete
+        with torch.cuda.graph(g, stream=compute_stream, capture_error_mode="relaxed"):
+            fork = torch.cuda.Event()
+            fork.record(compute_stream)
+            self.h2d_stream.wait_event(fork)
+            self.d2h_stream.wait_event(fork)
+            for k in range(k0, k0 + n):
+                self.submit(k, compute_stream)
+            for i in range(self.depth):      # join every copy back into the capture stream
+                if self.used[i]:
+                    compute_stream.wait_event(self.h2d_done[i])
+                    compute_stream.wait_event(self.d2h_done[i])
+        self.used = [False] * self.depth
+        return g
 
     def drain(self, k_last: int, compute_stream=None):
         """Make the compute stream wait for step k_last's outputs on the host."""
