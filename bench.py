@@ -35,10 +35,11 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MLA decode latent-cache GB/s (% of HBM peak) and decode tokens/s per layer"
 L2_FLUSH_BYTES = 512 * 1024 * 1024
+L2_BYTES = 129 * 1000 * 1000     # GB300 L2
 DECODE_SOURCES = ["csrc/mla_decode.cu", "csrc/sm103_ptx.cuh", "csrc/mla_internal.h"]
 
 
-def workload_description(w, batch) -> dict:
+def workload_description(w, batch, rotate: bool = False) -> dict:
     seq = batch.seq_lens
     d = {
         "workload": f"{w.name}: MLA decode, 1 layer, B={w.batch}, H={w.heads}, q_len={w.q_len}, "
@@ -51,8 +52,10 @@ def workload_description(w, batch) -> dict:
         "total_context_tokens": int(seq.sum()),
         "latent_bytes_per_step": int(batch.latent_bytes_read),
         "bytes_per_token_row": w.cache_row_bytes,
-        "l2": f"flushed before every timed step by writing {L2_FLUSH_BYTES >> 20} MiB "
-              "(step time from CUDA events excludes the flush)",
+        "l2": ("no flush: consecutive timed steps read two copies of the cache in turn "
+               "(each larger than the 129 MB L2)") if rotate else
+              (f"flushed before every timed step by writing {L2_FLUSH_BYTES >> 20} MiB "
+               "(step time from CUDA events excludes the flush)"),
     }
     return d
 
@@ -219,6 +222,14 @@ def _prefix_batch(batch, tokens):
     return sub
 
 
+def cache_bytes(batch) -> int:
+    """Bytes of one copy of the workload's latent cache."""
+    for c in (batch.cache_bf16, batch.cache_quant):
+        if c is not None:
+            return int(c.nbytes)
+    return 0
+
+
 def run_reference(args, world, rank):
     import numpy as np
     import workloads as W
@@ -246,7 +257,8 @@ def run_reference(args, world, rank):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": workload_description(w, batch),
+        "data": "synthetic",
+        "config": workload_description(w, batch, cache_bytes(batch) > L2_BYTES),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": f"each step: {what} (non-absorbed float64 numpy oracle)"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -285,11 +297,23 @@ def run_gpu(args, world, rank, local):
                       topk_idx=batch.topk_idx, causal=w.causal, sm_scale=w.sm_scale,
                       device=device)
     stream = torch.cuda.current_stream(device)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     byts = batch.latent_bytes_read
+    # Between timed steps: when the cache is larger than the L2, consecutive
+    # steps read two copies of it in turn (no step finds the previous one's
+    # lines in L2, and no flush leaves dirty lines for the step to write
+    # back); a smaller cache is flushed out of L2 before every step instead.
+    rotate = cache_bytes(batch) > L2_BYTES
+    caches = [step.cache, step.cache.clone()] if rotate else [step.cache]
+    flush = None if rotate else torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
 
-    for _ in range(args.warmup):
-        flush.zero_()
+    def between_steps(k):
+        if rotate:
+            step.cache = caches[k % 2]
+        else:
+            flush.zero_()
+
+    for k in range(args.warmup):
+        between_steps(k)
         step.step()
     torch.cuda.synchronize(device)
     if step.status() != 0:
@@ -308,7 +332,7 @@ def run_gpu(args, world, rank, local):
     with ClockSampler(local) as clocks:
         t_wall = time.perf_counter()
         for k in range(args.steps):
-            flush.zero_()
+            between_steps(k)
             ev[k][0].record(stream)
             step.run()
             if k % RUN_EVERY == RUN_EVERY - 1:
@@ -323,7 +347,7 @@ def run_gpu(args, world, rank, local):
     run_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(args.steps)
               if k % RUN_EVERY == RUN_EVERY - 1]
     if not run_ms:   # fewer steps than RUN_EVERY: time the last one's decode alone
-        flush.zero_()
+        between_steps(args.steps)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         step.run()
@@ -346,8 +370,8 @@ def run_gpu(args, world, rank, local):
     # arena), appends, runs the step and copies o and lse back (one copy);
     # HostPipeline overlaps step k's copies with the neighbouring steps'
     # kernels on two copy streams.  No L2 flush here (it would sit inside the
-    # pipelined region): every workload's cache is larger than the 129 MB L2,
-    # and consecutive steps read two different copies of it.
+    # pipelined region): the benchmark workloads' caches are larger than the
+    # 129 MB L2, and consecutive steps read two different copies of them.
     e2e = None
     if args.e2e_steps > 0:
         from head_latent_attention_paged_gb300.runner import HostPipeline
@@ -357,12 +381,11 @@ def run_gpu(args, world, rank, local):
         last_pos = (batch.seq_lens.astype(np.int64) - 1).astype(np.int32)
         rng = np.random.default_rng(w.seed + 1)
         rows_np = W.f32_to_bf16_bits(rng.standard_normal((w.batch, 576)).astype(np.float32))
-        # two copies of the cache, taken in turn: consecutive steps stream
-        # different memory (2 x the cache between reuses, far above the L2)
+        # the two copies of the cache, taken in turn as in the timed loop
         pipe = HostPipeline(step, q_hat_bits=step.q_hat.view(torch.int16).cpu().numpy(),
                             block_table=batch.block_table, seq_lens=batch.seq_lens,
                             new_rows=rows_np, positions=last_pos, topk_idx=batch.topk_idx,
-                            caches=[step.cache, step.cache.clone()])
+                            caches=caches if rotate else None)
         WARM = 3
         for k in range(WARM):
             pipe.submit(k, stream)
@@ -420,7 +443,7 @@ def run_gpu(args, world, rank, local):
         "dtype": {"bf16": "bf16", "fp8": "fp8-e4m3+e8m0 cache, bf16 tensor-core math",
                   "fp4": "fp4-e2m1+e8m0 cache, bf16 tensor-core math"}[w.kv_dtype],
         "data": "synthetic",
-        "config": workload_description(w, batch),
+        "config": workload_description(w, batch, rotate),
         "tokens_per_s_per_layer": w.batch * w.q_len * world / (max_s / args.steps),
         "hbm_fraction_of_measured": value / hbm,
         "kernel_ms": {"decode_with_merge": decode_ms, "step": statistics.mean(step_ms),
