@@ -38,7 +38,7 @@ MLA_TILE_TOKENS = 64
 EXPORTED = (
     "mla_decode_plan", "mla_q_absorb", "mla_decode_run", "mla_combine", "mla_uv_proj",
     "mla_get_status", "mla_clear_status", "mla_strerror", "mla_version",
-    "mla_decode_run_static", "mla_cache_append",
+    "mla_decode_run_static", "mla_cache_append", "mla_selftest_bounded_wait",
 )
 
 
@@ -91,6 +91,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.mla_decode_run_static.argtypes = [P(MlaPlan), vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.mla_uv_proj.argtypes = [vp, vp, vp, i32, i32, vp]
     lib.mla_cache_append.argtypes = [P(MlaProblem), vp, vp, vp, vp, vp, vp]
+    lib.mla_selftest_bounded_wait.argtypes = [vp, i64, vp, vp]
     lib.mla_get_status.argtypes = [P(MlaPlan), vp, P(ctypes.c_uint32), vp]
     lib.mla_clear_status.argtypes = [P(MlaPlan), vp, vp]
     lib.mla_strerror.argtypes = [ctypes.c_int]
@@ -187,6 +188,13 @@ def mla_cache_append(problem: MlaProblem, new_rows, positions, block_table, kv_c
     _check("mla_cache_append", load().mla_cache_append(
         ctypes.byref(problem), _ptr(new_rows), _ptr(positions), _ptr(block_table),
         _ptr(kv_cache), _ptr(status), _stream(stream)))
+
+
+def mla_selftest_bounded_wait(status, limit_ns: int, waited_ns=None, stream=None) -> None:
+    """Launch the bounded-wait self-test: a wait that nothing completes gives
+    up after limit_ns and ORs MLA_STATUS_TIMEOUT into the device word status."""
+    _check("mla_selftest_bounded_wait", load().mla_selftest_bounded_wait(
+        _ptr(status), int(limit_ns), _ptr(waited_ns), _stream(stream)))
 
 
 def mla_uv_proj(o_lat, w_uv, out, rows: int, num_heads: int, stream=None) -> None:

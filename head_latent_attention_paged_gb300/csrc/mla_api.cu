@@ -147,6 +147,11 @@ int plan_check(const mla_plan* plan) {
 
 }  // namespace
 
+namespace mla {
+cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, uint64_t* waited_ns,
+                                 cudaStream_t stream);
+}  // namespace mla
+
 extern "C" {
 
 int mla_version(void) { return kAbiVersion; }
@@ -326,6 +331,17 @@ int mla_cache_append(const mla_problem* problem, const void* new_rows, const int
   p.max_pages = problem->max_pages_per_seq;
   p.kv_dtype = problem->kv_dtype;
   const cudaError_t err = launch_append(p, reinterpret_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int mla_selftest_bounded_wait(uint32_t* status, int64_t limit_ns, uint64_t* waited_ns,
+                              mla_stream_t stream) {
+  if (status == nullptr || limit_ns < 1 || limit_ns > 1000000000) return MLA_ERR_INVALID_ARGUMENT;
+  if ((reinterpret_cast<uintptr_t>(status) & 3u) ||
+      (waited_ns && (reinterpret_cast<uintptr_t>(waited_ns) & 7u)))
+    return MLA_ERR_MISALIGNED;
+  const cudaError_t err = launch_wait_selftest(status, static_cast<uint64_t>(limit_ns), waited_ns,
+                                               reinterpret_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 

@@ -292,6 +292,35 @@ cudaError_t launch_uv_proj_tma(const CUtensorMap* w_map, const float* o_lat, uin
 }
 
 // ----------------------------------------------------------------------------
+// bounded-wait self-test: every thread waits for a phase of an mbarrier that
+// nothing arrives on; mbar_wait gives up after limit_ns, and the block
+// reports MLA_STATUS_TIMEOUT like a kernel whose pipeline stalled.
+// ----------------------------------------------------------------------------
+__global__ void __launch_bounds__(64) mla_wait_selftest_kernel(uint32_t* status, uint64_t limit_ns,
+                                                               uint64_t* waited_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const uint64_t t0 = globaltimer_ns();
+  const bool ok = mbar_wait(&bar, 0, nullptr, limit_ns);
+  const uint64_t dt = globaltimer_ns() - t0;
+  const bool any_gave_up = __syncthreads_or(!ok);
+  if (threadIdx.x == 0) {
+    if (any_gave_up) atomicOr(status, MLA_STATUS_TIMEOUT);
+    if (waited_ns != nullptr) *waited_ns = dt;
+  }
+}
+
+cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, uint64_t* waited_ns,
+                                 cudaStream_t stream) {
+  mla_wait_selftest_kernel<<<1, 64, 0, stream>>>(status, limit_ns, waited_ns);
+  return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------------------
 // query absorption: q_hat[r][h] = [bf16(W_UK[h] q_nope[r][h]) || q_rope[r][h]]
 // one block per (head, 8 rows); thread c computes latent dim c for the 8 rows
 // ----------------------------------------------------------------------------

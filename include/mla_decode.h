@@ -281,6 +281,23 @@ MLA_API int mla_get_status(const mla_plan* plan, const void* workspace, uint32_t
 /* Zero the status word (asynchronous). */
 MLA_API int mla_clear_status(const mla_plan* plan, void* workspace, mla_stream_t stream);
 
+/*
+ * mla_selftest_bounded_wait -- exercise, without any fault, the bounded
+ * waits every kernel of this library uses on its mbarriers.  One block of 64
+ * threads waits for an mbarrier phase that nothing completes; every wait gives
+ * up after limit_ns nanoseconds, after which MLA_STATUS_TIMEOUT is OR-ed into
+ * *status and the time thread 0 waited is written to *waited_ns.
+ *   status     : device uint32, 4-byte aligned (e.g. a plan's status word or any
+ *                caller word); never read, only OR-ed.
+ *   limit_ns   : 1 .. 1e9.
+ *   waited_ns  : device uint64, 8-byte aligned, or NULL.
+ * Returns MLA_OK once launched (asynchronous on `stream`); a null status or a
+ * limit out of range gives MLA_ERR_INVALID_ARGUMENT, a misaligned pointer
+ * MLA_ERR_MISALIGNED.
+ */
+MLA_API int mla_selftest_bounded_wait(uint32_t* status, int64_t limit_ns, uint64_t* waited_ns,
+                                      mla_stream_t stream);
+
 /* Static description of an error code; never NULL. */
 MLA_API const char* mla_strerror(int code);
 

@@ -258,3 +258,13 @@ def test_stream_split_matches_kernel_rule():
                 slots.add((s, c))
         keys = [s + c for s, c in slots]
         assert len(keys) == len(set(keys)) and max(keys) < S + C - 1 + 1
+
+
+def test_bounded_wait_selftest_rejects_bad_arguments_before_cuda(m):
+    A = 1 << 20
+    for status, limit, waited, code in [(None, 1000, None, -1), (A, 0, None, -1),
+                                        (A, 2_000_000_000, None, -1), (A + 2, 1000, None, -3),
+                                        (A, 1000, A + 4, -3)]:
+        with pytest.raises(m.MlaError) as e:
+            m.mla_selftest_bounded_wait(status, limit, waited)
+        assert e.value.code == code
