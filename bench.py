@@ -39,6 +39,30 @@ L2_BYTES = 129 * 1000 * 1000     # GB300 L2
 DECODE_SOURCES = ["csrc/mla_decode.cu", "csrc/sm103_ptx.cuh", "csrc/mla_internal.h"]
 
 
+def overhead_bytes(w, batch) -> dict:
+    """Bytes a step moves besides the cached rows: the absorbed queries, the
+    page tables, the top-k lists, W_UV, and the split partials (an upper
+    bound: every slot of the plan written once and read once)."""
+    import numpy as np
+    rows = w.batch * w.q_len
+    g = min(w.q_len, 48 // w.heads) if (w.kv_dtype == "bf16" and not w.topk and w.q_len >= 2) else 1
+    g = g if g >= 2 else 1
+    row_sets = w.batch * -(-w.q_len // g)
+    slots = row_sets + 152 - 1
+    d = {"q_hat": rows * w.heads * 576 * 2, "block_table": int(batch.block_table.nbytes),
+         "seq_lens": int(batch.seq_lens.nbytes), "w_uv": w.heads * 512 * 256 * 2,
+         "partials_max": slots * g * w.heads * (512 + 1) * 4 * 2}
+    if w.topk:
+        d["topk_idx"] = int(batch.topk_idx.nbytes)
+        # rows the drafts of a request share: each read once per request
+        uniq = 0
+        for b in range(w.batch):
+            idx = batch.topk_idx[b * w.q_len:(b + 1) * w.q_len]
+            uniq += int(np.unique(idx[idx >= 0]).size)
+        d["latent_bytes_union_of_drafts"] = uniq * w.cache_row_bytes
+    return d
+
+
 def workload_description(w, batch, rotate: bool = False) -> dict:
     seq = batch.seq_lens
     d = {
@@ -51,6 +75,7 @@ def workload_description(w, batch, rotate: bool = False) -> dict:
         "kv_dtype": w.kv_dtype, "topk": w.topk, "seed": w.seed,
         "total_context_tokens": int(seq.sum()),
         "latent_bytes_per_step": int(batch.latent_bytes_read),
+        "overhead_bytes_per_step": overhead_bytes(w, batch),
         "bytes_per_token_row": w.cache_row_bytes,
         "l2": ("no flush: consecutive timed steps read two copies of the cache in turn "
                "(each larger than the 129 MB L2)") if rotate else
@@ -181,27 +206,49 @@ def blas_threads() -> int:
     return os.cpu_count() or 1
 
 
-def oracle_sample(batch, budget_s: float, max_tokens: int = None):
-    """Time the (non-absorbed, float64) oracle on a bounded sample: whole
-    requests in order until `budget_s` is spent, or a prefix of the first
-    request of at most `max_tokens` tokens.  Returns (bytes, seconds, what)."""
+def oracle_sample(batch, budget_s: float, max_tokens: int = None, form: str = "non_absorbed",
+                  max_requests: int = None):
+    """Time the float64 oracle (the non-absorbed definition, or its absorbed
+    form) on a bounded sample: whole requests in order until `budget_s` is
+    spent (or `max_requests` are done), or a prefix of the first request of at
+    most `max_tokens` tokens.  Returns (bytes, seconds, what)."""
     import numpy as np
     import oracle as O
     w = batch.workload
     if max_tokens is not None:
         sub = _prefix_batch(batch, max_tokens)
         t0 = time.perf_counter()
-        O.decode(sub, requests=[0])
+        O.decode(sub, requests=[0], form=form)
         dt = time.perf_counter() - t0
         return sub.latent_bytes_read_req(0), dt, f"first {int(sub.seq_lens[0])} tokens of request 0, all {w.heads} heads"
     done_bytes, t0, n = 0, time.perf_counter(), 0
-    for b in range(w.batch):
-        O.decode(batch, requests=[b])
+    for b in range(w.batch if max_requests is None else min(w.batch, max_requests)):
+        O.decode(batch, requests=[b], form=form)
         n += 1
         done_bytes += _request_bytes(batch, b)
         if time.perf_counter() - t0 >= budget_s:
             break
     return done_bytes, time.perf_counter() - t0, f"{n} whole request(s) of {w.batch}, all {w.heads} heads"
+
+
+def one_thread_sample(workload: str):
+    """The non-absorbed oracle on one BLAS thread (a child process started
+    with the thread-count variables at 1), on the first 1024 tokens of
+    request 0: GB/s, or None if the child fails."""
+    env = dict(os.environ)
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[var] = "1"
+    code = ("import sys, json; sys.path.insert(0, %r); import bench, workloads as W; "
+            "b = W.generate(W.WORKLOADS[%r]); by, dt, what = bench.oracle_sample(b, 0, max_tokens=1024); "
+            "print(json.dumps([by, dt, what]))") % (ROOT, workload)
+    try:
+        out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True,
+                             timeout=300)
+        by, dt, what = json.loads(out.stdout.strip().splitlines()[-1])
+        return {"value": by / dt / 1e9, "unit": "GB/s", "threads": 1,
+                "sample": f"{what}: non-absorbed float64 numpy oracle, {dt:.2f} s"}
+    except Exception:
+        return None
 
 
 def _request_bytes(batch, b):
@@ -446,7 +493,9 @@ def run_gpu(args, world, rank, local):
         "config": workload_description(w, batch, rotate),
         "tokens_per_s_per_layer": w.batch * w.q_len * world / (max_s / args.steps),
         "hbm_fraction_of_measured": value / hbm,
-        "kernel_ms": {"decode_with_merge": decode_ms, "step": statistics.mean(step_ms),
+        "kernel_ms": {"decode_with_merge": decode_ms,
+                      "decode_with_merge_median": statistics.median(run_ms),
+                      "step": statistics.mean(step_ms), "step_median": statistics.median(step_ms),
                       "decode_timed_steps": len(run_ms)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": traffic,
@@ -464,9 +513,15 @@ def run_gpu(args, world, rank, local):
     }
     if world == 1 and not args.no_cpu_baseline:
         cb, ct, what = oracle_sample(batch, args.cpu_budget)
+        n_req = int(what.split()[0]) if what.split()[0].isdigit() else 1
+        ab, at, _ = oracle_sample(batch, 1e9, form="absorbed", max_requests=n_req)
         line["cpu_baseline"] = {"value": cb / ct / 1e9, "unit": "GB/s", "cores": blas_threads(),
                                 "kind": "oracle",
-                                "sample": f"{what}: non-absorbed float64 numpy oracle, {ct:.1f} s"}
+                                "sample": f"{what}: non-absorbed float64 numpy oracle, {ct:.1f} s",
+                                "cpu_count": os.cpu_count(),
+                                "absorbed_value": ab / at / 1e9,
+                                "absorbed_sample": f"the same requests, absorbed float64 form, {at:.1f} s",
+                                "one_thread": one_thread_sample(args.workload)}
     print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()
