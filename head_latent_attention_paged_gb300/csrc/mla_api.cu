@@ -85,7 +85,11 @@ int validate_problem(const mla_problem* pr) {
       pr->kv_dtype != MLA_KV_FP4_E2M1_E8M0)
     return MLA_ERR_UNSUPPORTED;
   if (pr->kv_dtype != MLA_KV_BF16 && pr->topk_width > 0) return MLA_ERR_UNSUPPORTED;
-  if (static_cast<int64_t>(pr->batch) * pr->q_len > kMaxStreams) return MLA_ERR_UNSUPPORTED;
+  {  // row sets (draft tokens grouped where the multi-token mode applies)
+    const int64_t g = group_of(*pr);
+    if (static_cast<int64_t>(pr->batch) * ((pr->q_len + g - 1) / g) > kMaxStreams)
+      return MLA_ERR_UNSUPPORTED;
+  }
   if (static_cast<int64_t>(pr->num_pages) * pr->page_size > INT32_MAX) return MLA_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(pr->max_pages_per_seq) * pr->page_size > INT32_MAX) return MLA_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(pr->batch) * pr->q_len * pr->num_heads > INT32_MAX) return MLA_ERR_UNSUPPORTED;

@@ -118,7 +118,9 @@ class HostPipeline:
     `input_copied(k - depth)` has been synchronised (the static inputs of a
     benchmark need no refill).  `caches` optionally lists identical copies of
     the latent cache that consecutive steps take in turn (a benchmark uses
-    two so that no step finds the previous one's cache lines in L2).
+    two so that no step finds the previous one's cache lines in L2).  Each
+    submitted step re-points the DecodeStep's input and output tensors (and
+    its cache) at that step's arena views.
     """
 
     ALIGN = 256

@@ -84,7 +84,8 @@ def test_plan_ok_and_workspace_layout(m):
     (dict(topk_width=100), -2), (dict(topk_width=-128), -1), (dict(kv_lora_rank=256), -2),
     (dict(rope_dim=32), -2), (dict(v_head_dim=128), -2), (dict(nope_dim=128), -2),
     (dict(causal=2), -1), (dict(sm_scale=0.0), -1), (dict(sm_scale=float("nan")), -1),
-    (dict(num_pages=0), -1), (dict(max_pages_per_seq=0), -1), (dict(batch=257), -2), (dict(batch=65, q_len=4), -2),
+    (dict(num_pages=0), -1), (dict(max_pages_per_seq=0), -1), (dict(batch=257), -2), (dict(batch=65, q_len=4, num_heads=32), -2),
+    (dict(batch=65, q_len=4, kv_dtype=1), -2), (dict(batch=129, q_len=4), -2),
     (dict(kv_dtype=1, topk_width=128), -2), (dict(kv_dtype=2, topk_width=128), -2),
     (dict(kv_dtype=3), -2), (dict(kv_dtype=-1), -2),
 ])
@@ -268,3 +269,12 @@ def test_bounded_wait_selftest_rejects_bad_arguments_before_cuda(m):
         with pytest.raises(m.MlaError) as e:
             m.mla_selftest_bounded_wait(status, limit, waited)
         assert e.value.code == code
+
+
+def test_row_set_limit_counts_grouped_drafts(m):
+    """The 256-row-set limit counts row sets, not query tokens: 64 requests
+    with 8 drafts of 6 heads are 64 grouped row sets (G = 8)."""
+    plan = m.mla_decode_plan(_problem(m, batch=64, q_len=8, num_heads=6), None, 152)
+    assert plan.num_streams == 64
+    plan = m.mla_decode_plan(_problem(m, batch=128, q_len=4), None, 152)   # G = 2
+    assert plan.num_streams == 256
