@@ -278,3 +278,32 @@ def test_row_set_limit_counts_grouped_drafts(m):
     assert plan.num_streams == 64
     plan = m.mla_decode_plan(_problem(m, batch=128, q_len=4), None, 152)   # G = 2
     assert plan.num_streams == 256
+
+
+def _stream_geom(s, q_len, group):
+    """Host restatement of the row-set geometry the kernels use."""
+    ng = -(-q_len // group)
+    b, gi = divmod(s, ng)
+    j0 = gi * group
+    return b, j0, min(group, q_len - j0)
+
+
+@pytest.mark.parametrize("batch,q_len,heads", [(3, 1, 20), (3, 2, 20), (2, 3, 20), (2, 5, 8),
+                                               (4, 7, 8), (2, 4, 12), (3, 2, 32)])
+def test_row_sets_partition_the_query_rows(m, batch, q_len, heads):
+    """Every (request, draft, head) output row belongs to exactly one row
+    set, as the contiguous block (b * Q + j0) * H .. + nq * H; the plan's row
+    set count matches the grouping rule."""
+    plan = m.mla_decode_plan(_problem(m, batch=batch, q_len=q_len, num_heads=heads), None, 152)
+    S = plan.num_streams
+    g_rule = min(q_len, 48 // heads)
+    group = g_rule if g_rule >= 2 else 1
+    assert S == batch * -(-q_len // group)
+    seen = np.zeros(batch * q_len * heads, dtype=np.int64)
+    for s in range(S):
+        b, j0, nq = _stream_geom(s, q_len, group)
+        assert 0 <= b < batch and nq >= 1
+        first = (b * q_len + j0) * heads
+        seen[first:first + nq * heads] += 1
+        assert nq * heads <= 48 or group == 1
+    assert (seen == 1).all()
