@@ -165,17 +165,20 @@ MLA_API int mla_q_absorb(const mla_plan* plan, const void* q_nope, const void* q
 
 /*
  * mla_decode_run -- the attention pass over the paged cache, followed by the
- * split-KV merge.  Each (request, query token) row set is cut into
+ * split-KV merge.  Each row set (request and query token; or request and a
+ * group of G draft tokens, see mla_plan.num_streams, whose G * H rows share
+ * every staged tile, each row keeping its own causal window) is cut into
  * contiguous 64-token tiles spread evenly over the plan's CTAs; a row set
  * handled by one CTA writes its result directly, one split over several
  * CTAs leaves normalised partials (o_i, lse_i) in the workspace, merged by a
  * second kernel launched right behind the first as a programmatic dependent
  * (its set-up overlaps the attention pass): lse = ln sum_i exp(lse_i),
- * o_lat = sum_i exp(lse_i - lse) o_i.  A row set with no visible token gets
- * o_lat = 0 and lse = -inf.
+ * o_lat = sum_i exp(lse_i - lse) o_i.  A row (query token, head) with no
+ * visible token gets o_lat = 0 and lse = -inf.
  *   q_hat       : bf16 [B*Q][H][576] absorbed queries
  *   kv_cache    : MLA_KV_BF16: bf16 [num_pages][P][576];
- *                 MLA_KV_FP8_E4M3_E8M0: uint8 [num_pages][P * 594]
+ *                 MLA_KV_FP8_E4M3_E8M0: uint8 [num_pages][P * 594];
+ *                 MLA_KV_FP4_E2M1_E8M0: uint8 [num_pages][P * 324]
  *   block_table : int32 [B][max_pages_per_seq]; entries past a request's
  *                 last page are never read
  *   seq_lens    : device int32 [B], 0 <= T_b <= max_pages_per_seq * P
@@ -227,6 +230,10 @@ MLA_API int mla_combine(const mla_plan* plan, const int32_t* seq_lens, const voi
  *                 448)) clamped to [-127, 127]; values round-to-nearest-even
  *                 e4m3 of x / 2^e, saturating at 448; an all-zero group gets
  *                 scale byte 0 and zero codes.
+ *                 MLA_KV_FP4_E2M1_E8M0: the same per 16-value group with 6
+ *                 for 448: e = ceil(log2(amax / 6)), codes the nearest e2m1
+ *                 value of x / 2^e, ties to the even code (the sign of a value
+ *                 rounding to zero kept), value 2i in the low nibble of byte i.
  *   status      : nullable device uint32; a position past the request's pages
  *                 sets MLA_STATUS_BAD_INDEX, a page id outside [0, num_pages)
  *                 MLA_STATUS_BAD_PAGE, and that row is not written.
