@@ -307,3 +307,23 @@ def test_row_sets_partition_the_query_rows(m, batch, q_len, heads):
         seen[first:first + nq * heads] += 1
         assert nq * heads <= 48 or group == 1
     assert (seen == 1).all()
+
+
+def test_plain_c_consumer_builds_and_plans(tmp_path):
+    """The header is valid C99 on its own, and a C program linked against the
+    library can plan a decode and read error strings (no GPU needed)."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    from head_latent_attention_paged_gb300 import LIB_PATH
+    libdir = os.path.dirname(LIB_PATH)
+    src = os.path.join(ROOT, "tests", "c_consumer", "plan_check.c")
+    exe = str(tmp_path / "plan_check")
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    src, "-o", exe, "-L", libdir, "-lmla_gb300", f"-Wl,-rpath,{libdir}"],
+                   check=True, capture_output=True)
+    out = subprocess.run([exe], capture_output=True, text=True)
+    assert out.returncode == 0, out.stderr
+    assert "plan_check ok" in out.stdout
