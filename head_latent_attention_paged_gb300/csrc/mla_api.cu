@@ -57,7 +57,8 @@ int group_of(const mla_problem& pr) {
 
 int decode_mode(const mla_problem& pr) {
   if (pr.kv_dtype == MLA_KV_FP8_E4M3_E8M0) return kModeDenseFp8;
-  if (pr.kv_dtype == MLA_KV_FP4_E2M1_E8M0) return kModeDenseFp4;
+  if (pr.kv_dtype == MLA_KV_FP4_E2M1_E8M0)
+    return group_of(pr) >= 2 ? kModeDenseFp4Multi : kModeDenseFp4;
   if (pr.topk_width > 0) return kModeSparseBf16;
   return group_of(pr) >= 2 ? kModeDenseMulti : kModeDenseBf16;
 }

@@ -71,14 +71,14 @@ constexpr int kGatherRows = kTile / kGatherWarps;   // 16 rows per gather warp
 template <int kMode>
 struct ModeTraits {
   static constexpr bool kFp8 = kMode == kModeDenseFp8;
-  static constexpr bool kFp4 = kMode == kModeDenseFp4;
+  static constexpr bool kFp4 = kMode == kModeDenseFp4 || kMode == kModeDenseFp4Multi;
   static constexpr bool kQuant = kFp8 || kFp4;   // quantised bytes, dequantised in the CTA
   static constexpr int kRowBytes = kFp4 ? kFp4RowBytes : kFp8RowBytes;    // quantised row
   static constexpr int kRawTileBytes = kTile * kRowBytes;
   static constexpr bool kSparse = kMode == kModeSparseBf16;
-  static constexpr bool kMulti = kMode == kModeDenseMulti;
+  static constexpr bool kMulti = kMode == kModeDenseMulti || kMode == kModeDenseFp4Multi;
   // dense bf16 staging (TMA tiles, dead rows zeroed by the softmax warps)
-  static constexpr bool kDenseBf16 = kMode == kModeDenseBf16 || kMulti;
+  static constexpr bool kDenseBf16 = kMode == kModeDenseBf16 || kMode == kModeDenseMulti;
   // the first softmax warp whose TMEM lanes hold rows: row r of a row set is
   // M-row 16 * kRowWarp0 + r of the QK accumulator
   static constexpr int kRowWarp0 = kMulti ? 1 : 2;
@@ -96,7 +96,7 @@ struct ModeTraits {
   // kRawTileBytes of the stage it is dequantised into.
   static constexpr bool kRawRing = kFp8;
   static constexpr int kNumStages = kRawRing ? kFp8Stages : kStages;   // bf16 tiles in flight
-  static constexpr int kQBatch = kThreads > 192 ? 3 : (kMulti ? 4 : 5);   // q_hat chunks per load batch
+  static constexpr int kQBatch = kThreads > 192 ? (kMulti ? 2 : 3) : (kMulti ? 4 : 5);   // q_hat chunks per load batch
   static constexpr int kRawSlots = kRawRing ? kFp8RawSlots : kStages;
   static constexpr int kRawOffset = kTileBytes - kRawTileBytes;
   static_assert(kRawSlots >= 1 && kRawOffset % 16 == 0, "raw tiles need 16-byte aligned slots");
@@ -489,7 +489,7 @@ DecodeLayout decode_layout(int heads, int heads_pad, int num_streams, int mode) 
   // the multi-token mode's RoPE query operand (1024-byte aligned after the stages)
   L.off_qrope = L.off_raw;
   L.off_ctrl = L.off_raw + (ring ? kFp8RawSlots * kFp8TileBytes : 0) +
-               (mode == kModeDenseMulti ? kQRopeBytes : 0);
+               (mode == kModeDenseMulti || mode == kModeDenseFp4Multi ? kQRopeBytes : 0);
   L.total = L.off_ctrl + static_cast<int>(sizeof(Ctrl)) + 2 * (num_streams + 1) * 4;
   return L;
 }
@@ -1386,6 +1386,13 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap* kv_map, int 
       if (err != cudaSuccess) return err;
       block = dim3(ModeTraits<kModeDenseMulti>::kThreads);
       mla_decode_kernel<kModeDenseMulti><<<grid, block, L.total, stream>>>(*kv_map, p, L);
+      break;
+    case kModeDenseFp4Multi:
+      err = cudaFuncSetAttribute(mla_decode_kernel<kModeDenseFp4Multi>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
+      if (err != cudaSuccess) return err;
+      block = dim3(ModeTraits<kModeDenseFp4Multi>::kThreads);
+      mla_decode_kernel<kModeDenseFp4Multi><<<grid, block, L.total, stream>>>(*kv_map, p, L);
       break;
     case kModeDenseFp4:
       err = cudaFuncSetAttribute(mla_decode_kernel<kModeDenseFp4>,

@@ -42,6 +42,7 @@ enum DecodeMode : int {
   kModeDenseFp8 = 2,
   kModeDenseFp4 = 3,
   kModeDenseMulti = 4,   // bf16, q_len > 1: draft tokens of a request share each staged tile
+  kModeDenseFp4Multi = 5,   // the same over an FP4 cache
 };
 
 struct DecodeParams {
@@ -121,10 +122,13 @@ __host__ __device__ inline StreamGeom stream_geom(int32_t s, int32_t q_len, int3
 
 // Query tokens per row set for a problem: the multi-token mode groups
 // min(q_len, 48 / H) draft tokens of a request when that is at least 2
-// (dense bf16 caches only).
+// (dense bf16 and FP4 caches; the FP8 kernel's shared memory has no room
+// for the RoPE query operand beside its raw-tile ring).
 __host__ __device__ inline int32_t row_set_group(int32_t q_len, int32_t heads, int32_t kv_dtype,
                                                  int32_t topk_width) {
-  if (kv_dtype != MLA_KV_BF16 || topk_width > 0 || q_len < 2) return 1;
+  if ((kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP4_E2M1_E8M0) || topk_width > 0 ||
+      q_len < 2)
+    return 1;
   const int32_t g = kMaxRows / heads;
   const int32_t gq = g < q_len ? g : q_len;
   return gq >= 2 ? gq : 1;

@@ -133,7 +133,10 @@ def test_multi_token_plan_groups_draft_tokens(m, q_len, heads, group):
     assert plan.ws_partial_lse >= plan.num_slots * rows * 512 * 4
     assert plan.ws_counters >= plan.ws_partial_lse + plan.num_slots * rows * 4
     assert plan.smem_bytes <= 232448
-    # quantised caches and top-k lists keep one row set per draft token
+    # FP4 caches group drafts the same way; FP8 caches keep one row set per draft
+    fp4 = m.mla_decode_plan(_problem(m, q_len=q_len, num_heads=heads,
+                                     kv_dtype=m.MLA_KV_FP4_E2M1_E8M0), seq, 152)
+    assert fp4.num_streams == plan.num_streams and fp4.smem_bytes <= 232448
     fp8 = m.mla_decode_plan(_problem(m, q_len=q_len, num_heads=heads,
                                      kv_dtype=m.MLA_KV_FP8_E4M3_E8M0), seq, 152)
     assert fp8.num_streams == 4 * q_len

@@ -54,17 +54,22 @@ def _run(batch, sm_count=None, label=""):
     (5, 8, True, 16, None),      # G = 5 (40 rows), 16-token pages
     (2, 32, True, 64, None),     # 48 / 32 = 1: one draft per row set
 ])
-def test_multi_token_matches_oracle(q_len, heads, causal, page_size, sm_count):
-    w = W.with_overrides(W.SMALL_WORKLOADS["dense_small"], q_len=q_len, heads=heads,
-                         causal=causal, page_size=page_size, batch=4, seq_lo=70, seq_hi=900)
-    _run(W.generate(w), sm_count=sm_count, label=f"q{q_len}/h{heads}/c{int(causal)}/p{page_size}")
+@pytest.mark.parametrize("kv", ["bf16", "fp4"])
+def test_multi_token_matches_oracle(q_len, heads, causal, page_size, sm_count, kv):
+    base = W.SMALL_WORKLOADS["dense_small" if kv == "bf16" else "fp4_small"]
+    w = W.with_overrides(base, q_len=q_len, heads=heads, causal=causal, page_size=page_size,
+                         batch=4, seq_lo=70, seq_hi=900)
+    _run(W.generate(w), sm_count=sm_count,
+         label=f"{kv}/q{q_len}/h{heads}/c{int(causal)}/p{page_size}")
 
 
-def test_multi_token_short_contexts():
+@pytest.mark.parametrize("kv", ["bf16", "fp4"])
+def test_multi_token_short_contexts(kv):
     """Contexts shorter than the drafts: with T = 1 and Q = 3 the first two
     drafts see no position (o = 0, lse = -inf) while the last sees one; other
     lengths end inside and at the edges of a tile for some drafts only."""
-    w = W.with_overrides(W.SMALL_WORKLOADS["dense_small"], q_len=3, heads=16,
+    base = W.SMALL_WORKLOADS["dense_small" if kv == "bf16" else "fp4_small"]
+    w = W.with_overrides(base, q_len=3, heads=16,
                          seq_lens=(1, 2, 3, 64, 65, 66, 127, 0), batch=8)
     batch = W.generate(w, garbage="nan")
     o_lat, lse = _run(batch, label="short")
