@@ -74,6 +74,42 @@ def test_visibility_golden():
         got = O.visible_positions(c["T"], c["Q"], c["j"], causal=True,
                                   topk_row=np.array(c["row"]))
         assert got.tolist() == c["visible"], c
+    # causal=0: every query token of a request sees the whole context
+    for c in g["dense_non_causal"]:
+        got = O.visible_positions(c["T"], c["Q"], c["j"], causal=False)
+        assert got.tolist() == c["visible"], c
+    for c in g["sparse_non_causal"]:
+        got = O.visible_positions(c["T"], c["Q"], c["j"], causal=False,
+                                  topk_row=np.array(c["row"]))
+        assert got.tolist() == c["visible"], c
+
+
+def test_bf16_codes_golden():
+    """Hand-decoded bf16 bit patterns (normal, subnormal, signed zero,
+    infinities, NaN) against the oracle's decoder."""
+    for code, val in _golden("bf16_codes.json")["codes"]:
+        got = O.bf16_to_f64(np.array([int(code, 16)], dtype=np.uint16))[0]
+        if val == "nan":
+            assert np.isnan(got), code
+        elif val in ("inf", "-inf"):
+            assert got == float(val), code
+        else:
+            assert got == val and math.copysign(1, got) == math.copysign(1, val), code
+
+
+def test_bf16_decoder_all_patterns_match_torch():
+    """All 65,536 bf16 bit patterns: the oracle's decoder agrees with torch's
+    bfloat16 -> float64 conversion (a library routine), NaNs by class and
+    zeros by sign."""
+    torch = pytest.importorskip("torch")
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    got = O.bf16_to_f64(bits)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert int(nan.sum()) == 2 * 127      # exponent field 255 with a non-zero mantissa
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(ref[~nan]))
 
 
 def _hex(s):
