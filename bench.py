@@ -2,14 +2,18 @@
 """Benchmark of one paged MLA decode step (one layer) on GB300.
 
 A step is the whole hot path over one synthetic decode batch: the attention
-pass over the paged latent cache, the LSE merge of split partials, and the
-W_UV up-projection (three kernels, each launched as a programmatic dependent
-of the one before; the absorbed query is an input, precomputed once).  The
+pass over the paged latent cache, then the LSE merge of split partials fused
+with the W_UV up-projection (two kernels, the second launched as a
+programmatic dependent of the first; the absorbed query is an input,
+precomputed once).  The
 default workload is the GLM-4.7-Flash-shaped dense decode: batch 64, 20
 heads, q_len 1, seq_lens ~ U[1024, 8192], page 64, bf16 latent cache.
 
 Metric: latent-cache GB/s (bytes of cached rows the step must read, over the
-step time) and decode tokens/s per layer.  Prints one JSON line.
+step time) and decode tokens/s per layer.  Prints one JSON line; besides the
+headline workload it carries, under per_workload, the decode kernel and the
+whole step of the long-context, FP8, sparse, FP4 and multi-token workloads,
+each timed launch by launch.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference ...   # the CPU oracle as the reference arm
@@ -317,13 +321,123 @@ def run_reference(args, world, rank):
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
+PER_WORKLOADS = ["long", "fp8", "sparse", "fp4", "mtp"]
+
+
+def kernel_label(w) -> str:
+    if w.kv_dtype in ("fp8", "fp4"):
+        return "mla_decode_kernel<dense %s%s>" % (w.kv_dtype, " multi-token" if w.q_len > 1 else "")
+    if w.topk:
+        return "mla_decode_kernel<sparse bf16>"
+    return "mla_decode_kernel<dense bf16%s>" % (" multi-token" if w.q_len > 1 else "")
+
+
+def prepare(w, device):
+    """The workload's batch and a DecodeStep on `device`.  FP8 and FP4 caches
+    are quantised on the GPU (mla_cache_append, scales from each group's
+    absolute maximum) from the workload's N(0, 1) latent rounded to bf16."""
+    import workloads as W
+    from head_latent_attention_paged_gb300 import (MLA_KV_BF16, MLA_KV_FP4_E2M1_E8M0,
+                                                   MLA_KV_FP8_E4M3_E8M0)
+    from head_latent_attention_paged_gb300.runner import DecodeStep, quantise_cache_on_device
+    kv = {"bf16": MLA_KV_BF16, "fp8": MLA_KV_FP8_E4M3_E8M0, "fp4": MLA_KV_FP4_E2M1_E8M0}[w.kv_dtype]
+    quant = w.kv_dtype in ("fp8", "fp4")
+    batch = W.generate(w, fp8_source="float" if quant else "codes")
+    cache = quantise_cache_on_device(batch.latent_f32, kv, device) if quant else batch.cache_bf16
+    if quant:
+        batch.latent_f32 = None     # the float latent is not needed any more
+    step = DecodeStep(q_nope=batch.q_nope, q_rope=batch.q_rope, w_uk=batch.w_uk, w_uv=batch.w_uv,
+                      cache=cache, block_table=batch.block_table, seq_lens=batch.seq_lens,
+                      page_size=w.page_size, kv_dtype=kv, topk_idx=batch.topk_idx,
+                      causal=w.causal, sm_scale=w.sm_scale, device=device)
+    return batch, step
+
+
+class Rotation:
+    """Between timed launches no launch may find the previous one's cache
+    lines in L2: a cache larger than the L2 is read from two copies in turn
+    (no flush, which would leave dirty lines for the next launch to write
+    back); a smaller one is flushed by writing 512 MiB before each launch."""
+
+    def __init__(self, step, device):
+        import torch
+        self.step = step
+        self.rotate = int(step.cache.numel()) * step.cache.element_size() > L2_BYTES
+        self.caches = [step.cache, step.cache.clone()] if self.rotate else [step.cache]
+        self.flush = None if self.rotate else torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8,
+                                                          device=device)
+
+    def before(self, k):
+        if self.rotate:
+            self.step.cache = self.caches[k % 2]
+        else:
+            self.flush.zero_()
+
+
+def timed(step, rot, n, stream, fn):
+    """n launches of fn(), each bracketed by CUDA events on `stream`: times
+    in ms."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    for k in range(n):
+        rot.before(k)
+        ev[k][0].record(stream)
+        fn()
+        ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def measure_workload(name, device, steps, hbm, warmup=3):
+    """Device-timed decode kernel alone and whole steps (decode, then merge +
+    W_UV) of one workload: medians and means over `steps` launches each."""
+    import gc
+    import torch
+    import workloads as W
+    w = W.WORKLOADS[name]
+    batch, step = prepare(w, device)
+    stream = torch.cuda.current_stream(device)
+    rot = Rotation(step, device)
+    for k in range(warmup):
+        rot.before(k)
+        step.step()
+    torch.cuda.synchronize()
+    if step.status() != 0:
+        raise SystemExit(f"{name}: decode reported status {step.status():#x}")
+    with ClockSampler(device.index or 0) as clocks:
+        dec = timed(step, rot, steps, stream, step.attend)
+        full = timed(step, rot, steps, stream, step.step)
+    byts = batch.latent_bytes_read
+    dm, fm = statistics.median(dec), statistics.median(full)
+    out = {
+        "workload": workload_description(w, batch, rot.rotate)["workload"],
+        "kernel": kernel_label(w),
+        "latent_bytes_per_step": int(byts),
+        "decode_us_median": 1e3 * dm, "decode_us_mean": 1e3 * statistics.mean(dec),
+        "decode_gbs": byts / (dm / 1e3) / 1e9, "decode_frac": byts / (dm / 1e3) / 1e9 / hbm,
+        "step_us_median": 1e3 * fm, "step_us_mean": 1e3 * statistics.mean(full),
+        "step_gbs": byts / (fm / 1e3) / 1e9, "step_frac": byts / (fm / 1e3) / 1e9 / hbm,
+        "tokens_per_s_per_layer": w.batch * w.q_len / (fm / 1e3),
+        "timed_launches": steps,
+        "traffic": recorded_traffic(name),
+        "l2": "two cache copies read in turn" if rot.rotate else "512 MiB flush before each launch",
+        "clocks": clocks.summary(),
+    }
+    if w.kv_dtype in ("fp8", "fp4"):
+        out["cache"] = ("N(0, 1) latent rounded to bf16, quantised on the GPU by mla_cache_append "
+                        "(one e8m0 scale per group from its absolute maximum)")
+    del step, rot, batch
+    gc.collect()
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_gpu(args, world, rank, local):
     import numpy as np
     import torch
     import workloads as W
     import __graft_entry__ as graft
-    from head_latent_attention_paged_gb300 import (MLA_KV_BF16, MLA_KV_FP4_E2M1_E8M0,
-                                                   MLA_KV_FP8_E4M3_E8M0)
     from head_latent_attention_paged_gb300.runner import DecodeStep
 
     torch.cuda.set_device(local)
@@ -332,93 +446,70 @@ def run_gpu(args, world, rank, local):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
     graft.build()
+    peaks = measured_peaks()
+    hbm = peaks.get("hbm_gbs")
+    peak_src = "measured (MEASURED_PEAKS.json hbm_gbs)"
+    if not hbm:
+        hbm, peak_src = 6800.0, "fallback 6.8 TB/s"
     w = W.WORKLOADS[args.workload]
-    batch = W.generate(w)
-    quant = w.kv_dtype in ("fp8", "fp4")
-    step = DecodeStep(q_nope=batch.q_nope, q_rope=batch.q_rope, w_uk=batch.w_uk, w_uv=batch.w_uv,
-                      cache=batch.cache_quant if quant else batch.cache_bf16,
-                      block_table=batch.block_table, seq_lens=batch.seq_lens,
-                      page_size=w.page_size,
-                      kv_dtype={"bf16": MLA_KV_BF16, "fp8": MLA_KV_FP8_E4M3_E8M0,
-                                "fp4": MLA_KV_FP4_E2M1_E8M0}[w.kv_dtype],
-                      topk_idx=batch.topk_idx, causal=w.causal, sm_scale=w.sm_scale,
-                      device=device)
+    batch, step = prepare(w, device)
     stream = torch.cuda.current_stream(device)
     byts = batch.latent_bytes_read
-    # Between timed steps: when the cache is larger than the L2, consecutive
-    # steps read two copies of it in turn (no step finds the previous one's
-    # lines in L2, and no flush leaves dirty lines for the step to write
-    # back); a smaller cache is flushed out of L2 before every step instead.
-    rotate = cache_bytes(batch) > L2_BYTES
-    caches = [step.cache, step.cache.clone()] if rotate else [step.cache]
-    flush = None if rotate else torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
-
-    def between_steps(k):
-        if rotate:
-            step.cache = caches[k % 2]
-        else:
-            flush.zero_()
+    rot = Rotation(step, device)
 
     for k in range(args.warmup):
-        between_steps(k)
+        rot.before(k)
         step.step()
     torch.cuda.synchronize(device)
     if step.status() != 0:
         raise SystemExit(f"decode reported status {step.status():#x}")
 
-    # Every step is bracketed by events; every RUN_EVERY-th step also gets an
-    # event between the attention pass (+ merge) and the W_UV launch, which
-    # times the decode kernels for the roofline.  That event breaks the
-    # programmatic-dependent overlap of W_UV with the merge, so it is kept
-    # off the other steps.
-    RUN_EVERY = 8
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    # The K timed steps: each one the attention pass and the merge fused with
+    # W_UV (two launches, the second a programmatic dependent of the first),
+    # bracketed by events on the launching stream.
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(device)
     with ClockSampler(local) as clocks:
         t_wall = time.perf_counter()
         for k in range(args.steps):
-            between_steps(k)
+            rot.before(k)
             ev[k][0].record(stream)
-            step.run()
-            if k % RUN_EVERY == RUN_EVERY - 1:
-                ev[k][1].record(stream)
-            step.uv()
-            ev[k][2].record(stream)
+            step.step()
+            ev[k][1].record(stream)
         torch.cuda.synchronize(device)
         t_wall = time.perf_counter() - t_wall
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize(device)
-    run_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(args.steps)
-              if k % RUN_EVERY == RUN_EVERY - 1]
-    if not run_ms:   # fewer steps than RUN_EVERY: time the last one's decode alone
-        between_steps(args.steps)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        step.run()
-        e1.record(stream)
+        if world > 1:
+            torch.distributed.barrier()
         torch.cuda.synchronize(device)
-        run_ms = [e0.elapsed_time(e1)]
-    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
+        # The decode kernel alone, timed on every one of its own launches
+        # (after the step loop, so the steps keep their launch overlap).
+        dec_ms = timed(step, rot, max(args.decode_steps, 20), stream, step.attend)
+    per_workload = {}
+    if world == 1 and args.per_workload:
+        for name in PER_WORKLOADS:
+            if name != args.workload:
+                per_workload[name] = measure_workload(name, device, args.per_workload_steps, hbm)
+    step_ms = [e[0].elapsed_time(e[1]) for e in ev]
     step_s = sum(step_ms) / 1e3
     tot_bytes, max_s = aggregate(float(byts) * args.steps, step_s, world, device)
     value = tot_bytes / max_s / 1e9
     ms_per_step = 1e3 * max_s / args.steps
-    decode_ms = statistics.mean(run_ms)
+    decode_ms = statistics.median(dec_ms)
 
     # End to end through the public API with host buffers.  The latent cache
     # is device-resident state (as in serving); what a decode step gets from
     # the host is its inputs: the absorbed queries, the block table, the
     # context lengths, the top-k lists (sparse) and each request's newest
-    # token row, which mla_cache_append writes at its slot.  Every step
-    # copies those in from pinned host memory (one copy of one packed
-    # arena), appends, runs the step and copies o and lse back (one copy);
-    # HostPipeline overlaps step k's copies with the neighbouring steps'
-    # kernels on two copy streams.  No L2 flush here (it would sit inside the
-    # pipelined region): the benchmark workloads' caches are larger than the
-    # 129 MB L2, and consecutive steps read two different copies of them.
+    # token row, which mla_cache_append rotates (RoPE, theta 1e6) and writes
+    # at its slot.  Every step copies those in from pinned host memory (one
+    # copy of one packed arena), appends, runs the step and copies o and lse
+    # back (one copy); HostPipeline overlaps step k's copies with the
+    # neighbouring steps' kernels on two copy streams.  No L2 flush here (it
+    # would sit inside the pipelined region): the benchmark workloads' caches
+    # are larger than the 129 MB L2, and consecutive steps read two different
+    # copies of them.
     e2e = None
     if args.e2e_steps > 0:
         from head_latent_attention_paged_gb300.runner import HostPipeline
@@ -428,11 +519,10 @@ def run_gpu(args, world, rank, local):
         last_pos = (batch.seq_lens.astype(np.int64) - 1).astype(np.int32)
         rng = np.random.default_rng(w.seed + 1)
         rows_np = W.f32_to_bf16_bits(rng.standard_normal((w.batch, 576)).astype(np.float32))
-        # the two copies of the cache, taken in turn as in the timed loop
         pipe = HostPipeline(step, q_hat_bits=step.q_hat.view(torch.int16).cpu().numpy(),
                             block_table=batch.block_table, seq_lens=batch.seq_lens,
                             new_rows=rows_np, positions=last_pos, topk_idx=batch.topk_idx,
-                            caches=caches if rotate else None)
+                            caches=rot.caches if rot.rotate else None, rope_theta=1.0e6)
         WARM = 3
         for k in range(WARM):
             pipe.submit(k, stream)
@@ -468,19 +558,15 @@ def run_gpu(args, world, rank, local):
                "ms_per_step": 1e3 * es / args.e2e_steps,
                "inputs": "q_hat, block table, seq_lens, top-k lists, newest token row and "
                          "position per request, one packed host->device copy per step "
-                         "(rows appended with mla_cache_append; cache resident); o and lse "
-                         "one device->host copy per step; copies pipelined against the "
-                         "neighbouring steps on two copy streams (double-buffered), the "
-                         "timed steps replayed as one CUDA graph; no L2 flush: consecutive "
-                         "steps read two copies of the cache (each larger than L2)"}
+                         "(rows RoPE-rotated and appended with mla_cache_append; cache "
+                         "resident); o and lse one device->host copy per step; copies "
+                         "pipelined against the neighbouring steps on two copy streams "
+                         "(double-buffered), the timed steps replayed as one CUDA graph; no "
+                         "L2 flush: consecutive steps read two copies of the cache (each "
+                         "larger than L2)"}
 
     if rank != 0:
         return 0
-    peaks = measured_peaks()
-    hbm = peaks.get("hbm_gbs")
-    peak_src = "measured (MEASURED_PEAKS.json hbm_gbs)"
-    if not hbm:
-        hbm, peak_src = 6800.0, "fallback 6.8 TB/s"
     achieved = byts / (decode_ms / 1e3) / 1e9
     traffic = recorded_traffic(args.workload)
     line = {
@@ -490,28 +576,31 @@ def run_gpu(args, world, rank, local):
         "dtype": {"bf16": "bf16", "fp8": "fp8-e4m3+e8m0 cache, bf16 tensor-core math",
                   "fp4": "fp4-e2m1+e8m0 cache, bf16 tensor-core math"}[w.kv_dtype],
         "data": "synthetic",
-        "config": workload_description(w, batch, rotate),
+        "config": workload_description(w, batch, rot.rotate),
         "tokens_per_s_per_layer": w.batch * w.q_len * world / (max_s / args.steps),
         "hbm_fraction_of_measured": value / hbm,
-        "kernel_ms": {"decode_with_merge": decode_ms,
-                      "decode_with_merge_median": statistics.median(run_ms),
+        "kernel_ms": {"decode": statistics.mean(dec_ms), "decode_median": decode_ms,
+                      "decode_timed_launches": len(dec_ms),
                       "step": statistics.mean(step_ms), "step_median": statistics.median(step_ms),
-                      "decode_timed_steps": len(run_ms)},
+                      "step_timed": len(step_ms)},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": traffic,
-                     "kernel": "mla_decode_kernel<%s>" % (
-                         "dense " + w.kv_dtype if quant else
-                         ("sparse bf16" if w.topk else
-                          ("dense bf16 multi-token" if w.q_len > 1 else "dense bf16"))),
+                     "kernel": kernel_label(w),
+                     "timing": f"median of {len(dec_ms)} launches of the decode kernel alone, "
+                               "each bracketed by CUDA events on its stream",
                      "peak_source": peak_src,
-                     "algorithmic_bytes_per_launch": int(byts)},
+                     "algorithmic_bytes_per_launch": int(byts),
+                     "step_frac": byts / (statistics.median(step_ms) / 1e3) / 1e9 / hbm},
+        "per_workload": per_workload or None,
         "e2e": e2e,
         "gpu_launches": DecodeStep.KERNELS_PER_STEP * args.steps,
         "clocks": clocks.summary(),
         "wall_s_timed_region": t_wall,
         "status": step.status(),
     }
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and w.kv_dtype != "bf16":
+        line["cpu_baseline"] = None   # the quantised cache exists on the GPU only
+    elif world == 1 and not args.no_cpu_baseline:
         cb, ct, what = oracle_sample(batch, args.cpu_budget)
         n_req = int(what.split()[0]) if what.split()[0].isdigit() else 1
         ab, at, _ = oracle_sample(batch, 1e9, form="absorbed", max_requests=n_req)
@@ -537,6 +626,13 @@ def main():
                     choices=["tiny", "dense", "long", "fp8", "sparse", "fp4", "mtp"])
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--decode-steps", type=int, default=1000,
+                    help="launches of the decode kernel alone timed one by one")
+    ap.add_argument("--per-workload-steps", type=int, default=300,
+                    help="launches of the decode kernel alone and of whole steps timed one by "
+                         "one for each of the other workloads")
+    ap.add_argument("--no-per-workload", dest="per_workload", action="store_false",
+                    help="skip the long / fp8 / sparse / fp4 / mtp measurements")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -60,7 +60,9 @@ class MlaPlan(ctypes.Structure):
         ("ws_partial_o", ctypes.c_int64), ("ws_partial_lse", ctypes.c_int64),
         ("ws_counters", ctypes.c_int64), ("ws_status", ctypes.c_int64),
         ("workspace_bytes", ctypes.c_int64),
-        ("planned_tiles", ctypes.c_int64), ("reserved", ctypes.c_int32 * 8),
+        ("planned_tiles", ctypes.c_int64), ("ws_q_hat", ctypes.c_int64),
+        ("split_tokens", ctypes.c_int32), ("sm_count", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 4),
     ]
 
 
@@ -84,13 +86,14 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib = ctypes.CDLL(p)
     vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
     P = ctypes.POINTER
-    lib.mla_decode_plan.argtypes = [P(MlaProblem), P(ctypes.c_int32), i32, P(MlaPlan)]
-    lib.mla_q_absorb.argtypes = [P(MlaPlan), vp, vp, vp, vp, vp]
-    lib.mla_decode_run.argtypes = [P(MlaPlan), vp, vp, vp, vp, vp, vp, vp, vp, vp]
-    lib.mla_combine.argtypes = [P(MlaPlan), vp, vp, vp, vp, vp]
+    sz = ctypes.c_size_t
+    lib.mla_decode_plan.argtypes = [P(MlaProblem), P(ctypes.c_int32), i32, i32, P(MlaPlan), P(sz)]
+    lib.mla_q_absorb.argtypes = [P(MlaPlan), vp, vp, vp, vp]
+    lib.mla_decode_run.argtypes = [P(MlaPlan), vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
+    lib.mla_combine.argtypes = [P(MlaPlan), vp, vp, sz, vp, vp, vp, vp, vp]
     lib.mla_decode_run_static.argtypes = [P(MlaPlan), vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.mla_uv_proj.argtypes = [vp, vp, vp, i32, i32, vp]
-    lib.mla_cache_append.argtypes = [P(MlaProblem), vp, vp, vp, vp, vp, vp]
+    lib.mla_cache_append.argtypes = [P(MlaProblem), vp, vp, vp, ctypes.c_float, vp, vp, vp]
     lib.mla_selftest_bounded_wait.argtypes = [vp, i64, vp, vp]
     lib.mla_get_status.argtypes = [P(MlaPlan), vp, P(ctypes.c_uint32), vp]
     lib.mla_clear_status.argtypes = [P(MlaPlan), vp, vp]
@@ -142,8 +145,20 @@ def make_problem(batch, q_len, num_heads, page_size, num_pages, max_pages_per_se
                       sm_scale)
 
 
-def mla_decode_plan(problem: MlaProblem, seq_lens_host=None, sm_count: int = 152) -> MlaPlan:
+def _nbytes(buf, given, plan) -> int:
+    """Byte size of a device buffer: as given, else a tensor's size, else the
+    plan's workspace size (a bare address carries no size)."""
+    if given is not None:
+        return int(given)
+    if hasattr(buf, "numel") and hasattr(buf, "element_size"):
+        return int(buf.numel()) * int(buf.element_size())
+    return int(plan.workspace_bytes)
+
+
+def mla_decode_plan(problem: MlaProblem, seq_lens_host=None, sm_count: int = 152,
+                    split_tokens: int = 0) -> MlaPlan:
     plan = MlaPlan()
+    ws = ctypes.c_size_t(0)
     arr = None
     if seq_lens_host is not None:
         arr = np.ascontiguousarray(seq_lens_host, dtype=np.int32)
@@ -151,43 +166,57 @@ def mla_decode_plan(problem: MlaProblem, seq_lens_host=None, sm_count: int = 152
     else:
         ptr = None
     _check("mla_decode_plan", load().mla_decode_plan(ctypes.byref(problem), ptr, int(sm_count),
-                                                     ctypes.byref(plan)))
+                                                     int(split_tokens), ctypes.byref(plan),
+                                                     ctypes.byref(ws)))
+    assert ws.value == plan.workspace_bytes
     return plan
 
 
-def mla_q_absorb(plan: MlaPlan, q_nope, q_rope, w_uk, q_hat, stream=None) -> None:
-    _check("mla_q_absorb", load().mla_q_absorb(ctypes.byref(plan), _ptr(q_nope), _ptr(q_rope),
-                                               _ptr(w_uk), _ptr(q_hat), _stream(stream)))
+def mla_q_absorb(plan: MlaPlan, q, w_uk, q_hat, stream=None) -> None:
+    """q_hat = [W_UK[h] q[..., :192] || q[..., 192:]] (q bf16 [B*Q][H][256])."""
+    _check("mla_q_absorb", load().mla_q_absorb(ctypes.byref(plan), _ptr(q), _ptr(w_uk),
+                                               _ptr(q_hat), _stream(stream)))
 
 
-def mla_decode_run(plan: MlaPlan, q_hat, kv_cache, block_table, seq_lens, topk_idx, workspace,
-                   o_lat, lse, stream=None) -> None:
+def mla_decode_run(plan: MlaPlan, q, w_uk, kv_cache, block_table, seq_lens, topk_idx, workspace,
+                   o_lat, lse, stream=None, workspace_bytes=None) -> None:
+    """The attention pass.  q is the absorbed q_hat (w_uk None) or the
+    un-absorbed [q_nope || q_rope] with w_uk.  Split row sets are completed
+    by mla_combine."""
     _check("mla_decode_run", load().mla_decode_run(
-        ctypes.byref(plan), _ptr(q_hat), _ptr(kv_cache), _ptr(block_table), _ptr(seq_lens),
-        _ptr(topk_idx), _ptr(workspace), _ptr(o_lat), _ptr(lse), _stream(stream)))
+        ctypes.byref(plan), _ptr(q), _ptr(w_uk), _ptr(kv_cache), _ptr(block_table),
+        _ptr(seq_lens), _ptr(topk_idx), _ptr(workspace), _nbytes(workspace, workspace_bytes, plan),
+        _ptr(o_lat), _ptr(lse), _stream(stream)))
 
 
 def mla_decode_run_static(plan: MlaPlan, q_hat, kv_cache, block_table, seq_lens, topk_idx,
                           o_lat, lse, status=None, stream=None) -> None:
-    """mla_decode_run without a caller workspace: the scratch is the library's
-    fixed 16 MiB device array (for callers that cannot allocate)."""
+    """mla_decode_run and the merge without a caller workspace: the scratch is
+    the library's fixed 16 MiB device array (for callers that cannot
+    allocate)."""
     _check("mla_decode_run_static", load().mla_decode_run_static(
         ctypes.byref(plan), _ptr(q_hat), _ptr(kv_cache), _ptr(block_table), _ptr(seq_lens),
         _ptr(topk_idx), _ptr(o_lat), _ptr(lse), _ptr(status), _stream(stream)))
 
 
-def mla_combine(plan: MlaPlan, seq_lens, workspace, o_lat, lse, stream=None) -> None:
-    _check("mla_combine", load().mla_combine(ctypes.byref(plan), _ptr(seq_lens), _ptr(workspace),
-                                             _ptr(o_lat), _ptr(lse), _stream(stream)))
+def mla_combine(plan: MlaPlan, seq_lens, workspace, o_lat, lse, w_uv=None, out=None,
+                stream=None, workspace_bytes=None) -> None:
+    """Merge split row sets into o_lat / lse; with w_uv also out = W_UV^T o_lat
+    (bf16 [B*Q][H][256]) in the same kernel."""
+    _check("mla_combine", load().mla_combine(
+        ctypes.byref(plan), _ptr(seq_lens), _ptr(workspace),
+        _nbytes(workspace, workspace_bytes, plan), _ptr(w_uv), _ptr(o_lat), _ptr(lse), _ptr(out),
+        _stream(stream)))
 
 
 def mla_cache_append(problem: MlaProblem, new_rows, positions, block_table, kv_cache,
-                     status=None, stream=None) -> None:
+                     status=None, stream=None, rope_theta: float = 0.0) -> None:
     """Write row b of new_rows (bf16 [batch][576]) at logical position
-    positions[b] of request b (bf16 copy or on-GPU FP8 / FP4 quantisation)."""
+    positions[b] of request b (bf16 copy or on-GPU FP8 / FP4 quantisation);
+    with rope_theta > 0 its RoPE key is rotated to that position first."""
     _check("mla_cache_append", load().mla_cache_append(
         ctypes.byref(problem), _ptr(new_rows), _ptr(positions), _ptr(block_table),
-        _ptr(kv_cache), _ptr(status), _stream(stream)))
+        float(rope_theta), _ptr(kv_cache), _ptr(status), _stream(stream)))
 
 
 def mla_selftest_bounded_wait(status, limit_ns: int, waited_ns=None, stream=None) -> None:

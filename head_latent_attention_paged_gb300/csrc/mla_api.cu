@@ -15,7 +15,7 @@ using namespace mla;
 
 namespace {
 
-constexpr int kAbiVersion = 10000;   // 1.0.0
+constexpr int kAbiVersion = 20000;   // 2.0.0
 constexpr int64_t kAlign = 256;
 
 int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
@@ -37,19 +37,100 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // 2-D bf16 tensor map: `rows` rows of `cols` elements (row stride
-// `row_bytes`), box of box_cols x box_rows, 128-byte swizzle.
+// `row_bytes`), box of box_cols x box_rows, 128-byte swizzle.  Encoded maps
+// are kept in a small table keyed by every argument, so a decode step that
+// reuses its cache and weights does no encoding on the host.
+struct MapKey {
+  const void* base;
+  uint64_t cols, rows, row_bytes;
+  uint32_t box_cols, box_rows;
+  bool operator==(const MapKey& o) const {
+    return base == o.base && cols == o.cols && rows == o.rows && row_bytes == o.row_bytes &&
+           box_cols == o.box_cols && box_rows == o.box_rows;
+  }
+};
+constexpr int kMapCacheSize = 32;
+std::mutex g_map_mutex;
+MapKey g_map_keys[kMapCacheSize];
+CUtensorMap g_maps[kMapCacheSize];
+int g_map_count = 0, g_map_next = 0;
+
 bool make_map_bf16(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows,
                    uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows) {
+  const MapKey key{base, cols, rows, row_bytes, box_cols, box_rows};
+  {
+    std::lock_guard<std::mutex> lock(g_map_mutex);
+    for (int i = 0; i < g_map_count; ++i)
+      if (g_map_keys[i] == key) {
+        *map = g_maps[i];
+        return true;
+      }
+  }
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {row_bytes};
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t es[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-             box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  if (enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+          es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  std::lock_guard<std::mutex> lock(g_map_mutex);
+  const int slot = g_map_count < kMapCacheSize ? g_map_count++ : (g_map_next++ % kMapCacheSize);
+  g_map_keys[slot] = key;
+  g_maps[slot] = *map;
+  return true;
 }
+
+}  // namespace
+
+namespace mla {
+
+// The current CUDA context (a driver handle, queried through the runtime's
+// entry-point lookup so the library needs no link-time driver dependency).
+// Per-context caches compare it to notice a context that was replaced.
+void* current_context() {
+  using Fn = CUresult (*)(CUcontext*);
+  static Fn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<Fn>(ptr);
+  });
+  CUcontext ctx = nullptr;
+  if (fn == nullptr || fn(&ctx) != CUDA_SUCCESS) return nullptr;
+  return ctx;
+}
+
+cudaError_t set_smem_attr_once(const void* func, int slot, int bytes) {
+  constexpr int kDevices = 64, kSlots = 16;
+  static std::mutex mu;
+  static int done[kDevices][kSlots] = {};
+  static void* ctx_of[kDevices][kSlots] = {};
+  int dev = -1;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= kDevices || slot < 0 || slot >= kSlots)
+    return cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  void* ctx = current_context();
+  std::lock_guard<std::mutex> lock(mu);
+  if (ctx != nullptr && ctx_of[dev][slot] == ctx && done[dev][slot] >= bytes) return cudaSuccess;
+  err = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (err == cudaSuccess) {
+    done[dev][slot] = ctx_of[dev][slot] == ctx ? (bytes > done[dev][slot] ? bytes : done[dev][slot]) : bytes;
+    ctx_of[dev][slot] = ctx;
+  }
+  return err;
+}
+
+}  // namespace mla
+
+namespace {
 
 int group_of(const mla_problem& pr) {
   return row_set_group(pr.q_len, pr.num_heads, pr.kv_dtype, pr.topk_width);
@@ -67,6 +148,25 @@ int decode_mode(const mla_problem& pr) {
 int32_t num_row_sets(const mla_problem& pr) {
   const int32_t g = group_of(pr);
   return pr.batch * ((pr.q_len + g - 1) / g);
+}
+
+// The cache shape and options every entry point shares (the append needs
+// no more than this).
+int validate_cache_shape(const mla_problem* pr) {
+  if (pr == nullptr) return MLA_ERR_INVALID_ARGUMENT;
+  if (pr->batch < 0 || pr->num_pages < 1 || pr->max_pages_per_seq < 1)
+    return MLA_ERR_INVALID_ARGUMENT;
+  if (pr->kv_lora_rank != kDc || pr->rope_dim != kDr || pr->nope_dim != kDnope ||
+      pr->v_head_dim != kDv)
+    return MLA_ERR_UNSUPPORTED;
+  if (pr->page_size != 16 && pr->page_size != 32 && pr->page_size != 64 && pr->page_size != 128)
+    return MLA_ERR_UNSUPPORTED;
+  if (pr->kv_dtype != MLA_KV_BF16 && pr->kv_dtype != MLA_KV_FP8_E4M3_E8M0 &&
+      pr->kv_dtype != MLA_KV_FP4_E2M1_E8M0)
+    return MLA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(pr->num_pages) * pr->page_size > INT32_MAX) return MLA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(pr->max_pages_per_seq) * pr->page_size > INT32_MAX) return MLA_ERR_UNSUPPORTED;
+  return MLA_OK;
 }
 
 int validate_problem(const mla_problem* pr) {
@@ -141,13 +241,17 @@ void fill_combine_params(const mla_plan& plan, const uint8_t* ws, const int32_t*
   p.num_ctas = plan.num_ctas;
 }
 
-int plan_check(const mla_plan* plan) {
-  if (plan == nullptr) return MLA_ERR_INVALID_ARGUMENT;
-  const int rc = validate_problem(&plan->problem);
-  if (rc != MLA_OK) return rc;
-  if (plan->num_streams != num_row_sets(plan->problem) || plan->num_ctas < 1)
-    return MLA_ERR_INVALID_ARGUMENT;
-  return MLA_OK;
+int absorb(const mla_plan& plan, const void* q, const void* w_uk, void* q_hat, cudaStream_t st) {
+  const mla_problem& pr = plan.problem;
+  const int rows = pr.batch * pr.q_len;
+  if (rows == 0) return MLA_OK;
+  CUtensorMap w_map;
+  if (!make_map_bf16(&w_map, w_uk, kDnope, static_cast<uint64_t>(pr.num_heads) * kDc, kDnope * 2,
+                     64, 128))
+    return MLA_ERR_CUDA;
+  const cudaError_t err = launch_q_absorb(&w_map, static_cast<const uint16_t*>(q),
+                                          static_cast<uint16_t*>(q_hat), rows, pr.num_heads, st);
+  return err == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
 }  // namespace
@@ -155,6 +259,98 @@ int plan_check(const mla_plan* plan) {
 namespace mla {
 cudaError_t launch_wait_selftest(uint32_t* status, uint64_t limit_ns, uint64_t* waited_ns,
                                  cudaStream_t stream);
+
+int plan_check(const mla_plan* plan) {
+  if (plan == nullptr) return MLA_ERR_INVALID_ARGUMENT;
+  const int rc = validate_problem(&plan->problem);
+  if (rc != MLA_OK) return rc;
+  if (plan->num_streams != num_row_sets(plan->problem) || plan->num_ctas < 1 || plan->sm_count < 1 ||
+      plan->num_ctas > kMaxCtas || plan->num_slots != plan->num_streams + plan->num_ctas - 1 ||
+      plan->ws_partial_o < 0 || plan->ws_partial_lse < plan->ws_partial_o ||
+      plan->ws_q_hat < plan->ws_partial_lse || plan->ws_counters < plan->ws_q_hat ||
+      plan->ws_status < plan->ws_counters || plan->ws_status + 4 > plan->workspace_bytes)
+    return MLA_ERR_INVALID_ARGUMENT;
+  return MLA_OK;
+}
+
+int check_run_args(const mla_plan* plan, const void* q, const void* w_uk, const void* kv_cache,
+                   const int32_t* block_table, const int32_t* seq_lens, const int32_t* topk_idx,
+                   const void* workspace, size_t workspace_bytes, const float* o_lat,
+                   const float* lse) {
+  const int rc = plan_check(plan);
+  if (rc != MLA_OK) return rc;
+  const mla_problem& pr = plan->problem;
+  if (!q || !kv_cache || !block_table || !seq_lens || !workspace || !o_lat || !lse)
+    return MLA_ERR_INVALID_ARGUMENT;
+  if ((pr.topk_width > 0) != (topk_idx != nullptr)) return MLA_ERR_INVALID_ARGUMENT;
+  if (workspace_bytes < static_cast<size_t>(plan->workspace_bytes)) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned16(q) || (w_uk && !aligned16(w_uk)) || !aligned16(kv_cache) ||
+      !aligned16(workspace) || !aligned16(o_lat) || (reinterpret_cast<uintptr_t>(lse) & 3u) ||
+      (reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
+      (topk_idx && (reinterpret_cast<uintptr_t>(topk_idx) & 3u)))
+    return MLA_ERR_MISALIGNED;
+  return MLA_OK;
+}
+
+int launch_attention(const mla_plan& plan, const void* q_hat, const void* kv_cache,
+                     const int32_t* block_table, const int32_t* seq_lens, const int32_t* topk_idx,
+                     uint8_t* ws, float* o_lat, float* lse, cudaStream_t st) {
+  const mla_problem& pr = plan.problem;
+  if (plan.num_streams == 0) return MLA_OK;
+  const int mode = decode_mode(pr);
+  CUtensorMap kv_map;
+  std::memset(&kv_map, 0, sizeof(kv_map));   // FP8 / FP4 caches are read with bulk copies
+  if (mode != kModeDenseFp8 && mode != kModeDenseFp4 && mode != kModeDenseFp4Multi &&
+      !make_map_bf16(&kv_map, kv_cache, kDqk, static_cast<uint64_t>(pr.num_pages) * pr.page_size,
+                     kDqk * 2, kChunkElems, pr.page_size < kTile ? pr.page_size : kTile))
+    return MLA_ERR_CUDA;
+  DecodeParams p;
+  p.q_hat = static_cast<const uint16_t*>(q_hat);
+  p.kv = static_cast<const uint8_t*>(kv_cache);
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.topk_idx = topk_idx;
+  p.part_o = reinterpret_cast<float*>(ws + plan.ws_partial_o);
+  p.part_lse = reinterpret_cast<float*>(ws + plan.ws_partial_lse);
+  p.o_lat = o_lat;
+  p.lse = lse;
+  p.status = reinterpret_cast<uint32_t*>(ws + plan.ws_status);
+  p.batch = pr.batch;
+  p.q_len = pr.q_len;
+  p.heads = pr.num_heads;
+  p.group = group_of(pr);
+  p.rows = p.group * pr.num_heads;
+  p.heads_pad = (p.rows + 15) / 16 * 16;
+  p.page_size = pr.page_size;
+  p.num_pages = pr.num_pages;
+  p.max_pages = pr.max_pages_per_seq;
+  p.topk_width = pr.topk_width;
+  p.causal = pr.causal;
+  p.num_streams = plan.num_streams;
+  p.num_ctas = plan.num_ctas;
+  p.scale_log2 = pr.sm_scale * 1.4426950408889634f;
+  return launch_decode(p, &kv_map, mode, st) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int launch_merge(const mla_plan& plan, const int32_t* seq_lens, const uint8_t* ws,
+                 const void* w_uv, float* o_lat, float* lse, void* out, cudaStream_t st) {
+  if (plan.num_streams == 0) return MLA_OK;
+  CombineParams cp;
+  fill_combine_params(plan, ws, seq_lens, o_lat, lse, &cp);
+  cudaError_t err;
+  if (w_uv == nullptr) {
+    err = launch_combine(cp, st);
+  } else {
+    const mla_problem& pr = plan.problem;
+    CUtensorMap w_map;
+    if (!make_map_bf16(&w_map, w_uv, kDv, static_cast<uint64_t>(pr.num_heads) * kDc, kDv * 2, 64,
+                       64))
+      return MLA_ERR_CUDA;
+    err = launch_combine_uv(&w_map, cp, static_cast<uint16_t*>(out), plan.sm_count, st);
+  }
+  return err == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
 }  // namespace mla
 
 extern "C" {
@@ -174,13 +370,17 @@ const char* mla_strerror(int code) {
 }
 
 int mla_decode_plan(const mla_problem* problem, const int32_t* seq_lens_host, int32_t sm_count,
-                    mla_plan* plan_out) {
+                    int32_t split_tokens, mla_plan* plan_out, size_t* workspace_bytes) {
   int rc = validate_problem(problem);
   if (rc != MLA_OK) return rc;
-  if (plan_out == nullptr || sm_count < 1) return MLA_ERR_INVALID_ARGUMENT;
+  if (plan_out == nullptr || sm_count < 1 || split_tokens < 0 || split_tokens % kTile != 0)
+    return MLA_ERR_INVALID_ARGUMENT;
+  if (split_tokens > 0 && seq_lens_host == nullptr) return MLA_ERR_INVALID_ARGUMENT;
   mla_plan pl;
   std::memset(&pl, 0, sizeof(pl));
   pl.problem = *problem;
+  pl.split_tokens = split_tokens;
+  pl.sm_count = sm_count;
   const mla_problem& pr = pl.problem;
   pl.num_streams = num_row_sets(pr);
   const int rows = group_of(pr) * pr.num_heads;   // rows of a full row set
@@ -193,7 +393,15 @@ int mla_decode_plan(const mla_problem* problem, const int32_t* seq_lens_host, in
   }
   pl.planned_tiles = tiles;
   int64_t ctas = sm_count;
-  if (seq_lens_host != nullptr) ctas = tiles < 1 ? 1 : (tiles < sm_count ? tiles : sm_count);
+  if (split_tokens > 0) {
+    // split-KV by length: about split_tokens tokens per CTA
+    const int64_t per = split_tokens / kTile;
+    ctas = (tiles + per - 1) / per;
+    if (ctas < 1) ctas = 1;
+    if (ctas > kMaxCtas) return MLA_ERR_UNSUPPORTED;
+  } else if (seq_lens_host != nullptr) {
+    ctas = tiles < 1 ? 1 : (tiles < sm_count ? tiles : sm_count);
+  }
   pl.num_ctas = static_cast<int32_t>(ctas);
   pl.num_slots = pl.num_streams + pl.num_ctas - 1;
   if (pl.num_slots < 1) pl.num_slots = 1;
@@ -204,99 +412,59 @@ int mla_decode_plan(const mla_problem* problem, const int32_t* seq_lens_host, in
   off = align_up(off + static_cast<int64_t>(pl.num_slots) * rows * kDc * 4, kAlign);
   pl.ws_partial_lse = off;
   off = align_up(off + static_cast<int64_t>(pl.num_slots) * rows * 4, kAlign);
+  pl.ws_q_hat = off;
+  off = align_up(off + static_cast<int64_t>(pr.batch) * pr.q_len * pr.num_heads * kDqk * 2, kAlign);
   pl.ws_counters = off;
   off = align_up(off + static_cast<int64_t>(pl.num_streams) * 4, kAlign);
   pl.ws_status = off;
   off = align_up(off + 4, kAlign);
   pl.workspace_bytes = off;
   *plan_out = pl;
+  if (workspace_bytes != nullptr) *workspace_bytes = static_cast<size_t>(off);
   return MLA_OK;
 }
 
-int mla_q_absorb(const mla_plan* plan, const void* q_nope, const void* q_rope, const void* w_uk,
-                 void* q_hat, mla_stream_t stream) {
+int mla_q_absorb(const mla_plan* plan, const void* q, const void* w_uk, void* q_hat,
+                 mla_stream_t stream) {
   int rc = plan_check(plan);
   if (rc != MLA_OK) return rc;
-  if (!q_nope || !q_rope || !w_uk || !q_hat) return MLA_ERR_INVALID_ARGUMENT;
-  if (!aligned16(q_nope) || !aligned16(q_rope) || !aligned16(w_uk) || !aligned16(q_hat))
-    return MLA_ERR_MISALIGNED;
-  const cudaError_t err = launch_q_absorb(
-      static_cast<const uint16_t*>(q_nope), static_cast<const uint16_t*>(q_rope),
-      static_cast<const uint16_t*>(w_uk), static_cast<uint16_t*>(q_hat),
-      plan->problem.batch * plan->problem.q_len, plan->problem.num_heads,
-      reinterpret_cast<cudaStream_t>(stream));
-  return err == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+  if (!q || !w_uk || !q_hat) return MLA_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(w_uk) || !aligned16(q_hat)) return MLA_ERR_MISALIGNED;
+  return absorb(*plan, q, w_uk, q_hat, reinterpret_cast<cudaStream_t>(stream));
 }
 
-int mla_decode_run(const mla_plan* plan, const void* q_hat, const void* kv_cache,
+int mla_decode_run(const mla_plan* plan, const void* q, const void* w_uk, const void* kv_cache,
                    const int32_t* block_table, const int32_t* seq_lens, const int32_t* topk_idx,
-                   void* workspace, float* o_lat, float* lse, mla_stream_t stream) {
-  int rc = plan_check(plan);
+                   void* workspace, size_t workspace_bytes, float* o_lat, float* lse,
+                   mla_stream_t stream) {
+  int rc = check_run_args(plan, q, w_uk, kv_cache, block_table, seq_lens, topk_idx, workspace,
+                          workspace_bytes, o_lat, lse);
   if (rc != MLA_OK) return rc;
-  const mla_problem& pr = plan->problem;
-  if (!q_hat || !kv_cache || !block_table || !seq_lens || !workspace || !o_lat || !lse)
-    return MLA_ERR_INVALID_ARGUMENT;
-  if ((pr.topk_width > 0) != (topk_idx != nullptr)) return MLA_ERR_INVALID_ARGUMENT;
-  if (!aligned16(q_hat) || !aligned16(kv_cache) || !aligned16(workspace) || !aligned16(o_lat) ||
-      (reinterpret_cast<uintptr_t>(lse) & 3u) ||
-      (reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
-      (topk_idx && (reinterpret_cast<uintptr_t>(topk_idx) & 3u)))
-    return MLA_ERR_MISALIGNED;
   if (plan->num_streams == 0) return MLA_OK;
-  const int mode = decode_mode(pr);
-  CUtensorMap kv_map;
-  std::memset(&kv_map, 0, sizeof(kv_map));   // FP8 / FP4 caches are read with bulk copies
-  if (mode != kModeDenseFp8 && mode != kModeDenseFp4 &&
-      !make_map_bf16(&kv_map, kv_cache, kDqk, static_cast<uint64_t>(pr.num_pages) * pr.page_size,
-                     kDqk * 2, kChunkElems, pr.page_size < kTile ? pr.page_size : kTile))
-    return MLA_ERR_CUDA;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  DecodeParams p;
-  p.q_hat = static_cast<const uint16_t*>(q_hat);
-  p.kv = static_cast<const uint8_t*>(kv_cache);
-  p.block_table = block_table;
-  p.seq_lens = seq_lens;
-  p.topk_idx = topk_idx;
-  p.part_o = reinterpret_cast<float*>(ws + plan->ws_partial_o);
-  p.part_lse = reinterpret_cast<float*>(ws + plan->ws_partial_lse);
-  p.o_lat = o_lat;
-  p.lse = lse;
-  p.status = reinterpret_cast<uint32_t*>(ws + plan->ws_status);
-  p.batch = pr.batch;
-  p.q_len = pr.q_len;
-  p.heads = pr.num_heads;
-  p.group = group_of(pr);
-  p.rows = p.group * pr.num_heads;
-  p.heads_pad = (p.rows + 15) / 16 * 16;
-  p.page_size = pr.page_size;
-  p.num_pages = pr.num_pages;
-  p.max_pages = pr.max_pages_per_seq;
-  p.topk_width = pr.topk_width;
-  p.causal = pr.causal;
-  p.num_streams = plan->num_streams;
-  p.num_ctas = plan->num_ctas;
-  p.scale_log2 = pr.sm_scale * 1.4426950408889634f;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t err = launch_decode(p, &kv_map, mode, st);
-  if (err != cudaSuccess) return MLA_ERR_CUDA;
-  // split row sets: merge their partials (all SMs, dependent launch)
-  CombineParams cp;
-  fill_combine_params(*plan, ws, seq_lens, o_lat, lse, &cp);
-  err = launch_combine(cp, st);
-  return err == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const void* q_hat = q;
+  if (w_uk != nullptr) {   // absorb the queries into the workspace first
+    q_hat = ws + plan->ws_q_hat;
+    rc = absorb(*plan, q, w_uk, ws + plan->ws_q_hat, st);
+    if (rc != MLA_OK) return rc;
+  }
+  return launch_attention(*plan, q_hat, kv_cache, block_table, seq_lens, topk_idx, ws, o_lat, lse,
+                          st);
 }
 
-int mla_combine(const mla_plan* plan, const int32_t* seq_lens, const void* workspace, float* o_lat,
-                float* lse, mla_stream_t stream) {
+int mla_combine(const mla_plan* plan, const int32_t* seq_lens, const void* workspace,
+                size_t workspace_bytes, const void* w_uv, float* o_lat, float* lse, void* out,
+                mla_stream_t stream) {
   int rc = plan_check(plan);
   if (rc != MLA_OK) return rc;
-  if (!seq_lens || !workspace || !o_lat || !lse) return MLA_ERR_INVALID_ARGUMENT;
-  if (!aligned16(workspace) || !aligned16(o_lat) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+  if (!seq_lens || !workspace || !o_lat || !lse || (w_uv && !out)) return MLA_ERR_INVALID_ARGUMENT;
+  if (workspace_bytes < static_cast<size_t>(plan->workspace_bytes)) return MLA_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned16(workspace) || !aligned16(o_lat) || (reinterpret_cast<uintptr_t>(lse) & 3u) ||
+      (w_uv && (!aligned16(w_uv) || !aligned16(out))) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
     return MLA_ERR_MISALIGNED;
-  CombineParams p;
-  fill_combine_params(*plan, static_cast<const uint8_t*>(workspace), seq_lens, o_lat, lse, &p);
-  const cudaError_t err = launch_combine(p, reinterpret_cast<cudaStream_t>(stream));
-  return err == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+  return launch_merge(*plan, seq_lens, static_cast<const uint8_t*>(workspace), w_uv, o_lat, lse,
+                      out, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int mla_uv_proj(const float* o_lat, const void* w_uv, void* out, int32_t rows, int32_t num_heads,
@@ -314,11 +482,13 @@ int mla_uv_proj(const float* o_lat, const void* w_uv, void* out, int32_t rows, i
 }
 
 int mla_cache_append(const mla_problem* problem, const void* new_rows, const int32_t* positions,
-                     const int32_t* block_table, void* kv_cache, uint32_t* status,
-                     mla_stream_t stream) {
-  const int rc = validate_problem(problem);
+                     const int32_t* block_table, float rope_theta, void* kv_cache,
+                     uint32_t* status, mla_stream_t stream) {
+  const int rc = validate_cache_shape(problem);
   if (rc != MLA_OK) return rc;
   if (!new_rows || !positions || !block_table || !kv_cache) return MLA_ERR_INVALID_ARGUMENT;
+  if (!std::isfinite(rope_theta) || rope_theta < 0.f || (rope_theta > 0.f && rope_theta <= 1.f))
+    return MLA_ERR_INVALID_ARGUMENT;
   if (!aligned16(new_rows) || !aligned16(kv_cache) ||
       (reinterpret_cast<uintptr_t>(positions) & 3u) ||
       (reinterpret_cast<uintptr_t>(block_table) & 3u) ||
@@ -335,6 +505,7 @@ int mla_cache_append(const mla_problem* problem, const void* new_rows, const int
   p.num_pages = problem->num_pages;
   p.max_pages = problem->max_pages_per_seq;
   p.kv_dtype = problem->kv_dtype;
+  p.rope_theta = rope_theta;
   const cudaError_t err = launch_append(p, reinterpret_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }

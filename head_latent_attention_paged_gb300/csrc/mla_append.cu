@@ -1,8 +1,9 @@
 // Cache append: write each request's newest token row (the shared latent
-// c_kv and the rotated RoPE key, 576 values) into the paged latent cache, as
-// bf16, in the FP8 layout (576 e4m3 || 18 e8m0 per token) or in the FP4
-// layout (288 bytes of packed e2m1 || 36 e8m0 per token) with the quantiser
-// run on the GPU.
+// c_kv and the RoPE key, 576 values; the key rotated here to the token's
+// position when a rope_theta is given) into the paged latent cache, as bf16,
+// in the FP8 layout (576 e4m3 || 18 e8m0 per token) or in the FP4 layout
+// (288 bytes of packed e2m1 || 36 e8m0 per token) with the quantiser run on
+// the GPU.
 //
 // One warp per row.  FP8: for each 32-value group the warp takes the group's
 // absolute maximum, picks the scale 2^e with e = ceil(log2(amax / 448))
@@ -65,6 +66,13 @@ __device__ __forceinline__ uint32_t f32_to_e2m1(float v) {
   return mag | ((__float_as_uint(v) >> 28) & 8u);
 }
 
+// Nearest bf16 (ties to even) of a double, as bits: one rounding.  The
+// rotated RoPE values are finite and far inside bf16's normal range.
+__device__ __forceinline__ uint32_t f64_to_bf16_bits(double x) {
+  const __nv_bfloat16 h = __double2bfloat16(x);
+  return *reinterpret_cast<const uint16_t*>(&h);
+}
+
 // 2^-e as a float for e in [-127, 127] (2^-127 is the subnormal 0x00400000).
 __device__ __forceinline__ float pow2_neg(int e) {
   return e == 127 ? __uint_as_float(0x00400000u) : __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
@@ -95,10 +103,35 @@ __global__ void __launch_bounds__(32 * kAppendWarps) mla_append_kernel(const App
   }
   const int64_t row = static_cast<int64_t>(page) * p.page_size + pos % p.page_size;
   const uint16_t* src = p.new_rows + static_cast<int64_t>(b) * kDqk;
+  // The RoPE key (values 512..575): lane i holds pair i = (x[512 + 2i],
+  // x[513 + 2i]) as two bf16, rotated to position pos when rope_theta > 0:
+  // angle pos * theta^(-2i/64), in double precision (positions reach 2^17
+  // radians at pair 0), rounded once to bf16.
+  uint32_t rope_pair = *reinterpret_cast<const uint32_t*>(src + kDc + 2 * lane);
+  if (p.rope_theta > 0.f) {
+    const double x0 = bf16_bits_to_f32(static_cast<uint16_t>(rope_pair & 0xFFFFu));
+    const double x1 = bf16_bits_to_f32(static_cast<uint16_t>(rope_pair >> 16));
+    const double inv_freq = pow(static_cast<double>(p.rope_theta), -2.0 * lane / kDr);
+    double sn, cs;
+    sincos(static_cast<double>(pos) * inv_freq, &sn, &cs);
+    const uint32_t y0 = f64_to_bf16_bits(x0 * cs - x1 * sn);
+    const uint32_t y1 = f64_to_bf16_bits(x0 * sn + x1 * cs);
+    rope_pair = y0 | (y1 << 16);
+  }
+  // value v of the row (as stored: RoPE part rotated), read by lane `lane`
+  // of the warp for v = 32 k + lane; every lane calls it with the same k
+  auto value32 = [&](int k) -> float {
+    if (k < kDc / 32) return bf16_bits_to_f32(src[32 * k + lane]);
+    const int e = 32 * (k - kDc / 32) + lane;      // RoPE element
+    const uint32_t pr = __shfl_sync(0xffffffffu, rope_pair, e >> 1);
+    return bf16_bits_to_f32(static_cast<uint16_t>((e & 1) ? (pr >> 16) : (pr & 0xFFFFu)));
+  };
   if (p.kv_dtype == MLA_KV_BF16) {
     const uint4* s4 = reinterpret_cast<const uint4*>(src);
-    uint4* d4 = reinterpret_cast<uint4*>(p.kv + row * (kDqk * 2));
-    for (int i = lane; i < kDqk * 2 / 16; i += 32) d4[i] = s4[i];
+    uint8_t* d = p.kv + row * (kDqk * 2);
+    uint4* d4 = reinterpret_cast<uint4*>(d);
+    for (int i = lane; i < kDc * 2 / 16; i += 32) d4[i] = s4[i];
+    reinterpret_cast<uint32_t*>(d + kDc * 2)[lane] = rope_pair;
     return;
   }
   if (p.kv_dtype == MLA_KV_FP4_E2M1_E8M0) {
@@ -106,7 +139,7 @@ __global__ void __launch_bounds__(32 * kAppendWarps) mla_append_kernel(const App
     uint8_t* dst = p.kv + row * kFp4RowBytes;
     for (int it = 0; it < kDqk / 32; ++it) {
       const int g = 2 * it + (lane >> 4);
-      const float x = bf16_bits_to_f32(src[32 * it + lane]);
+      const float x = value32(it);
       float amax = fabsf(x);
 #pragma unroll
       for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
@@ -124,7 +157,7 @@ __global__ void __launch_bounds__(32 * kAppendWarps) mla_append_kernel(const App
   }
   uint8_t* dst = p.kv + row * kFp8RowBytes;
   for (int g = 0; g < kDqk / 32; ++g) {
-    const float x = bf16_bits_to_f32(src[32 * g + lane]);
+    const float x = value32(g);
     float amax = fabsf(x);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));

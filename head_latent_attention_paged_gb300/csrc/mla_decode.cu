@@ -528,8 +528,9 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
   }
 
   // ---------------------------------------------------------------- setup
-  // Let a dependent launch (the W_UV projection) start its prologue as soon
-  // as SMs free up; it waits for this grid's completion before reading.
+  // Let a dependent launch (the merge, with or without W_UV) start its
+  // prologue as soon as SMs free up; it waits for this grid's completion
+  // before reading.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0) {
     for (int i = 0; i < kNumStages; ++i) {
@@ -1354,57 +1355,31 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
   }
 }
 
+namespace {
+template <int kMode>
+cudaError_t launch_mode(const CUtensorMap* kv_map, const DecodeParams& p, const DecodeLayout& L,
+                        cudaStream_t stream) {
+  const cudaError_t err =
+      set_smem_attr_once(reinterpret_cast<const void*>(mla_decode_kernel<kMode>), 3 + kMode, L.total);
+  if (err != cudaSuccess) return err;
+  mla_decode_kernel<kMode>
+      <<<dim3(p.num_ctas), dim3(ModeTraits<kMode>::kThreads), L.total, stream>>>(*kv_map, p, L);
+  return cudaGetLastError();
+}
+}  // namespace
+
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap* kv_map, int mode,
                           cudaStream_t stream) {
   const DecodeLayout L = decode_layout(p.heads, p.heads_pad, p.num_streams, mode);
-  dim3 grid(p.num_ctas), block(ModeTraits<kModeDenseBf16>::kThreads);
-  cudaError_t err;
   switch (mode) {
-    case kModeDenseBf16:
-      err = cudaFuncSetAttribute(mla_decode_kernel<kModeDenseBf16>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
-      if (err != cudaSuccess) return err;
-      mla_decode_kernel<kModeDenseBf16><<<grid, block, L.total, stream>>>(*kv_map, p, L);
-      break;
-    case kModeSparseBf16:
-      err = cudaFuncSetAttribute(mla_decode_kernel<kModeSparseBf16>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
-      if (err != cudaSuccess) return err;
-      block = dim3(ModeTraits<kModeSparseBf16>::kThreads);
-      mla_decode_kernel<kModeSparseBf16><<<grid, block, L.total, stream>>>(*kv_map, p, L);
-      break;
-    case kModeDenseFp8:
-      err = cudaFuncSetAttribute(mla_decode_kernel<kModeDenseFp8>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
-      if (err != cudaSuccess) return err;
-      block = dim3(ModeTraits<kModeDenseFp8>::kThreads);
-      mla_decode_kernel<kModeDenseFp8><<<grid, block, L.total, stream>>>(*kv_map, p, L);
-      break;
-    case kModeDenseMulti:
-      err = cudaFuncSetAttribute(mla_decode_kernel<kModeDenseMulti>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
-      if (err != cudaSuccess) return err;
-      block = dim3(ModeTraits<kModeDenseMulti>::kThreads);
-      mla_decode_kernel<kModeDenseMulti><<<grid, block, L.total, stream>>>(*kv_map, p, L);
-      break;
-    case kModeDenseFp4Multi:
-      err = cudaFuncSetAttribute(mla_decode_kernel<kModeDenseFp4Multi>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
-      if (err != cudaSuccess) return err;
-      block = dim3(ModeTraits<kModeDenseFp4Multi>::kThreads);
-      mla_decode_kernel<kModeDenseFp4Multi><<<grid, block, L.total, stream>>>(*kv_map, p, L);
-      break;
-    case kModeDenseFp4:
-      err = cudaFuncSetAttribute(mla_decode_kernel<kModeDenseFp4>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
-      if (err != cudaSuccess) return err;
-      block = dim3(ModeTraits<kModeDenseFp4>::kThreads);
-      mla_decode_kernel<kModeDenseFp4><<<grid, block, L.total, stream>>>(*kv_map, p, L);
-      break;
-    default:
-      return cudaErrorInvalidValue;
+    case kModeDenseBf16: return launch_mode<kModeDenseBf16>(kv_map, p, L, stream);
+    case kModeSparseBf16: return launch_mode<kModeSparseBf16>(kv_map, p, L, stream);
+    case kModeDenseFp8: return launch_mode<kModeDenseFp8>(kv_map, p, L, stream);
+    case kModeDenseFp4: return launch_mode<kModeDenseFp4>(kv_map, p, L, stream);
+    case kModeDenseMulti: return launch_mode<kModeDenseMulti>(kv_map, p, L, stream);
+    case kModeDenseFp4Multi: return launch_mode<kModeDenseFp4Multi>(kv_map, p, L, stream);
+    default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 int decode_smem_bytes(int heads, int heads_pad, int num_streams, int mode) {

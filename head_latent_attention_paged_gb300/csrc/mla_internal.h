@@ -28,6 +28,7 @@ constexpr int kMaxHeads = 32;     // TMEM: q_hat 288 + S 64 + O^T 4 x 32 columns
 // RoPE part of q_hat is a shared-memory operand).
 constexpr int kMaxRows = 48;
 constexpr int kMaxStreams = 256;  // per-stream tile prefix kept in shared memory
+constexpr int kMaxCtas = 65536;   // decode grid limit (split-KV by length)
 // 72 KB bf16 tiles in flight per CTA.  An FP4 tile of quantised rows
 // (20,736 B) is copied into the tail of the stage it is dequantised into;
 // FP8 tiles (38,016 B) have a ring of their own beside two bf16 stages.
@@ -86,6 +87,15 @@ struct CombineParams {
 };
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
 
+// The merge of split row sets fused with the W_UV up-projection: per (head,
+// 128 output dims, 32 rows), every row's o_lat (merged from the partials
+// when its row set was split, else as the decode wrote it) becomes the B
+// operand of D^T = W_UV[h]^T o_lat^T.  Writes out (bf16) for every row and,
+// in the blocks of the first 128 output dims, o_lat and lse of split rows.
+// sm_count sizes the row blocks (16, 32 or 64 rows) so the grid fits.
+cudaError_t launch_combine_uv(const CUtensorMap* w_map, const CombineParams& p, uint16_t* out,
+                              int sm_count, cudaStream_t stream);
+
 cudaError_t launch_uv_proj_tma(const CUtensorMap* w_map, const float* o_lat, uint16_t* out,
                                int rows, int heads, cudaStream_t stream);
 
@@ -97,12 +107,34 @@ struct AppendParams {
   uint32_t* status;             // nullable
   int32_t rows, page_size, num_pages, max_pages;
   int32_t kv_dtype;             // MLA_KV_BF16, MLA_KV_FP8_E4M3_E8M0 or MLA_KV_FP4_E2M1_E8M0
+  float rope_theta;             // > 0: rotate k_rope to the row's position first
 };
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
 
-cudaError_t launch_q_absorb(const uint16_t* q_nope, const uint16_t* q_rope,
-                            const uint16_t* w_uk, uint16_t* q_hat, int rows, int heads,
-                            cudaStream_t stream);
+// q_hat[r][h] = [bf16(W_UK[h] q[r][h][:192]) || q[r][h][192:256]] on the
+// tensor cores; w_map: W_UK as [H * 512 rows][192] bf16, boxes of 64 x 128.
+cudaError_t launch_q_absorb(const CUtensorMap* w_map, const uint16_t* q, uint16_t* q_hat,
+                            int rows, int heads, cudaStream_t stream);
+
+// Sets a kernel's maximum dynamic shared memory once per device (the
+// attribute belongs to the current device's context).
+cudaError_t set_smem_attr_once(const void* func, int slot, int bytes);
+
+// The current CUDA context (nullptr if none or unknown).
+void* current_context();
+
+// Host steps shared by the entry points (MLA_* return codes).
+int plan_check(const mla_plan* plan);
+// Everything mla_decode_run checks before it queues any work.
+int check_run_args(const mla_plan* plan, const void* q, const void* w_uk, const void* kv_cache,
+                   const int32_t* block_table, const int32_t* seq_lens, const int32_t* topk_idx,
+                   const void* workspace, size_t workspace_bytes, const float* o_lat,
+                   const float* lse);
+int launch_attention(const mla_plan& plan, const void* q_hat, const void* kv_cache,
+                     const int32_t* block_table, const int32_t* seq_lens, const int32_t* topk_idx,
+                     uint8_t* ws, float* o_lat, float* lse, cudaStream_t st);
+int launch_merge(const mla_plan& plan, const int32_t* seq_lens, const uint8_t* ws,
+                 const void* w_uv, float* o_lat, float* lse, void* out, cudaStream_t st);
 
 // Row set s covers request b and query tokens j0 .. j0 + nq - 1 (the group
 // of `group` consecutive draft tokens; group = 1 outside the multi-token

@@ -7,8 +7,9 @@ from typing import Optional
 import numpy as np
 import torch
 
-from . import (MLA_KV_BF16, MLA_KV_FP4_E2M1_E8M0, MLA_KV_FP8_E4M3_E8M0, make_problem, mla_clear_status, mla_combine,
-               mla_decode_plan, mla_decode_run, mla_get_status, mla_q_absorb, mla_uv_proj)
+from . import (MLA_KV_BF16, MLA_KV_FP4_E2M1_E8M0, MLA_KV_FP8_E4M3_E8M0, make_problem,
+               mla_clear_status, mla_combine, mla_decode_plan, mla_decode_run, mla_get_status,
+               mla_q_absorb, mla_uv_proj)
 
 
 def to_device_bf16(bits: np.ndarray, device) -> torch.Tensor:
@@ -26,14 +27,15 @@ class DecodeStep:
     Inputs (numpy, host): q_nope/q_rope bf16 bits [B, Q, H, 192/64],
     w_uk [H, 512, 192] and w_uv [H, 512, 256] bf16 bits, the cache (bf16 bits
     [num_pages, P, 576], FP8 bytes [num_pages, P*594] or FP4 bytes
-    [num_pages, P*324]), block_table int32
+    [num_pages, P*324], or such a cache already on the device as a torch
+    tensor), block_table int32
     [B, max_pages], seq_lens int32 [B], optional topk_idx int32 [B*Q, width].
     """
 
     def __init__(self, *, q_nope, q_rope, w_uk, w_uv, cache, block_table, seq_lens,
                  page_size: int, kv_dtype: int = MLA_KV_BF16, topk_idx=None, causal: bool = True,
                  sm_scale: float = 1.0 / 16.0, sm_count: Optional[int] = None, device="cuda:0",
-                 absorb_on_device: bool = True):
+                 absorb_on_device: bool = True, split_tokens: int = 0):
         self.device = torch.device(device)
         B, Q, H, _ = q_nope.shape
         self.B, self.Q, self.H = B, Q, H
@@ -45,13 +47,15 @@ class DecodeStep:
         self.problem = make_problem(B, Q, H, page_size, num_pages, int(block_table.shape[1]),
                                     kv_dtype=kv_dtype, topk_width=width, causal=int(causal),
                                     sm_scale=sm_scale)
-        self.plan = mla_decode_plan(self.problem, seq_lens, sm_count)
+        self.plan = mla_decode_plan(self.problem, seq_lens, sm_count, split_tokens)
         dev = self.device
-        self.q_nope = to_device_bf16(q_nope, dev)
-        self.q_rope = to_device_bf16(q_rope, dev)
+        # the un-absorbed query, one [q_nope (192) || q_rope (64)] per head
+        self.q = to_device_bf16(np.concatenate([q_nope, q_rope], axis=-1).reshape(B * Q, H, 256), dev)
         self.w_uk = to_device_bf16(w_uk, dev)
         self.w_uv = to_device_bf16(w_uv, dev)
-        if kv_dtype in (MLA_KV_FP8_E4M3_E8M0, MLA_KV_FP4_E2M1_E8M0):
+        if isinstance(cache, torch.Tensor):          # already on the device
+            self.cache = cache
+        elif kv_dtype in (MLA_KV_FP8_E4M3_E8M0, MLA_KV_FP4_E2M1_E8M0):
             self.cache = to_device(cache.astype(np.uint8, copy=False), dev)
         else:
             self.cache = to_device_bf16(cache, dev)
@@ -71,26 +75,43 @@ class DecodeStep:
         return torch.cuda.current_stream(self.device)
 
     def absorb(self):
-        mla_q_absorb(self.plan, self.q_nope, self.q_rope, self.w_uk, self.q_hat, self.stream)
+        mla_q_absorb(self.plan, self.q, self.w_uk, self.q_hat, self.stream)
+
+    def attend(self, w_uk=False):
+        """The attention pass alone (mla_decode_run): rows of row sets held by
+        one CTA are final, split ones wait in the workspace for combine().
+        w_uk=True hands the library the un-absorbed query and W_UK instead of
+        q_hat (it absorbs into the workspace first)."""
+        if w_uk:
+            mla_decode_run(self.plan, self.q, self.w_uk, self.cache, self.block_table,
+                           self.seq_lens, self.topk_idx, self.workspace, self.o_lat, self.lse,
+                           self.stream)
+        else:
+            mla_decode_run(self.plan, self.q_hat, None, self.cache, self.block_table,
+                           self.seq_lens, self.topk_idx, self.workspace, self.o_lat, self.lse,
+                           self.stream)
+
+    def combine(self, uv: bool = False):
+        """Merge split row sets (mla_combine); uv=True also writes out =
+        W_UV^T o_lat in the same kernel."""
+        mla_combine(self.plan, self.seq_lens, self.workspace, self.o_lat, self.lse,
+                    self.w_uv if uv else None, self.out if uv else None, self.stream)
 
     def run(self):
-        """Attention pass and the split merge (two kernels, the second a
-        programmatic dependent of the first): writes o_lat and lse."""
-        mla_decode_run(self.plan, self.q_hat, self.cache, self.block_table, self.seq_lens,
-                       self.topk_idx, self.workspace, self.o_lat, self.lse, self.stream)
-
-    def combine(self):
-        """Re-run the split merge from the partials left in the workspace."""
-        mla_combine(self.plan, self.seq_lens, self.workspace, self.o_lat, self.lse, self.stream)
+        """Attention pass and merge: o_lat and lse complete (two kernels, the
+        second a programmatic dependent of the first)."""
+        self.attend()
+        self.combine()
 
     def uv(self):
+        """W_UV as a pass of its own over o_lat (mla_uv_proj)."""
         mla_uv_proj(self.o_lat, self.w_uv, self.out, self.rows, self.H, self.stream)
 
     def step(self):
-        """Attention pass, split merge and W_UV projection; the absorbed
-        query is an input."""
-        self.run()
-        self.uv()
+        """One decode step: the attention pass, then the merge fused with the
+        W_UV projection (two kernels); the absorbed query is an input."""
+        self.attend()
+        self.combine(uv=True)
 
     def status(self) -> int:
         return mla_get_status(self.plan, self.workspace, self.stream)
@@ -98,7 +119,7 @@ class DecodeStep:
     def clear_status(self):
         mla_clear_status(self.plan, self.workspace, self.stream)
 
-    KERNELS_PER_STEP = 3
+    KERNELS_PER_STEP = 2
 
 
 class HostPipeline:
@@ -110,9 +131,9 @@ class HostPipeline:
     the step's outputs (o and lse) come back in one copy.  `depth` sets of
     arenas rotate, and the copies run on their own streams: the inputs of
     step k + 1 and the outputs of step k - 1 move while step k computes.
-    Each step appends its newest token rows to the cache (mla_cache_append)
-    and runs the decode, the merge and the W_UV projection on the compute
-    stream.
+    Each step appends its newest token rows to the cache (mla_cache_append,
+    RoPE applied to their keys when rope_theta > 0) and runs the decode and
+    the merge fused with the W_UV projection on the compute stream.
 
     The caller refills host arena `k % depth` for step k only after
     `input_copied(k - depth)` has been synchronised (the static inputs of a
@@ -126,8 +147,9 @@ class HostPipeline:
     ALIGN = 256
 
     def __init__(self, step: DecodeStep, *, q_hat_bits, block_table, seq_lens, new_rows,
-                 positions, topk_idx=None, depth: int = 2, caches=None):
+                 positions, topk_idx=None, depth: int = 2, caches=None, rope_theta: float = 0.0):
         self.step = step
+        self.rope_theta = rope_theta
         self.depth = depth
         self.caches = list(caches) if caches else [step.cache]
         dev = step.device
@@ -199,7 +221,7 @@ class HostPipeline:
         return o, lse
 
     def submit(self, k: int, compute_stream=None):
-        """Enqueue step k: input copy, append + decode + merge + W_UV, output copy."""
+        """Enqueue step k: input copy, append + decode + merge/W_UV, output copy."""
         from . import mla_cache_append
         i = k % self.depth
         st = self.step
@@ -220,7 +242,7 @@ class HostPipeline:
         st.cache = self.caches[k % len(self.caches)]
         with torch.cuda.stream(cs):
             mla_cache_append(st.problem, v["new_rows"], v["positions"], st.block_table, st.cache,
-                             stream=cs)
+                             stream=cs, rope_theta=self.rope_theta)
             st.step()
             self.computed[i].record(cs)
         self.d2h_stream.wait_event(self.computed[i])
@@ -255,3 +277,28 @@ class HostPipeline:
         """Make the compute stream wait for step k_last's outputs on the host."""
         cs = compute_stream if compute_stream is not None else torch.cuda.current_stream(self.step.device)
         cs.wait_event(self.d2h_done[k_last % self.depth])
+
+
+def quantise_cache_on_device(latent_f32: np.ndarray, kv_dtype: int, device,
+                             chunk_rows: int = 1 << 18) -> torch.Tensor:
+    """An FP8 or FP4 paged cache made on the GPU from a float latent
+    [num_pages, P, 576]: every slot's row, rounded to bf16, is quantised by
+    mla_cache_append (scales from each group's absolute maximum).  Returns the
+    cache bytes [num_pages, P * row_bytes] on `device`."""
+    from . import mla_cache_append
+    num_pages, P, D = latent_f32.shape
+    row_bytes = 594 if kv_dtype == MLA_KV_FP8_E4M3_E8M0 else 324
+    cache = torch.empty((num_pages, P * row_bytes), dtype=torch.uint8, device=device)
+    flat = latent_f32.reshape(-1, D)
+    n = flat.shape[0]
+    for s in range(0, n, chunk_rows):
+        e = min(n, s + chunk_rows)
+        rows = torch.from_numpy(np.ascontiguousarray(flat[s:e])).to(device).to(torch.bfloat16)
+        idx = torch.arange(s, e, dtype=torch.int64, device=device)
+        # row r of the chunk is slot r % P of page r // P: a one-page block
+        # table per row and its slot as the position
+        bt = (idx // P).to(torch.int32).view(-1, 1)
+        pos = (idx % P).to(torch.int32)
+        prob = make_problem(e - s, 1, 1, P, num_pages, 1, kv_dtype=kv_dtype)
+        mla_cache_append(prob, rows, pos, bt, cache)
+    return cache

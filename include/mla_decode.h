@@ -125,7 +125,7 @@ typedef struct {
   mla_problem problem;
   int32_t num_streams;      /* row sets: B * Q (one per request and query token), or
                                B * ceil(Q / G) when G draft tokens of a request share one
-                               (dense bf16 cache, Q >= 2, G = min(Q, 48 / H) >= 2) */
+                               (dense bf16 or FP4 cache, Q >= 2, G = min(Q, 48 / H) >= 2) */
   int32_t num_ctas;         /* decode grid size */
   int32_t num_slots;        /* partial-result slots: num_streams + num_ctas - 1 */
   int32_t smem_bytes;       /* dynamic shared memory of the decode kernel */
@@ -135,47 +135,74 @@ typedef struct {
   int64_t ws_status;        /* byte offset of the uint32 status word */
   int64_t workspace_bytes;  /* total workspace size */
   int64_t planned_tiles;    /* tiles implied by seq_lens_host (0 if not given) */
-  int32_t reserved[8];
+  int64_t ws_q_hat;         /* byte offset of bf16 [B*Q][H][576]: the absorbed queries
+                               mla_decode_run writes when it is given W_UK */
+  int32_t split_tokens;     /* as requested from mla_decode_plan (0 = automatic) */
+  int32_t sm_count;         /* as given to mla_decode_plan */
+  int32_t reserved[4];
 } mla_plan;
 
 /*
  * mla_decode_plan -- validate a problem and build the launch plan (host only,
- * no CUDA call).
- *   problem        : the step's shape and options (copied into the plan).
- *   seq_lens_host  : host int32 [batch] context lengths, or NULL.  Used only to
- *                    size the grid: the device kernels re-derive the exact
- *                    work split from the device seq_lens they are given.
- *   sm_count       : streaming multiprocessors to fill (152 on GB300); > 0.
- *   plan_out       : written on success.
+ * no CUDA call).  The plan / run split is the planner + kernel split of the
+ * FlashInfer MLA decode ("GLM-4.7-Flash" record, phantomic12
+ * inference-research: engine-kernel constraint (1), decode kernels
+ * instantiated per page-block size behind a planner).
+ *   problem         : the step's shape and options (copied into the plan).
+ *   seq_lens_host   : host int32 [batch] context lengths, or NULL.  Used only
+ *                     to size the grid: the device kernels re-derive the exact
+ *                     work split from the device seq_lens they are given.
+ *   sm_count        : streaming multiprocessors to fill (152 on GB300); > 0.
+ *   split_tokens    : 0 = automatic: one CTA per SM (at most sm_count CTAs,
+ *                     fewer when there are fewer tiles), the row sets' 64-token
+ *                     tiles spread evenly over them, so a long row set is split
+ *                     over several CTAs and a short one is not.  > 0 (a
+ *                     multiple of 64) = split-KV by length: the grid gets
+ *                     ceil(total tokens / split_tokens) CTAs (needs
+ *                     seq_lens_host), each taking an even share of about
+ *                     split_tokens tokens.
+ *   plan_out        : written on success.
+ *   workspace_bytes : nullable; receives plan_out->workspace_bytes.
  * Returns MLA_OK, MLA_ERR_INVALID_ARGUMENT or MLA_ERR_UNSUPPORTED.
  */
 MLA_API int mla_decode_plan(const mla_problem* problem, const int32_t* seq_lens_host,
-                    int32_t sm_count, mla_plan* plan_out);
+                    int32_t sm_count, int32_t split_tokens, mla_plan* plan_out,
+                    size_t* workspace_bytes);
 
 /*
- * mla_q_absorb -- q_hat[r][h] = [bf16(W_UK[h] q_nope[r][h]) || q_rope[r][h]]
- * (weight absorption of the kv_b_proj key half into the query; fp32
- * accumulation, one rounding to bf16).  r = b * Q + j.
- *   q_nope : bf16 [B*Q][H][192];  q_rope : bf16 [B*Q][H][64]
+ * mla_q_absorb -- q_hat[r][h] = [bf16(W_UK[h] q_nope[r][h]) || q_rope[r][h]],
+ * the weight absorption of the kv_b_proj key half into the query (the cached
+ * latent is shared by all heads and is never decompressed: "GLM-4.7-Flash"
+ * record, the serviceability join on the MLA family and the configuration
+ * clause on kv_a_proj_with_mqa and kv_b_proj).  fp32 accumulation on the
+ * tensor cores, one rounding to bf16.  r = b * Q + j.
+ *   q      : bf16 [B*Q][H][256], each head [q_nope (192) || q_rope (64)]
+ *            (the 256-wide query head is 192 + 64, same record, head_dim
+ *            paragraph)
  *   w_uk   : bf16 [H][512][192]   (k_nope[t] = W_UK[h]^T c_kv[t])
  *   q_hat  : bf16 [B*Q][H][576]   output
+ * Returns MLA_OK, MLA_ERR_INVALID_ARGUMENT, MLA_ERR_MISALIGNED or MLA_ERR_CUDA.
  */
-MLA_API int mla_q_absorb(const mla_plan* plan, const void* q_nope, const void* q_rope,
-                 const void* w_uk, void* q_hat, mla_stream_t stream);
+MLA_API int mla_q_absorb(const mla_plan* plan, const void* q, const void* w_uk, void* q_hat,
+                 mla_stream_t stream);
 
 /*
- * mla_decode_run -- the attention pass over the paged cache, followed by the
- * split-KV merge.  Each row set (request and query token; or request and a
- * group of G draft tokens, see mla_plan.num_streams, whose G * H rows share
- * every staged tile, each row keeping its own causal window) is cut into
- * contiguous 64-token tiles spread evenly over the plan's CTAs; a row set
- * handled by one CTA writes its result directly, one split over several
- * CTAs leaves normalised partials (o_i, lse_i) in the workspace, merged by a
- * second kernel launched right behind the first as a programmatic dependent
- * (its set-up overlaps the attention pass): lse = ln sum_i exp(lse_i),
- * o_lat = sum_i exp(lse_i - lse) o_i.  A row (query token, head) with no
- * visible token gets o_lat = 0 and lse = -inf.
- *   q_hat       : bf16 [B*Q][H][576] absorbed queries
+ * mla_decode_run -- the attention pass over the paged latent cache: scores of
+ * every query row against every visible cached row [c_kv || k_rope], online
+ * softmax and the weighted sum of latent rows ("GLM-4.7-Flash" record: the
+ * MLA decode kernel class; the cache is the shared latent plus the decoupled
+ * RoPE key, 576 values = 1,152 bytes per token and layer in bf16).  Each row
+ * set (request and query token; or request and a group of G draft tokens,
+ * see mla_plan.num_streams, whose G * H rows share every staged tile, each
+ * row keeping its own causal window) is cut into contiguous 64-token tiles
+ * spread over the plan's CTAs.  A row set handled by one CTA gets its final
+ * o_lat and lse here; one split over several CTAs leaves normalised partials
+ * (o_i, lse_i) in the workspace, which mla_combine merges.  A row (query
+ * token, head) with no visible token gets o_lat = 0 and lse = -inf.
+ *   q           : w_uk == NULL: bf16 [B*Q][H][576] absorbed queries q_hat;
+ *                 else bf16 [B*Q][H][256] ([q_nope || q_rope]), absorbed here
+ *                 through w_uk (as mla_q_absorb) into the workspace first.
+ *   w_uk        : NULL, or bf16 [H][512][192].
  *   kv_cache    : MLA_KV_BF16: bf16 [num_pages][P][576];
  *                 MLA_KV_FP8_E4M3_E8M0: uint8 [num_pages][P * 594];
  *                 MLA_KV_FP4_E2M1_E8M0: uint8 [num_pages][P * 324]
@@ -183,53 +210,74 @@ MLA_API int mla_q_absorb(const mla_plan* plan, const void* q_nope, const void* q
  *                 last page are never read
  *   seq_lens    : device int32 [B], 0 <= T_b <= max_pages_per_seq * P
  *   topk_idx    : NULL for dense; sparse: int32 [B*Q][topk_width] logical
- *                 positions of the request, -1 = masked slot
- *   workspace   : device buffer of plan->workspace_bytes, zeroed once before
- *                 its first use (its reserved words must stay zero; the
- *                 status word collects MLA_STATUS_* bits until cleared)
+ *                 positions of the request, -1 = masked slot (vllm API docs,
+ *                 vllm.models.glm5next.common.model, Glm5NextModel.__init__:
+ *                 the top-k buffer is tiled in 128 columns, padded slots
+ *                 stay masked)
+ *   workspace   : device buffer of workspace_bytes >= plan->workspace_bytes
+ *                 (else MLA_ERR_WORKSPACE_TOO_SMALL), zeroed once before its
+ *                 first use (its reserved words must stay zero; the status
+ *                 word collects MLA_STATUS_* bits until cleared)
  *   o_lat       : f32 [B*Q][H][512] output (latent-space attention output)
  *   lse         : f32 [B*Q][H] output (natural-log LSE of the scaled scores)
  * Calls on one workspace must not overlap on the device.
  * Returns MLA_OK, MLA_ERR_INVALID_ARGUMENT, MLA_ERR_MISALIGNED,
- * MLA_ERR_UNSUPPORTED or MLA_ERR_CUDA.
+ * MLA_ERR_UNSUPPORTED, MLA_ERR_WORKSPACE_TOO_SMALL or MLA_ERR_CUDA.
  */
-MLA_API int mla_decode_run(const mla_plan* plan, const void* q_hat, const void* kv_cache,
-                   const int32_t* block_table, const int32_t* seq_lens,
-                   const int32_t* topk_idx, void* workspace, float* o_lat, float* lse,
-                   mla_stream_t stream);
+MLA_API int mla_decode_run(const mla_plan* plan, const void* q, const void* w_uk,
+                   const void* kv_cache, const int32_t* block_table, const int32_t* seq_lens,
+                   const int32_t* topk_idx, void* workspace, size_t workspace_bytes,
+                   float* o_lat, float* lse, mla_stream_t stream);
 
 /*
- * mla_combine -- the split-KV merge as a separate pass over the partials a
- * previous mla_decode_run left in the workspace (same plan, seq_lens and
- * workspace): rewrites o_lat and lse of every row set that was split over
- * several CTAs and leaves the others untouched.  mla_decode_run already
- * launches this merge; the call exists to re-derive or check it.
+ * mla_combine -- completes a step after mla_decode_run (same plan, seq_lens,
+ * workspace, o_lat and lse): merges the partials of every row set that was
+ * split over several CTAs, lse = ln sum_i exp(lse_i), o_lat = sum_i
+ * exp(lse_i - lse) o_i, into o_lat and lse; and, when w_uv is given, applies
+ * the kv_b_proj value half to every row in the same kernel ("GLM-4.7-Flash"
+ * record, configuration clause: v_head_dim 256 read back out of the 512-rank
+ * latent through kv_b_proj): out[r][h] = bf16(W_UV[h]^T o_lat[r][h]).
+ * Launched as a programmatic dependent of the kernel before it on `stream`:
+ * its set-up (and its W_UV loads) overlap the attention pass's tail.
+ *   w_uv  : NULL, or bf16 [H][512][256]
+ *   out   : bf16 [B*Q][H][256] when w_uv is given, else ignored (may be NULL)
+ * After the call o_lat and lse are complete for every row.  Calling it again
+ * with the same workspace gives the same result.
+ * Returns MLA_OK, MLA_ERR_INVALID_ARGUMENT, MLA_ERR_MISALIGNED,
+ * MLA_ERR_WORKSPACE_TOO_SMALL or MLA_ERR_CUDA.
  */
 MLA_API int mla_combine(const mla_plan* plan, const int32_t* seq_lens, const void* workspace,
-                float* o_lat, float* lse, mla_stream_t stream);
+                size_t workspace_bytes, const void* w_uv, float* o_lat, float* lse, void* out,
+                mla_stream_t stream);
 
 /*
  * mla_cache_append -- write each request's newest token row into the paged
  * latent cache (the step before decode).  The row is the kv_a projection's
- * output for that token, [c_kv (512) || k_rope (64)] with the RoPE already
- * applied ("vllm.models.glm5next.common.model", load_weights: the
- * kv_a_proj_with_mqa output, fused into fused_qkv_a_proj).  Row b goes to
- * logical position positions[b] of request b: page
- * block_table[b][pos / P], slot pos % P.
+ * output for that token, [c_kv (512) || k_rope (64)] ("vllm.models.glm5next.
+ * common.model", load_weights: the kv_a_proj_with_mqa output, fused into
+ * fused_qkv_a_proj).  Row b goes to logical position positions[b] of request
+ * b: page block_table[b][pos / P], slot pos % P.
  *   problem     : the cache's shape (batch = number of rows, page_size,
  *                 num_pages, max_pages_per_seq, kv_dtype); other fields as
  *                 for mla_decode_plan
  *   new_rows    : bf16 [batch][576], 16-byte aligned
  *   positions   : device int32 [batch]; -1 appends nothing for that request
  *   block_table : device int32 [batch][max_pages_per_seq]
+ *   rope_theta  : > 0: k_rope (the last 64 values) is rotated here to the
+ *                 token's position before it is stored: pair i = (x[2i],
+ *                 x[2i+1]) turns by the angle pos * rope_theta^(-2i/64), in
+ *                 fp32, rounded once to bf16 ("GLM-4.7-Flash" record,
+ *                 configuration clause: rope_theta 1000000, qk_rope_head_dim
+ *                 64).  0: the row's RoPE key is already rotated and is
+ *                 stored as given.
  *   kv_cache    : written in place.  MLA_KV_BF16: the row is stored as is.
  *                 MLA_KV_FP8_E4M3_E8M0: each 32-value group is quantised on
- *                 the GPU (GLM-4.7-Flash record, phantomic12
- *                 inference-research: FP8 latent, one e8m0 scale per 32 e4m3
- *                 values inlined per token): scale 2^e, e = ceil(log2(amax /
- *                 448)) clamped to [-127, 127]; values round-to-nearest-even
- *                 e4m3 of x / 2^e, saturating at 448; an all-zero group gets
- *                 scale byte 0 and zero codes.
+ *                 the GPU (GLM-4.7-Flash record, engine-kernel constraint
+ *                 (2): FP8 latent, one e8m0 scale per 32 e4m3 values inlined
+ *                 per token): scale 2^e, e = ceil(log2(amax / 448)) clamped to
+ *                 [-127, 127]; values round-to-nearest-even e4m3 of x / 2^e,
+ *                 saturating at 448; an all-zero group gets scale byte 0 and
+ *                 zero codes.
  *                 MLA_KV_FP4_E2M1_E8M0: the same per 16-value group with 6
  *                 for 448: e = ceil(log2(amax / 6)), codes the nearest e2m1
  *                 value of x / 2^e, ties to the even code (the sign of a value
@@ -242,12 +290,14 @@ MLA_API int mla_combine(const mla_plan* plan, const int32_t* seq_lens, const voi
  * MLA_ERR_CUDA.
  */
 MLA_API int mla_cache_append(const mla_problem* problem, const void* new_rows,
-                     const int32_t* positions, const int32_t* block_table, void* kv_cache,
-                     uint32_t* status, mla_stream_t stream);
+                     const int32_t* positions, const int32_t* block_table, float rope_theta,
+                     void* kv_cache, uint32_t* status, mla_stream_t stream);
 
 /*
- * mla_uv_proj -- o[r][h] = bf16(W_UV[h]^T o_lat[r][h]) (the kv_b_proj value
- * half applied after attention, in latent space).
+ * mla_uv_proj -- o[r][h] = bf16(W_UV[h]^T o_lat[r][h]), the kv_b_proj value
+ * half applied after attention, in latent space, as a pass of its own
+ * ("GLM-4.7-Flash" record, configuration clause: v_head_dim 256 from the
+ * 512-rank latent).  mla_combine does the same inside the merge.
  *   o_lat : f32 [rows][num_heads][512];  w_uv : bf16 [num_heads][512][256]
  *   out   : bf16 [rows][num_heads][256]
  * rows >= 0, 1 <= num_heads <= 128.
@@ -256,23 +306,27 @@ MLA_API int mla_uv_proj(const float* o_lat, const void* w_uv, void* out, int32_t
                 int32_t num_heads, mla_stream_t stream);
 
 /*
- * mla_decode_run_static -- mla_decode_run for callers that cannot allocate
- * device memory (the pages describe no such call; this library adds it).
- * Code that runs while a CUDA graph is being captured, or inside a runtime
- * that only hands out the input and output buffers it owns, cannot create
- * the workspace mla_decode_run needs.  This call uses instead one fixed
- * 16 MiB scratch array that the library keeps in device memory (every GPU
- * that loads the library holds it until exit); it calls no allocator.
+ * mla_decode_run_static -- mla_decode_run followed by the merge of
+ * mla_combine (without W_UV), for callers that cannot allocate device memory
+ * (the pages describe no such call; this library adds it).  Code that runs
+ * while a CUDA graph is being captured, or inside a runtime that only hands
+ * out the input and output buffers it owns, cannot create the workspace
+ * mla_decode_run needs.  This call uses instead one fixed 16 MiB scratch
+ * array that the library keeps in device memory (every GPU that loads the
+ * library holds it until exit); it calls no allocator.
  *   plan            : from mla_decode_plan; plan->workspace_bytes must be at
  *                     most 16 MiB, else MLA_ERR_WORKSPACE_TOO_SMALL and
  *                     nothing is launched.
- *   q_hat ... lse   : as for mla_decode_run (caller-owned inputs, outputs).
+ *   q_hat ... lse   : as for mla_decode_run with w_uk == NULL (caller-owned
+ *                     inputs, outputs); o_lat and lse are complete on return.
  *   status          : optional device uint32 that receives this call's
  *                     status bits (MLA_STATUS_*), or NULL.
- * The scratch array is shared by all calls on a device and keeps the last
- * call's contents; each call clears the parts that must start at zero on
- * `stream` before launching.  Calls that overlap on the GPU race on the
- * array: order them on one stream.  The first call on a device looks up
+ * Arguments are checked before anything is queued: a rejected call leaves
+ * the scratch array untouched.  The scratch array is shared by all calls on
+ * a device and keeps the last call's contents; each call clears the parts
+ * that must start at zero on `stream` before launching.  Calls that overlap
+ * on the GPU race on the array: order them on one stream.  The first call on
+ * a device (and the first after that device's context is replaced) looks up
  * the array's address with that device current; make it before any stream
  * capture starts.
  */

@@ -50,7 +50,7 @@ def test_every_entry_point_has_declared_argument_types(m):
 
 
 def test_version_and_strerror(m):
-    assert m.version() == 10000
+    assert m.version() == 20000
     for code in (0, -1, -2, -3, -4, -5, -99):
         assert isinstance(m.strerror(code), str) and m.strerror(code)
 
@@ -154,36 +154,53 @@ def test_plan_rejects_negative_seq_len_and_bad_sm_count(m):
 def test_calls_reject_null_and_misaligned_pointers_before_cuda(m):
     plan = m.mla_decode_plan(_problem(m), None, 152)
     A = 1 << 20    # an aligned fake address: never dereferenced, the call fails first
-    with pytest.raises(m.MlaError) as e:
-        m.mla_decode_run(plan, None, A, A, A, None, A, A, A)
-    assert e.value.code == -1
-    with pytest.raises(m.MlaError) as e:   # dense problem given a top-k list
-        m.mla_decode_run(plan, A, A, A, A, A, A, A, A)
-    assert e.value.code == -1
-    with pytest.raises(m.MlaError) as e:
-        m.mla_decode_run(plan, A + 8, A, A, A, None, A, A, A)
-    assert e.value.code == -3
-    with pytest.raises(m.MlaError) as e:
-        m.mla_combine(plan, A, A, A + 4, A)
-    assert e.value.code == -3
-    with pytest.raises(m.MlaError) as e:   # output pointers are required
-        m.mla_decode_run(plan, A, A, A, A, None, A, None, A)
-    assert e.value.code == -1
-    with pytest.raises(m.MlaError) as e:
-        m.mla_decode_run(plan, A, A, A, A, None, A, A + 8, A)
-    assert e.value.code == -3
-    with pytest.raises(m.MlaError) as e:
-        m.mla_uv_proj(A, A, A, -1, 20)
-    assert e.value.code == -1
-    with pytest.raises(m.MlaError) as e:
-        m.mla_uv_proj(A, A + 2, A, 4, 20)
-    assert e.value.code == -3
-    with pytest.raises(m.MlaError) as e:
-        m.mla_q_absorb(plan, A, None, A, A)
-    assert e.value.code == -1
+    run = m.mla_decode_run
+
+    def code_of(fn, *args, **kw):
+        with pytest.raises(m.MlaError) as e:
+            fn(*args, **kw)
+        return e.value.code
+
+    # (plan, q, w_uk, kv, block_table, seq_lens, topk, workspace, o_lat, lse)
+    assert code_of(run, plan, None, None, A, A, A, None, A, A, A) == -1
+    assert code_of(run, plan, A, None, A, A, A, A, A, A, A) == -1        # dense given a top-k list
+    assert code_of(run, plan, A + 8, None, A, A, A, None, A, A, A) == -3
+    assert code_of(run, plan, A, A + 8, A, A, A, None, A, A, A) == -3    # W_UK misaligned
+    assert code_of(run, plan, A, None, A, A, A, None, A, None, A) == -1  # outputs are required
+    assert code_of(run, plan, A, None, A, A, A, None, A, A + 8, A) == -3
+    # a workspace smaller than the plan's
+    assert code_of(run, plan, A, None, A, A, A, None, A, A, A,
+                   workspace_bytes=plan.workspace_bytes - 1) == -4
+    assert code_of(m.mla_combine, plan, A, A, A + 4, A) == -3
+    assert code_of(m.mla_combine, plan, A, A, A, A, workspace_bytes=16) == -4
+    assert code_of(m.mla_combine, plan, A, A, A, A, w_uv=A, out=None) == -1   # W_UV needs out
+    assert code_of(m.mla_combine, plan, A, A, A, A, w_uv=A + 2, out=A) == -3
+    assert code_of(m.mla_uv_proj, A, A, A, -1, 20) == -1
+    assert code_of(m.mla_uv_proj, A, A + 2, A, 4, 20) == -3
+    assert code_of(m.mla_q_absorb, plan, A, None, A) == -1
+    assert code_of(m.mla_q_absorb, plan, A, A, A + 2) == -3
     sparse = m.mla_decode_plan(_problem(m, topk_width=256), None, 152)
-    with pytest.raises(m.MlaError) as e:   # sparse problem without a top-k list
-        m.mla_decode_run(sparse, A, A, A, A, None, A, A, A)
+    assert code_of(run, sparse, A, None, A, A, A, None, A, A, A) == -1   # sparse without a list
+
+
+def test_plan_split_tokens(m):
+    """split_tokens > 0 sizes the grid by length (about split_tokens tokens
+    per CTA; needs the host lengths; a multiple of 64), 0 is one CTA per SM;
+    the workspace out-parameter matches the plan."""
+    seq = np.array([100_000, 70_000, 1000, 0], dtype=np.int32)
+    tiles = sum((int(t) + 63) // 64 for t in seq)
+    for st in (256, 512, 1024):
+        plan = m.mla_decode_plan(_problem(m, max_pages_per_seq=2000), seq, 152, split_tokens=st)
+        assert plan.num_ctas == -(-tiles // (st // 64)) and plan.split_tokens == st
+        assert plan.num_slots == plan.num_streams + plan.num_ctas - 1
+    auto = m.mla_decode_plan(_problem(m, max_pages_per_seq=2000), seq, 152)
+    assert auto.num_ctas == 152 and auto.split_tokens == 0
+    for bad in (-64, 100):
+        with pytest.raises(m.MlaError) as e:
+            m.mla_decode_plan(_problem(m, max_pages_per_seq=2000), seq, 152, split_tokens=bad)
+        assert e.value.code == -1
+    with pytest.raises(m.MlaError) as e:   # a length split needs the host lengths
+        m.mla_decode_plan(_problem(m), None, 152, split_tokens=512)
     assert e.value.code == -1
 
 
@@ -225,6 +242,10 @@ def test_cache_append_rejects_bad_arguments_before_cuda(m):
     with pytest.raises(m.MlaError) as e:
         m.mla_cache_append(_problem(m, page_size=96), A, A, A, A)
     assert e.value.code == -2
+    for theta in (-1.0, 0.5, float("nan"), float("inf")):
+        with pytest.raises(m.MlaError) as e:
+            m.mla_cache_append(prob, A, A, A, A, rope_theta=theta)
+        assert e.value.code == -1
 
 
 def test_stream_split_matches_kernel_rule():

@@ -7,6 +7,7 @@ import pytest
 
 import oracle as O
 from oracle import cache_append as CA
+from oracle import fp4 as F4
 from oracle import fp8 as F
 import workloads as W
 from mla_testlib import compare, ensure_built, gpu_outputs, make_step, oracle_q_hat, upload_q_hat
@@ -52,9 +53,41 @@ def _problem(batch, w, num_pages, max_pages, fp8):
     return make_problem(batch, 1, w.heads, w.page_size, num_pages, max_pages, kv_dtype=kv)
 
 
+ROPE_THETA = 1.0e6   # GLM-4.7-Flash configuration clause
+
+
+def _assert_same_cache(got, expect, kv, rope):
+    """Byte for byte; with RoPE on, the rotated keys (float64 on both sides,
+    rounded once) may differ where the two float64 rotations straddle a
+    rounding boundary of the stored type: allowed for at most 0.5 % of the
+    RoPE values, each by at most one step of that type."""
+    if not rope:
+        assert np.array_equal(got, expect.view(np.uint8).reshape(got.shape))
+        return
+    if kv == "bf16":
+        g = got.view(np.uint16).reshape(-1, 576).astype(np.int64)
+        e = expect.view(np.uint16).reshape(-1, 576).astype(np.int64)
+        assert np.array_equal(g[:, :512], e[:, :512])
+        d = np.abs(g[:, 512:] - e[:, 512:])
+        assert d.max() <= 1 and (d > 0).mean() <= 5e-3, (int(d.max()), float((d > 0).mean()))
+        return
+    enc = F if kv == "fp8" else F4
+    g = got.reshape(-1, enc.ROW_BYTES)
+    e = expect.view(np.uint8).reshape(-1, enc.ROW_BYTES)
+    diff_rows = np.flatnonzero((g != e).any(axis=1))
+    gv, ev = enc.dequant_rows(g[diff_rows]), enc.dequant_rows(e[diff_rows])
+    assert np.array_equal(gv[:, :512], ev[:, :512])
+    bad = gv[:, 512:] != ev[:, 512:]
+    assert bad.sum() <= 5e-3 * 64 * max(1, g.shape[0] // 1000), int(bad.sum())
+    if bad.any():
+        step = np.abs(ev[:, 512:]).max(axis=1, keepdims=True) / (8.0 if kv == "fp8" else 2.0)
+        assert (np.abs(gv[:, 512:] - ev[:, 512:]) <= step + 1e-30).all()
+
+
+@pytest.mark.parametrize("rope", [False, True])
 @pytest.mark.parametrize("kv,page_size", [("bf16", 64), ("bf16", 128), ("fp8", 64), ("fp8", 128),
                                           ("fp4", 64), ("fp4", 128), ("fp4", 16)])
-def test_append_matches_oracle_bytes(kv, page_size):
+def test_append_matches_oracle_bytes(kv, page_size, rope):
     from head_latent_attention_paged_gb300 import mla_cache_append
     base = W.SMALL_WORKLOADS[{"bf16": "dense_small", "fp8": "fp8_small", "fp4": "fp4_small"}[kv]]
     w = W.with_overrides(base, page_size=page_size, batch=6, seq_lo=1, seq_hi=500)
@@ -68,7 +101,8 @@ def test_append_matches_oracle_bytes(kv, page_size):
     pos[2] = 0
     pos[4] = -1
     cache = batch.cache_bf16 if kv == "bf16" else batch.cache_quant
-    expect = CA.append_rows(cache, rows, pos, batch.block_table, page_size, kv)
+    theta = ROPE_THETA if rope else 0.0
+    expect = CA.append_rows(cache, rows, pos, batch.block_table, page_size, kv, rope_theta=theta)
     dev = torch.device("cuda", 0)
     cache_d = torch.from_numpy(cache.view(np.uint8).copy()).to(dev)
     rows_d = torch.from_numpy(rows.view(np.int16).copy()).to(dev)
@@ -76,11 +110,42 @@ def test_append_matches_oracle_bytes(kv, page_size):
     bt_d = torch.from_numpy(batch.block_table).to(dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     mla_cache_append(_problem(w.batch, w, batch.num_pages, batch.block_table.shape[1], kv),
-                     rows_d, pos_d, bt_d, cache_d, status)
+                     rows_d, pos_d, bt_d, cache_d, status, rope_theta=theta)
     torch.cuda.synchronize()
     got = cache_d.cpu().numpy()
     assert int(status.item()) == 0
-    assert np.array_equal(got, expect.view(np.uint8).reshape(got.shape))
+    _assert_same_cache(got, expect, kv, rope)
+
+
+def test_append_rope_at_long_positions():
+    """Positions up to 131,071 (the long workload's contexts): the rotation
+    angle of pair 0 reaches 2^17 radians; every stored RoPE key stays within
+    one bf16 step of the float64 rotation."""
+    from head_latent_attention_paged_gb300 import mla_cache_append
+    B, P = 64, 128
+    pages_per = 1024
+    rng = np.random.default_rng(31)
+    rows = W.f32_to_bf16_bits(rng.standard_normal((B, 576)).astype(np.float32))
+    pos = rng.integers(0, pages_per * P, size=B).astype(np.int32)
+    pos[:4] = [0, 1, 131071, 65536]
+    # request b's position lands on physical page b; the other entries are
+    # never read
+    bt = np.zeros((B, pages_per), dtype=np.int32)
+    bt[np.arange(B), pos // P] = np.arange(B, dtype=np.int32)
+    num_pages = B
+    w = W.with_overrides(W.SMALL_WORKLOADS["dense_small"], page_size=P)
+    dev = torch.device("cuda", 0)
+    cache_d = torch.zeros((num_pages, P, 576), dtype=torch.int16, device=dev)
+    mla_cache_append(_problem(B, w, num_pages, pages_per, "bf16"),
+                     torch.from_numpy(rows.view(np.int16)).to(dev), torch.from_numpy(pos).to(dev),
+                     torch.from_numpy(bt).to(dev), cache_d, rope_theta=ROPE_THETA)
+    torch.cuda.synchronize()
+    got = cache_d.view(-1, 576)[torch.from_numpy(bt[np.arange(B), pos // P] * P + pos % P).to(dev)]
+    got = got.cpu().numpy().view(np.uint16)
+    want = np.stack([CA.rotate_row(rows[b], int(pos[b]), ROPE_THETA) for b in range(B)])
+    assert np.array_equal(got[:, :512], rows[:, :512])
+    d = np.abs(got[:, 512:].astype(np.int64) - want[:, 512:].astype(np.int64))
+    assert d.max() <= 1 and (d > 0).mean() <= 5e-3
 
 
 def test_append_reports_bad_positions_and_pages():

@@ -283,3 +283,83 @@ def test_full_size_sampled(name, requests, heads):
     assert np.isfinite(o).all() and np.isfinite(lse).all()
     ref = O.decode(batch, requests=requests, heads=heads)
     compare(ref, o, o_lat, lse, heads=heads, label=name)
+
+
+@pytest.mark.parametrize("name,sm_count", [("dense_small", 7), ("long_small", 40),
+                                           ("mtp_small", 11), ("sparse_small", 5), ("tiny", None)])
+def test_fused_merge_and_uv_matches_separate_passes(name, sm_count):
+    """mla_combine with W_UV (merge and up-projection in one kernel) against
+    the merge alone followed by the stand-alone mla_uv_proj: the same o_lat
+    and lse (the two merges sum the partials in different orders: fp32
+    rounding) and outputs within one bf16 step; both against the oracle."""
+    batch = W.generate(W.SMALL_WORKLOADS[name])
+    step = make_step(batch, sm_count=sm_count)
+    step.run()
+    step.uv()
+    o1, lat1, lse1 = gpu_outputs(step)
+    for t in (step.out, step.o_lat, step.lse):
+        t.fill_(float("nan"))
+    step.step()                        # attention pass, then merge + W_UV fused
+    o2, lat2, lse2 = gpu_outputs(step)
+    assert np.allclose(lat2, lat1, rtol=1e-5, atol=1e-6)
+    live = np.isfinite(lse1)
+    assert np.array_equal(live, np.isfinite(lse2)) and np.allclose(lse2[live], lse1[live], atol=1e-5)
+    assert np.abs(o2 - o1).max() <= 2.0 ** -7 * max(1.0, np.abs(o1).max())
+    ref = O.decode(batch)
+    compare(ref, o1, lat1, lse1, label=f"separate/{name}")
+    compare(ref, o2, lat2, lse2, label=f"fused/{name}")
+
+
+@pytest.mark.parametrize("name", ["dense_small", "mtp_small", "tiny"])
+def test_run_with_w_uk_equals_absorbed_query(name):
+    """mla_decode_run given the un-absorbed query and W_UK (absorbed into the
+    workspace) gives the same bits as the run on mla_q_absorb's q_hat."""
+    batch = W.generate(W.SMALL_WORKLOADS[name])
+    step = make_step(batch, sm_count=9)
+    step.step()
+    o1, lat1, lse1 = gpu_outputs(step)
+    for t in (step.out, step.o_lat, step.lse):
+        t.fill_(float("nan"))
+    step.attend(w_uk=True)
+    step.combine(uv=True)
+    o2, lat2, lse2 = gpu_outputs(step)
+    assert np.array_equal(lat1.view(np.uint32), lat2.view(np.uint32))
+    assert np.array_equal(lse1.view(np.uint32), lse2.view(np.uint32))
+    assert np.array_equal(o1, o2)
+
+
+@pytest.mark.parametrize("split_tokens", [256, 512, 1024])
+def test_split_kv_by_length_matches_oracle(split_tokens):
+    """Split-KV with a fixed share of about split_tokens tokens per CTA (the
+    grid grows with the context: more CTAs than SMs run in waves)."""
+    from mla_testlib import make_step as mk
+    batch = W.generate(W.SMALL_WORKLOADS["long_small"])
+    step = mk(batch, split_tokens=split_tokens)
+    tiles = sum((int(t) + 63) // 64 for t in batch.seq_lens)
+    assert step.plan.num_ctas == -(-tiles // (split_tokens // 64))
+    step.step()
+    o, o_lat, lse = gpu_outputs(step)
+    assert step.status() == 0
+    compare(O.decode(batch), o, o_lat, lse, label=f"split_tokens{split_tokens}")
+
+
+@pytest.mark.parametrize("rows,heads", [(2, 4), (130, 20), (64, 32), (17, 1)])
+def test_absorb_tensor_core_matches_float64(rows, heads):
+    """Query absorption on the tensor cores: within one bf16 rounding of the
+    float64 product, ragged row blocks and head counts included; the RoPE
+    part is copied unchanged."""
+    from head_latent_attention_paged_gb300 import make_problem, mla_decode_plan, mla_q_absorb
+    rng = np.random.default_rng(rows * 100 + heads)
+    q = W.f32_to_bf16_bits(rng.standard_normal((rows, heads, 256)).astype(np.float32))
+    w_uk = W.f32_to_bf16_bits((rng.standard_normal((heads, 512, 192)) / np.sqrt(512)).astype(np.float32))
+    plan = mla_decode_plan(make_problem(rows, 1, heads, 64, 10, 4), None, 152)
+    dev = torch.device("cuda", 0)
+    q_d = torch.from_numpy(q.view(np.int16)).to(dev)
+    w_d = torch.from_numpy(w_uk.view(np.int16)).to(dev)
+    out = torch.full((rows, heads, 576), -1, dtype=torch.int16, device=dev)
+    mla_q_absorb(plan, q_d, w_d, out, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    got = O.bf16_to_f64(out.cpu().numpy().view(np.uint16))
+    ref = np.einsum("hdk,rhk->rhd", O.bf16_to_f64(w_uk), O.bf16_to_f64(q[..., :192]))
+    assert (np.abs(got[..., :512] - ref) <= np.abs(ref) * 2.0 ** -7 + 1e-6).all()
+    assert np.array_equal(got[..., 512:], O.bf16_to_f64(q[..., 192:]))

@@ -595,3 +595,72 @@ def test_cache_append_places_rows_and_leaves_the_rest():
         scale = np.repeat(F4.e8m0_to_f64(out4[pg, sl, F4.CODE_BYTES:]), 16)
         assert np.all(np.abs(F4.dequant_rows(out4[pg, sl]) - x) <= scale)
     assert not out4[mask8].any()
+
+
+# ---------------------------------------------------------------------------
+# RoPE on the cached key (append step)
+# ---------------------------------------------------------------------------
+from oracle import rope as R   # noqa: E402
+
+
+def test_rope_golden_hand_worked():
+    """Unit vectors rotated by hand from the closed form (golden fixture)."""
+    g = _golden("rope.json")
+    f = R.inverse_frequencies(g["dim"], g["theta"])
+    assert f[1] == pytest.approx(g["inverse_frequency_pair_1"], rel=1e-15)
+    assert f[16] == pytest.approx(g["inverse_frequency_pair_16"], rel=1e-15)
+    for c in g["cases"]:
+        x = np.zeros(g["dim"])
+        x[c["x_index"]] = 1.0
+        y = R.rope_rotate(x, c["pos"], g["theta"])
+        want = np.zeros(g["dim"])
+        for k, v in c["nonzero_out"].items():
+            want[int(k)] = v
+        np.testing.assert_allclose(y, want, rtol=0, atol=1e-12, err_msg=c["what"])
+
+
+def test_rope_invariants():
+    """Rotation preserves every pair's norm, position 0 is the identity, and
+    q . k depends only on the difference of the two positions."""
+    rng = np.random.default_rng(21)
+    q, k = rng.standard_normal(64), rng.standard_normal(64)
+    assert np.array_equal(R.rope_rotate(k, 0), k)
+    y = R.rope_rotate(k, 123457)
+    np.testing.assert_allclose(y[0::2] ** 2 + y[1::2] ** 2, k[0::2] ** 2 + k[1::2] ** 2, rtol=1e-12)
+    for m, n, d in [(5, 2, 7), (131071, 65536, 1000), (0, 9, 40000)]:
+        a = R.rope_rotate(q, m) @ R.rope_rotate(k, n)
+        b = R.rope_rotate(q, m + d) @ R.rope_rotate(k, n + d)
+        assert a == pytest.approx(b, rel=1e-9, abs=1e-9)
+    # rotating by m then n is rotating by m + n
+    np.testing.assert_allclose(R.rope_rotate(R.rope_rotate(k, 300), 700), R.rope_rotate(k, 1000),
+                               rtol=0, atol=1e-12)
+
+
+def test_rope_matches_complex_multiplication():
+    """Each pair (x0, x1) read as the complex number x0 + i x1 is multiplied
+    by exp(i a): an independent statement of the same rotation."""
+    rng = np.random.default_rng(22)
+    k = rng.standard_normal(64)
+    pos = 4321
+    z = (k[0::2] + 1j * k[1::2]) * np.exp(1j * pos * 1e6 ** (-np.arange(32) * 2 / 64))
+    y = R.rope_rotate(k, pos)
+    np.testing.assert_allclose(y[0::2], z.real, atol=1e-12)
+    np.testing.assert_allclose(y[1::2], z.imag, atol=1e-12)
+
+
+def test_append_rotates_only_the_rope_key():
+    """With rope_theta the appended row's latent is stored unchanged and its
+    RoPE key is the rotated key rounded to bf16; without it, the row as is."""
+    from oracle import cache_append as CA
+    rng = np.random.default_rng(23)
+    rows = W.f32_to_bf16_bits(rng.standard_normal((2, 576)).astype(np.float32))
+    cache = np.zeros((4, 64, 576), dtype=np.uint16)
+    bt = np.array([[2, 0], [1, 3]], dtype=np.int32)
+    out = CA.append_rows(cache, rows, np.array([70, 5]), bt, 64, "bf16", rope_theta=1e6)
+    got0, got1 = out[0, 6], out[1, 5]
+    assert np.array_equal(got0[:512], rows[0, :512]) and np.array_equal(got1[:512], rows[1, :512])
+    for got, row, pos in [(got0, rows[0], 70), (got1, rows[1], 5)]:
+        want = O.round_to_bf16(R.rope_rotate(O.bf16_to_f64(row[512:]), pos))
+        assert np.array_equal(O.bf16_to_f64(got[512:]), want)
+    plain = CA.append_rows(cache, rows, np.array([70, 5]), bt, 64, "bf16")
+    assert np.array_equal(plain[0, 6], rows[0]) and np.array_equal(plain[1, 5], rows[1])
