@@ -88,15 +88,23 @@ struct ModeTraits {
   static constexpr uint32_t kColS = kMulti ? 256 : 288;
   static constexpr uint32_t kColO = kColS + 64;
   static constexpr int kQTmemChunks = kMulti ? kChunks - 1 : kChunks;
-  static constexpr int kThreads = kQuant    ? 32 * (kDequantWarp0 + kDequantWarps)
-                                  : kSparse ? 32 * (kGatherWarp0 + kGatherWarps)
-                                            : 192;
+  // A tcgen05.mma costs its issuing thread a fixed time whatever its shape,
+  // and MMAs from different threads overlap in the tensor pipe: the PV
+  // products go out from a warp of their own, beside the QK issuer (the
+  // quantised-cache kernels, whose dequant warps take the register file,
+  // keep one issuer for both).
+  static constexpr bool kDualIssue = !kQuant;
+  static constexpr int kRoleWarps = kQuant ? kDequantWarp0 + kDequantWarps
+                                   : kSparse ? kGatherWarp0 + kGatherWarps
+                                             : 6;
+  static constexpr int kPvWarp = kRoleWarps;     // the PV issuer (dual-issue kernels)
+  static constexpr int kThreads = 32 * (kRoleWarps + (kDualIssue ? 1 : 0));
   // FP8: two bf16 stages and a two-slot ring of raw tiles beside them.
   // FP4: three bf16 stages, each raw tile landing in the last
   // kRawTileBytes of the stage it is dequantised into.
   static constexpr bool kRawRing = kFp8;
   static constexpr int kNumStages = kRawRing ? kFp8Stages : kStages;   // bf16 tiles in flight
-  static constexpr int kQBatch = kThreads > 192 ? (kMulti ? 2 : 3) : (kMulti ? 4 : 5);   // q_hat chunks per load batch
+  static constexpr int kQBatch = kThreads > 224 ? (kMulti ? 2 : 3) : (kMulti ? 4 : 5);   // q_hat chunks per load batch
   static constexpr int kRawSlots = kRawRing ? kFp8RawSlots : kStages;
   static constexpr int kRawOffset = kTileBytes - kRawTileBytes;
   static_assert(kRawSlots >= 1 && kRawOffset % 16 == 0, "raw tiles need 16-byte aligned slots");
@@ -119,9 +127,9 @@ struct __align__(8) Ctrl {
   uint64_t s_free;           // softmax -> MMA: S read
   uint64_t p_full[2];        // softmax -> MMA: P written (and O^T rescaled)
   uint64_t q_ready;          // softmax -> MMA: a stream's q_hat is in TMEM
-  uint64_t o_done;           // MMA -> softmax: one PV completed
+  uint64_t o_done[2];        // MMA -> softmax: PV(j) completed, on o_done[j % 2]
   uint64_t o_free;           // softmax -> MMA: epilogue has read O^T
-  uint64_t mma_drain;        // MMA warp's final commit
+  uint64_t mma_drain[2];     // the issuers' final commits (QK, PV)
   uint64_t mask[kStages];    // per-stage live-row mask (bit t = row t live)
   uint64_t raw_full[kStages];       // FP8 / FP4: producer -> dequant, bytes landed
   uint64_t raw_empty[kFp8RawSlots]; // FP8: dequant -> producer, raw slot consumed
@@ -548,9 +556,11 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
     mbar_init(&ctrl->s_full, 1);
     mbar_init(&ctrl->s_free, kSoftmaxWarps);
     mbar_init(&ctrl->q_ready, kSoftmaxWarps);
-    mbar_init(&ctrl->o_done, 1);
+    mbar_init(&ctrl->o_done[0], 1);
+    mbar_init(&ctrl->o_done[1], 1);
     mbar_init(&ctrl->o_free, kSoftmaxWarps);
-    mbar_init(&ctrl->mma_drain, 1);
+    mbar_init(&ctrl->mma_drain[0], 1);
+    mbar_init(&ctrl->mma_drain[1], 1);
     ctrl->abort_flag = 0;
     fence_mbar_init();
   }
@@ -783,7 +793,7 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
         }
       }
       __syncwarp();
-    } else if (warp == kMmaWarp) {
+    } else if (warp == kMmaWarp || (MT::kDualIssue && warp == MT::kPvWarp)) {
       // ================================================================= MMA
       const uint32_t idesc_qk = make_idesc_bf16(64, 64, false, false);
       const uint32_t idesc_pv = make_idesc_bf16(128, static_cast<uint32_t>(NP), true, false);
@@ -796,102 +806,179 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
                                             kSmemLayoutSW128);
       // multi-token mode: QK's RoPE steps read A (64 M-rows x 64 values, K-major)
       const uint64_t qr_a0 = make_smem_desc(smem_u32(sQr), 16, 1024, kSmemLayoutSW128);
-      // Single-thread event loop: issue PV(pv) as soon as its P is written
-      // (checked first: it releases a stage), and QK(qk) once its tile, the
-      // stream's q_hat and the S buffer are ready.  QK(qk) is only issued
-      // after PV(qk-2), so the commit that signals S(qk) also covers PV(qk-2)
-      // (the softmax's o_done parity waits rely on it).  Padded head rows of
-      // P hold stale RoPE bytes: they only reach O^T columns that are never
-      // read.
+      // PV(j): O^T += V^T P^T over the staged tile j (4 x 4 MMAs); it releases
+      // the stage and completes o_done[j % 2].
+      auto issue_pv = [&](int st, bool first) {
+        const uint64_t a0 = pv_a0 + static_cast<uint64_t>((st * kTileBytes) >> 4);
+        const uint64_t b0 = pv_b0 + static_cast<uint64_t>((st * kTileBytes) >> 4);
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ss(tmem + MT::kColO + mt * NP, a0 + ((2 * mt * kChunkBytes + kk * 2048) >> 4),
+                        b0 + ((kk * 32) >> 4), idesc_pv, (first && kk == 0) ? 0u : 1u);
+        }
+      };
+      // QK(j): S = q_hat . staged rows (36 MMAs; the RoPE steps from shared
+      // memory in the multi-token mode); completes s_full.
+      auto issue_qk = [&](int st) {
+        const uint64_t b0 = qk_b0 + static_cast<uint64_t>((st * kTileBytes) >> 4);
+#pragma unroll
+        for (int ch = 0; ch < MT::kQTmemChunks; ++ch) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_bf16_ts(tmem + MT::kColS, tmem + MT::kColQ + (ch * 4 + k) * 8,
+                        b0 + ((ch * kChunkBytes + k * 32) >> 4), idesc_qk, (ch | k) ? 1u : 0u);
+        }
+        if constexpr (MT::kMulti) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_bf16_ss(tmem + MT::kColS, qr_a0 + ((k * 32) >> 4),
+                        b0 + (((kChunks - 1) * kChunkBytes + k * 32) >> 4), idesc_qk, 1u);
+        }
+      };
+      // Polls until `ready()` holds; false on abort or after the time limit.
+      auto wait_until = [&](auto ready) -> bool {
+        if (ready()) return true;
+        const uint64_t t0 = globaltimer_ns();
+        while (!ready()) {
+          if (*abort_flag || globaltimer_ns() - t0 > kWaitLimitNs) return false;
+          __nanosleep(20);
+        }
+        return true;
+      };
       bool failed = false;
-      if (lane == 0) {
-        Walker wq, wp;
-        wq.init(prefix, S, g0);
-        wp.init(prefix, S, g0);
-        int32_t qk = 0, pv = 0, seg_q = -1, seg_p = -1;
-        uint64_t t_last = globaltimer_ns();
-        while (pv < ntiles) {
-          bool progressed = false;
-          if (pv < qk) {
-            const int st = pv % kNumStages;
-            const bool first = (pv == 0) || (wp.lt == 0);
-            const int32_t sp = first ? seg_p + 1 : seg_p;
-            const bool ready = mbar_poll(&ctrl->p_full[pv & 1], (pv >> 1) & 1) &&
-                               (!first || sp == 0 || mbar_poll(&ctrl->o_free, (sp - 1) & 1));
-            if (ready) {
-              seg_p = sp;
-              tc_fence_after();
-              const uint64_t a0 = pv_a0 + static_cast<uint64_t>((st * kTileBytes) >> 4);
-              const uint64_t b0 = pv_b0 + static_cast<uint64_t>((st * kTileBytes) >> 4);
-#pragma unroll
-              for (int mt = 0; mt < 4; ++mt) {
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                  mma_bf16_ss(tmem + MT::kColO + mt * NP, a0 + ((2 * mt * kChunkBytes + kk * 2048) >> 4),
-                              b0 + ((kk * 32) >> 4), idesc_pv, (first && kk == 0) ? 0u : 1u);
+      if constexpr (MT::kDualIssue) {
+        // Two issuers: this warp's lane 0 issues QK(qk) once its tile, the
+        // stream's q_hat and the S buffer are ready; the PV warp's lane 0
+        // issues PV(pv) once P(pv) is written (and, opening a segment, once
+        // the previous segment's epilogue has read O^T).  Padded head rows
+        // of P hold stale RoPE bytes: they only reach O^T columns that are
+        // never read.
+        const int role = warp == kMmaWarp ? 0 : 1;
+        if (lane == 0) {
+          Walker wk;
+          wk.init(prefix, S, g0);
+          int32_t seg = -1;
+          for (int32_t t = 0; t < ntiles; ++t) {
+            const int st = t % kNumStages;
+            const bool first = (t == 0) || (wk.lt == 0);
+            const int32_t sg = first ? seg + 1 : seg;
+            if (role == 0) {
+              if (!wait_until([&] {
+                    return (!first || mbar_poll(&ctrl->q_ready, sg & 1)) &&
+                           mbar_poll(&ctrl->full[st], (t / kNumStages) & 1) &&
+                           (t < 1 || mbar_poll(&ctrl->s_free, (t - 1) & 1));
+                  })) {
+                failed = true;
+                break;
               }
-              mma_commit(&ctrl->empty[st]);
-              mma_commit(&ctrl->o_done);
-              wp.next(prefix, S);
-              ++pv;
-              progressed = true;
-            }
-          }
-          if (qk < ntiles && qk - pv < 2) {
-            const int st = qk % kNumStages;
-            const bool first = (qk == 0) || (wq.lt == 0);
-            const int32_t sq = first ? seg_q + 1 : seg_q;
-            const bool ready = (!first || mbar_poll(&ctrl->q_ready, sq & 1)) &&
-                               mbar_poll(&ctrl->full[st], (qk / kNumStages) & 1) &&
-                               (qk < 1 || mbar_poll(&ctrl->s_free, (qk - 1) & 1));
-            if (ready) {
-              seg_q = sq;
               // cp.async fills are generic-proxy writes: order them before
               // the tensor core's async-proxy reads
               if constexpr (kMode == kModeSparseBf16) fence_proxy_async_smem();
               tc_fence_after();
-              const uint64_t b0 = qk_b0 + static_cast<uint64_t>((st * kTileBytes) >> 4);
-#pragma unroll
-              for (int ch = 0; ch < MT::kQTmemChunks; ++ch) {
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                  mma_bf16_ts(tmem + MT::kColS, tmem + MT::kColQ + (ch * 4 + k) * 8,
-                              b0 + ((ch * kChunkBytes + k * 32) >> 4), idesc_qk, (ch | k) ? 1u : 0u);
-              }
-              if constexpr (MT::kMulti) {
-                // RoPE dims: A = the shared-memory rows of q_hat's RoPE part
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                  mma_bf16_ss(tmem + MT::kColS, qr_a0 + ((k * 32) >> 4),
-                              b0 + (((kChunks - 1) * kChunkBytes + k * 32) >> 4), idesc_qk, 1u);
-              }
+              issue_qk(st);
               mma_commit(&ctrl->s_full);
-              wq.next(prefix, S);
-              ++qk;
-              progressed = true;
+            } else {
+              if (!wait_until([&] {
+                    return mbar_poll(&ctrl->p_full[t & 1], (t >> 1) & 1) &&
+                           (!first || sg == 0 || mbar_poll(&ctrl->o_free, (sg - 1) & 1));
+                  })) {
+                failed = true;
+                break;
+              }
+              tc_fence_after();
+              issue_pv(st, first);
+              // o_done before empty: a stage seen free implies its PV seen done
+              mma_commit(&ctrl->o_done[t & 1]);
+              mma_commit(&ctrl->empty[st]);
             }
-          }
-          if (progressed) {
-            t_last = globaltimer_ns();
-          } else if (*abort_flag || globaltimer_ns() - t_last > kWaitLimitNs) {
-            failed = true;
-            break;
-          } else {
-            __nanosleep(20);   // back off: polling shares the SM with the math
+            seg = sg;
+            wk.next(prefix, S);
           }
         }
+        __syncwarp();
+        if (failed && lane == 0) {
+          set_status(p.status, MLA_STATUS_TIMEOUT);
+          ctrl->abort_flag = 1;
+        }
+        // drain: every issued MMA completes before tensor memory is released
+        if (lane == 0) {
+          mma_commit(&ctrl->mma_drain[role]);
+          (void)mbar_wait(&ctrl->mma_drain[role], 0, nullptr, kWaitLimitNs);
+        }
+        __syncwarp();
+      } else {
+        // Single-thread event loop: issue PV(pv) as soon as its P is written
+        // (checked first: it releases a stage), and QK(qk) once its tile, the
+        // stream's q_hat and the S buffer are ready, at most two tiles ahead
+        // of PV.  Padded head rows of P hold stale RoPE bytes: they only reach
+        // O^T columns that are never read.
+        if (lane == 0) {
+          Walker wq, wp;
+          wq.init(prefix, S, g0);
+          wp.init(prefix, S, g0);
+          int32_t qk = 0, pv = 0, seg_q = -1, seg_p = -1;
+          uint64_t t_last = globaltimer_ns();
+          while (pv < ntiles) {
+            bool progressed = false;
+            if (pv < qk) {
+              const int st = pv % kNumStages;
+              const bool first = (pv == 0) || (wp.lt == 0);
+              const int32_t sp = first ? seg_p + 1 : seg_p;
+              const bool ready = mbar_poll(&ctrl->p_full[pv & 1], (pv >> 1) & 1) &&
+                                 (!first || sp == 0 || mbar_poll(&ctrl->o_free, (sp - 1) & 1));
+              if (ready) {
+                seg_p = sp;
+                tc_fence_after();
+                issue_pv(st, first);
+                mma_commit(&ctrl->o_done[pv & 1]);
+                mma_commit(&ctrl->empty[st]);
+                wp.next(prefix, S);
+                ++pv;
+                progressed = true;
+              }
+            }
+            if (qk < ntiles && qk - pv < 2) {
+              const int st = qk % kNumStages;
+              const bool first = (qk == 0) || (wq.lt == 0);
+              const int32_t sq = first ? seg_q + 1 : seg_q;
+              const bool ready = (!first || mbar_poll(&ctrl->q_ready, sq & 1)) &&
+                                 mbar_poll(&ctrl->full[st], (qk / kNumStages) & 1) &&
+                                 (qk < 1 || mbar_poll(&ctrl->s_free, (qk - 1) & 1));
+              if (ready) {
+                seg_q = sq;
+                if constexpr (kMode == kModeSparseBf16) fence_proxy_async_smem();
+                tc_fence_after();
+                issue_qk(st);
+                mma_commit(&ctrl->s_full);
+                wq.next(prefix, S);
+                ++qk;
+                progressed = true;
+              }
+            }
+            if (progressed) {
+              t_last = globaltimer_ns();
+            } else if (*abort_flag || globaltimer_ns() - t_last > kWaitLimitNs) {
+              failed = true;
+              break;
+            } else {
+              __nanosleep(20);   // back off: polling shares the SM with the math
+            }
+          }
+        }
+        __syncwarp();
+        if (failed && lane == 0) {
+          set_status(p.status, MLA_STATUS_TIMEOUT);
+          ctrl->abort_flag = 1;
+        }
+        // drain: every issued MMA completes before tensor memory is released
+        if (lane == 0) {
+          mma_commit(&ctrl->mma_drain[0]);
+          (void)mbar_wait(&ctrl->mma_drain[0], 0, nullptr, kWaitLimitNs);
+        }
+        __syncwarp();
       }
-      __syncwarp();
-      if (failed && lane == 0) {
-        set_status(p.status, MLA_STATUS_TIMEOUT);
-        ctrl->abort_flag = 1;
-      }
-      // drain: every issued MMA completes before tensor memory is released
-      if (lane == 0) {
-        mma_commit(&ctrl->mma_drain);
-        (void)mbar_wait(&ctrl->mma_drain, 0, nullptr, kWaitLimitNs);
-      }
-      __syncwarp();
     } else if (MT::kQuant && warp >= kDequantWarp0) {
       // ============================================================ dequant
       // Thread t of the 192 owns row t % 64 and groups t / 64 + 3k: a warp
@@ -1103,6 +1190,14 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
       Walker wk;
       wk.init(prefix, S, g0);
       bool failed = false;
+      // PV(j) has completed: o_done[j % 2] has finished its phase j / 2.  At
+      // tile i every PV up to i - kNumStages has completed and been signalled
+      // (tile i's stage was released by that PV's commit to empty, issued
+      // after its commit to o_done), so each barrier has at most one phase
+      // in flight when it is waited on here.
+      auto pv_done = [&](int32_t j) -> bool {
+        return warp_wait(&ctrl->o_done[j & 1], (j >> 1) & 1, abort_flag);
+      };
       // q_hat / o_lat rows of row set s and how many there are
       auto first_row = [&](int32_t s) -> int64_t {
         const StreamGeom gm = stream_geom(s, p.q_len, G);
@@ -1255,9 +1350,7 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
         if (named_bar_or(1, 128, !ok)) { failed = true; break; }
         if (!first && ctrl->rescale_tile[pb] == i) {
           // every earlier PV has completed before O^T is rescaled in place
-          // (PV(i-2) is covered by the commit that signalled S(i), so the
-          // barrier is at most one phase behind this wait)
-          ok = warp_wait(&ctrl->o_done, (i - 1) & 1, abort_flag);
+          ok = (i < 2 || pv_done(i - 2)) && pv_done(i - 1);
           failed = !ok;
           if (ok) {
             tc_fence_after();
@@ -1277,13 +1370,11 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
             }
           }
         }
-        // A segment ends here: its epilogue waits for PV(i), one phase after
-        // PV(i-1).  A parity wait must never run more than one phase ahead of
-        // the barrier, so PV(i-1) is awaited first, while PV(i) cannot have
-        // been issued yet (P(i) is not announced).  PV(i-2) is complete: the
-        // commit that signalled S(i) covers it.
-        if (last && i >= 1 && !failed) {
-          ok = warp_wait(&ctrl->o_done, (i - 1) & 1, abort_flag);
+        // A segment ends here: its epilogue waits for PV(i), which shares
+        // o_done[i % 2] with PV(i-2); PV(i-2) is awaited first (PV(i-4) is
+        // complete: the stage tile i fills was released by PV(i-3)).
+        if (last && i >= 2 && !failed) {
+          ok = pv_done(i - 2);
           if (!ok) failed = true;
         }
         fence_proxy_async_smem();
@@ -1292,7 +1383,7 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
         if (lane == 0) mbar_arrive(&ctrl->p_full[pb]);
         if (last) {
           // ---- segment epilogue
-          ok = !failed && warp_wait(&ctrl->o_done, i & 1, abort_flag);
+          ok = !failed && pv_done(i);   // PVs complete in order: all of them
           const int32_t s = wk.s;
           const int32_t c_first = tile_owner(tile_cost_pos(cprefix[s], 0), ucost, p.num_ctas);
           const int32_t c_last = tile_owner(
