@@ -82,12 +82,23 @@ struct ModeTraits {
   // the first softmax warp whose TMEM lanes hold rows: row r of a row set is
   // M-row 16 * kRowWarp0 + r of the QK accumulator
   static constexpr int kRowWarp0 = kMulti ? 1 : 2;
+  // Split QK (dense one-token bf16 kernel): two issuers each take half of
+  // QK's K range into an S accumulator of their own (S = S_a + S_b, summed
+  // by the softmax): latent chunks 0-3 into S_a, 4-7 and the RoPE chunk into
+  // S_b.  (The sparse kernel's gather warps leave no registers for the
+  // second S in the softmax.)
+  static constexpr bool kSplitQK = kMode == kModeDenseBf16;
+  // q_hat's RoPE part is a shared-memory A operand (multi-token and split-QK
+  // kernels), so that TMEM holds the extra accumulator.
+  static constexpr bool kQRopeSmem = kMulti || kSplitQK;
   // TMEM columns: q_hat (all 576 values, or the 512 latent ones when the
-  // RoPE part is a shared-memory operand), S (64), O^T (4 x heads_pad)
+  // RoPE part is a shared-memory operand), S (64; two of them when QK is
+  // split), O^T (4 x heads_pad)
   static constexpr uint32_t kColQ = 0;
-  static constexpr uint32_t kColS = kMulti ? 256 : 288;
-  static constexpr uint32_t kColO = kColS + 64;
-  static constexpr int kQTmemChunks = kMulti ? kChunks - 1 : kChunks;
+  static constexpr uint32_t kColS = kQRopeSmem ? 256 : 288;
+  static constexpr uint32_t kColS2 = kColS + 64;
+  static constexpr uint32_t kColO = kColS + (kSplitQK ? 128 : 64);
+  static constexpr int kQTmemChunks = kQRopeSmem ? kChunks - 1 : kChunks;
   // A tcgen05.mma costs its issuing thread a fixed time whatever its shape,
   // and MMAs from different threads overlap in the tensor pipe: the PV
   // products go out from a warp of their own, beside the QK issuer (the
@@ -98,13 +109,14 @@ struct ModeTraits {
                                    : kSparse ? kGatherWarp0 + kGatherWarps
                                              : 6;
   static constexpr int kPvWarp = kRoleWarps;     // the PV issuer (dual-issue kernels)
-  static constexpr int kThreads = 32 * (kRoleWarps + (kDualIssue ? 1 : 0));
+  static constexpr int kQk2Warp = kRoleWarps + 1; // the second QK issuer (split-QK kernels)
+  static constexpr int kThreads = 32 * (kRoleWarps + (kDualIssue ? 1 : 0) + (kSplitQK ? 1 : 0));
   // FP8: two bf16 stages and a two-slot ring of raw tiles beside them.
   // FP4: three bf16 stages, each raw tile landing in the last
   // kRawTileBytes of the stage it is dequantised into.
   static constexpr bool kRawRing = kFp8;
   static constexpr int kNumStages = kRawRing ? kFp8Stages : kStages;   // bf16 tiles in flight
-  static constexpr int kQBatch = kThreads > 224 ? (kMulti ? 2 : 3) : (kMulti ? 4 : 5);   // q_hat chunks per load batch
+  static constexpr int kQBatch = kThreads > 256 ? (kQRopeSmem ? 2 : 3) : (kQRopeSmem ? 4 : 5);   // q_hat chunks per load batch
   static constexpr int kRawSlots = kRawRing ? kFp8RawSlots : kStages;
   static constexpr int kRawOffset = kTileBytes - kRawTileBytes;
   static_assert(kRawSlots >= 1 && kRawOffset % 16 == 0, "raw tiles need 16-byte aligned slots");
@@ -117,7 +129,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 // layout, 576 bf16 = 288 columns; 256 in the multi-token mode), S (64 token
 // columns), O^T (4 x padded rows).
 constexpr uint32_t kTmemCols = 512;
-constexpr int kQRopeBytes = 64 * 128;   // multi-token mode: RoPE part of q_hat, 64 M-rows x 128 B
+constexpr int kQRopeBytes = 64 * 128;   // RoPE part of q_hat as a shared-memory operand, 64 M-rows x 128 B
 
 // Control block placed after the data buffers in shared memory.
 struct __align__(8) Ctrl {
@@ -129,7 +141,7 @@ struct __align__(8) Ctrl {
   uint64_t q_ready;          // softmax -> MMA: a stream's q_hat is in TMEM
   uint64_t o_done[2];        // MMA -> softmax: PV(j) completed, on o_done[j % 2]
   uint64_t o_free;           // softmax -> MMA: epilogue has read O^T
-  uint64_t mma_drain[2];     // the issuers' final commits (QK, PV)
+  uint64_t mma_drain[3];     // the issuers' final commits (QK, PV, second QK)
   uint64_t mask[kStages];    // per-stage live-row mask (bit t = row t live)
   uint64_t raw_full[kStages];       // FP8 / FP4: producer -> dequant, bytes landed
   uint64_t raw_empty[kFp8RawSlots]; // FP8: dequant -> producer, raw slot consumed
@@ -278,19 +290,19 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 // M=64 layout, which lives in TMEM lane (m/16)*32 + m%16: lanes 0-15 of
 // softmax warp kRowWarp0 + r/16.  Heads of a one-token row set sit in rows
 // 32 + h (warps 2 and 3 only, so warps 0 and 1 leave their SM sub-partitions
-// to the producer and MMA warps) with all 576 values in TMEM, packed two per
-// column.  A multi-token row set (up to 48 rows) starts at M-row 16 (warps
-// 1-3); its 512 latent values go to TMEM and its 64 RoPE values to a
-// shared-memory operand (row m at m * 128 bytes, 16-byte units swizzled by
-// m % 8), where M-rows without a row are written as zeros.  Every softmax
+// to the producer and MMA warps); a multi-token row set (up to 48 rows)
+// starts at M-row 16 (warps 1-3).  The 512 latent values go to TMEM, packed
+// two per column, and the 64 RoPE values either to TMEM as well or
+// (kRopeSmem) to a shared-memory operand (row m at m * 128 bytes, 16-byte
+// units swizzled by m % 8), where M-rows without a row are written as
+// zeros.  Every softmax
 // warp calls this; absent rows get zeros.  TMEM loads go in batches of
 // kBatch chunks of 64 values to keep many in flight (fewer in the kernels
 // whose thread count leaves fewer registers per thread).
-template <bool kMulti, int kBatch>
+template <int kRowWarp0, bool kRopeSmem, int kBatch>
 __device__ __forceinline__ void load_q(const uint16_t* q_rows, int nrows, uint32_t taddr_lane,
                                        uint8_t* q_rope, int lane, int w) {
-  constexpr int kRowWarp0 = kMulti ? 1 : 2;
-  constexpr int kTmemChunks = kMulti ? kChunks - 1 : kChunks;
+  constexpr int kTmemChunks = kRopeSmem ? kChunks - 1 : kChunks;
   const int r = (w - kRowWarp0) * 16 + (lane & 15);
   const bool live = w >= kRowWarp0 && lane < 16 && r < nrows;
   const uint4* src = reinterpret_cast<const uint4*>(q_rows + static_cast<int64_t>(live ? r : 0) * kDqk);
@@ -320,7 +332,7 @@ __device__ __forceinline__ void load_q(const uint16_t* q_rows, int nrows, uint32
       }
     }
   }
-  if constexpr (kMulti) {
+  if constexpr (kRopeSmem) {
     if (lane < 16) {
       const int m = 16 * w + lane;
       uint8_t* row = q_rope + m * 128;
@@ -497,7 +509,9 @@ DecodeLayout decode_layout(int heads, int heads_pad, int num_streams, int mode) 
   // the multi-token mode's RoPE query operand (1024-byte aligned after the stages)
   L.off_qrope = L.off_raw;
   L.off_ctrl = L.off_raw + (ring ? kFp8RawSlots * kFp8TileBytes : 0) +
-               (mode == kModeDenseMulti || mode == kModeDenseFp4Multi ? kQRopeBytes : 0);
+               (mode == kModeDenseMulti || mode == kModeDenseFp4Multi || mode == kModeDenseBf16
+                    ? kQRopeBytes
+                    : 0);
   L.total = L.off_ctrl + static_cast<int>(sizeof(Ctrl)) + 2 * (num_streams + 1) * 4;
   return L;
 }
@@ -553,14 +567,13 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
       mbar_init(&ctrl->p_full[i], kSoftmaxWarps);
       ctrl->rescale_tile[i] = -1;
     }
-    mbar_init(&ctrl->s_full, 1);
+    mbar_init(&ctrl->s_full, MT::kSplitQK ? 2 : 1);   // one commit per QK issuer
     mbar_init(&ctrl->s_free, kSoftmaxWarps);
     mbar_init(&ctrl->q_ready, kSoftmaxWarps);
     mbar_init(&ctrl->o_done[0], 1);
     mbar_init(&ctrl->o_done[1], 1);
     mbar_init(&ctrl->o_free, kSoftmaxWarps);
-    mbar_init(&ctrl->mma_drain[0], 1);
-    mbar_init(&ctrl->mma_drain[1], 1);
+    for (int d = 0; d < 3; ++d) mbar_init(&ctrl->mma_drain[d], 1);
     ctrl->abort_flag = 0;
     fence_mbar_init();
   }
@@ -793,7 +806,8 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
         }
       }
       __syncwarp();
-    } else if (warp == kMmaWarp || (MT::kDualIssue && warp == MT::kPvWarp)) {
+    } else if (warp == kMmaWarp || (MT::kDualIssue && warp == MT::kPvWarp) ||
+               (MT::kSplitQK && warp == MT::kQk2Warp)) {
       // ================================================================= MMA
       const uint32_t idesc_qk = make_idesc_bf16(64, 64, false, false);
       const uint32_t idesc_pv = make_idesc_bf16(128, static_cast<uint32_t>(NP), true, false);
@@ -819,22 +833,34 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
                         b0 + ((kk * 32) >> 4), idesc_pv, (first && kk == 0) ? 0u : 1u);
         }
       };
-      // QK(j): S = q_hat . staged rows (36 MMAs; the RoPE steps from shared
-      // memory in the multi-token mode); completes s_full.
-      auto issue_qk = [&](int st) {
+      // QK(j) over chunks [c0, c1) of the staged rows into the S accumulator
+      // at column `col` (A = q_hat from TMEM, 4 MMAs per chunk), then, with
+      // `rope`, the RoPE chunk with A = q_hat's RoPE part in shared memory.
+      auto issue_qk = [&](int st, int c0, int c1, uint32_t col, bool rope) {
         const uint64_t b0 = qk_b0 + static_cast<uint64_t>((st * kTileBytes) >> 4);
-#pragma unroll
-        for (int ch = 0; ch < MT::kQTmemChunks; ++ch) {
+        for (int ch = c0; ch < c1; ++ch) {
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_bf16_ts(tmem + MT::kColS, tmem + MT::kColQ + (ch * 4 + k) * 8,
-                        b0 + ((ch * kChunkBytes + k * 32) >> 4), idesc_qk, (ch | k) ? 1u : 0u);
+            mma_bf16_ts(tmem + col, tmem + MT::kColQ + (ch * 4 + k) * 8,
+                        b0 + ((ch * kChunkBytes + k * 32) >> 4), idesc_qk,
+                        (ch > c0 || k > 0) ? 1u : 0u);
         }
-        if constexpr (MT::kMulti) {
+        if (rope) {
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_bf16_ss(tmem + MT::kColS, qr_a0 + ((k * 32) >> 4),
-                        b0 + (((kChunks - 1) * kChunkBytes + k * 32) >> 4), idesc_qk, 1u);
+            mma_bf16_ss(tmem + col, qr_a0 + ((k * 32) >> 4),
+                        b0 + (((kChunks - 1) * kChunkBytes + k * 32) >> 4), idesc_qk,
+                        (c1 > c0 || k > 0) ? 1u : 0u);
+        }
+      };
+      // This issuer's share of QK: all of it (S), or half of its K range
+      // (chunks 0-3 into S_a; 4-7 and the RoPE chunk into S_b).
+      auto issue_my_qk = [&](int st, bool second) {
+        if constexpr (MT::kSplitQK) {
+          if (!second) issue_qk(st, 0, 4, MT::kColS, false);
+          else issue_qk(st, 4, kChunks - 1, MT::kColS2, true);
+        } else {
+          issue_qk(st, 0, MT::kQTmemChunks, MT::kColS, MT::kQRopeSmem);
         }
       };
       // Polls until `ready()` holds; false on abort or after the time limit.
@@ -855,7 +881,8 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
         // the previous segment's epilogue has read O^T).  Padded head rows
         // of P hold stale RoPE bytes: they only reach O^T columns that are
         // never read.
-        const int role = warp == kMmaWarp ? 0 : 1;
+        // role 0: QK (or its first half), 1: PV, 2: the second half of QK
+        const int role = warp == kMmaWarp ? 0 : (warp == MT::kPvWarp ? 1 : 2);
         if (lane == 0) {
           Walker wk;
           wk.init(prefix, S, g0);
@@ -864,7 +891,7 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
             const int st = t % kNumStages;
             const bool first = (t == 0) || (wk.lt == 0);
             const int32_t sg = first ? seg + 1 : seg;
-            if (role == 0) {
+            if (role != 1) {
               if (!wait_until([&] {
                     return (!first || mbar_poll(&ctrl->q_ready, sg & 1)) &&
                            mbar_poll(&ctrl->full[st], (t / kNumStages) & 1) &&
@@ -877,7 +904,7 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
               // the tensor core's async-proxy reads
               if constexpr (kMode == kModeSparseBf16) fence_proxy_async_smem();
               tc_fence_after();
-              issue_qk(st);
+              issue_my_qk(st, role == 2);
               mma_commit(&ctrl->s_full);
             } else {
               if (!wait_until([&] {
@@ -950,7 +977,7 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
                 seg_q = sq;
                 if constexpr (kMode == kModeSparseBf16) fence_proxy_async_smem();
                 tc_fence_after();
-                issue_qk(st);
+                issue_my_qk(st, false);
                 mma_commit(&ctrl->s_full);
                 wq.next(prefix, S);
                 ++qk;
@@ -1205,9 +1232,10 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
       };
       auto rows_of = [&](int32_t s) -> int { return stream_geom(s, p.q_len, G).nq * H; };
       // the first stream's queries
-      load_q<MT::kMulti, MT::kQBatch>(p.q_hat + first_row(wk.s) * kDqk, rows_of(wk.s),
-                                      tmem + lane_base, sQr, lane, w);
-      if constexpr (MT::kMulti) fence_proxy_async_smem();   // RoPE rows -> tensor-core reads
+      load_q<MT::kRowWarp0, MT::kQRopeSmem, MT::kQBatch>(p.q_hat + first_row(wk.s) * kDqk,
+                                                         rows_of(wk.s), tmem + lane_base, sQr,
+                                                         lane, w);
+      if constexpr (MT::kQRopeSmem) fence_proxy_async_smem();   // RoPE rows -> tensor-core reads
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctrl->q_ready);
@@ -1252,10 +1280,23 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
             tmem_ld32(tmem + lane_base + MT::kColS, r);
 #pragma unroll
             for (int t = 0; t < 32; ++t) y[t] = __uint_as_float(r[t]);
+            if constexpr (MT::kSplitQK) {   // S = S_a + S_b
+              tmem_ld32(tmem + lane_base + MT::kColS2, r);
+#pragma unroll
+              for (int t = 0; t < 32; ++t) y[t] += __uint_as_float(r[t]);
+            }
+            float z[32];
             tmem_ld32(tmem + lane_base + MT::kColS + 32, r);
 #pragma unroll
+            for (int t = 0; t < 32; ++t) z[t] = __uint_as_float(r[t]);
+            if constexpr (MT::kSplitQK) {
+              tmem_ld32(tmem + lane_base + MT::kColS2 + 32, r);
+#pragma unroll
+              for (int t = 0; t < 32; ++t) z[t] += __uint_as_float(r[t]);
+            }
+#pragma unroll
             for (int t = 0; t < 32; ++t) {
-              const float hi_col = __shfl_xor_sync(0xffffffffu, __uint_as_float(r[t]), 16);
+              const float hi_col = __shfl_xor_sync(0xffffffffu, z[t], 16);
               if (half) y[t] = hi_col;   // lane l+16 <- columns 32..63 of lane l
             }
           }
@@ -1268,9 +1309,10 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
             // completed, so nothing reads the old queries any more.
             Walker nx = wk;
             nx.next(prefix, S);
-            load_q<MT::kMulti, MT::kQBatch>(p.q_hat + first_row(nx.s) * kDqk, rows_of(nx.s),
-                                            tmem + lane_base, sQr, lane, w);
-            if constexpr (MT::kMulti) fence_proxy_async_smem();
+            load_q<MT::kRowWarp0, MT::kQRopeSmem, MT::kQBatch>(p.q_hat + first_row(nx.s) * kDqk,
+                                                               rows_of(nx.s), tmem + lane_base,
+                                                               sQr, lane, w);
+            if constexpr (MT::kQRopeSmem) fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctrl->q_ready);
