@@ -302,7 +302,8 @@ int launch_attention(const mla_plan& plan, const void* q_hat, const void* kv_cac
   std::memset(&kv_map, 0, sizeof(kv_map));   // FP8 / FP4 caches are read with bulk copies
   if (mode != kModeDenseFp8 && mode != kModeDenseFp4 && mode != kModeDenseFp4Multi &&
       !make_map_bf16(&kv_map, kv_cache, kDqk, static_cast<uint64_t>(pr.num_pages) * pr.page_size,
-                     kDqk * 2, kChunkElems, pr.page_size < kTile ? pr.page_size : kTile))
+                     kDqk * 2, kChunkElems,
+                     mode == kModeSparseBf16 ? 1 : (pr.page_size < kTile ? pr.page_size : kTile)))
     return MLA_ERR_CUDA;
   DecodeParams p;
   p.q_hat = static_cast<const uint16_t*>(q_hat);

@@ -8,8 +8,8 @@
 //
 //   producer warp : stages the 64 cached rows (576 bf16 each) in shared
 //                   memory once -- TMA tiles for dense pages (for sparse
-//                   top-k rows, four gather warps issue 16-byte cp.async
-//                   copies, 16 rows each) -- as nine
+//                   top-k rows, four gather warps issue TMA gather4 loads,
+//                   16 rows each) -- as nine
 //                   [64 rows x 128 B] chunks in the 128-byte swizzle layout,
 //                   three tiles in flight.  FP8 / FP4 caches: one bulk copy
 //                   of the tile's quantised rows (594 or 324 bytes), FP8
@@ -556,9 +556,9 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0) {
     for (int i = 0; i < kNumStages; ++i) {
-      // sparse: every gather lane's cp.async arrival plus one arrive per warp
+      // sparse: one byte-count arrival per gather warp
       mbar_init(&ctrl->full[i],
-                MT::kQuant ? kDequantWarps : (MT::kSparse ? kGatherWarps * 33 : 1));
+                MT::kQuant ? kDequantWarps : (MT::kSparse ? kGatherWarps : 1));
       mbar_init(&ctrl->empty[i], 1);
     }
     for (int i = 0; i < kStages; ++i) mbar_init(&ctrl->raw_full[i], 1);
@@ -581,7 +581,7 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
     tmem_alloc(&ctrl->tmem_base, kTmemCols);
     tmem_relinquish();
   }
-  if (warp == kProducerWarp && lane == 0 && MT::kDenseBf16) prefetch_tmap(&kv_map);
+  if (warp == kProducerWarp && lane == 0 && (MT::kDenseBf16 || MT::kSparse)) prefetch_tmap(&kv_map);
   // tiles and cost per stream (stream lengths from the device seq_lens)
   for (int s = tid; s < S; s += kThreads) {
     const StreamGeom gm = stream_geom(s, p.q_len, G);
@@ -900,9 +900,6 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
                 failed = true;
                 break;
               }
-              // cp.async fills are generic-proxy writes: order them before
-              // the tensor core's async-proxy reads
-              if constexpr (kMode == kModeSparseBf16) fence_proxy_async_smem();
               tc_fence_after();
               issue_my_qk(st, role == 2);
               mma_commit(&ctrl->s_full);
@@ -975,7 +972,6 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
                                  (qk < 1 || mbar_poll(&ctrl->s_free, (qk - 1) & 1));
               if (ready) {
                 seg_q = sq;
-                if constexpr (kMode == kModeSparseBf16) fence_proxy_async_smem();
                 tc_fence_after();
                 issue_my_qk(st, false);
                 mma_commit(&ctrl->s_full);
@@ -1126,15 +1122,17 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
     } else if (MT::kSparse && warp >= kGatherWarp0) {
       // ============================================================= gather
       // Gather warp gw stages tile rows [16 gw, 16 gw + 16): lanes 0..15
-      // resolve one top-k slot each (index -> page -> cache row), then the
-      // warp copies the 16 rows as 16-byte cp.async pieces, zero-filling dead
-      // rows, and writes its 16 bits of the tile's live-row mask.
+      // resolve one top-k slot each (index -> page -> physical cache row, or
+      // -1 for a dead slot), then lanes 0..35 issue one TMA gather4 each:
+      // rows 16 gw + 4 g .. + 3 of 64-dim chunk c (t = 9 g + c) into the
+      // swizzled tile, a dead row reading the map's zero fill.  The warp's
+      // 16 bits of the live-row mask go out with its byte count.
       const int gw = warp - kGatherWarp0;
       const uint64_t pol = l2_policy_evict_first();
-      (void)pol;
       Walker wk;
       wk.init(prefix, S, g0);
       bool failed = false;
+      int32_t issued = 0;
       for (int32_t i = 0; i < ntiles; ++i) {
         const int stage = i % kNumStages;
         const uint32_t reuse_parity = ((i / kNumStages) - 1) & 1;
@@ -1157,33 +1155,31 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
           }
         }
         if (bad && lane < 16) set_status(p.status, bad);
-        const uint8_t* src =
-            v ? p.kv + (static_cast<int64_t>(page) * p.page_size + idx % p.page_size) * (kDqk * 2)
-              : p.kv;
+        const int32_t prow = v ? page * p.page_size + idx % p.page_size : -1;
         const uint32_t live = __ballot_sync(0xffffffffu, v) & 0xFFFFu;
         if (i >= kNumStages && !warp_wait(&ctrl->empty[stage], reuse_parity, abort_flag)) {
           failed = true;
           break;
         }
-        for (int rr = 0; rr < kGatherRows; ++rr) {
-          const int r = kGatherRows * gw + rr;
-          const uint8_t* s_row = reinterpret_cast<const uint8_t*>(
-              __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(src), rr));
-          const uint32_t nbytes = ((live >> rr) & 1u) ? 16u : 0u;
-#pragma unroll
-          for (int q = 0; q < 3; ++q) {
-            const int piece = lane + 32 * q;   // 16-byte piece of the row, 0..71
-            if (piece < kDqk * 2 / 16) {
-              const int ch = piece >> 3, w16 = piece & 7;
-              cp_async_16(dst + ch * kChunkBytes + r * 128 + ((w16 ^ (r & 7)) << 4),
-                          s_row + piece * 16, nbytes);
-            }
-          }
-        }
-        if (lane == 0)
+        if (lane == 0) {
           reinterpret_cast<volatile uint16_t*>(&ctrl->mask[stage])[gw] = static_cast<uint16_t>(live);
-        cp_async_mbar_arrive(&ctrl->full[stage]);
-        if (lane == 0) mbar_arrive(&ctrl->full[stage]);
+          mbar_arrive_expect_tx(&ctrl->full[stage], kGatherRows * kChunks * 128);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int round = 0; round < 2; ++round) {
+          const int t = lane + 32 * round;              // 36 gathers: 4 row groups x 9 chunks
+          const int tt = t < 4 * kChunks ? t : 0;
+          const int g = tt / kChunks, ch = tt - g * kChunks;
+          const int32_t y0 = __shfl_sync(0xffffffffu, prow, 4 * g);
+          const int32_t y1 = __shfl_sync(0xffffffffu, prow, 4 * g + 1);
+          const int32_t y2 = __shfl_sync(0xffffffffu, prow, 4 * g + 2);
+          const int32_t y3 = __shfl_sync(0xffffffffu, prow, 4 * g + 3);
+          if (t < 4 * kChunks)
+            tma_gather4(dst + ch * kChunkBytes + (kGatherRows * gw + 4 * g) * 128, &kv_map,
+                        &ctrl->full[stage], ch * kChunkElems, y0, y1, y2, y3, pol);
+        }
+        ++issued;
         wk.next(prefix, S);
       }
       if (failed && lane == 0) {
@@ -1191,7 +1187,9 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
         ctrl->abort_flag = 1;
       }
       // every copy this warp issued has landed before the CTA exits
-      asm volatile("cp.async.wait_all;" ::: "memory");
+      if (lane == 0)
+        for (int32_t i = max(0, issued - kNumStages); i < issued; ++i)
+          (void)mbar_wait(&ctrl->full[i % kNumStages], (i / kNumStages) & 1, nullptr, kWaitLimitNs);
       __syncwarp();
     } else if (warp == kProducerWarp) {
       // sparse mode: the gather warps stage the tiles
