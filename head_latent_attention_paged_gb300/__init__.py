@@ -38,7 +38,7 @@ MLA_TILE_TOKENS = 64
 EXPORTED = (
     "mla_decode_plan", "mla_q_absorb", "mla_decode_run", "mla_combine", "mla_uv_proj",
     "mla_get_status", "mla_clear_status", "mla_strerror", "mla_version",
-    "mla_decode_run_static", "mla_cache_append", "mla_selftest_bounded_wait",
+    "mla_decode_run_static", "mla_cache_append", "mla_selftest_bounded_wait", "mla_decode_step",
 )
 
 
@@ -91,6 +91,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.mla_q_absorb.argtypes = [P(MlaPlan), vp, vp, vp, vp]
     lib.mla_decode_run.argtypes = [P(MlaPlan), vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
     lib.mla_combine.argtypes = [P(MlaPlan), vp, vp, sz, vp, vp, vp, vp, vp]
+    lib.mla_decode_step.argtypes = [P(MlaPlan), vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp, vp, vp]
     lib.mla_decode_run_static.argtypes = [P(MlaPlan), vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.mla_uv_proj.argtypes = [vp, vp, vp, i32, i32, vp]
     lib.mla_cache_append.argtypes = [P(MlaProblem), vp, vp, vp, ctypes.c_float, vp, vp, vp]
@@ -207,6 +208,16 @@ def mla_combine(plan: MlaPlan, seq_lens, workspace, o_lat, lse, w_uv=None, out=N
         ctypes.byref(plan), _ptr(seq_lens), _ptr(workspace),
         _nbytes(workspace, workspace_bytes, plan), _ptr(w_uv), _ptr(o_lat), _ptr(lse), _ptr(out),
         _stream(stream)))
+
+
+def mla_decode_step(plan: MlaPlan, q, w_uk, kv_cache, block_table, seq_lens, topk_idx, workspace,
+                    w_uv, o_lat, lse, out, stream=None, workspace_bytes=None) -> None:
+    """A whole decode step (attention, merge, W_UV) in one cooperative launch
+    where the plan's grid fits the SMs, else mla_decode_run + mla_combine."""
+    _check("mla_decode_step", load().mla_decode_step(
+        ctypes.byref(plan), _ptr(q), _ptr(w_uk), _ptr(kv_cache), _ptr(block_table),
+        _ptr(seq_lens), _ptr(topk_idx), _ptr(workspace), _nbytes(workspace, workspace_bytes, plan),
+        _ptr(w_uv), _ptr(o_lat), _ptr(lse), _ptr(out), _stream(stream)))
 
 
 def mla_cache_append(problem: MlaProblem, new_rows, positions, block_table, kv_cache,

@@ -338,16 +338,18 @@ int launch_merge(const mla_plan& plan, const int32_t* seq_lens, const uint8_t* w
   if (plan.num_streams == 0) return MLA_OK;
   CombineParams cp;
   fill_combine_params(plan, ws, seq_lens, o_lat, lse, &cp);
-  cudaError_t err;
-  if (w_uv == nullptr) {
-    err = launch_combine(cp, st);
-  } else {
+  // the merge over all SMs (one block per row of a row set), then, with
+  // W_UV, the up-projection per head: each a programmatic dependent of the
+  // launch before it
+  cudaError_t err = launch_combine(cp, st);
+  if (err == cudaSuccess && w_uv != nullptr) {
     const mla_problem& pr = plan.problem;
     CUtensorMap w_map;
     if (!make_map_bf16(&w_map, w_uv, kDv, static_cast<uint64_t>(pr.num_heads) * kDc, kDv * 2, 64,
                        64))
       return MLA_ERR_CUDA;
-    err = launch_combine_uv(&w_map, cp, static_cast<uint16_t*>(out), plan.sm_count, st);
+    err = launch_uv_proj_tma(&w_map, o_lat, static_cast<uint16_t*>(out),
+                             pr.batch * pr.q_len, pr.num_heads, plan.sm_count, st);
   }
   return err == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
@@ -468,6 +470,29 @@ int mla_combine(const mla_plan* plan, const int32_t* seq_lens, const void* works
                       out, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int mla_decode_step(const mla_plan* plan, const void* q, const void* w_uk, const void* kv_cache,
+                    const int32_t* block_table, const int32_t* seq_lens, const int32_t* topk_idx,
+                    void* workspace, size_t workspace_bytes, const void* w_uv, float* o_lat,
+                    float* lse, void* out, mla_stream_t stream) {
+  int rc = check_run_args(plan, q, w_uk, kv_cache, block_table, seq_lens, topk_idx, workspace,
+                          workspace_bytes, o_lat, lse);
+  if (rc != MLA_OK) return rc;
+  if (!w_uv || !out) return MLA_ERR_INVALID_ARGUMENT;
+  if (!aligned16(w_uv) || !aligned16(out)) return MLA_ERR_MISALIGNED;
+  if (plan->num_streams == 0) return MLA_OK;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const void* q_hat = q;
+  if (w_uk != nullptr) {
+    q_hat = ws + plan->ws_q_hat;
+    rc = absorb(*plan, q, w_uk, ws + plan->ws_q_hat, st);
+    if (rc != MLA_OK) return rc;
+  }
+  rc = launch_attention(*plan, q_hat, kv_cache, block_table, seq_lens, topk_idx, ws, o_lat, lse, st);
+  if (rc != MLA_OK) return rc;
+  return launch_merge(*plan, seq_lens, ws, w_uv, o_lat, lse, out, st);
+}
+
 int mla_uv_proj(const float* o_lat, const void* w_uv, void* out, int32_t rows, int32_t num_heads,
                 mla_stream_t stream) {
   if (!o_lat || !w_uv || !out || rows < 0 || num_heads < 1 || num_heads > 128)
@@ -477,8 +502,12 @@ int mla_uv_proj(const float* o_lat, const void* w_uv, void* out, int32_t rows, i
   CUtensorMap w_map;
   if (!make_map_bf16(&w_map, w_uv, kDv, static_cast<uint64_t>(num_heads) * kDc, kDv * 2, 64, 64))
     return MLA_ERR_CUDA;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return MLA_ERR_CUDA;
   const cudaError_t err = launch_uv_proj_tma(&w_map, o_lat, static_cast<uint16_t*>(out), rows,
-                                             num_heads, reinterpret_cast<cudaStream_t>(stream));
+                                             num_heads, sms, reinterpret_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 

@@ -2,7 +2,6 @@
 //   * mla_combine_kernel : LSE merge of the split-KV partials of each row set
 //                          (one block per row: a head, or a draft token x head);
 //   * mla_uv_kernel      : o = W_UV[h]^T o_lat (tcgen05, per head);
-//   * mla_combine_uv_kernel : the merge and W_UV in one pass (tcgen05, per head);
 //   * mla_absorb_kernel  : q_hat = [W_UK[h] q_nope || q_rope] (query absorption,
 //                          tcgen05).
 #include <cuda_bf16.h>
@@ -143,42 +142,50 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {
 }
 
 // ----------------------------------------------------------------------------
-// UV projection: per (head h, 128 output dims, 32 rows):
+// UV projection: per (head h, 128 output dims, N rows):
 //   D^T[n, r] = sum_k W_UV[h][k][n] * o_lat[r][h][k]
-// A = W_UV[h] slice (MN-major, TMA), B = o_lat rows converted to bf16
-// (K-major, written by the threads), D in TMEM (128 lanes x 32 columns).
-// 32 rows per CTA keeps the grid wide (dense batch 64 x 20 heads: 80 CTAs)
-// and each thread issues all its o_lat loads (16 x 32 B) before using them.
+// A = W_UV slice (MN-major, TMA), B = o_lat rows converted to bf16 (K-major,
+// written by the threads, all loads issued before any is used), D in TMEM.
+// A tcgen05.mma costs its issuing thread a fixed time, so the 32 K-steps go
+// out from four threads (warps 0-3, 128 latent dims each) into four
+// accumulators that the epilogue sums.  N (16, 32 or 64 rows) is the smallest
+// row block whose grid fits the SMs, where one does.
 // ----------------------------------------------------------------------------
 namespace {
-constexpr int kUvRows = 32;                 // N of the MMA
 constexpr int kUvA = 8 * 2 * kChunkBytes;   // 8 K-blocks x 2 n-chunks x 8 KB = 128 KB
-constexpr int kUvB = 8 * kUvRows * 128;     // 8 K-blocks x 32 rows x 128 B = 32 KB
-constexpr int kUvItems = kUvRows * 64 / 128;   // 16-byte B pieces per thread
-constexpr int kUvSmem = kUvA + kUvB + 1024 + 64;
+template <int N>
+struct Uv {
+  static constexpr int kThreads = N == 64 ? 256 : 128;
+  static constexpr int kB = 8 * N * 128;                     // 8 K-blocks x N rows x 128 B
+  static constexpr int kPieces = N * 64 / kThreads;          // 16-byte B pieces per thread
+  static constexpr int kTmemCols = 4 * N < 32 ? 32 : 4 * N;  // four accumulators
+  static constexpr int kSmem = kUvA + kB + 1024 + 64;
+};
 }  // namespace
 
-__global__ void __launch_bounds__(128, 1)
+template <int N>
+__global__ void __launch_bounds__(Uv<N>::kThreads, 1)
     mla_uv_kernel(const __grid_constant__ CUtensorMap w_map, const float* o_lat,
                   uint16_t* __restrict__ out, int rows, int heads) {
+  constexpr int kThreads = Uv<N>::kThreads;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + kUvA;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kUvA + kUvB);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kUvA + Uv<N>::kB);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.x;
   const int mt = blockIdx.y;          // output dims [128 mt, 128 mt + 128)
-  const int r0 = blockIdx.z * kUvRows;
+  const int r0 = blockIdx.z * N;
   if (tid == 0) {
     mbar_init(&bars[0], 1);
-    mbar_init(&bars[1], 1);
+    mbar_init(&bars[1], 4);           // one commit per issuer
     fence_mbar_init();
   }
   if (warp == 0) {
-    tmem_alloc(tslot, 32);
+    tmem_alloc(tslot, Uv<N>::kTmemCols);
     tmem_relinquish();
   }
   __syncthreads();
@@ -196,12 +203,12 @@ __global__ void __launch_bounds__(128, 1)
   // could be scheduled ahead of this wait.
   asm volatile("griddepcontrol.wait;" ::: "memory");
   // B: o_lat[r0 + r][h][k] -> bf16, [kb][r][128 B] swizzled.  Item e of
-  // this thread is piece (tid + 128 e): row (tid + 128 e) / 64, 8 consecutive
-  // k; all loads are issued before any is used.
-  float4 va[kUvItems], vb[kUvItems];
+  // this thread is piece (tid + kThreads e): row (tid + kThreads e) / 64,
+  // 8 consecutive k.
+  float4 va[Uv<N>::kPieces], vb[Uv<N>::kPieces];
 #pragma unroll
-  for (int e = 0; e < kUvItems; ++e) {
-    const int idx = tid + 128 * e;
+  for (int e = 0; e < Uv<N>::kPieces; ++e) {
+    const int idx = tid + kThreads * e;
     const int r = idx >> 6, piece = idx & 63;
     if (r0 + r < rows) {
       const float4* src = reinterpret_cast<const float4*>(
@@ -213,14 +220,14 @@ __global__ void __launch_bounds__(128, 1)
     }
   }
 #pragma unroll
-  for (int e = 0; e < kUvItems; ++e) {
-    const int idx = tid + 128 * e;
+  for (int e = 0; e < Uv<N>::kPieces; ++e) {
+    const int idx = tid + kThreads * e;
     const int r = idx >> 6, piece = idx & 63;
     const int kb = piece >> 3, w16 = piece & 7;
     const float4 a = va[e], b = vb[e];
     __nv_bfloat162 x0 = __floats2bfloat162_rn(a.x, a.y), x1 = __floats2bfloat162_rn(a.z, a.w);
     __nv_bfloat162 x2 = __floats2bfloat162_rn(b.x, b.y), x3 = __floats2bfloat162_rn(b.z, b.w);
-    *reinterpret_cast<uint4*>(sB + kb * (kUvRows * 128) + r * 128 + ((w16 ^ (r & 7)) << 4)) =
+    *reinterpret_cast<uint4*>(sB + kb * (N * 128) + r * 128 + ((w16 ^ (r & 7)) << 4)) =
         make_uint4(*reinterpret_cast<uint32_t*>(&x0), *reinterpret_cast<uint32_t*>(&x1),
                    *reinterpret_cast<uint32_t*>(&x2), *reinterpret_cast<uint32_t*>(&x3));
   }
@@ -229,427 +236,91 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  bool ok = true;
-  if (warp == 0) {
-    ok = mbar_wait(&bars[0], 0, nullptr, kWaitLimitNs);
-    ok = __all_sync(0xffffffffu, ok);
-    tc_fence_after();
-    if (ok && lane == 0) {
-      const uint32_t idesc = make_idesc_bf16(128, kUvRows, true, false);
-      const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
-      for (int kb = 0; kb < 8; ++kb) {
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t ad = make_smem_desc(a_base + kb * 2 * kChunkBytes + kk * 2048, kChunkBytes,
-                                             1024, kSmemLayoutSW128);
-          const uint64_t bd = make_smem_desc(b_base + kb * (kUvRows * 128) + kk * 32, 16, 1024,
-                                             kSmemLayoutSW128);
-          mma_bf16_ss(tmem, ad, bd, idesc, (kb | kk) ? 1u : 0u);
-        }
-      }
-      mma_commit(&bars[1]);
-    }
-    __syncwarp();
-  }
-  __syncthreads();
-  if (mbar_wait(&bars[1], 0, nullptr, kWaitLimitNs)) {
-    tc_fence_after();
-    const int n = mt * 128 + warp * 32 + lane;
-    for (int cb = 0; cb < kUvRows; cb += 16) {
-      uint32_t v[16];
-      tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + cb, v);
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const int r = r0 + cb + e;
-        if (r < rows) out[(static_cast<int64_t>(r) * heads + h) * kDv + n] = float_to_bf16_bits(__uint_as_float(v[e]));
-      }
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 0) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 32);
-  }
-}
-
-cudaError_t launch_uv_proj_tma(const CUtensorMap* w_map, const float* o_lat, uint16_t* out,
-                               int rows, int heads, cudaStream_t stream) {
-  if (rows == 0) return cudaSuccess;
-  cudaError_t err = set_smem_attr_once(reinterpret_cast<const void*>(mla_uv_kernel), 1, kUvSmem);
-  if (err != cudaSuccess) return err;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(heads, kDv / 128, (rows + kUvRows - 1) / kUvRows);
-  cfg.blockDim = dim3(128);
-  cfg.dynamicSmemBytes = kUvSmem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  err = cudaLaunchKernelEx(&cfg, mla_uv_kernel, *w_map, o_lat, out, rows, heads);
-  if (err != cudaSuccess) return err;
-  return cudaGetLastError();
-}
-
-// ----------------------------------------------------------------------------
-// merge + W_UV, per (head h, 128 output dims, N rows r = b * Q + j):
-//   o_lat[r][h] = sum_i exp(lse_i - lse) o_i,  lse = ln sum_i exp(lse_i)
-//                 over the partials of a split row set (else as the decode
-//                 wrote it),
-//   out[r][h]   = bf16(W_UV[h]^T o_lat[r][h])      (tcgen05, as mla_uv_kernel).
-// A programmatic dependent of the decode kernel: the W_UV slice (128 KB) and
-// the work split are fetched and derived before the dependency wait.  The
-// two blocks of a (head, row block), one per half of the output dims, form a
-// cluster and share the merge: each block of the pair merges half of the
-// live rows and writes their bf16 B rows into both blocks' shared memory.
-// 8N threads; a thread owns one 16-byte piece of up to four rows and merges
-// them online (running max, rescaled sum), a few segments at a time with all
-// of those loads in flight together; it also writes the merged o_lat and lse
-// of split rows.  N (16, 32 or 64 rows) is chosen so that the grid fits the
-// SMs where it can.
-// ----------------------------------------------------------------------------
-namespace {
-template <int N>
-struct Cuv {
-  static constexpr int kThreads = 8 * N;
-  static constexpr int kB = 8 * N * 128;                  // 8 K-blocks x N rows x 128 B
-  static constexpr int kTmemCols = N < 32 ? 32 : N;
-  static constexpr int kSmem = kUvA + kB + 1024 + 64 + 3 * N * 4;
-};
-}  // namespace
-
-template <int N>
-__global__ void __launch_bounds__(Cuv<N>::kThreads, 1)
-    mla_combine_uv_kernel(const __grid_constant__ CUtensorMap w_map, const CombineParams p,
-                          uint16_t* __restrict__ out) {
-  constexpr int kThreads = Cuv<N>::kThreads;
-  constexpr int kRowStep = N / 8;                         // rows between a thread's pieces
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* sA = smem;
-  uint8_t* sB = smem + kUvA;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kUvA + Cuv<N>::kB);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2);
-  int32_t* r_slot0 = reinterpret_cast<int32_t*>(smem + kUvA + Cuv<N>::kB + 64);   // or -1
-  int32_t* r_nseg = r_slot0 + N;
-  __shared__ int64_t red64[2][kThreads / 32];
-  __shared__ int32_t s_cost[64];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int h = blockIdx.x;
-  const int mt = blockIdx.y;          // output dims [128 mt, 128 mt + 128)
-  const int r0 = blockIdx.z * N;
-  const int rows = p.batch * p.q_len;
-  const int H = p.heads, Q = p.q_len, G = p.group;
-  const int ng = (Q + G - 1) / G;     // row sets per request
-  const int S = p.num_streams;
-  const int max_tokens = p.max_pages * p.page_size;
-  if (tid == 0) {
-    mbar_init(&bars[0], 1);
-    mbar_init(&bars[1], 1);
-    fence_mbar_init();
-  }
-  if (warp == 0) {
-    tmem_alloc(tslot, Cuv<N>::kTmemCols);
-    tmem_relinquish();
-  }
-  __syncthreads();
-  if (tid == 0) {
-    prefetch_tmap(&w_map);
-    mbar_arrive_expect_tx(&bars[0], kUvA);
-    for (int kb = 0; kb < 8; ++kb)
-      for (int nc = 0; nc < 2; ++nc)
-        tma_load_2d(sA + (kb * 2 + nc) * kChunkBytes, &w_map, &bars[0], mt * 128 + nc * 64,
-                    h * kDc + kb * 64, 0ull);
-  }
-  // Row sets of this block's rows: s(r) = b * ng + j / G, a contiguous range
-  // [s_lo, s_hi] of at most N.  The decode split the cost prefix over row
-  // sets evenly across its CTAs; derive where each of ours fell.
-  const int r_last = min(r0 + N, rows) - 1;
-  const int s_lo = (r0 / Q) * ng + (r0 % Q) / G;
-  const int s_hi = (r_last / Q) * ng + (r_last % Q) / G;
-  auto cost_of = [&](int t) -> int64_t {
-    const StreamGeom gt = stream_geom(t, Q, G);
-    const int32_t len = stream_len(p.seq_lens[gt.b], Q, gt.j0 + gt.nq - 1, p.causal, p.topk_width,
-                                   max_tokens);
-    return stream_cost((len + kTile - 1) / kTile);
-  };
-  int64_t before = 0, tot = 0;
-  for (int t = tid; t < S; t += kThreads) {
-    const int64_t n = cost_of(t);
-    tot += n;
-    if (t < s_lo) before += n;
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    before += __shfl_xor_sync(0xffffffffu, before, o);
-    tot += __shfl_xor_sync(0xffffffffu, tot, o);
-  }
-  if (lane == 0) { red64[0][warp] = before; red64[1][warp] = tot; }
-  if (tid < 64) s_cost[tid] = (s_lo + tid <= s_hi) ? static_cast<int32_t>(cost_of(s_lo + tid)) : 0;
-  __syncthreads();
-  before = tot = 0;
-#pragma unroll
-  for (int w = 0; w < kThreads / 32; ++w) { before += red64[0][w]; tot += red64[1][w]; }
-  if (warp == 0) {
-    // each lane takes two row sets (s_lo + lane, s_lo + 32 + lane): exclusive
-    // cost prefix, then its CTA range; then each row its row set's segments
-    int64_t v0 = s_cost[lane], v1 = s_cost[32 + lane];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int64_t n0 = __shfl_up_sync(0xffffffffu, v0, o);
-      const int64_t n1 = __shfl_up_sync(0xffffffffu, v1, o);
-      if (lane >= o) { v0 += n0; v1 += n1; }
-    }
-    const int64_t half = __shfl_sync(0xffffffffu, v0, 31);
-    int32_t c0[2], c1[2];
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int32_t cost = s_cost[32 * u + lane];
-      const int64_t cst = before + (u ? half + v1 : v0) - cost;   // cost before the row set
-      const int32_t nt = cost > 0 ? (cost - kStreamCost) / kTileCost : 0;
-      c0[u] = c1[u] = -1;
-      if (nt > 0) {
-        c0[u] = tile_owner(tile_cost_pos(cst, 0), tot, p.num_ctas);
-        c1[u] = tile_owner(tile_cost_pos(cst, nt - 1), tot, p.num_ctas);
-      }
-    }
-    for (int rb = 0; rb < N; rb += 32) {   // every lane takes part in the shuffles
-      const int rr = rb + lane;
-      const int r = min(r0 + rr, r_last);
-      const int s = (r / Q) * ng + (r % Q) / G;
-      const int k = s - s_lo;
-      int32_t slot0 = -1, nseg = 0;
-      // the row set's range is held by lane k % 32 in slot k / 32
-      const int32_t a0 = __shfl_sync(0xffffffffu, c0[0], k & 31);
-      const int32_t e0 = __shfl_sync(0xffffffffu, c1[0], k & 31);
-      const int32_t a1 = __shfl_sync(0xffffffffu, c0[1], k & 31);
-      const int32_t e1 = __shfl_sync(0xffffffffu, c1[1], k & 31);
-      const int32_t a = k < 32 ? a0 : a1, e = k < 32 ? e0 : e1;
-      if (r0 + rr <= r_last && a >= 0 && a != e) {
-        slot0 = s + a;
-        nseg = e - a + 1;
-      }
-      if (rr < N) {
-        r_slot0[rr] = slot0;
-        r_nseg[rr] = nseg;
-      }
-    }
-  }
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  __syncthreads();
-  // B: o_lat rows (merged where split) -> bf16, [kb][r][128 B] swizzled, in
-  // this block's and its partner's shared memory (rows past the end: zeros).
-  // The pair splits the block's live rows: cluster rank mt merges rows
-  // [lo, hi).  Thread t takes the 16-byte pieces t % 64 of rows lo + t / 64 +
-  // (N/8) e (at most four), and walks their partials kSU segments at a time,
-  // all of those loads in flight together.
-  constexpr int kSlots = N / 8;                 // rows taken side by side
-  constexpr int kPB = 4;                        // rows per thread, at most
-  constexpr int kSU = N == 64 ? 2 : 4;          // segments per round (register budget)
-  const int piece = tid & 63;
-  const int slot = tid >> 6;
-  const uint32_t peer = static_cast<uint32_t>(mt ^ 1);
-  const int nvalid = min(N, rows - r0);
-  const int lo = mt == 0 ? 0 : (nvalid + 1) / 2;
-  const int hi = mt == 0 ? (nvalid + 1) / 2 : nvalid;
-  cluster_sync();   // the partner block has started: its shared memory may be written
-  // rows past the live ones are zeros in both blocks' B (written by rank 0)
-  if (mt == 0) {
-    for (int idx = tid; idx < (N - nvalid) * 64; idx += kThreads) {
-      const int rr = nvalid + idx / 64, pc = idx & 63;
-      uint8_t* dstp = sB + (pc >> 3) * (N * 128) + rr * 128 + (((pc & 7) ^ (rr & 7)) << 4);
-      *reinterpret_cast<uint4*>(dstp) = make_uint4(0, 0, 0, 0);
-      st_shared_cluster_v4(mapa_shared(smem_u32(dstp), peer), make_uint4(0, 0, 0, 0));
-    }
-  }
-  {
-    int maxseg = 1;
-#pragma unroll
-    for (int e = 0; e < kPB; ++e) {
-      const int rr = lo + slot + kSlots * e;
-      if (rr < hi) maxseg = max(maxseg, r_nseg[rr]);
-    }
-    float m[kPB], sum[kPB];
-    float4 acc_a[kPB], acc_b[kPB];
-#pragma unroll
-    for (int e = 0; e < kPB; ++e) {
-      m[e] = -INFINITY;
-      sum[e] = 0.f;
-      acc_a[e] = acc_b[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    for (int seg0 = 0; seg0 < maxseg; seg0 += kSU) {
-      float lv[kPB][kSU];
-      float4 xa[kPB][kSU], xb[kPB][kSU];
-#pragma unroll
-      for (int e = 0; e < kPB; ++e) {
-        const int rr = lo + slot + kSlots * e;
-        const int r = r0 + rr;
-        const int nseg = rr < hi ? r_nseg[rr] : -1;
-        const int64_t in_set = static_cast<int64_t>(r % Q % G) * H + h;
-#pragma unroll
-        for (int u = 0; u < kSU; ++u) {
-          const int seg = seg0 + u;
-          lv[e][u] = -INFINITY;
-          xa[e][u] = xb[e][u] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (nseg == 0 && seg == 0) {   // a row set one CTA held: its o_lat is final
-            const float4* src = reinterpret_cast<const float4*>(
-                p.o_lat + (static_cast<int64_t>(r) * H + h) * kDc + piece * 8);
-            xa[e][u] = src[0];
-            xb[e][u] = src[1];
-            lv[e][u] = 0.f;
-          } else if (seg < nseg) {
-            const int64_t sl = static_cast<int64_t>(r_slot0[rr]) + seg;
-            lv[e][u] = p.part_lse[sl * p.rows + in_set];
-            const float4* src = reinterpret_cast<const float4*>(
-                p.part_o + (sl * p.rows + in_set) * kDc + piece * 8);
-            xa[e][u] = src[0];
-            xb[e][u] = src[1];
-          }
-        }
-      }
-#pragma unroll
-      for (int e = 0; e < kPB; ++e) {
-#pragma unroll
-        for (int u = 0; u < kSU; ++u) {
-          const float li = lv[e][u];
-          if (li == -INFINITY) continue;      // nothing from this segment
-          if (li > m[e]) {
-            const float sc = (m[e] == -INFINITY) ? 0.f : __expf(m[e] - li);
-            sum[e] *= sc;
-            acc_a[e].x *= sc; acc_a[e].y *= sc; acc_a[e].z *= sc; acc_a[e].w *= sc;
-            acc_b[e].x *= sc; acc_b[e].y *= sc; acc_b[e].z *= sc; acc_b[e].w *= sc;
-            m[e] = li;
-          }
-          const float wgt = __expf(li - m[e]);
-          const float4 x = xa[e][u], y = xb[e][u];
-          sum[e] += wgt;
-          acc_a[e].x = fmaf(wgt, x.x, acc_a[e].x); acc_a[e].y = fmaf(wgt, x.y, acc_a[e].y);
-          acc_a[e].z = fmaf(wgt, x.z, acc_a[e].z); acc_a[e].w = fmaf(wgt, x.w, acc_a[e].w);
-          acc_b[e].x = fmaf(wgt, y.x, acc_b[e].x); acc_b[e].y = fmaf(wgt, y.y, acc_b[e].y);
-          acc_b[e].z = fmaf(wgt, y.z, acc_b[e].z); acc_b[e].w = fmaf(wgt, y.w, acc_b[e].w);
-        }
-      }
-    }
-#pragma unroll
-    for (int e = 0; e < kPB; ++e) {
-      const int rr = lo + slot + kSlots * e;
-      if (rr >= hi) continue;
-      const int r = r0 + rr;
-      float4 a = acc_a[e], b = acc_b[e];
-      if (r_nseg[rr] > 0) {
-        // a split row: normalise; store its merged o_lat and lse
-        const float inv = sum[e] > 0.f ? 1.f / sum[e] : 0.f;
-        a.x *= inv; a.y *= inv; a.z *= inv; a.w *= inv;
-        b.x *= inv; b.y *= inv; b.z *= inv; b.w *= inv;
-        const int64_t orow = static_cast<int64_t>(r) * H + h;
-        float4* dst = reinterpret_cast<float4*>(p.o_lat + orow * kDc + piece * 8);
-        dst[0] = a;
-        dst[1] = b;
-        if (piece == 0) p.lse[orow] = (m[e] == -INFINITY) ? -INFINITY : m[e] + __logf(sum[e]);
-      }
-      const int kb = piece >> 3, w16 = piece & 7;
-      __nv_bfloat162 x0 = __floats2bfloat162_rn(a.x, a.y), x1 = __floats2bfloat162_rn(a.z, a.w);
-      __nv_bfloat162 x2 = __floats2bfloat162_rn(b.x, b.y), x3 = __floats2bfloat162_rn(b.z, b.w);
-      const uint4 v = make_uint4(*reinterpret_cast<uint32_t*>(&x0), *reinterpret_cast<uint32_t*>(&x1),
-                                 *reinterpret_cast<uint32_t*>(&x2), *reinterpret_cast<uint32_t*>(&x3));
-      uint8_t* dstp = sB + kb * (N * 128) + rr * 128 + ((w16 ^ (rr & 7)) << 4);
-      *reinterpret_cast<uint4*>(dstp) = v;
-      st_shared_cluster_v4(mapa_shared(smem_u32(dstp), peer), v);
-    }
-  }
-  // both blocks' B rows are complete and visible to the tensor core
-  fence_proxy_async_cluster();
-  tc_fence_before();
-  cluster_sync();
-  tc_fence_after();
-  const uint32_t tmem = *tslot;
-  if (warp == 0) {
-    bool ok = mbar_wait(&bars[0], 0, nullptr, kWaitLimitNs);
-    ok = __all_sync(0xffffffffu, ok);
-    tc_fence_after();
+  if (warp < 4) {
+    // issuer w: K-blocks 2w, 2w + 1 (latent dims [128 w, 128 w + 128)) into
+    // the accumulator at column N w
     if (lane == 0) {
+      const bool ok = mbar_wait(&bars[0], 0, nullptr, kWaitLimitNs);
+      tc_fence_after();
       if (ok) {
         const uint32_t idesc = make_idesc_bf16(128, N, true, false);
         const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
-        for (int kb = 0; kb < 8; ++kb) {
+        for (int kb = 2 * warp; kb < 2 * warp + 2; ++kb) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t ad = make_smem_desc(a_base + kb * 2 * kChunkBytes + kk * 2048,
                                                kChunkBytes, 1024, kSmemLayoutSW128);
             const uint64_t bd = make_smem_desc(b_base + kb * (N * 128) + kk * 32, 16, 1024,
                                                kSmemLayoutSW128);
-            mma_bf16_ss(tmem, ad, bd, idesc, (kb | kk) ? 1u : 0u);
+            mma_bf16_ss(tmem + N * warp, ad, bd, idesc, (kb > 2 * warp || kk > 0) ? 1u : 0u);
           }
         }
       }
       mma_commit(&bars[1]);
     }
     __syncwarp();
-  }
-  __syncthreads();
-  if (mbar_wait(&bars[1], 0, nullptr, kWaitLimitNs)) {
-    tc_fence_after();
-    // warp w reads TMEM lanes 32 (w % 4) .. (output dims) and the 16 columns
-    // (rows) 16 (w / 4) ..
-    const int n = mt * 128 + (warp & 3) * 32 + lane;
-    const int cb = (warp >> 2) * 16;
-    uint32_t v[16];
-    tmem_ld16(tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + cb, v);
+    if (mbar_wait(&bars[1], 0, nullptr, kWaitLimitNs)) {
+      tc_fence_after();
+      // warp w reads TMEM lanes 32 w .. (output dims), every column (row)
+      const int n = mt * 128 + warp * 32 + lane;
+      const uint32_t lb = static_cast<uint32_t>(warp * 32) << 16;
+      for (int cb = 0; cb < N; cb += 16) {
+        float acc[16];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      const int r = r0 + cb + e;
-      if (r < rows)
-        out[(static_cast<int64_t>(r) * H + h) * kDv + n] = float_to_bf16_bits(__uint_as_float(v[e]));
+        for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t v[16];
+          tmem_ld16(tmem + lb + N * q + cb, v);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) acc[e] += __uint_as_float(v[e]);
+        }
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int r = r0 + cb + e;
+          if (r < rows) out[(static_cast<int64_t>(r) * heads + h) * kDv + n] = float_to_bf16_bits(acc[e]);
+        }
+      }
     }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, Cuv<N>::kTmemCols);
+    tmem_dealloc(tmem, Uv<N>::kTmemCols);
   }
 }
 
 namespace {
 template <int N>
-cudaError_t launch_cuv(const CUtensorMap* w_map, const CombineParams& p, uint16_t* out,
-                       cudaStream_t stream) {
-  const int rows = p.batch * p.q_len;
-  cudaError_t err = set_smem_attr_once(reinterpret_cast<const void*>(mla_combine_uv_kernel<N>),
-                                       N == 16 ? 10 : (N == 32 ? 11 : 12), Cuv<N>::kSmem);
+cudaError_t launch_uv(const CUtensorMap* w_map, const float* o_lat, uint16_t* out, int rows,
+                      int heads, cudaStream_t stream) {
+  cudaError_t err = set_smem_attr_once(reinterpret_cast<const void*>(mla_uv_kernel<N>),
+                                       N == 16 ? 1 : (N == 32 ? 2 : 10), Uv<N>::kSmem);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.heads, kDv / 128, (rows + N - 1) / N);
-  cfg.blockDim = dim3(Cuv<N>::kThreads);
-  cfg.dynamicSmemBytes = Cuv<N>::kSmem;
+  cfg.gridDim = dim3(heads, kDv / 128, (rows + N - 1) / N);
+  cfg.blockDim = dim3(Uv<N>::kThreads);
+  cfg.dynamicSmemBytes = Uv<N>::kSmem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;   // the two output halves of a row block
-  attr[1].val.clusterDim.x = 1;
-  attr[1].val.clusterDim.y = 2;
-  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  err = cudaLaunchKernelEx(&cfg, mla_combine_uv_kernel<N>, *w_map, p, out);
+  cfg.numAttrs = 1;
+  err = cudaLaunchKernelEx(&cfg, mla_uv_kernel<N>, *w_map, o_lat, out, rows, heads);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 }  // namespace
 
-cudaError_t launch_combine_uv(const CUtensorMap* w_map, const CombineParams& p, uint16_t* out,
-                              int sm_count, cudaStream_t stream) {
-  const int rows = p.batch * p.q_len;
+cudaError_t launch_uv_proj_tma(const CUtensorMap* w_map, const float* o_lat, uint16_t* out,
+                               int rows, int heads, int sm_count, cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
-  // the smallest row block whose grid fits the SMs (else the largest)
-  auto blocks = [&](int n) { return p.heads * (kDv / 128) * ((rows + n - 1) / n); };
-  if (blocks(16) <= sm_count && rows <= 16) return launch_cuv<16>(w_map, p, out, stream);
-  if (blocks(32) <= sm_count) return launch_cuv<32>(w_map, p, out, stream);
-  return launch_cuv<64>(w_map, p, out, stream);
+  auto blocks = [&](int n) { return heads * (kDv / 128) * ((rows + n - 1) / n); };
+  if (rows <= 16) return launch_uv<16>(w_map, o_lat, out, rows, heads, stream);
+  if (blocks(32) <= sm_count) return launch_uv<32>(w_map, o_lat, out, rows, heads, stream);
+  return launch_uv<64>(w_map, o_lat, out, rows, heads, stream);
 }
 
 // ----------------------------------------------------------------------------

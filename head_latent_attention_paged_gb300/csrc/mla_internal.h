@@ -87,17 +87,11 @@ struct CombineParams {
 };
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
 
-// The merge of split row sets fused with the W_UV up-projection: per (head,
-// 128 output dims, 32 rows), every row's o_lat (merged from the partials
-// when its row set was split, else as the decode wrote it) becomes the B
-// operand of D^T = W_UV[h]^T o_lat^T.  Writes out (bf16) for every row and,
-// in the blocks of the first 128 output dims, o_lat and lse of split rows.
-// sm_count sizes the row blocks (16, 32 or 64 rows) so the grid fits.
-cudaError_t launch_combine_uv(const CUtensorMap* w_map, const CombineParams& p, uint16_t* out,
-                              int sm_count, cudaStream_t stream);
-
+// o = W_UV[h]^T o_lat per (head, 128 output dims, row block), a programmatic
+// dependent of the launch before it; sm_count sizes the row blocks (16, 32
+// or 64 rows) so the grid fits the SMs where it can.
 cudaError_t launch_uv_proj_tma(const CUtensorMap* w_map, const float* o_lat, uint16_t* out,
-                               int rows, int heads, cudaStream_t stream);
+                               int rows, int heads, int sm_count, cudaStream_t stream);
 
 struct AppendParams {
   const uint16_t* new_rows;     // bf16 [rows][576]

@@ -8,8 +8,8 @@ import numpy as np
 import torch
 
 from . import (MLA_KV_BF16, MLA_KV_FP4_E2M1_E8M0, MLA_KV_FP8_E4M3_E8M0, make_problem,
-               mla_clear_status, mla_combine, mla_decode_plan, mla_decode_run, mla_get_status,
-               mla_q_absorb, mla_uv_proj)
+               mla_clear_status, mla_combine, mla_decode_plan, mla_decode_run, mla_decode_step,
+               mla_get_status, mla_q_absorb, mla_uv_proj)
 
 
 def to_device_bf16(bits: np.ndarray, device) -> torch.Tensor:
@@ -108,8 +108,16 @@ class DecodeStep:
         mla_uv_proj(self.o_lat, self.w_uv, self.out, self.rows, self.H, self.stream)
 
     def step(self):
-        """One decode step: the attention pass, then the merge fused with the
-        W_UV projection (two kernels); the absorbed query is an input."""
+        """One decode step (mla_decode_step): the attention pass, the merge of
+        split row sets and the W_UV projection (three kernels, each a
+        programmatic dependent of the one before); the absorbed query is an
+        input."""
+        mla_decode_step(self.plan, self.q_hat, None, self.cache, self.block_table, self.seq_lens,
+                        self.topk_idx, self.workspace, self.w_uv, self.o_lat, self.lse, self.out,
+                        self.stream)
+
+    def step_two_calls(self):
+        """The same step as mla_decode_run then mla_combine with W_UV."""
         self.attend()
         self.combine(uv=True)
 
@@ -119,7 +127,7 @@ class DecodeStep:
     def clear_status(self):
         mla_clear_status(self.plan, self.workspace, self.stream)
 
-    KERNELS_PER_STEP = 2
+    KERNELS_PER_STEP = 3
 
 
 class HostPipeline:
@@ -132,8 +140,8 @@ class HostPipeline:
     arenas rotate, and the copies run on their own streams: the inputs of
     step k + 1 and the outputs of step k - 1 move while step k computes.
     Each step appends its newest token rows to the cache (mla_cache_append,
-    RoPE applied to their keys when rope_theta > 0) and runs the decode and
-    the merge fused with the W_UV projection on the compute stream.
+    RoPE applied to their keys when rope_theta > 0) and runs the whole decode
+    step (mla_decode_step) on the compute stream.
 
     The caller refills host arena `k % depth` for step k only after
     `input_copied(k - depth)` has been synchronised (the static inputs of a

@@ -234,11 +234,13 @@ MLA_API int mla_decode_run(const mla_plan* plan, const void* q, const void* w_uk
  * workspace, o_lat and lse): merges the partials of every row set that was
  * split over several CTAs, lse = ln sum_i exp(lse_i), o_lat = sum_i
  * exp(lse_i - lse) o_i, into o_lat and lse; and, when w_uv is given, applies
- * the kv_b_proj value half to every row in the same kernel ("GLM-4.7-Flash"
+ * the kv_b_proj value half to every row in the same call ("GLM-4.7-Flash"
  * record, configuration clause: v_head_dim 256 read back out of the 512-rank
  * latent through kv_b_proj): out[r][h] = bf16(W_UV[h]^T o_lat[r][h]).
- * Launched as a programmatic dependent of the kernel before it on `stream`:
- * its set-up (and its W_UV loads) overlap the attention pass's tail.
+ * The merge runs over all SMs (one block per row of each split row set) and
+ * the up-projection per (head, 128 output dims, row block); each is launched
+ * as a programmatic dependent of the kernel before it on `stream`, so its
+ * set-up (and the W_UV loads) overlap that kernel's tail.
  *   w_uv  : NULL, or bf16 [H][512][256]
  *   out   : bf16 [B*Q][H][256] when w_uv is given, else ignored (may be NULL)
  * After the call o_lat and lse are complete for every row.  Calling it again
@@ -249,6 +251,23 @@ MLA_API int mla_decode_run(const mla_plan* plan, const void* q, const void* w_uk
 MLA_API int mla_combine(const mla_plan* plan, const int32_t* seq_lens, const void* workspace,
                 size_t workspace_bytes, const void* w_uv, float* o_lat, float* lse, void* out,
                 mla_stream_t stream);
+
+/*
+ * mla_decode_step -- one whole decode step in one call: mla_decode_run, then
+ * mla_combine with W_UV (the attention pass, the merge of split row sets over
+ * all SMs, and the W_UV up-projection per head, each kernel a programmatic
+ * dependent of the one before).  Same arguments as mla_decode_run, plus
+ *   w_uv : bf16 [H][512][256]
+ *   out  : bf16 [B*Q][H][256] output, out[r][h] = bf16(W_UV[h]^T o_lat[r][h])
+ * o_lat and lse are complete on return.  ("GLM-4.7-Flash" record: the MLA
+ * decode kernel class and the configuration clause's kv_b_proj value half.)
+ * Returns MLA_OK, MLA_ERR_INVALID_ARGUMENT, MLA_ERR_MISALIGNED,
+ * MLA_ERR_UNSUPPORTED, MLA_ERR_WORKSPACE_TOO_SMALL or MLA_ERR_CUDA.
+ */
+MLA_API int mla_decode_step(const mla_plan* plan, const void* q, const void* w_uk,
+                    const void* kv_cache, const int32_t* block_table, const int32_t* seq_lens,
+                    const int32_t* topk_idx, void* workspace, size_t workspace_bytes,
+                    const void* w_uv, float* o_lat, float* lse, void* out, mla_stream_t stream);
 
 /*
  * mla_cache_append -- write each request's newest token row into the paged

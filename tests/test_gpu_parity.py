@@ -287,11 +287,11 @@ def test_full_size_sampled(name, requests, heads):
 
 @pytest.mark.parametrize("name,sm_count", [("dense_small", 7), ("long_small", 40),
                                            ("mtp_small", 11), ("sparse_small", 5), ("tiny", None)])
-def test_fused_merge_and_uv_matches_separate_passes(name, sm_count):
-    """mla_combine with W_UV (merge and up-projection in one kernel) against
-    the merge alone followed by the stand-alone mla_uv_proj: the same o_lat
-    and lse (the two merges sum the partials in different orders: fp32
-    rounding) and outputs within one bf16 step; both against the oracle."""
+def test_combine_with_w_uv_matches_separate_passes(name, sm_count):
+    """mla_combine with W_UV against the merge alone followed by the
+    stand-alone mla_uv_proj (whose row block follows the device's SM count,
+    not the plan's): the same o_lat and lse, outputs within one bf16 step;
+    both against the oracle."""
     batch = W.generate(W.SMALL_WORKLOADS[name])
     step = make_step(batch, sm_count=sm_count)
     step.run()
@@ -299,7 +299,7 @@ def test_fused_merge_and_uv_matches_separate_passes(name, sm_count):
     o1, lat1, lse1 = gpu_outputs(step)
     for t in (step.out, step.o_lat, step.lse):
         t.fill_(float("nan"))
-    step.step()                        # attention pass, then merge + W_UV fused
+    step.step()                        # attention pass, merge, W_UV
     o2, lat2, lse2 = gpu_outputs(step)
     assert np.allclose(lat2, lat1, rtol=1e-5, atol=1e-6)
     live = np.isfinite(lse1)
@@ -307,7 +307,7 @@ def test_fused_merge_and_uv_matches_separate_passes(name, sm_count):
     assert np.abs(o2 - o1).max() <= 2.0 ** -7 * max(1.0, np.abs(o1).max())
     ref = O.decode(batch)
     compare(ref, o1, lat1, lse1, label=f"separate/{name}")
-    compare(ref, o2, lat2, lse2, label=f"fused/{name}")
+    compare(ref, o2, lat2, lse2, label=f"combine-uv/{name}")
 
 
 @pytest.mark.parametrize("name", ["dense_small", "mtp_small", "tiny"])
@@ -363,3 +363,29 @@ def test_absorb_tensor_core_matches_float64(rows, heads):
     ref = np.einsum("hdk,rhk->rhd", O.bf16_to_f64(w_uk), O.bf16_to_f64(q[..., :192]))
     assert (np.abs(got[..., :512] - ref) <= np.abs(ref) * 2.0 ** -7 + 1e-6).all()
     assert np.array_equal(got[..., 512:], O.bf16_to_f64(q[..., 192:]))
+
+
+@pytest.mark.parametrize("name,sm_count", [("dense_small", None), ("long_small", 40),
+                                           ("mtp_small", 11), ("sparse_small", 5), ("tiny", None),
+                                           ("fp8_small", 9), ("fp4_small", 152)])
+def test_decode_step_matches_run_and_combine(name, sm_count):
+    """mla_decode_step (one call) gives the bits of mla_decode_run followed by
+    mla_combine with W_UV, twice in a row on one workspace; against the
+    oracle with the decode's own bf16 absorbed query for lse."""
+    batch = with_fp8(W.generate(W.SMALL_WORKLOADS[name]))
+    step = make_step(batch, sm_count=sm_count, absorb=False)
+    q_hat = oracle_q_hat(batch)
+    upload_q_hat(step, q_hat)
+    step.step_two_calls()
+    o1, lat1, lse1 = gpu_outputs(step)
+    for trial in range(2):
+        for t in (step.out, step.o_lat, step.lse):
+            t.fill_(float("nan"))
+        step.step()
+        o2, lat2, lse2 = gpu_outputs(step)
+        assert step.status() == 0, trial
+        assert np.array_equal(lat2.view(np.uint32), lat1.view(np.uint32)), trial
+        assert np.array_equal(lse2.view(np.uint32), lse1.view(np.uint32)), trial
+        assert np.array_equal(o2, o1), trial
+    compare(O.decode(batch), o2, lat2, lse2, label=f"decode-step/{name}",
+            lse_ref=O.decode(batch, q_hat=q_hat))
