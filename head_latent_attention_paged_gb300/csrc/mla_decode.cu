@@ -59,6 +59,7 @@ constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kDequantWarp0 = 6;    // FP8 / FP4 modes: warps 6..11 dequantise
 constexpr int kDequantWarps = 6;
+constexpr int kGroupSets = kDequantWarps * 32 / kTile;   // threads per row in the dequant
 // P (bf16 [padded heads][64 tokens], the B operand of PV) lives in the RoPE
 // chunk of its own tile's stage: QK(i) is the only reader of that chunk and
 // P(i) is written after S(i) is complete, so every stage carries its own P.
@@ -101,16 +102,20 @@ struct ModeTraits {
   static constexpr int kQTmemChunks = kQRopeSmem ? kChunks - 1 : kChunks;
   // A tcgen05.mma costs its issuing thread a fixed time whatever its shape,
   // and MMAs from different threads overlap in the tensor pipe: the PV
-  // products go out from a warp of their own, beside the QK issuer (the
-  // quantised-cache kernels, whose dequant warps take the register file,
-  // keep one issuer for both).
-  static constexpr bool kDualIssue = !kQuant;
+  // products go out from a thread of their own, beside the QK issuer.
+  // In the FP8 kernel, whose dequant warps take the register file, the
+  // producer warp issues PV while it waits for raw slots.  The FP4 kernels'
+  // raw tiles land in the bf16 stages PV frees, so their producer must not
+  // be kept busy: there one MMA thread issues both QK and PV.
+  static constexpr bool kPvInProducer = kFp8;
+  static constexpr bool kSingleIssuer = kFp4;
   static constexpr int kRoleWarps = kQuant ? kDequantWarp0 + kDequantWarps
                                    : kSparse ? kGatherWarp0 + kGatherWarps
                                              : 6;
-  static constexpr int kPvWarp = kRoleWarps;     // the PV issuer (dual-issue kernels)
-  static constexpr int kQk2Warp = kRoleWarps + 1; // the second QK issuer (split-QK kernels)
-  static constexpr int kThreads = 32 * (kRoleWarps + (kDualIssue ? 1 : 0) + (kSplitQK ? 1 : 0));
+  static constexpr bool kPvWarpOwn = !kPvInProducer && !kSingleIssuer;
+  static constexpr int kPvWarp = kPvWarpOwn ? kRoleWarps : -1;   // the PV issuer's warp
+  static constexpr int kQk2Warp = kRoleWarps + (kPvWarpOwn ? 1 : 0);   // second QK issuer
+  static constexpr int kThreads = 32 * (kRoleWarps + (kPvWarpOwn ? 1 : 0) + (kSplitQK ? 1 : 0));
   // FP8: two bf16 stages and a two-slot ring of raw tiles beside them.
   // FP4: three bf16 stages, each raw tile landing in the last
   // kRawTileBytes of the stage it is dequantised into.
@@ -630,6 +635,61 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
       wk.init(prefix, S, g0);
       int32_t issued = 0;
       bool failed = false;
+      // Quantised caches: this warp's lane 0 also issues PV (O^T += V^T P^T,
+      // 4 x 4 MMAs over the staged tile; see the MMA role), serving every P
+      // that is ready whenever it waits for a raw slot, and the rest after
+      // its last copy.
+      Walker pv_wk;
+      int32_t pv = 0, pv_seg = -1;
+      if constexpr (MT::kPvInProducer) pv_wk.init(prefix, S, g0);
+      auto try_pv = [&]() -> bool {
+        if (pv >= ntiles) return false;
+        const int st = pv % kNumStages;
+        const bool first = (pv == 0) || (pv_wk.lt == 0);
+        const int32_t sg = first ? pv_seg + 1 : pv_seg;
+        if (!mbar_poll(&ctrl->p_full[pv & 1], (pv >> 1) & 1) ||
+            (first && sg > 0 && !mbar_poll(&ctrl->o_free, (sg - 1) & 1)))
+          return false;
+        tc_fence_after();
+        const uint32_t idesc_pv = make_idesc_bf16(128, static_cast<uint32_t>(NP), true, false);
+        const uint64_t a0 = make_smem_desc(smem_u32(sStage + st * kTileBytes), kChunkBytes, 1024,
+                                           kSmemLayoutSW128);
+        const uint64_t b0 = make_smem_desc(smem_u32(sStage + st * kTileBytes + kPChunkOffset), 16,
+                                           1024, kSmemLayoutSW128);
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ss(tmem + MT::kColO + mt * NP, a0 + ((2 * mt * kChunkBytes + kk * 2048) >> 4),
+                        b0 + ((kk * 32) >> 4), idesc_pv, (first && kk == 0) ? 0u : 1u);
+        }
+        // o_done before empty: a stage seen free implies its PV seen done
+        mma_commit(&ctrl->o_done[pv & 1]);
+        mma_commit(&ctrl->empty[st]);
+        pv_seg = sg;
+        pv_wk.next(prefix, S);
+        ++pv;
+        return true;
+      };
+      // warp-wide wait for a raw slot, lane 0 issuing ready PVs meanwhile
+      // (polled with a short sleep: measured faster than suspending on the
+      // slot's barrier between looks at P)
+      auto wait_serving_pv = [&](uint64_t* bar, uint32_t par) -> bool {
+        if constexpr (!MT::kPvInProducer) return warp_wait(bar, par, abort_flag);
+        uint64_t t_last = globaltimer_ns();
+        while (!__shfl_sync(0xffffffffu, mbar_poll(bar, par), 0)) {
+          bool progressed = false;
+          if (lane == 0) progressed = try_pv();
+          if (__shfl_sync(0xffffffffu, progressed, 0)) {
+            t_last = globaltimer_ns();
+          } else if (*abort_flag || globaltimer_ns() - t_last > kWaitLimitNs) {
+            return false;
+          } else {
+            __nanosleep(20);
+          }
+        }
+        return true;
+      };
       for (int32_t i = 0; i < ntiles; ++i) {
         const int stage = i % kNumStages;
         const uint32_t reuse_parity = ((i / kNumStages) - 1) & 1;
@@ -737,7 +797,7 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
                                MT::kRowBytes;
               bytes = static_cast<uint32_t>((nvalid + 7) & ~7) * MT::kRowBytes;
             }
-            if (i >= MT::kRawSlots && !warp_wait(reuse_bar, reuse_par, abort_flag)) {
+            if (i >= MT::kRawSlots && !wait_serving_pv(reuse_bar, reuse_par)) {
               failed = true;
               break;
             }
@@ -755,7 +815,7 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
             const TilePieces tp = describe_tile(p, b, j, wk.lt, lane, max_tokens);
             const uint64_t mask = tile_mask(tp);
             if (lane == 0 && tp.bad) set_status(p.status, tp.bad);
-            if (i >= MT::kRawSlots && !warp_wait(reuse_bar, reuse_par, abort_flag)) {
+            if (i >= MT::kRawSlots && !wait_serving_pv(reuse_bar, reuse_par)) {
               failed = true;
               break;
             }
@@ -789,9 +849,34 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
         ++issued;
         wk.next(prefix, S);
       }
+      if constexpr (MT::kPvInProducer) {
+        // the PVs after the last copy
+        if (lane == 0 && !failed) {
+          uint64_t t_last = globaltimer_ns();
+          while (pv < ntiles) {
+            if (try_pv()) {
+              t_last = globaltimer_ns();
+            } else if (*abort_flag || globaltimer_ns() - t_last > kWaitLimitNs) {
+              failed = true;
+              break;
+            } else {
+              __nanosleep(20);
+            }
+          }
+        }
+        failed = __shfl_sync(0xffffffffu, failed, 0);
+      }
       if (failed && lane == 0) {
         set_status(p.status, MLA_STATUS_TIMEOUT);
         ctrl->abort_flag = 1;
+      }
+      if constexpr (MT::kPvInProducer) {
+        // every PV issued here completes before tensor memory is released
+        if (lane == 0) {
+          mma_commit(&ctrl->mma_drain[1]);
+          (void)mbar_wait(&ctrl->mma_drain[1], 0, nullptr, kWaitLimitNs);
+        }
+        __syncwarp();
       }
       // drain: everything this warp issued has landed before the CTA exits
       if (lane == 0) {
@@ -806,7 +891,7 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
         }
       }
       __syncwarp();
-    } else if (warp == kMmaWarp || (MT::kDualIssue && warp == MT::kPvWarp) ||
+    } else if (warp == kMmaWarp || warp == MT::kPvWarp ||
                (MT::kSplitQK && warp == MT::kQk2Warp)) {
       // ================================================================= MMA
       const uint32_t idesc_qk = make_idesc_bf16(64, 64, false, false);
@@ -874,7 +959,7 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
         return true;
       };
       bool failed = false;
-      if constexpr (MT::kDualIssue) {
+      if constexpr (!MT::kSingleIssuer) {
         // Two issuers: this warp's lane 0 issues QK(qk) once its tile, the
         // stream's q_hat and the S buffer are ready; the PV warp's lane 0
         // issues PV(pv) once P(pv) is written (and, opening a segment, once
@@ -1040,8 +1125,8 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
           const uint8_t* row_ptr = sRaw + rs * MT::kRawTileBytes + r * MT::kRowBytes;
           uint8_t* dst = sStage + bs * kTileBytes + r * 128;
 #pragma unroll 2
-          for (int k = 0; k < kDqk / 96; ++k) {
-            const int g = gset + 3 * k;
+          for (int k = 0; k < kDqk / 32 / kGroupSets; ++k) {
+            const int g = gset + kGroupSets * k;
             uint4 o[4];
             if (live) {
               Fp8Group f;
@@ -1075,13 +1160,13 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
           uint8_t* tile = sStage + stage * kTileBytes;
           const uint8_t* row_ptr = tile + MT::kRawOffset + r * MT::kRowBytes;
           uint8_t* dst = tile + r * 128;
-          constexpr int kDirect = 8;
-          constexpr int kKept = kDqk / 48 - kDirect;
+          constexpr int kDirect = 24 / kGroupSets;            // groups 0-23 lie in chunks 0-5
+          constexpr int kKept = kDqk / 16 / kGroupSets - kDirect;
           Fp4Group keep[kKept];
           if (ok) {
 #pragma unroll 4
             for (int k = 0; k < kDirect; ++k) {
-              const int g = gset + 3 * k;
+              const int g = gset + kGroupSets * k;
               uint4 o[2];
               if (live) {
                 Fp4Group f;
@@ -1094,7 +1179,8 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
             }
             if (live) {
 #pragma unroll
-              for (int k = 0; k < kKept; ++k) load_fp4_group(row_ptr, gset + 3 * (kDirect + k), keep[k]);
+              for (int k = 0; k < kKept; ++k)
+                load_fp4_group(row_ptr, gset + kGroupSets * (kDirect + k), keep[k]);
             }
           }
           // every dequant warp reaches this barrier once per tile; a failed
@@ -1108,7 +1194,7 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
             uint4 o[2];
             if (live) convert_fp4_group(keep[k], o);
             else o[0] = o[1] = make_uint4(0, 0, 0, 0);
-            store_group(dst, gset + 3 * (kDirect + k), o);
+            store_group(dst, gset + kGroupSets * (kDirect + k), o);
           }
           fence_proxy_async_smem();   // generic stores -> tensor-core reads
           __syncwarp();
