@@ -146,3 +146,36 @@ def test_fp8_full_size_sampled():
     step = _run_and_compare(batch, requests=[0, 64, 127], heads=[0, 9, 19], label="fp8-full")
     o, _, lse = gpu_outputs(step)
     assert np.isfinite(o).all() and np.isfinite(lse).all()
+
+
+def test_fp8_full_size_from_the_absmax_quantiser():
+    """The FP8 workload as stated (B=128, seq_lens U[2048, 16384], page 64):
+    an N(0, 1) latent quantised by the oracle's quantiser (one e8m0 scale per
+    32 values from the group's absolute maximum), decoded in the benchmark's
+    launch configuration; sampled requests and heads against the oracle on
+    the same bytes."""
+    batch = with_fp8(W.generate(W.WORKLOADS["fp8"], fp8_source="float"))
+    batch.latent_f32 = None
+    step = _run_and_compare(batch, requests=[0, 50, 101, 127], heads=[0, 6, 13, 19],
+                            label="fp8-full-absmax")
+    o, _, lse = gpu_outputs(step)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+
+
+def test_gpu_quantiser_matches_oracle_on_full_size_rows():
+    """The GPU quantiser the benchmark uses for its FP8 and FP4 caches
+    (mla_cache_append over every slot) against the oracle's quantisers, byte
+    for byte, on 4096 rows drawn from the full-size FP8 workload's latent."""
+    from head_latent_attention_paged_gb300 import (MLA_KV_FP4_E2M1_E8M0, MLA_KV_FP8_E4M3_E8M0)
+    from head_latent_attention_paged_gb300.runner import quantise_cache_on_device
+    from oracle import fp4 as F4
+    batch = W.generate(W.WORKLOADS["fp8"], fp8_source="float")
+    rng = np.random.default_rng(17)
+    rows = rng.choice(batch.latent_f32.shape[0] * batch.latent_f32.shape[1], size=4096, replace=False)
+    flat = batch.latent_f32.reshape(-1, 576)[rows]
+    bits = W.f32_to_bf16_bits(flat)
+    lat = W.bf16_bits_to_f32(bits).reshape(64, 64, 576)     # 64 pages of the sampled rows
+    for kv, enc in [(MLA_KV_FP8_E4M3_E8M0, F), (MLA_KV_FP4_E2M1_E8M0, F4)]:
+        got = quantise_cache_on_device(lat, kv, "cuda:0").cpu().numpy().reshape(-1, enc.ROW_BYTES)
+        want = enc.quantize_rows(lat.reshape(-1, 576).astype(np.float64))
+        assert np.array_equal(got, want), (enc.__name__, int((got != want).any(axis=1).sum()))

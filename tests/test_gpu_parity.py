@@ -285,6 +285,21 @@ def test_full_size_sampled(name, requests, heads):
     compare(ref, o, o_lat, lse, heads=heads, label=name)
 
 
+def test_long_full_size_every_request_and_head():
+    """The long-context workload (8 requests of 64K-128K tokens split over
+    all SMs, ~19 partials per request) in full: every request and every head
+    against the oracle's absorbed form (pinned equal to the definition), and
+    request 5, heads 0 and 10, against the definition itself."""
+    batch = W.generate(W.WORKLOADS["long"])
+    step = make_step(batch)
+    step.step()
+    o, o_lat, lse = gpu_outputs(step)
+    assert step.status() == 0
+    compare(O.decode(batch, form="absorbed"), o, o_lat, lse, label="long-absorbed")
+    compare(O.decode(batch, requests=[5], heads=[0, 10]), o, o_lat, lse, heads=[0, 10],
+            label="long-definition")
+
+
 @pytest.mark.parametrize("name,sm_count", [("dense_small", 7), ("long_small", 40),
                                            ("mtp_small", 11), ("sparse_small", 5), ("tiny", None)])
 def test_combine_with_w_uv_matches_separate_passes(name, sm_count):
