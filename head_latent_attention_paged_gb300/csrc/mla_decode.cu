@@ -65,6 +65,8 @@ constexpr int kGroupSets = kDequantWarps * 32 / kTile;   // threads per row in t
 // P(i) is written after S(i) is complete, so every stage carries its own P.
 constexpr int kPChunkOffset = (kChunks - 1) * kChunkBytes;
 
+constexpr int kPvLanes = 4;         // PV issuing lanes: lane l issues O^T block l (128 dims)
+
 constexpr int kGatherWarp0 = 6;     // sparse mode: warps 6..9 gather top-k rows
 constexpr int kGatherWarps = 4;
 constexpr int kGatherRows = kTile / kGatherWarps;   // 16 rows per gather warp
@@ -83,39 +85,38 @@ struct ModeTraits {
   // the first softmax warp whose TMEM lanes hold rows: row r of a row set is
   // M-row 16 * kRowWarp0 + r of the QK accumulator
   static constexpr int kRowWarp0 = kMulti ? 1 : 2;
-  // Split QK (dense one-token bf16 kernel): two issuers each take half of
-  // QK's K range into an S accumulator of their own (S = S_a + S_b, summed
-  // by the softmax): latent chunks 0-3 into S_a, 4-7 and the RoPE chunk into
-  // S_b.  (The sparse kernel's gather warps leave no registers for the
-  // second S in the softmax.)
+  // Split QK: two issuers each take half of QK's K range into an S
+  // accumulator of their own (S = S_a + S_b, summed by the softmax): latent
+  // chunks 0-3 and the first half of the RoPE chunk into S_a, chunks 4-7 and
+  // the second half into S_b.  A tcgen05.mma costs its issuing thread a
+  // fixed time whatever its shape, and MMAs from different threads overlap
+  // in the tensor pipe, whether the threads are lanes of one warp or sit in
+  // different warps (two warps overlap better).  The dense one-token bf16
+  // kernel issues the halves from two warps; the one-token FP8, FP4 and
+  // sparse kernels, whose dequant or gather warps take the register file,
+  // from two lanes of the MMA warp.  The multi-token kernels keep one QK
+  // issuer: their O^T (48 padded rows) leaves no TMEM for a second S.
   static constexpr bool kSplitQK = kMode == kModeDenseBf16;
+  static constexpr bool kSplitQKLanes =
+      kMode == kModeDenseFp8 || kMode == kModeDenseFp4 || kMode == kModeSparseBf16;
+  static constexpr bool kSplitS = kSplitQK || kSplitQKLanes;
+  static constexpr int kQkLanes = kSplitQKLanes ? 2 : 1;   // QK issuing lanes of the MMA warp
   // q_hat's RoPE part is a shared-memory A operand (multi-token and split-QK
   // kernels), so that TMEM holds the extra accumulator.
-  static constexpr bool kQRopeSmem = kMulti || kSplitQK;
+  static constexpr bool kQRopeSmem = kMulti || kSplitS;
   // TMEM columns: q_hat (all 576 values, or the 512 latent ones when the
   // RoPE part is a shared-memory operand), S (64; two of them when QK is
   // split), O^T (4 x heads_pad)
   static constexpr uint32_t kColQ = 0;
   static constexpr uint32_t kColS = kQRopeSmem ? 256 : 288;
   static constexpr uint32_t kColS2 = kColS + 64;
-  static constexpr uint32_t kColO = kColS + (kSplitQK ? 128 : 64);
+  static constexpr uint32_t kColO = kColS + (kSplitS ? 128 : 64);
   static constexpr int kQTmemChunks = kQRopeSmem ? kChunks - 1 : kChunks;
-  // A tcgen05.mma costs its issuing thread a fixed time whatever its shape,
-  // and MMAs from different threads overlap in the tensor pipe: the PV
-  // products go out from a thread of their own, beside the QK issuer.
-  // In the FP8 kernel, whose dequant warps take the register file, the
-  // producer warp issues PV while it waits for raw slots.  The FP4 kernels'
-  // raw tiles land in the bf16 stages PV frees, so their producer must not
-  // be kept busy: there one MMA thread issues both QK and PV.
-  static constexpr bool kPvInProducer = kFp8;
-  static constexpr bool kSingleIssuer = kFp4;
   static constexpr int kRoleWarps = kQuant ? kDequantWarp0 + kDequantWarps
                                    : kSparse ? kGatherWarp0 + kGatherWarps
                                              : 6;
-  static constexpr bool kPvWarpOwn = !kPvInProducer && !kSingleIssuer;
-  static constexpr int kPvWarp = kPvWarpOwn ? kRoleWarps : -1;   // the PV issuer's warp
-  static constexpr int kQk2Warp = kRoleWarps + (kPvWarpOwn ? 1 : 0);   // second QK issuer
-  static constexpr int kThreads = 32 * (kRoleWarps + (kPvWarpOwn ? 1 : 0) + (kSplitQK ? 1 : 0));
+  static constexpr int kQk2Warp = kRoleWarps;   // second QK issuer (dense one-token kernel)
+  static constexpr int kThreads = 32 * (kRoleWarps + (kSplitQK ? 1 : 0));
   // FP8: two bf16 stages and a two-slot ring of raw tiles beside them.
   // FP4: three bf16 stages, each raw tile landing in the last
   // kRawTileBytes of the stage it is dequantised into.
@@ -139,13 +140,11 @@ constexpr int kQRopeBytes = 64 * 128;   // RoPE part of q_hat as a shared-memory
 // Control block placed after the data buffers in shared memory.
 struct __align__(8) Ctrl {
   uint64_t full[kStages];    // producer -> MMA/softmax: tile staged
-  uint64_t empty[kStages];   // MMA -> producer: stage consumed by PV
+  uint64_t empty[kStages];   // PV -> producer: stage consumed
   uint64_t s_full;           // MMA -> softmax: S written
   uint64_t s_free;           // softmax -> MMA: S read
-  uint64_t p_full[2];        // softmax -> MMA: P written (and O^T rescaled)
   uint64_t q_ready;          // softmax -> MMA: a stream's q_hat is in TMEM
-  uint64_t o_done[2];        // MMA -> softmax: PV(j) completed, on o_done[j % 2]
-  uint64_t o_free;           // softmax -> MMA: epilogue has read O^T
+  uint64_t o_done[2];        // PV(j) completed, on o_done[j % 2]
   uint64_t mma_drain[3];     // the issuers' final commits (QK, PV, second QK)
   uint64_t mask[kStages];    // per-stage live-row mask (bit t = row t live)
   uint64_t raw_full[kStages];       // FP8 / FP4: producer -> dequant, bytes landed
@@ -276,6 +275,17 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// PV into block mt of O^T (latent dims 128 mt .. 128 mt + 127): O^T[mt]
+// (+)= V^T[mt] P^T over one staged tile, K = 64 tokens in 4 MMAs.  a0 / b0
+// are the descriptors of the tile's chunk 0 (read MN-major) and of its P.
+__device__ __forceinline__ void issue_pv_block(uint32_t d_tmem, uint64_t a0, uint64_t b0,
+                                               uint32_t idesc, int mt, bool first) {
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk)
+    mma_bf16_ss(d_tmem, a0 + ((2 * mt * kChunkBytes + kk * 2048) >> 4), b0 + ((kk * 32) >> 4),
+                idesc, (first && kk == 0) ? 0u : 1u);
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
@@ -299,9 +309,9 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 // starts at M-row 16 (warps 1-3).  The 512 latent values go to TMEM, packed
 // two per column, and the 64 RoPE values either to TMEM as well or
 // (kRopeSmem) to a shared-memory operand (row m at m * 128 bytes, 16-byte
-// units swizzled by m % 8), where M-rows without a row are written as
-// zeros.  Every softmax
-// warp calls this; absent rows get zeros.  TMEM loads go in batches of
+// units swizzled by m % 8).  Every softmax warp calls this; M-rows of warps
+// kRowWarp0.. without a row get zeros, the M-rows below are not written
+// (their S rows are never read).  TMEM loads go in batches of
 // kBatch chunks of 64 values to keep many in flight (fewer in the kernels
 // whose thread count leaves fewer registers per thread).
 template <int kRowWarp0, bool kRopeSmem, int kBatch>
@@ -338,7 +348,7 @@ __device__ __forceinline__ void load_q(const uint16_t* q_rows, int nrows, uint32
     }
   }
   if constexpr (kRopeSmem) {
-    if (lane < 16) {
+    if (w >= kRowWarp0 && lane < 16) {
       const int m = 16 * w + lane;
       uint8_t* row = q_rope + m * 128;
 #pragma unroll
@@ -505,18 +515,26 @@ __device__ __forceinline__ void convert_fp4_group(const Fp4Group& f, uint4 (&o)[
 
 DecodeLayout decode_layout(int heads, int heads_pad, int num_streams, int mode) {
   (void)heads;
+  (void)heads_pad;
   const bool ring = mode == kModeDenseFp8;   // FP8: bf16 stages plus a raw ring
   DecodeLayout L;
   L.off_stage = 0;
   L.off_raw = (ring ? kFp8Stages : kStages) * kTileBytes;
-  (void)heads_pad;
   L.off_p = L.off_stage + kPChunkOffset;     // first stage's P; stride kTileBytes
-  // the multi-token mode's RoPE query operand (1024-byte aligned after the stages)
-  L.off_qrope = L.off_raw;
-  L.off_ctrl = L.off_raw + (ring ? kFp8RawSlots * kFp8TileBytes : 0) +
-               (mode == kModeDenseMulti || mode == kModeDenseFp4Multi || mode == kModeDenseBf16
-                    ? kQRopeBytes
-                    : 0);
+  // q_hat's RoPE part as a shared-memory A operand: 64 M-rows x 128 B from
+  // off_qrope, 1024-byte aligned.  Only the M-rows of the row set's softmax
+  // warps are written and read back into S; in the FP8 kernel, which has no
+  // room for all 8 KB, M-rows 0-31 (no row of a one-token row set) overlap
+  // the end of the raw ring: the MMA reads whatever bytes are there into S
+  // rows no one reads.
+  const int raw_end = L.off_raw + (ring ? kFp8RawSlots * kFp8TileBytes : 0);
+  if (ring) {
+    L.off_qrope = ((raw_end + 1023) & ~1023) - kQRopeBytes / 2;
+    L.off_ctrl = L.off_qrope + kQRopeBytes;
+  } else {
+    L.off_qrope = raw_end;
+    L.off_ctrl = raw_end + kQRopeBytes;
+  }
   L.total = L.off_ctrl + static_cast<int>(sizeof(Ctrl)) + 2 * (num_streams + 1) * 4;
   return L;
 }
@@ -533,7 +551,7 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* sStage = smem + L.off_stage;
   uint8_t* sRaw = smem + L.off_raw;   // FP8 raw ring
-  uint8_t* sQr = smem + L.off_qrope;  // multi-token mode: RoPE part of q_hat
+  uint8_t* sQr = smem + L.off_qrope;  // RoPE part of q_hat (A operand base, M-row 0)
   Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + L.off_ctrl);
   int32_t* prefix = reinterpret_cast<int32_t*>(smem + L.off_ctrl + sizeof(Ctrl));  // tiles
   int32_t* cprefix = prefix + (p.num_streams + 1);                                   // cost
@@ -564,21 +582,21 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
       // sparse: one byte-count arrival per gather warp
       mbar_init(&ctrl->full[i],
                 MT::kQuant ? kDequantWarps : (MT::kSparse ? kGatherWarps : 1));
-      mbar_init(&ctrl->empty[i], 1);
+      mbar_init(&ctrl->empty[i], kPvLanes);   // one commit per PV lane
     }
     for (int i = 0; i < kStages; ++i) mbar_init(&ctrl->raw_full[i], 1);
     for (int i = 0; i < kFp8RawSlots; ++i) mbar_init(&ctrl->raw_empty[i], kDequantWarps);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&ctrl->p_full[i], kSoftmaxWarps);
-      ctrl->rescale_tile[i] = -1;
-    }
-    mbar_init(&ctrl->s_full, MT::kSplitQK ? 2 : 1);   // one commit per QK issuer
+    for (int i = 0; i < 2; ++i) ctrl->rescale_tile[i] = -1;
+    mbar_init(&ctrl->s_full, MT::kSplitS ? 2 : 1);   // one commit per QK issuer
     mbar_init(&ctrl->s_free, kSoftmaxWarps);
     mbar_init(&ctrl->q_ready, kSoftmaxWarps);
-    mbar_init(&ctrl->o_done[0], 1);
-    mbar_init(&ctrl->o_done[1], 1);
-    mbar_init(&ctrl->o_free, kSoftmaxWarps);
-    for (int d = 0; d < 3; ++d) mbar_init(&ctrl->mma_drain[d], 1);
+    mbar_init(&ctrl->o_done[0], kPvLanes);
+    mbar_init(&ctrl->o_done[1], kPvLanes);
+    // final commits: the MMA warp's issuing lanes, the PV lanes, the second
+    // QK warp
+    mbar_init(&ctrl->mma_drain[0], MT::kQkLanes);
+    mbar_init(&ctrl->mma_drain[1], kPvLanes);
+    mbar_init(&ctrl->mma_drain[2], 1);
     ctrl->abort_flag = 0;
     fence_mbar_init();
   }
@@ -635,61 +653,6 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
       wk.init(prefix, S, g0);
       int32_t issued = 0;
       bool failed = false;
-      // Quantised caches: this warp's lane 0 also issues PV (O^T += V^T P^T,
-      // 4 x 4 MMAs over the staged tile; see the MMA role), serving every P
-      // that is ready whenever it waits for a raw slot, and the rest after
-      // its last copy.
-      Walker pv_wk;
-      int32_t pv = 0, pv_seg = -1;
-      if constexpr (MT::kPvInProducer) pv_wk.init(prefix, S, g0);
-      auto try_pv = [&]() -> bool {
-        if (pv >= ntiles) return false;
-        const int st = pv % kNumStages;
-        const bool first = (pv == 0) || (pv_wk.lt == 0);
-        const int32_t sg = first ? pv_seg + 1 : pv_seg;
-        if (!mbar_poll(&ctrl->p_full[pv & 1], (pv >> 1) & 1) ||
-            (first && sg > 0 && !mbar_poll(&ctrl->o_free, (sg - 1) & 1)))
-          return false;
-        tc_fence_after();
-        const uint32_t idesc_pv = make_idesc_bf16(128, static_cast<uint32_t>(NP), true, false);
-        const uint64_t a0 = make_smem_desc(smem_u32(sStage + st * kTileBytes), kChunkBytes, 1024,
-                                           kSmemLayoutSW128);
-        const uint64_t b0 = make_smem_desc(smem_u32(sStage + st * kTileBytes + kPChunkOffset), 16,
-                                           1024, kSmemLayoutSW128);
-#pragma unroll
-        for (int mt = 0; mt < 4; ++mt) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_bf16_ss(tmem + MT::kColO + mt * NP, a0 + ((2 * mt * kChunkBytes + kk * 2048) >> 4),
-                        b0 + ((kk * 32) >> 4), idesc_pv, (first && kk == 0) ? 0u : 1u);
-        }
-        // o_done before empty: a stage seen free implies its PV seen done
-        mma_commit(&ctrl->o_done[pv & 1]);
-        mma_commit(&ctrl->empty[st]);
-        pv_seg = sg;
-        pv_wk.next(prefix, S);
-        ++pv;
-        return true;
-      };
-      // warp-wide wait for a raw slot, lane 0 issuing ready PVs meanwhile
-      // (polled with a short sleep: measured faster than suspending on the
-      // slot's barrier between looks at P)
-      auto wait_serving_pv = [&](uint64_t* bar, uint32_t par) -> bool {
-        if constexpr (!MT::kPvInProducer) return warp_wait(bar, par, abort_flag);
-        uint64_t t_last = globaltimer_ns();
-        while (!__shfl_sync(0xffffffffu, mbar_poll(bar, par), 0)) {
-          bool progressed = false;
-          if (lane == 0) progressed = try_pv();
-          if (__shfl_sync(0xffffffffu, progressed, 0)) {
-            t_last = globaltimer_ns();
-          } else if (*abort_flag || globaltimer_ns() - t_last > kWaitLimitNs) {
-            return false;
-          } else {
-            __nanosleep(20);
-          }
-        }
-        return true;
-      };
       for (int32_t i = 0; i < ntiles; ++i) {
         const int stage = i % kNumStages;
         const uint32_t reuse_parity = ((i / kNumStages) - 1) & 1;
@@ -797,7 +760,7 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
                                MT::kRowBytes;
               bytes = static_cast<uint32_t>((nvalid + 7) & ~7) * MT::kRowBytes;
             }
-            if (i >= MT::kRawSlots && !wait_serving_pv(reuse_bar, reuse_par)) {
+            if (i >= MT::kRawSlots && !warp_wait(reuse_bar, reuse_par, abort_flag)) {
               failed = true;
               break;
             }
@@ -815,7 +778,7 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
             const TilePieces tp = describe_tile(p, b, j, wk.lt, lane, max_tokens);
             const uint64_t mask = tile_mask(tp);
             if (lane == 0 && tp.bad) set_status(p.status, tp.bad);
-            if (i >= MT::kRawSlots && !wait_serving_pv(reuse_bar, reuse_par)) {
+            if (i >= MT::kRawSlots && !warp_wait(reuse_bar, reuse_par, abort_flag)) {
               failed = true;
               break;
             }
@@ -849,34 +812,9 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
         ++issued;
         wk.next(prefix, S);
       }
-      if constexpr (MT::kPvInProducer) {
-        // the PVs after the last copy
-        if (lane == 0 && !failed) {
-          uint64_t t_last = globaltimer_ns();
-          while (pv < ntiles) {
-            if (try_pv()) {
-              t_last = globaltimer_ns();
-            } else if (*abort_flag || globaltimer_ns() - t_last > kWaitLimitNs) {
-              failed = true;
-              break;
-            } else {
-              __nanosleep(20);
-            }
-          }
-        }
-        failed = __shfl_sync(0xffffffffu, failed, 0);
-      }
       if (failed && lane == 0) {
         set_status(p.status, MLA_STATUS_TIMEOUT);
         ctrl->abort_flag = 1;
-      }
-      if constexpr (MT::kPvInProducer) {
-        // every PV issued here completes before tensor memory is released
-        if (lane == 0) {
-          mma_commit(&ctrl->mma_drain[1]);
-          (void)mbar_wait(&ctrl->mma_drain[1], 0, nullptr, kWaitLimitNs);
-        }
-        __syncwarp();
       }
       // drain: everything this warp issued has landed before the CTA exits
       if (lane == 0) {
@@ -891,37 +829,25 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
         }
       }
       __syncwarp();
-    } else if (warp == kMmaWarp || warp == MT::kPvWarp ||
-               (MT::kSplitQK && warp == MT::kQk2Warp)) {
-      // ================================================================= MMA
+    } else if (warp == kMmaWarp || (MT::kSplitQK && warp == MT::kQk2Warp)) {
+      // =================================================================== QK
+      // Issuer(s) of S = q_hat . rows (or of one half of its K range, each
+      // into an S accumulator of its own): lane 0 of this warp, lanes 0 and
+      // 1 when QK is split over lanes, or lane 0 of the second QK warp.  QK(t)
+      // goes out once tile t is staged, the stream's q_hat is in TMEM and the
+      // softmax has read S(t-1).
       const uint32_t idesc_qk = make_idesc_bf16(64, 64, false, false);
-      const uint32_t idesc_pv = make_idesc_bf16(128, static_cast<uint32_t>(NP), true, false);
       // Descriptors at the buffers' bases; an operand at byte offset x is
       // base + (x >> 4) (the start-address field holds address >> 4 and the
       // whole buffer lies below 256 KB, so the field never carries).
       const uint64_t qk_b0 = make_smem_desc(smem_u32(sStage), 16, 1024, kSmemLayoutSW128);
-      const uint64_t pv_a0 = make_smem_desc(smem_u32(sStage), kChunkBytes, 1024, kSmemLayoutSW128);
-      const uint64_t pv_b0 = make_smem_desc(smem_u32(sStage + kPChunkOffset), 16, 1024,
-                                            kSmemLayoutSW128);
-      // multi-token mode: QK's RoPE steps read A (64 M-rows x 64 values, K-major)
+      // q_hat's RoPE part as QK's A operand (64 M-rows x 64 values, K-major)
       const uint64_t qr_a0 = make_smem_desc(smem_u32(sQr), 16, 1024, kSmemLayoutSW128);
-      // PV(j): O^T += V^T P^T over the staged tile j (4 x 4 MMAs); it releases
-      // the stage and completes o_done[j % 2].
-      auto issue_pv = [&](int st, bool first) {
-        const uint64_t a0 = pv_a0 + static_cast<uint64_t>((st * kTileBytes) >> 4);
-        const uint64_t b0 = pv_b0 + static_cast<uint64_t>((st * kTileBytes) >> 4);
-#pragma unroll
-        for (int mt = 0; mt < 4; ++mt) {
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_bf16_ss(tmem + MT::kColO + mt * NP, a0 + ((2 * mt * kChunkBytes + kk * 2048) >> 4),
-                        b0 + ((kk * 32) >> 4), idesc_pv, (first && kk == 0) ? 0u : 1u);
-        }
-      };
       // QK(j) over chunks [c0, c1) of the staged rows into the S accumulator
-      // at column `col` (A = q_hat from TMEM, 4 MMAs per chunk), then, with
-      // `rope`, the RoPE chunk with A = q_hat's RoPE part in shared memory.
-      auto issue_qk = [&](int st, int c0, int c1, uint32_t col, bool rope) {
+      // at column `col` (A = q_hat from TMEM, 4 MMAs per chunk), then the
+      // RoPE chunk's K steps [k0, k1) with A = q_hat's RoPE part in shared
+      // memory (or from TMEM when it is there).
+      auto issue_qk = [&](int st, int c0, int c1, uint32_t col, int k0, int k1) {
         const uint64_t b0 = qk_b0 + static_cast<uint64_t>((st * kTileBytes) >> 4);
         for (int ch = c0; ch < c1; ++ch) {
 #pragma unroll
@@ -930,163 +856,75 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
                         b0 + ((ch * kChunkBytes + k * 32) >> 4), idesc_qk,
                         (ch > c0 || k > 0) ? 1u : 0u);
         }
-        if (rope) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
+        if constexpr (MT::kQRopeSmem) {
+          for (int k = k0; k < k1; ++k)
             mma_bf16_ss(tmem + col, qr_a0 + ((k * 32) >> 4),
                         b0 + (((kChunks - 1) * kChunkBytes + k * 32) >> 4), idesc_qk,
-                        (c1 > c0 || k > 0) ? 1u : 0u);
+                        (c1 > c0 || k > k0) ? 1u : 0u);
         }
       };
-      // This issuer's share of QK: all of it (S), or half of its K range
-      // (chunks 0-3 into S_a; 4-7 and the RoPE chunk into S_b).
+      // An issuer's share of QK: all of it into S, or half of its K range
+      // (`second` picks the half: chunks 0-3 and RoPE steps 0-1 into S_a,
+      // chunks 4-7 and RoPE steps 2-3 into S_b).
       auto issue_my_qk = [&](int st, bool second) {
-        if constexpr (MT::kSplitQK) {
-          if (!second) issue_qk(st, 0, 4, MT::kColS, false);
-          else issue_qk(st, 4, kChunks - 1, MT::kColS2, true);
+        if constexpr (MT::kSplitS) {
+          const int c0 = second ? 4 : 0;
+          issue_qk(st, c0, c0 + 4, second ? MT::kColS2 : MT::kColS, second ? 2 : 0, second ? 4 : 2);
         } else {
-          issue_qk(st, 0, MT::kQTmemChunks, MT::kColS, MT::kQRopeSmem);
+          issue_qk(st, 0, MT::kQTmemChunks, MT::kColS, 0, 4);
         }
       };
-      // Polls until `ready()` holds; false on abort or after the time limit.
-      auto wait_until = [&](auto ready) -> bool {
-        if (ready()) return true;
-        const uint64_t t0 = globaltimer_ns();
-        while (!ready()) {
-          if (*abort_flag || globaltimer_ns() - t0 > kWaitLimitNs) return false;
-          __nanosleep(20);
-        }
-        return true;
-      };
+      const int role = warp == kMmaWarp ? 0 : 2;    // index of the drain barrier
+      const int nl = warp == kMmaWarp ? MT::kQkLanes : 1;
+      const uint32_t gmask = (1u << nl) - 1u;
       bool failed = false;
-      if constexpr (!MT::kSingleIssuer) {
-        // Two issuers: this warp's lane 0 issues QK(qk) once its tile, the
-        // stream's q_hat and the S buffer are ready; the PV warp's lane 0
-        // issues PV(pv) once P(pv) is written (and, opening a segment, once
-        // the previous segment's epilogue has read O^T).  Padded head rows
-        // of P hold stale RoPE bytes: they only reach O^T columns that are
-        // never read.
-        // role 0: QK (or its first half), 1: PV, 2: the second half of QK
-        const int role = warp == kMmaWarp ? 0 : (warp == MT::kPvWarp ? 1 : 2);
-        if (lane == 0) {
-          Walker wk;
-          wk.init(prefix, S, g0);
-          int32_t seg = -1;
-          for (int32_t t = 0; t < ntiles; ++t) {
-            const int st = t % kNumStages;
-            const bool first = (t == 0) || (wk.lt == 0);
-            const int32_t sg = first ? seg + 1 : seg;
-            if (role != 1) {
-              if (!wait_until([&] {
-                    return (!first || mbar_poll(&ctrl->q_ready, sg & 1)) &&
-                           mbar_poll(&ctrl->full[st], (t / kNumStages) & 1) &&
-                           (t < 1 || mbar_poll(&ctrl->s_free, (t - 1) & 1));
-                  })) {
-                failed = true;
-                break;
-              }
-              tc_fence_after();
-              issue_my_qk(st, role == 2);
-              mma_commit(&ctrl->s_full);
-            } else {
-              if (!wait_until([&] {
-                    return mbar_poll(&ctrl->p_full[t & 1], (t >> 1) & 1) &&
-                           (!first || sg == 0 || mbar_poll(&ctrl->o_free, (sg - 1) & 1));
-                  })) {
-                failed = true;
-                break;
-              }
-              tc_fence_after();
-              issue_pv(st, first);
-              // o_done before empty: a stage seen free implies its PV seen done
-              mma_commit(&ctrl->o_done[t & 1]);
-              mma_commit(&ctrl->empty[st]);
+      if (lane < nl) {
+        // polled by lane 0 with a short sleep (measured to wake sooner than a
+        // suspending mbarrier.try_wait); the other issuing lane follows it
+        auto ready = [&](int32_t t, int st, bool first, int32_t sg) -> bool {
+          bool r = false;
+          if (lane == 0)
+            r = (!first || mbar_poll(&ctrl->q_ready, sg & 1)) &&
+                mbar_poll(&ctrl->full[st], (t / kNumStages) & 1) &&
+                (t < 1 || mbar_poll(&ctrl->s_free, (t - 1) & 1));
+          return __shfl_sync(gmask, r, 0);
+        };
+        Walker wk;
+        wk.init(prefix, S, g0);
+        int32_t seg = -1;
+        for (int32_t t = 0; t < ntiles; ++t) {
+          const int st = t % kNumStages;
+          const bool first = (t == 0) || (wk.lt == 0);
+          const int32_t sg = first ? seg + 1 : seg;
+          if (!ready(t, st, first, sg)) {
+            const uint64_t t0 = globaltimer_ns();
+            bool ok = false;
+            while (true) {
+              __nanosleep(20);
+              if (ready(t, st, first, sg)) { ok = true; break; }
+              if (__shfl_sync(gmask, *abort_flag || globaltimer_ns() - t0 > kWaitLimitNs, 0)) break;
             }
-            seg = sg;
-            wk.next(prefix, S);
-          }
-        }
-        __syncwarp();
-        if (failed && lane == 0) {
-          set_status(p.status, MLA_STATUS_TIMEOUT);
-          ctrl->abort_flag = 1;
-        }
-        // drain: every issued MMA completes before tensor memory is released
-        if (lane == 0) {
-          mma_commit(&ctrl->mma_drain[role]);
-          (void)mbar_wait(&ctrl->mma_drain[role], 0, nullptr, kWaitLimitNs);
-        }
-        __syncwarp();
-      } else {
-        // Single-thread event loop: issue PV(pv) as soon as its P is written
-        // (checked first: it releases a stage), and QK(qk) once its tile, the
-        // stream's q_hat and the S buffer are ready, at most two tiles ahead
-        // of PV.  Padded head rows of P hold stale RoPE bytes: they only reach
-        // O^T columns that are never read.
-        if (lane == 0) {
-          Walker wq, wp;
-          wq.init(prefix, S, g0);
-          wp.init(prefix, S, g0);
-          int32_t qk = 0, pv = 0, seg_q = -1, seg_p = -1;
-          uint64_t t_last = globaltimer_ns();
-          while (pv < ntiles) {
-            bool progressed = false;
-            if (pv < qk) {
-              const int st = pv % kNumStages;
-              const bool first = (pv == 0) || (wp.lt == 0);
-              const int32_t sp = first ? seg_p + 1 : seg_p;
-              const bool ready = mbar_poll(&ctrl->p_full[pv & 1], (pv >> 1) & 1) &&
-                                 (!first || sp == 0 || mbar_poll(&ctrl->o_free, (sp - 1) & 1));
-              if (ready) {
-                seg_p = sp;
-                tc_fence_after();
-                issue_pv(st, first);
-                mma_commit(&ctrl->o_done[pv & 1]);
-                mma_commit(&ctrl->empty[st]);
-                wp.next(prefix, S);
-                ++pv;
-                progressed = true;
-              }
-            }
-            if (qk < ntiles && qk - pv < 2) {
-              const int st = qk % kNumStages;
-              const bool first = (qk == 0) || (wq.lt == 0);
-              const int32_t sq = first ? seg_q + 1 : seg_q;
-              const bool ready = (!first || mbar_poll(&ctrl->q_ready, sq & 1)) &&
-                                 mbar_poll(&ctrl->full[st], (qk / kNumStages) & 1) &&
-                                 (qk < 1 || mbar_poll(&ctrl->s_free, (qk - 1) & 1));
-              if (ready) {
-                seg_q = sq;
-                tc_fence_after();
-                issue_my_qk(st, false);
-                mma_commit(&ctrl->s_full);
-                wq.next(prefix, S);
-                ++qk;
-                progressed = true;
-              }
-            }
-            if (progressed) {
-              t_last = globaltimer_ns();
-            } else if (*abort_flag || globaltimer_ns() - t_last > kWaitLimitNs) {
+            if (!ok) {
               failed = true;
               break;
-            } else {
-              __nanosleep(20);   // back off: polling shares the SM with the math
             }
           }
+          tc_fence_after();
+          issue_my_qk(st, warp != kMmaWarp || lane == 1);
+          mma_commit(&ctrl->s_full);
+          seg = sg;
+          wk.next(prefix, S);
         }
-        __syncwarp();
-        if (failed && lane == 0) {
-          set_status(p.status, MLA_STATUS_TIMEOUT);
-          ctrl->abort_flag = 1;
-        }
-        // drain: every issued MMA completes before tensor memory is released
-        if (lane == 0) {
-          mma_commit(&ctrl->mma_drain[0]);
-          (void)mbar_wait(&ctrl->mma_drain[0], 0, nullptr, kWaitLimitNs);
-        }
-        __syncwarp();
       }
+      __syncwarp();
+      if (failed && lane == 0) {
+        set_status(p.status, MLA_STATUS_TIMEOUT);
+        ctrl->abort_flag = 1;
+      }
+      // drain: every issued MMA completes before tensor memory is released
+      if (lane < nl) mma_commit(&ctrl->mma_drain[role]);
+      if (lane == 0) (void)mbar_wait(&ctrl->mma_drain[role], 0, nullptr, kWaitLimitNs);
+      __syncwarp();
     } else if (MT::kQuant && warp >= kDequantWarp0) {
       // ============================================================ dequant
       // Thread t of the 192 owns row t % 64 and groups t / 64 + 3k: a warp
@@ -1309,6 +1147,11 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
       auto pv_done = [&](int32_t j) -> bool {
         return warp_wait(&ctrl->o_done[j & 1], (j >> 1) & 1, abort_flag);
       };
+      // PV operands: A = the staged tile read MN-major (V^T), B = its P
+      const uint32_t idesc_pv = make_idesc_bf16(128, static_cast<uint32_t>(NP), true, false);
+      const uint64_t pv_a0 = make_smem_desc(smem_u32(sStage), kChunkBytes, 1024, kSmemLayoutSW128);
+      const uint64_t pv_b0 = make_smem_desc(smem_u32(sStage + kPChunkOffset), 16, 1024,
+                                            kSmemLayoutSW128);
       // q_hat / o_lat rows of row set s and how many there are
       auto first_row = [&](int32_t s) -> int64_t {
         const StreamGeom gm = stream_geom(s, p.q_len, G);
@@ -1360,28 +1203,49 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
           tc_fence_after();
           float y[32];
           if (warp_has_heads) {
-            uint32_t r[32];
-            tmem_ld32(tmem + lane_base + MT::kColS, r);
+            {
+              uint32_t r[32];
+              tmem_ld32(tmem + lane_base + MT::kColS, r);
 #pragma unroll
-            for (int t = 0; t < 32; ++t) y[t] = __uint_as_float(r[t]);
-            if constexpr (MT::kSplitQK) {   // S = S_a + S_b
-              tmem_ld32(tmem + lane_base + MT::kColS2, r);
+              for (int t = 0; t < 32; ++t) y[t] = __uint_as_float(r[t]);
+              if constexpr (MT::kSplitS) {   // S = S_a + S_b
+                tmem_ld32(tmem + lane_base + MT::kColS2, r);
 #pragma unroll
-              for (int t = 0; t < 32; ++t) y[t] += __uint_as_float(r[t]);
-            }
-            float z[32];
-            tmem_ld32(tmem + lane_base + MT::kColS + 32, r);
+                for (int t = 0; t < 32; ++t) y[t] += __uint_as_float(r[t]);
+              }
+              if constexpr (MT::kSplitS && kThreads > 256) {
+                // fewer registers per thread: columns 32..63 in two halves
 #pragma unroll
-            for (int t = 0; t < 32; ++t) z[t] = __uint_as_float(r[t]);
-            if constexpr (MT::kSplitQK) {
-              tmem_ld32(tmem + lane_base + MT::kColS2 + 32, r);
+                for (int q = 0; q < 2; ++q) {
+                  uint32_t a[16];
+                  float z[16];
+                  tmem_ld16(tmem + lane_base + MT::kColS + 32 + 16 * q, a);
 #pragma unroll
-              for (int t = 0; t < 32; ++t) z[t] += __uint_as_float(r[t]);
-            }
+                  for (int e = 0; e < 16; ++e) z[e] = __uint_as_float(a[e]);
+                  tmem_ld16(tmem + lane_base + MT::kColS2 + 32 + 16 * q, a);
 #pragma unroll
-            for (int t = 0; t < 32; ++t) {
-              const float hi_col = __shfl_xor_sync(0xffffffffu, z[t], 16);
-              if (half) y[t] = hi_col;   // lane l+16 <- columns 32..63 of lane l
+                  for (int e = 0; e < 16; ++e) {
+                    z[e] += __uint_as_float(a[e]);
+                    const float hi_col = __shfl_xor_sync(0xffffffffu, z[e], 16);
+                    if (half) y[16 * q + e] = hi_col;   // lane l+16 <- columns 32..63 of lane l
+                  }
+                }
+              } else {
+                float z[32];
+                tmem_ld32(tmem + lane_base + MT::kColS + 32, r);
+#pragma unroll
+                for (int t = 0; t < 32; ++t) z[t] = __uint_as_float(r[t]);
+                if constexpr (MT::kSplitS) {
+                  tmem_ld32(tmem + lane_base + MT::kColS2 + 32, r);
+#pragma unroll
+                  for (int t = 0; t < 32; ++t) z[t] += __uint_as_float(r[t]);
+                }
+#pragma unroll
+                for (int t = 0; t < 32; ++t) {
+                  const float hi_col = __shfl_xor_sync(0xffffffffu, z[t], 16);
+                  if (half) y[t] = hi_col;   // lane l+16 <- columns 32..63 of lane l
+                }
+              }
             }
           }
           tc_fence_before();
@@ -1473,11 +1337,19 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
             }
           }
         }
+        // A segment ends at this tile: its epilogue waits for PV(i), which
+        // shares o_done[i % 2] with PV(i-2).  A parity wait cannot tell a
+        // phase from the one two later, so every warp awaits PV(i-2) before
+        // the warps meet and PV(i) is issued (PV(i-4) is complete: the stage
+        // tile i fills was released by PV(i-3)).
+        if (last && i >= 2 && ok) ok = pv_done(i - 2);
+        // P(i) and the zeroed dead rows are generic stores the tensor core
+        // reads: fenced by their writers before the warps meet
+        fence_proxy_async_smem();
         if (named_bar_or(1, 128, !ok)) { failed = true; break; }
         if (!first && ctrl->rescale_tile[pb] == i) {
           // every earlier PV has completed before O^T is rescaled in place
           ok = (i < 2 || pv_done(i - 2)) && pv_done(i - 1);
-          failed = !ok;
           if (ok) {
             tc_fence_after();
             for (int mt = 0; mt < 4; ++mt) {
@@ -1495,18 +1367,26 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
               }
             }
           }
+          // the rescaled O^T is in place before PV(i) adds to it
+          tc_fence_before();
+          if (named_bar_or(1, 128, !ok)) { failed = true; break; }
         }
-        // A segment ends here: its epilogue waits for PV(i), which shares
-        // o_done[i % 2] with PV(i-2); PV(i-2) is awaited first (PV(i-4) is
-        // complete: the stage tile i fills was released by PV(i-3)).
-        if (last && i >= 2 && !failed) {
-          ok = pv_done(i - 2);
-          if (!ok) failed = true;
+        if (w == 0) {
+          // PV(i): lanes 0-3 of this warp (which holds no rows) each issue
+          // one 128-dim block of O^T += V^T P^T over the staged tile, then
+          // commit it to o_done[i % 2] and to the stage's empty barrier
+          // (o_done first: a stage seen free implies its PV seen done).
+          if (lane < kPvLanes) {
+            tc_fence_after();
+            issue_pv_block(tmem + MT::kColO + lane * NP,
+                           pv_a0 + static_cast<uint64_t>((stage * kTileBytes) >> 4),
+                           pv_b0 + static_cast<uint64_t>((stage * kTileBytes) >> 4), idesc_pv,
+                           lane, first);
+            mma_commit(&ctrl->o_done[i & 1]);
+            mma_commit(&ctrl->empty[stage]);
+          }
+          __syncwarp();
         }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ctrl->p_full[pb]);
         if (last) {
           // ---- segment epilogue
           ok = !failed && pv_done(i);   // PVs complete in order: all of them
@@ -1539,15 +1419,21 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
               }
             }
           }
+          // O^T is read before the next PV (issued after the warps next
+          // meet) overwrites it
           tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&ctrl->o_free);
         }
         wk.next(prefix, S);
       }
       if (failed && lane == 0) {
         set_status(p.status, MLA_STATUS_TIMEOUT);
         ctrl->abort_flag = 1;
+      }
+      // drain: every PV issued here completes before tensor memory is released
+      if (w == 0) {
+        if (lane < kPvLanes) mma_commit(&ctrl->mma_drain[1]);
+        if (lane == 0) (void)mbar_wait(&ctrl->mma_drain[1], 0, nullptr, kWaitLimitNs);
+        __syncwarp();
       }
     }
   }
