@@ -198,7 +198,7 @@ int validate_problem(const mla_problem* pr) {
     const int64_t longest = pr->topk_width > 0
                                 ? pr->topk_width
                                 : static_cast<int64_t>(pr->max_pages_per_seq) * pr->page_size;
-    const int64_t per_stream = (longest + kTile - 1) / kTile * kTileCost + kStreamCost;
+    const int64_t per_stream = (longest + kTile - 1) / kTile * kTileCost + kStreamCostMax;
     if (static_cast<int64_t>(pr->batch) * pr->q_len * per_stream > INT32_MAX)
       return MLA_ERR_UNSUPPORTED;
   }
@@ -239,6 +239,7 @@ void fill_combine_params(const mla_plan& plan, const uint8_t* ws, const int32_t*
   p.rows = p.group * pr.num_heads;
   p.num_streams = plan.num_streams;
   p.num_ctas = plan.num_ctas;
+  p.stream_cost = stream_cost_of_mode(decode_mode(pr));
 }
 
 int absorb(const mla_plan& plan, const void* q, const void* w_uk, void* q_hat, cudaStream_t st) {
@@ -329,6 +330,7 @@ int launch_attention(const mla_plan& plan, const void* q_hat, const void* kv_cac
   p.causal = pr.causal;
   p.num_streams = plan.num_streams;
   p.num_ctas = plan.num_ctas;
+  p.stream_cost = stream_cost_of_mode(mode);
   p.scale_log2 = pr.sm_scale * 1.4426950408889634f;
   return launch_decode(p, &kv_map, mode, st) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }

@@ -52,7 +52,7 @@ __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(const Comb
     const StreamGeom gt = stream_geom(t, p.q_len, p.group);
     const int32_t len = stream_len(p.seq_lens[gt.b], p.q_len, gt.j0 + gt.nq - 1, p.causal,
                                    p.topk_width, max_tokens);
-    const int64_t n = stream_cost((len + kTile - 1) / kTile);
+    const int64_t n = stream_cost((len + kTile - 1) / kTile, p.stream_cost);
     tot += n;
     if (t < s) before += n;
   }
@@ -73,8 +73,9 @@ __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(const Comb
                                  p.topk_width, max_tokens);
   const int64_t ntiles = (len + kTile - 1) / kTile;
   if (ntiles == 0) return;   // the decode wrote o_lat = 0, lse = -inf
-  const int c0 = tile_owner(tile_cost_pos(before, 0), tot, p.num_ctas);
-  const int c1 = tile_owner(tile_cost_pos(before, static_cast<int32_t>(ntiles - 1)), tot, p.num_ctas);
+  const int c0 = tile_owner(tile_cost_pos(before, 0, p.stream_cost), tot, p.num_ctas);
+  const int c1 = tile_owner(tile_cost_pos(before, static_cast<int32_t>(ntiles - 1), p.stream_cost),
+                            tot, p.num_ctas);
   if (c0 == c1) return;      // one CTA held the whole row set: its result is final
   const int nseg = c1 - c0 + 1;
   // One pass over the partials, 8 at a time (their lse values and this

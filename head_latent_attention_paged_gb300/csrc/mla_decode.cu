@@ -168,9 +168,9 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 }
 
 // First global tile (in stream order) whose cost position is >= u; tile and
-// cost prefixes over the S streams, U = cost[S].
+// cost prefixes over the S streams, U = cost[S], sc a stream's fixed cost.
 __device__ __forceinline__ int32_t first_tile_at(const int32_t* tiles, const int32_t* cost,
-                                                 int32_t S, int32_t u) {
+                                                 int32_t S, int32_t u, int32_t sc) {
   if (u >= cost[S]) return tiles[S];
   int32_t lo = 0, hi = S;                 // largest s with cost[s] <= u
   while (hi - lo > 1) {
@@ -178,7 +178,7 @@ __device__ __forceinline__ int32_t first_tile_at(const int32_t* tiles, const int
     if (cost[mid] <= u) lo = mid; else hi = mid;
   }
   const int32_t off = u - cost[lo];
-  const int32_t k = off <= kStreamCost ? 0 : (off - kStreamCost + kTileCost - 1) / kTileCost;
+  const int32_t k = off <= sc ? 0 : (off - sc + kTileCost - 1) / kTileCost;
   return (k < tiles[lo + 1] - tiles[lo]) ? tiles[lo] + k : tiles[lo + 1];
 }
 
@@ -612,7 +612,7 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
                                    p.topk_width, max_tokens);
     const int32_t nt = (len + kTile - 1) / kTile;
     prefix[s + 1] = nt;
-    cprefix[s + 1] = stream_cost(nt);
+    cprefix[s + 1] = stream_cost(nt, p.stream_cost);
   }
   __syncthreads();
   if (warp < 2) {   // exclusive prefix sums: warp 0 of tiles, warp 1 of cost
@@ -639,9 +639,11 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
   const int32_t ucost = cprefix[S];
   const int32_t c = blockIdx.x;
   const int32_t g0 = first_tile_at(
-      prefix, cprefix, S, static_cast<int32_t>((static_cast<int64_t>(c) * ucost) / p.num_ctas));
+      prefix, cprefix, S, static_cast<int32_t>((static_cast<int64_t>(c) * ucost) / p.num_ctas),
+      p.stream_cost);
   const int32_t g1 = first_tile_at(
-      prefix, cprefix, S, static_cast<int32_t>((static_cast<int64_t>(c + 1) * ucost) / p.num_ctas));
+      prefix, cprefix, S, static_cast<int32_t>((static_cast<int64_t>(c + 1) * ucost) / p.num_ctas),
+      p.stream_cost);
   const int32_t ntiles = g1 - g0;
   const uint32_t tmem = ctrl->tmem_base;
 
@@ -1391,9 +1393,11 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
           // ---- segment epilogue
           ok = !failed && pv_done(i);   // PVs complete in order: all of them
           const int32_t s = wk.s;
-          const int32_t c_first = tile_owner(tile_cost_pos(cprefix[s], 0), ucost, p.num_ctas);
+          const int32_t c_first =
+              tile_owner(tile_cost_pos(cprefix[s], 0, p.stream_cost), ucost, p.num_ctas);
           const int32_t c_last = tile_owner(
-              tile_cost_pos(cprefix[s], prefix[s + 1] - prefix[s] - 1), ucost, p.num_ctas);
+              tile_cost_pos(cprefix[s], prefix[s + 1] - prefix[s] - 1, p.stream_cost), ucost,
+              p.num_ctas);
           const bool split = c_first != c_last;
           // an unsplit stream's result is final: straight to the outputs
           // (partial slots hold RMAX rows each)

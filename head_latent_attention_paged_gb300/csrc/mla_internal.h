@@ -62,6 +62,7 @@ struct DecodeParams {
   int32_t rows;                 // rows of a full row set: group * heads
   int32_t page_size, num_pages, max_pages, topk_width, causal;
   int32_t num_streams, num_ctas;
+  int32_t stream_cost;          // a stream's fixed cost in the work split (stream_cost_of_mode)
   float scale_log2;             // sm_scale * log2(e)
 };
 
@@ -83,7 +84,7 @@ struct CombineParams {
   float* lse;
   int32_t batch, q_len, heads, page_size, max_pages, topk_width, causal;
   int32_t group, rows;          // as in DecodeParams
-  int32_t num_streams, num_ctas;
+  int32_t num_streams, num_ctas, stream_cost;
 };
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
 
@@ -174,20 +175,31 @@ __host__ __device__ inline int32_t stream_len(int32_t seq_len, int32_t q_len, in
 }
 
 // Work split.  Every tile gets a cost position: a stream with n > 0 tiles
-// spans kStreamCost + n * kTileCost cost units, its fixed overhead (query
-// load into TMEM, epilogue) first, then one kTileCost slot per tile, so tile
-// k of a stream starting at cost pc sits at pc + kStreamCost + k * kTileCost.
-// CTA c takes the tiles whose position lies in [c*U/C, (c+1)*U/C) for U the
-// total cost: a CTA that opens more streams gets fewer tiles.
+// spans sc + n * kTileCost cost units, its fixed overhead sc (query load into
+// TMEM, epilogue, the pipeline refill behind them) first, then one kTileCost
+// slot per tile, so tile k of a stream starting at cost pc sits at pc + sc +
+// k * kTileCost.  CTA c takes the tiles whose position lies in [c*U/C,
+// (c+1)*U/C) for U the total cost: a CTA that opens more streams gets fewer
+// tiles.  The overhead was measured at about three tile times in the kernels
+// over bf16 caches and about two in those over quantised caches, whose tiles
+// take longer.
 constexpr int32_t kTileCost = 4;
-constexpr int32_t kStreamCost = 7;
+constexpr int32_t kStreamCostBf16 = 13;
+constexpr int32_t kStreamCostQuant = 8;
+constexpr int32_t kStreamCostMax = 13;
 
-__host__ __device__ inline int32_t stream_cost(int32_t ntiles) {
-  return ntiles > 0 ? kStreamCost + ntiles * kTileCost : 0;
+__host__ __device__ inline int32_t stream_cost_of_mode(int mode) {
+  return (mode == kModeDenseFp8 || mode == kModeDenseFp4 || mode == kModeDenseFp4Multi)
+             ? kStreamCostQuant
+             : kStreamCostBf16;
 }
 
-__host__ __device__ inline int64_t tile_cost_pos(int64_t stream_cost_start, int32_t k) {
-  return stream_cost_start + kStreamCost + static_cast<int64_t>(k) * kTileCost;
+__host__ __device__ inline int32_t stream_cost(int32_t ntiles, int32_t sc) {
+  return ntiles > 0 ? sc + ntiles * kTileCost : 0;
+}
+
+__host__ __device__ inline int64_t tile_cost_pos(int64_t stream_cost_start, int32_t k, int32_t sc) {
+  return stream_cost_start + sc + static_cast<int64_t>(k) * kTileCost;
 }
 
 // CTA that owns cost position x when `total` cost units are split over
