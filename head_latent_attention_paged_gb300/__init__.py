@@ -58,7 +58,7 @@ class MlaPlan(ctypes.Structure):
         ("problem", MlaProblem), ("num_streams", ctypes.c_int32), ("num_ctas", ctypes.c_int32),
         ("num_slots", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
         ("ws_partial_o", ctypes.c_int64), ("ws_partial_lse", ctypes.c_int64),
-        ("ws_counters", ctypes.c_int64), ("ws_status", ctypes.c_int64),
+        ("ws_prefix", ctypes.c_int64), ("ws_status", ctypes.c_int64),
         ("workspace_bytes", ctypes.c_int64),
         ("planned_tiles", ctypes.c_int64), ("ws_q_hat", ctypes.c_int64),
         ("split_tokens", ctypes.c_int32), ("sm_count", ctypes.c_int32),

@@ -15,7 +15,7 @@ using namespace mla;
 
 namespace {
 
-constexpr int kAbiVersion = 20000;   // 2.0.0
+constexpr int kAbiVersion = 20100;   // 2.1.0
 constexpr int64_t kAlign = 256;
 
 int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
@@ -219,6 +219,15 @@ int64_t stream_tiles_host(const mla_problem& pr, const int32_t* seq_lens) {
   return total;
 }
 
+// Whether the row-set prefixes of the work split come from the pre-pass
+// (too many row sets for the decode kernel's shared memory).
+bool prefix_in_workspace(const mla_plan& plan) {
+  const mla_problem& pr = plan.problem;
+  const int rows = group_of(pr) * pr.num_heads;
+  return !decode_layout(pr.num_heads, (rows + 15) / 16 * 16, plan.num_streams, decode_mode(pr))
+              .prefix_in_smem;
+}
+
 void fill_combine_params(const mla_plan& plan, const uint8_t* ws, const int32_t* seq_lens,
                          float* o_lat, float* lse, CombineParams* out) {
   const mla_problem& pr = plan.problem;
@@ -240,6 +249,8 @@ void fill_combine_params(const mla_plan& plan, const uint8_t* ws, const int32_t*
   p.num_streams = plan.num_streams;
   p.num_ctas = plan.num_ctas;
   p.stream_cost = stream_cost_of_mode(decode_mode(pr));
+  p.prefix_ws = prefix_in_workspace(plan) ? reinterpret_cast<const int32_t*>(ws + plan.ws_prefix)
+                                          : nullptr;
 }
 
 int absorb(const mla_plan& plan, const void* q, const void* w_uk, void* q_hat, cudaStream_t st) {
@@ -268,8 +279,8 @@ int plan_check(const mla_plan* plan) {
   if (plan->num_streams != num_row_sets(plan->problem) || plan->num_ctas < 1 || plan->sm_count < 1 ||
       plan->num_ctas > kMaxCtas || plan->num_slots != plan->num_streams + plan->num_ctas - 1 ||
       plan->ws_partial_o < 0 || plan->ws_partial_lse < plan->ws_partial_o ||
-      plan->ws_q_hat < plan->ws_partial_lse || plan->ws_counters < plan->ws_q_hat ||
-      plan->ws_status < plan->ws_counters || plan->ws_status + 4 > plan->workspace_bytes)
+      plan->ws_q_hat < plan->ws_partial_lse || plan->ws_prefix < plan->ws_q_hat ||
+      plan->ws_status < plan->ws_prefix + 8 * (static_cast<int64_t>(plan->num_streams) + 1) || plan->ws_status + 4 > plan->workspace_bytes)
     return MLA_ERR_INVALID_ARGUMENT;
   return MLA_OK;
 }
@@ -332,6 +343,11 @@ int launch_attention(const mla_plan& plan, const void* q_hat, const void* kv_cac
   p.num_ctas = plan.num_ctas;
   p.stream_cost = stream_cost_of_mode(mode);
   p.scale_log2 = pr.sm_scale * 1.4426950408889634f;
+  p.prefix_ws = nullptr;
+  if (prefix_in_workspace(plan)) {
+    p.prefix_ws = reinterpret_cast<int32_t*>(ws + plan.ws_prefix);
+    if (launch_prefix(p, st) != cudaSuccess) return MLA_ERR_CUDA;
+  }
   return launch_decode(p, &kv_map, mode, st) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
@@ -411,7 +427,7 @@ int mla_decode_plan(const mla_problem* problem, const int32_t* seq_lens_host, in
   pl.num_slots = pl.num_streams + pl.num_ctas - 1;
   if (pl.num_slots < 1) pl.num_slots = 1;
   pl.smem_bytes = decode_smem_bytes(pr.num_heads, heads_pad, pl.num_streams, decode_mode(pr));
-  if (pl.smem_bytes > 232448) return MLA_ERR_UNSUPPORTED;
+  if (pl.smem_bytes > kMaxSmemBytes) return MLA_ERR_UNSUPPORTED;
   int64_t off = 0;
   pl.ws_partial_o = off;
   off = align_up(off + static_cast<int64_t>(pl.num_slots) * rows * kDc * 4, kAlign);
@@ -419,8 +435,8 @@ int mla_decode_plan(const mla_problem* problem, const int32_t* seq_lens_host, in
   off = align_up(off + static_cast<int64_t>(pl.num_slots) * rows * 4, kAlign);
   pl.ws_q_hat = off;
   off = align_up(off + static_cast<int64_t>(pr.batch) * pr.q_len * pr.num_heads * kDqk * 2, kAlign);
-  pl.ws_counters = off;
-  off = align_up(off + static_cast<int64_t>(pl.num_streams) * 4, kAlign);
+  pl.ws_prefix = off;
+  off = align_up(off + 8 * (static_cast<int64_t>(pl.num_streams) + 1), kAlign);
   pl.ws_status = off;
   off = align_up(off + 4, kAlign);
   pl.workspace_bytes = off;

@@ -46,27 +46,34 @@ __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(const Comb
   const int S = p.num_streams;
   const int max_tokens = p.max_pages * p.page_size;
   __shared__ int64_t red64[2][kCombineThreads / 32];
-  // cost before stream s and in total (the decode grid's split)
+  // cost before stream s and in total (the decode grid's split): summed here
+  // while the decode runs, or read from the pre-pass's prefixes
   int64_t before = 0, tot = 0;
-  for (int t = tid; t < S; t += kCombineThreads) {
-    const StreamGeom gt = stream_geom(t, p.q_len, p.group);
-    const int32_t len = stream_len(p.seq_lens[gt.b], p.q_len, gt.j0 + gt.nq - 1, p.causal,
-                                   p.topk_width, max_tokens);
-    const int64_t n = stream_cost((len + kTile - 1) / kTile, p.stream_cost);
-    tot += n;
-    if (t < s) before += n;
-  }
+  if (p.prefix_ws == nullptr) {
+    for (int t = tid; t < S; t += kCombineThreads) {
+      const StreamGeom gt = stream_geom(t, p.q_len, p.group);
+      const int32_t len = stream_len(p.seq_lens[gt.b], p.q_len, gt.j0 + gt.nq - 1, p.causal,
+                                     p.topk_width, max_tokens);
+      const int64_t n = stream_cost((len + kTile - 1) / kTile, p.stream_cost);
+      tot += n;
+      if (t < s) before += n;
+    }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    before += __shfl_xor_sync(0xffffffffu, before, o);
-    tot += __shfl_xor_sync(0xffffffffu, tot, o);
-  }
-  if (lane == 0) { red64[0][warp] = before; red64[1][warp] = tot; }
-  __syncthreads();
-  before = tot = 0;
+    for (int o = 16; o > 0; o >>= 1) {
+      before += __shfl_xor_sync(0xffffffffu, before, o);
+      tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    }
+    if (lane == 0) { red64[0][warp] = before; red64[1][warp] = tot; }
+    __syncthreads();
+    before = tot = 0;
 #pragma unroll
-  for (int w = 0; w < kCombineThreads / 32; ++w) { before += red64[0][w]; tot += red64[1][w]; }
+    for (int w = 0; w < kCombineThreads / 32; ++w) { before += red64[0][w]; tot += red64[1][w]; }
+  }
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (p.prefix_ws != nullptr) {
+    before = p.prefix_ws[S + 1 + s];
+    tot = p.prefix_ws[S + 1 + S];
+  }
   const StreamGeom gm = stream_geom(s, p.q_len, p.group);
   if (h >= gm.nq * p.heads) return;   // a short last group of draft tokens
   const int32_t len = stream_len(p.seq_lens[gm.b], p.q_len, gm.j0 + gm.nq - 1, p.causal,
@@ -139,6 +146,83 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {
   cfg.numAttrs = 1;
   const cudaError_t err = cudaLaunchKernelEx(&cfg, mla_combine_kernel, p);
   if (err != cudaSuccess) return err;
+  return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------------------
+// Row-set prefixes for the work split (grids with more row sets than the
+// decode kernel keeps in shared memory): tiles[s] and cost[s] = tiles and
+// cost units of the row sets before s, for s = 0..S, in p.prefix_ws as
+// int32 [2][S + 1].  One block of 1024 threads scans 1024 row sets at a time.
+constexpr int kPrefixThreads = 1024;
+
+__global__ void __launch_bounds__(kPrefixThreads) mla_prefix_kernel(const DecodeParams p) {
+  __shared__ int32_t wsum[2][kPrefixThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int S = p.num_streams;
+  const int32_t max_tokens = p.max_pages * p.page_size;
+  int32_t* tiles = p.prefix_ws;
+  int32_t* cost = p.prefix_ws + S + 1;
+  if (tid == 0) {
+    tiles[0] = 0;
+    cost[0] = 0;
+  }
+  int32_t carry_t = 0, carry_c = 0;
+  for (int base = 0; base < S; base += kPrefixThreads) {
+    const int s = base + tid;
+    int32_t vt = 0, vc = 0;
+    if (s < S) {
+      const StreamGeom gm = stream_geom(s, p.q_len, p.group);
+      const int32_t len = stream_len(p.seq_lens[gm.b], p.q_len, gm.j0 + gm.nq - 1, p.causal,
+                                     p.topk_width, max_tokens);
+      vt = (len + kTile - 1) / kTile;
+      vc = stream_cost(vt, p.stream_cost);
+    }
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {   // inclusive scan within the warp
+      const int32_t nt = __shfl_up_sync(0xffffffffu, vt, o);
+      const int32_t nc = __shfl_up_sync(0xffffffffu, vc, o);
+      if (lane >= o) {
+        vt += nt;
+        vc += nc;
+      }
+    }
+    if (lane == 31) {
+      wsum[0][warp] = vt;
+      wsum[1][warp] = vc;
+    }
+    __syncthreads();
+    if (warp == 0) {   // inclusive scan of the warp totals
+      int32_t wt = wsum[0][lane], wc = wsum[1][lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t nt = __shfl_up_sync(0xffffffffu, wt, o);
+        const int32_t nc = __shfl_up_sync(0xffffffffu, wc, o);
+        if (lane >= o) {
+          wt += nt;
+          wc += nc;
+        }
+      }
+      wsum[0][lane] = wt;
+      wsum[1][lane] = wc;
+    }
+    __syncthreads();
+    if (warp > 0) {
+      vt += wsum[0][warp - 1];
+      vc += wsum[1][warp - 1];
+    }
+    if (s < S) {
+      tiles[s + 1] = carry_t + vt;
+      cost[s + 1] = carry_c + vc;
+    }
+    carry_t += wsum[0][kPrefixThreads / 32 - 1];
+    carry_c += wsum[1][kPrefixThreads / 32 - 1];
+    __syncthreads();   // wsum is rewritten by the next round
+  }
+}
+
+cudaError_t launch_prefix(const DecodeParams& p, cudaStream_t stream) {
+  mla_prefix_kernel<<<1, kPrefixThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -535,7 +535,12 @@ DecodeLayout decode_layout(int heads, int heads_pad, int num_streams, int mode) 
     L.off_qrope = raw_end;
     L.off_ctrl = raw_end + kQRopeBytes;
   }
-  L.total = L.off_ctrl + static_cast<int>(sizeof(Ctrl)) + 2 * (num_streams + 1) * 4;
+  // the row-set tile and cost prefixes, when they fit; else the pre-pass
+  // writes them to the workspace
+  const int base = L.off_ctrl + static_cast<int>(sizeof(Ctrl));
+  const int with_prefix = base + 2 * (num_streams + 1) * 4;
+  L.prefix_in_smem = num_streams <= kSmemStreams && with_prefix <= kMaxSmemBytes;
+  L.total = L.prefix_in_smem ? with_prefix : base;
   return L;
 }
 
@@ -553,8 +558,12 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
   uint8_t* sRaw = smem + L.off_raw;   // FP8 raw ring
   uint8_t* sQr = smem + L.off_qrope;  // RoPE part of q_hat (A operand base, M-row 0)
   Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + L.off_ctrl);
-  int32_t* prefix = reinterpret_cast<int32_t*>(smem + L.off_ctrl + sizeof(Ctrl));  // tiles
-  int32_t* cprefix = prefix + (p.num_streams + 1);                                   // cost
+  // the row sets' tile and cost prefixes: computed below into shared memory,
+  // or written to the workspace by the pre-pass this launch depends on
+  int32_t* prefix = p.prefix_ws != nullptr
+                        ? p.prefix_ws
+                        : reinterpret_cast<int32_t*>(smem + L.off_ctrl + sizeof(Ctrl));   // tiles
+  int32_t* cprefix = prefix + (p.num_streams + 1);                                         // cost
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -605,17 +614,23 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
     tmem_relinquish();
   }
   if (warp == kProducerWarp && lane == 0 && (MT::kDenseBf16 || MT::kSparse)) prefetch_tmap(&kv_map);
+  // A launch behind the prefix pre-pass waits for it here (a no-op for a
+  // launch that depends on nothing); nothing above reads memory a kernel
+  // before this one may write.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // tiles and cost per stream (stream lengths from the device seq_lens)
-  for (int s = tid; s < S; s += kThreads) {
-    const StreamGeom gm = stream_geom(s, p.q_len, G);
-    const int32_t len = stream_len(p.seq_lens[gm.b], p.q_len, gm.j0 + gm.nq - 1, p.causal,
-                                   p.topk_width, max_tokens);
-    const int32_t nt = (len + kTile - 1) / kTile;
-    prefix[s + 1] = nt;
-    cprefix[s + 1] = stream_cost(nt, p.stream_cost);
+  if (p.prefix_ws == nullptr) {
+    for (int s = tid; s < S; s += kThreads) {
+      const StreamGeom gm = stream_geom(s, p.q_len, G);
+      const int32_t len = stream_len(p.seq_lens[gm.b], p.q_len, gm.j0 + gm.nq - 1, p.causal,
+                                     p.topk_width, max_tokens);
+      const int32_t nt = (len + kTile - 1) / kTile;
+      prefix[s + 1] = nt;
+      cprefix[s + 1] = stream_cost(nt, p.stream_cost);
+    }
   }
   __syncthreads();
-  if (warp < 2) {   // exclusive prefix sums: warp 0 of tiles, warp 1 of cost
+  if (p.prefix_ws == nullptr && warp < 2) {   // exclusive prefix sums: warp 0 of tiles, warp 1 of cost
     int32_t* arr = warp == 0 ? prefix : cprefix;
     int32_t carry = 0;
     if (lane == 0) arr[0] = 0;
@@ -1469,9 +1484,24 @@ cudaError_t launch_mode(const CUtensorMap* kv_map, const DecodeParams& p, const 
   const cudaError_t err =
       set_smem_attr_once(reinterpret_cast<const void*>(mla_decode_kernel<kMode>), 3 + kMode, L.total);
   if (err != cudaSuccess) return err;
-  mla_decode_kernel<kMode>
-      <<<dim3(p.num_ctas), dim3(ModeTraits<kMode>::kThreads), L.total, stream>>>(*kv_map, p, L);
-  return cudaGetLastError();
+  if (p.prefix_ws == nullptr) {
+    mla_decode_kernel<kMode>
+        <<<dim3(p.num_ctas), dim3(ModeTraits<kMode>::kThreads), L.total, stream>>>(*kv_map, p, L);
+    return cudaGetLastError();
+  }
+  // behind the prefix pre-pass: a programmatic dependent of it (the kernel
+  // waits for it before reading memory)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.num_ctas);
+  cfg.blockDim = dim3(ModeTraits<kMode>::kThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(L.total);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mla_decode_kernel<kMode>, *kv_map, p, L);
 }
 }  // namespace
 

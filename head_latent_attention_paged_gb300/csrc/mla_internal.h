@@ -27,7 +27,12 @@ constexpr int kMaxHeads = 32;     // TMEM: q_hat 288 + S 64 + O^T 4 x 32 columns
 // G * H <= 48 rows (TMEM: latent q_hat 256 + S 64 + O^T 4 x 48 columns; the
 // RoPE part of q_hat is a shared-memory operand).
 constexpr int kMaxRows = 48;
-constexpr int kMaxStreams = 256;  // per-stream tile prefix kept in shared memory
+constexpr int kMaxStreams = 1 << 20;   // row sets per plan
+// Up to this many row sets the decode kernel keeps their tile and cost
+// prefixes in shared memory (when they fit beside its buffers); beyond, a
+// one-block pre-pass writes them to the workspace.
+constexpr int kSmemStreams = 256;
+constexpr int kMaxSmemBytes = 232448;   // dynamic shared memory per CTA (227 KB)
 constexpr int kMaxCtas = 65536;   // decode grid limit (split-KV by length)
 // 72 KB bf16 tiles in flight per CTA.  An FP4 tile of quantised rows
 // (20,736 B) is copied into the tail of the stage it is dequantised into;
@@ -63,11 +68,14 @@ struct DecodeParams {
   int32_t page_size, num_pages, max_pages, topk_width, causal;
   int32_t num_streams, num_ctas;
   int32_t stream_cost;          // a stream's fixed cost in the work split (stream_cost_of_mode)
+  int32_t* prefix_ws;           // int32 [2][S + 1] tile and cost prefixes written by the
+                                // pre-pass, or null: the decode kernel computes them itself
   float scale_log2;             // sm_scale * log2(e)
 };
 
 struct DecodeLayout {   // dynamic shared memory layout of the decode kernel
   int32_t off_stage, off_raw, off_p, off_qrope, off_ctrl, total;
+  int32_t prefix_in_smem;   // 1: the row-set prefixes follow the control block
 };
 
 DecodeLayout decode_layout(int heads, int heads_pad, int num_streams, int mode);
@@ -85,8 +93,11 @@ struct CombineParams {
   int32_t batch, q_len, heads, page_size, max_pages, topk_width, causal;
   int32_t group, rows;          // as in DecodeParams
   int32_t num_streams, num_ctas, stream_cost;
+  const int32_t* prefix_ws;     // the pre-pass's prefixes (as in DecodeParams), or null
 };
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
+// One block: the tile and cost prefixes over the row sets into p.prefix_ws.
+cudaError_t launch_prefix(const DecodeParams& p, cudaStream_t stream);
 
 // o = W_UV[h]^T o_lat per (head, 128 output dims, row block), a programmatic
 // dependent of the launch before it; sm_count sizes the row blocks (16, 32

@@ -83,10 +83,11 @@ extern "C" MLA_API int mla_decode_run_static(const mla_plan* plan, const void* q
   if (rc != MLA_OK) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(scratch);
-  // The reserved words and the status word must start at zero; they sit at
-  // the end of the workspace layout, from ws_counters on.
-  if (cudaMemsetAsync(ws + plan->ws_counters, 0,
-                      static_cast<size_t>(plan->workspace_bytes - plan->ws_counters),
+  // The status word must start at zero; it sits at the end of the workspace
+  // layout, after the row-set prefixes (cleared with it; the decode launch
+  // writes them when it uses them).
+  if (cudaMemsetAsync(ws + plan->ws_prefix, 0,
+                      static_cast<size_t>(plan->workspace_bytes - plan->ws_prefix),
                       st) != cudaSuccess)
     return MLA_ERR_CUDA;
   rc = mla::launch_attention(*plan, q_hat, kv_cache, block_table, seq_lens, topk_idx, ws, o_lat,

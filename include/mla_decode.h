@@ -131,7 +131,10 @@ typedef struct {
   int32_t smem_bytes;       /* dynamic shared memory of the decode kernel */
   int64_t ws_partial_o;     /* byte offset of f32 [num_slots][G * H][512] */
   int64_t ws_partial_lse;   /* byte offset of f32 [num_slots][G * H] */
-  int64_t ws_counters;      /* byte offset of int32 [num_streams], reserved (left at 0) */
+  int64_t ws_prefix;        /* byte offset of int32 [2][num_streams + 1]: the row sets'
+                               tile and cost prefixes of the work split, written by the
+                               decode launch when the row sets are too many for the
+                               decode kernel's shared memory (else left untouched) */
   int64_t ws_status;        /* byte offset of the uint32 status word */
   int64_t workspace_bytes;  /* total workspace size */
   int64_t planned_tiles;    /* tiles implied by seq_lens_host (0 if not given) */

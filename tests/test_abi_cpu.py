@@ -50,7 +50,7 @@ def test_every_entry_point_has_declared_argument_types(m):
 
 
 def test_version_and_strerror(m):
-    assert m.version() == 20000
+    assert m.version() == 20100
     for code in (0, -1, -2, -3, -4, -5, -99):
         assert isinstance(m.strerror(code), str) and m.strerror(code)
 
@@ -70,13 +70,27 @@ def test_plan_ok_and_workspace_layout(m):
     assert plan.num_slots == 4 + plan.num_ctas - 1
     assert plan.ws_partial_o == 0
     assert plan.ws_partial_lse >= plan.num_slots * 20 * 512 * 4
-    assert plan.ws_counters >= plan.ws_partial_lse + plan.num_slots * 20 * 4
-    assert plan.ws_status >= plan.ws_counters + 4 * 4
+    assert plan.ws_prefix >= plan.ws_partial_lse + plan.num_slots * 20 * 4
+    assert plan.ws_status >= plan.ws_prefix + 2 * 4 * (4 + 1)
     assert plan.workspace_bytes > plan.ws_status
     assert plan.smem_bytes <= 232448
     # no host seq_lens: fill every SM
     assert m.mla_decode_plan(_problem(m), None, 152).num_ctas == 152
 
+
+@pytest.mark.parametrize("kw", [dict(batch=257), dict(batch=65, q_len=4, num_heads=32),
+                                dict(batch=65, q_len=4, kv_dtype=1), dict(batch=129, q_len=4),
+                                dict(batch=4096), dict(batch=1000, kv_dtype=2)])
+def test_plans_beyond_256_row_sets(m, kw):
+    """More row sets than the decode kernel keeps prefixes for in shared
+    memory: the plan leaves them out of its shared memory and sizes the
+    workspace's prefix area, int32 [2][S + 1], for the pre-pass."""
+    plan = m.mla_decode_plan(_problem(m, **kw), None, 152)
+    assert plan.num_streams > 256
+    assert plan.smem_bytes <= 232448
+    assert plan.ws_status >= plan.ws_prefix + 8 * (plan.num_streams + 1)
+    small = m.mla_decode_plan(_problem(m, **dict(kw, batch=2)), None, 152)
+    assert plan.smem_bytes <= small.smem_bytes
 
 @pytest.mark.parametrize("kw,code", [
     (dict(page_size=96), -2), (dict(page_size=8), -2), (dict(page_size=256), -2), (dict(num_heads=0), -1),
@@ -84,8 +98,7 @@ def test_plan_ok_and_workspace_layout(m):
     (dict(topk_width=100), -2), (dict(topk_width=-128), -1), (dict(kv_lora_rank=256), -2),
     (dict(rope_dim=32), -2), (dict(v_head_dim=128), -2), (dict(nope_dim=128), -2),
     (dict(causal=2), -1), (dict(sm_scale=0.0), -1), (dict(sm_scale=float("nan")), -1),
-    (dict(num_pages=0), -1), (dict(max_pages_per_seq=0), -1), (dict(batch=257), -2), (dict(batch=65, q_len=4, num_heads=32), -2),
-    (dict(batch=65, q_len=4, kv_dtype=1), -2), (dict(batch=129, q_len=4), -2),
+    (dict(num_pages=0), -1), (dict(max_pages_per_seq=0), -1), (dict(batch=2**20 + 1), -2),
     (dict(kv_dtype=1, topk_width=128), -2), (dict(kv_dtype=2, topk_width=128), -2),
     (dict(kv_dtype=3), -2), (dict(kv_dtype=-1), -2),
 ])
@@ -133,7 +146,7 @@ def test_multi_token_plan_groups_draft_tokens(m, q_len, heads, group):
     assert plan.num_streams == 4 * -(-q_len // group)
     rows = group * heads
     assert plan.ws_partial_lse >= plan.num_slots * rows * 512 * 4
-    assert plan.ws_counters >= plan.ws_partial_lse + plan.num_slots * rows * 4
+    assert plan.ws_prefix >= plan.ws_partial_lse + plan.num_slots * rows * 4
     assert plan.smem_bytes <= 232448
     # FP4 caches group drafts the same way; FP8 caches keep one row set per draft
     fp4 = m.mla_decode_plan(_problem(m, q_len=q_len, num_heads=heads,

@@ -62,16 +62,12 @@ def test_split_invariance(sm_count):
 @pytest.mark.parametrize("q_len", [1, 3])
 def test_merge_is_repeatable_and_matches_separate_combine(sm_count, q_len):
     """The merge launched by mla_decode_run and a separate combine pass over
-    the same partials give the same o_lat and lse; the reserved workspace
-    words stay zero and a second run on the same workspace gives identical
-    results.  q_len 3: multi-token row sets (two drafts, then one)."""
+    the same partials give the same o_lat and lse, and a second run on the
+    same workspace gives identical results.  q_len 3: multi-token row sets (two drafts, then one)."""
     batch = W.generate(W.with_overrides(W.SMALL_WORKLOADS["long_small"], q_len=q_len))
     step = make_step(batch, sm_count=sm_count)
     step.run()
     _, lat1, lse1 = gpu_outputs(step)
-    pl = step.plan
-    counters = step.workspace[pl.ws_counters: pl.ws_counters + 4 * pl.num_streams]
-    assert int(counters.view(torch.int32).abs().sum()) == 0
     step.o_lat.fill_(float("nan"))
     step.lse.fill_(float("nan"))
     step.run()
@@ -404,3 +400,37 @@ def test_decode_step_matches_run_and_combine(name, sm_count):
         assert np.array_equal(o2, o1), trial
     compare(O.decode(batch), o2, lat2, lse2, label=f"decode-step/{name}",
             lse_ref=O.decode(batch, q_hat=q_hat))
+
+
+@pytest.mark.parametrize("name,q_len", [("dense_small", 1), ("fp8_small", 1), ("mtp_small", 2),
+                                        ("fp4_small", 1)])
+def test_more_row_sets_than_shared_memory_holds(name, q_len):
+    """512 requests of short contexts: more row sets than the decode kernel
+    keeps work-split prefixes for in shared memory, so a pre-pass writes the
+    tile and cost prefixes to the workspace and the decode and the merge read
+    them there.  Forced splits (40 CTAs), sampled requests on both sides of
+    row set 256 against the oracle; the prefixes against the tile counts."""
+    w = W.with_overrides(W.SMALL_WORKLOADS[name], batch=512, seq_lo=1, seq_hi=400, q_len=q_len)
+    batch = W.generate(w)
+    # contexts down to one token: the decode gets the oracle's bf16 absorbed
+    # query, so lse compares against the absorbed form on exactly that query
+    q_hat = oracle_q_hat(batch)
+    step = make_step(batch, sm_count=40, absorb=False)
+    upload_q_hat(step, q_hat)
+    step.step()
+    o, o_lat, lse = gpu_outputs(step)
+    assert step.status() == 0
+    pl = step.plan
+    S = pl.num_streams
+    assert S == 512
+    words = step.workspace[pl.ws_prefix: pl.ws_prefix + 8 * (S + 1)].cpu().view(torch.int32).numpy()
+    tiles, cost = words[:S + 1].astype(np.int64), words[S + 1:].astype(np.int64)
+    nt = (batch.seq_lens.astype(np.int64) + 63) // 64      # one row set per request here
+    assert tiles[0] == 0 and np.array_equal(np.diff(tiles), nt)
+    dc = np.diff(cost)
+    assert cost[0] == 0 and np.all(dc[nt == 0] == 0)
+    fixed = dc[nt > 0] - 4 * nt[nt > 0]                       # a row set's fixed cost, one value
+    assert fixed.min() == fixed.max() > 0
+    req = [0, 3, 255, 256, 257, 400, 511]
+    compare(O.decode(batch, requests=req), o, o_lat, lse, label=f"{name}-512",
+            lse_ref=O.decode(batch, requests=req, q_hat=q_hat))
