@@ -321,7 +321,7 @@ def run_reference(args, world, rank):
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
-PER_WORKLOADS = ["long", "fp8", "sparse", "fp4", "mtp"]
+PER_WORKLOADS = ["long", "fp8", "sparse", "fp4", "mtp", "mtp_fp8"]
 
 
 def kernel_label(w) -> str:
@@ -623,7 +623,7 @@ def main():
     ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="dense",
-                    choices=["tiny", "dense", "long", "fp8", "sparse", "fp4", "mtp"])
+                    choices=["tiny", "dense", "long", "fp8", "sparse", "fp4", "mtp", "mtp_fp8"])
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--decode-steps", type=int, default=1000,
@@ -632,7 +632,7 @@ def main():
                     help="launches of the decode kernel alone and of whole steps timed one by "
                          "one for each of the other workloads")
     ap.add_argument("--no-per-workload", dest="per_workload", action="store_false",
-                    help="skip the long / fp8 / sparse / fp4 / mtp measurements")
+                    help="skip the long / fp8 / sparse / fp4 / mtp / mtp_fp8 measurements")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

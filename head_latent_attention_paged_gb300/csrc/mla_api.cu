@@ -137,7 +137,8 @@ int group_of(const mla_problem& pr) {
 }
 
 int decode_mode(const mla_problem& pr) {
-  if (pr.kv_dtype == MLA_KV_FP8_E4M3_E8M0) return kModeDenseFp8;
+  if (pr.kv_dtype == MLA_KV_FP8_E4M3_E8M0)
+    return group_of(pr) >= 2 ? kModeDenseFp8Multi : kModeDenseFp8;
   if (pr.kv_dtype == MLA_KV_FP4_E2M1_E8M0)
     return group_of(pr) >= 2 ? kModeDenseFp4Multi : kModeDenseFp4;
   if (pr.topk_width > 0) return kModeSparseBf16;
@@ -313,6 +314,7 @@ int launch_attention(const mla_plan& plan, const void* q_hat, const void* kv_cac
   CUtensorMap kv_map;
   std::memset(&kv_map, 0, sizeof(kv_map));   // FP8 / FP4 caches are read with bulk copies
   if (mode != kModeDenseFp8 && mode != kModeDenseFp4 && mode != kModeDenseFp4Multi &&
+      mode != kModeDenseFp8Multi &&
       !make_map_bf16(&kv_map, kv_cache, kDqk, static_cast<uint64_t>(pr.num_pages) * pr.page_size,
                      kDqk * 2, kChunkElems,
                      mode == kModeSparseBf16 ? 1 : (pr.page_size < kTile ? pr.page_size : kTile)))

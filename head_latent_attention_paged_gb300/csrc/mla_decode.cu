@@ -73,13 +73,14 @@ constexpr int kGatherRows = kTile / kGatherWarps;   // 16 rows per gather warp
 
 template <int kMode>
 struct ModeTraits {
-  static constexpr bool kFp8 = kMode == kModeDenseFp8;
+  static constexpr bool kFp8 = kMode == kModeDenseFp8 || kMode == kModeDenseFp8Multi;
   static constexpr bool kFp4 = kMode == kModeDenseFp4 || kMode == kModeDenseFp4Multi;
   static constexpr bool kQuant = kFp8 || kFp4;   // quantised bytes, dequantised in the CTA
   static constexpr int kRowBytes = kFp4 ? kFp4RowBytes : kFp8RowBytes;    // quantised row
   static constexpr int kRawTileBytes = kTile * kRowBytes;
   static constexpr bool kSparse = kMode == kModeSparseBf16;
-  static constexpr bool kMulti = kMode == kModeDenseMulti || kMode == kModeDenseFp4Multi;
+  static constexpr bool kMulti =
+      kMode == kModeDenseMulti || kMode == kModeDenseFp4Multi || kMode == kModeDenseFp8Multi;
   // dense bf16 staging (TMA tiles, dead rows zeroed by the softmax warps)
   static constexpr bool kDenseBf16 = kMode == kModeDenseBf16 || kMode == kModeDenseMulti;
   // the first softmax warp whose TMEM lanes hold rows: row r of a row set is
@@ -516,20 +517,20 @@ __device__ __forceinline__ void convert_fp4_group(const Fp4Group& f, uint4 (&o)[
 DecodeLayout decode_layout(int heads, int heads_pad, int num_streams, int mode) {
   (void)heads;
   (void)heads_pad;
-  const bool ring = mode == kModeDenseFp8;   // FP8: bf16 stages plus a raw ring
+  const bool ring = mode == kModeDenseFp8 || mode == kModeDenseFp8Multi;   // bf16 stages + raw ring
   DecodeLayout L;
   L.off_stage = 0;
   L.off_raw = (ring ? kFp8Stages : kStages) * kTileBytes;
   L.off_p = L.off_stage + kPChunkOffset;     // first stage's P; stride kTileBytes
   // q_hat's RoPE part as a shared-memory A operand: 64 M-rows x 128 B from
   // off_qrope, 1024-byte aligned.  Only the M-rows of the row set's softmax
-  // warps are written and read back into S; in the FP8 kernel, which has no
-  // room for all 8 KB, M-rows 0-31 (no row of a one-token row set) overlap
-  // the end of the raw ring: the MMA reads whatever bytes are there into S
-  // rows no one reads.
+  // warps are written and read back into S; in the FP8 kernels, which have
+  // no room for all 8 KB, the M-rows below them (0-31 one-token, 0-15 with
+  // draft rows) overlap the end of the raw ring: the MMA reads whatever bytes
+  // are there into S rows no one reads.
   const int raw_end = L.off_raw + (ring ? kFp8RawSlots * kFp8TileBytes : 0);
   if (ring) {
-    L.off_qrope = ((raw_end + 1023) & ~1023) - kQRopeBytes / 2;
+    L.off_qrope = ((raw_end + 1023) & ~1023) - (mode == kModeDenseFp8Multi ? 16 : 32) * 128;
     L.off_ctrl = L.off_qrope + kQRopeBytes;
   } else {
     L.off_qrope = raw_end;
@@ -1515,6 +1516,7 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap* kv_map, int 
     case kModeDenseFp4: return launch_mode<kModeDenseFp4>(kv_map, p, L, stream);
     case kModeDenseMulti: return launch_mode<kModeDenseMulti>(kv_map, p, L, stream);
     case kModeDenseFp4Multi: return launch_mode<kModeDenseFp4Multi>(kv_map, p, L, stream);
+    case kModeDenseFp8Multi: return launch_mode<kModeDenseFp8Multi>(kv_map, p, L, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -49,6 +49,7 @@ enum DecodeMode : int {
   kModeDenseFp4 = 3,
   kModeDenseMulti = 4,   // bf16, q_len > 1: draft tokens of a request share each staged tile
   kModeDenseFp4Multi = 5,   // the same over an FP4 cache
+  kModeDenseFp8Multi = 6,   // the same over an FP8 cache
 };
 
 struct DecodeParams {
@@ -164,9 +165,8 @@ __host__ __device__ inline StreamGeom stream_geom(int32_t s, int32_t q_len, int3
 // for the RoPE query operand beside its raw-tile ring).
 __host__ __device__ inline int32_t row_set_group(int32_t q_len, int32_t heads, int32_t kv_dtype,
                                                  int32_t topk_width) {
-  if ((kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP4_E2M1_E8M0) || topk_width > 0 ||
-      q_len < 2)
-    return 1;
+  (void)kv_dtype;   // every cache type groups draft rows (the sparse top-k lists do not)
+  if (topk_width > 0 || q_len < 2) return 1;
   const int32_t g = kMaxRows / heads;
   const int32_t gq = g < q_len ? g : q_len;
   return gq >= 2 ? gq : 1;
@@ -200,7 +200,8 @@ constexpr int32_t kStreamCostQuant = 8;
 constexpr int32_t kStreamCostMax = 13;
 
 __host__ __device__ inline int32_t stream_cost_of_mode(int mode) {
-  return (mode == kModeDenseFp8 || mode == kModeDenseFp4 || mode == kModeDenseFp4Multi)
+  return (mode == kModeDenseFp8 || mode == kModeDenseFp4 || mode == kModeDenseFp4Multi ||
+          mode == kModeDenseFp8Multi)
              ? kStreamCostQuant
              : kStreamCostBf16;
 }

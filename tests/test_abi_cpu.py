@@ -79,7 +79,7 @@ def test_plan_ok_and_workspace_layout(m):
 
 
 @pytest.mark.parametrize("kw", [dict(batch=257), dict(batch=65, q_len=4, num_heads=32),
-                                dict(batch=65, q_len=4, kv_dtype=1), dict(batch=129, q_len=4),
+                                dict(batch=200, q_len=4, kv_dtype=1), dict(batch=129, q_len=4),
                                 dict(batch=4096), dict(batch=1000, kv_dtype=2)])
 def test_plans_beyond_256_row_sets(m, kw):
     """More row sets than the decode kernel keeps prefixes for in shared
@@ -148,13 +148,10 @@ def test_multi_token_plan_groups_draft_tokens(m, q_len, heads, group):
     assert plan.ws_partial_lse >= plan.num_slots * rows * 512 * 4
     assert plan.ws_prefix >= plan.ws_partial_lse + plan.num_slots * rows * 4
     assert plan.smem_bytes <= 232448
-    # FP4 caches group drafts the same way; FP8 caches keep one row set per draft
-    fp4 = m.mla_decode_plan(_problem(m, q_len=q_len, num_heads=heads,
-                                     kv_dtype=m.MLA_KV_FP4_E2M1_E8M0), seq, 152)
-    assert fp4.num_streams == plan.num_streams and fp4.smem_bytes <= 232448
-    fp8 = m.mla_decode_plan(_problem(m, q_len=q_len, num_heads=heads,
-                                     kv_dtype=m.MLA_KV_FP8_E4M3_E8M0), seq, 152)
-    assert fp8.num_streams == 4 * q_len
+    # FP4 and FP8 caches group drafts the same way
+    for kv in (m.MLA_KV_FP4_E2M1_E8M0, m.MLA_KV_FP8_E4M3_E8M0):
+        quant = m.mla_decode_plan(_problem(m, q_len=q_len, num_heads=heads, kv_dtype=kv), seq, 152)
+        assert quant.num_streams == plan.num_streams and quant.smem_bytes <= 232448
 
 
 def test_plan_rejects_negative_seq_len_and_bad_sm_count(m):
@@ -310,11 +307,14 @@ def test_bounded_wait_selftest_rejects_bad_arguments_before_cuda(m):
         assert e.value.code == code
 
 
-def test_row_set_limit_counts_grouped_drafts(m):
-    """The 256-row-set limit counts row sets, not query tokens: 64 requests
-    with 8 drafts of 6 heads are 64 grouped row sets (G = 8)."""
+def test_row_set_count_counts_grouped_drafts(m):
+    """Row sets, not query tokens: 64 requests with 8 drafts of 6 heads are
+    64 grouped row sets (G = 8), over every cache type."""
     plan = m.mla_decode_plan(_problem(m, batch=64, q_len=8, num_heads=6), None, 152)
     assert plan.num_streams == 64
+    for kv in (m.MLA_KV_FP4_E2M1_E8M0, m.MLA_KV_FP8_E4M3_E8M0):
+        assert m.mla_decode_plan(_problem(m, batch=64, q_len=8, num_heads=6, kv_dtype=kv), None,
+                                 152).num_streams == 64
     plan = m.mla_decode_plan(_problem(m, batch=128, q_len=4), None, 152)   # G = 2
     assert plan.num_streams == 256
 

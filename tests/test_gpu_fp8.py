@@ -179,3 +179,15 @@ def test_gpu_quantiser_matches_oracle_on_full_size_rows():
         got = quantise_cache_on_device(lat, kv, "cuda:0").cpu().numpy().reshape(-1, enc.ROW_BYTES)
         want = enc.quantize_rows(lat.reshape(-1, 576).astype(np.float64))
         assert np.array_equal(got, want), (enc.__name__, int((got != want).any(axis=1).sum()))
+
+
+def test_fp8_draft_pairs_full_size_sampled():
+    """The FP8 workload with two causal draft tokens per request (an MTP
+    draft pair over an FP8 cache): both drafts of a request form one row set
+    of 40 rows that shares every staged page.  Benchmark launch
+    configuration, sampled requests and heads."""
+    batch = W.generate(W.WORKLOADS["mtp_fp8"])
+    step = _run_and_compare(batch, requests=[0, 77, 127], heads=[0, 9, 19], label="mtp-fp8-full")
+    assert step.plan.num_streams == 128
+    o, _, lse = gpu_outputs(step)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()

@@ -1,5 +1,5 @@
 """GPU parity of the dense multi-token decode (speculative draft tokens that
-share each staged page).
+share each staged page), over bf16, FP4 and FP8 caches.
 
 With q_len = Q draft tokens per request and H heads, G = min(Q, 48 / H)
 consecutive draft tokens of a request form one row set of G * H rows: every
@@ -24,6 +24,9 @@ torch = pytest.importorskip("torch")
 def _built():
     ensure_built()
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+
+
+BASE = {"bf16": "dense_small", "fp4": "fp4_small", "fp8": "fp8_small"}
 
 
 def _group(q_len, heads):
@@ -54,21 +57,21 @@ def _run(batch, sm_count=None, label=""):
     (5, 8, True, 16, None),      # G = 5 (40 rows), 16-token pages
     (2, 32, True, 64, None),     # 48 / 32 = 1: one draft per row set
 ])
-@pytest.mark.parametrize("kv", ["bf16", "fp4"])
+@pytest.mark.parametrize("kv", ["bf16", "fp4", "fp8"])
 def test_multi_token_matches_oracle(q_len, heads, causal, page_size, sm_count, kv):
-    base = W.SMALL_WORKLOADS["dense_small" if kv == "bf16" else "fp4_small"]
+    base = W.SMALL_WORKLOADS[BASE[kv]]
     w = W.with_overrides(base, q_len=q_len, heads=heads, causal=causal, page_size=page_size,
                          batch=4, seq_lo=70, seq_hi=900)
     _run(W.generate(w), sm_count=sm_count,
          label=f"{kv}/q{q_len}/h{heads}/c{int(causal)}/p{page_size}")
 
 
-@pytest.mark.parametrize("kv", ["bf16", "fp4"])
+@pytest.mark.parametrize("kv", ["bf16", "fp4", "fp8"])
 def test_multi_token_short_contexts(kv):
     """Contexts shorter than the drafts: with T = 1 and Q = 3 the first two
     drafts see no position (o = 0, lse = -inf) while the last sees one; other
     lengths end inside and at the edges of a tile for some drafts only."""
-    base = W.SMALL_WORKLOADS["dense_small" if kv == "bf16" else "fp4_small"]
+    base = W.SMALL_WORKLOADS[BASE[kv]]
     w = W.with_overrides(base, q_len=3, heads=16,
                          seq_lens=(1, 2, 3, 64, 65, 66, 127, 0), batch=8)
     batch = W.generate(w, garbage="nan")

@@ -128,6 +128,10 @@ WORKLOADS = {
     # FP4 latent (e2m1 + e8m0 per 16), on the FP8 workload's shape
     "fp4": Workload("fp4", batch=128, heads=20, seq_lo=2048, seq_hi=16384, page_size=64,
                     kv_dtype="fp4"),
+    # speculative verify over the FP8 cache: the FP8 workload with 2 causal
+    # draft tokens per request, both drafts sharing each staged page
+    "mtp_fp8": Workload("mtp_fp8", batch=128, heads=20, q_len=2, seq_lo=2048, seq_hi=16384,
+                        page_size=64, kv_dtype="fp8"),
 }
 
 # Reduced sizes the oracle checks element by element: several tiles and a
