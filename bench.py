@@ -593,7 +593,7 @@ def run_gpu(args, world, rank, local):
                      "step_frac": byts / (statistics.median(step_ms) / 1e3) / 1e9 / hbm},
         "per_workload": per_workload or None,
         "e2e": e2e,
-        "gpu_launches": DecodeStep.KERNELS_PER_STEP * args.steps,
+        "gpu_launches": step.kernels_per_step * args.steps,
         "clocks": clocks.summary(),
         "wall_s_timed_region": t_wall,
         "status": step.status(),

@@ -62,7 +62,7 @@ class MlaPlan(ctypes.Structure):
         ("workspace_bytes", ctypes.c_int64),
         ("planned_tiles", ctypes.c_int64), ("ws_q_hat", ctypes.c_int64),
         ("split_tokens", ctypes.c_int32), ("sm_count", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 4),
+        ("prefix_pass", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3),
     ]
 
 

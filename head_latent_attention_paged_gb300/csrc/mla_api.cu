@@ -429,6 +429,8 @@ int mla_decode_plan(const mla_problem* problem, const int32_t* seq_lens_host, in
   pl.num_slots = pl.num_streams + pl.num_ctas - 1;
   if (pl.num_slots < 1) pl.num_slots = 1;
   pl.smem_bytes = decode_smem_bytes(pr.num_heads, heads_pad, pl.num_streams, decode_mode(pr));
+  pl.prefix_pass = decode_layout(pr.num_heads, heads_pad, pl.num_streams, decode_mode(pr))
+                       .prefix_in_smem ? 0 : 1;
   if (pl.smem_bytes > kMaxSmemBytes) return MLA_ERR_UNSUPPORTED;
   int64_t off = 0;
   pl.ws_partial_o = off;

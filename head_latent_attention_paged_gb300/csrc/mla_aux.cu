@@ -10,6 +10,7 @@
 #include <cmath>
 
 #include "mla_internal.h"
+#include "mla_merge.cuh"
 #include "sm103_ptx.cuh"
 
 namespace mla {
@@ -45,91 +46,64 @@ __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(const Comb
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = p.num_streams;
   const int max_tokens = p.max_pages * p.page_size;
-  __shared__ int64_t red64[2][kCombineThreads / 32];
-  // cost before stream s and in total (the decode grid's split): summed here
-  // while the decode runs, or read from the pre-pass's prefixes
-  int64_t before = 0, tot = 0;
+  __shared__ int64_t red64[3][kCombineThreads / 32];
+  // cost before stream s, in total, and the total tile count (the decode
+  // grid's split): summed here while the decode runs, or read from the
+  // pre-pass's prefixes
+  int64_t before = 0, tot = 0, tiles = 0;
   if (p.prefix_ws == nullptr) {
     for (int t = tid; t < S; t += kCombineThreads) {
       const StreamGeom gt = stream_geom(t, p.q_len, p.group);
       const int32_t len = stream_len(p.seq_lens[gt.b], p.q_len, gt.j0 + gt.nq - 1, p.causal,
                                      p.topk_width, max_tokens);
-      const int64_t n = stream_cost((len + kTile - 1) / kTile, p.stream_cost);
+      const int32_t nt = (len + kTile - 1) / kTile;
+      const int64_t n = stream_cost(nt, p.stream_cost);
       tot += n;
+      tiles += nt;
       if (t < s) before += n;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       before += __shfl_xor_sync(0xffffffffu, before, o);
       tot += __shfl_xor_sync(0xffffffffu, tot, o);
+      tiles += __shfl_xor_sync(0xffffffffu, tiles, o);
     }
-    if (lane == 0) { red64[0][warp] = before; red64[1][warp] = tot; }
+    if (lane == 0) { red64[0][warp] = before; red64[1][warp] = tot; red64[2][warp] = tiles; }
     __syncthreads();
-    before = tot = 0;
+    before = tot = tiles = 0;
 #pragma unroll
-    for (int w = 0; w < kCombineThreads / 32; ++w) { before += red64[0][w]; tot += red64[1][w]; }
+    for (int w = 0; w < kCombineThreads / 32; ++w) {
+      before += red64[0][w];
+      tot += red64[1][w];
+      tiles += red64[2][w];
+    }
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (p.prefix_ws != nullptr) {
     before = p.prefix_ws[S + 1 + s];
     tot = p.prefix_ws[S + 1 + S];
+    tiles = p.prefix_ws[S];
   }
+  const int32_t nctas = work_ctas(p.num_ctas, static_cast<int32_t>(tiles));
   const StreamGeom gm = stream_geom(s, p.q_len, p.group);
   if (h >= gm.nq * p.heads) return;   // a short last group of draft tokens
   const int32_t len = stream_len(p.seq_lens[gm.b], p.q_len, gm.j0 + gm.nq - 1, p.causal,
                                  p.topk_width, max_tokens);
   const int64_t ntiles = (len + kTile - 1) / kTile;
   if (ntiles == 0) return;   // the decode wrote o_lat = 0, lse = -inf
-  const int c0 = tile_owner(tile_cost_pos(before, 0, p.stream_cost), tot, p.num_ctas);
+  const int c0 = tile_owner(tile_cost_pos(before, 0, p.stream_cost), tot, nctas);
   const int c1 = tile_owner(tile_cost_pos(before, static_cast<int32_t>(ntiles - 1), p.stream_cost),
-                            tot, p.num_ctas);
+                            tot, nctas);
   if (c0 == c1) return;      // one CTA held the whole row set: its result is final
   const int nseg = c1 - c0 + 1;
-  // One pass over the partials, 8 at a time (their lse values and this
-  // thread's 4 dims loaded together): running max m, sum = sum_i exp(lse_i -
-  // m), acc = sum_i exp(lse_i - m) o_i, rescaled when m grows; finally
-  // lse = m + ln(sum), o = acc / sum.
   // partial slots hold p.rows rows each
   const float* plse = p.part_lse + static_cast<int64_t>(s + c0) * p.rows + h;
   const float4* po = reinterpret_cast<const float4*>(p.part_o) +
                      (static_cast<int64_t>(s + c0) * p.rows + h) * (kDc / 4) + tid;
-  const int64_t lstride = p.rows;
-  const int64_t ostride = static_cast<int64_t>(p.rows) * (kDc / 4);
-  float m = -INFINITY, sum = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int k0 = 0; k0 < nseg; k0 += 8) {
-    float lv[8];
-    float4 v[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const bool in = k0 + u < nseg;
-      lv[u] = in ? plse[(k0 + u) * lstride] : -INFINITY;
-      v[u] = in ? po[(k0 + u) * ostride] : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    float mc = m;
-#pragma unroll
-    for (int u = 0; u < 8; ++u) mc = fmaxf(mc, lv[u]);
-    if (mc == -INFINITY) continue;     // nothing live so far
-    const float r = (m == -INFINITY) ? 0.f : __expf(m - mc);
-    sum *= r;
-    acc.x *= r; acc.y *= r; acc.z *= r; acc.w *= r;
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const float w = (lv[u] == -INFINITY) ? 0.f : __expf(lv[u] - mc);
-      sum += w;
-      acc.x = fmaf(w, v[u].x, acc.x);
-      acc.y = fmaf(w, v[u].y, acc.y);
-      acc.z = fmaf(w, v[u].z, acc.z);
-      acc.w = fmaf(w, v[u].w, acc.w);
-    }
-    m = mc;
-  }
-  const float lse = (m == -INFINITY) ? -INFINITY : m + __logf(sum);
-  const float inv = (m == -INFINITY) ? 0.f : 1.f / sum;
-  acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
+  const MergedRow mr = merge_partials(plse, po, nseg, p.rows, static_cast<int64_t>(p.rows) * (kDc / 4));
   const int64_t row = (static_cast<int64_t>(gm.b) * p.q_len + gm.j0) * p.heads + h;
-  reinterpret_cast<float4*>(p.o_lat + row * kDc)[tid] = acc;
-  if (tid == 0) p.lse[row] = lse;
+  reinterpret_cast<float4*>(p.o_lat + row * kDc)[tid] = mr.o;
+  if (tid == 0) p.lse[row] = mr.lse;
 }
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {

@@ -654,11 +654,16 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
 
   const int32_t ucost = cprefix[S];
   const int32_t c = blockIdx.x;
-  const int32_t g0 = first_tile_at(
-      prefix, cprefix, S, static_cast<int32_t>((static_cast<int64_t>(c) * ucost) / p.num_ctas),
+  // CTAs that take part in the split (work_ctas): the plan's, but at most
+  // one per tile, so that each CTA's cost range spans at least kTileCost
+  // units and every CTA between the first and the last owner of a row set's
+  // tiles owns some of them (and writes a partial)
+  const int32_t nctas = work_ctas(p.num_ctas, prefix[S]);
+  const int32_t g0 = c >= nctas ? 0 : first_tile_at(
+      prefix, cprefix, S, static_cast<int32_t>((static_cast<int64_t>(c) * ucost) / nctas),
       p.stream_cost);
-  const int32_t g1 = first_tile_at(
-      prefix, cprefix, S, static_cast<int32_t>((static_cast<int64_t>(c + 1) * ucost) / p.num_ctas),
+  const int32_t g1 = c >= nctas ? 0 : first_tile_at(
+      prefix, cprefix, S, static_cast<int32_t>((static_cast<int64_t>(c + 1) * ucost) / nctas),
       p.stream_cost);
   const int32_t ntiles = g1 - g0;
   const uint32_t tmem = ctrl->tmem_base;
@@ -1410,10 +1415,10 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
           ok = !failed && pv_done(i);   // PVs complete in order: all of them
           const int32_t s = wk.s;
           const int32_t c_first =
-              tile_owner(tile_cost_pos(cprefix[s], 0, p.stream_cost), ucost, p.num_ctas);
+              tile_owner(tile_cost_pos(cprefix[s], 0, p.stream_cost), ucost, nctas);
           const int32_t c_last = tile_owner(
               tile_cost_pos(cprefix[s], prefix[s + 1] - prefix[s] - 1, p.stream_cost), ucost,
-              p.num_ctas);
+              nctas);
           const bool split = c_first != c_last;
           // an unsplit stream's result is final: straight to the outputs
           // (partial slots hold RMAX rows each)

@@ -214,6 +214,13 @@ __host__ __device__ inline int64_t tile_cost_pos(int64_t stream_cost_start, int3
   return stream_cost_start + sc + static_cast<int64_t>(k) * kTileCost;
 }
 
+// CTAs the work is split over: the plan's count, but at most one per tile
+// (a cost range of at least kTileCost units per CTA leaves no CTA between a
+// row set's first and last tile owners without a tile of it).
+__host__ __device__ inline int32_t work_ctas(int32_t plan_ctas, int32_t total_tiles) {
+  return total_tiles < 1 ? 1 : (plan_ctas < total_tiles ? plan_ctas : total_tiles);
+}
+
 // CTA that owns cost position x when `total` cost units are split over
 // `ctas` CTAs as [c*total/ctas, (c+1)*total/ctas).
 __host__ __device__ inline int32_t tile_owner(int64_t x, int64_t total, int32_t ctas) {

@@ -35,7 +35,8 @@ class DecodeStep:
     def __init__(self, *, q_nope, q_rope, w_uk, w_uv, cache, block_table, seq_lens,
                  page_size: int, kv_dtype: int = MLA_KV_BF16, topk_idx=None, causal: bool = True,
                  sm_scale: float = 1.0 / 16.0, sm_count: Optional[int] = None, device="cuda:0",
-                 absorb_on_device: bool = True, split_tokens: int = 0):
+                 absorb_on_device: bool = True, split_tokens: int = 0,
+                 plan_with_host_lengths: bool = True):
         self.device = torch.device(device)
         B, Q, H, _ = q_nope.shape
         self.B, self.Q, self.H = B, Q, H
@@ -47,7 +48,11 @@ class DecodeStep:
         self.problem = make_problem(B, Q, H, page_size, num_pages, int(block_table.shape[1]),
                                     kv_dtype=kv_dtype, topk_width=width, causal=int(causal),
                                     sm_scale=sm_scale)
-        self.plan = mla_decode_plan(self.problem, seq_lens, sm_count, split_tokens)
+        # the plan sizes its grid from the host lengths when given them (else
+        # it fills every SM; the kernels derive the split from the device
+        # lengths either way)
+        self.plan = mla_decode_plan(self.problem, seq_lens if plan_with_host_lengths else None,
+                                    sm_count, split_tokens)
         dev = self.device
         # the un-absorbed query, one [q_nope (192) || q_rope (64)] per head
         self.q = to_device_bf16(np.concatenate([q_nope, q_rope], axis=-1).reshape(B * Q, H, 256), dev)
@@ -92,8 +97,8 @@ class DecodeStep:
                            self.stream)
 
     def combine(self, uv: bool = False):
-        """Merge split row sets (mla_combine); uv=True also writes out =
-        W_UV^T o_lat in the same kernel."""
+        """Merge split row sets (mla_combine); uv=True then also writes out =
+        W_UV^T o_lat."""
         mla_combine(self.plan, self.seq_lens, self.workspace, self.o_lat, self.lse,
                     self.w_uv if uv else None, self.out if uv else None, self.stream)
 
@@ -110,7 +115,8 @@ class DecodeStep:
     def step(self):
         """One decode step (mla_decode_step): the attention pass, the merge of
         split row sets and the W_UV projection (three kernels, each a
-        programmatic dependent of the one before); the absorbed query is an
+        programmatic dependent of the one before, behind a one-block prefix
+        pre-pass when the row sets are many); the absorbed query is an
         input."""
         mla_decode_step(self.plan, self.q_hat, None, self.cache, self.block_table, self.seq_lens,
                         self.topk_idx, self.workspace, self.w_uv, self.o_lat, self.lse, self.out,
@@ -127,7 +133,11 @@ class DecodeStep:
     def clear_status(self):
         mla_clear_status(self.plan, self.workspace, self.stream)
 
-    KERNELS_PER_STEP = 3
+    @property
+    def kernels_per_step(self) -> int:
+        """Kernels one step() launches: the decode, the merge and W_UV, behind
+        the prefix pre-pass when the plan has one."""
+        return 3 + int(self.plan.prefix_pass)
 
 
 class HostPipeline:

@@ -142,7 +142,9 @@ typedef struct {
                                mla_decode_run writes when it is given W_UK */
   int32_t split_tokens;     /* as requested from mla_decode_plan (0 = automatic) */
   int32_t sm_count;         /* as given to mla_decode_plan */
-  int32_t reserved[4];
+  int32_t prefix_pass;      /* 1: each decode launch runs the one-block prefix pre-pass
+                               first (row sets too many for the kernel's shared memory) */
+  int32_t reserved[3];
 } mla_plan;
 
 /*

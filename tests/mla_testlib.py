@@ -22,7 +22,7 @@ def ensure_built():
 
 
 def make_step(batch: W.Batch, sm_count=None, absorb=True, device="cuda:0", fp8_bytes=None,
-              split_tokens=0):
+              split_tokens=0, plan_with_host_lengths=True):
     from head_latent_attention_paged_gb300 import (MLA_KV_BF16, MLA_KV_FP4_E2M1_E8M0,
                                                    MLA_KV_FP8_E4M3_E8M0)
     from head_latent_attention_paged_gb300.runner import DecodeStep
@@ -37,7 +37,8 @@ def make_step(batch: W.Batch, sm_count=None, absorb=True, device="cuda:0", fp8_b
                       cache=cache, block_table=batch.block_table, seq_lens=batch.seq_lens,
                       page_size=w.page_size, kv_dtype=kv_dtype, topk_idx=batch.topk_idx,
                       causal=w.causal, sm_scale=w.sm_scale, sm_count=sm_count, device=device,
-                      absorb_on_device=absorb, split_tokens=split_tokens)
+                      absorb_on_device=absorb, split_tokens=split_tokens,
+                      plan_with_host_lengths=plan_with_host_lengths)
 
 
 def gpu_outputs(step):

@@ -63,7 +63,8 @@ def test_split_invariance(sm_count):
 def test_merge_is_repeatable_and_matches_separate_combine(sm_count, q_len):
     """The merge launched by mla_decode_run and a separate combine pass over
     the same partials give the same o_lat and lse, and a second run on the
-    same workspace gives identical results.  q_len 3: multi-token row sets (two drafts, then one)."""
+    same workspace gives identical results.  q_len 3: multi-token row sets
+    (two drafts, then one)."""
     batch = W.generate(W.with_overrides(W.SMALL_WORKLOADS["long_small"], q_len=q_len))
     step = make_step(batch, sm_count=sm_count)
     step.run()
@@ -75,7 +76,22 @@ def test_merge_is_repeatable_and_matches_separate_combine(sm_count, q_len):
     assert np.array_equal(lat1, lat2) and np.array_equal(lse1, lse2)
     step.combine()
     _, lat3, lse3 = gpu_outputs(step)
-    assert np.allclose(lat3, lat1, rtol=1e-5, atol=1e-6) and np.allclose(lse3, lse1, atol=1e-5)
+    assert np.array_equal(lat3, lat1) and np.array_equal(lse3, lse1)
+
+
+def test_plan_without_host_lengths_on_few_tiles():
+    """A plan made without host lengths fills every SM (152 CTAs) while the
+    device lengths hold fewer tiles than that: the kernels split the work
+    over at most one CTA per tile, so every CTA between a row set's first
+    and last tile owners holds a partial, and the merge sees all of them."""
+    batch = W.generate(W.with_overrides(W.SMALL_WORKLOADS["dense_small"], batch=3,
+                                        seq_lo=300, seq_hi=900))
+    step = make_step(batch, sm_count=152, plan_with_host_lengths=False)
+    assert step.plan.num_ctas == 152 and sum((int(t) + 63) // 64 for t in batch.seq_lens) < 152
+    step.step()
+    o, o_lat, lse = gpu_outputs(step)
+    assert step.status() == 0
+    compare(O.decode(batch), o, o_lat, lse, label="no-host-lengths")
 
 
 @pytest.mark.parametrize("name", ["dense_small", "fp8_small", "mtp_small"])
