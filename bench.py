@@ -374,12 +374,21 @@ class Rotation:
             self.flush.zero_()
 
 
+def hold_device(n):
+    """Queue a spin of about 0.1 ms per launch group ahead of n timed ones, so
+    that the host has queued them all before the device reaches the first:
+    the events then bracket device work only, not the host's launch calls."""
+    import torch
+    torch.cuda._sleep(int(min(n, 2000) * 2.0e5))
+
+
 def timed(step, rot, n, stream, fn):
     """n launches of fn(), each bracketed by CUDA events on `stream`: times
     in ms."""
     import torch
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(n)]
+    hold_device(n)
     for k in range(n):
         rot.before(k)
         ev[k][0].record(stream)
@@ -472,6 +481,7 @@ def run_gpu(args, world, rank, local):
         torch.distributed.barrier()
     torch.cuda.synchronize(device)
     with ClockSampler(local) as clocks:
+        hold_device(args.steps)
         t_wall = time.perf_counter()
         for k in range(args.steps):
             rot.before(k)
