@@ -1274,20 +1274,6 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&ctrl->s_free);
-          if (last && i + 1 < ntiles) {
-            // The next tile opens another stream: its queries replace this
-            // stream's in TMEM.  S(i) was this stream's last QK and it has
-            // completed, so nothing reads the old queries any more.
-            Walker nx = wk;
-            nx.next(prefix, S);
-            load_q<MT::kRowWarp0, MT::kQRopeSmem, MT::kQBatch>(p.q_hat + first_row(nx.s) * kDqk,
-                                                               rows_of(nx.s), tmem + lane_base,
-                                                               sQr, lane, w);
-            if constexpr (MT::kQRopeSmem) fence_proxy_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ctrl->q_ready);
-          }
           if (ok && warp_has_heads) {
             // token of y[t] is 32*half + t
             uint32_t hmask = static_cast<uint32_t>(mask >> (32 * half));
@@ -1409,6 +1395,22 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
             mma_commit(&ctrl->empty[stage]);
           }
           __syncwarp();
+        }
+        if (last && i + 1 < ntiles) {
+          // The next tile opens another stream: its queries replace this
+          // stream's in TMEM.  S(i) was this stream's last QK and it has
+          // completed, so nothing reads the old queries any more.  Loaded
+          // once P(i) is out, so that the load overlaps this segment's
+          // epilogue (which first waits for PV(i)) instead of delaying P(i).
+          Walker nx = wk;
+          nx.next(prefix, S);
+          load_q<MT::kRowWarp0, MT::kQRopeSmem, MT::kQBatch>(p.q_hat + first_row(nx.s) * kDqk,
+                                                             rows_of(nx.s), tmem + lane_base, sQr,
+                                                             lane, w);
+          if constexpr (MT::kQRopeSmem) fence_proxy_async_smem();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctrl->q_ready);
         }
         if (last) {
           // ---- segment epilogue
