@@ -65,7 +65,7 @@ constexpr int kGroupSets = kDequantWarps * 32 / kTile;   // threads per row in t
 // P(i) is written after S(i) is complete, so every stage carries its own P.
 constexpr int kPChunkOffset = (kChunks - 1) * kChunkBytes;
 
-constexpr int kPvLanes = 4;         // PV issuing lanes: lane l issues O^T block l (128 dims)
+constexpr int kPvLanes = 4;         // PV issuers, one per 128-dim block of O^T
 
 constexpr int kGatherWarp0 = 6;     // sparse mode: warps 6..9 gather top-k rows
 constexpr int kGatherWarps = 4;
@@ -117,6 +117,10 @@ struct ModeTraits {
                                    : kSparse ? kGatherWarp0 + kGatherWarps
                                              : 6;
   static constexpr int kQk2Warp = kRoleWarps;   // second QK issuer (dense one-token kernel)
+  // PV issuers: lanes 0-3 of softmax warp 0 in the FP8 and multi-token
+  // kernels (in the latter warps 1-3 hold rows), else lane 0 of each softmax
+  // warp (measured faster in the one-token bf16, FP4 and sparse kernels)
+  static constexpr bool kPvOneWarp = kFp8 || kMulti;
   static constexpr int kThreads = 32 * (kRoleWarps + (kSplitQK ? 1 : 0));
   // FP8: two bf16 stages and a two-slot ring of raw tiles beside them.
   // FP4: three bf16 stages, each raw tile landing in the last
@@ -592,7 +596,7 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
       // sparse: one byte-count arrival per gather warp
       mbar_init(&ctrl->full[i],
                 MT::kQuant ? kDequantWarps : (MT::kSparse ? kGatherWarps : 1));
-      mbar_init(&ctrl->empty[i], kPvLanes);   // one commit per PV lane
+      mbar_init(&ctrl->empty[i], kPvLanes);   // one commit per PV issuer
     }
     for (int i = 0; i < kStages; ++i) mbar_init(&ctrl->raw_full[i], 1);
     for (int i = 0; i < kFp8RawSlots; ++i) mbar_init(&ctrl->raw_empty[i], kDequantWarps);
@@ -1380,17 +1384,21 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
           tc_fence_before();
           if (named_bar_or(1, 128, !ok)) { failed = true; break; }
         }
-        if (w == 0) {
-          // PV(i): lanes 0-3 of this warp (which holds no rows) each issue
-          // one 128-dim block of O^T += V^T P^T over the staged tile, then
-          // commit it to o_done[i % 2] and to the stage's empty barrier
-          // (o_done first: a stage seen free implies its PV seen done).
-          if (lane < kPvLanes) {
+        {
+          // PV(i), one 128-dim block b of O^T += V^T P^T over the staged tile
+          // per issuer: lane 0 of each softmax warp w (b = w; four warps
+          // overlap in the tensor pipe), or, in the FP8 and multi-token
+          // kernels, lanes 0-3 of warp 0, which holds no rows (b = lane).  Each issuer then commits its block to o_done[i % 2] and
+          // to the stage's empty barrier (o_done first: a stage seen free
+          // implies its PV seen done).
+          const bool issuer = MT::kPvOneWarp ? (w == 0 && lane < kPvLanes) : lane == 0;
+          if (issuer) {
+            const int b = MT::kPvOneWarp ? lane : w;
             tc_fence_after();
-            issue_pv_block(tmem + MT::kColO + lane * NP,
+            issue_pv_block(tmem + MT::kColO + b * NP,
                            pv_a0 + static_cast<uint64_t>((stage * kTileBytes) >> 4),
-                           pv_b0 + static_cast<uint64_t>((stage * kTileBytes) >> 4), idesc_pv,
-                           lane, first);
+                           pv_b0 + static_cast<uint64_t>((stage * kTileBytes) >> 4), idesc_pv, b,
+                           first);
             mma_commit(&ctrl->o_done[i & 1]);
             mma_commit(&ctrl->empty[stage]);
           }
@@ -1457,11 +1465,11 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
         ctrl->abort_flag = 1;
       }
       // drain: every PV issued here completes before tensor memory is released
-      if (w == 0) {
-        if (lane < kPvLanes) mma_commit(&ctrl->mma_drain[1]);
-        if (lane == 0) (void)mbar_wait(&ctrl->mma_drain[1], 0, nullptr, kWaitLimitNs);
-        __syncwarp();
-      }
+      if (MT::kPvOneWarp ? (w == 0 && lane < kPvLanes) : lane == 0)
+        mma_commit(&ctrl->mma_drain[1]);
+      if (lane == 0 && (!MT::kPvOneWarp || w == 0))
+        (void)mbar_wait(&ctrl->mma_drain[1], 0, nullptr, kWaitLimitNs);
+      __syncwarp();
     }
   }
 
