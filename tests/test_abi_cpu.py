@@ -92,6 +92,21 @@ def test_plans_beyond_256_row_sets(m, kw):
     small = m.mla_decode_plan(_problem(m, **dict(kw, batch=2)), None, 152)
     assert plan.smem_bytes <= small.smem_bytes
 
+
+@pytest.mark.parametrize("kw,S,prefix_pass", [
+    (dict(batch=64), 64, 0), (dict(batch=256), 256, 0), (dict(batch=257), 257, 1),
+    (dict(batch=150, q_len=2, kv_dtype=1), 150, 0),    # FP8 drafts: room for 150 rows' prefixes
+    (dict(batch=160, q_len=2, kv_dtype=1), 160, 1),    # ... not for 160 beside its buffers
+    (dict(batch=80, q_len=4, topk_width=2048), 320, 1),
+])
+def test_plan_reports_its_prefix_pass(m, kw, S, prefix_pass):
+    """The decode kernel keeps the work split's per-row-set prefixes in
+    shared memory when they fit (at most 256 row sets); otherwise each launch
+    runs the one-block prefix pre-pass first, which the plan reports."""
+    plan = m.mla_decode_plan(_problem(m, **kw), None, 152)
+    assert plan.num_streams == S and plan.prefix_pass == prefix_pass
+    assert plan.smem_bytes <= 232448
+
 @pytest.mark.parametrize("kw,code", [
     (dict(page_size=96), -2), (dict(page_size=8), -2), (dict(page_size=256), -2), (dict(num_heads=0), -1),
     (dict(num_heads=33), -2), (dict(q_len=0), -1), (dict(batch=-1), -1),

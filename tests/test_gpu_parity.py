@@ -450,3 +450,24 @@ def test_more_row_sets_than_shared_memory_holds(name, q_len):
     req = [0, 3, 255, 256, 257, 400, 511]
     compare(O.decode(batch, requests=req), o, o_lat, lse, label=f"{name}-512",
             lse_ref=O.decode(batch, requests=req, q_hat=q_hat))
+
+
+@pytest.mark.parametrize("name,batch,q_len", [("sparse_small", 80, 4), ("fp8_small", 160, 2)])
+def test_prefix_pass_sparse_and_fp8_drafts(name, batch, q_len):
+    """Row-set counts that need the prefix pre-pass in the sparse kernel (320
+    row sets of one draft each) and in the FP8 multi-token kernel (160 draft
+    pairs: too many prefixes for the shared memory beside its buffers);
+    split over 40 CTAs, sampled requests against the oracle."""
+    w = W.with_overrides(W.SMALL_WORKLOADS[name], batch=batch, q_len=q_len, seq_lo=200,
+                         seq_hi=700)
+    batch_ = W.generate(w)
+    q_hat = oracle_q_hat(batch_)
+    step = make_step(batch_, sm_count=40, absorb=False)
+    assert step.plan.prefix_pass == 1
+    upload_q_hat(step, q_hat)
+    step.step()
+    o, o_lat, lse = gpu_outputs(step)
+    assert step.status() == 0
+    req = [0, 1, batch // 2, batch - 1]
+    compare(O.decode(batch_, requests=req), o, o_lat, lse, label=f"{name}-prefix",
+            lse_ref=O.decode(batch_, requests=req, q_hat=q_hat))
