@@ -60,6 +60,7 @@ constexpr int kMmaWarp = 5;
 constexpr int kDequantWarp0 = 6;    // FP8 / FP4 modes: warps 6..11 dequantise
 constexpr int kDequantWarps = 6;
 constexpr int kGroupSets = kDequantWarps * 32 / kTile;   // threads per row in the dequant
+constexpr int kFp8Items = 36;       // FP8 dequant work items per tile: 18 groups x 2 row halves
 // P (bf16 [padded heads][64 tokens], the B operand of PV) lives in the RoPE
 // chunk of its own tile's stage: QK(i) is the only reader of that chunk and
 // P(i) is written after S(i) is complete, so every stage carries its own P.
@@ -152,6 +153,7 @@ struct __align__(8) Ctrl {
   uint64_t o_done[2];        // PV(j) completed, on o_done[j % 2]
   uint64_t mma_drain[3];     // the issuers' final commits (QK, PV, second QK)
   uint64_t mask[kStages];    // per-stage live-row mask (bit t = row t live)
+  uint64_t dq_part[kStages];  // FP8: dequant -> QK, a stage's first phase converted
   uint64_t raw_full[kStages];       // FP8 / FP4: producer -> dequant, bytes landed
   uint64_t raw_empty[kFp8RawSlots]; // FP8: dequant -> producer, raw slot consumed
   uint64_t raw_mask[kFp8RawSlots];  // FP8: live-row mask of the raw tile
@@ -599,6 +601,7 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
       mbar_init(&ctrl->empty[i], kPvLanes);   // one commit per PV issuer
     }
     for (int i = 0; i < kStages; ++i) mbar_init(&ctrl->raw_full[i], 1);
+    for (int i = 0; i < kStages; ++i) mbar_init(&ctrl->dq_part[i], kDequantWarps);
     for (int i = 0; i < kFp8RawSlots; ++i) mbar_init(&ctrl->raw_empty[i], kDequantWarps);
     for (int i = 0; i < 2; ++i) ctrl->rescale_tile[i] = -1;
     mbar_init(&ctrl->s_full, MT::kSplitS ? 2 : 1);   // one commit per QK issuer
@@ -908,13 +911,29 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
       if (lane < nl) {
         // polled by lane 0 with a short sleep (measured to wake sooner than a
         // suspending mbarrier.try_wait); the other issuing lane follows it
+        // (FP8: the tile's first dequant phase, not the whole tile)
         auto ready = [&](int32_t t, int st, bool first, int32_t sg) -> bool {
           bool r = false;
           if (lane == 0)
             r = (!first || mbar_poll(&ctrl->q_ready, sg & 1)) &&
-                mbar_poll(&ctrl->full[st], (t / kNumStages) & 1) &&
+                mbar_poll(MT::kRawRing ? &ctrl->dq_part[st] : &ctrl->full[st],
+                          (t / kNumStages) & 1) &&
                 (t < 1 || mbar_poll(&ctrl->s_free, (t - 1) & 1));
           return __shfl_sync(gmask, r, 0);
+        };
+        // bounded wait for one barrier phase, lane 0 polling
+        auto wait_phase = [&](uint64_t* bar, uint32_t parity) -> bool {
+          bool r = false;
+          if (lane == 0) r = mbar_poll(bar, parity);
+          if (__shfl_sync(gmask, r, 0)) return true;
+          const uint64_t t0 = globaltimer_ns();
+          while (true) {
+            __nanosleep(20);
+            if (lane == 0) r = mbar_poll(bar, parity);
+            if (__shfl_sync(gmask, r, 0)) return true;
+            if (__shfl_sync(gmask, *abort_flag || globaltimer_ns() - t0 > kWaitLimitNs, 0))
+              return false;
+          }
         };
         Walker wk;
         wk.init(prefix, S, g0);
@@ -937,7 +956,47 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
             }
           }
           tc_fence_after();
-          issue_my_qk(st, warp != kMmaWarp || lane == 1);
+          if constexpr (MT::kRawRing) {
+            // FP8: QK follows the dequant's two phases (chunks {0, 1, 4, 5},
+            // then {2, 3, 6, 7} and RoPE); each lane of a split QK takes its
+            // half: lane L chunks 4L .. 4L + 3 and RoPE steps 2L, 2L + 1
+            const uint64_t b0 = qk_b0 + static_cast<uint64_t>((st * kTileBytes) >> 4);
+            const int hl = MT::kSplitS ? lane : 0;
+            const uint32_t col = hl ? MT::kColS2 : MT::kColS;
+            auto chunk = [&](int ch, bool first_mma) {
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                mma_bf16_ts(tmem + col, tmem + MT::kColQ + (ch * 4 + k) * 8,
+                            b0 + ((ch * kChunkBytes + k * 32) >> 4), idesc_qk,
+                            (first_mma && k == 0) ? 0u : 1u);
+            };
+            chunk(4 * hl, true);
+            chunk(4 * hl + 1, false);
+            if constexpr (!MT::kSplitS) {
+              chunk(4, false);
+              chunk(5, false);
+            }
+            bool ok = wait_phase(&ctrl->full[st], (t / kNumStages) & 1);
+            if (ok) {
+              tc_fence_after();
+              chunk(4 * hl + 2, false);
+              chunk(4 * hl + 3, false);
+              if constexpr (!MT::kSplitS) {
+                chunk(6, false);
+                chunk(7, false);
+              }
+              const int k0 = MT::kSplitS ? 2 * hl : 0, k1 = MT::kSplitS ? k0 + 2 : 4;
+              for (int k = k0; k < k1; ++k)
+                mma_bf16_ss(tmem + col, qr_a0 + ((k * 32) >> 4),
+                            b0 + (((kChunks - 1) * kChunkBytes + k * 32) >> 4), idesc_qk, 1u);
+            }
+            if (!ok) {
+              failed = true;
+              break;
+            }
+          } else {
+            issue_my_qk(st, warp != kMmaWarp || lane == 1);
+          }
           mma_commit(&ctrl->s_full);
           seg = sg;
           wk.next(prefix, S);
@@ -975,7 +1034,17 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
                                     (((u0 + q) ^ (r & 7)) << 4)) = o[q];
       };
       if constexpr (MT::kRawRing) {
-        // FP8: raw slot rs -> bf16 stage bs, all 18 groups of a row at once
+        // FP8: raw slot rs -> bf16 stage bs in two phases, the first
+        // published on its own barrier as soon as every dequant warp has
+        // finished it, so that QK starts on a tile before the whole tile is
+        // converted: chunks {0, 1, 4, 5} (the first two chunks of each QK
+        // half), then {2, 3, 6, 7} and the RoPE chunk.  (Each publication
+        // costs every warp a proxy fence: five phases measured slower.)  The
+        // work is 36 items (one group of 32 values for 32 rows) in that
+        // order; warp dw takes items dw + 6k at step k, so the first phase
+        // (items 0-15) is complete after step 2 (dq_part) and the second
+        // after step 5 (full).
+        const int dw = warp - kDequantWarp0;
         for (int32_t i = 0; i < ntiles; ++i) {
           const int rs = i % MT::kRawSlots;
           const int bs = i % kNumStages;
@@ -986,22 +1055,40 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
             break;
           }
           const uint64_t mask = ctrl->raw_mask[rs];
-          const bool live = (mask >> r) & 1ull;
-          const uint8_t* row_ptr = sRaw + rs * MT::kRawTileBytes + r * MT::kRowBytes;
-          uint8_t* dst = sStage + bs * kTileBytes + r * 128;
+          const uint8_t* raw_tile = sRaw + rs * MT::kRawTileBytes;
+          uint8_t* tile = sStage + bs * kTileBytes;
 #pragma unroll 2
-          for (int k = 0; k < kDqk / 32 / kGroupSets; ++k) {
-            const int g = gset + kGroupSets * k;
+          for (int k = 0; k < kFp8Items / kDequantWarps; ++k) {
+            const int item = dw + kDequantWarps * k;
+            int g, h;
+            if (item >= 32) {                        // the RoPE chunk: groups 16, 17
+              g = 16 + ((item - 32) >> 1);
+              h = (item - 32) & 1;
+            } else {                                 // chunk pair {cp, cp + 4}
+              const int cp = item >> 3, within = item & 7, gi = within >> 1;
+              h = within & 1;
+              g = gi < 2 ? 2 * cp + gi : 2 * cp + 6 + gi;
+            }
+            const int rr = 32 * h + lane;
+            const bool odd_r = (rr & 1) != 0;   // rows of odd index start 2 bytes past a word
             uint4 o[4];
-            if (live) {
+            if ((mask >> rr) & 1ull) {
               Fp8Group f;
-              load_fp8_group(row_ptr, g, odd, f);
-              convert_fp8_group(f, odd, o);
+              load_fp8_group(raw_tile + rr * MT::kRowBytes, g, odd_r, f);
+              convert_fp8_group(f, odd_r, o);
             } else {
 #pragma unroll
               for (int q = 0; q < 4; ++q) o[q] = make_uint4(0, 0, 0, 0);
             }
-            store_group(dst, g, o);
+            uint8_t* dst = tile + (g >> 1) * kChunkBytes + rr * 128;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              *reinterpret_cast<uint4*>(dst + ((((g & 1) * 4 + q) ^ (rr & 7)) << 4)) = o[q];
+            if (k == 2) {
+              fence_proxy_async_smem();   // generic stores -> tensor-core reads
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&ctrl->dq_part[bs]);
+            }
           }
           if (dt == 0) ctrl->mask[bs] = mask;
           fence_proxy_async_smem();   // generic stores -> tensor-core reads
