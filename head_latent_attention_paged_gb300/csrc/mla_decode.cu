@@ -1317,49 +1317,16 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
           tc_fence_after();
           float y[32];
           if (warp_has_heads) {
-            {
-              uint32_t r[32];
-              tmem_ld32(tmem + lane_base + MT::kColS, r);
+            // lane l < 16 reads columns 0..31 of its row, lane l + 16
+            // columns 32..63 of the same row (S = S_a + S_b when split)
+            uint32_t r[32];
+            tmem_ld_rows16_split32(tmem + lane_base + MT::kColS, r);
 #pragma unroll
-              for (int t = 0; t < 32; ++t) y[t] = __uint_as_float(r[t]);
-              if constexpr (MT::kSplitS) {   // S = S_a + S_b
-                tmem_ld32(tmem + lane_base + MT::kColS2, r);
+            for (int t = 0; t < 32; ++t) y[t] = __uint_as_float(r[t]);
+            if constexpr (MT::kSplitS) {
+              tmem_ld_rows16_split32(tmem + lane_base + MT::kColS2, r);
 #pragma unroll
-                for (int t = 0; t < 32; ++t) y[t] += __uint_as_float(r[t]);
-              }
-              if constexpr (MT::kSplitS && kThreads > 256) {
-                // fewer registers per thread: columns 32..63 in two halves
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                  uint32_t a[16];
-                  float z[16];
-                  tmem_ld16(tmem + lane_base + MT::kColS + 32 + 16 * q, a);
-#pragma unroll
-                  for (int e = 0; e < 16; ++e) z[e] = __uint_as_float(a[e]);
-                  tmem_ld16(tmem + lane_base + MT::kColS2 + 32 + 16 * q, a);
-#pragma unroll
-                  for (int e = 0; e < 16; ++e) {
-                    z[e] += __uint_as_float(a[e]);
-                    const float hi_col = __shfl_xor_sync(0xffffffffu, z[e], 16);
-                    if (half) y[16 * q + e] = hi_col;   // lane l+16 <- columns 32..63 of lane l
-                  }
-                }
-              } else {
-                float z[32];
-                tmem_ld32(tmem + lane_base + MT::kColS + 32, r);
-#pragma unroll
-                for (int t = 0; t < 32; ++t) z[t] = __uint_as_float(r[t]);
-                if constexpr (MT::kSplitS) {
-                  tmem_ld32(tmem + lane_base + MT::kColS2 + 32, r);
-#pragma unroll
-                  for (int t = 0; t < 32; ++t) z[t] += __uint_as_float(r[t]);
-                }
-#pragma unroll
-                for (int t = 0; t < 32; ++t) {
-                  const float hi_col = __shfl_xor_sync(0xffffffffu, z[t], 16);
-                  if (half) y[t] = hi_col;   // lane l+16 <- columns 32..63 of lane l
-                }
-              }
+              for (int t = 0; t < 32; ++t) y[t] += __uint_as_float(r[t]);
             }
           }
           tc_fence_before();
