@@ -118,10 +118,12 @@ struct ModeTraits {
                                    : kSparse ? kGatherWarp0 + kGatherWarps
                                              : 6;
   static constexpr int kQk2Warp = kRoleWarps;   // second QK issuer (dense one-token kernel)
-  // PV issuers: lanes 0-3 of softmax warp 0 in the FP8 and multi-token
-  // kernels (in the latter warps 1-3 hold rows), else lane 0 of each softmax
-  // warp (measured faster in the one-token bf16, FP4 and sparse kernels)
-  static constexpr bool kPvOneWarp = kFp8 || kMulti;
+  // PV issuers, as measured per kernel: lanes 0-1 of softmax warps 0 and 1
+  // (which hold no rows) in the one-token FP8 kernel; lanes 0-3 of softmax
+  // warp 0 in the multi-token kernels (whose warps 1-3 hold rows); lane 0 of
+  // each softmax warp in the one-token bf16, FP4 and sparse kernels
+  static constexpr bool kPvTwoWarps = kMode == kModeDenseFp8;
+  static constexpr bool kPvOneWarp = (kFp8 || kMulti) && !kPvTwoWarps;
   static constexpr int kThreads = 32 * (kRoleWarps + (kSplitQK ? 1 : 0));
   // FP8: two bf16 stages and a two-slot ring of raw tiles beside them.
   // FP4: three bf16 stages, each raw tile landing in the last
@@ -1441,13 +1443,15 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
         {
           // PV(i), one 128-dim block b of O^T += V^T P^T over the staged tile
           // per issuer: lane 0 of each softmax warp w (b = w; four warps
-          // overlap in the tensor pipe), or, in the FP8 and multi-token
-          // kernels, lanes 0-3 of warp 0, which holds no rows (b = lane).  Each issuer then commits its block to o_done[i % 2] and
+          // overlap in the tensor pipe), lanes 0-1 of warps 0-1 (b = 2w +
+          // lane; one-token FP8), or lanes 0-3 of warp 0, which holds no rows
+          // (b = lane; multi-token).  Each issuer then commits its block to o_done[i % 2] and
           // to the stage's empty barrier (o_done first: a stage seen free
           // implies its PV seen done).
-          const bool issuer = MT::kPvOneWarp ? (w == 0 && lane < kPvLanes) : lane == 0;
+          const bool issuer = MT::kPvTwoWarps ? (w < 2 && lane < 2)
+                              : MT::kPvOneWarp ? (w == 0 && lane < kPvLanes) : lane == 0;
           if (issuer) {
-            const int b = MT::kPvOneWarp ? lane : w;
+            const int b = MT::kPvTwoWarps ? 2 * w + lane : MT::kPvOneWarp ? lane : w;
             tc_fence_after();
             issue_pv_block(tmem + MT::kColO + b * NP,
                            pv_a0 + static_cast<uint64_t>((stage * kTileBytes) >> 4),
@@ -1519,9 +1523,9 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
         ctrl->abort_flag = 1;
       }
       // drain: every PV issued here completes before tensor memory is released
-      if (MT::kPvOneWarp ? (w == 0 && lane < kPvLanes) : lane == 0)
+      if (MT::kPvTwoWarps ? (w < 2 && lane < 2) : MT::kPvOneWarp ? (w == 0 && lane < kPvLanes) : lane == 0)
         mma_commit(&ctrl->mma_drain[1]);
-      if (lane == 0 && (!MT::kPvOneWarp || w == 0))
+      if (lane == 0 && (MT::kPvTwoWarps ? w < 2 : (!MT::kPvOneWarp || w == 0)))
         (void)mbar_wait(&ctrl->mma_drain[1], 0, nullptr, kWaitLimitNs);
       __syncwarp();
     }
