@@ -116,6 +116,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
+    __nanosleep(32);   // leave the issue slots to the warps doing work
     if (mbar_test(bar, parity)) return true;
     if (abort != nullptr && *abort) return false;
     if (globaltimer_ns() - t0 > limit_ns) return false;
