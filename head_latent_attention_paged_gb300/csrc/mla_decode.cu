@@ -130,6 +130,11 @@ struct ModeTraits {
   // kRawTileBytes of the stage it is dequantised into.
   static constexpr bool kRawRing = kFp8;
   static constexpr int kNumStages = kRawRing ? kFp8Stages : kStages;   // bf16 tiles in flight
+  // q_hat rows loaded by both lanes of a pair (measured faster in these
+  // kernels; the FP8, sparse and quantised multi-token ones keep one lane
+  // per row)
+  static constexpr bool kQLoadSplit =
+      kMode == kModeDenseBf16 || kMode == kModeDenseFp4 || kMode == kModeDenseMulti;
   static constexpr int kQBatch = kThreads > 256 ? (kQRopeSmem ? 2 : 3) : (kQRopeSmem ? 4 : 5);   // q_hat chunks per load batch
   static constexpr int kRawSlots = kRawRing ? kFp8RawSlots : kStages;
   static constexpr int kRawOffset = kTileBytes - kRawTileBytes;
@@ -316,13 +321,13 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 // 32 + h (warps 2 and 3 only, so warps 0 and 1 leave their SM sub-partitions
 // to the producer and MMA warps); a multi-token row set (up to 48 rows)
 // starts at M-row 16 (warps 1-3).  The 512 latent values go to TMEM, packed
-// two per column, and the 64 RoPE values either to TMEM as well or
-// (kRopeSmem) to a shared-memory operand (row m at m * 128 bytes, 16-byte
-// units swizzled by m % 8).  Every softmax warp calls this; M-rows of warps
-// kRowWarp0.. without a row get zeros, the M-rows below are not written
-// (their S rows are never read).  TMEM loads go in batches of
-// kBatch chunks of 64 values to keep many in flight (fewer in the kernels
-// whose thread count leaves fewer registers per thread).
+// two per column, and the 64 RoPE values to a shared-memory operand (row m
+// at m * 128 bytes, 16-byte units swizzled by m % 8).  Every softmax warp
+// calls this; M-rows of warps kRowWarp0.. without a row get zeros, the
+// M-rows below are not written (their S rows are never read).  Global loads
+// go in batches of kBatch chunks of 64 values to keep many in flight (fewer
+// in the kernels whose thread count leaves fewer registers per thread).
+// One thread per row (lanes 0-15): the kernels where that measured faster.
 template <int kRowWarp0, bool kRopeSmem, int kBatch>
 __device__ __forceinline__ void load_q(const uint16_t* q_rows, int nrows, uint32_t taddr_lane,
                                        uint8_t* q_rope, int lane, int w) {
@@ -366,6 +371,50 @@ __device__ __forceinline__ void load_q(const uint16_t* q_rows, int nrows, uint32
         *reinterpret_cast<uint4*>(row + ((u ^ (m & 7)) << 4)) = v;
       }
     }
+  }
+}
+
+// Both lanes of a pair per row (l and l + 16).
+template <int kRowWarp0, bool kRopeSmem, int kBatch>
+__device__ __forceinline__ void load_q_split(const uint16_t* q_rows, int nrows, uint32_t taddr_lane,
+                                       uint8_t* q_rope, int lane, int w) {
+  static_assert(kRopeSmem && 4 % kBatch == 0, "q_hat's RoPE part is a shared-memory operand");
+  if (w < kRowWarp0) return;
+  // Lanes l and l + 16 share row l: lane l takes the latent chunks 0-3 and
+  // RoPE units 0-3, lane l + 16 chunks 4-7 and units 4-7 (one 16x32bx2
+  // store writes both halves of a row)
+  const int hf = lane >> 4;
+  const int r = (w - kRowWarp0) * 16 + (lane & 15);
+  const bool live = r < nrows;
+  const uint4* src = reinterpret_cast<const uint4*>(q_rows + static_cast<int64_t>(live ? r : 0) * kDqk);
+#pragma unroll
+  for (int cb = 0; cb < 4; cb += kBatch) {
+    uint4 v[kBatch][8];
+#pragma unroll
+    for (int c = 0; c < kBatch; ++c)
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        v[c][q] = live ? __ldg(src + (4 * hf + cb + c) * 8 + q) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int c = 0; c < kBatch; ++c) {
+      uint32_t rr[32];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        rr[4 * q] = v[c][q].x;
+        rr[4 * q + 1] = v[c][q].y;
+        rr[4 * q + 2] = v[c][q].z;
+        rr[4 * q + 3] = v[c][q].w;
+      }
+      tmem_st_rows16_split128(taddr_lane + (cb + c) * 32, rr);
+    }
+  }
+  const int m = 16 * w + (lane & 15);
+  uint8_t* row = q_rope + m * 128;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int uu = 4 * hf + u;
+    const uint4 v = live ? __ldg(src + (kChunks - 1) * 8 + uu) : make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint4*>(row + ((uu ^ (m & 7)) << 4)) = v;
   }
 }
 
@@ -1274,10 +1323,17 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
         return (static_cast<int64_t>(gm.b) * p.q_len + gm.j0) * H;
       };
       auto rows_of = [&](int32_t s) -> int { return stream_geom(s, p.q_len, G).nq * H; };
+      // a row set's queries into TMEM (and the RoPE part into shared memory)
+      auto load_rows = [&](int32_t st_) {
+        if constexpr (MT::kQLoadSplit)
+          load_q_split<MT::kRowWarp0, MT::kQRopeSmem, MT::kQBatch>(
+              p.q_hat + first_row(st_) * kDqk, rows_of(st_), tmem + lane_base, sQr, lane, w);
+        else
+          load_q<MT::kRowWarp0, MT::kQRopeSmem, MT::kQBatch>(
+              p.q_hat + first_row(st_) * kDqk, rows_of(st_), tmem + lane_base, sQr, lane, w);
+      };
       // the first stream's queries
-      load_q<MT::kRowWarp0, MT::kQRopeSmem, MT::kQBatch>(p.q_hat + first_row(wk.s) * kDqk,
-                                                         rows_of(wk.s), tmem + lane_base, sQr,
-                                                         lane, w);
+      load_rows(wk.s);
       if constexpr (MT::kQRopeSmem) fence_proxy_async_smem();   // RoPE rows -> tensor-core reads
       tc_fence_before();
       __syncwarp();
@@ -1470,9 +1526,7 @@ __global__ void __launch_bounds__(ModeTraits<kMode>::kThreads, 1)
           // epilogue (which first waits for PV(i)) instead of delaying P(i).
           Walker nx = wk;
           nx.next(prefix, S);
-          load_q<MT::kRowWarp0, MT::kQRopeSmem, MT::kQBatch>(p.q_hat + first_row(nx.s) * kDqk,
-                                                             rows_of(nx.s), tmem + lane_base, sQr,
-                                                             lane, w);
+          load_rows(nx.s);
           if constexpr (MT::kQRopeSmem) fence_proxy_async_smem();
           tc_fence_before();
           __syncwarp();
