@@ -2,41 +2,44 @@
 //
 // One CTA per SM walks a contiguous range of 64-token tiles of the
 // concatenated row sets ("streams"): one per (request, query token), or, in
-// the multi-token mode (dense bf16 cache, several draft tokens), one per
-// group of G draft tokens of a request whose G * H rows share every staged
-// tile.  Per tile:
+// the multi-token mode (several draft tokens over a bf16, FP4 or FP8 cache),
+// one per group of G draft tokens of a request whose G * H rows share every
+// staged tile.  Per tile:
 //
 //   producer warp : stages the 64 cached rows (576 bf16 each) in shared
 //                   memory once -- TMA tiles for dense pages (for sparse
 //                   top-k rows, four gather warps issue TMA gather4 loads,
-//                   16 rows each) -- as nine
-//                   [64 rows x 128 B] chunks in the 128-byte swizzle layout,
-//                   three tiles in flight.  FP8 / FP4 caches: one bulk copy
-//                   of the tile's quantised rows (594 or 324 bytes), FP8
-//                   into a ring of two raw slots beside two bf16 stages, FP4
-//                   into the tail of the bf16 stage it becomes, and
+//                   16 rows each) -- as nine [64 rows x 128 B] chunks in the
+//                   128-byte swizzle layout, three tiles in flight.  FP8 /
+//                   FP4 caches: one bulk copy of the tile's quantised rows
+//                   (594 or 324 bytes), FP8 into a ring of two raw slots
+//                   beside two bf16 stages, FP4 into the tail of the bf16
+//                   stage it becomes, and
 //   dequant warps : (FP8 / FP4) turn each row's codes and e8m0 scales into
 //                   bf16 values code * 2^(scale - 127), exactly, written as
-//                   the swizzled bf16 tile (FP4 in place: first the chunks
+//                   the swizzled bf16 tile (FP8 in two phases, the first
+//                   published early for QK; FP4 in place: first the chunks
 //                   below the raw bytes, then, once every dequant warp holds
 //                   the rest of its groups in registers, the chunks over
 //                   them); rows with no live token become zeros.
-//   MMA warp      : S[h, t]   = q_hat[h, :576] . row[t, :576]      (tcgen05,
-//                   M = 64 rows with q_hat read from TMEM -- its RoPE part
-//                   from shared memory in the multi-token mode -- N = 64
-//                   tokens from shared memory, K = 576, f32 in TMEM);
-//                   O^T[d, h] += sum_t row[t, d] P[h, t]            (tcgen05,
-//                   M = 128 latent dims x 4, N = padded rows, K = 64 tokens,
-//                   A = the same staged tile read MN-major).
+//   QK issuers    : S[h, t] = q_hat[h, :576] . row[t, :576]          (tcgen05,
+//                   M = 64 rows with q_hat's latent part read from TMEM and
+//                   its RoPE part from shared memory, N = 64 tokens from
+//                   shared memory, K = 576, f32 in TMEM), split into two
+//                   halves of K (two S accumulators) where TMEM allows.
 //   softmax warps : online softmax in the exp2 domain on S read from TMEM
 //                   (two lanes per row; in the multi-token mode each row
-//                   masked past its own draft's causal window), P written to shared memory as
-//                   bf16, lazy rescale of O^T in TMEM when the running max
-//                   grows by more than 2^8; at a stream change they write the
-//                   next stream's q_hat into TMEM, and at the end of each
-//                   segment the normalised result (or, for a stream split
-//                   over several CTAs, a partial plus its lse, merged by the
-//                   combine kernel that follows this one).
+//                   masked past its own draft's causal window), P written to
+//                   shared memory as bf16, lazy rescale of O^T in TMEM when
+//                   the running max grows by more than 2^8; then four of
+//                   their lanes issue O^T[d, h] += sum_t row[t, d] P[h, t]
+//                   (tcgen05, M = 128 latent dims x 4, N = padded rows, K =
+//                   64 tokens, A = the staged tile read MN-major).  At a
+//                   stream change they write the next stream's q_hat into
+//                   TMEM, and at the end of each segment the normalised
+//                   result (or, for a stream split over several CTAs, a
+//                   partial plus its lse, merged by the combine kernel that
+//                   follows this one).
 //
 // All heads of a row set reuse each staged tile, so every cached byte is read
 // from HBM once per row set.  Waits are bounded (sm103_ptx.cuh); a timeout
