@@ -3,9 +3,9 @@
 
 A step is the whole hot path over one synthetic decode batch, one call of
 mla_decode_step: the attention pass over the paged latent cache, the LSE
-merge of split partials and the W_UV up-projection (three kernels, each
-launched as a programmatic dependent of the one before; the absorbed query is
-an input, precomputed once).  The
+merge of split partials inside the W_UV up-projection (two kernels, the
+second launched as a programmatic dependent of the first; the absorbed query
+is an input, precomputed once).  The
 default workload is the GLM-4.7-Flash-shaped dense decode: batch 64, 20
 heads, q_len 1, seq_lens ~ U[1024, 8192], page 64, bf16 latent cache.
 
@@ -474,8 +474,8 @@ def run_gpu(args, world, rank, local):
         raise SystemExit(f"decode reported status {step.status():#x}")
 
     # The K timed steps: each one call of mla_decode_step (the attention pass,
-    # the merge and W_UV: three launches, each a programmatic dependent of the
-    # one before), bracketed by events on the launching stream.
+    # then the merge inside the W_UV launch, a programmatic dependent of the
+    # first), bracketed by events on the launching stream.
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     if world > 1:
         torch.distributed.barrier()

@@ -358,18 +358,20 @@ int launch_merge(const mla_plan& plan, const int32_t* seq_lens, const uint8_t* w
   if (plan.num_streams == 0) return MLA_OK;
   CombineParams cp;
   fill_combine_params(plan, ws, seq_lens, o_lat, lse, &cp);
-  // the merge over all SMs (one block per row of a row set), then, with
-  // W_UV, the up-projection per head: each a programmatic dependent of the
-  // launch before it
-  cudaError_t err = launch_combine(cp, st);
-  if (err == cudaSuccess && w_uv != nullptr) {
+  // without W_UV: the merge over all SMs (one block per row of a row set);
+  // with it: the merge inside the up-projection's blocks (per head, 128
+  // output dims and a row block).  Either is a programmatic dependent of the
+  // decode launch.
+  cudaError_t err;
+  if (w_uv == nullptr) {
+    err = launch_combine(cp, st);
+  } else {
     const mla_problem& pr = plan.problem;
     CUtensorMap w_map;
     if (!make_map_bf16(&w_map, w_uv, kDv, static_cast<uint64_t>(pr.num_heads) * kDc, kDv * 2, 64,
                        64))
       return MLA_ERR_CUDA;
-    err = launch_uv_proj_tma(&w_map, o_lat, static_cast<uint16_t*>(out),
-                             pr.batch * pr.q_len, pr.num_heads, plan.sm_count, st);
+    err = launch_merge_uv(&w_map, cp, static_cast<uint16_t*>(out), plan.sm_count, st);
   }
   return err == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }

@@ -1,7 +1,9 @@
 // The smaller kernels of the decode step:
 //   * mla_combine_kernel : LSE merge of the split-KV partials of each row set
 //                          (one block per row: a head, or a draft token x head);
-//   * mla_uv_kernel      : o = W_UV[h]^T o_lat (tcgen05, per head);
+//   * mla_uv_kernel      : o = W_UV[h]^T o_lat (tcgen05, per head); its
+//                          merging variant also does the LSE merge of the
+//                          split rows (the decode step's second launch);
 //   * mla_absorb_kernel  : q_hat = [W_UK[h] q_nope || q_rope] (query absorption,
 //                          tcgen05).
 #include <cuda_bf16.h>
@@ -18,9 +20,6 @@ namespace mla {
 namespace {
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
-__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
-  return __uint_as_float(static_cast<uint32_t>(b) << 16);
-}
 __device__ __forceinline__ uint16_t float_to_bf16_bits(float f) {
   __nv_bfloat16 h = __float2bfloat16_rn(f);
   return *reinterpret_cast<uint16_t*>(&h);
@@ -100,10 +99,27 @@ __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(const Comb
   const float* plse = p.part_lse + static_cast<int64_t>(s + c0) * p.rows + h;
   const float4* po = reinterpret_cast<const float4*>(p.part_o) +
                      (static_cast<int64_t>(s + c0) * p.rows + h) * (kDc / 4) + tid;
-  const MergedRow mr = merge_partials(plse, po, nseg, p.rows, static_cast<int64_t>(p.rows) * (kDc / 4));
+  const int64_t ostride = static_cast<int64_t>(p.rows) * (kDc / 4);
+  // every warp finds the weights (the same bits), then each thread merges
+  // its 4 dims, 8 partials' loads in flight at a time
+  const RowWeights rw = merge_weights(plse, nseg, p.rows);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k0 = 0; k0 < nseg; k0 += 8) {
+    float lv[8];
+    float4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const bool in = k0 + u < nseg;
+      lv[u] = in ? __ldcg(plse + (k0 + u) * static_cast<int64_t>(p.rows)) : -INFINITY;
+      v[u] = in ? __ldcg(po + (k0 + u) * ostride) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (k0 + u < nseg) merge_fma(acc, merge_weight(lv[u], rw.m), v[u]);
+  }
   const int64_t row = (static_cast<int64_t>(gm.b) * p.q_len + gm.j0) * p.heads + h;
-  reinterpret_cast<float4*>(p.o_lat + row * kDc)[tid] = mr.o;
-  if (tid == 0) p.lse[row] = mr.lse;
+  reinterpret_cast<float4*>(p.o_lat + row * kDc)[tid] = merge_scale(acc, rw.inv);
+  if (tid == 0) p.lse[row] = rw.lse;
 }
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {
@@ -209,31 +225,75 @@ cudaError_t launch_prefix(const DecodeParams& p, cudaStream_t stream) {
 // out from four threads (warps 0-3, 128 latent dims each) into four
 // accumulators that the epilogue sums.  N (16, 32 or 64 rows) is the smallest
 // row block whose grid fits the SMs, where one does.
+//
+// The merging variant (kMerge) is the step's last launch: it builds B from
+// the decode's output directly, merging the partials of the rows whose row
+// set was split over several CTAs (the same arithmetic as the merge kernel)
+// and writing those rows' merged o_lat and lse.  The two CTAs of the output
+// halves of one (head, row block) form a cluster: each merges half of the
+// rows and stores them, as bf16, into its own B and into the other's
+// (distributed shared memory), so every partial is read once.  The 512
+// threads keep four partials' loads in flight each; the work split is found
+// while the decode still runs.
 // ----------------------------------------------------------------------------
 namespace {
 constexpr int kUvA = 8 * 2 * kChunkBytes;   // 8 K-blocks x 2 n-chunks x 8 KB = 128 KB
-template <int N>
-struct Uv {
-  static constexpr int kThreads = N == 64 ? 256 : 128;
-  static constexpr int kB = 8 * N * 128;                     // 8 K-blocks x N rows x 128 B
-  static constexpr int kPieces = N * 64 / kThreads;          // 16-byte B pieces per thread
-  static constexpr int kTmemCols = 4 * N < 32 ? 32 : 4 * N;  // four accumulators
-  static constexpr int kSmem = kUvA + kB + 1024 + 64;
+
+struct MergeRow {   // one row of a merging block
+  int64_t obase;    // float4 index: the first partial's o (nseg > 0), the o_lat row (nseg == 0)
+  int64_t lbase;    // float index of the first partial's lse
+  int64_t orow;     // the row of o_lat and lse
+  int32_t nseg;     // > 0: partials to merge; 0: the decode's o_lat row is final; -1: no row
+  float m, inv;
+  int32_t pad;
 };
+
+template <int N, bool kMerge>
+struct Uv {
+  static constexpr int kThreads = kMerge ? 512 : (N == 64 ? 256 : 128);
+  static constexpr int kWarps = kThreads / 32;
+  static constexpr int kB = 8 * N * 128;                     // 8 K-blocks x N rows x 128 B
+  // 16-byte B pieces per thread (a merging CTA builds half of the rows)
+  static constexpr int kPieces = (kMerge ? N / 2 : N) * 64 / kThreads;
+  static constexpr int kTmemCols = 4 * N < 32 ? 32 : 4 * N;  // four accumulators
+  // merging blocks: N MergeRow, N + 1 row-set cost prefixes, 2 x kWarps scan sums
+  static constexpr int kScratch =
+      kMerge ? static_cast<int>(N * sizeof(MergeRow)) + (N + 1 + 2 * kWarps) * 4 : 0;
+  static constexpr int kSmem = kUvA + kB + 1024 + 64 + kScratch;
+};
+
+// Piece (row r, 8 latent dims 8 piece ..) of B as bf16: K-block piece / 8 of
+// the 128-byte-swizzled [kb][N rows][128 B] layout.  Returns its byte offset.
+template <int N>
+__device__ __forceinline__ uint32_t store_b_piece(uint8_t* sB, int r, int piece, float4 a, float4 b) {
+  const int kb = piece >> 3, w16 = piece & 7;
+  __nv_bfloat162 x0 = __floats2bfloat162_rn(a.x, a.y), x1 = __floats2bfloat162_rn(a.z, a.w);
+  __nv_bfloat162 x2 = __floats2bfloat162_rn(b.x, b.y), x3 = __floats2bfloat162_rn(b.z, b.w);
+  const uint32_t off = kb * (N * 128) + r * 128 + ((w16 ^ (r & 7)) << 4);
+  *reinterpret_cast<uint4*>(sB + off) =
+      make_uint4(*reinterpret_cast<uint32_t*>(&x0), *reinterpret_cast<uint32_t*>(&x1),
+                 *reinterpret_cast<uint32_t*>(&x2), *reinterpret_cast<uint32_t*>(&x3));
+  return off;
+}
 }  // namespace
 
-template <int N>
-__global__ void __launch_bounds__(Uv<N>::kThreads, 1)
+template <int N, bool kMerge>
+__global__ void __launch_bounds__(Uv<N, kMerge>::kThreads, 1)
     mla_uv_kernel(const __grid_constant__ CUtensorMap w_map, const float* o_lat,
-                  uint16_t* __restrict__ out, int rows, int heads) {
-  constexpr int kThreads = Uv<N>::kThreads;
+                  uint16_t* __restrict__ out, int rows, int heads,
+                  const __grid_constant__ CombineParams mp) {
+  constexpr int kThreads = Uv<N, kMerge>::kThreads;
+  constexpr int kWarps = Uv<N, kMerge>::kWarps;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + kUvA;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kUvA + Uv<N>::kB);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kUvA + Uv<N, kMerge>::kB);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2);
+  MergeRow* mrow = reinterpret_cast<MergeRow*>(smem + kUvA + Uv<N, kMerge>::kB + 64);
+  int32_t* sbefore = reinterpret_cast<int32_t*>(mrow + N);   // cost before row set s_lo + i
+  int32_t* wsum = sbefore + N + 1;                           // [2][kWarps]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.x;
   const int mt = blockIdx.y;          // output dims [128 mt, 128 mt + 128)
@@ -244,10 +304,13 @@ __global__ void __launch_bounds__(Uv<N>::kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 0) {
-    tmem_alloc(tslot, Uv<N>::kTmemCols);
+    tmem_alloc(tslot, Uv<N, kMerge>::kTmemCols);
     tmem_relinquish();
   }
   __syncthreads();
+  // merging blocks write into the other CTA of their cluster: it must have
+  // started first (this arrive; the matching wait precedes the first store)
+  if constexpr (kMerge) cluster_arrive_relaxed();
   if (tid == 0) {
     prefetch_tmap(&w_map);
     mbar_arrive_expect_tx(&bars[0], kUvA);
@@ -256,41 +319,240 @@ __global__ void __launch_bounds__(Uv<N>::kThreads, 1)
         tma_load_2d(sA + (kb * 2 + nc) * kChunkBytes, &w_map, &bars[0], mt * 128 + nc * 64,
                     h * kDc + kb * 64, 0ull);
   }
-  // o_lat is produced by the launches this one depends on: wait for them
-  // (the W_UV loads above already overlap their tail).  o_lat is not a
-  // restrict-qualified pointer on purpose: read-only-for-the-kernel loads
-  // could be scheduled ahead of this wait.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  // B: o_lat[r0 + r][h][k] -> bf16, [kb][r][128 B] swizzled.  Item e of
-  // this thread is piece (tid + kThreads e): row (tid + kThreads e) / 64,
-  // 8 consecutive k.
-  float4 va[Uv<N>::kPieces], vb[Uv<N>::kPieces];
+  // Merging blocks: row set s of token row R (request b = R / q_len, draft
+  // j = R % q_len) is b * ng + j / group.  This block's rows span the row
+  // sets s_lo .. s_hi (at most N of them).  The cost before each of them,
+  // the total cost and the total tile count give the decode grid's split
+  // (the CTAs c0 .. c1 whose partials hold the row set): summed here from
+  // seq_lens (an input of the step) before the wait when the decode kernel
+  // kept its prefixes in shared memory, else read from the pre-pass's.
+  [[maybe_unused]] const int S = mp.num_streams;
+  [[maybe_unused]] const int32_t ng = kMerge ? (mp.q_len + mp.group - 1) / mp.group : 1;
+  [[maybe_unused]] const int32_t max_tokens = mp.max_pages * mp.page_size;
+  // merging blocks run as clusters of the two output halves of one (head,
+  // row block): of the block's cnt rows, cluster CTA q merges the q-th half
+  // (rows first .. first + mine - 1) and hands them as bf16 to both halves' B
+  constexpr int kHalf = N / 2;
+  [[maybe_unused]] const uint32_t crank = kMerge ? cluster_ctarank() : 0u;
+  [[maybe_unused]] const int cnt = rows - r0 < N ? rows - r0 : N;
+  [[maybe_unused]] const int first = static_cast<int>(crank) * ((cnt + 1) / 2);
+  [[maybe_unused]] const int mine = crank == 0 ? (cnt + 1) / 2 : cnt / 2;
+  [[maybe_unused]] const int my_r = warp * 4 + (lane >> 3);   // a row of the half per 8 lanes
+  [[maybe_unused]] int32_t s_lo = 0, s_hi = 0, tot = 0, tiles = 0;
+  [[maybe_unused]] int32_t g_nseg = -1;
+  [[maybe_unused]] int64_t g_lbase = 0, g_obase = 0, g_orow = 0;
+  [[maybe_unused]] auto geometry = [&]() {
+    const int R = r0 + first + my_r;
+    if (my_r >= mine) return;
+    const int b = R / mp.q_len, j = R - b * mp.q_len;
+    const int32_t s = b * ng + j / mp.group;
+    const StreamGeom gm = stream_geom(s, mp.q_len, mp.group);
+    g_orow = static_cast<int64_t>(R) * heads + h;
+    g_obase = g_orow * (kDc / 4);
+    g_nseg = 0;
+    const int32_t len = stream_len(mp.seq_lens[b], mp.q_len, gm.j0 + gm.nq - 1, mp.causal,
+                                   mp.topk_width, max_tokens);
+    const int32_t nt = (len + kTile - 1) / kTile;
+    if (nt == 0) return;   // the decode wrote o_lat = 0, lse = -inf
+    const int32_t nctas = work_ctas(mp.num_ctas, tiles);
+    const int64_t before = sbefore[s - s_lo];
+    const int c0 = tile_owner(tile_cost_pos(before, 0, mp.stream_cost), tot, nctas);
+    const int c1 = tile_owner(tile_cost_pos(before, nt - 1, mp.stream_cost), tot, nctas);
+    if (c0 == c1) return;  // one CTA held the whole row set: its o_lat row is final
+    g_nseg = c1 - c0 + 1;
+    // partial slots hold mp.rows rows each; the row's index in its row set
+    g_lbase = static_cast<int64_t>(s + c0) * mp.rows + (j - gm.j0) * heads + h;
+    g_obase = g_lbase * (kDc / 4);
+  };
+  if constexpr (kMerge) {
+    const int last = (r0 + N < rows ? r0 + N : rows) - 1;
+    s_lo = (r0 / mp.q_len) * ng + (r0 % mp.q_len) / mp.group;
+    s_hi = (last / mp.q_len) * ng + (last % mp.q_len) / mp.group;
+    if (mp.prefix_ws == nullptr) {
+      int32_t carry_c = 0, carry_t = 0;
+      for (int base = 0; base < S; base += kThreads) {
+        const int t = base + tid;
+        int32_t vt = 0, vc = 0;
+        if (t < S) {
+          const StreamGeom gt = stream_geom(t, mp.q_len, mp.group);
+          const int32_t len = stream_len(mp.seq_lens[gt.b], mp.q_len, gt.j0 + gt.nq - 1,
+                                         mp.causal, mp.topk_width, max_tokens);
+          vt = (len + kTile - 1) / kTile;
+          vc = stream_cost(vt, mp.stream_cost);
+        }
+        const int32_t own = vc;
 #pragma unroll
-  for (int e = 0; e < Uv<N>::kPieces; ++e) {
-    const int idx = tid + kThreads * e;
-    const int r = idx >> 6, piece = idx & 63;
-    if (r0 + r < rows) {
-      const float4* src = reinterpret_cast<const float4*>(
-          o_lat + (static_cast<int64_t>(r0 + r) * heads + h) * kDc + piece * 8);
-      va[e] = src[0];
-      vb[e] = src[1];
-    } else {
-      va[e] = vb[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int o = 1; o < 32; o <<= 1) {   // inclusive scans within the warp
+          const int32_t nt = __shfl_up_sync(0xffffffffu, vt, o);
+          const int32_t nc = __shfl_up_sync(0xffffffffu, vc, o);
+          if (lane >= o) {
+            vt += nt;
+            vc += nc;
+          }
+        }
+        if (lane == 31) {
+          wsum[warp] = vc;
+          wsum[kWarps + warp] = vt;
+        }
+        __syncthreads();
+        if (warp == 0) {   // inclusive scans of the warp totals
+          int32_t wc = lane < kWarps ? wsum[lane] : 0, wt = lane < kWarps ? wsum[kWarps + lane] : 0;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int32_t nc = __shfl_up_sync(0xffffffffu, wc, o);
+            const int32_t nt = __shfl_up_sync(0xffffffffu, wt, o);
+            if (lane >= o) {
+              wc += nc;
+              wt += nt;
+            }
+          }
+          if (lane < kWarps) {
+            wsum[lane] = wc;
+            wsum[kWarps + lane] = wt;
+          }
+        }
+        __syncthreads();
+        if (t >= s_lo && t <= s_hi)
+          sbefore[t - s_lo] = carry_c + (warp > 0 ? wsum[warp - 1] : 0) + vc - own;
+        carry_c += wsum[kWarps - 1];
+        carry_t += wsum[2 * kWarps - 1];
+        __syncthreads();   // sbefore is complete; wsum is rewritten by the next round
+      }
+      tot = carry_c;
+      tiles = carry_t;
+      geometry();
     }
   }
+  // o_lat and the partials are produced by the launch this one depends on:
+  // wait for it (the W_UV loads above already overlap its tail).  o_lat is
+  // not a restrict-qualified pointer on purpose: read-only-for-the-kernel
+  // loads could be scheduled ahead of this wait.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if constexpr (kMerge) {
+    if (mp.prefix_ws != nullptr) {
+      tiles = __ldcg(mp.prefix_ws + S);
+      tot = __ldcg(mp.prefix_ws + 2 * S + 1);
+      for (int t = s_lo + tid; t <= s_hi; t += kThreads)
+        sbefore[t - s_lo] = __ldcg(mp.prefix_ws + S + 1 + t);
+      __syncthreads();
+      geometry();
+    }
+    // every warp calls this (each 8-lane group for its own row, or none)
+    const RowWeights rw = merge_weights(mp.part_lse + g_lbase, g_nseg > 0 ? g_nseg : 0, mp.rows);
+    if (my_r < kHalf && (lane & (kMergeLanes - 1)) == 0) {
+      MergeRow& mr = mrow[my_r];
+      mr.obase = g_obase;
+      mr.lbase = g_lbase;
+      mr.orow = g_orow;
+      mr.nseg = g_nseg;
+      mr.m = rw.m;
+      mr.inv = rw.inv;
+      if (g_nseg > 0) mp.lse[g_orow] = rw.lse;
+    }
+    __syncthreads();
+    // B: thread t takes piece t % 64 (8 latent dims) of this CTA's rows
+    // t / 64 + 8 e (the 32 threads of a warp share their rows), up to four
+    // rows at a time, with the loads of 4 / rows partials of each in flight
+    const int piece = tid & 63;
+    const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4* po4 = reinterpret_cast<const float4*>(mp.part_o);
+    const float4* ol4 = reinterpret_cast<const float4*>(o_lat);
+    float4* ow4 = reinterpret_cast<float4*>(mp.o_lat);
+    const int64_t lstride = mp.rows;
+    const int64_t ostride = static_cast<int64_t>(mp.rows) * (kDc / 4);
+    constexpr int kPieces = Uv<N, kMerge>::kPieces;
+    constexpr int kPass = kPieces < 4 ? kPieces : 4;   // rows per pass
+    constexpr int kSegU = 4 / kPass;                    // partials per row per load round
+    cluster_wait();   // both CTAs of the cluster run
+#pragma unroll 1
+    for (int p0 = 0; p0 < kPieces; p0 += kPass) {
+      float4 va[kPass], vb[kPass];
+      int32_t nseg[kPass];
+      int64_t ob[kPass], lb[kPass];
+      float wm[kPass];
+      int32_t maxseg = 0;
 #pragma unroll
-  for (int e = 0; e < Uv<N>::kPieces; ++e) {
-    const int idx = tid + kThreads * e;
-    const int r = idx >> 6, piece = idx & 63;
-    const int kb = piece >> 3, w16 = piece & 7;
-    const float4 a = va[e], b = vb[e];
-    __nv_bfloat162 x0 = __floats2bfloat162_rn(a.x, a.y), x1 = __floats2bfloat162_rn(a.z, a.w);
-    __nv_bfloat162 x2 = __floats2bfloat162_rn(b.x, b.y), x3 = __floats2bfloat162_rn(b.z, b.w);
-    *reinterpret_cast<uint4*>(sB + kb * (N * 128) + r * 128 + ((w16 ^ (r & 7)) << 4)) =
-        make_uint4(*reinterpret_cast<uint32_t*>(&x0), *reinterpret_cast<uint32_t*>(&x1),
-                   *reinterpret_cast<uint32_t*>(&x2), *reinterpret_cast<uint32_t*>(&x3));
+      for (int e = 0; e < kPass; ++e) {
+        const MergeRow& mr = mrow[(tid >> 6) + (kThreads / 64) * (p0 + e)];
+        nseg[e] = mr.nseg;
+        ob[e] = mr.obase + 2 * piece;
+        lb[e] = mr.lbase;
+        wm[e] = mr.m;
+        const bool direct = mr.nseg == 0;
+        va[e] = direct ? __ldcg(ol4 + ob[e]) : zero;
+        vb[e] = direct ? __ldcg(ol4 + ob[e] + 1) : zero;
+        maxseg = mr.nseg > maxseg ? mr.nseg : maxseg;
+      }
+      for (int i0 = 0; i0 < maxseg; i0 += kSegU) {
+        float lv[kPass][kSegU];
+        float4 xa[kPass][kSegU], xb[kPass][kSegU];
+#pragma unroll
+        for (int e = 0; e < kPass; ++e)
+#pragma unroll
+          for (int u = 0; u < kSegU; ++u) {
+            const int64_t i = i0 + u;
+            const bool in = i < nseg[e];
+            lv[e][u] = in ? __ldcg(mp.part_lse + lb[e] + i * lstride) : -INFINITY;
+            xa[e][u] = in ? __ldcg(po4 + ob[e] + i * ostride) : zero;
+            xb[e][u] = in ? __ldcg(po4 + ob[e] + i * ostride + 1) : zero;
+          }
+#pragma unroll
+        for (int e = 0; e < kPass; ++e)
+#pragma unroll
+          for (int u = 0; u < kSegU; ++u)
+            if (i0 + u < nseg[e]) {   // partials in increasing order
+              const float w = merge_weight(lv[e][u], wm[e]);
+              merge_fma(va[e], w, xa[e][u]);
+              merge_fma(vb[e], w, xb[e][u]);
+            }
+      }
+#pragma unroll
+      for (int e = 0; e < kPass; ++e) {
+        const int rr = (tid >> 6) + (kThreads / 64) * (p0 + e);   // row of the half
+        if (rr >= mine) continue;   // the other CTA's row, or past the block's last
+        const int r = first + rr;
+        if (nseg[e] > 0) {
+          const MergeRow& mr = mrow[rr];
+          va[e] = merge_scale(va[e], mr.inv);
+          vb[e] = merge_scale(vb[e], mr.inv);
+          ow4[mr.orow * (kDc / 4) + 2 * piece] = va[e];
+          ow4[mr.orow * (kDc / 4) + 2 * piece + 1] = vb[e];
+        }
+        const uint32_t off = store_b_piece<N>(sB, r, piece, va[e], vb[e]);
+        st_cluster_v4(mapa_shared(smem_u32(sB) + off, crank ^ 1u),
+                      *reinterpret_cast<const uint4*>(sB + off));
+      }
+    }
+  } else {
+    // B: o_lat[r0 + r][h][k] -> bf16, [kb][r][128 B] swizzled.  Item e of
+    // this thread is piece (tid + kThreads e): row (tid + kThreads e) / 64,
+    // 8 consecutive k.
+    float4 va[Uv<N, kMerge>::kPieces], vb[Uv<N, kMerge>::kPieces];
+#pragma unroll
+    for (int e = 0; e < Uv<N, kMerge>::kPieces; ++e) {
+      const int idx = tid + kThreads * e;
+      const int r = idx >> 6, piece = idx & 63;
+      if (r0 + r < rows) {
+        const float4* src = reinterpret_cast<const float4*>(
+            o_lat + (static_cast<int64_t>(r0 + r) * heads + h) * kDc + piece * 8);
+        va[e] = src[0];
+        vb[e] = src[1];
+      } else {
+        va[e] = vb[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < Uv<N, kMerge>::kPieces; ++e) {
+      const int idx = tid + kThreads * e;
+      store_b_piece<N>(sB, idx >> 6, idx & 63, va[e], vb[e]);
+    }
   }
   fence_proxy_async_smem();
+  if constexpr (kMerge) {
+    fence_proxy_async_all();   // this thread's stores into the other CTA's B, too
+    cluster_sync_all();        // both halves of B are in both CTAs
+    fence_proxy_async_all();
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -346,40 +608,61 @@ __global__ void __launch_bounds__(Uv<N>::kThreads, 1)
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, Uv<N>::kTmemCols);
+    tmem_dealloc(tmem, Uv<N, kMerge>::kTmemCols);
   }
 }
 
 namespace {
-template <int N>
+template <int N, bool kMerge>
 cudaError_t launch_uv(const CUtensorMap* w_map, const float* o_lat, uint16_t* out, int rows,
-                      int heads, cudaStream_t stream) {
-  cudaError_t err = set_smem_attr_once(reinterpret_cast<const void*>(mla_uv_kernel<N>),
-                                       N == 16 ? 1 : (N == 32 ? 2 : 10), Uv<N>::kSmem);
+                      int heads, const CombineParams& mp, cudaStream_t stream) {
+  // attribute slots: 1, 2, 10 (projection), 11, 12, 13 (merging projection)
+  const int slot = (kMerge ? 11 : 1) + (N == 16 ? 0 : (N == 32 ? 1 : (kMerge ? 2 : 9)));
+  cudaError_t err = set_smem_attr_once(reinterpret_cast<const void*>(mla_uv_kernel<N, kMerge>),
+                                       slot, Uv<N, kMerge>::kSmem);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(heads, kDv / 128, (rows + N - 1) / N);
-  cfg.blockDim = dim3(Uv<N>::kThreads);
-  cfg.dynamicSmemBytes = Uv<N>::kSmem;
+  cfg.blockDim = dim3(Uv<N, kMerge>::kThreads);
+  cfg.dynamicSmemBytes = Uv<N, kMerge>::kSmem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;   // the two output halves
+  attr[1].val.clusterDim.x = 1;
+  attr[1].val.clusterDim.y = kDv / 128;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  err = cudaLaunchKernelEx(&cfg, mla_uv_kernel<N>, *w_map, o_lat, out, rows, heads);
+  cfg.numAttrs = kMerge ? 2 : 1;
+  err = cudaLaunchKernelEx(&cfg, mla_uv_kernel<N, kMerge>, *w_map, o_lat, out, rows, heads, mp);
   if (err != cudaSuccess) return err;
   return cudaGetLastError();
+}
+
+// The row block: 16 rows for at most 16, else the smallest of 32 and 64
+// whose grid fits the SMs (64 when none does).
+template <bool kMerge>
+cudaError_t launch_uv_rows(const CUtensorMap* w_map, const float* o_lat, uint16_t* out, int rows,
+                           int heads, int sm_count, const CombineParams& mp, cudaStream_t stream) {
+  if (rows == 0) return cudaSuccess;
+  const int blocks32 = heads * (kDv / 128) * ((rows + 31) / 32);
+  if (rows <= 16) return launch_uv<16, kMerge>(w_map, o_lat, out, rows, heads, mp, stream);
+  if (blocks32 <= sm_count) return launch_uv<32, kMerge>(w_map, o_lat, out, rows, heads, mp, stream);
+  return launch_uv<64, kMerge>(w_map, o_lat, out, rows, heads, mp, stream);
 }
 }  // namespace
 
 cudaError_t launch_uv_proj_tma(const CUtensorMap* w_map, const float* o_lat, uint16_t* out,
                                int rows, int heads, int sm_count, cudaStream_t stream) {
-  if (rows == 0) return cudaSuccess;
-  auto blocks = [&](int n) { return heads * (kDv / 128) * ((rows + n - 1) / n); };
-  if (rows <= 16) return launch_uv<16>(w_map, o_lat, out, rows, heads, stream);
-  if (blocks(32) <= sm_count) return launch_uv<32>(w_map, o_lat, out, rows, heads, stream);
-  return launch_uv<64>(w_map, o_lat, out, rows, heads, stream);
+  const CombineParams none = {};
+  return launch_uv_rows<false>(w_map, o_lat, out, rows, heads, sm_count, none, stream);
+}
+
+cudaError_t launch_merge_uv(const CUtensorMap* w_map, const CombineParams& p, uint16_t* out,
+                            int sm_count, cudaStream_t stream) {
+  if (p.num_streams == 0) return cudaSuccess;
+  return launch_uv_rows<true>(w_map, p.o_lat, out, p.batch * p.q_len, p.heads, sm_count, p, stream);
 }
 
 // ----------------------------------------------------------------------------

@@ -105,6 +105,12 @@ cudaError_t launch_prefix(const DecodeParams& p, cudaStream_t stream);
 // or 64 rows) so the grid fits the SMs where it can.
 cudaError_t launch_uv_proj_tma(const CUtensorMap* w_map, const float* o_lat, uint16_t* out,
                                int rows, int heads, int sm_count, cudaStream_t stream);
+// The merge and the up-projection in one launch (a programmatic dependent
+// of the decode): out = W_UV[h]^T o for every row, o the decode's o_lat row
+// or, for a split row set, the merge of its partials (also written to
+// p.o_lat and p.lse, the bits the merge kernel gives).
+cudaError_t launch_merge_uv(const CUtensorMap* w_map, const CombineParams& p, uint16_t* out,
+                            int sm_count, cudaStream_t stream);
 
 struct AppendParams {
   const uint16_t* new_rows;     // bf16 [rows][576]

@@ -113,10 +113,10 @@ class DecodeStep:
         mla_uv_proj(self.o_lat, self.w_uv, self.out, self.rows, self.H, self.stream)
 
     def step(self):
-        """One decode step (mla_decode_step): the attention pass, the merge of
-        split row sets and the W_UV projection (three kernels, each a
-        programmatic dependent of the one before, behind a one-block prefix
-        pre-pass when the row sets are many); the absorbed query is an
+        """One decode step (mla_decode_step): the attention pass, then the
+        merge of split row sets inside the W_UV projection (two kernels, the
+        second a programmatic dependent of the first, behind a one-block
+        prefix pre-pass when the row sets are many); the absorbed query is an
         input."""
         mla_decode_step(self.plan, self.q_hat, None, self.cache, self.block_table, self.seq_lens,
                         self.topk_idx, self.workspace, self.w_uv, self.o_lat, self.lse, self.out,
@@ -135,9 +135,9 @@ class DecodeStep:
 
     @property
     def kernels_per_step(self) -> int:
-        """Kernels one step() launches: the decode, the merge and W_UV, behind
-        the prefix pre-pass when the plan has one."""
-        return 3 + int(self.plan.prefix_pass)
+        """Kernels one step() launches: the decode, then the merge with W_UV,
+        behind the prefix pre-pass when the plan has one."""
+        return 2 + int(self.plan.prefix_pass)
 
 
 class HostPipeline:

@@ -242,10 +242,12 @@ MLA_API int mla_decode_run(const mla_plan* plan, const void* q, const void* w_uk
  * the kv_b_proj value half to every row in the same call ("GLM-4.7-Flash"
  * record, configuration clause: v_head_dim 256 read back out of the 512-rank
  * latent through kv_b_proj): out[r][h] = bf16(W_UV[h]^T o_lat[r][h]).
- * The merge runs over all SMs (one block per row of each split row set) and
- * the up-projection per (head, 128 output dims, row block); each is launched
- * as a programmatic dependent of the kernel before it on `stream`, so its
- * set-up (and the W_UV loads) overlap that kernel's tail.
+ * Without w_uv the merge runs over all SMs (one block per row of each split
+ * row set); with it, one kernel per (head, 128 output dims, row block) merges
+ * its rows and projects them.  Either is launched as a programmatic
+ * dependent of the kernel before it on `stream`, so its set-up (the work
+ * split, the W_UV loads) overlaps that kernel's tail.  Both merges give the
+ * same bits.
  *   w_uv  : NULL, or bf16 [H][512][256]
  *   out   : bf16 [B*Q][H][256] when w_uv is given, else ignored (may be NULL)
  * After the call o_lat and lse are complete for every row.  Calling it again
@@ -259,9 +261,9 @@ MLA_API int mla_combine(const mla_plan* plan, const int32_t* seq_lens, const voi
 
 /*
  * mla_decode_step -- one whole decode step in one call: mla_decode_run, then
- * mla_combine with W_UV (the attention pass, the merge of split row sets over
- * all SMs, and the W_UV up-projection per head, each kernel a programmatic
- * dependent of the one before).  Same arguments as mla_decode_run, plus
+ * mla_combine with W_UV (two kernels: the attention pass, then the merge of
+ * split row sets inside the W_UV up-projection per head, a programmatic
+ * dependent of the first).  Same arguments as mla_decode_run, plus
  *   w_uv : bf16 [H][512][256]
  *   out  : bf16 [B*Q][H][256] output, out[r][h] = bf16(W_UV[h]^T o_lat[r][h])
  * o_lat and lse are complete on return.  ("GLM-4.7-Flash" record: the MLA

@@ -96,8 +96,8 @@ def test_plan_without_host_lengths_on_few_tiles():
 
 @pytest.mark.parametrize("name", ["dense_small", "fp8_small", "mtp_small"])
 def test_chained_launches_see_their_inputs(name):
-    """The decode, merge and W_UV kernels run as programmatic dependents of
-    one another: each must read what the one before wrote.  Outputs are
+    """The decode and the merge + W_UV kernel run as programmatic dependents
+    of one another: each must read what the one before wrote.  Outputs are
     filled with NaN before every step; a step over split row sets must
     rewrite all of them with the same values every time."""
     w = W.with_overrides(W.SMALL_WORKLOADS[name], seq_lo=1500, seq_hi=4000, batch=3)
@@ -313,28 +313,44 @@ def test_long_full_size_every_request_and_head():
 
 
 @pytest.mark.parametrize("name,sm_count", [("dense_small", 7), ("long_small", 40),
-                                           ("mtp_small", 11), ("sparse_small", 5), ("tiny", None)])
+                                           ("long_small", 152), ("mtp_small", 11),
+                                           ("sparse_small", 5), ("tiny", None)])
 def test_combine_with_w_uv_matches_separate_passes(name, sm_count):
-    """mla_combine with W_UV against the merge alone followed by the
-    stand-alone mla_uv_proj (whose row block follows the device's SM count,
-    not the plan's): the same o_lat and lse, outputs within one bf16 step;
-    both against the oracle."""
-    batch = W.generate(W.SMALL_WORKLOADS[name])
+    """The step's merge inside the W_UV launch against the merge kernel alone
+    followed by the stand-alone mla_uv_proj (whose row block follows the
+    device's SM count, not the plan's): the same o_lat and lse bits (one
+    merge arithmetic; long_small on 152 CTAs splits a row set over more than
+    32), outputs within one bf16 step; both against the oracle."""
+    _merge_uv_against_separate_passes(W.generate(W.SMALL_WORKLOADS[name]), sm_count, name)
+
+
+def _merge_uv_against_separate_passes(batch, sm_count, label):
     step = make_step(batch, sm_count=sm_count)
     step.run()
     step.uv()
     o1, lat1, lse1 = gpu_outputs(step)
     for t in (step.out, step.o_lat, step.lse):
         t.fill_(float("nan"))
-    step.step()                        # attention pass, merge, W_UV
+    step.step()                        # attention pass, then merge + W_UV
     o2, lat2, lse2 = gpu_outputs(step)
-    assert np.allclose(lat2, lat1, rtol=1e-5, atol=1e-6)
-    live = np.isfinite(lse1)
-    assert np.array_equal(live, np.isfinite(lse2)) and np.allclose(lse2[live], lse1[live], atol=1e-5)
+    assert step.status() == 0
+    assert np.array_equal(lat2.view(np.uint32), lat1.view(np.uint32))
+    assert np.array_equal(lse2.view(np.uint32), lse1.view(np.uint32))
     assert np.abs(o2 - o1).max() <= 2.0 ** -7 * max(1.0, np.abs(o1).max())
     ref = O.decode(batch)
-    compare(ref, o1, lat1, lse1, label=f"separate/{name}")
-    compare(ref, o2, lat2, lse2, label=f"combine-uv/{name}")
+    compare(ref, o1, lat1, lse1, label=f"separate/{label}")
+    compare(ref, o2, lat2, lse2, label=f"combine-uv/{label}")
+
+
+@pytest.mark.parametrize("batch,q_len,sm_count", [(1, 1, 152), (17, 1, 39), (40, 1, 152),
+                                                  (33, 2, 152), (1, 3, 60)])
+def test_merge_uv_ragged_row_blocks(batch, q_len, sm_count):
+    """The merge inside the W_UV launch splits each row block's rows between
+    the two CTAs of a cluster: one row (the second CTA merges none), 17 rows
+    in a block of 64 (9 and 8), a last block of 8 or 2 rows, three drafts of
+    one request; each row set split over many CTAs.  Same checks as above."""
+    w = W.with_overrides(W.SMALL_WORKLOADS["long_small"], batch=batch, q_len=q_len)
+    _merge_uv_against_separate_passes(W.generate(w), sm_count, f"{batch}x{q_len}/{sm_count}")
 
 
 @pytest.mark.parametrize("name", ["dense_small", "mtp_small", "tiny"])
