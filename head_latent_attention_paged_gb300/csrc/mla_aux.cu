@@ -255,7 +255,8 @@ struct Uv {
   static constexpr int kB = 8 * N * 128;                     // 8 K-blocks x N rows x 128 B
   // 16-byte B pieces per thread (a merging CTA builds half of the rows)
   static constexpr int kPieces = (kMerge ? N / 2 : N) * 64 / kThreads;
-  static constexpr int kTmemCols = 4 * N < 32 ? 32 : 4 * N;  // four accumulators
+  // four accumulators of N columns, in an allocation of a power of two >= 32
+  static constexpr int kTmemCols = 4 * N <= 32 ? 32 : (4 * N <= 64 ? 64 : (4 * N <= 128 ? 128 : 256));
   // merging blocks: N MergeRow, N + 1 row-set cost prefixes, 2 x kWarps scan sums
   static constexpr int kScratch =
       kMerge ? static_cast<int>(N * sizeof(MergeRow)) + (N + 1 + 2 * kWarps) * 4 : 0;
@@ -616,8 +617,9 @@ namespace {
 template <int N, bool kMerge>
 cudaError_t launch_uv(const CUtensorMap* w_map, const float* o_lat, uint16_t* out, int rows,
                       int heads, const CombineParams& mp, cudaStream_t stream) {
-  // attribute slots: 1, 2, 10 (projection), 11, 12, 13 (merging projection)
-  const int slot = (kMerge ? 11 : 1) + (N == 16 ? 0 : (N == 32 ? 1 : (kMerge ? 2 : 9)));
+  // attribute slots: 1, 2, 10 (projection), 11, 12, 14, 13 (merging projection)
+  const int slot = kMerge ? (N == 16 ? 11 : (N == 32 ? 12 : (N == 48 ? 14 : 13)))
+                          : (N == 16 ? 1 : (N == 32 ? 2 : 10));
   cudaError_t err = set_smem_attr_once(reinterpret_cast<const void*>(mla_uv_kernel<N, kMerge>),
                                        slot, Uv<N, kMerge>::kSmem);
   if (err != cudaSuccess) return err;
@@ -640,15 +642,17 @@ cudaError_t launch_uv(const CUtensorMap* w_map, const float* o_lat, uint16_t* ou
   return cudaGetLastError();
 }
 
-// The row block: 16 rows for at most 16, else the smallest of 32 and 64
-// whose grid fits the SMs (64 when none does).
+// The row block: 16 rows for at most 16, else the smallest of 32, 48
+// (merging blocks only) and 64 whose grid fits the SMs (64 when none does).
 template <bool kMerge>
 cudaError_t launch_uv_rows(const CUtensorMap* w_map, const float* o_lat, uint16_t* out, int rows,
                            int heads, int sm_count, const CombineParams& mp, cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
-  const int blocks32 = heads * (kDv / 128) * ((rows + 31) / 32);
+  auto blocks = [&](int n) { return heads * (kDv / 128) * ((rows + n - 1) / n); };
   if (rows <= 16) return launch_uv<16, kMerge>(w_map, o_lat, out, rows, heads, mp, stream);
-  if (blocks32 <= sm_count) return launch_uv<32, kMerge>(w_map, o_lat, out, rows, heads, mp, stream);
+  if (blocks(32) <= sm_count) return launch_uv<32, kMerge>(w_map, o_lat, out, rows, heads, mp, stream);
+  if (kMerge && blocks(48) <= sm_count)
+    return launch_uv<48, kMerge>(w_map, o_lat, out, rows, heads, mp, stream);
   return launch_uv<64, kMerge>(w_map, o_lat, out, rows, heads, mp, stream);
 }
 }  // namespace

@@ -343,12 +343,13 @@ def _merge_uv_against_separate_passes(batch, sm_count, label):
 
 
 @pytest.mark.parametrize("batch,q_len,sm_count", [(1, 1, 152), (17, 1, 39), (40, 1, 152),
-                                                  (33, 2, 152), (1, 3, 60)])
+                                                  (33, 2, 152), (1, 3, 60), (50, 2, 130)])
 def test_merge_uv_ragged_row_blocks(batch, q_len, sm_count):
     """The merge inside the W_UV launch splits each row block's rows between
     the two CTAs of a cluster: one row (the second CTA merges none), 17 rows
     in a block of 64 (9 and 8), a last block of 8 or 2 rows, three drafts of
-    one request; each row set split over many CTAs.  Same checks as above."""
+    one request, 100 rows in blocks of 48 (the last of 4); each row set split
+    over many CTAs.  Same checks as above."""
     w = W.with_overrides(W.SMALL_WORKLOADS["long_small"], batch=batch, q_len=q_len)
     _merge_uv_against_separate_passes(W.generate(w), sm_count, f"{batch}x{q_len}/{sm_count}")
 
