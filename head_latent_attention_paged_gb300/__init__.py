@@ -212,8 +212,9 @@ def mla_combine(plan: MlaPlan, seq_lens, workspace, o_lat, lse, w_uv=None, out=N
 
 def mla_decode_step(plan: MlaPlan, q, w_uk, kv_cache, block_table, seq_lens, topk_idx, workspace,
                     w_uv, o_lat, lse, out, stream=None, workspace_bytes=None) -> None:
-    """A whole decode step (attention, merge, W_UV) in one cooperative launch
-    where the plan's grid fits the SMs, else mla_decode_run + mla_combine."""
+    """A whole decode step, mla_decode_run then mla_combine with W_UV: two
+    kernels, the attention pass and then the merge of split row sets inside
+    the W_UV projection (a programmatic dependent of the first)."""
     _check("mla_decode_step", load().mla_decode_step(
         ctypes.byref(plan), _ptr(q), _ptr(w_uk), _ptr(kv_cache), _ptr(block_table),
         _ptr(seq_lens), _ptr(topk_idx), _ptr(workspace), _nbytes(workspace, workspace_bytes, plan),
